@@ -1,0 +1,231 @@
+"""CPU oracle for one GQA decode step over a KV cache (fp64, plain and slow).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg use it. The CUDA library never imports, links or
+calls anything here, and nothing here imports the CUDA library.
+
+Functions and the passages they follow:
+
+* ``decode``             -- GQA attention, "分组查询注意力 (GQA)", 技术原理 steps 2-4
+                            and its attention equation (C, fp64, ``gqa_oracle.c``).
+* ``gather_dense``       -- the block-table lookup of "LLM 推理性能优化实战" section 8.2:
+                            token t of a sequence lives in physical block
+                            ``table[t // 16]``, slot ``t % 16`` (block_size 16, the
+                            KV-cache essay's "block_size=16" paragraph).
+* ``append``             -- the paged write of one new token per sequence: slot
+                            ``pos % 16`` of block ``table[pos // 16]``.
+* ``quantize_int8`` / ``dequantize_int8`` -- symmetric per-(token, kv-head) int8,
+                            "LLM 推理性能优化实战" sections 15.1, 15.2 and 15.5
+                            (rounding rule in ``gqa_oracle.c``).
+* ``kv_cache_elements``  -- the KV-size closed form 2 * layers * K * d * S * B,
+                            "分组查询注意力 (GQA)" 关键参数 item 2 and
+                            "LLM 推理性能优化实战" section 6.1.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gqa_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+BLOCK_SIZE = 16
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (plain C99, no fast-math, no contraction)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c99", "-D_POSIX_C_SOURCE=200809L", "-O2", "-fno-fast-math",
+           "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int32)
+            lib.oracle_gqa_decode.argtypes = [dp, dp, dp, ip, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_double, dp, ctypes.c_int32]
+            lib.oracle_gqa_decode.restype = ctypes.c_int
+            lib.oracle_quantize_int8.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int64,
+                                                 ctypes.c_int32, ctypes.POINTER(ctypes.c_int8),
+                                                 ctypes.POINTER(ctypes.c_uint16)]
+            lib.oracle_quantize_int8.restype = None
+            lib.oracle_f32_to_f16_bits.argtypes = [ctypes.c_float]
+            lib.oracle_f32_to_f16_bits.restype = ctypes.c_uint16
+            lib.oracle_f16_bits_to_f32.argtypes = [ctypes.c_uint16]
+            lib.oracle_f16_bits_to_f32.restype = ctypes.c_float
+            lib.oracle_num_cpus.argtypes = []
+            lib.oracle_num_cpus.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def num_cpus() -> int:
+    return int(_load().oracle_num_cpus())
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def decode(q, k, v, lens, scale: float, nthreads: int = 0) -> np.ndarray:
+    """o[b,h,:] = softmax(scale * q[b,h] . K[b,:lens[b],g]^T) V[b,:lens[b],g], g = h // (H/K).
+
+    q: [B, H, d]; k, v: dense [B, S_max, K, d]; lens: [B]. Inputs are converted to
+    fp64 exactly (bf16/fp16/fp32 values are all representable). Returns fp64 [B, H, d].
+    """
+    q = np.ascontiguousarray(np.asarray(q, dtype=np.float64))
+    k = np.ascontiguousarray(np.asarray(k, dtype=np.float64))
+    v = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
+    lens = np.ascontiguousarray(np.asarray(lens, dtype=np.int32))
+    B, H, d = q.shape
+    if k.ndim != 4 or k.shape[0] != B or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError("k/v must be [B, S_max, K, d] matching q")
+    S_max, K = k.shape[1], k.shape[2]
+    out = np.empty((B, H, d), dtype=np.float64)
+    rc = _load().oracle_gqa_decode(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                                   _ptr(v, ctypes.c_double), _ptr(lens, ctypes.c_int32),
+                                   B, H, K, d, S_max, float(scale),
+                                   _ptr(out, ctypes.c_double), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_gqa_decode failed with {rc}")
+    return out
+
+
+def gather_dense(pool, block_table, lens, stride_block: int, stride_head: int,
+                 stride_token: int, num_kv_heads: int, head_dim: int,
+                 batch_index=None) -> np.ndarray:
+    """Dense [B, S_max, K, d] view of sequences held in a paged pool.
+
+    ``pool`` is the flat element array of the cache; token t of sequence b, head g,
+    element i sits at ``table[b, t // 16] * stride_block + g * stride_head +
+    (t % 16) * stride_token + i``. Returns the pool's dtype (no arithmetic)."""
+    flat = np.asarray(pool).reshape(-1)
+    table = np.asarray(block_table)
+    lens = np.asarray(lens).reshape(-1)
+    rows = range(len(lens)) if batch_index is None else batch_index
+    rows = list(rows)
+    S_max = int(max([int(lens[b]) for b in rows] + [0]))
+    K, d = num_kv_heads, head_dim
+    out = np.zeros((len(rows), S_max, K, d), dtype=flat.dtype)
+    i = np.arange(d)
+    for n, b in enumerate(rows):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        t = np.arange(L)
+        phys = table[b, t // BLOCK_SIZE].astype(np.int64)
+        base = (phys * stride_block + (t % BLOCK_SIZE) * stride_token)        # [L]
+        idx = base[:, None, None] + (np.arange(K) * stride_head)[None, :, None] + i[None, None, :]
+        out[n, :L] = flat[idx]
+    return out
+
+
+def gather_scales(scale_pool, block_table, lens, num_kv_heads: int, batch_index=None):
+    """Dense [B, S_max, K] view of per-(token, kv-head) scales held as [NB, K, 16]."""
+    sp = np.asarray(scale_pool)
+    table = np.asarray(block_table)
+    lens = np.asarray(lens).reshape(-1)
+    rows = list(range(len(lens)) if batch_index is None else batch_index)
+    S_max = int(max([int(lens[b]) for b in rows] + [0]))
+    out = np.zeros((len(rows), S_max, num_kv_heads), dtype=sp.dtype)
+    for n, b in enumerate(rows):
+        L = int(lens[b])
+        t = np.arange(L)
+        phys = table[b, t // BLOCK_SIZE].astype(np.int64)
+        out[n, :L] = sp[phys, :, t % BLOCK_SIZE]
+    return out
+
+
+def append(pool, new, block_table, positions, stride_block: int, stride_head: int,
+           stride_token: int):
+    """Write new[b, g, :] into slot positions[b] % 16 of block table[b, positions[b] // 16].
+
+    ``pool``: flat element array (modified in place, any dtype); ``new``: [B, K, d]
+    of the pool's dtype. Returns the pool."""
+    flat = np.asarray(pool).reshape(-1)
+    new = np.asarray(new)
+    B, K, d = new.shape
+    for b in range(B):
+        pos = int(positions[b])
+        phys = int(block_table[b, pos // BLOCK_SIZE])
+        for g in range(K):
+            off = phys * stride_block + g * stride_head + (pos % BLOCK_SIZE) * stride_token
+            flat[off:off + d] = new[b, g]
+    return pool
+
+
+def append_scales(scale_pool, new_scales, block_table, positions):
+    """Scale counterpart of ``append`` for a [NB, K, 16] scale array."""
+    sp = np.asarray(scale_pool)
+    for b in range(new_scales.shape[0]):
+        pos = int(positions[b])
+        phys = int(block_table[b, pos // BLOCK_SIZE])
+        sp[phys, :, pos % BLOCK_SIZE] = new_scales[b]
+    return scale_pool
+
+
+def quantize_int8(x) -> tuple[np.ndarray, np.ndarray]:
+    """Rows of x (last axis = d, converted to fp32) -> (int8 codes, fp16 scale bits as uint16)."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    d = x.shape[-1]
+    rows = x.size // d if d else 0
+    codes = np.empty(x.shape, dtype=np.int8)
+    scales = np.empty(x.shape[:-1], dtype=np.uint16)
+    _load().oracle_quantize_int8(_ptr(x, ctypes.c_float), rows, d,
+                                 _ptr(codes, ctypes.c_int8), _ptr(scales, ctypes.c_uint16))
+    return codes, scales
+
+
+def f16_bits_to_f64(bits) -> np.ndarray:
+    """Exact value of fp16 bit patterns (uint16) as fp64."""
+    b = np.asarray(bits, dtype=np.uint16)
+    lib = _load()
+    flat = [lib.oracle_f16_bits_to_f32(int(v)) for v in b.reshape(-1)]
+    return np.asarray(flat, dtype=np.float64).reshape(b.shape)
+
+
+def f32_to_f16_bits(x) -> np.ndarray:
+    """Round fp32 values to fp16 (nearest-even); returns the bit patterns."""
+    a = np.asarray(x, dtype=np.float32)
+    lib = _load()
+    flat = [lib.oracle_f32_to_f16_bits(float(v)) for v in a.reshape(-1)]
+    return np.asarray(flat, dtype=np.uint16).reshape(a.shape)
+
+
+def dequantize_int8(codes, scale_values) -> np.ndarray:
+    """codes[..., i] * scale[...] in fp64 (exact: both factors are short)."""
+    c = np.asarray(codes, dtype=np.float64)
+    s = np.asarray(scale_values, dtype=np.float64)
+    return c * s[..., None]
+
+
+def kv_cache_elements(layers: int, kv_heads: int, head_dim: int, seq_len: int,
+                      batch: int) -> int:
+    """Elements of K and V cached for ``batch`` sequences of ``seq_len`` tokens:
+    2 * layers * kv_heads * head_dim * seq_len * batch."""
+    return 2 * layers * kv_heads * head_dim * seq_len * batch
+
+
+def blocks_for_tokens(n_tokens: int) -> int:
+    """Physical 16-token blocks a sequence of n_tokens occupies (last one may be partial)."""
+    return -(-int(n_tokens) // BLOCK_SIZE)

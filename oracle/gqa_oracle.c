@@ -1,0 +1,250 @@
+/*
+ * gqa_oracle.c -- plain, slow, fp64 CPU oracle for one GQA decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path links, loads or calls
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg do. It shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes, and where the pages define it:
+ *
+ *  - oracle_gqa_decode: grouped-query attention for one new token per sequence,
+ *    "分组查询注意力 (GQA)", section 技术原理, steps 2-4 and the attention
+ *    equation softmax(Q_group K_g^T / sqrt(d_k)) V_g. Query head h uses KV head
+ *    g = h / (H/K) (the [K, H/K] reshape of step 2; the head mapping j = i // 4
+ *    of the KV-cache essay's GQA section is the H/K = 4 case). The softmax is
+ *    the plain definition: subtract the maximum score, exponentiate, divide by
+ *    the sum. The cache is dense [B, S_max, K, d] (the [batch, seq,
+ *    num_kv_heads, head_dim] index of "LLM 推理性能优化实战", section 7.3).
+ *    An empty context (length 0) yields a zero output (reading: the pages never
+ *    decode an empty sequence).
+ *
+ *  - oracle_quantize_int8: symmetric int8 quantisation with one scale per
+ *    (token, kv-head) row ("LLM 推理性能优化实战", section 15.1: symmetric range
+ *    [-127, 127]; sections 15.2 and 15.5: per-token scales for the KV cache).
+ *    The pages leave rounding and scale precision open; the reading used here:
+ *      amax = max_i |x_i|                     (fp32)
+ *      s    = fp16_rne(min(amax / 127, 65504)) (fp32 IEEE division, then RNE)
+ *      q_i  = 0 if s == 0 else clamp(rint(x_i / s), -127, 127)
+ *    with fp32 IEEE division and round-half-to-even. Dequantisation is q_i * s
+ *    evaluated exactly in fp64.
+ *
+ *  - oracle_f32_to_f16_bits / oracle_f16_bits_to_f32: IEEE 754 binary16
+ *    conversion with round-to-nearest-even, written from the format's
+ *    definition (1 sign, 5 exponent, 10 fraction bits, bias 15).
+ *
+ * Build: plain C99, -O2 -fno-fast-math -ffp-contract=off, pthreads.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* ------------------------------------------------------------------------- */
+/* IEEE binary16 conversions                                                 */
+/* ------------------------------------------------------------------------- */
+
+uint16_t oracle_f32_to_f16_bits(float f)
+{
+    uint32_t x;
+    memcpy(&x, &f, sizeof x);
+    uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    uint32_t ax = x & 0x7fffffffu;
+
+    if (ax >= 0x7f800000u)                       /* inf or NaN */
+        return (uint16_t)(sign | 0x7c00u | (ax > 0x7f800000u ? 0x0200u : 0u));
+
+    int32_t e32 = (int32_t)(ax >> 23);           /* biased fp32 exponent */
+    uint32_t frac = ax & 0x007fffffu;
+    if (e32 == 0)                                /* fp32 subnormal: far below fp16 range */
+        return sign;
+    uint32_t mant = frac | 0x00800000u;          /* 24-bit significand, value = mant * 2^(e32-150) */
+    int32_t e16 = e32 - 127 + 15;                /* biased fp16 exponent if normal */
+
+    if (e16 >= 31)                               /* at or above 2^16: overflow */
+        return (uint16_t)(sign | 0x7c00u);
+
+    if (e16 <= 0) {
+        /* fp16 subnormal: value / 2^-24 = mant * 2^(e32 - 126); shift right by 126 - e32 */
+        int32_t shift = 126 - e32;               /* >= 14 here */
+        if (shift > 24)
+            return sign;                         /* below half the smallest subnormal */
+        uint32_t q = mant >> shift;
+        uint32_t rem = mant & ((1u << shift) - 1u);
+        uint32_t half = 1u << (shift - 1);
+        if (rem > half || (rem == half && (q & 1u)))
+            q += 1u;                             /* may carry into the smallest normal: still correct */
+        return (uint16_t)(sign | q);
+    }
+
+    /* normal: keep 10 of the 23 fraction bits, round to nearest even */
+    uint32_t q = ((uint32_t)e16 << 10) | (frac >> 13);
+    uint32_t rem = frac & 0x1fffu;
+    if (rem > 0x1000u || (rem == 0x1000u && (q & 1u)))
+        q += 1u;                                 /* carry may reach the exponent, or inf at 65520 */
+    return (uint16_t)(sign | q);
+}
+
+float oracle_f16_bits_to_f32(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+    uint32_t e = (h >> 10) & 0x1fu;
+    uint32_t frac = h & 0x3ffu;
+    float out;
+    if (e == 0) {
+        /* zero or subnormal: frac * 2^-24, exact in fp32 */
+        out = (float)frac * (1.0f / 16777216.0f);
+        if (sign) out = -out;
+        return out;
+    }
+    uint32_t bits;
+    if (e == 31)
+        bits = sign | 0x7f800000u | (frac << 13);
+    else
+        bits = sign | ((e - 15 + 127) << 23) | (frac << 13);
+    memcpy(&out, &bits, sizeof out);
+    return out;
+}
+
+/* ------------------------------------------------------------------------- */
+/* int8 KV quantisation, one scale per row                                   */
+/* ------------------------------------------------------------------------- */
+
+void oracle_quantize_int8(const float *x, int64_t rows, int32_t d,
+                          int8_t *codes, uint16_t *scale_bits)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * (int64_t)d;
+        float amax = 0.0f;
+        for (int32_t i = 0; i < d; ++i) {
+            float a = fabsf(xr[i]);
+            if (a > amax) amax = a;
+        }
+        volatile float s32 = amax / 127.0f;      /* IEEE fp32 division */
+        float s = s32;
+        if (s > 65504.0f) s = 65504.0f;
+        uint16_t sb = oracle_f32_to_f16_bits(s);
+        float sf = oracle_f16_bits_to_f32(sb);
+        scale_bits[r] = sb;
+        for (int32_t i = 0; i < d; ++i) {
+            int32_t q = 0;
+            if (sf != 0.0f) {
+                volatile float t = xr[i] / sf;   /* IEEE fp32 division */
+                float rq = rintf(t);             /* round half to even (default mode) */
+                if (rq > 127.0f) rq = 127.0f;
+                if (rq < -127.0f) rq = -127.0f;
+                q = (int32_t)rq;
+            }
+            codes[r * (int64_t)d + i] = (int8_t)q;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* GQA decode attention, fp64                                                */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    const double *q, *k, *v;
+    const int32_t *lens;
+    int32_t B, H, K, d, S_max;
+    double scale;
+    double *out;
+    int64_t next;              /* next (b, h) work item, shared */
+    pthread_mutex_t lock;
+} decode_job;
+
+/* One (b, h) output row, straight from the definition. */
+static void decode_one(const decode_job *J, int32_t b, int32_t h, double *s)
+{
+    const int32_t G = J->H / J->K;
+    const int32_t g = h / G;                     /* query head h reads KV head h / (H/K) */
+    const int32_t d = J->d, K = J->K;
+    const int32_t n = J->lens[b];
+    const double *qh = J->q + ((int64_t)b * J->H + h) * d;
+    double *o = J->out + ((int64_t)b * J->H + h) * d;
+
+    for (int32_t i = 0; i < d; ++i) o[i] = 0.0;
+    if (n <= 0) return;
+
+    /* scores s_t = scale * <q_h, k_{t,g}> */
+    double mx = -INFINITY;
+    for (int32_t t = 0; t < n; ++t) {
+        const double *kt = J->k + (((int64_t)b * J->S_max + t) * K + g) * d;
+        double acc = 0.0;
+        for (int32_t i = 0; i < d; ++i) acc += qh[i] * kt[i];
+        s[t] = J->scale * acc;
+        if (s[t] > mx) mx = s[t];
+    }
+    /* softmax weights and the weighted sum of values */
+    double denom = 0.0;
+    for (int32_t t = 0; t < n; ++t) {
+        double w = exp(s[t] - mx);
+        denom += w;
+        const double *vt = J->v + (((int64_t)b * J->S_max + t) * K + g) * d;
+        for (int32_t i = 0; i < d; ++i) o[i] += w * vt[i];
+    }
+    for (int32_t i = 0; i < d; ++i) o[i] /= denom;
+}
+
+static void *decode_worker(void *arg)
+{
+    decode_job *J = (decode_job *)arg;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(J->S_max > 0 ? J->S_max : 1));
+    if (!s) return (void *)1;
+    const int64_t total = (int64_t)J->B * J->H;
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        int64_t it = J->next++;
+        pthread_mutex_unlock(&J->lock);
+        if (it >= total) break;
+        decode_one(J, (int32_t)(it / J->H), (int32_t)(it % J->H), s);
+    }
+    free(s);
+    return NULL;
+}
+
+int oracle_num_cpus(void)
+{
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+/* q [B,H,d], k/v [B,S_max,K,d], lens [B], out [B,H,d]; all fp64, host memory.
+ * nthreads <= 0 uses every online CPU. Returns 0, or -1 on bad arguments,
+ * -2 when a thread or buffer could not be created. */
+int oracle_gqa_decode(const double *q, const double *k, const double *v,
+                      const int32_t *lens, int32_t B, int32_t H, int32_t K,
+                      int32_t d, int32_t S_max, double scale, double *out,
+                      int32_t nthreads)
+{
+    if (B < 0 || H <= 0 || K <= 0 || d <= 0 || S_max < 0 || H % K != 0)
+        return -1;
+    for (int32_t b = 0; b < B; ++b)
+        if (lens[b] < 0 || lens[b] > S_max) return -1;
+    decode_job J = {q, k, v, lens, B, H, K, d, S_max, scale, out, 0,
+                    PTHREAD_MUTEX_INITIALIZER};
+    int32_t nt = nthreads > 0 ? nthreads : oracle_num_cpus();
+    int64_t items = (int64_t)B * H;
+    if (nt > items) nt = (int32_t)(items > 0 ? items : 1);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
+    if (!th) return -2;
+    /* workers pull items until none are left, so any number of started
+       threads completes the whole job */
+    int32_t started = 0, rc = 0;
+    for (; started < nt; ++started)
+        if (pthread_create(&th[started], NULL, decode_worker, &J) != 0) break;
+    for (int32_t i = 0; i < started; ++i) {
+        void *ret = NULL;
+        pthread_join(th[i], &ret);
+        if (ret) rc = -2;
+    }
+    if (started == 0) {                          /* no thread could start: run inline */
+        void *ret = decode_worker(&J);
+        rc = ret ? -2 : 0;
+    }
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    return rc;
+}

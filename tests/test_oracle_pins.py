@@ -1,0 +1,298 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself --
+figures the pages print, closed forms, library routines (torch SDPA, numpy's
+fp16 rounding) and invariants that a dropped term, a wrong sign, index or
+transposed operand would break. CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_inputs as gi
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def _sdpa_reference(q, k, v, lens, scale):
+    """Library reference: torch SDPA in fp64 on CPU, K/V repeat-interleaved to H heads."""
+    B, H, d = q.shape
+    K = k.shape[2]
+    G = H // K
+    out = np.zeros((B, H, d))
+    for b in range(B):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        qb = torch.from_numpy(q[b]).reshape(1, H, 1, d)
+        kb = torch.from_numpy(k[b, :L]).permute(1, 0, 2).repeat_interleave(G, dim=0).unsqueeze(0)
+        vb = torch.from_numpy(v[b, :L]).permute(1, 0, 2).repeat_interleave(G, dim=0).unsqueeze(0)
+        o = torch.nn.functional.scaled_dot_product_attention(qb, kb, vb, scale=scale)
+        out[b] = o.reshape(H, d).numpy()
+    return out
+
+
+# --------------------------------------------------------------------------- decode
+
+
+@pytest.mark.parametrize("B,H,K,d,lens", [
+    (2, 8, 2, 64, [37, 100]),          # the tiny contiguous workload's shape
+    (3, 8, 8, 16, [1, 5, 33]),         # G = 1: plain multi-head attention
+    (2, 8, 1, 32, [17, 9]),            # K = 1: multi-query attention
+    (1, 12, 3, 128, [70]),
+])
+def test_decode_matches_torch_sdpa_with_repeat_interleave(oracle_mod, B, H, K, d, lens):
+    q = _rand((B, H, d), 1)
+    k = _rand((B, max(lens), K, d), 2)
+    v = _rand((B, max(lens), K, d), 3)
+    scale = 1.0 / math.sqrt(d)
+    got = oracle_mod.decode(q, k, v, lens, scale)
+    ref = _sdpa_reference(q, k, v, lens, scale)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_decode_matches_sdpa_native_gqa(oracle_mod):
+    """torch's own grouped-query mode (enable_gqa) fixes the head-to-group map."""
+    B, H, K, d, S = 2, 8, 2, 32, 11
+    q, k, v = _rand((B, H, d), 4), _rand((B, S, K, d), 5), _rand((B, S, K, d), 6)
+    got = oracle_mod.decode(q, k, v, [S, S], 0.3)
+    qt = torch.from_numpy(q).unsqueeze(2)
+    kt = torch.from_numpy(k).permute(0, 2, 1, 3)
+    vt = torch.from_numpy(v).permute(0, 2, 1, 3)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=0.3, enable_gqa=True)
+    np.testing.assert_allclose(got, ref.squeeze(2).numpy(), rtol=0, atol=1e-12)
+
+
+def test_group_mapping_is_contiguous_not_modulo(oracle_mod):
+    """Head h must read KV head h // G. Give each KV head a constant V value equal to
+    its index: the output of head h is then exactly h // G."""
+    B, H, K, d, S = 1, 8, 2, 4, 6
+    q = _rand((B, H, d), 7)
+    k = _rand((B, S, K, d), 8)
+    v = np.zeros((B, S, K, d))
+    for g in range(K):
+        v[:, :, g, :] = g
+    out = oracle_mod.decode(q, k, v, [S], 0.5)
+    for h in range(H):
+        assert np.all(out[0, h] == h // (H // K))
+
+
+def test_one_token_context_returns_v_exactly(oracle_mod):
+    q, k, v = _rand((2, 4, 8), 9), _rand((2, 3, 2, 8), 10), _rand((2, 3, 2, 8), 11)
+    out = oracle_mod.decode(q, k, v, [1, 1], 0.7)
+    for b in range(2):
+        for h in range(4):
+            assert np.array_equal(out[b, h], v[b, 0, h // 2])
+
+
+def test_zero_query_gives_mean_of_values(oracle_mod):
+    q = np.zeros((1, 4, 16))
+    k, v = _rand((1, 40, 2, 16), 12), _rand((1, 40, 2, 16), 13)
+    out = oracle_mod.decode(q, k, v, [29], 1.0)
+    for h in range(4):
+        np.testing.assert_allclose(out[0, h], v[0, :29, h // 2].mean(axis=0), rtol=0, atol=1e-14)
+
+
+def test_two_token_closed_form_fixes_sign_and_scale(oracle_mod):
+    """d=1, k_1=1, k_2=0: s_1 = scale*a, s_2 = 0, so o = (v1 e^{s1} + v2) / (e^{s1} + 1)."""
+    a, scale = 3.0, 0.25
+    q = np.array([[[a]]])
+    k = np.array([[[[1.0]], [[0.0]]]])
+    v = np.array([[[[2.0]], [[-5.0]]]])
+    out = oracle_mod.decode(q, k, v, [2], scale)
+    s1 = scale * a
+    expect = (2.0 * math.exp(s1) - 5.0) / (math.exp(s1) + 1.0)
+    assert out[0, 0, 0] == pytest.approx(expect, abs=1e-15)
+
+
+def test_large_scores_do_not_overflow_and_pick_dominant_key(oracle_mod):
+    d = 8
+    k = np.zeros((1, 5, 1, d))
+    k[0, :, 0, 0] = [1.0, 2.0, 3.0, 50.0, 4.0]
+    v = _rand((1, 5, 1, d), 14)
+    q = np.zeros((1, 1, d))
+    q[0, 0, 0] = 100.0                      # scores up to 5000: exp would overflow unshifted
+    out = oracle_mod.decode(q, k, v, [5], 1.0)
+    np.testing.assert_array_equal(out[0, 0], v[0, 3, 0])
+
+
+def test_permuting_tokens_leaves_output_unchanged(oracle_mod):
+    q, k, v = _rand((1, 4, 16), 15), _rand((1, 23, 2, 16), 16), _rand((1, 23, 2, 16), 17)
+    perm = np.random.default_rng(18).permutation(23)
+    a = oracle_mod.decode(q, k, v, [23], 0.25)
+    b = oracle_mod.decode(q, k[:, perm], v[:, perm], [23], 0.25)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
+
+
+def test_tokens_past_length_are_ignored(oracle_mod):
+    q, k, v = _rand((2, 4, 8), 19), _rand((2, 30, 2, 8), 20), _rand((2, 30, 2, 8), 21)
+    a = oracle_mod.decode(q, k, v, [12, 30], 0.5)
+    k2, v2 = k.copy(), v.copy()
+    k2[0, 12:] = np.nan
+    v2[0, 12:] = np.nan
+    b = oracle_mod.decode(q, k2, v2, [12, 30], 0.5)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_empty_context_gives_zero(oracle_mod):
+    q, k, v = _rand((2, 2, 8), 22), _rand((2, 4, 1, 8), 23), _rand((2, 4, 1, 8), 24)
+    out = oracle_mod.decode(q, k, v, [0, 4], 0.5)
+    assert np.all(out[0] == 0.0) and np.all(np.isfinite(out[1]))
+
+
+def test_thread_count_does_not_change_result(oracle_mod):
+    q, k, v = _rand((3, 8, 32), 25), _rand((3, 50, 2, 32), 26), _rand((3, 50, 2, 32), 27)
+    a = oracle_mod.decode(q, k, v, [50, 7, 31], 0.2, nthreads=1)
+    b = oracle_mod.decode(q, k, v, [50, 7, 31], 0.2, nthreads=5)
+    np.testing.assert_array_equal(a, b)
+
+
+# --------------------------------------------------------------------------- paging
+
+
+def test_gather_with_identity_table_is_a_reshape(oracle_mod):
+    B, S_pad, K, d = 2, 48, 2, 8
+    dense = _rand((B, S_pad, K, d), 28)
+    table = np.arange(B * 3).reshape(B, 3)
+    got = oracle_mod.gather_dense(dense, table, [40, 48], 16 * K * d, d, K * d, K, d)
+    np.testing.assert_array_equal(got[0, :40], dense[0, :40])
+    np.testing.assert_array_equal(got[1], dense[1])
+
+
+def test_append_then_gather_round_trips_through_a_shuffled_pool(oracle_mod):
+    """Scatter a sequence token by token into a pool with a shuffled table, then
+    gather it back: the block/slot arithmetic must invert exactly."""
+    B, K, d, S = 3, 2, 8, 37
+    nb_per = -(-S // 16)
+    NB = B * nb_per + 2
+    rng = np.random.default_rng(29)
+    perm = rng.permutation(NB)
+    table = perm[:B * nb_per].reshape(B, nb_per)
+    pool = np.full((NB, K, 16, d), np.nan)
+    seq = _rand((B, S, K, d), 30)
+    for t in range(S):
+        oracle_mod.append(pool, seq[:, t], table, [t] * B, K * 16 * d, 16 * d, d)
+    got = oracle_mod.gather_dense(pool, table, [S] * B, K * 16 * d, 16 * d, d, K, d)
+    np.testing.assert_array_equal(got, seq)
+    # exactly the slots written are non-NaN: B * S tokens * K heads * d elements
+    assert np.count_nonzero(~np.isnan(pool)) == B * S * K * d
+
+
+def test_block_padding_example_from_the_pages(oracle_mod):
+    with open(os.path.join(GOLDEN, "block_padding.json")) as f:
+        gold = json.load(f)
+    for case in gold["cases"]:
+        nb = oracle_mod.blocks_for_tokens(case["tokens"])
+        assert nb == case["blocks"]
+        assert nb * gold["block_size"] == case["slots"]
+        assert nb * gold["block_size"] - case["tokens"] == case["wasted"]
+        assert case["wasted"] <= gold["block_size"] - 1
+
+
+# --------------------------------------------------------------------------- KV size
+
+
+def test_kv_size_closed_form_reproduces_printed_figures(oracle_mod):
+    with open(os.path.join(GOLDEN, "kv_size_figures.json")) as f:
+        gold = json.load(f)
+    for key, g in gold.items():
+        if key.startswith("_"):
+            continue
+        n = oracle_mod.kv_cache_elements(g["layers"], g["kv_heads"], g["head_dim"],
+                                         g["seq_len"], g["batch"])
+        n_bytes = n * g.get("bytes_per_element", 1)
+        unit = {"1e9 elements": 1e9, "1e9 bytes": 1e9, "MiB": 2 ** 20}[g["unit"]]
+        scaled = n_bytes / unit
+        trunc = math.floor(scaled * 10 ** g["decimals"]) / 10 ** g["decimals"]
+        assert trunc == pytest.approx(g["printed"]), key
+    mha = oracle_mod.kv_cache_elements(80, 64, 128, 2048, 1)
+    gqa = oracle_mod.kv_cache_elements(80, 8, 128, 2048, 1)
+    assert (mha, gqa) == (2_684_354_560, 335_544_320)
+    assert mha == 8 * gqa                                  # KV bytes scale as 1/G
+
+
+# --------------------------------------------------------------------------- fp16 / int8
+
+
+def test_fp16_rounding_matches_numpy_everywhere(oracle_mod):
+    rng = np.random.default_rng(31)
+    vals = np.concatenate([
+        rng.standard_normal(4000).astype(np.float32) * np.float32(10.0) ** rng.integers(-9, 6, 4000),
+        np.array([0.0, -0.0, 65504.0, 65519.996, 65520.0, 1e6, -1e6, 2 ** -24, 2 ** -25,
+                  3 * 2 ** -26, 2 ** -14, 2 ** -14 - 2 ** -25, 6.1e-5, 1.0 + 2 ** -11,
+                  1.0 + 3 * 2 ** -11, 1.0 + 2 ** -11 + 2 ** -20, np.inf, -np.inf], dtype=np.float32),
+    ])
+    got = oracle_mod.f32_to_f16_bits(vals)
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    np.testing.assert_array_equal(got, ref)
+    back = oracle_mod.f16_bits_to_f64(ref)
+    np.testing.assert_array_equal(back, ref.view(np.float16).astype(np.float64))
+
+
+def test_int8_rounding_worked_example():
+    """amax = 127 gives scale exactly 1.0, so codes are rint(x) with ties to even."""
+    import oracle
+    x = np.array([[127.0, -63.5, 0.5, 1.5, 2.5, -2.5, 126.4, 0.0]], dtype=np.float32)
+    codes, scale = oracle.quantize_int8(x)
+    assert scale[0] == np.float16(1.0).view(np.uint16)
+    assert codes[0].tolist() == [127, -64, 0, 2, 2, -2, 126, 0]
+
+
+def test_int8_quantisation_invariants(oracle_mod):
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((500, 128)).astype(np.float32) * np.float32(10.0) ** rng.integers(-3, 4, (500, 1))
+    codes, sbits = oracle_mod.quantize_int8(x)
+    s = oracle_mod.f16_bits_to_f64(sbits)
+    # the row maximum lands on +-127 (scale is amax/127 within fp16 rounding)
+    assert np.all(np.abs(codes.astype(np.int32)).max(axis=1) == 127)
+    assert codes.min() >= -127
+    # reconstruction error of each element is at most half a step
+    err = np.abs(x.astype(np.float64) - codes * s[:, None])
+    assert np.all(err <= s[:, None] / 2 * (1 + 1e-6))
+    # symmetric: negating the input negates the codes and keeps the scale
+    c2, s2 = oracle_mod.quantize_int8(-x)
+    np.testing.assert_array_equal(c2, -codes)
+    np.testing.assert_array_equal(s2, sbits)
+    # a power-of-two rescale moves only the scale, while the scale stays a normal
+    # fp16 number (below 2**-14 fp16 has a fixed absolute step, so rounding differs)
+    c3, s3 = oracle_mod.quantize_int8(x * np.float32(4.0))
+    normal = s >= 2.0 ** -14
+    assert normal.sum() > 300
+    np.testing.assert_array_equal(c3[normal], codes[normal])
+    np.testing.assert_array_equal(oracle_mod.f16_bits_to_f64(s3)[normal], 4 * s[normal])
+    # an all-zero row quantises to scale 0 and codes 0
+    cz, sz = oracle_mod.quantize_int8(np.zeros((1, 64), dtype=np.float32))
+    assert sz[0] == 0 and not cz.any()
+
+
+def test_dequantised_attention_equals_attention_on_dequantised_values(oracle_mod):
+    """The int8 path is the float path fed q*s: the dequantised cache is exact in fp64."""
+    rng = np.random.default_rng(33)
+    x = rng.standard_normal((1, 20, 2, 64)).astype(np.float32)
+    codes, sb = oracle_mod.quantize_int8(x)
+    kv = oracle_mod.dequantize_int8(codes, oracle_mod.f16_bits_to_f64(sb))
+    q = _rand((1, 4, 64), 34)
+    got = oracle_mod.decode(q, kv, kv, [20], 0.125)
+    ref = _sdpa_reference(q, kv, kv, [20], 0.125)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    assert np.abs(kv - x).max() <= oracle_mod.f16_bits_to_f64(sb).max() / 2 * (1 + 1e-6)
+
+
+# --------------------------------------------------------------------------- generator
+
+
+def test_generator_poisons_only_unowned_slots(oracle_mod):
+    case = gi.make_case(3, 4, 2, 16, [5, 16, 33], "f32", seed=3)
+    pool = case.k_cache.numpy()
+    dense = oracle_mod.gather_dense(pool, case.block_table.numpy(), case.context_lens.numpy(),
+                                    case.stride_block, case.stride_head, case.stride_token, 2, 16)
+    for b, L in enumerate([5, 16, 33]):
+        assert np.isfinite(dense[b, :L]).all()
+    owned = 5 + 16 + 33
+    assert np.count_nonzero(~np.isnan(pool)) == owned * 2 * 16
