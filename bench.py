@@ -1,0 +1,443 @@
+"""Benchmark: one GQA decode step (paged KV append + split-KV decode + combine).
+
+Default workload: the Llama-3-8B-shaped paged decode (bf16, H=32, K=8, d=128,
+batch 64, every context 4096 tokens, block_size 16, shuffled block table).
+Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--kernel auto|mma|fma]
+
+N > 1 runs under torchrun as independent replicas (the step has no exchange):
+every rank decodes its own copy of the workload; value = bytes of all ranks /
+the slowest rank's time.
+
+Metric: achieved decode-attention bandwidth = algorithmic bytes of the step
+(K/V (+int8 scales) of every cached token read once, Q read, O written, block
+table and lengths read, the appended token's K/V written) / step time; also
+tokens/s = batch / step time for one attention layer.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention HBM GB/s (% of GB300 peak) and tokens/s per decode step, 1 GPU"
+DEFAULT_WORKLOAD = "llama3_8b_bf16_b64_s4096"
+L2_BYTES = 129 * 2 ** 20
+KERNEL_NAME = "split_kv_kernel"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kv_kernel_traffic.txt")
+
+
+def algorithmic_bytes(wl, lens) -> dict:
+    """Bytes a decode step must move: KV (+scales) of every cached token once,
+    q in, out (fp32) out, block-table entries and lengths, plus the append."""
+    es = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1}[wl.cache_dtype]
+    qes = {"f32": 4, "f16": 2, "bf16": 2}[wl.q_dtype]
+    tokens = int(sum(int(x) for x in lens))
+    per_token = 2 * wl.num_kv_heads * wl.head_dim * es
+    if wl.cache_dtype == "i8":
+        per_token += 2 * wl.num_kv_heads * 2
+    blocks = int(sum(-(-int(x) // 16) for x in lens))
+    B = len(lens)
+    kv = tokens * per_token
+    q = B * wl.num_heads * wl.head_dim * qes
+    o = B * wl.num_heads * wl.head_dim * 4
+    meta = blocks * 4 + B * 4
+    new_es = qes if wl.cache_dtype == "i8" else es
+    append = B * 2 * wl.num_kv_heads * wl.head_dim * (new_es + es) + B * 4
+    decode = kv + q + o + meta
+    return {"kv": kv, "decode": decode, "append": append, "step": decode + append,
+            "tokens": tokens, "blocks": blocks}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "gqa_decode_attention_kv_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source for this workload; else None."""
+    try:
+        lines = open(TRAFFIC_FILE).read().splitlines()
+    except OSError:
+        return None
+    vals = {}
+    for ln in lines:
+        if ":" in ln and not ln.startswith("#"):
+            k, _, v = ln.partition(":")
+            vals[k.strip()] = v.strip()
+    if vals.get("source_hash") != kernel_source_hash():
+        return None
+    if vals.get("workload") != workload or vals.get("kernel_variant", "auto") != kernel:
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ln in open(self.path).read().splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def kernel_code(name: str) -> int:
+    return {"auto": 0, "mma": 1, "fma": 2}[name]
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import gqa_inputs as gi
+    import gqa_decode_attention_kv_gb300 as gq
+    from gqa_decode_attention_kv_gb300 import build as gbuild
+
+    world, rank, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gbuild.build()
+    gq.load()
+
+    wl = gi.WORKLOADS[args.workload]
+    case = gi.case_for(wl, seed=args.seed + rank, device=str(dev), extra_tokens=0)
+    cache = gq.cache_from_case(case)
+    lens = case.context_lens
+    pos = (lens - 1).clamp(min=0)             # the step re-appends the last token
+    ab = algorithmic_bytes(wl, lens.cpu().tolist())
+    out = torch.empty((wl.batch, wl.num_heads, wl.head_dim), dtype=torch.float32, device=dev)
+    ws = gq.workspace_for(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kern = kernel_code(args.kernel)
+    stream = torch.cuda.current_stream()
+    launches_per_step = 3
+
+    def step(events=None):
+        gq.kv_append(cache, case.k_new, case.v_new, case.block_table, pos, err=err)
+        gq.gqa_decode(cache, case.q, case.block_table, lens, case.scale, out=out, workspace=ws,
+                      kernel=kern, events=events, err=err)
+
+    # warm-up
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if err.item() != 0:
+        raise RuntimeError(f"device error flags {err.item()}")
+
+    # per-launch events for the split-KV kernel (recorded inside the library)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in kev:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)                            # let the sampler see the load start
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(events=kev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+
+    # end to end through the public API with host buffers
+    q_h = torch.empty_like(case.q, device="cpu").pin_memory()
+    kn_h = torch.empty_like(case.k_new, device="cpu").pin_memory()
+    vn_h = torch.empty_like(case.v_new, device="cpu").pin_memory()
+    q_h.copy_(case.q)
+    kn_h.copy_(case.k_new)
+    vn_h.copy_(case.v_new)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, kn_d, vn_d = torch.empty_like(case.q), torch.empty_like(case.k_new), torch.empty_like(case.v_new)
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        kn_d.copy_(kn_h, non_blocking=True)
+        vn_d.copy_(vn_h, non_blocking=True)
+        gq.kv_append(cache, kn_d, vn_d, case.block_table, pos, err=err)
+        gq.gqa_decode(cache, q_d, case.block_table, lens, case.scale, out=out, workspace=ws,
+                      kernel=kern, err=err)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = q_h.numel() * q_h.element_size() + 2 * kn_h.numel() * kn_h.element_size()
+    d2h = out_h.numel() * out_h.element_size()
+    if err.item() != 0:
+        raise RuntimeError(f"device error flags {err.item()}")
+
+    # slowest rank decides
+    t = torch.tensor([ms, e2e_ms, kern_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms, e2e_ms, kern_ms = (float(x) for x in t.tolist())
+
+    if rank == 0:
+        peaks, peak_kind = measured_peaks()
+        hbm = float(peaks["hbm_gbs"])
+        gbs = ab["step"] * world / (ms * 1e-3) / 1e9
+        kern_gbs = ab["decode"] / (kern_ms * 1e-3) / 1e9
+        traffic = read_traffic(args.workload, args.kernel)
+        line = {
+            "metric": METRIC,
+            "value": round(gbs, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": max(3, args.warmup),
+            "ms_per_step": round(ms, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": wl.cache_dtype,
+            "data": "synthetic",
+            "config": {"workload": wl.name, "batch": wl.batch, "num_heads": wl.num_heads,
+                       "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                       "context_lens": wl.lens, "cache_dtype": wl.cache_dtype,
+                       "q_dtype": wl.q_dtype, "block_size": 16, "block_table": "seeded shuffle",
+                       "kernel": args.kernel,
+                       "l2": f"inputs larger than L2: {ab['kv'] / 1e9:.2f} GB of K/V per step > 129 MB",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "step": "kv_append + gqa_decode (split-KV + combine), one attention layer"},
+            "tokens_per_s": round(wl.batch * world / (ms * 1e-3), 1),
+            "pct_of_peak": {"measured_hbm": round(100 * gbs / world / hbm, 2),
+                            "nominal_8tbs": round(100 * gbs / world / 8000.0, 2)},
+            "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 2), "peak": hbm,
+                         "unit": "GB/s", "frac": round(kern_gbs / hbm, 4),
+                         "traffic": traffic, "kernel": KERNEL_NAME,
+                         "algorithmic_bytes_per_launch": ab["decode"],
+                         "avg_launch_ms": round(kern_ms, 5),
+                         "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"},
+            "e2e": {"value": round(ab["step"] * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 5)},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl, case, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def _oracle_inputs(wl, case, rows):
+    import numpy as np
+    import oracle
+    lens = case.context_lens.cpu().numpy()
+    table = case.block_table.cpu().numpy()
+    sel = []
+    for b in rows:
+        nb = -(-int(lens[b]) // 16)
+        sel.append(table[b, :nb])
+    # copy only the blocks the sampled sequences use
+    import torch
+    ids = torch.from_numpy(np.concatenate(sel).astype(np.int64)).to(case.k_cache.device)
+    def host(t):
+        t = t.index_select(0, ids)
+        return t.cpu().numpy() if t.dtype == torch.int8 else t.float().cpu().numpy()
+    kp, vp = host(case.k_cache), host(case.v_cache)
+    new_table = np.zeros((len(rows), table.shape[1]), dtype=np.int64)
+    off = 0
+    for i, s in enumerate(sel):
+        new_table[i, :len(s)] = np.arange(off, off + len(s))
+        off += len(s)
+    sub_lens = lens[rows]
+    K, d = wl.num_kv_heads, wl.head_dim
+    sb, sh, st = K * 16 * d, 16 * d, d
+    kd = oracle.gather_dense(kp, new_table, sub_lens, sb, sh, st, K, d).astype(np.float64)
+    vd = oracle.gather_dense(vp, new_table, sub_lens, sb, sh, st, K, d).astype(np.float64)
+    if wl.cache_dtype == "i8":
+        ksp = case.k_scale.index_select(0, ids).float().cpu().numpy()
+        vsp = case.v_scale.index_select(0, ids).float().cpu().numpy()
+        kd = oracle.dequantize_int8(kd, oracle.gather_scales(ksp, new_table, sub_lens, K))
+        vd = oracle.dequantize_int8(vd, oracle.gather_scales(vsp, new_table, sub_lens, K))
+    q = case.q.float().cpu().numpy().astype(np.float64)[rows]
+    return q, kd, vd, sub_lens
+
+
+def cpu_baseline(wl, case, seconds: float) -> dict:
+    """Time the oracle, as it stands, on a bounded sample of the workload."""
+    import oracle
+    oracle.build()
+    threads = oracle.num_cpus()
+    rows = [0]
+    q, kd, vd, sl = _oracle_inputs(wl, case, rows)
+    t = time.perf_counter()
+    oracle.decode(q, kd, vd, sl, case.scale, nthreads=threads)
+    one = time.perf_counter() - t
+    n = max(1, min(wl.batch, int(seconds / max(one, 1e-3))))
+    rows = list(range(n))
+    q, kd, vd, sl = _oracle_inputs(wl, case, rows)
+    t = time.perf_counter()
+    oracle.decode(q, kd, vd, sl, case.scale, nthreads=threads)
+    dt = time.perf_counter() - t
+    lens = case.context_lens.cpu().tolist()
+    sub = algorithmic_bytes(wl, [lens[b] for b in rows])
+    return {"value": round(sub["decode"] / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"{n} of {wl.batch} sequences (all {wl.num_heads} heads), fp64 C oracle, "
+                      f"decode only"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step decodes a bounded sample of the
+    workload on the host cores (rank 0 only)."""
+    import torch
+    world, rank, local = dist_info()
+    if rank != 0:
+        return
+    import gqa_inputs as gi
+    import oracle
+    oracle.build()
+    wl = gi.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    case = gi.case_for(wl, seed=args.seed, device=dev, extra_tokens=0)
+    threads = oracle.num_cpus()
+    rows = [0]
+    q, kd, vd, sl = _oracle_inputs(wl, case, rows)
+    lens = case.context_lens.cpu().tolist()
+    sample_bytes = algorithmic_bytes(wl, [lens[b] for b in rows])["decode"]
+    for _ in range(max(3, args.warmup)):
+        oracle.decode(q, kd, vd, sl, case.scale, nthreads=threads)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.decode(q, kd, vd, sl, case.scale, nthreads=threads)
+        times.append(time.perf_counter() - t)
+    dt = statistics.mean(times)
+    v = round(sample_bytes / dt / 1e9, 4)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "num_heads": wl.num_heads,
+                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "context_lens": wl.lens, "cache_dtype": wl.cache_dtype},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"1 of {wl.batch} sequences (all {wl.num_heads} heads) per step, "
+                                   "fp64 C oracle"},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--kernel", choices=["auto", "mma", "fma"], default="auto")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

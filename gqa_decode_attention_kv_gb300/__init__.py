@@ -1,0 +1,236 @@
+"""Python binding of the GB300 grouped-query decode-attention library.
+
+Argument marshalling only: tensors are passed to the C ABI in
+``include/gqa_decode.h`` as raw device pointers with the current CUDA stream;
+every step of the computation runs in the library's CUDA kernels. PyTorch
+provides device memory and streams. There is no fallback: if the compiled
+library is missing, loading raises.
+
+Entry points (same names as the C ABI, without the ``gqa_`` prefix where it
+would repeat the module name):
+
+* ``kv_append``            -- write one new token per sequence into the paged cache
+* ``gqa_decode``           -- grouped-query decode attention over the paged cache
+* ``decode_workspace_size``-- workspace bytes ``gqa_decode`` needs
+* ``kv_pool_elements``     -- elements a pool of ``num_blocks`` blocks holds (K and V)
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+BLOCK_SIZE = 16
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int8: 3}
+
+GQA_DEVERR_BLOCK_INDEX = 1
+GQA_DEVERR_CONTEXT_LEN = 2
+GQA_DEVERR_POSITION = 4
+GQA_DEVERR_TIMEOUT = 8
+
+KERNEL_AUTO, KERNEL_MMA, KERNEL_FMA = 0, 1, 2
+
+
+class GqaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class KVCacheDesc(ctypes.Structure):
+    """Mirror of gqa_kv_cache_t."""
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("num_blocks", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("stride_block", ctypes.c_int64),
+                ("stride_head", ctypes.c_int64), ("stride_token", ctypes.c_int64)]
+
+
+class DecodeOpts(ctypes.Structure):
+    """Mirror of gqa_decode_opts_t."""
+    _fields_ = [("kernel", ctypes.c_int32), ("max_warps", ctypes.c_int32),
+                ("min_blocks_per_warp", ctypes.c_int32),
+                ("event_main_begin", ctypes.c_void_p), ("event_main_end", ctypes.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load the compiled library (build it first with ``build.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(f"CUDA library not built: {path} is missing "
+                                   "(run gqa_decode_attention_kv_gb300.build.build())")
+            lib = ctypes.CDLL(path)
+            vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            lib.gqa_status_string.argtypes = [ctypes.c_int]
+            lib.gqa_status_string.restype = ctypes.c_char_p
+            lib.gqa_version.argtypes = []
+            lib.gqa_version.restype = ctypes.c_int
+            lib.gqa_kv_pool_elements.argtypes = [i64, i32, i32]
+            lib.gqa_kv_pool_elements.restype = i64
+            lib.gqa_kv_append.argtypes = [ctypes.POINTER(KVCacheDesc), vp, vp, i32, vp, i32, vp,
+                                          i32, vp, vp]
+            lib.gqa_kv_append.restype = ctypes.c_int
+            lib.gqa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+            lib.gqa_decode_workspace_size.restype = ctypes.c_size_t
+            lib.gqa_decode.argtypes = [ctypes.POINTER(KVCacheDesc), vp, i32, i32, vp, i32, vp, i32,
+                                       ctypes.c_float, vp, i32, vp, ctypes.c_size_t,
+                                       ctypes.POINTER(DecodeOpts), vp, vp]
+            lib.gqa_decode.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().gqa_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(load().gqa_version())
+
+
+def kv_pool_elements(num_blocks: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(load().gqa_kv_pool_elements(num_blocks, num_kv_heads, head_dim))
+
+
+@dataclasses.dataclass
+class PagedKVCache:
+    """Device tensors of one paged KV cache plus their element strides.
+
+    Default layout is the pool ``[num_blocks, K, 16, d]``; any layout whose
+    element of (block p, kv-head g, slot s, dim i) is at
+    ``p*stride_block + g*stride_head + s*stride_token + i`` works."""
+    k: torch.Tensor
+    v: torch.Tensor
+    num_blocks: int
+    num_kv_heads: int
+    head_dim: int
+    stride_block: int
+    stride_head: int
+    stride_token: int
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
+
+    @staticmethod
+    def allocate(num_blocks: int, num_kv_heads: int, head_dim: int, dtype: torch.dtype,
+                 device="cuda") -> "PagedKVCache":
+        shape = (num_blocks, num_kv_heads, BLOCK_SIZE, head_dim)
+        k = torch.empty(shape, dtype=dtype, device=device)
+        v = torch.empty(shape, dtype=dtype, device=device)
+        ks = vs = None
+        if dtype == torch.int8:
+            ks = torch.empty((num_blocks, num_kv_heads, BLOCK_SIZE), dtype=torch.float16, device=device)
+            vs = torch.empty_like(ks)
+        return PagedKVCache(k, v, num_blocks, num_kv_heads, head_dim,
+                            num_kv_heads * BLOCK_SIZE * head_dim, BLOCK_SIZE * head_dim, head_dim,
+                            ks, vs)
+
+    @property
+    def dtype(self) -> torch.dtype:
+        return self.k.dtype
+
+    def desc(self) -> KVCacheDesc:
+        return KVCacheDesc(
+            self.k.data_ptr(), self.v.data_ptr(),
+            self.k_scale.data_ptr() if self.k_scale is not None else None,
+            self.v_scale.data_ptr() if self.v_scale is not None else None,
+            self.num_blocks, self.num_kv_heads, BLOCK_SIZE, self.head_dim,
+            DTYPE_CODE[self.k.dtype], self.stride_block, self.stride_head, self.stride_token)
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise GqaError(status, where)
+
+
+def kv_append(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tensor,
+              block_tables: torch.Tensor, positions: torch.Tensor,
+              err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Write k_new/v_new [B, K, d] at slot positions[b] of each sequence's paged cache."""
+    desc = cache.desc()
+    st = load().gqa_kv_append(ctypes.byref(desc), _ptr(k_new), _ptr(v_new),
+                              DTYPE_CODE[k_new.dtype], _ptr(block_tables),
+                              int(block_tables.shape[1]), _ptr(positions), int(positions.shape[0]),
+                              _ptr(err), _stream_ptr(stream))
+    _check(st, "gqa_kv_append")
+
+
+def decode_workspace_size(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                          device: int = -1) -> int:
+    return int(load().gqa_decode_workspace_size(batch, num_heads, num_kv_heads, head_dim, device))
+
+
+_ws_cache: dict = {}
+
+
+def workspace_for(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                  device: torch.device) -> torch.Tensor:
+    """A cached device workspace large enough for this shape (grown on demand)."""
+    dev = torch.device(device)
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    need = decode_workspace_size(batch, num_heads, num_kv_heads, head_dim, idx)
+    if need == 0:
+        raise ValueError("no workspace size for this shape")
+    buf = _ws_cache.get(idx)
+    if buf is None or buf.numel() < need:
+        buf = torch.empty(need, dtype=torch.uint8, device=dev)
+        _ws_cache[idx] = buf
+    return buf
+
+
+def gqa_decode(cache: PagedKVCache, q: torch.Tensor, block_tables: torch.Tensor,
+               context_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+               out_dtype: torch.dtype = torch.float32, workspace: Optional[torch.Tensor] = None,
+               kernel: int = KERNEL_AUTO, max_warps: int = 0, min_blocks_per_warp: int = 0,
+               events: Optional[tuple] = None, err: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """out[b,h] = softmax(scale * q[b,h] . K_g^T) V_g over context_lens[b] cached tokens."""
+    B, H, d = q.shape
+    if out is None:
+        out = torch.empty((B, H, d), dtype=out_dtype, device=q.device)
+    if workspace is None:
+        workspace = workspace_for(B, H, cache.num_kv_heads, d, q.device)
+    opts = DecodeOpts(kernel, max_warps, min_blocks_per_warp, None, None)
+    if events is not None:
+        opts.event_main_begin = events[0].cuda_event
+        opts.event_main_end = events[1].cuda_event
+    desc = cache.desc()
+    st = load().gqa_decode(ctypes.byref(desc), _ptr(q), DTYPE_CODE[q.dtype], H, _ptr(block_tables),
+                           int(block_tables.shape[1]), _ptr(context_lens), B, float(scale),
+                           _ptr(out), DTYPE_CODE[out.dtype], _ptr(workspace), workspace.numel(),
+                           ctypes.byref(opts), _ptr(err), _stream_ptr(stream))
+    _check(st, "gqa_decode")
+    return out
+
+
+def cache_from_case(case) -> PagedKVCache:
+    """Wrap the device tensors of a generated decode case (gqa_inputs.DecodeCase)."""
+    return PagedKVCache(case.k_cache, case.v_cache, case.num_blocks, case.num_kv_heads,
+                        case.head_dim, case.stride_block, case.stride_head, case.stride_token,
+                        case.k_scale, case.v_scale)

@@ -1,0 +1,179 @@
+// gqa_append.cu -- paged KV append: the new token's K and V of every
+// (sequence, kv-head) go to slot pos % 16 of block block_tables[b][pos / 16]
+// ("LLM 推理性能优化实战", sections 5.3-5.4 and 8.2). One warp per
+// (sequence, kv-head) writes both rows, so K and V of a token leave together.
+// For an int8 cache each row is quantised on the way (symmetric, one fp16
+// scale per (token, kv-head); sections 15.1, 15.2 and 15.5 of that page).
+#include "gqa_device.cuh"
+#include "gqa_internal.h"
+
+namespace gqa {
+
+namespace {
+
+struct AppendArgs {
+    void* k_cache;
+    void* v_cache;
+    __half* k_scale;
+    __half* v_scale;
+    const void* k_new;
+    const void* v_new;
+    const int32_t* block_tables;
+    const int32_t* positions;
+    int32_t* err;
+    long long num_blocks;
+    long long sb, sh, st;   // element strides of the cache
+    int batch, K, d, max_blocks, es;
+};
+
+constexpr int kWarpsPerCta = 4;
+
+// Resolve (b, g) -> element offset of the destination row, or -1 after flagging.
+__device__ __forceinline__ long long dest_offset(const AppendArgs& a, int b, int g, int lane) {
+    const int pos = a.positions[b];
+    if (pos < 0 || pos >= a.max_blocks * kBlock) {
+        if (lane == 0 && g == 0) flag_error(a.err, GQA_DEVERR_POSITION);
+        return -1;
+    }
+    const int phys = a.block_tables[(long long)b * a.max_blocks + pos / kBlock];
+    if (phys < 0 || phys >= a.num_blocks) {
+        if (lane == 0 && g == 0) flag_error(a.err, GQA_DEVERR_BLOCK_INDEX);
+        return -1;
+    }
+    return (long long)phys * a.sb + (long long)g * a.sh + (long long)(pos % kBlock) * a.st;
+}
+
+// Bit-exact copy for f32/f16/bf16 caches, 16 bytes per lane step.
+__global__ void __launch_bounds__(kWarpsPerCta * 32) append_copy_kernel(const AppendArgs a) {
+    const int lane = threadIdx.x & 31;
+    const long long pair = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    if (pair >= (long long)a.batch * a.K) return;
+    const int b = (int)(pair / a.K), g = (int)(pair % a.K);
+    const long long off = dest_offset(a, b, g, lane);
+    if (off < 0) return;
+    const int row_bytes = a.d * a.es;
+    const int nvec = row_bytes / 16;                 // 16-byte vectors per row
+    const long long src = ((long long)b * a.K + g) * row_bytes;
+    for (int i = lane; i < 2 * nvec; i += 32) {
+        const bool is_v = i >= nvec;
+        const int vi = is_v ? i - nvec : i;
+        const uint8_t* s = static_cast<const uint8_t*>(is_v ? a.v_new : a.k_new) + src + vi * 16;
+        uint8_t* dptr = static_cast<uint8_t*>(is_v ? a.v_cache : a.k_cache) + off * a.es + vi * 16;
+        *reinterpret_cast<uint4*>(dptr) = *reinterpret_cast<const uint4*>(s);
+    }
+}
+
+template <typename In>
+__device__ __forceinline__ float load_as_float(const void* p, long long i) {
+    if constexpr (sizeof(In) == 4) return static_cast<const float*>(p)[i];
+    else if constexpr (std::is_same<In, __half>::value) return __half2float(static_cast<const __half*>(p)[i]);
+    else return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+}
+
+// Quantise one row of d values held EPL per lane; returns the scale, writes codes.
+template <typename In, int EPL>
+__device__ __forceinline__ void quantise_row(const void* src, long long src_off, int8_t* dst,
+                                             __half* scale_dst, int lane) {
+    float x[EPL];
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+        x[e] = load_as_float<In>(src, src_off + lane * EPL + e);
+        amax = fmaxf(amax, fabsf(x[e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    float s32 = __fdiv_rn(amax, 127.0f);
+    s32 = fminf(s32, 65504.0f);
+    const __half sh = __float2half_rn(s32);
+    const float sf = __half2float(sh);
+    uint32_t packed[EPL / 4 > 0 ? EPL / 4 : 1] = {};
+    int8_t codes[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+        int q = 0;
+        if (sf != 0.f) {
+            q = __float2int_rn(__fdiv_rn(x[e], sf));
+            q = max(-127, min(127, q));
+        }
+        codes[e] = static_cast<int8_t>(q);
+    }
+    if constexpr (EPL % 4 == 0) {
+#pragma unroll
+        for (int w = 0; w < EPL / 4; ++w)
+            packed[w] = (uint32_t)(uint8_t)codes[4 * w] | ((uint32_t)(uint8_t)codes[4 * w + 1] << 8) |
+                        ((uint32_t)(uint8_t)codes[4 * w + 2] << 16) |
+                        ((uint32_t)(uint8_t)codes[4 * w + 3] << 24);
+#pragma unroll
+        for (int w = 0; w < EPL / 4; ++w)
+            reinterpret_cast<uint32_t*>(dst + lane * EPL)[w] = packed[w];
+    } else {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) dst[lane * EPL + e] = codes[e];
+    }
+    if (lane == 0) *scale_dst = sh;
+}
+
+template <typename In, int EPL>
+__global__ void __launch_bounds__(kWarpsPerCta * 32) append_quant_kernel(const AppendArgs a) {
+    const int lane = threadIdx.x & 31;
+    const long long pair = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    if (pair >= (long long)a.batch * a.K) return;
+    const int b = (int)(pair / a.K), g = (int)(pair % a.K);
+    const long long off = dest_offset(a, b, g, lane);
+    if (off < 0) return;
+    const int pos = a.positions[b];
+    const int phys = a.block_tables[(long long)b * a.max_blocks + pos / kBlock];
+    const long long sidx = ((long long)phys * a.K + g) * kBlock + pos % kBlock;
+    const long long src = ((long long)b * a.K + g) * a.d;
+    quantise_row<In, EPL>(a.k_new, src, static_cast<int8_t*>(a.k_cache) + off, a.k_scale + sidx, lane);
+    quantise_row<In, EPL>(a.v_new, src, static_cast<int8_t*>(a.v_cache) + off, a.v_scale + sidx, lane);
+}
+
+template <typename In>
+cudaError_t launch_quant(const AppendArgs& a, int grid, cudaStream_t s) {
+    if (a.d == 64) append_quant_kernel<In, 2><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
+    else append_quant_kernel<In, 4><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const void* v_new,
+                             int new_dtype, const int32_t* block_tables, int max_blocks,
+                             const int32_t* positions, int batch, int32_t* err,
+                             cudaStream_t stream) {
+    AppendArgs a;
+    a.k_cache = c.k;
+    a.v_cache = c.v;
+    a.k_scale = static_cast<__half*>(c.k_scale);
+    a.v_scale = static_cast<__half*>(c.v_scale);
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.block_tables = block_tables;
+    a.positions = positions;
+    a.err = err;
+    a.num_blocks = c.num_blocks;
+    a.sb = c.stride_block;
+    a.sh = c.stride_head;
+    a.st = c.stride_token;
+    a.batch = batch;
+    a.K = c.num_kv_heads;
+    a.d = c.head_dim;
+    a.max_blocks = max_blocks;
+    a.es = dtype_size(c.dtype);
+    const long long warps = (long long)batch * c.num_kv_heads;
+    const int grid = (int)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
+    if (grid == 0) return cudaSuccess;
+    if (c.dtype != GQA_DTYPE_I8) {
+        append_copy_kernel<<<grid, kWarpsPerCta * 32, 0, stream>>>(a);
+        return cudaGetLastError();
+    }
+    switch (new_dtype) {
+        case GQA_DTYPE_F32: return launch_quant<float>(a, grid, stream);
+        case GQA_DTYPE_F16: return launch_quant<__half>(a, grid, stream);
+        default: return launch_quant<__nv_bfloat16>(a, grid, stream);
+    }
+}
+
+}  // namespace gqa

@@ -1,0 +1,205 @@
+// gqa_capi.cu -- the extern "C" entry points of include/gqa_decode.h: argument
+// validation, TMA descriptor encoding and dispatch to the kernels.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "gqa_internal.h"
+
+namespace gqa {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int num_sms_of(int device) {
+    if (device < 0 && cudaGetDevice(&device) != cudaSuccess) return -1;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return -1;
+    return n;
+}
+
+// Checks shared by append and decode.
+int check_cache(const gqa_kv_cache_t* c) {
+    if (!c || !c->k || !c->v) return GQA_ERR_INVALID;
+    if (c->block_size != GQA_BLOCK_SIZE) return GQA_ERR_UNSUPPORTED;
+    if (c->num_blocks <= 0 || c->num_blocks > 0x7fffffffLL || c->num_kv_heads <= 0)
+        return GQA_ERR_INVALID;
+    if (c->head_dim != 64 && c->head_dim != 128) return GQA_ERR_UNSUPPORTED;
+    const int es = dtype_size(c->dtype);
+    if (es == 0) return GQA_ERR_INVALID;
+    if (c->stride_block <= 0 || c->stride_head <= 0 || c->stride_token < c->head_dim)
+        return GQA_ERR_INVALID;
+    if ((c->stride_block * es) % 16 || (c->stride_head * es) % 16 || (c->stride_token * es) % 16)
+        return GQA_ERR_INVALID;
+    if (!aligned16(c->k) || !aligned16(c->v)) return GQA_ERR_INVALID;
+    if (c->dtype == GQA_DTYPE_I8) {
+        if (!c->k_scale || !c->v_scale) return GQA_ERR_INVALID;
+        if (!aligned16(c->k_scale) || !aligned16(c->v_scale)) return GQA_ERR_INVALID;
+    }
+    return GQA_OK;
+}
+
+}  // namespace
+
+bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int box_inner,
+                      bool swizzle128, int perm[3]) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return false;
+    CUtensorMapDataType dt;
+    switch (c.dtype) {
+        case GQA_DTYPE_F32: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; break;
+        case GQA_DTYPE_F16: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; break;
+        case GQA_DTYPE_BF16: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; break;
+        default: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;
+    }
+    const int es = dtype_size(c.dtype);
+    // outer axes: 0 slot, 1 kv-head, 2 block; sort by stride
+    const long long stride[3] = {c.stride_token, c.stride_head, c.stride_block};
+    const long long extent[3] = {GQA_BLOCK_SIZE, c.num_kv_heads, c.num_blocks};
+    int order[3] = {0, 1, 2};
+    std::stable_sort(order, order + 3, [&](int x, int y) { return stride[x] < stride[y]; });
+    cuuint64_t gdim[4] = {(cuuint64_t)c.head_dim, 0, 0, 0};
+    cuuint64_t gstride[3];
+    cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, 1, 1};
+    cuuint32_t estride[4] = {1, 1, 1, 1};
+    for (int i = 0; i < 3; ++i) {
+        perm[i] = order[i];
+        gdim[i + 1] = (cuuint64_t)extent[order[i]];
+        gstride[i] = (cuuint64_t)(stride[order[i]] * es);
+        if (order[i] == 0) box[i + 1] = GQA_BLOCK_SIZE;
+    }
+    const CUresult r = enc(map, dt, 4, const_cast<void*>(base), gdim, gstride, box, estride,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace gqa
+
+using namespace gqa;
+
+extern "C" {
+
+const char* gqa_status_string(int status) {
+    switch (status) {
+        case GQA_OK: return "ok";
+        case GQA_ERR_INVALID: return "invalid argument";
+        case GQA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case GQA_ERR_WORKSPACE: return "workspace missing or too small";
+        case GQA_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+int gqa_version(void) { return 100; }
+
+int64_t gqa_kv_pool_elements(int64_t num_blocks, int32_t num_kv_heads, int32_t head_dim) {
+    if (num_blocks < 0 || num_kv_heads < 0 || head_dim < 0) return -1;
+    return 2 * num_blocks * (int64_t)num_kv_heads * GQA_BLOCK_SIZE * (int64_t)head_dim;
+}
+
+int gqa_kv_append(const gqa_kv_cache_t* cache, const void* k_new, const void* v_new,
+                  int32_t new_dtype, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                  const int32_t* positions, int32_t batch, int32_t* err_flag, void* stream) {
+    int st = check_cache(cache);
+    if (st != GQA_OK) return st;
+    if (batch < 0 || max_blocks_per_seq <= 0) return GQA_ERR_INVALID;
+    if (batch == 0) return GQA_OK;
+    if (!k_new || !v_new || !block_tables || !positions) return GQA_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new)) return GQA_ERR_INVALID;
+    if ((long long)max_blocks_per_seq * GQA_BLOCK_SIZE > 0x7fffffffLL) return GQA_ERR_INVALID;
+    if (cache->dtype == GQA_DTYPE_I8) {
+        if (new_dtype != GQA_DTYPE_F32 && new_dtype != GQA_DTYPE_F16 && new_dtype != GQA_DTYPE_BF16)
+            return GQA_ERR_UNSUPPORTED;
+    } else if (new_dtype != cache->dtype) {
+        return GQA_ERR_UNSUPPORTED;
+    }
+    const cudaError_t e = launch_kv_append(*cache, k_new, v_new, new_dtype, block_tables,
+                                           max_blocks_per_seq, positions, batch, err_flag,
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+size_t gqa_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t device) {
+    if (batch < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return 0;
+    if (head_dim != 64 && head_dim != 128) return 0;
+    const int sms = num_sms_of(device);
+    if (sms <= 0) return 0;
+    return decode_workspace_bytes(batch, num_heads, num_kv_heads, head_dim, sms);
+}
+
+int gqa_decode(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int32_t num_heads,
+               const int32_t* block_tables, int32_t max_blocks_per_seq,
+               const int32_t* context_lens, int32_t batch, float scale, void* out,
+               int32_t out_dtype, void* workspace, size_t workspace_bytes,
+               const gqa_decode_opts_t* opts, int32_t* err_flag, void* stream) {
+    int st = check_cache(cache);
+    if (st != GQA_OK) return st;
+    if (batch < 0 || num_heads <= 0 || max_blocks_per_seq <= 0) return GQA_ERR_INVALID;
+    if (num_heads % cache->num_kv_heads) return GQA_ERR_INVALID;
+    if (num_heads / cache->num_kv_heads > kMaxGroup) return GQA_ERR_UNSUPPORTED;
+    if (batch > kMaxBatch) return GQA_ERR_UNSUPPORTED;
+    if ((long long)batch * cache->num_kv_heads * max_blocks_per_seq >= 0x7fffffffLL)
+        return GQA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return GQA_ERR_INVALID;
+    if (batch == 0) return GQA_OK;
+    if (!q || !block_tables || !context_lens || !out) return GQA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(out)) return GQA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GQA_ERR_INVALID;
+    if (out_dtype != GQA_DTYPE_F32 && out_dtype != GQA_DTYPE_BF16 && out_dtype != GQA_DTYPE_F16)
+        return GQA_ERR_UNSUPPORTED;
+    const int cd = cache->dtype;
+    const bool q_ok = (cd == GQA_DTYPE_I8) ? (q_dtype == GQA_DTYPE_BF16 || q_dtype == GQA_DTYPE_F16)
+                                           : (q_dtype == cd);
+    if (!q_ok) return GQA_ERR_UNSUPPORTED;
+    int kernel = opts ? opts->kernel : 0;
+    if (kernel < 0 || kernel > 2) return GQA_ERR_INVALID;
+    const int sms = num_sms_of(-1);
+    if (sms <= 0) return GQA_ERR_CUDA;
+
+    DecodeLaunch L;
+    L.cache = cache;
+    L.q = q;
+    L.q_dtype = q_dtype;
+    L.num_heads = num_heads;
+    L.block_tables = block_tables;
+    L.max_blocks = max_blocks_per_seq;
+    L.context_lens = context_lens;
+    L.batch = batch;
+    L.scale = scale;
+    L.out = out;
+    L.out_dtype = out_dtype;
+    L.workspace = workspace;
+    L.workspace_bytes = workspace_bytes;
+    L.kernel = kernel;
+    L.max_warps = opts ? std::max(0, opts->max_warps) : 0;
+    L.min_blocks_per_warp = opts ? std::max(0, opts->min_blocks_per_warp) : 0;
+    L.ev_begin = opts ? static_cast<cudaEvent_t>(opts->event_main_begin) : nullptr;
+    L.ev_end = opts ? static_cast<cudaEvent_t>(opts->event_main_end) : nullptr;
+    L.err = err_flag;
+    L.stream = static_cast<cudaStream_t>(stream);
+    return launch_decode(L, sms);
+}
+
+}  // extern "C"

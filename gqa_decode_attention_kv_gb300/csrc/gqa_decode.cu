@@ -1,0 +1,931 @@
+// gqa_decode.cu -- split-KV grouped-query decode attention over a paged cache.
+//
+// What is computed (per sequence b, query head h, group g = h / G, G = H/K):
+//   out[b,h,:] = sum_t softmax_t(scale * q[b,h,:] . K[b,t,g,:]) V[b,t,g,:]
+// ("分组查询注意力 (GQA)", 技术原理 steps 2-4 and its attention equation).
+//
+// How (GB300 design):
+//  * Work unit = one 16-token cache block of one (sequence, kv-head) pair. All
+//    units are laid out in (b, g, block) order and cut into equal contiguous
+//    ranges, one per warp of a single resident wave (persistent, stream-K
+//    style). A pair that straddles ranges becomes several KV splits
+//    (Flash-Decoding, "LLM 推理性能优化实战" section 10.2); the cut is found on
+//    the device from context_lens, so no host synchronisation is needed.
+//  * Each warp streams its blocks through a private ring of shared-memory
+//    stages filled by TMA (cp.async.bulk.tensor, 4-D tensor map over the
+//    paged pool, mbarrier completion). The block table is consulted per unit;
+//    each K/V tile is read from HBM exactly once and serves all G query heads
+//    of its group (the group broadcast of the GQA page's 下游 section).
+//  * Tensor-core kernel: scores S^T[16 tokens x 8 heads] = K_tile Q^T and the
+//    update O^T[d x 8 heads] += V_tile^T P^T with mma.sync m16n8k16 (bf16 or
+//    f16 in, fp32 accumulate). P is split into a high and a low 16-bit part
+//    so the product keeps ~16 significant bits. Online softmax in fp32 with
+//    the running (m, l, o) state of "LLM 推理性能优化实战" section 9.2; the
+//    rescale is skipped while the block maximum stays within 2^kRescaleSlack
+//    of the running one (o and l share the stale maximum, so o/l is exact).
+//  * CUDA-core kernel: same pipeline, one token at a time with fp32 FMAs and
+//    warp-shuffle reductions; used for fp32 caches and as the measured
+//    alternative to the tensor-core kernel.
+//  * A second kernel merges the splits of each pair with their log-sum-exp
+//    weights: M = max m_s, L = sum l_s 2^(m_s-M), o = sum o_s 2^(m_s-M) / L
+//    (the "global max and sum" reduction of section 10.2), in base 2.
+#include <algorithm>
+#include <type_traits>
+
+#include "gqa_device.cuh"
+#include "gqa_internal.h"
+
+namespace gqa {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeArgs {
+    const void* q;
+    const __half* k_scale;
+    const __half* v_scale;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    void* out;
+    int32_t* err;
+    int32_t* ws_hdr;     // [0] units per warp R, [1] total units U
+    int32_t* ws_pref;    // [B+1] exclusive prefix of blocks per sequence
+    float2* ws_ml;       // [slots][G] (running max m in log2 units, running sum l)
+    float* ws_o;         // [slots][G][D] un-normalised partial outputs
+    long long num_blocks;
+    int B, H, K, G, max_blocks, out_dtype, q_dtype, P, min_units;
+    int map_perm[3];     // tensor-map dims 1..3 -> 0 slot, 1 kv-head, 2 block
+    float scale_log2;    // scale * log2(e)
+};
+
+template <int kKind, typename T, int D>
+struct Cfg {
+    static constexpr bool kI8 = std::is_same<T, int8_t>::value;
+    static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    static constexpr int kEs = sizeof(T);
+    static constexpr int kTile = 16 * D * kEs;                       // one (block, head) tile
+    static constexpr int kScaleBytes = kI8 ? 64 : 0;                // 16 k + 16 v fp16 scales
+    static constexpr int kStage = ((2 * kTile + kScaleBytes + 1023) / 1024) * 1024;
+    static constexpr int kStages = std::max(2, std::min(6, 24576 / kStage));
+    static constexpr int kWarps = 4;
+    static constexpr bool kSwizzle = (kKind == kKernelMma);
+    static constexpr int kBoxInner = kSwizzle ? 128 / kEs : D;        // elements per box row
+    static constexpr int kNumBox = kSwizzle ? (D * kEs) / 128 : 1;
+    static constexpr int kBoxBytes = 16 * kBoxInner * kEs;
+    static constexpr uint32_t kTxBytes = 2 * kTile + kScaleBytes;
+    // log2 of how far the block maximum may exceed the running maximum before
+    // the state is rescaled (0 = always exact). The int8 path folds the V
+    // scale into the fp16 P operand, so it keeps P <= 1.
+    static constexpr float kRescaleSlack = kI8 ? 0.f : 8.f;
+    static constexpr int kMt = D / 16;                              // m-tiles of the P.V product
+    static constexpr int kRuns = D / 64;                            // 8-dim output runs per head
+    static constexpr int kDpl = D / 32;                             // CUDA-core kernel: dims per lane
+};
+
+// Dynamic shared memory layout shared by host and device.
+template <class C>
+struct Smem {
+    static constexpr int kRing = C::kWarps * C::kStages * C::kStage;
+    static constexpr int kBars = kRing;                                   // 8 B per stage
+    static constexpr int kBad = kBars + C::kWarps * C::kStages * 8;       // 4 B per stage
+    static constexpr int kScan = kBad + C::kWarps * C::kStages * 4;       // 64 ints
+    static constexpr int kLens = kScan + 64 * 4;                          // B ints, then B+1 prefix
+    static int bytes(int B) { return 1024 + kLens + (2 * B + 1) * 4; }
+};
+
+// ------------------------------------------------------------------ prologue
+
+// Validated lengths into lens_s and the block prefix pref[0..B] (pref[0] = 0).
+__device__ void block_prefix(const DecodeArgs& a, int* lens_s, int* pref, int* tmp) {
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, wid = tid >> 5;
+    const int nw = nthr >> 5;
+    const int maxtok = a.max_blocks * kBlock;
+    int carry = 0;
+    for (int base = 0; base < a.B; base += nthr) {
+        const int i = base + tid;
+        int L = 0;
+        if (i < a.B) {
+            L = a.context_lens[i];
+            if (L < 0 || L > maxtok) {
+                if (blockIdx.x == 0) flag_error(a.err, GQA_DEVERR_CONTEXT_LEN);
+                L = 0;
+            }
+            lens_s[i] = L;
+        }
+        int x = (L + kBlock - 1) / kBlock;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) tmp[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            int t = lane < nw ? tmp[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, t, o);
+                if (lane >= o) t += y;
+            }
+            tmp[32 + lane] = t;
+        }
+        __syncthreads();
+        if (i < a.B) pref[i + 1] = carry + (wid ? tmp[32 + wid - 1] : 0) + x;
+        carry += tmp[32 + nw - 1];
+        __syncthreads();
+    }
+    if (tid == 0) pref[0] = 0;
+    __syncthreads();
+}
+
+// Unit u -> (b, g, j): the largest b with K*pref[b] <= u, then the head and block.
+__device__ __forceinline__ void locate(int u, const int* pref, int B, int K, int& b, int& g,
+                                       int& j) {
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (K * pref[mid] <= u) lo = mid;
+        else hi = mid;
+    }
+    const int nb = pref[lo + 1] - pref[lo];
+    const int rem = u - K * pref[lo];
+    b = lo;
+    g = rem / nb;
+    j = rem - g * nb;
+}
+
+// The pair after (b, g) in unit order (skipping empty sequences); b = B if none.
+__device__ __forceinline__ void next_pair(const int* pref, int B, int K, int& b, int& g) {
+    if (g + 1 < K) {
+        ++g;
+        return;
+    }
+    g = 0;
+    ++b;
+    while (b < B && pref[b + 1] == pref[b]) ++b;
+}
+
+// ------------------------------------------------------------------ loads
+
+template <typename T, int N>
+__device__ __forceinline__ void lds_row_as_float(uint32_t addr, float (&v)[N]) {
+    if constexpr (std::is_same<T, float>::value) {
+        if constexpr (N == 4) {
+            const uint4 x = lds128(addr);
+            v[0] = __uint_as_float(x.x); v[1] = __uint_as_float(x.y);
+            v[2] = __uint_as_float(x.z); v[3] = __uint_as_float(x.w);
+        } else {
+            const uint2 x = lds64(addr);
+            v[0] = __uint_as_float(x.x); v[1] = __uint_as_float(x.y);
+        }
+    } else if constexpr (std::is_same<T, int8_t>::value) {
+        uint32_t w;
+        if constexpr (N == 4) {
+            w = lds32(addr);
+        } else {
+            unsigned short h;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr));
+            w = h;
+        }
+#pragma unroll
+        for (int e = 0; e < N; ++e) v[e] = (float)(int8_t)((w >> (8 * e)) & 0xff);
+    } else {
+        constexpr bool bf = std::is_same<T, __nv_bfloat16>::value;
+        if constexpr (N == 4) {
+            const uint2 x = lds64(addr);
+            const float2 a = unpack2<bf>(x.x), b = unpack2<bf>(x.y);
+            v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+        } else {
+            const float2 a = unpack2<bf>(lds32(addr));
+            v[0] = a.x; v[1] = a.y;
+        }
+    }
+}
+
+__device__ __forceinline__ float load_q_float(const void* q, int q_dtype, long long i) {
+    if (q_dtype == GQA_DTYPE_F32) return static_cast<const float*>(q)[i];
+    if (q_dtype == GQA_DTYPE_F16) return __half2float(static_cast<const __half*>(q)[i]);
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(q)[i]);
+}
+
+__device__ __forceinline__ uint4 ldg128(const void* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    const float2 f = unpack2<true>(w);
+    return pack2<false>(f.x, f.y);
+}
+
+// Store 8 consecutive output floats (scaled) in the output dtype.
+__device__ __forceinline__ void store8(void* out, int out_dtype, long long idx, const float (&v)[8],
+                                       float mul) {
+    if (out_dtype == GQA_DTYPE_F32) {
+        float4* p = reinterpret_cast<float4*>(static_cast<float*>(out) + idx);
+        p[0] = make_float4(v[0] * mul, v[1] * mul, v[2] * mul, v[3] * mul);
+        p[1] = make_float4(v[4] * mul, v[5] * mul, v[6] * mul, v[7] * mul);
+    } else {
+        uint4 w;
+        if (out_dtype == GQA_DTYPE_BF16) {
+            w.x = pack2<true>(v[0] * mul, v[1] * mul); w.y = pack2<true>(v[2] * mul, v[3] * mul);
+            w.z = pack2<true>(v[4] * mul, v[5] * mul); w.w = pack2<true>(v[6] * mul, v[7] * mul);
+        } else {
+            w.x = pack2<false>(v[0] * mul, v[1] * mul); w.y = pack2<false>(v[2] * mul, v[3] * mul);
+            w.z = pack2<false>(v[4] * mul, v[5] * mul); w.w = pack2<false>(v[6] * mul, v[7] * mul);
+        }
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + idx) = w;
+    }
+}
+
+__device__ __forceinline__ void store1(void* out, int out_dtype, long long idx, float v) {
+    if (out_dtype == GQA_DTYPE_F32) static_cast<float*>(out)[idx] = v;
+    else if (out_dtype == GQA_DTYPE_BF16) static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+    else static_cast<__half*>(out)[idx] = __float2half_rn(v);
+}
+
+// ------------------------------------------------------------------ tensor-core state
+
+template <class C, int D>
+struct MmaState {
+    float m[2], l[2];          // heads 2c, 2c+1 of the group (log2 units)
+    float acc[C::kMt][4];      // O^T fragments: rows = dims, cols = heads 2c, 2c+1
+    uint4 qf[D / 32];          // Q^T B-fragments for the current pair
+    uint4 qn[D / 32];          // prefetched fragments of the next pair
+
+    __device__ __forceinline__ void reset() {
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+#pragma unroll
+        for (int j = 0; j < C::kMt; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    }
+};
+
+// Q fragments of query head g*G + r (zero for padded heads r >= G).
+// bf16/f16 caches: qf[qc] holds dims qc*32 + 8c .. +7 (matching the K-tile loads).
+// int8 cache: qf[2t + h] holds dims 16(c + 4t) + 8h .. +7, converted to f16.
+template <class C, int D>
+__device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int b, int g, int r, int c,
+                                             uint4 (&qf)[D / 32]) {
+    if (r >= a.G || b >= a.B) {
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) qf[i] = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const uint8_t* base = static_cast<const uint8_t*>(a.q) + ((long long)b * a.H + (long long)g * a.G + r) * D * 2;
+    if constexpr (!C::kI8) {
+#pragma unroll
+        for (int qc = 0; qc < D / 32; ++qc) qf[qc] = ldg128(base + (qc * 32 + 8 * c) * 2);
+    } else {
+#pragma unroll
+        for (int t = 0; t < D / 64; ++t) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint4 raw = ldg128(base + (16 * (c + 4 * t) + 8 * hh) * 2);
+                if (a.q_dtype == GQA_DTYPE_BF16) {
+                    raw.x = bf16x2_to_f16x2(raw.x); raw.y = bf16x2_to_f16x2(raw.y);
+                    raw.z = bf16x2_to_f16x2(raw.z); raw.w = bf16x2_to_f16x2(raw.w);
+                }
+                qf[2 * t + hh] = raw;
+            }
+        }
+    }
+}
+
+// First output dim of the 8-dim run k owned by row-group r.
+template <class C, int D>
+__device__ __forceinline__ int run_dim(int k, int r) {
+    if constexpr (C::kI8) return 16 * r + 8 * k;
+    else if constexpr (D == 128) return 16 * r + 8 * (k ^ (r >> 2));
+    else return 8 * r;
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void mma_t(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                      uint32_t a3, uint32_t b0, uint32_t b1) {
+    if constexpr (kBf16) mma_bf16(d, a0, a1, a2, a3, b0, b1);
+    else mma_f16(d, a0, a1, a2, a3, b0, b1);
+}
+
+// One 16-token block on the tensor cores.
+template <class C, int D>
+__device__ __forceinline__ void mma_block(MmaState<C, D>& st, uint32_t stage, int nvalid, int r,
+                                          int c, int lane, float scale_log2) {
+    constexpr bool kB = C::kBf16;            // P and V operand type: bf16, else f16
+    const uint32_t sk = stage, sv = stage + C::kTile;
+
+    // ---- scores: S^T[tok][head] = K_tile . Q^T
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (!C::kI8) {
+#pragma unroll
+        for (int qc = 0; qc < D / 32; ++qc) {
+            const uint32_t bx = sk + (qc >> 1) * 2048;
+            const uint32_t ch = (uint32_t)((((qc & 1) << 2) | c) ^ r) << 4;
+            const uint4 x = lds128(bx + r * 128 + ch);
+            const uint4 y = lds128(bx + (r + 8) * 128 + ch);
+            mma_t<kB>(sa, x.x, y.x, x.y, y.y, st.qf[qc].x, st.qf[qc].y);
+            mma_t<kB>(sb, x.z, y.z, x.w, y.w, st.qf[qc].z, st.qf[qc].w);
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < D / 64; ++t) {
+            const uint32_t ch = (uint32_t)((c + 4 * t) ^ r) << 4;
+            const uint4 x = lds128(sk + r * 128 + ch);
+            const uint4 y = lds128(sk + (r + 8) * 128 + ch);
+            uint32_t xl[4], xh[4], yl[4], yh[4];
+            i8x4_to_f16x4(x.x, xl[0], xh[0]); i8x4_to_f16x4(x.y, xl[1], xh[1]);
+            i8x4_to_f16x4(x.z, xl[2], xh[2]); i8x4_to_f16x4(x.w, xl[3], xh[3]);
+            i8x4_to_f16x4(y.x, yl[0], yh[0]); i8x4_to_f16x4(y.y, yl[1], yh[1]);
+            i8x4_to_f16x4(y.z, yl[2], yh[2]); i8x4_to_f16x4(y.w, yl[3], yh[3]);
+            const uint32_t qw[8] = {st.qf[2 * t].x, st.qf[2 * t].y, st.qf[2 * t].z, st.qf[2 * t].w,
+                                    st.qf[2 * t + 1].x, st.qf[2 * t + 1].y, st.qf[2 * t + 1].z,
+                                    st.qf[2 * t + 1].w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                if (m & 1) mma_f16(sb, xl[m], yl[m], xh[m], yh[m], qw[2 * m], qw[2 * m + 1]);
+                else mma_f16(sa, xl[m], yl[m], xh[m], yh[m], qw[2 * m], qw[2 * m + 1]);
+            }
+        }
+    }
+    // fragment: [0] = (tok r, head 2c), [1] = (tok r, head 2c+1), [2]/[3] = tok r+8
+    float kr = scale_log2, kr8 = scale_log2, vr_s = 1.f, vr8_s = 1.f;
+    if constexpr (C::kI8) {
+        const uint32_t sc = stage + 2 * C::kTile;
+        unsigned short h0, h1, h2, h3;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h0) : "r"(sc + 2 * r));
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h1) : "r"(sc + 2 * (r + 8)));
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h2) : "r"(sc + 32 + 2 * r));
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h3) : "r"(sc + 32 + 2 * (r + 8)));
+        kr = __half2float(__ushort_as_half(h0)) * scale_log2;
+        kr8 = __half2float(__ushort_as_half(h1)) * scale_log2;
+        vr_s = __half2float(__ushort_as_half(h2));
+        vr8_s = __half2float(__ushort_as_half(h3));
+    }
+    float s0 = (sa[0] + sb[0]) * kr, s1 = (sa[1] + sb[1]) * kr;
+    float s2 = (sa[2] + sb[2]) * kr8, s3 = (sa[3] + sb[3]) * kr8;
+    const bool ok_r = r < nvalid, ok_r8 = r + 8 < nvalid;
+    if (!ok_r) { s0 = -INFINITY; s1 = -INFINITY; vr_s = 0.f; }
+    if (!ok_r8) { s2 = -INFINITY; s3 = -INFINITY; vr8_s = 0.f; }
+
+    // ---- online softmax (per head, over the 16 tokens of this block)
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+    }
+    const bool up0 = mx0 > st.m[0] + C::kRescaleSlack, up1 = mx1 > st.m[1] + C::kRescaleSlack;
+    if (__any_sync(kFull, up0 || up1)) {
+        const float n0 = up0 ? mx0 : st.m[0], n1 = up1 ? mx1 : st.m[1];
+        const float a0 = up0 ? fast_exp2(st.m[0] - n0) : 1.f;
+        const float a1 = up1 ? fast_exp2(st.m[1] - n1) : 1.f;
+        st.m[0] = n0; st.m[1] = n1;
+        st.l[0] *= a0; st.l[1] *= a1;
+#pragma unroll
+        for (int j = 0; j < C::kMt; ++j) {
+            st.acc[j][0] *= a0; st.acc[j][1] *= a1; st.acc[j][2] *= a0; st.acc[j][3] *= a1;
+        }
+    }
+    const float p0 = fast_exp2(s0 - st.m[0]), p1 = fast_exp2(s1 - st.m[1]);
+    const float p2 = fast_exp2(s2 - st.m[0]), p3 = fast_exp2(s3 - st.m[1]);
+    st.l[0] += p0 + p2;
+    st.l[1] += p1 + p3;
+
+    // ---- P -> 16-bit high + low parts, transposed to the B layout of P.V
+    const float w0 = p0 * vr_s, w1 = p1 * vr_s, w2 = p2 * vr8_s, w3 = p3 * vr8_s;
+    const uint32_t hr = pack2<kB>(w0, w1), hr8 = pack2<kB>(w2, w3);
+    const float2 fr = unpack2<kB>(hr), fr8 = unpack2<kB>(hr8);
+    const uint32_t lr = pack2<kB>(w0 - fr.x, w1 - fr.y), lr8 = pack2<kB>(w2 - fr8.x, w3 - fr8.y);
+    const int srcA = 8 * c + (r >> 1), srcB = srcA + 4;
+    const uint32_t sel = (r & 1) ? 0x7632u : 0x5410u;
+    const uint32_t bh0 = __byte_perm(__shfl_sync(kFull, hr, srcA), __shfl_sync(kFull, hr, srcB), sel);
+    const uint32_t bh1 = __byte_perm(__shfl_sync(kFull, hr8, srcA), __shfl_sync(kFull, hr8, srcB), sel);
+    const uint32_t bl0 = __byte_perm(__shfl_sync(kFull, lr, srcA), __shfl_sync(kFull, lr, srcB), sel);
+    const uint32_t bl1 = __byte_perm(__shfl_sync(kFull, lr8, srcA), __shfl_sync(kFull, lr8, srcB), sel);
+
+    // ---- V^T fragments for tokens 2c, 2c+1, 2c+8, 2c+9
+    uint32_t vr[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int tok = 2 * c + (i & 1) + 8 * (i >> 1);
+        const uint32_t row = sv + tok * 128;
+        if constexpr (C::kI8) {
+            const uint4 raw = lds128(row + ((uint32_t)(r ^ (tok & 7)) << 4));
+            i8x4_to_f16x4(raw.x, vr[i][0], vr[i][1]); i8x4_to_f16x4(raw.y, vr[i][2], vr[i][3]);
+            i8x4_to_f16x4(raw.z, vr[i][4], vr[i][5]); i8x4_to_f16x4(raw.w, vr[i][6], vr[i][7]);
+        } else if constexpr (D == 128) {
+            const int h = r >> 2;
+            const uint32_t bx = row + h * 2048;
+            const uint4 x0 = lds128(bx + ((uint32_t)((2 * (r & 3) + h) ^ (tok & 7)) << 4));
+            const uint4 x1 = lds128(bx + ((uint32_t)((2 * (r & 3) + 1 - h) ^ (tok & 7)) << 4));
+            vr[i][0] = x0.x; vr[i][1] = x0.y; vr[i][2] = x0.z; vr[i][3] = x0.w;
+            vr[i][4] = x1.x; vr[i][5] = x1.y; vr[i][6] = x1.z; vr[i][7] = x1.w;
+        } else {
+            const uint4 x0 = lds128(row + ((uint32_t)(r ^ (tok & 7)) << 4));
+            vr[i][0] = x0.x; vr[i][1] = x0.y; vr[i][2] = x0.z; vr[i][3] = x0.w;
+            vr[i][4] = vr[i][5] = vr[i][6] = vr[i][7] = 0u;
+        }
+        if (tok >= nvalid) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) vr[i][e] = 0u;
+        }
+    }
+
+    // ---- O^T[dim][head] += V^T . P^T (high part, then low part)
+#pragma unroll
+    for (int j = 0; j < C::kMt; ++j) {
+        const uint32_t a0 = __byte_perm(vr[0][j], vr[1][j], 0x5410);
+        const uint32_t a1 = __byte_perm(vr[0][j], vr[1][j], 0x7632);
+        const uint32_t a2 = __byte_perm(vr[2][j], vr[3][j], 0x5410);
+        const uint32_t a3 = __byte_perm(vr[2][j], vr[3][j], 0x7632);
+        mma_t<kB>(st.acc[j], a0, a1, a2, a3, bh0, bh1);
+        mma_t<kB>(st.acc[j], a0, a1, a2, a3, bl0, bl1);
+    }
+    (void)lane;
+}
+
+// Write the state of pair (b, g): final output if this warp saw the whole pair,
+// else a partial (o, m, l) into split slot (b*K + g) + warp.
+template <class C, int D>
+__device__ __forceinline__ void mma_flush(const DecodeArgs& a, MmaState<C, D>& st, int b, int g,
+                                          bool whole, int w, int r, int c) {
+    float l0 = st.l[0], l1 = st.l[1];
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(kFull, l0, o);
+        l1 += __shfl_xor_sync(kFull, l1, o);
+    }
+    const long long slot = (long long)b * a.K + g + w;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int hh = 2 * c + e;
+        if (hh >= a.G) continue;
+        const float lsum = e ? l1 : l0;
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+        for (int k = 0; k < C::kRuns; ++k) {
+            float v[8];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                v[2 * jj] = st.acc[4 * k + jj][e];
+                v[2 * jj + 1] = st.acc[4 * k + jj][e + 2];
+            }
+            const int dim = run_dim<C, D>(k, r);
+            if (whole) {
+                store8(a.out, a.out_dtype, ((long long)b * a.H + (long long)g * a.G + hh) * D + dim, v, inv);
+            } else {
+                store8(a.ws_o, GQA_DTYPE_F32, (slot * a.G + hh) * D + dim, v, 1.f);
+            }
+        }
+        if (!whole && r == 0) a.ws_ml[slot * a.G + hh] = make_float2(st.m[e], lsum);
+    }
+}
+
+// ------------------------------------------------------------------ CUDA-core state
+
+template <class C, int D>
+struct FmaState {
+    static constexpr int kN = C::kDpl;
+    float m[kMaxGroup], l[kMaxGroup];
+    float acc[kMaxGroup][kN];
+    float q[kMaxGroup][kN];
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int h = 0; h < kMaxGroup; ++h) {
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+#pragma unroll
+            for (int i = 0; i < kN; ++i) acc[h][i] = 0.f;
+        }
+    }
+};
+
+template <class C, int D>
+__device__ __forceinline__ void fma_load_q(const DecodeArgs& a, FmaState<C, D>& st, int b, int g,
+                                           int lane) {
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h)
+#pragma unroll
+        for (int i = 0; i < C::kDpl; ++i)
+            st.q[h][i] = (h < a.G) ? load_q_float(a.q, a.q_dtype,
+                                                  ((long long)b * a.H + (long long)g * a.G + h) * D + lane * C::kDpl + i)
+                                   : 0.f;
+}
+
+// One block, token by token: fp32 FMAs, butterfly reductions, per-token online softmax.
+template <class C, int D, typename T>
+__device__ __forceinline__ void fma_block(const DecodeArgs& a, FmaState<C, D>& st, uint32_t stage,
+                                          int nvalid, int lane) {
+    constexpr int kN = C::kDpl;
+    const uint32_t sk = stage, sv = stage + C::kTile;
+    const int G = a.G;
+    for (int t = 0; t < nvalid; ++t) {
+        float kf[kN], vf[kN];
+        lds_row_as_float<T, kN>(sk + t * D * C::kEs + lane * kN * C::kEs, kf);
+        lds_row_as_float<T, kN>(sv + t * D * C::kEs + lane * kN * C::kEs, vf);
+        float ksc = a.scale_log2, vsc = 1.f;
+        if constexpr (C::kI8) {
+            unsigned short hk, hv;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hk) : "r"(stage + 2 * C::kTile + 2 * t));
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(stage + 2 * C::kTile + 32 + 2 * t));
+            ksc *= __half2float(__ushort_as_half(hk));
+            vsc = __half2float(__ushort_as_half(hv));
+        }
+#pragma unroll
+        for (int h = 0; h < kMaxGroup; ++h) {
+            if (h >= G) break;
+            float dot = 0.f;
+#pragma unroll
+            for (int i = 0; i < kN; ++i) dot = fmaf(st.q[h][i], kf[i], dot);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(kFull, dot, o);
+            const float s = dot * ksc;
+            const float mn = fmaxf(st.m[h], s);
+            const float al = fast_exp2(st.m[h] - mn);
+            const float p = fast_exp2(s - mn);
+            st.l[h] = st.l[h] * al + p;
+            const float pv = p * vsc;
+#pragma unroll
+            for (int i = 0; i < kN; ++i) st.acc[h][i] = fmaf(st.acc[h][i], al, pv * vf[i]);
+            st.m[h] = mn;
+        }
+    }
+}
+
+template <class C, int D>
+__device__ __forceinline__ void fma_flush(const DecodeArgs& a, FmaState<C, D>& st, int b, int g,
+                                          bool whole, int w, int lane) {
+    const long long slot = (long long)b * a.K + g + w;
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h) {
+        if (h >= a.G) break;
+        const float inv = st.l[h] > 0.f ? 1.f / st.l[h] : 0.f;
+#pragma unroll
+        for (int i = 0; i < C::kDpl; ++i) {
+            const int dim = lane * C::kDpl + i;
+            if (whole) store1(a.out, a.out_dtype, ((long long)b * a.H + (long long)g * a.G + h) * D + dim, st.acc[h][i] * inv);
+            else a.ws_o[(slot * a.G + h) * D + dim] = st.acc[h][i];
+        }
+        if (!whole && lane == 0) a.ws_ml[slot * a.G + h] = make_float2(st.m[h], st.l[h]);
+    }
+}
+
+// ------------------------------------------------------------------ the split-KV kernel
+
+template <int kKind, typename T, int D>
+__global__ void __launch_bounds__(Cfg<kKind, T, D>::kWarps * 32)
+split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                const DecodeArgs a) {
+    using C = Cfg<kKind, T, D>;
+    using S = Smem<C>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (sbase - raw);
+    int* tmp = reinterpret_cast<int*>(gbase + S::kScan);
+    int* lens_s = reinterpret_cast<int*>(gbase + S::kLens);
+    int* pref = lens_s + a.B;
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    block_prefix(a, lens_s, pref, tmp);
+    const int U = a.K * pref[a.B];
+    const int R = max((U + a.P - 1) / max(a.P, 1), a.min_units);
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i <= a.B; i += blockDim.x) a.ws_pref[i] = pref[i];
+        if (threadIdx.x == 0) {
+            a.ws_hdr[0] = R;
+            a.ws_hdr[1] = U;
+        }
+    }
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int w = blockIdx.x * C::kWarps + warp;
+    const long long ub = (long long)w * R;
+    if (ub >= U) return;                       // no CTA-wide barrier follows
+    const int u_begin = (int)ub;
+    const int u_end = (int)min((long long)U, ub + R);
+    const int n_units = u_end - u_begin;
+
+    const uint32_t ring = sbase + warp * C::kStages * C::kStage;
+    const uint32_t bar0 = sbase + S::kBars + warp * C::kStages * 8;
+    volatile int* bad = reinterpret_cast<volatile int*>(gbase + S::kBad) + warp * C::kStages;
+    if (lane == 0) {
+        for (int s = 0; s < C::kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const uint64_t pol = l2_policy_evict_first();
+
+    // Window of physical blocks: lane l holds unit win_base + l.
+    int win_base = -(1 << 30), win_phys = -1, win_g = 0;
+    auto refill = [&](int base) {
+        win_base = base;
+        const int u = base + lane;
+        win_phys = -1;
+        win_g = 0;
+        if (u < u_end) {
+            int b, g, j;
+            locate(u, pref, a.B, a.K, b, g, j);
+            const int ph = a.block_tables[(long long)b * a.max_blocks + j];
+            if (ph < 0 || ph >= a.num_blocks) flag_error(a.err, GQA_DEVERR_BLOCK_INDEX);
+            else win_phys = ph;
+            win_g = g;
+        }
+    };
+    auto issue = [&](int u, int s) {
+        if (u - win_base >= 32) refill(u);
+        const int ph = __shfl_sync(kFull, win_phys, u - win_base);
+        const int gg = __shfl_sync(kFull, win_g, u - win_base);
+        if (lane == 0) {
+            const uint32_t bar = bar0 + 8 * s;
+            const uint32_t dst = ring + s * C::kStage;
+            if (ph >= 0) {
+                auto coord = [&](int which) { return which == 0 ? 0 : (which == 1 ? gg : ph); };
+                const int y = coord(a.map_perm[0]), z = coord(a.map_perm[1]), ww = coord(a.map_perm[2]);
+                bad[s] = 0;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar, C::kTxBytes);
+#pragma unroll
+                for (int x = 0; x < C::kNumBox; ++x)
+                    tma_load_4d(dst + x * C::kBoxBytes, &kmap, x * C::kBoxInner, y, z, ww, bar, pol);
+#pragma unroll
+                for (int x = 0; x < C::kNumBox; ++x)
+                    tma_load_4d(dst + C::kTile + x * C::kBoxBytes, &vmap, x * C::kBoxInner, y, z, ww, bar, pol);
+                if constexpr (C::kI8) {
+                    const long long si = ((long long)ph * a.K + gg) * kBlock;
+                    bulk_load(dst + 2 * C::kTile, a.k_scale + si, 32, bar, pol);
+                    bulk_load(dst + 2 * C::kTile + 32, a.v_scale + si, 32, bar, pol);
+                }
+            } else {
+                bad[s] = 1;
+                mbar_arrive(bar);
+            }
+        }
+    };
+
+    const int npro = min((int)C::kStages, n_units);
+    for (int s = 0; s < npro; ++s) issue(u_begin + s, s);
+
+    // Compute-side cursor.
+    int cb, cg, cj;
+    locate(u_begin, pref, a.B, a.K, cb, cg, cj);
+    int cnb = pref[cb + 1] - pref[cb];
+    int clen = lens_s[cb];
+    int first_j = cj;
+    int cu_pair = a.K * pref[cb] + cg * cnb;      // first unit of the current pair
+    const int r = lane >> 2, c = lane & 3;
+
+    using State = typename std::conditional<kKind == kKernelMma, MmaState<C, D>, FmaState<C, D>>::type;
+    State st;
+    st.reset();
+    int nb_b = cb, nb_g = cg;                   // next pair (for the q prefetch)
+    next_pair(pref, a.B, a.K, nb_b, nb_g);
+    if constexpr (kKind == kKernelMma) {
+        load_q_frags<C, D>(a, cb, cg, r, c, st.qf);
+        if (cu_pair + cnb < u_end) load_q_frags<C, D>(a, nb_b, nb_g, r, c, st.qn);
+    } else {
+        fma_load_q<C, D>(a, st, cb, cg, lane);
+    }
+
+    for (int i = 0; i < n_units; ++i) {
+        const int s = i % C::kStages;
+        const uint32_t parity = (uint32_t)(i / C::kStages) & 1u;
+        // every lane observes the phase (acquiring the TMA writes); the verdict is
+        // made warp-uniform so a timeout can never split the warp
+        if (!__all_sync(kFull, mbar_wait(bar0 + 8 * s, parity))) {
+            // A copy did not land in time: report, let in-flight copies finish, leave.
+            if (lane == 0) flag_error(a.err, GQA_DEVERR_TIMEOUT);
+            for (int k = i; k < min(n_units, i + (int)C::kStages); ++k) {
+                const int s2 = k % C::kStages;
+                mbar_wait(bar0 + 8 * s2, (uint32_t)(k / C::kStages) & 1u, kWaitLimitNs / 4);
+            }
+            return;
+        }
+        const int nvalid = min((int)kBlock, clen - kBlock * cj);
+        if (!bad[s]) {
+            if constexpr (kKind == kKernelMma) mma_block<C, D>(st, ring + s * C::kStage, nvalid, r, c, lane, a.scale_log2);
+            else fma_block<C, D, T>(a, st, ring + s * C::kStage, nvalid, lane);
+        }
+        __syncwarp();
+        if (i + C::kStages < n_units) issue(u_begin + i + C::kStages, s);
+
+        const bool last_of_pair = (cj == cnb - 1);
+        if (last_of_pair || i == n_units - 1) {
+            const bool whole = (first_j == 0) && last_of_pair;
+            if constexpr (kKind == kKernelMma) mma_flush<C, D>(a, st, cb, cg, whole, w, r, c);
+            else fma_flush<C, D>(a, st, cb, cg, whole, w, lane);
+            if (i == n_units - 1) break;
+            cb = nb_b;
+            cg = nb_g;
+            cj = 0;
+            first_j = 0;
+            cnb = pref[cb + 1] - pref[cb];
+            clen = lens_s[cb];
+            cu_pair = a.K * pref[cb] + cg * cnb;
+            st.reset();
+            next_pair(pref, a.B, a.K, nb_b, nb_g);
+            if constexpr (kKind == kKernelMma) {
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k) st.qf[k] = st.qn[k];
+                if (cu_pair + cnb < u_end) load_q_frags<C, D>(a, nb_b, nb_g, r, c, st.qn);
+            } else {
+                fma_load_q<C, D>(a, st, cb, cg, lane);
+            }
+        } else {
+            ++cj;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ combine
+
+// Merge the splits of each (sequence, kv-head) pair; zero rows of empty sequences.
+template <int D>
+__global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
+    const int pair = blockIdx.x;
+    const int b = pair / a.K, g = pair % a.K;
+    const int R = a.ws_hdr[0];
+    const int p0 = a.ws_pref[b];
+    const int nb = a.ws_pref[b + 1] - p0;
+    const int items = a.G * (D / 4);
+    if (nb == 0) {
+        for (int it = threadIdx.x; it < items; it += blockDim.x) {
+            const int hh = it / (D / 4), d4 = (it % (D / 4)) * 4;
+            const long long o = ((long long)b * a.H + (long long)g * a.G + hh) * D + d4;
+            for (int e = 0; e < 4; ++e) store1(a.out, a.out_dtype, o + e, 0.f);
+        }
+        return;
+    }
+    const long long u0 = (long long)a.K * p0 + (long long)g * nb;
+    const long long u1 = u0 + nb;
+    const int w0 = (int)(u0 / R), w1 = (int)((u1 - 1) / R);
+    if (w0 == w1) return;                      // one warp saw the whole pair and wrote it
+    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+        const int hh = it / (D / 4), d4 = (it % (D / 4)) * 4;
+        float M = -INFINITY;
+        for (int w = w0; w <= w1; ++w) M = fmaxf(M, a.ws_ml[((long long)pair + w) * a.G + hh].x);
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+            for (int w = w0; w <= w1; ++w) {
+                const long long slot = (long long)pair + w;
+                const float2 ml = a.ws_ml[slot * a.G + hh];
+                const float e = fast_exp2(ml.x - M);
+                L += ml.y * e;
+                const float4 o = *reinterpret_cast<const float4*>(a.ws_o + (slot * a.G + hh) * D + d4);
+                acc.x += o.x * e; acc.y += o.y * e; acc.z += o.z * e; acc.w += o.w * e;
+            }
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const long long o = ((long long)b * a.H + (long long)g * a.G + hh) * D + d4;
+        store1(a.out, a.out_dtype, o + 0, acc.x * inv);
+        store1(a.out, a.out_dtype, o + 1, acc.y * inv);
+        store1(a.out, a.out_dtype, o + 2, acc.z * inv);
+        store1(a.out, a.out_dtype, o + 3, acc.w * inv);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+struct Variant {
+    const void* fn;
+    int warps;
+    int box_inner;       // elements per TMA box row
+    bool swizzle;
+    int (*smem)(int);
+};
+
+template <int kKind, typename T, int D>
+Variant make_variant() {
+    using C = Cfg<kKind, T, D>;
+    return Variant{reinterpret_cast<const void*>(&split_kv_kernel<kKind, T, D>), C::kWarps,
+                   C::kBoxInner, C::kSwizzle, &Smem<C>::bytes};
+}
+
+template <typename T, int D>
+bool pick_kind(int kind, Variant& v) {
+    if (kind == kKernelMma) {
+        if constexpr (std::is_same<T, float>::value || (std::is_same<T, int8_t>::value && D != 128)) {
+            return false;
+        } else {
+            v = make_variant<kKernelMma, T, D>();
+            return true;
+        }
+    }
+    v = make_variant<kKernelFma, T, D>();
+    return true;
+}
+
+template <typename T>
+bool pick_dim(int kind, int d, Variant& v) {
+    if (d == 64) return pick_kind<T, 64>(kind, v);
+    if (d == 128) return pick_kind<T, 128>(kind, v);
+    return false;
+}
+
+struct WsLayout {
+    size_t hdr, pref, ml, o, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WsLayout ws_layout(int B, int K, int G, int D, long long slots) {
+    WsLayout w;
+    w.hdr = 0;
+    w.pref = align256(kWsHeaderInts * 4);
+    w.ml = w.pref + align256((size_t)(B + 1) * 4);
+    w.o = w.ml + align256((size_t)slots * G * 8);
+    w.total = w.o + align256((size_t)slots * G * D * 4);
+    return w;
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int head_dim, int num_sms) {
+    const long long slots = (long long)batch * num_kv_heads + (long long)num_sms * kMaxWarpsPerSm;
+    return ws_layout(batch, num_kv_heads, num_heads / num_kv_heads, head_dim, slots).total;
+}
+
+int launch_decode(const DecodeLaunch& L, int num_sms) {
+    const gqa_kv_cache_t& c = *L.cache;
+    const int D = c.head_dim, K = c.num_kv_heads, G = L.num_heads / K;
+    int kind = L.kernel;
+    if (kind == 0) kind = (c.dtype == GQA_DTYPE_F32 || (c.dtype == GQA_DTYPE_I8 && D != 128)) ? kKernelFma : kKernelMma;
+    Variant v{};
+    bool ok = false;
+    switch (c.dtype) {
+        case GQA_DTYPE_F32: ok = pick_dim<float>(kind, D, v); break;
+        case GQA_DTYPE_F16: ok = pick_dim<__half>(kind, D, v); break;
+        case GQA_DTYPE_BF16: ok = pick_dim<__nv_bfloat16>(kind, D, v); break;
+        case GQA_DTYPE_I8: ok = pick_dim<int8_t>(kind, D, v); break;
+        default: ok = false;
+    }
+    if (!ok) return GQA_ERR_UNSUPPORTED;
+
+    CUtensorMap kmap, vmap;
+    int perm[3];
+    if (!encode_cache_map(&kmap, c, c.k, v.box_inner, v.swizzle, perm) ||
+        !encode_cache_map(&vmap, c, c.v, v.box_inner, v.swizzle, perm))
+        return GQA_ERR_UNSUPPORTED;
+
+    const int smem = v.smem(L.batch);
+    cudaError_t e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return GQA_ERR_CUDA;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, v.fn, v.warps * 32, smem);
+    if (e != cudaSuccess) return GQA_ERR_CUDA;
+    if (per_sm < 1) return GQA_ERR_UNSUPPORTED;
+    int grid = num_sms * per_sm;
+    if (L.max_warps > 0) grid = std::min(grid, std::max(1, (L.max_warps + v.warps - 1) / v.warps));
+    const int P = grid * v.warps;
+
+    const long long slots = (long long)L.batch * K + P;
+    const WsLayout wl = ws_layout(L.batch, K, G, D, slots);
+    if (L.workspace == nullptr || L.workspace_bytes < wl.total) return GQA_ERR_WORKSPACE;
+
+    DecodeArgs a;
+    a.q = L.q;
+    a.k_scale = static_cast<const __half*>(c.k_scale);
+    a.v_scale = static_cast<const __half*>(c.v_scale);
+    a.block_tables = L.block_tables;
+    a.context_lens = L.context_lens;
+    a.out = L.out;
+    a.err = L.err;
+    uint8_t* ws = static_cast<uint8_t*>(L.workspace);
+    a.ws_hdr = reinterpret_cast<int32_t*>(ws + wl.hdr);
+    a.ws_pref = reinterpret_cast<int32_t*>(ws + wl.pref);
+    a.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
+    a.ws_o = reinterpret_cast<float*>(ws + wl.o);
+    a.num_blocks = c.num_blocks;
+    a.B = L.batch;
+    a.H = L.num_heads;
+    a.K = K;
+    a.G = G;
+    a.max_blocks = L.max_blocks;
+    a.out_dtype = L.out_dtype;
+    a.q_dtype = L.q_dtype;
+    a.P = P;
+    a.map_perm[0] = perm[0];
+    a.map_perm[1] = perm[1];
+    a.map_perm[2] = perm[2];
+    a.min_units = L.min_blocks_per_warp > 0 ? L.min_blocks_per_warp : 4;
+    a.scale_log2 = L.scale * kLog2e;
+
+    if (L.ev_begin && cudaEventRecord(L.ev_begin, L.stream) != cudaSuccess) return GQA_ERR_CUDA;
+    void* args[] = {&kmap, &vmap, &a};
+    e = cudaLaunchKernel(v.fn, dim3(grid), dim3(v.warps * 32), args, smem, L.stream);
+    if (e != cudaSuccess) return GQA_ERR_CUDA;
+    if (L.ev_end && cudaEventRecord(L.ev_end, L.stream) != cudaSuccess) return GQA_ERR_CUDA;
+
+    const int pairs = L.batch * K;
+    if (D == 64) combine_kernel<64><<<pairs, 128, 0, L.stream>>>(a);
+    else combine_kernel<128><<<pairs, 128, 0, L.stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    return GQA_OK;
+}
+
+}  // namespace gqa

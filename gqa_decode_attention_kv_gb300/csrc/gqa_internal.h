@@ -1,0 +1,73 @@
+// gqa_internal.h -- declarations shared between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gqa_decode.h"
+
+namespace gqa {
+
+inline int dtype_size(int dt) {
+    switch (dt) {
+        case GQA_DTYPE_F32: return 4;
+        case GQA_DTYPE_F16: return 2;
+        case GQA_DTYPE_BF16: return 2;
+        case GQA_DTYPE_I8: return 1;
+        default: return 0;
+    }
+}
+
+// Which split-KV kernel runs.
+enum KernelKind { kKernelMma = 1, kKernelFma = 2 };
+
+// Fixed part of the decode workspace (header ints) before the block prefix.
+constexpr int kWsHeaderInts = 64;
+// Upper bound on decode warps per SM used for sizing the workspace.
+constexpr int kMaxWarpsPerSm = 64;
+constexpr int kMaxBatch = 8191;
+constexpr int kMaxGroup = 8;
+
+cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const void* v_new,
+                             int new_dtype, const int32_t* block_tables, int max_blocks,
+                             const int32_t* positions, int batch, int32_t* err,
+                             cudaStream_t stream);
+
+struct DecodeLaunch {
+    const gqa_kv_cache_t* cache;
+    const void* q;
+    int q_dtype;
+    int num_heads;
+    const int32_t* block_tables;
+    int max_blocks;
+    const int32_t* context_lens;
+    int batch;
+    float scale;
+    void* out;
+    int out_dtype;
+    void* workspace;
+    size_t workspace_bytes;
+    int kernel;                 // KernelKind
+    int max_warps;              // 0 = fill the GPU
+    int min_blocks_per_warp;
+    cudaEvent_t ev_begin, ev_end;
+    int32_t* err;
+    cudaStream_t stream;
+};
+
+// Bytes of workspace for a shape given the device's SM count.
+size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int head_dim, int num_sms);
+
+// Validated launch; returns a gqa_status_t.
+int launch_decode(const DecodeLaunch& L, int num_sms);
+
+// 4-D tensor map over one cache tensor. Dim 0 is the head dimension d; dims
+// 1..3 are the slot (16), kv-head (K) and block (num_blocks) axes sorted by
+// increasing stride, and perm[i] names which of them (0 slot, 1 head, 2 block)
+// map dim i+1 is. The box is box_inner elements by 16 slots. 128-byte swizzle or
+// none. Returns false if the driver rejects the description.
+bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base,
+                      int box_inner, bool swizzle128, int perm[3]);
+
+}  // namespace gqa

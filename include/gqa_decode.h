@@ -1,0 +1,198 @@
+/*
+ * gqa_decode.h -- C ABI of the GB300 (sm_103a) grouped-query decode-attention
+ * library over a paged KV cache.
+ *
+ * One autoregressive decode step of grouped-query attention: each of the H
+ * query heads of the new token attends to the shared K/V head of its group,
+ * g = h / (H/K), over the whole cached context ("分组查询注意力 (GQA)",
+ * 技术原理 steps 1-4 and the attention equation
+ * softmax(Q_group K_g^T / sqrt(d_k)) V_g). The cache is paged: fixed blocks of
+ * 16 tokens, addressed per sequence through a block table
+ * ("LLM 推理性能优化实战", section 8.2; block_size 16 from the KV-cache essay's
+ * padding paragraph).
+ *
+ * Conventions for every call:
+ *  - Pointers named "device" are CUDA device pointers owned by the caller; the
+ *    library never frees or keeps them. Structs passed by pointer are host
+ *    memory and are read during the call only.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). All GPU work
+ *    is enqueued on it; no call synchronises the host with the device, and no
+ *    call allocates device memory.
+ *  - Host-detectable argument errors return a non-zero gqa_status_t before any
+ *    launch. Data-dependent faults found on the device (a block-table entry
+ *    outside [0, num_blocks), a context length outside [0, max_blocks*16], an
+ *    append position out of range) never trap: the offending unit is skipped
+ *    and a GQA_DEVERR_* bit is OR-ed into *err_flag (a device int32, may be
+ *    NULL). Outputs of a sequence that raised a device error are unspecified.
+ *  - Tensor layouts are row-major with the innermost index last.
+ */
+#ifndef GQA_DECODE_H
+#define GQA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GQA_API __attribute__((visibility("default")))
+#else
+#define GQA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+typedef enum {
+    GQA_DTYPE_F32 = 0,
+    GQA_DTYPE_F16 = 1,
+    GQA_DTYPE_BF16 = 2,
+    GQA_DTYPE_I8 = 3          /* cache only: int8 codes + one fp16 scale per (token, kv-head) */
+} gqa_dtype_t;
+
+/* Return codes. */
+typedef enum {
+    GQA_OK = 0,
+    GQA_ERR_INVALID = 1,      /* null pointer, bad size or stride, misaligned address */
+    GQA_ERR_UNSUPPORTED = 2,  /* well-formed but not built: head_dim, group size, dtype mix */
+    GQA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than gqa_decode_workspace_size */
+    GQA_ERR_CUDA = 4          /* a CUDA runtime call or a kernel launch failed */
+} gqa_status_t;
+
+/* Device-side error bits OR-ed into *err_flag. */
+#define GQA_DEVERR_BLOCK_INDEX 1   /* block-table entry outside [0, num_blocks) */
+#define GQA_DEVERR_CONTEXT_LEN 2   /* context length < 0 or > max_blocks_per_seq * 16 */
+#define GQA_DEVERR_POSITION    4   /* append position < 0 or >= max_blocks_per_seq * 16 */
+#define GQA_DEVERR_TIMEOUT     8   /* a bounded wait for an asynchronous copy expired */
+
+#define GQA_BLOCK_SIZE 16
+
+/*
+ * A paged KV cache. Token t (slot t % 16) of kv-head g in physical block p
+ * starts at element  p*stride_block + g*stride_head + (t % 16)*stride_token
+ * of `k` (and of `v`). The default pool layout [num_blocks, K, 16, d] has
+ * stride_block = K*16*d, stride_head = 16*d, stride_token = d (one 16 x d tile
+ * per (block, kv-head), contiguous). A contiguous un-paged cache
+ * [B, S_pad, K, d] is the same thing with stride_block = 16*K*d,
+ * stride_head = d, stride_token = K*d and the identity block table
+ * table[b][j] = b*(S_pad/16) + j.
+ *
+ * For GQA_DTYPE_I8, k_scale / v_scale hold one fp16 scale per (block, kv-head,
+ * slot) as [num_blocks, K, 16]; the cached value is code * scale. Other dtypes
+ * leave them NULL.
+ *
+ * Requirements: block_size == 16; head_dim in {64, 128}; k, v, k_scale,
+ * v_scale 16-byte aligned; every stride times the element size a multiple of
+ * 16 bytes; stride_token >= head_dim.
+ */
+typedef struct {
+    void   *k;                /* device */
+    void   *v;                /* device */
+    void   *k_scale;          /* device, fp16 [num_blocks, K, 16], I8 only */
+    void   *v_scale;          /* device, fp16 [num_blocks, K, 16], I8 only */
+    int64_t num_blocks;
+    int32_t num_kv_heads;     /* K */
+    int32_t block_size;       /* must be 16 */
+    int32_t head_dim;         /* d */
+    int32_t dtype;            /* gqa_dtype_t */
+    int64_t stride_block;     /* elements */
+    int64_t stride_head;      /* elements */
+    int64_t stride_token;     /* elements */
+} gqa_kv_cache_t;
+
+/* Optional knobs of gqa_decode (pass NULL for the defaults). */
+typedef struct {
+    int32_t kernel;               /* 0 auto, 1 tensor-core (mma.sync) kernel, 2 CUDA-core kernel */
+    int32_t max_warps;            /* 0 = fill the GPU; > 0 caps the decode warps, i.e. KV splits */
+    int32_t min_blocks_per_warp;  /* 0 = default (4): smallest KV range one warp takes */
+    void   *event_main_begin;     /* optional cudaEvent_t recorded just before the split-KV kernel */
+    void   *event_main_end;       /* optional cudaEvent_t recorded just after it */
+} gqa_decode_opts_t;
+
+/* Human-readable name of a gqa_status_t. Never NULL. */
+GQA_API const char *gqa_status_string(int status);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+GQA_API int gqa_version(void);
+
+/*
+ * Elements of K and V together that a pool of num_blocks 16-token blocks holds:
+ * 2 * num_blocks * num_kv_heads * 16 * head_dim. The closed form of
+ * "分组查询注意力 (GQA)", 关键参数 item 2 (2*K*d_k per token per layer) and
+ * "LLM 推理性能优化实战", section 6.1, sized by the allocator. Returns -1 on a
+ * negative argument. Host only; needs no GPU.
+ */
+GQA_API int64_t gqa_kv_pool_elements(int64_t num_blocks, int32_t num_kv_heads, int32_t head_dim);
+
+/*
+ * Paged KV append: write the new token of every sequence into the cache.
+ * For each b < batch and kv-head g < K, with pos = positions[b]:
+ *   block = block_tables[b*max_blocks_per_seq + pos/16], slot = pos % 16,
+ *   K[block, g, slot, :] = k_new[b, g, :],  V[...] = v_new[b, g, :].
+ * (The write of one token's K and V per step, "LLM 推理性能优化实战" sections
+ * 5.3-5.4; the block table of section 8.2.)
+ *
+ *  k_new, v_new   device, [batch, K, head_dim] of new_dtype, 16-byte aligned.
+ *                 For F32/F16/BF16 caches new_dtype must equal the cache dtype
+ *                 and the copy is bit-exact. For an I8 cache new_dtype is F32,
+ *                 F16 or BF16 and each (token, kv-head) row is quantised on the
+ *                 device: amax = max|x| (fp32); s = fp16_rne(min(amax/127, 65504));
+ *                 code = s == 0 ? 0 : clamp(rint(x/s), -127, 127) with IEEE fp32
+ *                 division (symmetric int8, "LLM 推理性能优化实战" sections 15.1,
+ *                 15.2, 15.5). The scale goes to k_scale / v_scale.
+ *  block_tables   device int32 [batch, max_blocks_per_seq].
+ *  positions      device int32 [batch]: slot index of the new token, i.e. the
+ *                 context length BEFORE the append. Not modified; the caller
+ *                 advances its context lengths.
+ *  err_flag       device int32 or NULL (GQA_DEVERR_POSITION / _BLOCK_INDEX).
+ */
+GQA_API int gqa_kv_append(const gqa_kv_cache_t *cache, const void *k_new, const void *v_new,
+                  int32_t new_dtype, const int32_t *block_tables,
+                  int32_t max_blocks_per_seq, const int32_t *positions, int32_t batch,
+                  int32_t *err_flag, void *stream);
+
+/*
+ * Bytes of device workspace gqa_decode needs for this shape on `device`
+ * (-1 = the current device). Returns 0 on bad arguments. The bound covers every
+ * kernel choice and every context-length mix of this shape.
+ */
+GQA_API size_t gqa_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t device);
+
+/*
+ * Grouped-query decode attention over the paged cache:
+ *   out[b, h, :] = sum_t softmax_t(scale * q[b,h,:] . K[b, t, g]) V[b, t, g],
+ *   g = h / (num_heads / K), t in [0, context_lens[b]),
+ * where K[b, t, g] is read through block_tables as in gqa_kv_append.
+ * The KV range of each (sequence, kv-head) is split across warps
+ * (split-KV flash decoding, "LLM 推理性能优化实战" section 10.2); each split
+ * keeps a running (max, sum, weighted V) state (online softmax, section 9.2)
+ * and a second kernel merges the splits with their log-sum-exp weights
+ * ("global max and sum" reduction of section 10.2). An empty context
+ * (length 0) yields a zero output row.
+ *
+ *  q              device [batch, num_heads, head_dim]; BF16 for a BF16 cache,
+ *                 F16 for F16, F32 for F32, BF16 or F16 for an I8 cache.
+ *  block_tables   device int32 [batch, max_blocks_per_seq].
+ *  context_lens   device int32 [batch], lengths AFTER the append, each in
+ *                 [0, max_blocks_per_seq*16].
+ *  scale          softmax scale (1/sqrt(head_dim) for standard attention).
+ *  out            device [batch, num_heads, head_dim] of out_dtype (F32, BF16
+ *                 or F16); 16-byte aligned.
+ *  workspace      device, >= gqa_decode_workspace_size(...) bytes, 256-byte
+ *                 aligned; contents need no initialisation and are clobbered.
+ *  opts           NULL or tuning knobs (gqa_decode_opts_t).
+ *  Limits: num_heads % K == 0; num_heads / K <= 8; batch <= 8191;
+ *  batch * K * max_blocks_per_seq < 2^31.
+ */
+GQA_API int gqa_decode(const gqa_kv_cache_t *cache, const void *q, int32_t q_dtype,
+               int32_t num_heads, const int32_t *block_tables, int32_t max_blocks_per_seq,
+               const int32_t *context_lens, int32_t batch, float scale, void *out,
+               int32_t out_dtype, void *workspace, size_t workspace_bytes,
+               const gqa_decode_opts_t *opts, int32_t *err_flag, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_DECODE_H */
