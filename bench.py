@@ -101,8 +101,9 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle sampling; keeps the samples taken inside the
+    timed window (host wall clock, the GPU being busy for all of it)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -117,12 +118,13 @@ class ClockSampler:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t_begin: float, t_end: float):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -130,20 +132,39 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        import datetime
         rows = []
         for ln in open(self.path).read().splitlines():
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) >= 9:
-                rows.append(parts)
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            rows.append((ts, parts))
         os.unlink(self.path)
-        if not rows:
+        inside = [p for ts, p in rows if t_begin <= ts <= t_end]
+        window = "timed region"
+        if not inside and rows:             # timed region shorter than the sampling period
+            mid = 0.5 * (t_begin + t_end)
+            inside = [min(rows, key=lambda r: abs(r[0] - mid))[1]]
+            window = "nearest sample (timed region shorter than sampling period)"
+        if not inside:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[2]) for r in inside) if v is not None]
+        mx = [v for v in (num(r[3]) for r in inside) if v is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[6 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "window": window}
 
 
 def dist_info():
@@ -213,15 +234,18 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)                            # let the sampler see the load start
+    time.sleep(0.5)                            # sampler start-up
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    w0 = time.time()
     t0.record(stream)
     for i in range(args.steps):
         step(events=kev[i])
     t1.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    w1 = time.time()
+    clk = clocks.stop(w0, w1)
     if world > 1:
         dist.barrier()
     ms = t0.elapsed_time(t1) / args.steps
@@ -424,7 +448,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)

@@ -94,6 +94,10 @@ def load() -> ctypes.CDLL:
                                        ctypes.c_float, vp, i32, vp, ctypes.c_size_t,
                                        ctypes.POINTER(DecodeOpts), vp, vp]
             lib.gqa_decode.restype = ctypes.c_int
+            lib.gqa_decode_noalloc.argtypes = [ctypes.POINTER(KVCacheDesc), vp, i32, i32, vp, i32,
+                                               vp, i32, ctypes.c_float, vp, i32,
+                                               ctypes.POINTER(DecodeOpts), vp, vp]
+            lib.gqa_decode_noalloc.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -226,6 +230,29 @@ def gqa_decode(cache: PagedKVCache, q: torch.Tensor, block_tables: torch.Tensor,
                            _ptr(out), DTYPE_CODE[out.dtype], _ptr(workspace), workspace.numel(),
                            ctypes.byref(opts), _ptr(err), _stream_ptr(stream))
     _check(st, "gqa_decode")
+    return out
+
+
+def gqa_decode_noalloc(cache: PagedKVCache, q: torch.Tensor, block_tables: torch.Tensor,
+                       context_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
+                       out_dtype: torch.dtype = torch.float32, kernel: int = KERNEL_AUTO,
+                       err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """gqa_decode with the library's built-in scratch instead of a workspace.
+
+    For callers that may not allocate device memory; the output tensor is still
+    the caller's (pass ``out`` to avoid even that allocation here). Calls that
+    overlap on the GPU share one scratch array and race."""
+    B, H, d = q.shape
+    if out is None:
+        out = torch.empty((B, H, d), dtype=out_dtype, device=q.device)
+    opts = DecodeOpts(kernel, 0, 0, None, None)
+    desc = cache.desc()
+    st = load().gqa_decode_noalloc(ctypes.byref(desc), _ptr(q), DTYPE_CODE[q.dtype], H,
+                                   _ptr(block_tables), int(block_tables.shape[1]),
+                                   _ptr(context_lens), B, float(scale), _ptr(out),
+                                   DTYPE_CODE[out.dtype], ctypes.byref(opts), _ptr(err),
+                                   _stream_ptr(stream))
+    _check(st, "gqa_decode_noalloc")
     return out
 
 

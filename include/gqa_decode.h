@@ -191,6 +191,35 @@ GQA_API int gqa_decode(const gqa_kv_cache_t *cache, const void *q, int32_t q_dty
                int32_t out_dtype, void *workspace, size_t workspace_bytes,
                const gqa_decode_opts_t *opts, int32_t *err_flag, void *stream);
 
+/*
+ * gqa_decode without a caller-supplied workspace. The pages have no
+ * counterpart for this call; it exists for callers that cannot allocate device
+ * memory: a plugin running inside a host engine whose device allocator it does
+ * not own, or a runtime that plans every device byte before serving starts and
+ * forbids allocation in the decode loop. Such callers can still pass their
+ * inputs and outputs, but have nowhere to put the split-KV partial results.
+ *
+ * The scratch lives in one fixed array of GQA_NOALLOC_SCRATCH_BYTES compiled
+ * into the library; every GPU that loads the library holds it until the
+ * process exits. Arguments and results are those of gqa_decode minus the
+ * workspace. This call allocates nothing (no cudaMalloc, no library allocator).
+ *  - Returns GQA_ERR_WORKSPACE when the shape needs more scratch than the array
+ *    holds (the five workloads of the benchmark need under 10 MiB).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture on the device.
+ *  - Every call shares the one array and it keeps the last call's contents
+ *    (nothing in it needs to start at zero). Calls whose GPU work overlaps --
+ *    different streams, or different host threads -- race on it; serialise them.
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+GQA_API int gqa_decode_noalloc(const gqa_kv_cache_t *cache, const void *q, int32_t q_dtype,
+                               int32_t num_heads, const int32_t *block_tables,
+                               int32_t max_blocks_per_seq, const int32_t *context_lens,
+                               int32_t batch, float scale, void *out, int32_t out_dtype,
+                               const gqa_decode_opts_t *opts, int32_t *err_flag, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
