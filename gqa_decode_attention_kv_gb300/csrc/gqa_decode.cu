@@ -59,6 +59,15 @@ struct DecodeArgs {
     float scale_log2;    // scale * log2(e)
 };
 
+// Warps per CTA and shared-memory ring bytes per warp of the split-KV kernel
+// (overridable at build time for tuning sweeps).
+#ifndef GQA_WARPS_PER_CTA
+#define GQA_WARPS_PER_CTA 4
+#endif
+#ifndef GQA_RING_BYTES_PER_WARP
+#define GQA_RING_BYTES_PER_WARP 16384
+#endif
+
 template <int kKind, typename T, int D>
 struct Cfg {
     static constexpr bool kI8 = std::is_same<T, int8_t>::value;
@@ -67,8 +76,8 @@ struct Cfg {
     static constexpr int kTile = 16 * D * kEs;                       // one (block, head) tile
     static constexpr int kScaleBytes = kI8 ? 64 : 0;                // 16 k + 16 v fp16 scales
     static constexpr int kStage = ((2 * kTile + kScaleBytes + 1023) / 1024) * 1024;
-    static constexpr int kStages = std::max(2, std::min(6, 24576 / kStage));
-    static constexpr int kWarps = 4;
+    static constexpr int kStages = std::max(2, std::min(8, GQA_RING_BYTES_PER_WARP / kStage));
+    static constexpr int kWarps = GQA_WARPS_PER_CTA;
     static constexpr bool kSwizzle = (kKind == kKernelMma);
     static constexpr int kBoxInner = kSwizzle ? 128 / kEs : D;        // elements per box row
     static constexpr int kNumBox = kSwizzle ? (D * kEs) / 128 : 1;
@@ -250,8 +259,8 @@ template <class C, int D>
 struct MmaState {
     float m[2], l[2];          // heads 2c, 2c+1 of the group (log2 units)
     float acc[C::kMt][4];      // O^T fragments: rows = dims, cols = heads 2c, 2c+1
-    uint4 qf[D / 32];          // Q^T B-fragments for the current pair
-    uint4 qn[D / 32];          // prefetched fragments of the next pair
+    uint2 qf[D / 16];          // Q^T B-fragments of the current pair, one per 16-dim k-step
+    uint2 qn[D / 16];          // prefetched fragments of the next pair
 
     __device__ __forceinline__ void reset() {
         m[0] = m[1] = -INFINITY;
@@ -261,43 +270,49 @@ struct MmaState {
     }
 };
 
-// Q fragments of query head g*G + r (zero for padded heads r >= G).
-// bf16/f16 caches: qf[qc] holds dims qc*32 + 8c .. +7 (matching the K-tile loads).
-// int8 cache: qf[2t + h] holds dims 16(c + 4t) + 8h .. +7, converted to f16.
+// Everything one block needs from shared memory, gathered before any math so
+// the ring slot can be refilled while the block is being computed.
+template <class C, int D>
+struct MmaFrags {
+    uint32_t k[D / 16][4];     // bf16/f16: A fragments of K per k-step; int8: raw code quads
+    uint32_t v[C::kMt][4];     // bf16/f16: A fragments of V^T per m-tile; int8: raw rows of 4 tokens
+    float ks_r, ks_r8, vs_r, vs_r8;   // int8 scales of tokens r and r+8
+};
+
+// Q fragments (B operand of the score MMA) of query head g*G + r; zero for
+// padded heads r >= G. k-step t covers dims 16t..16t+15:
+//  bf16/f16: .x = dims 16t + 2c, +1;     .y = dims 16t + 2c + 8, +9  (standard layout)
+//  int8:     .x = dims 16t + 4c, +1;     .y = dims 16t + 4c + 2, +3  (matches the code quads)
 template <class C, int D>
 __device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int b, int g, int r, int c,
-                                             uint4 (&qf)[D / 32]) {
+                                             uint2 (&qf)[D / 16]) {
     if (r >= a.G || b >= a.B) {
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i) qf[i] = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < D / 16; ++i) qf[i] = make_uint2(0, 0);
         return;
     }
-    const uint8_t* base = static_cast<const uint8_t*>(a.q) + ((long long)b * a.H + (long long)g * a.G + r) * D * 2;
-    if constexpr (!C::kI8) {
+    const uint16_t* base = static_cast<const uint16_t*>(a.q) + ((long long)b * a.H + (long long)g * a.G + r) * D;
 #pragma unroll
-        for (int qc = 0; qc < D / 32; ++qc) qf[qc] = ldg128(base + (qc * 32 + 8 * c) * 2);
-    } else {
-#pragma unroll
-        for (int t = 0; t < D / 64; ++t) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint4 raw = ldg128(base + (16 * (c + 4 * t) + 8 * hh) * 2);
-                if (a.q_dtype == GQA_DTYPE_BF16) {
-                    raw.x = bf16x2_to_f16x2(raw.x); raw.y = bf16x2_to_f16x2(raw.y);
-                    raw.z = bf16x2_to_f16x2(raw.z); raw.w = bf16x2_to_f16x2(raw.w);
-                }
-                qf[2 * t + hh] = raw;
+    for (int t = 0; t < D / 16; ++t) {
+        if constexpr (!C::kI8) {
+            qf[t].x = __ldg(reinterpret_cast<const uint32_t*>(base + 16 * t + 2 * c));
+            qf[t].y = __ldg(reinterpret_cast<const uint32_t*>(base + 16 * t + 2 * c + 8));
+        } else {
+            uint2 raw = __ldg(reinterpret_cast<const uint2*>(base + 16 * t + 4 * c));
+            if (a.q_dtype == GQA_DTYPE_BF16) {
+                raw.x = bf16x2_to_f16x2(raw.x);
+                raw.y = bf16x2_to_f16x2(raw.y);
             }
+            qf[t] = raw;
         }
     }
 }
 
-// First output dim of the 8-dim run k owned by row-group r.
+// Output dim of accumulator row (j, rh): row r + 8*rh of m-tile j.
 template <class C, int D>
-__device__ __forceinline__ int run_dim(int k, int r) {
-    if constexpr (C::kI8) return 16 * r + 8 * k;
-    else if constexpr (D == 128) return 16 * r + 8 * (k ^ (r >> 2));
-    else return 8 * r;
+__device__ __forceinline__ int acc_dim(int j, int rh, int r) {
+    if constexpr (C::kI8) return 16 * r + 2 * j + rh;
+    else return 16 * j + r + 8 * rh;
 }
 
 template <bool kBf16>
@@ -307,65 +322,90 @@ __device__ __forceinline__ void mma_t(float (&d)[4], uint32_t a0, uint32_t a1, u
     else mma_f16(d, a0, a1, a2, a3, b0, b1);
 }
 
-// One 16-token block on the tensor cores.
-template <class C, int D>
-__device__ __forceinline__ void mma_block(MmaState<C, D>& st, uint32_t stage, int nvalid, int r,
-                                          int c, int lane, float scale_log2) {
-    constexpr bool kB = C::kBf16;            // P and V operand type: bf16, else f16
-    const uint32_t sk = stage, sv = stage + C::kTile;
+// Address of 16-byte chunk `chunk` of row `tok` in a tile written by TMA with
+// 128-byte swizzle (2 KB boxes of 16 rows x 128 B; chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int tok, int chunk) {
+    return tile + (uint32_t)(chunk >> 3) * 2048u + (uint32_t)tok * 128u +
+           ((uint32_t)((chunk & 7) ^ (tok & 7)) << 4);
+}
 
-    // ---- scores: S^T[tok][head] = K_tile . Q^T
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+// Gather one block's operands from shared memory (all reads of the slot).
+template <class C, int D>
+__device__ __forceinline__ void mma_load(MmaFrags<C, D>& f, uint32_t stage, int lane, int r, int c) {
+    const uint32_t sk = stage, sv = stage + C::kTile;
+    const int mi = lane >> 3, rr = lane & 7;
     if constexpr (!C::kI8) {
+        // K: matrices (toks 0-7 | 8-15) x (dims 16t..+7 | +8..+15) = a0, a1, a2, a3
 #pragma unroll
-        for (int qc = 0; qc < D / 32; ++qc) {
-            const uint32_t bx = sk + (qc >> 1) * 2048;
-            const uint32_t ch = (uint32_t)((((qc & 1) << 2) | c) ^ r) << 4;
-            const uint4 x = lds128(bx + r * 128 + ch);
-            const uint4 y = lds128(bx + (r + 8) * 128 + ch);
-            mma_t<kB>(sa, x.x, y.x, x.y, y.y, st.qf[qc].x, st.qf[qc].y);
-            mma_t<kB>(sb, x.z, y.z, x.w, y.w, st.qf[qc].z, st.qf[qc].w);
-        }
+        for (int t = 0; t < D / 16; ++t)
+            ldsm_x4(swz(sk, rr + 8 * (mi & 1), 2 * t + (mi >> 1)), f.k[t]);
+        // V^T: transposed matrices (dims 16j..+7 | +8..+15) x (toks 0-7 | 8-15)
+#pragma unroll
+        for (int j = 0; j < C::kMt; ++j)
+            ldsm_x4_t(swz(sv, rr + 8 * (mi >> 1), 2 * j + (mi & 1)), f.v[j]);
     } else {
+        // K codes: x4 number t holds chunks 2t (a0/a1) and 2t+1 (a2/a3), 16 codes each
 #pragma unroll
-        for (int t = 0; t < D / 64; ++t) {
-            const uint32_t ch = (uint32_t)((c + 4 * t) ^ r) << 4;
-            const uint4 x = lds128(sk + r * 128 + ch);
-            const uint4 y = lds128(sk + (r + 8) * 128 + ch);
-            uint32_t xl[4], xh[4], yl[4], yh[4];
-            i8x4_to_f16x4(x.x, xl[0], xh[0]); i8x4_to_f16x4(x.y, xl[1], xh[1]);
-            i8x4_to_f16x4(x.z, xl[2], xh[2]); i8x4_to_f16x4(x.w, xl[3], xh[3]);
-            i8x4_to_f16x4(y.x, yl[0], yh[0]); i8x4_to_f16x4(y.y, yl[1], yh[1]);
-            i8x4_to_f16x4(y.z, yl[2], yh[2]); i8x4_to_f16x4(y.w, yl[3], yh[3]);
-            const uint32_t qw[8] = {st.qf[2 * t].x, st.qf[2 * t].y, st.qf[2 * t].z, st.qf[2 * t].w,
-                                    st.qf[2 * t + 1].x, st.qf[2 * t + 1].y, st.qf[2 * t + 1].z,
-                                    st.qf[2 * t + 1].w};
+        for (int t = 0; t < D / 32; ++t)
+            ldsm_x4(swz(sk, rr + 8 * (mi & 1), 2 * t + (mi >> 1)), f.k[t]);
+        // V codes: dims 16r..16r+15 of tokens 2c, 2c+1, 2c+8, 2c+9
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                if (m & 1) mma_f16(sb, xl[m], yl[m], xh[m], yh[m], qw[2 * m], qw[2 * m + 1]);
-                else mma_f16(sa, xl[m], yl[m], xh[m], yh[m], qw[2 * m], qw[2 * m + 1]);
-            }
+        for (int i = 0; i < 4; ++i) {
+            const int tok = 2 * c + (i & 1) + 8 * (i >> 1);
+            const uint4 raw = lds128(swz(sv, tok, r));
+            f.v[i][0] = raw.x; f.v[i][1] = raw.y; f.v[i][2] = raw.z; f.v[i][3] = raw.w;
         }
-    }
-    // fragment: [0] = (tok r, head 2c), [1] = (tok r, head 2c+1), [2]/[3] = tok r+8
-    float kr = scale_log2, kr8 = scale_log2, vr_s = 1.f, vr8_s = 1.f;
-    if constexpr (C::kI8) {
         const uint32_t sc = stage + 2 * C::kTile;
         unsigned short h0, h1, h2, h3;
         asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h0) : "r"(sc + 2 * r));
         asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h1) : "r"(sc + 2 * (r + 8)));
         asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h2) : "r"(sc + 32 + 2 * r));
         asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h3) : "r"(sc + 32 + 2 * (r + 8)));
-        kr = __half2float(__ushort_as_half(h0)) * scale_log2;
-        kr8 = __half2float(__ushort_as_half(h1)) * scale_log2;
-        vr_s = __half2float(__ushort_as_half(h2));
-        vr8_s = __half2float(__ushort_as_half(h3));
+        f.ks_r = __half2float(__ushort_as_half(h0));
+        f.ks_r8 = __half2float(__ushort_as_half(h1));
+        f.vs_r = __half2float(__ushort_as_half(h2));
+        f.vs_r8 = __half2float(__ushort_as_half(h3));
+    }
+}
+
+// One 16-token block on the tensor cores, from gathered operands.
+template <class C, int D>
+__device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& f, int nvalid,
+                                            int r, int c, float scale_log2) {
+    constexpr bool kB = C::kBf16;            // P and V operand type: bf16, else f16
+
+    // ---- scores: S^T[tok][head] = K_tile . Q^T (two accumulators halve the chain)
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (!C::kI8) {
+#pragma unroll
+        for (int t = 0; t < D / 16; ++t) {
+            if (t & 1) mma_t<kB>(sb, f.k[t][0], f.k[t][1], f.k[t][2], f.k[t][3], st.qf[t].x, st.qf[t].y);
+            else mma_t<kB>(sa, f.k[t][0], f.k[t][1], f.k[t][2], f.k[t][3], st.qf[t].x, st.qf[t].y);
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < D / 32; ++t) {
+            uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
+            i8x4_to_f16x4(f.k[t][0], l0, h0);          // tok r,   chunk 2t
+            i8x4_to_f16x4(f.k[t][1], l1, h1);          // tok r+8, chunk 2t
+            i8x4_to_f16x4(f.k[t][2], l2, h2);          // tok r,   chunk 2t+1
+            i8x4_to_f16x4(f.k[t][3], l3, h3);          // tok r+8, chunk 2t+1
+            mma_f16(sa, l0, l1, h0, h1, st.qf[2 * t].x, st.qf[2 * t].y);
+            mma_f16(sb, l2, l3, h2, h3, st.qf[2 * t + 1].x, st.qf[2 * t + 1].y);
+        }
+    }
+    // fragment: [0] = (tok r, head 2c), [1] = (tok r, head 2c+1), [2]/[3] = tok r+8
+    float kr = scale_log2, kr8 = scale_log2, vr_s = 1.f, vr8_s = 1.f;
+    if constexpr (C::kI8) {
+        kr = f.ks_r * scale_log2;
+        kr8 = f.ks_r8 * scale_log2;
+        vr_s = f.vs_r;
+        vr8_s = f.vs_r8;
     }
     float s0 = (sa[0] + sb[0]) * kr, s1 = (sa[1] + sb[1]) * kr;
     float s2 = (sa[2] + sb[2]) * kr8, s3 = (sa[3] + sb[3]) * kr8;
-    const bool ok_r = r < nvalid, ok_r8 = r + 8 < nvalid;
-    if (!ok_r) { s0 = -INFINITY; s1 = -INFINITY; vr_s = 0.f; }
-    if (!ok_r8) { s2 = -INFINITY; s3 = -INFINITY; vr8_s = 0.f; }
+    if (r >= nvalid) { s0 = -INFINITY; s1 = -INFINITY; vr_s = 0.f; }
+    if (r + 8 >= nvalid) { s2 = -INFINITY; s3 = -INFINITY; vr8_s = 0.f; }
 
     // ---- online softmax (per head, over the 16 tokens of this block)
     float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
@@ -403,45 +443,45 @@ __device__ __forceinline__ void mma_block(MmaState<C, D>& st, uint32_t stage, in
     const uint32_t bl0 = __byte_perm(__shfl_sync(kFull, lr, srcA), __shfl_sync(kFull, lr, srcB), sel);
     const uint32_t bl1 = __byte_perm(__shfl_sync(kFull, lr8, srcA), __shfl_sync(kFull, lr8, srcB), sel);
 
-    // ---- V^T fragments for tokens 2c, 2c+1, 2c+8, 2c+9
-    uint32_t vr[4][8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int tok = 2 * c + (i & 1) + 8 * (i >> 1);
-        const uint32_t row = sv + tok * 128;
-        if constexpr (C::kI8) {
-            const uint4 raw = lds128(row + ((uint32_t)(r ^ (tok & 7)) << 4));
-            i8x4_to_f16x4(raw.x, vr[i][0], vr[i][1]); i8x4_to_f16x4(raw.y, vr[i][2], vr[i][3]);
-            i8x4_to_f16x4(raw.z, vr[i][4], vr[i][5]); i8x4_to_f16x4(raw.w, vr[i][6], vr[i][7]);
-        } else if constexpr (D == 128) {
-            const int h = r >> 2;
-            const uint32_t bx = row + h * 2048;
-            const uint4 x0 = lds128(bx + ((uint32_t)((2 * (r & 3) + h) ^ (tok & 7)) << 4));
-            const uint4 x1 = lds128(bx + ((uint32_t)((2 * (r & 3) + 1 - h) ^ (tok & 7)) << 4));
-            vr[i][0] = x0.x; vr[i][1] = x0.y; vr[i][2] = x0.z; vr[i][3] = x0.w;
-            vr[i][4] = x1.x; vr[i][5] = x1.y; vr[i][6] = x1.z; vr[i][7] = x1.w;
-        } else {
-            const uint4 x0 = lds128(row + ((uint32_t)(r ^ (tok & 7)) << 4));
-            vr[i][0] = x0.x; vr[i][1] = x0.y; vr[i][2] = x0.z; vr[i][3] = x0.w;
-            vr[i][4] = vr[i][5] = vr[i][6] = vr[i][7] = 0u;
-        }
-        if (tok >= nvalid) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) vr[i][e] = 0u;
-        }
-    }
-
     // ---- O^T[dim][head] += V^T . P^T (high part, then low part)
+    if constexpr (!C::kI8) {
+        if (nvalid < kBlock) {
+            // zero V of tokens past the end: the slots hold arbitrary (even NaN) bits
+            const uint32_t m01 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
+            const uint32_t m89 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
 #pragma unroll
-    for (int j = 0; j < C::kMt; ++j) {
-        const uint32_t a0 = __byte_perm(vr[0][j], vr[1][j], 0x5410);
-        const uint32_t a1 = __byte_perm(vr[0][j], vr[1][j], 0x7632);
-        const uint32_t a2 = __byte_perm(vr[2][j], vr[3][j], 0x5410);
-        const uint32_t a3 = __byte_perm(vr[2][j], vr[3][j], 0x7632);
-        mma_t<kB>(st.acc[j], a0, a1, a2, a3, bh0, bh1);
-        mma_t<kB>(st.acc[j], a0, a1, a2, a3, bl0, bl1);
+            for (int j = 0; j < C::kMt; ++j) {
+                f.v[j][0] &= m01; f.v[j][1] &= m01; f.v[j][2] &= m89; f.v[j][3] &= m89;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < C::kMt; ++j) {
+            mma_t<kB>(st.acc[j], f.v[j][0], f.v[j][1], f.v[j][2], f.v[j][3], bh0, bh1);
+            mma_t<kB>(st.acc[j], f.v[j][0], f.v[j][1], f.v[j][2], f.v[j][3], bl0, bl1);
+        }
+    } else {
+        // codes -> f16 pairs: vr[i][jj] = dims (16r + 2jj, +1) of token i
+        uint32_t vr[4][8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int tok = 2 * c + (i & 1) + 8 * (i >> 1);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) i8x4_to_f16x4(f.v[i][w], vr[i][2 * w], vr[i][2 * w + 1]);
+            if (tok >= nvalid) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) vr[i][e] = 0u;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < C::kMt; ++j) {
+            const uint32_t a0 = __byte_perm(vr[0][j], vr[1][j], 0x5410);
+            const uint32_t a1 = __byte_perm(vr[0][j], vr[1][j], 0x7632);
+            const uint32_t a2 = __byte_perm(vr[2][j], vr[3][j], 0x5410);
+            const uint32_t a3 = __byte_perm(vr[2][j], vr[3][j], 0x7632);
+            mma_f16(st.acc[j], a0, a1, a2, a3, bh0, bh1);
+            mma_f16(st.acc[j], a0, a1, a2, a3, bl0, bl1);
+        }
     }
-    (void)lane;
 }
 
 // Write the state of pair (b, g): final output if this warp saw the whole pair,
@@ -462,19 +502,16 @@ __device__ __forceinline__ void mma_flush(const DecodeArgs& a, MmaState<C, D>& s
         if (hh >= a.G) continue;
         const float lsum = e ? l1 : l0;
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const long long obase = whole ? ((long long)b * a.H + (long long)g * a.G + hh) * D
+                                      : (slot * a.G + hh) * D;
 #pragma unroll
-        for (int k = 0; k < C::kRuns; ++k) {
-            float v[8];
+        for (int j = 0; j < C::kMt; ++j) {
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                v[2 * jj] = st.acc[4 * k + jj][e];
-                v[2 * jj + 1] = st.acc[4 * k + jj][e + 2];
-            }
-            const int dim = run_dim<C, D>(k, r);
-            if (whole) {
-                store8(a.out, a.out_dtype, ((long long)b * a.H + (long long)g * a.G + hh) * D + dim, v, inv);
-            } else {
-                store8(a.ws_o, GQA_DTYPE_F32, (slot * a.G + hh) * D + dim, v, 1.f);
+            for (int rh = 0; rh < 2; ++rh) {
+                const int dim = acc_dim<C, D>(j, rh, r);
+                const float v = st.acc[j][e + 2 * rh];
+                if (whole) store1(a.out, a.out_dtype, obase + dim, v * inv);
+                else a.ws_o[obase + dim] = v;
             }
         }
         if (!whole && r == 0) a.ws_ml[slot * a.G + hh] = make_float2(st.m[e], lsum);
@@ -706,12 +743,19 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             return;
         }
         const int nvalid = min((int)kBlock, clen - kBlock * cj);
-        if (!bad[s]) {
-            if constexpr (kKind == kKernelMma) mma_block<C, D>(st, ring + s * C::kStage, nvalid, r, c, lane, a.scale_log2);
-            else fma_block<C, D, T>(a, st, ring + s * C::kStage, nvalid, lane);
+        const bool unit_ok = !bad[s];
+        if constexpr (kKind == kKernelMma) {
+            // read the whole slot, hand it back to TMA, then compute from registers
+            MmaFrags<C, D> fr;
+            if (unit_ok) mma_load<C, D>(fr, ring + s * C::kStage, lane, r, c);
+            __syncwarp();
+            if (i + C::kStages < n_units) issue(u_begin + i + C::kStages, s);
+            if (unit_ok) mma_compute<C, D>(st, fr, nvalid, r, c, a.scale_log2);
+        } else {
+            if (unit_ok) fma_block<C, D, T>(a, st, ring + s * C::kStage, nvalid, lane);
+            __syncwarp();
+            if (i + C::kStages < n_units) issue(u_begin + i + C::kStages, s);
         }
-        __syncwarp();
-        if (i + C::kStages < n_units) issue(u_begin + i + C::kStages, s);
 
         const bool last_of_pair = (cj == cnb - 1);
         if (last_of_pair || i == n_units - 1) {
@@ -730,7 +774,7 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             next_pair(pref, a.B, a.K, nb_b, nb_g);
             if constexpr (kKind == kKernelMma) {
 #pragma unroll
-                for (int k = 0; k < D / 32; ++k) st.qf[k] = st.qn[k];
+                for (int k = 0; k < D / 16; ++k) st.qf[k] = st.qn[k];
                 if (cu_pair + cnb < u_end) load_q_frags<C, D>(a, nb_b, nb_g, r, c, st.qn);
             } else {
                 fma_load_q<C, D>(a, st, cb, cg, lane);
@@ -743,49 +787,78 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 
 // ------------------------------------------------------------------ combine
 
-// Merge the splits of each (sequence, kv-head) pair; zero rows of empty sequences.
+constexpr int kCombineWarps = 8;
+
+// Merge the splits of one (sequence, query head); zero rows of empty sequences.
+// Warp w takes splits w, w+8, ...; lane l owns dims 4l..4l+3; the eight partial
+// sums meet in shared memory.
 template <int D>
-__global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
-    const int pair = blockIdx.x;
-    const int b = pair / a.K, g = pair % a.K;
-    const int R = a.ws_hdr[0];
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecodeArgs a) {
+    __shared__ float s_red[kCombineWarps];
+    __shared__ float s_acc[kCombineWarps][D];
+    __shared__ float s_l[kCombineWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int bh = blockIdx.x;
+    const int b = bh / a.H, h = bh % a.H, g = h / a.G, hh = h % a.G;
+    const long long orow = (long long)bh * D;
     const int p0 = a.ws_pref[b];
     const int nb = a.ws_pref[b + 1] - p0;
-    const int items = a.G * (D / 4);
     if (nb == 0) {
-        for (int it = threadIdx.x; it < items; it += blockDim.x) {
-            const int hh = it / (D / 4), d4 = (it % (D / 4)) * 4;
-            const long long o = ((long long)b * a.H + (long long)g * a.G + hh) * D + d4;
-            for (int e = 0; e < 4; ++e) store1(a.out, a.out_dtype, o + e, 0.f);
-        }
+        for (int i = tid; i < D; i += blockDim.x) store1(a.out, a.out_dtype, orow + i, 0.f);
         return;
     }
+    const int R = a.ws_hdr[0];
     const long long u0 = (long long)a.K * p0 + (long long)g * nb;
-    const long long u1 = u0 + nb;
-    const int w0 = (int)(u0 / R), w1 = (int)((u1 - 1) / R);
+    const int w0 = (int)(u0 / R), w1 = (int)((u0 + nb - 1) / R);
     if (w0 == w1) return;                      // one warp saw the whole pair and wrote it
-    for (int it = threadIdx.x; it < items; it += blockDim.x) {
-        const int hh = it / (D / 4), d4 = (it % (D / 4)) * 4;
-        float M = -INFINITY;
-        for (int w = w0; w <= w1; ++w) M = fmaxf(M, a.ws_ml[((long long)pair + w) * a.G + hh].x);
-        float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
-            for (int w = w0; w <= w1; ++w) {
-                const long long slot = (long long)pair + w;
-                const float2 ml = a.ws_ml[slot * a.G + hh];
-                const float e = fast_exp2(ml.x - M);
-                L += ml.y * e;
-                const float4 o = *reinterpret_cast<const float4*>(a.ws_o + (slot * a.G + hh) * D + d4);
+    const long long first = (long long)b * a.K + g + w0;   // slot of the first split
+    const int n = w1 - w0 + 1;
+
+    // pass 1: the largest running maximum
+    float M = -INFINITY;
+    for (int p = tid; p < n; p += blockDim.x) M = fmaxf(M, a.ws_ml[(first + p) * a.G + hh].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    if (lane == 0) s_red[warp] = M;
+    __syncthreads();
+    M = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, s_red[w]);
+
+    // pass 2: weighted sums
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const bool has_dims = 4 * lane < D;
+    if (M != -INFINITY) {
+#pragma unroll 4
+        for (int p = warp; p < n; p += kCombineWarps) {
+            const long long slot = first + p;
+            const float2 ml = a.ws_ml[slot * a.G + hh];
+            const float e = fast_exp2(ml.x - M);
+            L += ml.y * e;
+            if (has_dims) {
+                const float4 o = *reinterpret_cast<const float4*>(a.ws_o + (slot * a.G + hh) * D + 4 * lane);
                 acc.x += o.x * e; acc.y += o.y * e; acc.z += o.z * e; acc.w += o.w * e;
             }
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        const long long o = ((long long)b * a.H + (long long)g * a.G + hh) * D + d4;
-        store1(a.out, a.out_dtype, o + 0, acc.x * inv);
-        store1(a.out, a.out_dtype, o + 1, acc.y * inv);
-        store1(a.out, a.out_dtype, o + 2, acc.z * inv);
-        store1(a.out, a.out_dtype, o + 3, acc.w * inv);
+    }
+    if (has_dims) {
+        s_acc[warp][4 * lane + 0] = acc.x;
+        s_acc[warp][4 * lane + 1] = acc.y;
+        s_acc[warp][4 * lane + 2] = acc.z;
+        s_acc[warp][4 * lane + 3] = acc.w;
+    }
+    if (lane == 0) s_l[warp] = L;
+    __syncthreads();
+    float Lt = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) Lt += s_l[w];
+    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+    for (int i = tid; i < D; i += blockDim.x) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCombineWarps; ++w) v += s_acc[w][i];
+        store1(a.out, a.out_dtype, orow + i, v * inv);
     }
 }
 
@@ -921,9 +994,9 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     if (e != cudaSuccess) return GQA_ERR_CUDA;
     if (L.ev_end && cudaEventRecord(L.ev_end, L.stream) != cudaSuccess) return GQA_ERR_CUDA;
 
-    const int pairs = L.batch * K;
-    if (D == 64) combine_kernel<64><<<pairs, 128, 0, L.stream>>>(a);
-    else combine_kernel<128><<<pairs, 128, 0, L.stream>>>(a);
+    const int rows = L.batch * L.num_heads;
+    if (D == 64) combine_kernel<64><<<rows, kCombineWarps * 32, 0, L.stream>>>(a);
+    else combine_kernel<128><<<rows, kCombineWarps * 32, 0, L.stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     return GQA_OK;
 }
