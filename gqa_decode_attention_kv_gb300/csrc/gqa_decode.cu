@@ -67,8 +67,18 @@ struct DecodeArgs {
 #ifndef GQA_RING_BYTES_PER_WARP
 #define GQA_RING_BYTES_PER_WARP 16384
 #endif
+// Ring bytes of a CTA whose warps share one ring (groups of more than 8 heads).
+#ifndef GQA_SHARED_RING_BYTES
+#define GQA_SHARED_RING_BYTES 32768
+#endif
 
-template <int kKind, typename T, int D>
+constexpr int kHeadsPerWarp = 8;   // query heads one warp serves (the MMA N dimension)
+
+// kHeadWarps == 1: every warp is an independent split-KV worker with its own
+// ring and serves all (<= 8) heads of its group. kHeadWarps > 1: the CTA is one
+// worker; its kHeadWarps warps take 8 heads each of a larger group and share
+// one ring, so each K/V tile is still loaded once for the whole group.
+template <int kKind, typename T, int D, int kHeadWarps = 1>
 struct Cfg {
     static constexpr bool kI8 = std::is_same<T, int8_t>::value;
     static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -76,8 +86,11 @@ struct Cfg {
     static constexpr int kTile = 16 * D * kEs;                       // one (block, head) tile
     static constexpr int kScaleBytes = kI8 ? 64 : 0;                // 16 k + 16 v fp16 scales
     static constexpr int kStage = ((2 * kTile + kScaleBytes + 1023) / 1024) * 1024;
-    static constexpr int kStages = std::max(2, std::min(8, GQA_RING_BYTES_PER_WARP / kStage));
-    static constexpr int kWarps = GQA_WARPS_PER_CTA;
+    static constexpr int kNw = kHeadWarps;
+    static constexpr int kWarps = kHeadWarps == 1 ? GQA_WARPS_PER_CTA : kHeadWarps;
+    static constexpr int kRings = kHeadWarps == 1 ? kWarps : 1;
+    static constexpr int kStages =
+        std::max(2, std::min(8, (kHeadWarps == 1 ? GQA_RING_BYTES_PER_WARP : GQA_SHARED_RING_BYTES) / kStage));
     static constexpr bool kSwizzle = (kKind == kKernelMma);
     static constexpr int kBoxInner = kSwizzle ? 128 / kEs : D;        // elements per box row
     static constexpr int kNumBox = kSwizzle ? (D * kEs) / 128 : 1;
@@ -95,10 +108,11 @@ struct Cfg {
 // Dynamic shared memory layout shared by host and device.
 template <class C>
 struct Smem {
-    static constexpr int kRing = C::kWarps * C::kStages * C::kStage;
-    static constexpr int kBars = kRing;                                   // 8 B per stage
-    static constexpr int kBad = kBars + C::kWarps * C::kStages * 8;       // 4 B per stage
-    static constexpr int kScan = kBad + C::kWarps * C::kStages * 4;       // 64 ints
+    static constexpr int kRing = C::kRings * C::kStages * C::kStage;
+    static constexpr int kBars = kRing;                                   // "full", 8 B per stage
+    static constexpr int kEmpty = kBars + C::kRings * C::kStages * 8;     // "empty" (shared ring)
+    static constexpr int kBad = kEmpty + C::kStages * 8;                  // 4 B per stage
+    static constexpr int kScan = kBad + C::kRings * C::kStages * 4;       // 64 ints
     static constexpr int kLens = kScan + 64 * 4;                          // B ints, then B+1 prefix
     static int bytes(int B) { return 1024 + kLens + (2 * B + 1) * 4; }
 };
@@ -284,8 +298,9 @@ struct MmaFrags {
 //  bf16/f16: .x = dims 16t + 2c, +1;     .y = dims 16t + 2c + 8, +9  (standard layout)
 //  int8:     .x = dims 16t + 4c, +1;     .y = dims 16t + 4c + 2, +3  (matches the code quads)
 template <class C, int D>
-__device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int b, int g, int r, int c,
-                                             uint2 (&qf)[D / 16]) {
+__device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int b, int g, int hbase, int r,
+                                             int c, uint2 (&qf)[D / 16]) {
+    r += hbase;
     if (r >= a.G || b >= a.B) {
 #pragma unroll
         for (int i = 0; i < D / 16; ++i) qf[i] = make_uint2(0, 0);
@@ -488,7 +503,7 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
 // else a partial (o, m, l) into split slot (b*K + g) + warp.
 template <class C, int D>
 __device__ __forceinline__ void mma_flush(const DecodeArgs& a, MmaState<C, D>& st, int b, int g,
-                                          bool whole, int w, int r, int c) {
+                                          int hbase, bool whole, int w, int r, int c) {
     float l0 = st.l[0], l1 = st.l[1];
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
@@ -498,7 +513,7 @@ __device__ __forceinline__ void mma_flush(const DecodeArgs& a, MmaState<C, D>& s
     const long long slot = (long long)b * a.K + g + w;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-        const int hh = 2 * c + e;
+        const int hh = hbase + 2 * c + e;
         if (hh >= a.G) continue;
         const float lsum = e ? l1 : l0;
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
@@ -523,13 +538,13 @@ __device__ __forceinline__ void mma_flush(const DecodeArgs& a, MmaState<C, D>& s
 template <class C, int D>
 struct FmaState {
     static constexpr int kN = C::kDpl;
-    float m[kMaxGroup], l[kMaxGroup];
-    float acc[kMaxGroup][kN];
-    float q[kMaxGroup][kN];
+    float m[kHeadsPerWarp], l[kHeadsPerWarp];
+    float acc[kHeadsPerWarp][kN];
+    float q[kHeadsPerWarp][kN];
 
     __device__ __forceinline__ void reset() {
 #pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h) {
+        for (int h = 0; h < kHeadsPerWarp; ++h) {
             m[h] = -INFINITY;
             l[h] = 0.f;
 #pragma unroll
@@ -540,23 +555,24 @@ struct FmaState {
 
 template <class C, int D>
 __device__ __forceinline__ void fma_load_q(const DecodeArgs& a, FmaState<C, D>& st, int b, int g,
-                                           int lane) {
+                                           int hbase, int lane) {
 #pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h)
+    for (int h = 0; h < kHeadsPerWarp; ++h)
 #pragma unroll
         for (int i = 0; i < C::kDpl; ++i)
-            st.q[h][i] = (h < a.G) ? load_q_float(a.q, a.q_dtype,
-                                                  ((long long)b * a.H + (long long)g * a.G + h) * D + lane * C::kDpl + i)
-                                   : 0.f;
+            st.q[h][i] = (hbase + h < a.G && b < a.B)
+                             ? load_q_float(a.q, a.q_dtype,
+                                            ((long long)b * a.H + (long long)g * a.G + hbase + h) * D + lane * C::kDpl + i)
+                             : 0.f;
 }
 
 // One block, token by token: fp32 FMAs, butterfly reductions, per-token online softmax.
 template <class C, int D, typename T>
 __device__ __forceinline__ void fma_block(const DecodeArgs& a, FmaState<C, D>& st, uint32_t stage,
-                                          int nvalid, int lane) {
+                                          int nvalid, int hbase, int lane) {
     constexpr int kN = C::kDpl;
     const uint32_t sk = stage, sv = stage + C::kTile;
-    const int G = a.G;
+    const int G = a.G - hbase;                   // heads of this warp: hbase .. hbase+7
     for (int t = 0; t < nvalid; ++t) {
         float kf[kN], vf[kN];
         lds_row_as_float<T, kN>(sk + t * D * C::kEs + lane * kN * C::kEs, kf);
@@ -570,7 +586,7 @@ __device__ __forceinline__ void fma_block(const DecodeArgs& a, FmaState<C, D>& s
             vsc = __half2float(__ushort_as_half(hv));
         }
 #pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h) {
+        for (int h = 0; h < kHeadsPerWarp; ++h) {
             if (h >= G) break;
             float dot = 0.f;
 #pragma unroll
@@ -592,30 +608,32 @@ __device__ __forceinline__ void fma_block(const DecodeArgs& a, FmaState<C, D>& s
 
 template <class C, int D>
 __device__ __forceinline__ void fma_flush(const DecodeArgs& a, FmaState<C, D>& st, int b, int g,
-                                          bool whole, int w, int lane) {
+                                          int hbase, bool whole, int w, int lane) {
     const long long slot = (long long)b * a.K + g + w;
 #pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h) {
-        if (h >= a.G) break;
+    for (int h = 0; h < kHeadsPerWarp; ++h) {
+        const int hh = hbase + h;
+        if (hh >= a.G) break;
         const float inv = st.l[h] > 0.f ? 1.f / st.l[h] : 0.f;
 #pragma unroll
         for (int i = 0; i < C::kDpl; ++i) {
             const int dim = lane * C::kDpl + i;
-            if (whole) store1(a.out, a.out_dtype, ((long long)b * a.H + (long long)g * a.G + h) * D + dim, st.acc[h][i] * inv);
-            else a.ws_o[(slot * a.G + h) * D + dim] = st.acc[h][i];
+            if (whole) store1(a.out, a.out_dtype, ((long long)b * a.H + (long long)g * a.G + hh) * D + dim, st.acc[h][i] * inv);
+            else a.ws_o[(slot * a.G + hh) * D + dim] = st.acc[h][i];
         }
-        if (!whole && lane == 0) a.ws_ml[slot * a.G + h] = make_float2(st.m[h], st.l[h]);
+        if (!whole && lane == 0) a.ws_ml[slot * a.G + hh] = make_float2(st.m[h], st.l[h]);
     }
 }
 
 // ------------------------------------------------------------------ the split-KV kernel
 
-template <int kKind, typename T, int D>
-__global__ void __launch_bounds__(Cfg<kKind, T, D>::kWarps * 32)
+template <int kKind, typename T, int D, int kHeadWarps>
+__global__ void __launch_bounds__(Cfg<kKind, T, D, kHeadWarps>::kWarps * 32)
 split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const DecodeArgs a) {
-    using C = Cfg<kKind, T, D>;
+    using C = Cfg<kKind, T, D, kHeadWarps>;
     using S = Smem<C>;
+    constexpr bool kShared = kHeadWarps > 1;     // one ring, one worker per CTA
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -640,24 +658,39 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     }
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int w = blockIdx.x * C::kWarps + warp;
+    const int w = kShared ? (int)blockIdx.x : (int)blockIdx.x * C::kWarps + warp;   // worker
+    const int hbase = kShared ? warp * kHeadsPerWarp : 0;
     const long long ub = (long long)w * R;
-    if (ub >= U) return;                       // no CTA-wide barrier follows
+    if (ub >= U) return;                       // uniform per worker; no CTA barrier follows
     const int u_begin = (int)ub;
     const int u_end = (int)min((long long)U, ub + R);
     const int n_units = u_end - u_begin;
 
-    const uint32_t ring = sbase + warp * C::kStages * C::kStage;
-    const uint32_t bar0 = sbase + S::kBars + warp * C::kStages * 8;
-    volatile int* bad = reinterpret_cast<volatile int*>(gbase + S::kBad) + warp * C::kStages;
-    if (lane == 0) {
-        for (int s = 0; s < C::kStages; ++s) mbar_init(bar0 + 8 * s, 1);
-        fence_mbar_init();
+    const int ring_id = kShared ? 0 : warp;
+    const uint32_t ring = sbase + ring_id * C::kStages * C::kStage;
+    const uint32_t bar0 = sbase + S::kBars + ring_id * C::kStages * 8;
+    const uint32_t ebar0 = sbase + S::kEmpty;
+    volatile int* bad = reinterpret_cast<volatile int*>(gbase + S::kBad) + ring_id * C::kStages;
+    const bool producer = !kShared || warp == 0;  // the warp that issues this ring's copies
+    if (kShared) {
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < C::kStages; ++s) {
+                mbar_init(bar0 + 8 * s, 1);
+                mbar_init(ebar0 + 8 * s, kHeadWarps);
+            }
+            fence_mbar_init();
+        }
+        __syncthreads();                       // every warp of this CTA reached here (same worker)
+    } else {
+        if (lane == 0) {
+            for (int s = 0; s < C::kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+            fence_mbar_init();
+        }
+        __syncwarp();
     }
-    __syncwarp();
     const uint64_t pol = l2_policy_evict_first();
 
-    // Window of physical blocks: lane l holds unit win_base + l.
+    // Window of physical blocks (producer warp): lane l holds unit win_base + l.
     int win_base = -(1 << 30), win_phys = -1, win_g = 0;
     auto refill = [&](int base) {
         win_base = base;
@@ -703,9 +736,33 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             }
         }
     };
+    // Bounded waits whose verdict is warp-uniform, so a timeout never splits a warp.
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(kFull, mbar_wait(bar, parity));
+    };
+    auto bail = [&](int i) {
+        // A copy (or a peer warp) did not arrive in time: report, let this ring's
+        // in-flight copies land, leave.
+        if (lane == 0) flag_error(a.err, GQA_DEVERR_TIMEOUT);
+        if (producer)
+            for (int k = i; k < min(n_units, i + (int)C::kStages); ++k)
+                mbar_wait(bar0 + 8 * (k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimitNs / 4);
+    };
+    // Hand slot s (just read) back; the producer refills it with unit i + kStages.
+    auto release_and_refill = [&](int i, int s) -> bool {
+        __syncwarp();
+        if (kShared && lane == 0) mbar_arrive(ebar0 + 8 * s);
+        if (producer && i + C::kStages < n_units) {
+            if (kShared && !wait_all(ebar0 + 8 * s, (uint32_t)(i / C::kStages) & 1u)) return false;
+            issue(u_begin + i + C::kStages, s);
+        }
+        return true;
+    };
 
-    const int npro = min((int)C::kStages, n_units);
-    for (int s = 0; s < npro; ++s) issue(u_begin + s, s);
+    if (producer) {
+        const int npro = min((int)C::kStages, n_units);
+        for (int s = 0; s < npro; ++s) issue(u_begin + s, s);
+    }
 
     // Compute-side cursor.
     int cb, cg, cj;
@@ -722,24 +779,18 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     int nb_b = cb, nb_g = cg;                   // next pair (for the q prefetch)
     next_pair(pref, a.B, a.K, nb_b, nb_g);
     if constexpr (kKind == kKernelMma) {
-        load_q_frags<C, D>(a, cb, cg, r, c, st.qf);
-        if (cu_pair + cnb < u_end) load_q_frags<C, D>(a, nb_b, nb_g, r, c, st.qn);
+        load_q_frags<C, D>(a, cb, cg, hbase, r, c, st.qf);
+        if (cu_pair + cnb < u_end) load_q_frags<C, D>(a, nb_b, nb_g, hbase, r, c, st.qn);
     } else {
-        fma_load_q<C, D>(a, st, cb, cg, lane);
+        fma_load_q<C, D>(a, st, cb, cg, hbase, lane);
     }
 
     for (int i = 0; i < n_units; ++i) {
         const int s = i % C::kStages;
         const uint32_t parity = (uint32_t)(i / C::kStages) & 1u;
-        // every lane observes the phase (acquiring the TMA writes); the verdict is
-        // made warp-uniform so a timeout can never split the warp
-        if (!__all_sync(kFull, mbar_wait(bar0 + 8 * s, parity))) {
-            // A copy did not land in time: report, let in-flight copies finish, leave.
-            if (lane == 0) flag_error(a.err, GQA_DEVERR_TIMEOUT);
-            for (int k = i; k < min(n_units, i + (int)C::kStages); ++k) {
-                const int s2 = k % C::kStages;
-                mbar_wait(bar0 + 8 * s2, (uint32_t)(k / C::kStages) & 1u, kWaitLimitNs / 4);
-            }
+        // every lane observes the phase, which acquires the TMA writes
+        if (!wait_all(bar0 + 8 * s, parity)) {
+            bail(i);
             return;
         }
         const int nvalid = min((int)kBlock, clen - kBlock * cj);
@@ -748,20 +799,24 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             // read the whole slot, hand it back to TMA, then compute from registers
             MmaFrags<C, D> fr;
             if (unit_ok) mma_load<C, D>(fr, ring + s * C::kStage, lane, r, c);
-            __syncwarp();
-            if (i + C::kStages < n_units) issue(u_begin + i + C::kStages, s);
+            if (!release_and_refill(i, s)) {
+                bail(i + 1);
+                return;
+            }
             if (unit_ok) mma_compute<C, D>(st, fr, nvalid, r, c, a.scale_log2);
         } else {
-            if (unit_ok) fma_block<C, D, T>(a, st, ring + s * C::kStage, nvalid, lane);
-            __syncwarp();
-            if (i + C::kStages < n_units) issue(u_begin + i + C::kStages, s);
+            if (unit_ok) fma_block<C, D, T>(a, st, ring + s * C::kStage, nvalid, hbase, lane);
+            if (!release_and_refill(i, s)) {
+                bail(i + 1);
+                return;
+            }
         }
 
         const bool last_of_pair = (cj == cnb - 1);
         if (last_of_pair || i == n_units - 1) {
             const bool whole = (first_j == 0) && last_of_pair;
-            if constexpr (kKind == kKernelMma) mma_flush<C, D>(a, st, cb, cg, whole, w, r, c);
-            else fma_flush<C, D>(a, st, cb, cg, whole, w, lane);
+            if constexpr (kKind == kKernelMma) mma_flush<C, D>(a, st, cb, cg, hbase, whole, w, r, c);
+            else fma_flush<C, D>(a, st, cb, cg, hbase, whole, w, lane);
             if (i == n_units - 1) break;
             cb = nb_b;
             cg = nb_g;
@@ -775,9 +830,9 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             if constexpr (kKind == kKernelMma) {
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) st.qf[k] = st.qn[k];
-                if (cu_pair + cnb < u_end) load_q_frags<C, D>(a, nb_b, nb_g, r, c, st.qn);
+                if (cu_pair + cnb < u_end) load_q_frags<C, D>(a, nb_b, nb_g, hbase, r, c, st.qn);
             } else {
-                fma_load_q<C, D>(a, st, cb, cg, lane);
+                fma_load_q<C, D>(a, st, cb, cg, hbase, lane);
             }
         } else {
             ++cj;
@@ -866,37 +921,53 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
 
 struct Variant {
     const void* fn;
-    int warps;
+    int warps;           // threads / 32
+    int workers_per_cta; // split-KV workers per CTA
     int box_inner;       // elements per TMA box row
     bool swizzle;
     int (*smem)(int);
 };
 
-template <int kKind, typename T, int D>
+template <int kKind, typename T, int D, int NW>
 Variant make_variant() {
-    using C = Cfg<kKind, T, D>;
-    return Variant{reinterpret_cast<const void*>(&split_kv_kernel<kKind, T, D>), C::kWarps,
-                   C::kBoxInner, C::kSwizzle, &Smem<C>::bytes};
+    using C = Cfg<kKind, T, D, NW>;
+    return Variant{reinterpret_cast<const void*>(&split_kv_kernel<kKind, T, D, NW>), C::kWarps,
+                   NW == 1 ? C::kWarps : 1, C::kBoxInner, C::kSwizzle, &Smem<C>::bytes};
+}
+
+template <int kKind, typename T, int D>
+Variant pick_width(int nw) {
+    if (nw == 1) return make_variant<kKind, T, D, 1>();
+    if (nw == 2) return make_variant<kKind, T, D, 2>();
+    if (nw == 4) return make_variant<kKind, T, D, 4>();
+    return make_variant<kKind, T, D, 8>();
 }
 
 template <typename T, int D>
-bool pick_kind(int kind, Variant& v) {
+bool pick_kind(int kind, int nw, Variant& v) {
     if (kind == kKernelMma) {
         if constexpr (std::is_same<T, float>::value || (std::is_same<T, int8_t>::value && D != 128)) {
             return false;
         } else {
-            v = make_variant<kKernelMma, T, D>();
+            v = pick_width<kKernelMma, T, D>(nw);
             return true;
         }
     }
-    v = make_variant<kKernelFma, T, D>();
-    return true;
+    if constexpr (std::is_same<T, float>::value) {
+        v = pick_width<kKernelFma, T, D>(nw);
+        return true;
+    } else {
+        // the CUDA-core kernel serves fp32 caches, and <= 8-head groups of the others
+        if (nw > 1) return false;
+        v = make_variant<kKernelFma, T, D, 1>();
+        return true;
+    }
 }
 
 template <typename T>
-bool pick_dim(int kind, int d, Variant& v) {
-    if (d == 64) return pick_kind<T, 64>(kind, v);
-    if (d == 128) return pick_kind<T, 128>(kind, v);
+bool pick_dim(int kind, int d, int nw, Variant& v) {
+    if (d == 64) return pick_kind<T, 64>(kind, nw, v);
+    if (d == 128) return pick_kind<T, 128>(kind, nw, v);
     return false;
 }
 
@@ -918,9 +989,13 @@ WsLayout ws_layout(int B, int K, int G, int D, long long slots) {
 
 }  // namespace
 
+// Workers of one wave are at most 64 warps per SM, divided by the warps that
+// share a group's tiles; every (pair, worker) overlap is one split slot.
 size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int head_dim, int num_sms) {
-    const long long slots = (long long)batch * num_kv_heads + (long long)num_sms * kMaxWarpsPerSm;
-    return ws_layout(batch, num_kv_heads, num_heads / num_kv_heads, head_dim, slots).total;
+    const int G = num_heads / num_kv_heads;
+    const int nw = G <= 8 ? 1 : G <= 16 ? 2 : G <= 32 ? 4 : 8;
+    const long long slots = (long long)batch * num_kv_heads + (long long)num_sms * (kMaxWarpsPerSm / nw);
+    return ws_layout(batch, num_kv_heads, G, head_dim, slots).total;
 }
 
 int launch_decode(const DecodeLaunch& L, int num_sms) {
@@ -928,13 +1003,14 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     const int D = c.head_dim, K = c.num_kv_heads, G = L.num_heads / K;
     int kind = L.kernel;
     if (kind == 0) kind = (c.dtype == GQA_DTYPE_F32 || (c.dtype == GQA_DTYPE_I8 && D != 128)) ? kKernelFma : kKernelMma;
+    const int nw = G <= 8 ? 1 : G <= 16 ? 2 : G <= 32 ? 4 : 8;   // warps sharing one group's tiles
     Variant v{};
     bool ok = false;
     switch (c.dtype) {
-        case GQA_DTYPE_F32: ok = pick_dim<float>(kind, D, v); break;
-        case GQA_DTYPE_F16: ok = pick_dim<__half>(kind, D, v); break;
-        case GQA_DTYPE_BF16: ok = pick_dim<__nv_bfloat16>(kind, D, v); break;
-        case GQA_DTYPE_I8: ok = pick_dim<int8_t>(kind, D, v); break;
+        case GQA_DTYPE_F32: ok = pick_dim<float>(kind, D, nw, v); break;
+        case GQA_DTYPE_F16: ok = pick_dim<__half>(kind, D, nw, v); break;
+        case GQA_DTYPE_BF16: ok = pick_dim<__nv_bfloat16>(kind, D, nw, v); break;
+        case GQA_DTYPE_I8: ok = pick_dim<int8_t>(kind, D, nw, v); break;
         default: ok = false;
     }
     if (!ok) return GQA_ERR_UNSUPPORTED;
@@ -953,8 +1029,9 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     if (e != cudaSuccess) return GQA_ERR_CUDA;
     if (per_sm < 1) return GQA_ERR_UNSUPPORTED;
     int grid = num_sms * per_sm;
-    if (L.max_warps > 0) grid = std::min(grid, std::max(1, (L.max_warps + v.warps - 1) / v.warps));
-    const int P = grid * v.warps;
+    if (L.max_warps > 0)
+        grid = std::min(grid, std::max(1, (L.max_warps + v.workers_per_cta - 1) / v.workers_per_cta));
+    const int P = grid * v.workers_per_cta;   // split-KV workers (KV splits per pass)
 
     const long long slots = (long long)L.batch * K + P;
     const WsLayout wl = ws_layout(L.batch, K, G, D, slots);

@@ -27,7 +27,7 @@ constexpr int kWsHeaderInts = 64;
 // Upper bound on decode warps per SM used for sizing the workspace.
 constexpr int kMaxWarpsPerSm = 64;
 constexpr int kMaxBatch = 8191;
-constexpr int kMaxGroup = 8;
+constexpr int kMaxGroup = 64;   // query heads per KV head the kernels serve
 
 cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const void* v_new,
                              int new_dtype, const int32_t* block_tables, int max_blocks,

@@ -103,7 +103,7 @@ typedef struct {
 /* Optional knobs of gqa_decode (pass NULL for the defaults). */
 typedef struct {
     int32_t kernel;               /* 0 auto, 1 tensor-core (mma.sync) kernel, 2 CUDA-core kernel */
-    int32_t max_warps;            /* 0 = fill the GPU; > 0 caps the decode warps, i.e. KV splits */
+    int32_t max_warps;            /* 0 = fill the GPU; > 0 caps the split-KV workers, i.e. KV splits */
     int32_t min_blocks_per_warp;  /* 0 = default (4): smallest KV range one warp takes */
     void   *event_main_begin;     /* optional cudaEvent_t recorded just before the split-KV kernel */
     void   *event_main_end;       /* optional cudaEvent_t recorded just after it */
@@ -182,7 +182,8 @@ GQA_API size_t gqa_decode_workspace_size(int32_t batch, int32_t num_heads, int32
  *  workspace      device, >= gqa_decode_workspace_size(...) bytes, 256-byte
  *                 aligned; contents need no initialisation and are clobbered.
  *  opts           NULL or tuning knobs (gqa_decode_opts_t).
- *  Limits: num_heads % K == 0; num_heads / K <= 8; batch <= 8191;
+ *  Limits: num_heads % K == 0; num_heads / K <= 64 (groups above 8 need a
+ *  BF16/F16/I8 cache with head_dim 128 for I8, or an F32 cache); batch <= 8191;
  *  batch * K * max_blocks_per_seq < 2^31.
  */
 GQA_API int gqa_decode(const gqa_kv_cache_t *cache, const void *q, int32_t q_dtype,

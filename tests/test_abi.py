@@ -89,7 +89,7 @@ def test_cache_description_checks(lib, kw, expect):
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(H=30), INVALID),                           # H not a multiple of K
-    (dict(H=8 * 16), UNSUPPORTED),                   # G = 16 > 8
+    (dict(H=8 * 128), UNSUPPORTED),                  # G = 128 > 64
     (dict(B=9000), UNSUPPORTED),
     (dict(q=0x30004), INVALID),
     (dict(ws=0x70010), INVALID),                     # workspace not 256-byte aligned

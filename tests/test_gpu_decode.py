@@ -49,6 +49,19 @@ def test_tiny_fp32_contiguous_workload(gq):
     ("bf16", 128, 8, 8), ("bf16", 128, 16, 8), ("f16", 64, 8, 1),
 ])
 def test_ragged_multi_tile(gq, kernel, dtype, d, H, K):
+    _ragged(gq, kernel, dtype, d, H, K)
+
+
+@pytest.mark.parametrize("dtype,d,H,K,kernel", [
+    ("bf16", 128, 64, 4, 1), ("bf16", 128, 48, 4, 1), ("bf16", 128, 64, 2, 1),
+    ("bf16", 128, 64, 1, 1), ("f16", 64, 32, 1, 1), ("f32", 64, 64, 1, 2), ("f32", 128, 16, 1, 2),
+])
+def test_groups_larger_than_one_warp(gq, dtype, d, H, K, kernel):
+    """G = 16, 12, 32, 64: the CTA's warps split the heads and share one ring."""
+    _ragged(gq, kernel, dtype, d, H, K)
+
+
+def _ragged(gq, kernel, dtype, d, H, K):
     lens = [1, 15, 16, 17, 33, 200, 511, 0, 1000]
     case = gi.make_case(len(lens), H, K, d, lens, dtype, seed=21, device="cuda")
     ref = oracle_for_case(case)
@@ -56,6 +69,14 @@ def test_ragged_multi_tile(gq, kernel, dtype, d, H, K):
         out = _run(gq, case, kernel=kernel, max_warps=mw, min_blocks_per_warp=1)
         err = max_abs_err(out, ref)
         assert err <= TOL, (mw, err)
+
+
+def test_int8_wide_group(gq):
+    lens = [1, 16, 17, 300, 2047, 0, 64]
+    case = gi.make_case(len(lens), 64, 2, 128, lens, "i8", q_dtype="bf16", seed=35, device="cuda")
+    ref = oracle_for_case(case)
+    for mw in (0, 3):
+        assert max_abs_err(_run(gq, case, max_warps=mw, min_blocks_per_warp=1), ref) <= TOL
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -255,9 +276,9 @@ def test_full_size_long_context_b4_sampled(gq):
     assert _sampled(gq, gi.WORKLOADS["long_ctx_bf16_b4_s131072"], [3]) <= TOL
 
 
-@pytest.mark.parametrize("kv_heads", [64, 32, 16, 8])
+@pytest.mark.parametrize("kv_heads", [64, 32, 16, 8, 1])
 def test_kv_head_sweep_sampled(gq, kv_heads):
-    """H=64 with K from MHA (G=1) to G=8 on the 70B-shaped ragged lengths
+    """H=64 with K from MHA (G=1) to MQA (G=64) on the 70B-shaped ragged lengths
     (first 6 sequences, so the MHA point stays a few GB)."""
     import dataclasses
     wl = dataclasses.replace(gi.kv_sweep_workload(kv_heads), batch=6)
