@@ -45,6 +45,8 @@ __device__ __forceinline__ long long dest_offset(const AppendArgs& a, int b, int
 
 // Bit-exact copy for f32/f16/bf16 caches, 16 bytes per lane step.
 __global__ void __launch_bounds__(kWarpsPerCta * 32) append_copy_kernel(const AppendArgs a) {
+    grid_dependency_wait();
+    launch_dependents();
     const int lane = threadIdx.x & 31;
     const long long pair = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
     if (pair >= (long long)a.batch * a.K) return;
@@ -116,6 +118,8 @@ __device__ __forceinline__ void quantise_row(const void* src, long long src_off,
 
 template <typename In, int EPL>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) append_quant_kernel(const AppendArgs a) {
+    grid_dependency_wait();
+    launch_dependents();
     const int lane = threadIdx.x & 31;
     const long long pair = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
     if (pair >= (long long)a.batch * a.K) return;
@@ -128,13 +132,6 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) append_quant_kernel(const A
     const long long src = ((long long)b * a.K + g) * a.d;
     quantise_row<In, EPL>(a.k_new, src, static_cast<int8_t*>(a.k_cache) + off, a.k_scale + sidx, lane);
     quantise_row<In, EPL>(a.v_new, src, static_cast<int8_t*>(a.v_cache) + off, a.v_scale + sidx, lane);
-}
-
-template <typename In>
-cudaError_t launch_quant(const AppendArgs& a, int grid, cudaStream_t s) {
-    if (a.d == 64) append_quant_kernel<In, 2><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
-    else append_quant_kernel<In, 4><<<grid, kWarpsPerCta * 32, 0, s>>>(a);
-    return cudaGetLastError();
 }
 
 }  // namespace
@@ -165,15 +162,37 @@ cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const v
     const long long warps = (long long)batch * c.num_kv_heads;
     const int grid = (int)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
     if (grid == 0) return cudaSuccess;
+    const void* fn;
     if (c.dtype != GQA_DTYPE_I8) {
-        append_copy_kernel<<<grid, kWarpsPerCta * 32, 0, stream>>>(a);
-        return cudaGetLastError();
+        fn = reinterpret_cast<const void*>(&append_copy_kernel);
+    } else {
+        const bool d64 = a.d == 64;
+        switch (new_dtype) {
+            case GQA_DTYPE_F32:
+                fn = d64 ? reinterpret_cast<const void*>(&append_quant_kernel<float, 2>)
+                         : reinterpret_cast<const void*>(&append_quant_kernel<float, 4>);
+                break;
+            case GQA_DTYPE_F16:
+                fn = d64 ? reinterpret_cast<const void*>(&append_quant_kernel<__half, 2>)
+                         : reinterpret_cast<const void*>(&append_quant_kernel<__half, 4>);
+                break;
+            default:
+                fn = d64 ? reinterpret_cast<const void*>(&append_quant_kernel<__nv_bfloat16, 2>)
+                         : reinterpret_cast<const void*>(&append_quant_kernel<__nv_bfloat16, 4>);
+        }
     }
-    switch (new_dtype) {
-        case GQA_DTYPE_F32: return launch_quant<float>(a, grid, stream);
-        case GQA_DTYPE_F16: return launch_quant<__half>(a, grid, stream);
-        default: return launch_quant<__nv_bfloat16>(a, grid, stream);
-    }
+    // programmatic serialisation: the kernel waits on the device for its predecessor
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kWarpsPerCta * 32);
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    void* args[] = {&a};
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace gqa

@@ -646,6 +646,8 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
     }
+    launch_dependents();                       // the combine kernel may take its place now
+    grid_dependency_wait();                    // inputs may come from the previous kernel
     block_prefix(a, lens_s, pref, tmp);
     const int U = a.K * pref[a.B];
     const int R = max((U + a.P - 1) / max(a.P, 1), a.min_units);
@@ -854,6 +856,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
     __shared__ float s_l[kCombineWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int bh = blockIdx.x;
+    launch_dependents();
+    grid_dependency_wait();                    // the split-KV kernel's partials
     const int b = bh / a.H, h = bh % a.H, g = h / a.G, hh = h % a.G;
     const long long orow = (long long)bh * D;
     const int p0 = a.ws_pref[b];
@@ -1065,16 +1069,37 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     a.min_units = L.min_blocks_per_warp > 0 ? L.min_blocks_per_warp : 4;
     a.scale_log2 = L.scale * kLog2e;
 
+    // Both kernels go out with programmatic stream serialisation: each may be
+    // scheduled while its predecessor drains and waits on the device
+    // (griddepcontrol.wait) before it reads any input. Timing events split the
+    // chain, so with events the launches are plain.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    const bool timed = L.ev_begin || L.ev_end;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(v.warps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = L.stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = timed ? 0 : 1;
     if (L.ev_begin && cudaEventRecord(L.ev_begin, L.stream) != cudaSuccess) return GQA_ERR_CUDA;
     void* args[] = {&kmap, &vmap, &a};
-    e = cudaLaunchKernel(v.fn, dim3(grid), dim3(v.warps * 32), args, smem, L.stream);
+    e = cudaLaunchKernelExC(&cfg, v.fn, args);
     if (e != cudaSuccess) return GQA_ERR_CUDA;
     if (L.ev_end && cudaEventRecord(L.ev_end, L.stream) != cudaSuccess) return GQA_ERR_CUDA;
 
-    const int rows = L.batch * L.num_heads;
-    if (D == 64) combine_kernel<64><<<rows, kCombineWarps * 32, 0, L.stream>>>(a);
-    else combine_kernel<128><<<rows, kCombineWarps * 32, 0, L.stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    cudaLaunchConfig_t ccfg = {};
+    ccfg.gridDim = dim3(L.batch * L.num_heads);
+    ccfg.blockDim = dim3(kCombineWarps * 32);
+    ccfg.stream = L.stream;
+    ccfg.attrs = pdl;
+    ccfg.numAttrs = timed ? 0 : 1;
+    const void* cfn = D == 64 ? reinterpret_cast<const void*>(&combine_kernel<64>)
+                              : reinterpret_cast<const void*>(&combine_kernel<128>);
+    void* cargs[] = {&a};
+    if (cudaLaunchKernelExC(&ccfg, cfn, cargs) != cudaSuccess) return GQA_ERR_CUDA;
     return GQA_OK;
 }
 

@@ -35,6 +35,20 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Wait until the grid this one depends on (previous kernel in the stream) has
+// completed and its memory is visible. A no-op without programmatic launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel in the stream be scheduled now (it still waits for this
+// grid's completion before it reads anything).
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
