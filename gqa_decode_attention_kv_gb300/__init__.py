@@ -195,7 +195,7 @@ _ws_cache: dict = {}
 
 def workspace_for(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
                   device: torch.device) -> torch.Tensor:
-    """A cached device workspace large enough for this shape (grown on demand)."""
+    """A cached, zero-initialised device workspace large enough for this shape."""
     dev = torch.device(device)
     idx = dev.index if dev.index is not None else torch.cuda.current_device()
     need = decode_workspace_size(batch, num_heads, num_kv_heads, head_dim, idx)
@@ -203,7 +203,8 @@ def workspace_for(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
         raise ValueError("no workspace size for this shape")
     buf = _ws_cache.get(idx)
     if buf is None or buf.numel() < need:
-        buf = torch.empty(need, dtype=torch.uint8, device=dev)
+        # zero-filled once: the library keeps its run-time work counter at zero between calls
+        buf = torch.zeros(need, dtype=torch.uint8, device=dev)
         _ws_cache[idx] = buf
     return buf
 

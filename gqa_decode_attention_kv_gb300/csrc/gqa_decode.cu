@@ -49,13 +49,15 @@ struct DecodeArgs {
     const int32_t* context_lens;
     void* out;
     int32_t* err;
-    int32_t* ws_hdr;     // [0] units per warp R, [1] total units U
+    int32_t* ws_hdr;     // the Partition: [0] R, [1] U, [2] Rs, [3] Cz, [4] P, [5] cpw
+    unsigned long long* ws_ctr;   // next dynamic chunk; zero between calls
     int32_t* ws_pref;    // [B+1] exclusive prefix of blocks per sequence
     float2* ws_ml;       // [slots][G] (running max m in log2 units, running sum l)
     float* ws_o;         // [slots][G][D] un-normalised partial outputs
     long long num_blocks;
     int B, H, K, G, max_blocks, out_dtype, q_dtype, P, min_units;
     int map_perm[3];     // tensor-map dims 1..3 -> 0 slot, 1 kv-head, 2 block
+    int max_tail_chunks; // pooled chunks per worker range (0 = static partition only)
     float scale_log2;    // scale * log2(e)
 };
 
@@ -67,10 +69,23 @@ struct DecodeArgs {
 #ifndef GQA_RING_BYTES_PER_WARP
 #define GQA_RING_BYTES_PER_WARP 16384
 #endif
+// CTAs per SM the narrow int8 tensor-core kernel is compiled to fit (registers).
+#ifndef GQA_MIN_CTAS_PER_SM_I8
+#define GQA_MIN_CTAS_PER_SM_I8 3
+#endif
 // Ring bytes of a CTA whose warps share one ring (groups of more than 8 heads).
 #ifndef GQA_SHARED_RING_BYTES
 #define GQA_SHARED_RING_BYTES 32768
 #endif
+
+// Tail balancing: about 1/8 of every worker's range, in at most kMaxTailChunks
+// chunks of at least kMinChunk blocks, is pooled and taken at run time by
+// whichever worker finishes its own part first.
+#ifndef GQA_MAX_TAIL_CHUNKS
+#define GQA_MAX_TAIL_CHUNKS 4
+#endif
+constexpr int kMaxTailChunks = GQA_MAX_TAIL_CHUNKS;
+constexpr int kMinChunk = 4;
 
 constexpr int kHeadsPerWarp = 8;   // query heads one warp serves (the MMA N dimension)
 
@@ -87,6 +102,14 @@ struct Cfg {
     static constexpr int kScaleBytes = kI8 ? 64 : 0;                // 16 k + 16 v fp16 scales
     static constexpr int kStage = ((2 * kTile + kScaleBytes + 1023) / 1024) * 1024;
     static constexpr int kNw = kHeadWarps;
+    // The int8 kernel is issue-bound: the pool's bookkeeping costs it more than
+    // the tail it removes (measured), so it keeps the static partition.
+    static constexpr int kTailChunks = kI8 ? 0 : kMaxTailChunks;
+    // CTAs per SM the register budget is cut for. The int8 kernel is bound by
+    // issue and latency and gains from 12 warps per SM; the bf16/f16 kernels
+    // would spill at that budget and keep 8 (both measured).
+    static constexpr int kMinCtas =
+        (kHeadWarps == 1 && kKind == kKernelMma && D == 128) ? (kI8 ? GQA_MIN_CTAS_PER_SM_I8 : 2) : 1;
     static constexpr int kWarps = kHeadWarps == 1 ? GQA_WARPS_PER_CTA : kHeadWarps;
     static constexpr int kRings = kHeadWarps == 1 ? kWarps : 1;
     static constexpr int kStages =
@@ -111,8 +134,8 @@ struct Smem {
     static constexpr int kRing = C::kRings * C::kStages * C::kStage;
     static constexpr int kBars = kRing;                                   // "full", 8 B per stage
     static constexpr int kEmpty = kBars + C::kRings * C::kStages * 8;     // "empty" (shared ring)
-    static constexpr int kBad = kEmpty + C::kStages * 8;                  // 4 B per stage
-    static constexpr int kScan = kBad + C::kRings * C::kStages * 4;       // 64 ints
+    static constexpr int kMeta = kEmpty + C::kStages * 8;                 // 4 ints per stage
+    static constexpr int kScan = kMeta + C::kRings * C::kStages * 16;     // 64 ints
     static constexpr int kLens = kScan + 64 * 4;                          // B ints, then B+1 prefix
     static int bytes(int B) { return 1024 + kLens + (2 * B + 1) * 4; }
 };
@@ -627,8 +650,37 @@ __device__ __forceinline__ void fma_flush(const DecodeArgs& a, FmaState<C, D>& s
 
 // ------------------------------------------------------------------ the split-KV kernel
 
+// Slot metadata the producer writes before a slot's barrier completes.
+enum SlotKind : int { kSlotData = 0, kSlotSkip = 1, kSlotEnd = 2 };
+
+// The partition of the U units, identical on every CTA and in the combine.
+// Worker w's range is [w*R, min(U, (w+1)*R)); its first Rs units are its own
+// (static segment), the remaining cpw chunks of Cz units go to a pool. Segment
+// index of worker w's static part is w*(1+cpw), of its chunk i w*(1+cpw)+1+i:
+// indices grow with unit position, so a split slot (b*K + g) + segment is unique
+// and every pair's pieces are the consecutive segments that cover it.
+struct Partition {
+    int U, R, Rs, Cz, cpw, P;
+    __device__ __forceinline__ int segment_of(int u) const {
+        const int w = u / R, off = u - w * R;
+        return w * (1 + cpw) + (off < Rs ? 0 : 1 + (off - Rs) / Cz);
+    }
+};
+
+__device__ __forceinline__ Partition make_partition(const DecodeArgs& a, int U) {
+    Partition pt;
+    pt.U = U;
+    pt.P = max(a.P, 1);
+    pt.R = max((U + pt.P - 1) / pt.P, a.min_units);
+    pt.Cz = max(kMinChunk, (pt.R + 31) / 32);
+    pt.cpw = min(a.max_tail_chunks, pt.R / (8 * pt.Cz));
+    pt.Rs = pt.R - pt.cpw * pt.Cz;
+    return pt;
+}
+
 template <int kKind, typename T, int D, int kHeadWarps>
-__global__ void __launch_bounds__(Cfg<kKind, T, D, kHeadWarps>::kWarps * 32)
+__global__ void __launch_bounds__(Cfg<kKind, T, D, kHeadWarps>::kWarps * 32,
+                                  Cfg<kKind, T, D, kHeadWarps>::kMinCtas)
 split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const DecodeArgs a) {
     using C = Cfg<kKind, T, D, kHeadWarps>;
@@ -649,30 +701,33 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     launch_dependents();                       // the combine kernel may take its place now
     grid_dependency_wait();                    // inputs may come from the previous kernel
     block_prefix(a, lens_s, pref, tmp);
-    const int U = a.K * pref[a.B];
-    const int R = max((U + a.P - 1) / max(a.P, 1), a.min_units);
+    const Partition pt = make_partition(a, a.K * pref[a.B]);
     if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i <= a.B; i += blockDim.x) a.ws_pref[i] = pref[i];
         if (threadIdx.x == 0) {
-            a.ws_hdr[0] = R;
-            a.ws_hdr[1] = U;
+            a.ws_hdr[0] = pt.R;
+            a.ws_hdr[1] = pt.U;
+            a.ws_hdr[2] = pt.Rs;
+            a.ws_hdr[3] = pt.Cz;
+            a.ws_hdr[4] = pt.P;
+            a.ws_hdr[5] = pt.cpw;
         }
     }
+    if (pt.U == 0) return;                     // uniform: every row is empty (combine zeroes them)
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int w = kShared ? (int)blockIdx.x : (int)blockIdx.x * C::kWarps + warp;   // worker
     const int hbase = kShared ? warp * kHeadsPerWarp : 0;
-    const long long ub = (long long)w * R;
-    if (ub >= U) return;                       // uniform per worker; no CTA barrier follows
-    const int u_begin = (int)ub;
-    const int u_end = (int)min((long long)U, ub + R);
-    const int n_units = u_end - u_begin;
+    if (w >= pt.P) return;                     // uniform per worker (grid is sized to P)
+    const long long sl = (long long)w * pt.R;
+    const int st_lo = (int)min((long long)pt.U, sl);
+    const int st_hi = (int)min((long long)pt.U, sl + pt.Rs);
 
     const int ring_id = kShared ? 0 : warp;
     const uint32_t ring = sbase + ring_id * C::kStages * C::kStage;
     const uint32_t bar0 = sbase + S::kBars + ring_id * C::kStages * 8;
     const uint32_t ebar0 = sbase + S::kEmpty;
-    volatile int* bad = reinterpret_cast<volatile int*>(gbase + S::kBad) + ring_id * C::kStages;
+    volatile int* meta = reinterpret_cast<volatile int*>(gbase + S::kMeta) + ring_id * C::kStages * 4;
     const bool producer = !kShared || warp == 0;  // the warp that issues this ring's copies
     if (kShared) {
         if (threadIdx.x == 0) {
@@ -692,14 +747,23 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     }
     const uint64_t pol = l2_policy_evict_first();
 
-    // Window of physical blocks (producer warp): lane l holds unit win_base + l.
-    int win_base = -(1 << 30), win_phys = -1, win_g = 0;
+    // ---- producer: segments (static range first, then pooled chunks) and copies
+    // The pool is asked for the next chunk kLookahead units before the current
+    // segment runs out, and that chunk's block-table entries are fetched as soon
+    // as its id is known, so switching segments costs no round trip.
+    constexpr int kLookahead = 2;
+    const unsigned long long pool = (unsigned long long)pt.P * pt.cpw;
+    int iss_u = 0, iss_hi = 0, iss_seg = -1, n_issued = 0;
+    int nxt_lo = 0, nxt_hi = 0, nxt_seg = -1;
+    bool iss_done = false, nxt_ok = false, pend_out = false, exhausted = pool == 0;
+    unsigned long long pend = 0;                           // lane 0: in-flight pool ticket
+    int win_base = -(1 << 30), win_phys = -1, win_g = 0;   // lane l: unit win_base + l
     auto refill = [&](int base) {
         win_base = base;
         const int u = base + lane;
         win_phys = -1;
         win_g = 0;
-        if (u < u_end) {
+        if (u < pt.U) {
             int b, g, j;
             locate(u, pref, a.B, a.K, b, g, j);
             const int ph = a.block_tables[(long long)b * a.max_blocks + j];
@@ -708,17 +772,79 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             win_g = g;
         }
     };
-    auto issue = [&](int u, int s) {
-        if (u - win_base >= 32) refill(u);
+    auto request = [&]() {
+        if (pend_out || exhausted) return;
+        if (lane == 0) pend = atomicAdd(a.ws_ctr, 1ull);
+        pend_out = true;
+    };
+    auto resolve = [&]() {                 // the in-flight ticket -> the next segment
+        while (pend_out) {
+            const unsigned long long cidx = __shfl_sync(kFull, pend, 0);
+            pend_out = false;
+            if (cidx >= pool) {
+                exhausted = true;
+                return;
+            }
+            const int wc = (int)(cidx % pt.P), ic = (int)(cidx / pt.P);
+            const long long lo = (long long)wc * pt.R + pt.Rs + (long long)ic * pt.Cz;
+            if (lo >= pt.U) {              // a chunk past the last unit: take another
+                request();
+                continue;
+            }
+            nxt_lo = (int)lo;
+            nxt_hi = (int)min((long long)pt.U, lo + pt.Cz);
+            nxt_seg = wc * (1 + pt.cpw) + 1 + ic;
+            nxt_ok = true;
+        }
+    };
+    if (producer) {
+        if (st_lo < st_hi) {
+            iss_u = st_lo;
+            iss_hi = st_hi;
+            iss_seg = w * (1 + pt.cpw);
+            if (iss_hi - iss_u <= kLookahead) request();
+        } else {
+            request();
+        }
+    }
+    // Fill ring slot s with the next unit of this worker, or with the end marker.
+    auto issue_next = [&](int s) {
+        if (iss_done) return;
+        const uint32_t bar = bar0 + 8 * s;
+        ++n_issued;
+        if (iss_u >= iss_hi) {
+            if (!nxt_ok) {
+                request();
+                resolve();
+            }
+            if (!nxt_ok) {
+                iss_done = true;
+                if (lane == 0) {
+                    meta[4 * s] = kSlotEnd;
+                    mbar_arrive(bar);
+                }
+                return;
+            }
+            iss_u = nxt_lo;
+            iss_hi = nxt_hi;
+            iss_seg = nxt_seg;
+            nxt_ok = false;
+            if (iss_hi - iss_u <= kLookahead) request();
+        }
+        const int u = iss_u++;
+        // pooled chunks can lie before this worker's own range: refill on any jump
+        if (u < win_base || u - win_base >= 32) refill(u);
         const int ph = __shfl_sync(kFull, win_phys, u - win_base);
         const int gg = __shfl_sync(kFull, win_g, u - win_base);
         if (lane == 0) {
-            const uint32_t bar = bar0 + 8 * s;
-            const uint32_t dst = ring + s * C::kStage;
+            meta[4 * s + 1] = u;
+            meta[4 * s + 2] = iss_seg;
+            meta[4 * s + 3] = iss_hi;
             if (ph >= 0) {
+                const uint32_t dst = ring + s * C::kStage;
                 auto coord = [&](int which) { return which == 0 ? 0 : (which == 1 ? gg : ph); };
                 const int y = coord(a.map_perm[0]), z = coord(a.map_perm[1]), ww = coord(a.map_perm[2]);
-                bad[s] = 0;
+                meta[4 * s] = kSlotData;
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar, C::kTxBytes);
 #pragma unroll
@@ -733,93 +859,107 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                     bulk_load(dst + 2 * C::kTile + 32, a.v_scale + si, 32, bar, pol);
                 }
             } else {
-                bad[s] = 1;
+                meta[4 * s] = kSlotSkip;
                 mbar_arrive(bar);
             }
+        }
+        if (iss_hi - iss_u == kLookahead) request();
+        if (iss_u == iss_hi) {             // segment issued: learn the next one, prefetch its table
+            resolve();
+            if (nxt_ok) refill(nxt_lo);
         }
     };
     // Bounded waits whose verdict is warp-uniform, so a timeout never splits a warp.
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
         return __all_sync(kFull, mbar_wait(bar, parity));
     };
-    auto bail = [&](int i) {
+    auto bail = [&](int k) {
         // A copy (or a peer warp) did not arrive in time: report, let this ring's
         // in-flight copies land, leave.
         if (lane == 0) flag_error(a.err, GQA_DEVERR_TIMEOUT);
         if (producer)
-            for (int k = i; k < min(n_units, i + (int)C::kStages); ++k)
-                mbar_wait(bar0 + 8 * (k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimitNs / 4);
+            for (int q = k; q < n_issued; ++q)
+                mbar_wait(bar0 + 8 * (q % C::kStages), (uint32_t)(q / C::kStages) & 1u, kWaitLimitNs / 4);
     };
-    // Hand slot s (just read) back; the producer refills it with unit i + kStages.
-    auto release_and_refill = [&](int i, int s) -> bool {
+    // Hand slot s (use k, just read) back; the producer refills it.
+    auto release_and_refill = [&](int k, int s) -> bool {
         __syncwarp();
         if (kShared && lane == 0) mbar_arrive(ebar0 + 8 * s);
-        if (producer && i + C::kStages < n_units) {
-            if (kShared && !wait_all(ebar0 + 8 * s, (uint32_t)(i / C::kStages) & 1u)) return false;
-            issue(u_begin + i + C::kStages, s);
+        if (producer && !iss_done) {
+            if (kShared && !wait_all(ebar0 + 8 * s, (uint32_t)(k / C::kStages) & 1u)) return false;
+            issue_next(s);
         }
         return true;
     };
 
-    if (producer) {
-        const int npro = min((int)C::kStages, n_units);
-        for (int s = 0; s < npro; ++s) issue(u_begin + s, s);
-    }
+    if (producer)
+        for (int s = 0; s < C::kStages; ++s) issue_next(s);
 
-    // Compute-side cursor.
-    int cb, cg, cj;
-    locate(u_begin, pref, a.B, a.K, cb, cg, cj);
-    int cnb = pref[cb + 1] - pref[cb];
-    int clen = lens_s[cb];
-    int first_j = cj;
-    int cu_pair = a.K * pref[cb] + cg * cnb;      // first unit of the current pair
+    // ---- consumer: walk the units as they arrive
     const int r = lane >> 2, c = lane & 3;
-
     using State = typename std::conditional<kKind == kKernelMma, MmaState<C, D>, FmaState<C, D>>::type;
     State st;
-    st.reset();
-    int nb_b = cb, nb_g = cg;                   // next pair (for the q prefetch)
-    next_pair(pref, a.B, a.K, nb_b, nb_g);
-    if constexpr (kKind == kKernelMma) {
-        load_q_frags<C, D>(a, cb, cg, hbase, r, c, st.qf);
-        if (cu_pair + cnb < u_end) load_q_frags<C, D>(a, nb_b, nb_g, hbase, r, c, st.qn);
-    } else {
-        fma_load_q<C, D>(a, st, cb, cg, hbase, lane);
-    }
+    int cb = 0, cg = 0, cj = 0, cnb = 1, clen = 0, first_j = 0, cu_pair = 0;
+    int nb_b = 0, nb_g = 0, next_u = -1;
 
-    for (int i = 0; i < n_units; ++i) {
-        const int s = i % C::kStages;
-        const uint32_t parity = (uint32_t)(i / C::kStages) & 1u;
-        // every lane observes the phase, which acquires the TMA writes
-        if (!wait_all(bar0 + 8 * s, parity)) {
-            bail(i);
+    for (int k = 0;; ++k) {
+        const int s = k % C::kStages;
+        // every lane observes the phase, which acquires the TMA writes and the metadata
+        if (!wait_all(bar0 + 8 * s, (uint32_t)(k / C::kStages) & 1u)) {
+            bail(k);
             return;
         }
+        const int kind = meta[4 * s];
+        if (kind == kSlotEnd) break;
+        const int u = meta[4 * s + 1], seg = meta[4 * s + 2], seg_end = meta[4 * s + 3];
+        if (u != next_u) {
+            // first unit of a segment: find its pair and load that pair's queries
+            locate(u, pref, a.B, a.K, cb, cg, cj);
+            cnb = pref[cb + 1] - pref[cb];
+            clen = lens_s[cb];
+            first_j = cj;
+            cu_pair = a.K * pref[cb] + cg * cnb;
+            st.reset();
+            nb_b = cb;
+            nb_g = cg;
+            next_pair(pref, a.B, a.K, nb_b, nb_g);
+            if constexpr (kKind == kKernelMma) {
+                load_q_frags<C, D>(a, cb, cg, hbase, r, c, st.qf);
+                if (cu_pair + cnb < seg_end) load_q_frags<C, D>(a, nb_b, nb_g, hbase, r, c, st.qn);
+            } else {
+                fma_load_q<C, D>(a, st, cb, cg, hbase, lane);
+            }
+        }
         const int nvalid = min((int)kBlock, clen - kBlock * cj);
-        const bool unit_ok = !bad[s];
+        const bool unit_ok = kind == kSlotData;
         if constexpr (kKind == kKernelMma) {
             // read the whole slot, hand it back to TMA, then compute from registers
             MmaFrags<C, D> fr;
             if (unit_ok) mma_load<C, D>(fr, ring + s * C::kStage, lane, r, c);
-            if (!release_and_refill(i, s)) {
-                bail(i + 1);
+            if (!release_and_refill(k, s)) {
+                bail(k + 1);
                 return;
             }
             if (unit_ok) mma_compute<C, D>(st, fr, nvalid, r, c, a.scale_log2);
         } else {
             if (unit_ok) fma_block<C, D, T>(a, st, ring + s * C::kStage, nvalid, hbase, lane);
-            if (!release_and_refill(i, s)) {
-                bail(i + 1);
+            if (!release_and_refill(k, s)) {
+                bail(k + 1);
                 return;
             }
         }
 
         const bool last_of_pair = (cj == cnb - 1);
-        if (last_of_pair || i == n_units - 1) {
+        const bool last_of_seg = (u == seg_end - 1);
+        next_u = u + 1;
+        if (last_of_pair || last_of_seg) {
             const bool whole = (first_j == 0) && last_of_pair;
-            if constexpr (kKind == kKernelMma) mma_flush<C, D>(a, st, cb, cg, hbase, whole, w, r, c);
-            else fma_flush<C, D>(a, st, cb, cg, hbase, whole, w, lane);
-            if (i == n_units - 1) break;
+            if constexpr (kKind == kKernelMma) mma_flush<C, D>(a, st, cb, cg, hbase, whole, seg, r, c);
+            else fma_flush<C, D>(a, st, cb, cg, hbase, whole, seg, lane);
+            if (last_of_seg) {
+                next_u = -1;                   // the next unit starts a new segment
+                continue;
+            }
             cb = nb_b;
             cg = nb_g;
             cj = 0;
@@ -831,8 +971,8 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             next_pair(pref, a.B, a.K, nb_b, nb_g);
             if constexpr (kKind == kKernelMma) {
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) st.qf[k] = st.qn[k];
-                if (cu_pair + cnb < u_end) load_q_frags<C, D>(a, nb_b, nb_g, hbase, r, c, st.qn);
+                for (int q = 0; q < D / 16; ++q) st.qf[q] = st.qn[q];
+                if (cu_pair + cnb < seg_end) load_q_frags<C, D>(a, nb_b, nb_g, hbase, r, c, st.qn);
             } else {
                 fma_load_q<C, D>(a, st, cb, cg, hbase, lane);
             }
@@ -844,80 +984,104 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 
 // ------------------------------------------------------------------ combine
 
-constexpr int kCombineWarps = 8;
-
-// Merge the splits of one (sequence, query head); zero rows of empty sequences.
-// Warp w takes splits w, w+8, ...; lane l owns dims 4l..4l+3; the eight partial
-// sums meet in shared memory.
-template <int D>
-__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecodeArgs a) {
-    __shared__ float s_red[kCombineWarps];
-    __shared__ float s_acc[kCombineWarps][D];
-    __shared__ float s_l[kCombineWarps];
+// Merge the splits of each (sequence, query head) row; zero rows of empty
+// sequences. kRowWarps warps share a row (they take its splits in turn and meet
+// in shared memory); a CTA holds kRows rows. CTA 0 also rewinds the run-time
+// work counter for the next call (every split-KV CTA has finished by now).
+template <int D, int kRowWarps, int kRows>
+__global__ void __launch_bounds__(kRowWarps * kRows * 32) combine_kernel(const DecodeArgs a) {
+    static_assert(kRowWarps == 1 || kRows == 1, "rows of several warps need a CTA each");
+    __shared__ float s_red[kRowWarps];
+    __shared__ float s_acc[kRowWarps > 1 ? kRowWarps : 1][kRowWarps > 1 ? D : 1];
+    __shared__ float s_l[kRowWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int bh = blockIdx.x;
+    const int sub = warp % kRowWarps;
+    const long long bh = (long long)blockIdx.x * kRows + warp / kRowWarps;
     launch_dependents();
     grid_dependency_wait();                    // the split-KV kernel's partials
-    const int b = bh / a.H, h = bh % a.H, g = h / a.G, hh = h % a.G;
-    const long long orow = (long long)bh * D;
+    if (blockIdx.x == 0 && tid == 0) *a.ws_ctr = 0ull;
+    if (bh >= (long long)a.B * a.H) return;
+    const int b = (int)(bh / a.H), h = (int)(bh % a.H), g = h / a.G, hh = h % a.G;
+    const long long orow = bh * D;
     const int p0 = a.ws_pref[b];
     const int nb = a.ws_pref[b + 1] - p0;
     if (nb == 0) {
-        for (int i = tid; i < D; i += blockDim.x) store1(a.out, a.out_dtype, orow + i, 0.f);
+        for (int i = sub * 32 + lane; i < D; i += kRowWarps * 32) store1(a.out, a.out_dtype, orow + i, 0.f);
         return;
     }
-    const int R = a.ws_hdr[0];
-    const long long u0 = (long long)a.K * p0 + (long long)g * nb;
-    const int w0 = (int)(u0 / R), w1 = (int)((u0 + nb - 1) / R);
-    if (w0 == w1) return;                      // one warp saw the whole pair and wrote it
-    const long long first = (long long)b * a.K + g + w0;   // slot of the first split
-    const int n = w1 - w0 + 1;
+    Partition pt;
+    pt.R = a.ws_hdr[0];
+    pt.U = a.ws_hdr[1];
+    pt.Rs = a.ws_hdr[2];
+    pt.Cz = a.ws_hdr[3];
+    pt.P = a.ws_hdr[4];
+    pt.cpw = a.ws_hdr[5];
+    const int u0 = a.K * p0 + g * nb;
+    const int s0 = pt.segment_of(u0), s1 = pt.segment_of(u0 + nb - 1);
+    if (s0 == s1) return;                      // one segment held the whole pair and wrote it
+    const long long first = (long long)b * a.K + g + s0;   // slot of the first piece
+    const int n = s1 - s0 + 1;
 
     // pass 1: the largest running maximum
     float M = -INFINITY;
-    for (int p = tid; p < n; p += blockDim.x) M = fmaxf(M, a.ws_ml[(first + p) * a.G + hh].x);
+    for (int p = sub * 32 + lane; p < n; p += kRowWarps * 32)
+        M = fmaxf(M, __ldcg(&a.ws_ml[(first + p) * a.G + hh]).x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-    if (lane == 0) s_red[warp] = M;
-    __syncthreads();
-    M = s_red[0];
+    if constexpr (kRowWarps > 1) {
+        if (lane == 0) s_red[sub] = M;
+        __syncthreads();
+        M = s_red[0];
 #pragma unroll
-    for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, s_red[w]);
+        for (int w = 1; w < kRowWarps; ++w) M = fmaxf(M, s_red[w]);
+    }
 
-    // pass 2: weighted sums
+    // pass 2: weighted sums (pieces with m = -inf saw only skipped blocks)
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const bool has_dims = 4 * lane < D;
     if (M != -INFINITY) {
 #pragma unroll 4
-        for (int p = warp; p < n; p += kCombineWarps) {
+        for (int p = sub; p < n; p += kRowWarps) {
             const long long slot = first + p;
-            const float2 ml = a.ws_ml[slot * a.G + hh];
+            const float2 ml = __ldcg(&a.ws_ml[slot * a.G + hh]);
+            if (ml.x == -INFINITY) continue;
             const float e = fast_exp2(ml.x - M);
             L += ml.y * e;
             if (has_dims) {
-                const float4 o = *reinterpret_cast<const float4*>(a.ws_o + (slot * a.G + hh) * D + 4 * lane);
+                const float4 o = __ldcg(reinterpret_cast<const float4*>(a.ws_o + (slot * a.G + hh) * D + 4 * lane));
                 acc.x += o.x * e; acc.y += o.y * e; acc.z += o.z * e; acc.w += o.w * e;
             }
         }
     }
-    if (has_dims) {
-        s_acc[warp][4 * lane + 0] = acc.x;
-        s_acc[warp][4 * lane + 1] = acc.y;
-        s_acc[warp][4 * lane + 2] = acc.z;
-        s_acc[warp][4 * lane + 3] = acc.w;
-    }
-    if (lane == 0) s_l[warp] = L;
-    __syncthreads();
-    float Lt = 0.f;
+    if constexpr (kRowWarps > 1) {
+        if (has_dims) {
+            s_acc[sub][4 * lane + 0] = acc.x;
+            s_acc[sub][4 * lane + 1] = acc.y;
+            s_acc[sub][4 * lane + 2] = acc.z;
+            s_acc[sub][4 * lane + 3] = acc.w;
+        }
+        if (lane == 0) s_l[sub] = L;
+        __syncthreads();
+        float Lt = 0.f;
 #pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) Lt += s_l[w];
-    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
-    for (int i = tid; i < D; i += blockDim.x) {
-        float v = 0.f;
+        for (int w = 0; w < kRowWarps; ++w) Lt += s_l[w];
+        const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+        for (int i = tid; i < D; i += blockDim.x) {
+            float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < kCombineWarps; ++w) v += s_acc[w][i];
-        store1(a.out, a.out_dtype, orow + i, v * inv);
+            for (int w = 0; w < kRowWarps; ++w) v += s_acc[w][i];
+            store1(a.out, a.out_dtype, orow + i, v * inv);
+        }
+    } else {
+        // every lane walked every piece, so L is the same on all lanes
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        if (has_dims) {
+            store1(a.out, a.out_dtype, orow + 4 * lane + 0, acc.x * inv);
+            store1(a.out, a.out_dtype, orow + 4 * lane + 1, acc.y * inv);
+            store1(a.out, a.out_dtype, orow + 4 * lane + 2, acc.z * inv);
+            store1(a.out, a.out_dtype, orow + 4 * lane + 3, acc.w * inv);
+        }
     }
 }
 
@@ -925,6 +1089,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
 
 struct Variant {
     const void* fn;
+    int tail_chunks;     // pooled chunks per worker range
     int warps;           // threads / 32
     int workers_per_cta; // split-KV workers per CTA
     int box_inner;       // elements per TMA box row
@@ -935,7 +1100,7 @@ struct Variant {
 template <int kKind, typename T, int D, int NW>
 Variant make_variant() {
     using C = Cfg<kKind, T, D, NW>;
-    return Variant{reinterpret_cast<const void*>(&split_kv_kernel<kKind, T, D, NW>), C::kWarps,
+    return Variant{reinterpret_cast<const void*>(&split_kv_kernel<kKind, T, D, NW>), C::kTailChunks, C::kWarps,
                    NW == 1 ? C::kWarps : 1, C::kBoxInner, C::kSwizzle, &Smem<C>::bytes};
 }
 
@@ -981,6 +1146,20 @@ struct WsLayout {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Split slots: one per (pair, segment) overlap, at most pairs + segments. A
+// worker's range has R <= max(ceil(B*K*max_blocks / P), min_units) units and at
+// most min(kMaxTailChunks, R / 32) pooled chunks (make_partition); max_blocks
+// <= 0 means unknown.
+long long max_slots(int B, int K, int P, int max_blocks, int min_units, int tail_chunks) {
+    int cpw = tail_chunks;
+    if (max_blocks > 0) {
+        const long long u_max = (long long)B * K * max_blocks;
+        const long long r_max = std::max<long long>((u_max + P - 1) / P, min_units);
+        cpw = (int)std::min<long long>(tail_chunks, r_max / (8 * kMinChunk));
+    }
+    return (long long)B * K + (long long)P * (1 + cpw);
+}
+
 WsLayout ws_layout(int B, int K, int G, int D, long long slots) {
     WsLayout w;
     w.hdr = 0;
@@ -991,15 +1170,36 @@ WsLayout ws_layout(int B, int K, int G, int D, long long slots) {
     return w;
 }
 
+// Split-KV workers one launch uses for variant v at this batch (occupancy of a
+// single resident wave); 0 if the variant cannot launch.
+int workers_of(const Variant& v, int batch, int num_sms) {
+    const int smem = v.smem(batch);
+    if (cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return 0;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, v.fn, v.warps * 32, smem) != cudaSuccess)
+        return 0;
+    return num_sms * per_sm * v.workers_per_cta;
+}
+
 }  // namespace
 
-// Workers of one wave are at most 64 warps per SM, divided by the warps that
-// share a group's tiles; every (pair, worker) overlap is one split slot.
+// The largest workspace any kernel choice needs for this shape: workers are
+// taken from the occupancy of every variant that can serve (G, head_dim).
 size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int head_dim, int num_sms) {
     const int G = num_heads / num_kv_heads;
     const int nw = G <= 8 ? 1 : G <= 16 ? 2 : G <= 32 ? 4 : 8;
-    const long long slots = (long long)batch * num_kv_heads + (long long)num_sms * (kMaxWarpsPerSm / nw);
-    return ws_layout(batch, num_kv_heads, G, head_dim, slots).total;
+    int P = 0;
+    for (int kind : {kKernelMma, kKernelFma}) {
+        Variant v{};
+        if (pick_dim<float>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
+        if (pick_dim<__half>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
+        if (pick_dim<__nv_bfloat16>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
+        if (pick_dim<int8_t>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
+    }
+    if (P == 0) P = num_sms * (kMaxWarpsPerSm / nw);      // no occupancy answer: the hard bound
+    return ws_layout(batch, num_kv_heads, G, head_dim,
+                     max_slots(batch, num_kv_heads, P, 0, 0, kMaxTailChunks)).total;
 }
 
 int launch_decode(const DecodeLaunch& L, int num_sms) {
@@ -1026,19 +1226,17 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
         return GQA_ERR_UNSUPPORTED;
 
     const int smem = v.smem(L.batch);
-    cudaError_t e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return GQA_ERR_CUDA;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, v.fn, v.warps * 32, smem);
-    if (e != cudaSuccess) return GQA_ERR_CUDA;
-    if (per_sm < 1) return GQA_ERR_UNSUPPORTED;
-    int grid = num_sms * per_sm;
+    const int workers = workers_of(v, L.batch, num_sms);
+    if (workers < 1) return GQA_ERR_UNSUPPORTED;
+    int grid = workers / v.workers_per_cta;
+    cudaError_t e;
     if (L.max_warps > 0)
         grid = std::min(grid, std::max(1, (L.max_warps + v.workers_per_cta - 1) / v.workers_per_cta));
     const int P = grid * v.workers_per_cta;   // split-KV workers (KV splits per pass)
 
-    const long long slots = (long long)L.batch * K + P;
-    const WsLayout wl = ws_layout(L.batch, K, G, D, slots);
+    const int min_units = L.min_blocks_per_warp > 0 ? L.min_blocks_per_warp : 4;
+    const WsLayout wl =
+        ws_layout(L.batch, K, G, D, max_slots(L.batch, K, P, L.max_blocks, min_units, v.tail_chunks));
     if (L.workspace == nullptr || L.workspace_bytes < wl.total) return GQA_ERR_WORKSPACE;
 
     DecodeArgs a;
@@ -1051,6 +1249,7 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     a.err = L.err;
     uint8_t* ws = static_cast<uint8_t*>(L.workspace);
     a.ws_hdr = reinterpret_cast<int32_t*>(ws + wl.hdr);
+    a.ws_ctr = reinterpret_cast<unsigned long long*>(ws + wl.hdr + 32 * sizeof(int32_t));
     a.ws_pref = reinterpret_cast<int32_t*>(ws + wl.pref);
     a.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
     a.ws_o = reinterpret_cast<float*>(ws + wl.o);
@@ -1066,7 +1265,8 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     a.map_perm[0] = perm[0];
     a.map_perm[1] = perm[1];
     a.map_perm[2] = perm[2];
-    a.min_units = L.min_blocks_per_warp > 0 ? L.min_blocks_per_warp : 4;
+    a.min_units = min_units;
+    a.max_tail_chunks = v.tail_chunks;
     a.scale_log2 = L.scale * kLog2e;
 
     // Both kernels go out with programmatic stream serialisation: each may be
@@ -1090,14 +1290,35 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     if (e != cudaSuccess) return GQA_ERR_CUDA;
     if (L.ev_end && cudaEventRecord(L.ev_end, L.stream) != cudaSuccess) return GQA_ERR_CUDA;
 
+    // Combine width from the expected pieces per row (about 1.5 workers' worth
+    // of segments per pair when lengths are even).
+    const long long pairs = (long long)L.batch * K;
+    const long long est = (3LL * P) / (2 * pairs) + 1;
+    const void* cfn;
+    int rows_per_cta, cthreads;
+    if (est <= 8) {
+        cfn = D == 64 ? reinterpret_cast<const void*>(&combine_kernel<64, 1, 8>)
+                      : reinterpret_cast<const void*>(&combine_kernel<128, 1, 8>);
+        rows_per_cta = 8;
+        cthreads = 256;
+    } else if (est <= 64) {
+        cfn = D == 64 ? reinterpret_cast<const void*>(&combine_kernel<64, 8, 1>)
+                      : reinterpret_cast<const void*>(&combine_kernel<128, 8, 1>);
+        rows_per_cta = 1;
+        cthreads = 256;
+    } else {
+        cfn = D == 64 ? reinterpret_cast<const void*>(&combine_kernel<64, 32, 1>)
+                      : reinterpret_cast<const void*>(&combine_kernel<128, 32, 1>);
+        rows_per_cta = 1;
+        cthreads = 1024;
+    }
+    const long long rows = (long long)L.batch * L.num_heads;
     cudaLaunchConfig_t ccfg = {};
-    ccfg.gridDim = dim3(L.batch * L.num_heads);
-    ccfg.blockDim = dim3(kCombineWarps * 32);
+    ccfg.gridDim = dim3((unsigned)((rows + rows_per_cta - 1) / rows_per_cta));
+    ccfg.blockDim = dim3(cthreads);
     ccfg.stream = L.stream;
     ccfg.attrs = pdl;
     ccfg.numAttrs = timed ? 0 : 1;
-    const void* cfn = D == 64 ? reinterpret_cast<const void*>(&combine_kernel<64>)
-                              : reinterpret_cast<const void*>(&combine_kernel<128>);
     void* cargs[] = {&a};
     if (cudaLaunchKernelExC(&ccfg, cfn, cargs) != cudaSuccess) return GQA_ERR_CUDA;
     return GQA_OK;

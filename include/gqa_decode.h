@@ -180,7 +180,10 @@ GQA_API size_t gqa_decode_workspace_size(int32_t batch, int32_t num_heads, int32
  *  out            device [batch, num_heads, head_dim] of out_dtype (F32, BF16
  *                 or F16); 16-byte aligned.
  *  workspace      device, >= gqa_decode_workspace_size(...) bytes, 256-byte
- *                 aligned; contents need no initialisation and are clobbered.
+ *                 aligned, zero-filled before its first use (one word of it, the
+ *                 run-time work counter, must start at zero; every call leaves it
+ *                 at zero again). Otherwise clobbered by each call. Calls that
+ *                 share a workspace must not overlap on the GPU.
  *  opts           NULL or tuning knobs (gqa_decode_opts_t).
  *  Limits: num_heads % K == 0; num_heads / K <= 64 (groups above 8 need a
  *  BF16/F16/I8 cache with head_dim 128 for I8, or an F32 cache); batch <= 8191;
@@ -205,15 +208,17 @@ GQA_API int gqa_decode(const gqa_kv_cache_t *cache, const void *q, int32_t q_dty
  * process exits. Arguments and results are those of gqa_decode minus the
  * workspace. This call allocates nothing (no cudaMalloc, no library allocator).
  *  - Returns GQA_ERR_WORKSPACE when the shape needs more scratch than the array
- *    holds (the five workloads of the benchmark need under 10 MiB).
+ *    holds (the five workloads of the benchmark need under 48 MiB).
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    before any stream capture on the device.
- *  - Every call shares the one array and it keeps the last call's contents
- *    (nothing in it needs to start at zero). Calls whose GPU work overlaps --
- *    different streams, or different host threads -- race on it; serialise them.
+ *  - Every call shares the one array and it keeps the last call's contents.
+ *    The one word that must start at zero does: the array is zero when the
+ *    library loads and every call leaves that word at zero. Calls whose GPU
+ *    work overlaps -- different streams, or different host threads -- race on
+ *    it; serialise them.
  */
-#define GQA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+#define GQA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 
 GQA_API int gqa_decode_noalloc(const gqa_kv_cache_t *cache, const void *q, int32_t q_dtype,
                                int32_t num_heads, const int32_t *block_tables,
