@@ -1022,7 +1022,7 @@ __global__ void __launch_bounds__(kRowWarps * kRows * 32) combine_kernel(const D
     const long long first = (long long)b * a.K + g + s0;   // slot of the first piece
     const int n = s1 - s0 + 1;
 
-    // pass 1: the largest running maximum
+    // pass 1: the largest running maximum (one piece per lane)
     float M = -INFINITY;
     for (int p = sub * 32 + lane; p < n; p += kRowWarps * 32)
         M = fmaxf(M, __ldcg(&a.ws_ml[(first + p) * a.G + hh]).x);
@@ -1036,24 +1036,36 @@ __global__ void __launch_bounds__(kRowWarps * kRows * 32) combine_kernel(const D
         for (int w = 1; w < kRowWarps; ++w) M = fmaxf(M, s_red[w]);
     }
 
-    // pass 2: weighted sums (pieces with m = -inf saw only skipped blocks)
+    // pass 2: each warp takes 32 pieces at a time: lane j learns piece j's weight,
+    // then every lane gathers its dims of all 32 partial vectors with independent
+    // loads. Pieces that saw only skipped blocks hold m = -inf and o = 0.
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const bool has_dims = 4 * lane < D;
     if (M != -INFINITY) {
-#pragma unroll 4
-        for (int p = sub; p < n; p += kRowWarps) {
-            const long long slot = first + p;
-            const float2 ml = __ldcg(&a.ws_ml[slot * a.G + hh]);
-            if (ml.x == -INFINITY) continue;
-            const float e = fast_exp2(ml.x - M);
-            L += ml.y * e;
-            if (has_dims) {
-                const float4 o = __ldcg(reinterpret_cast<const float4*>(a.ws_o + (slot * a.G + hh) * D + 4 * lane));
-                acc.x += o.x * e; acc.y += o.y * e; acc.z += o.z * e; acc.w += o.w * e;
+        for (int base = sub * 32; base < n; base += kRowWarps * 32) {
+            const int p = base + lane;
+            float e = 0.f;
+            if (p < n) {
+                const float2 ml = __ldcg(&a.ws_ml[(first + p) * a.G + hh]);
+                e = fast_exp2(ml.x - M);
+                L += ml.y * e;
+            }
+            const int cnt = min(32, n - base);
+            const float* op = a.ws_o + ((first + base) * a.G + hh) * D + 4 * lane;
+            const long long step = (long long)a.G * D;
+#pragma unroll 8
+            for (int j = 0; j < cnt; ++j) {
+                const float ej = __shfl_sync(kFull, e, j);
+                if (has_dims) {
+                    const float4 o = __ldcg(reinterpret_cast<const float4*>(op + j * step));
+                    acc.x += o.x * ej; acc.y += o.y * ej; acc.z += o.z * ej; acc.w += o.w * ej;
+                }
             }
         }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
     if constexpr (kRowWarps > 1) {
         if (has_dims) {
             s_acc[sub][4 * lane + 0] = acc.x;
@@ -1074,7 +1086,6 @@ __global__ void __launch_bounds__(kRowWarps * kRows * 32) combine_kernel(const D
             store1(a.out, a.out_dtype, orow + i, v * inv);
         }
     } else {
-        // every lane walked every piece, so L is the same on all lanes
         const float inv = L > 0.f ? 1.f / L : 0.f;
         if (has_dims) {
             store1(a.out, a.out_dtype, orow + 4 * lane + 0, acc.x * inv);
