@@ -498,26 +498,41 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
             mma_t<kB>(st.acc[j], f.v[j][0], f.v[j][1], f.v[j][2], f.v[j][3], bl0, bl1);
         }
     } else {
-        // codes -> f16 pairs: vr[i][jj] = dims (16r + 2jj, +1) of token i
-        uint32_t vr[4][8];
+        // f.v[i][w] holds dims 16r + 4w .. +3 (one byte each) of token i in
+        // {2c, 2c+1, 2c+8, 2c+9}. Tokens past the end hold arbitrary codes.
+        if (nvalid < kBlock) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int tok = 2 * c + (i & 1) + 8 * (i >> 1);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) i8x4_to_f16x4(f.v[i][w], vr[i][2 * w], vr[i][2 * w + 1]);
-            if (tok >= nvalid) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) vr[i][e] = 0u;
+            for (int i = 0; i < 4; ++i) {
+                const int tok = 2 * c + (i & 1) + 8 * (i >> 1);
+                if (tok >= nvalid) f.v[i][0] = f.v[i][1] = f.v[i][2] = f.v[i][3] = 0u;
             }
         }
+        // A fragment of m-tile j = 2w + e (dims 16r + 4w + 2e, +1) for the token
+        // pair (x, y): interleave the two tokens' bytes, then widen each byte to
+        // f16 exactly (1024 + (code ^ 0x80) - 1152).
+        const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+        auto widen = [&](uint32_t t, uint32_t sel) -> uint32_t {
+            const uint32_t hv = __byte_perm(t, 0x64646464u, sel);
+            __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&hv), bias);
+            return as_u32(h);
+        };
 #pragma unroll
-        for (int j = 0; j < C::kMt; ++j) {
-            const uint32_t a0 = __byte_perm(vr[0][j], vr[1][j], 0x5410);
-            const uint32_t a1 = __byte_perm(vr[0][j], vr[1][j], 0x7632);
-            const uint32_t a2 = __byte_perm(vr[2][j], vr[3][j], 0x5410);
-            const uint32_t a3 = __byte_perm(vr[2][j], vr[3][j], 0x7632);
-            mma_f16(st.acc[j], a0, a1, a2, a3, bh0, bh1);
-            mma_f16(st.acc[j], a0, a1, a2, a3, bl0, bl1);
+        for (int wd = 0; wd < 4; ++wd) {
+            const uint32_t x0 = f.v[0][wd] ^ 0x80808080u, y0 = f.v[1][wd] ^ 0x80808080u;
+            const uint32_t x1 = f.v[2][wd] ^ 0x80808080u, y1 = f.v[3][wd] ^ 0x80808080u;
+            // bytes (x.b0, y.b0, x.b1, y.b1) and (x.b2, y.b2, x.b3, y.b3)
+            const uint32_t lo0 = __byte_perm(x0, y0, 0x5140), hi0 = __byte_perm(x0, y0, 0x7362);
+            const uint32_t lo1 = __byte_perm(x1, y1, 0x5140), hi1 = __byte_perm(x1, y1, 0x7362);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const uint32_t t0 = e ? hi0 : lo0, t1 = e ? hi1 : lo1;
+                // rows r (dim 4wd + 2e) and r+8 (dim 4wd + 2e + 1): tokens (2c, 2c+1)
+                const uint32_t a0 = widen(t0, 0x4140), a1 = widen(t0, 0x4342);
+                const uint32_t a2 = widen(t1, 0x4140), a3 = widen(t1, 0x4342);
+                const int j = 2 * wd + e;
+                mma_f16(st.acc[j], a0, a1, a2, a3, bh0, bh1);
+                mma_f16(st.acc[j], a0, a1, a2, a3, bl0, bl1);
+            }
         }
     }
 }
