@@ -42,11 +42,11 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kv_kernel_traffic.txt")
 def algorithmic_bytes(wl, lens) -> dict:
     """Bytes a decode step must move: KV (+scales) of every cached token once,
     q in, out (fp32) out, block-table entries and lengths, plus the append."""
-    es = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1}[wl.cache_dtype]
+    es = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1, "fp8": 1}[wl.cache_dtype]
     qes = {"f32": 4, "f16": 2, "bf16": 2}[wl.q_dtype]
     tokens = int(sum(int(x) for x in lens))
     per_token = 2 * wl.num_kv_heads * wl.head_dim * es
-    if wl.cache_dtype == "i8":
+    if wl.cache_dtype in ("i8", "fp8"):
         per_token += 2 * wl.num_kv_heads * 2
     blocks = int(sum(-(-int(x) // 16) for x in lens))
     B = len(lens)
@@ -54,7 +54,7 @@ def algorithmic_bytes(wl, lens) -> dict:
     q = B * wl.num_heads * wl.head_dim * qes
     o = B * wl.num_heads * wl.head_dim * 4
     meta = blocks * 4 + B * 4
-    new_es = qes if wl.cache_dtype == "i8" else es
+    new_es = qes if wl.cache_dtype in ("i8", "fp8") else es
     append = B * 2 * wl.num_kv_heads * wl.head_dim * (new_es + es) + B * 4
     decode = kv + q + o + meta
     return {"kv": kv, "decode": decode, "append": append, "step": decode + append,
@@ -374,7 +374,11 @@ def _oracle_inputs(wl, case, rows):
     ids = torch.from_numpy(np.concatenate(sel).astype(np.int64)).to(case.k_cache.device)
     def host(t):
         t = t.index_select(0, ids)
-        return t.cpu().numpy() if t.dtype == torch.int8 else t.float().cpu().numpy()
+        if t.dtype == torch.int8:
+            return t.cpu().numpy()
+        if t.dtype == torch.float8_e4m3fn:
+            return t.cpu().view(torch.uint8).numpy()
+        return t.float().cpu().numpy()
     kp, vp = host(case.k_cache), host(case.v_cache)
     new_table = np.zeros((len(rows), table.shape[1]), dtype=np.int64)
     off = 0
@@ -386,11 +390,17 @@ def _oracle_inputs(wl, case, rows):
     sb, sh, st = K * 16 * d, 16 * d, d
     kd = oracle.gather_dense(kp, new_table, sub_lens, sb, sh, st, K, d).astype(np.float64)
     vd = oracle.gather_dense(vp, new_table, sub_lens, sb, sh, st, K, d).astype(np.float64)
-    if wl.cache_dtype == "i8":
+    if wl.cache_dtype in ("i8", "fp8"):
         ksp = case.k_scale.index_select(0, ids).float().cpu().numpy()
         vsp = case.v_scale.index_select(0, ids).float().cpu().numpy()
-        kd = oracle.dequantize_int8(kd, oracle.gather_scales(ksp, new_table, sub_lens, K))
-        vd = oracle.dequantize_int8(vd, oracle.gather_scales(vsp, new_table, sub_lens, K))
+        kss = oracle.gather_scales(ksp, new_table, sub_lens, K)
+        vss = oracle.gather_scales(vsp, new_table, sub_lens, K)
+        if wl.cache_dtype == "i8":
+            kd = oracle.dequantize_int8(kd, kss)
+            vd = oracle.dequantize_int8(vd, vss)
+        else:
+            kd = oracle.dequantize_fp8(kd.astype(np.uint8), kss)
+            vd = oracle.dequantize_fp8(vd.astype(np.uint8), vss)
     q = case.q.float().cpu().numpy().astype(np.float64)[rows]
     return q, kd, vd, sub_lens
 

@@ -27,7 +27,8 @@ import torch
 from . import build as _build
 
 BLOCK_SIZE = 16
-DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int8: 3}
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.int8: 3,
+              torch.float8_e4m3fn: 4}
 
 GQA_DEVERR_BLOCK_INDEX = 1
 GQA_DEVERR_CONTEXT_LEN = 2
@@ -139,7 +140,7 @@ class PagedKVCache:
         k = torch.empty(shape, dtype=dtype, device=device)
         v = torch.empty(shape, dtype=dtype, device=device)
         ks = vs = None
-        if dtype == torch.int8:
+        if dtype in (torch.int8, torch.float8_e4m3fn):
             ks = torch.empty((num_blocks, num_kv_heads, BLOCK_SIZE), dtype=torch.float16, device=device)
             vs = torch.empty_like(ks)
         return PagedKVCache(k, v, num_blocks, num_kv_heads, head_dim,

@@ -2,7 +2,7 @@
 // (sequence, kv-head) go to slot pos % 16 of block block_tables[b][pos / 16]
 // ("LLM 推理性能优化实战", sections 5.3-5.4 and 8.2). One warp per
 // (sequence, kv-head) writes both rows, so K and V of a token leave together.
-// For an int8 cache each row is quantised on the way (symmetric, one fp16
+// For an int8 or FP8 (e4m3) cache each row is quantised on the way (one fp16
 // scale per (token, kv-head); sections 15.1, 15.2 and 15.5 of that page).
 #include "gqa_device.cuh"
 #include "gqa_internal.h"
@@ -72,9 +72,11 @@ __device__ __forceinline__ float load_as_float(const void* p, long long i) {
     else return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
 }
 
-// Quantise one row of d values held EPL per lane; returns the scale, writes codes.
-template <typename In, int EPL>
-__device__ __forceinline__ void quantise_row(const void* src, long long src_off, int8_t* dst,
+// Quantise one row of d values held EPL per lane; writes codes and the scale.
+// kFp8: e4m3 codes, s = amax/448, nearest-even with saturation to +-448;
+// else int8 codes, s = amax/127, rint with ties to even, clamped to +-127.
+template <typename In, int EPL, bool kFp8>
+__device__ __forceinline__ void quantise_row(const void* src, long long src_off, uint8_t* dst,
                                              __half* scale_dst, int lane) {
     float x[EPL];
     float amax = 0.f;
@@ -85,30 +87,30 @@ __device__ __forceinline__ void quantise_row(const void* src, long long src_off,
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-    float s32 = __fdiv_rn(amax, 127.0f);
+    float s32 = __fdiv_rn(amax, kFp8 ? 448.0f : 127.0f);
     s32 = fminf(s32, 65504.0f);
     const __half sh = __float2half_rn(s32);
     const float sf = __half2float(sh);
-    uint32_t packed[EPL / 4 > 0 ? EPL / 4 : 1] = {};
-    int8_t codes[EPL];
+    uint8_t codes[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
-        int q = 0;
+        uint8_t q = 0;
         if (sf != 0.f) {
-            q = __float2int_rn(__fdiv_rn(x[e], sf));
-            q = max(-127, min(127, q));
+            const float t = __fdiv_rn(x[e], sf);
+            if constexpr (kFp8) {
+                q = (uint8_t)__nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
+            } else {
+                q = (uint8_t)(int8_t)max(-127, min(127, __float2int_rn(t)));
+            }
         }
-        codes[e] = static_cast<int8_t>(q);
+        codes[e] = q;
     }
     if constexpr (EPL % 4 == 0) {
 #pragma unroll
         for (int w = 0; w < EPL / 4; ++w)
-            packed[w] = (uint32_t)(uint8_t)codes[4 * w] | ((uint32_t)(uint8_t)codes[4 * w + 1] << 8) |
-                        ((uint32_t)(uint8_t)codes[4 * w + 2] << 16) |
-                        ((uint32_t)(uint8_t)codes[4 * w + 3] << 24);
-#pragma unroll
-        for (int w = 0; w < EPL / 4; ++w)
-            reinterpret_cast<uint32_t*>(dst + lane * EPL)[w] = packed[w];
+            reinterpret_cast<uint32_t*>(dst + lane * EPL)[w] =
+                (uint32_t)codes[4 * w] | ((uint32_t)codes[4 * w + 1] << 8) |
+                ((uint32_t)codes[4 * w + 2] << 16) | ((uint32_t)codes[4 * w + 3] << 24);
     } else {
 #pragma unroll
         for (int e = 0; e < EPL; ++e) dst[lane * EPL + e] = codes[e];
@@ -116,7 +118,7 @@ __device__ __forceinline__ void quantise_row(const void* src, long long src_off,
     if (lane == 0) *scale_dst = sh;
 }
 
-template <typename In, int EPL>
+template <typename In, int EPL, bool kFp8>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) append_quant_kernel(const AppendArgs a) {
     grid_dependency_wait();
     launch_dependents();
@@ -130,8 +132,23 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) append_quant_kernel(const A
     const int phys = a.block_tables[(long long)b * a.max_blocks + pos / kBlock];
     const long long sidx = ((long long)phys * a.K + g) * kBlock + pos % kBlock;
     const long long src = ((long long)b * a.K + g) * a.d;
-    quantise_row<In, EPL>(a.k_new, src, static_cast<int8_t*>(a.k_cache) + off, a.k_scale + sidx, lane);
-    quantise_row<In, EPL>(a.v_new, src, static_cast<int8_t*>(a.v_cache) + off, a.v_scale + sidx, lane);
+    quantise_row<In, EPL, kFp8>(a.k_new, src, static_cast<uint8_t*>(a.k_cache) + off, a.k_scale + sidx, lane);
+    quantise_row<In, EPL, kFp8>(a.v_new, src, static_cast<uint8_t*>(a.v_cache) + off, a.v_scale + sidx, lane);
+}
+
+template <bool kFp8>
+const void* quant_kernel(int new_dtype, bool d64) {
+    switch (new_dtype) {
+        case GQA_DTYPE_F32:
+            return d64 ? reinterpret_cast<const void*>(&append_quant_kernel<float, 2, kFp8>)
+                       : reinterpret_cast<const void*>(&append_quant_kernel<float, 4, kFp8>);
+        case GQA_DTYPE_F16:
+            return d64 ? reinterpret_cast<const void*>(&append_quant_kernel<__half, 2, kFp8>)
+                       : reinterpret_cast<const void*>(&append_quant_kernel<__half, 4, kFp8>);
+        default:
+            return d64 ? reinterpret_cast<const void*>(&append_quant_kernel<__nv_bfloat16, 2, kFp8>)
+                       : reinterpret_cast<const void*>(&append_quant_kernel<__nv_bfloat16, 4, kFp8>);
+    }
 }
 
 }  // namespace
@@ -163,24 +180,9 @@ cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const v
     const int grid = (int)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
     if (grid == 0) return cudaSuccess;
     const void* fn;
-    if (c.dtype != GQA_DTYPE_I8) {
-        fn = reinterpret_cast<const void*>(&append_copy_kernel);
-    } else {
-        const bool d64 = a.d == 64;
-        switch (new_dtype) {
-            case GQA_DTYPE_F32:
-                fn = d64 ? reinterpret_cast<const void*>(&append_quant_kernel<float, 2>)
-                         : reinterpret_cast<const void*>(&append_quant_kernel<float, 4>);
-                break;
-            case GQA_DTYPE_F16:
-                fn = d64 ? reinterpret_cast<const void*>(&append_quant_kernel<__half, 2>)
-                         : reinterpret_cast<const void*>(&append_quant_kernel<__half, 4>);
-                break;
-            default:
-                fn = d64 ? reinterpret_cast<const void*>(&append_quant_kernel<__nv_bfloat16, 2>)
-                         : reinterpret_cast<const void*>(&append_quant_kernel<__nv_bfloat16, 4>);
-        }
-    }
+    if (c.dtype == GQA_DTYPE_I8) fn = quant_kernel<false>(new_dtype, a.d == 64);
+    else if (c.dtype == GQA_DTYPE_FP8_E4M3) fn = quant_kernel<true>(new_dtype, a.d == 64);
+    else fn = reinterpret_cast<const void*>(&append_copy_kernel);
     // programmatic serialisation: the kernel waits on the device for its predecessor
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -51,7 +51,7 @@ int check_cache(const gqa_kv_cache_t* c) {
     if ((c->stride_block * es) % 16 || (c->stride_head * es) % 16 || (c->stride_token * es) % 16)
         return GQA_ERR_INVALID;
     if (!aligned16(c->k) || !aligned16(c->v)) return GQA_ERR_INVALID;
-    if (c->dtype == GQA_DTYPE_I8) {
+    if (dtype_coded(c->dtype)) {
         if (!c->k_scale || !c->v_scale) return GQA_ERR_INVALID;
         if (!aligned16(c->k_scale) || !aligned16(c->v_scale)) return GQA_ERR_INVALID;
     }
@@ -69,7 +69,7 @@ bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* bas
         case GQA_DTYPE_F32: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; break;
         case GQA_DTYPE_F16: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; break;
         case GQA_DTYPE_BF16: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; break;
-        default: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;
+        default: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;   // one-byte codes
     }
     const int es = dtype_size(c.dtype);
     // outer axes: 0 slot, 1 kv-head, 2 block; sort by stride
@@ -128,7 +128,7 @@ int gqa_kv_append(const gqa_kv_cache_t* cache, const void* k_new, const void* v_
     if (!k_new || !v_new || !block_tables || !positions) return GQA_ERR_INVALID;
     if (!aligned16(k_new) || !aligned16(v_new)) return GQA_ERR_INVALID;
     if ((long long)max_blocks_per_seq * GQA_BLOCK_SIZE > 0x7fffffffLL) return GQA_ERR_INVALID;
-    if (cache->dtype == GQA_DTYPE_I8) {
+    if (dtype_coded(cache->dtype)) {
         if (new_dtype != GQA_DTYPE_F32 && new_dtype != GQA_DTYPE_F16 && new_dtype != GQA_DTYPE_BF16)
             return GQA_ERR_UNSUPPORTED;
     } else if (new_dtype != cache->dtype) {
@@ -170,7 +170,7 @@ int gqa_decode(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int3
     if (out_dtype != GQA_DTYPE_F32 && out_dtype != GQA_DTYPE_BF16 && out_dtype != GQA_DTYPE_F16)
         return GQA_ERR_UNSUPPORTED;
     const int cd = cache->dtype;
-    const bool q_ok = (cd == GQA_DTYPE_I8) ? (q_dtype == GQA_DTYPE_BF16 || q_dtype == GQA_DTYPE_F16)
+    const bool q_ok = dtype_coded(cd) ? (q_dtype == GQA_DTYPE_BF16 || q_dtype == GQA_DTYPE_F16)
                                            : (q_dtype == cd);
     if (!q_ok) return GQA_ERR_UNSUPPORTED;
     int kernel = opts ? opts->kernel : 0;

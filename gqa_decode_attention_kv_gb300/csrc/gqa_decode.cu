@@ -96,20 +96,23 @@ constexpr int kHeadsPerWarp = 8;   // query heads one warp serves (the MMA N dim
 template <int kKind, typename T, int D, int kHeadWarps = 1>
 struct Cfg {
     static constexpr bool kI8 = std::is_same<T, int8_t>::value;
+    static constexpr bool kFp8 = std::is_same<T, __nv_fp8_e4m3>::value;
+    static constexpr bool kCoded = kI8 || kFp8;     // one-byte codes with fp16 scales
     static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     static constexpr int kEs = sizeof(T);
     static constexpr int kTile = 16 * D * kEs;                       // one (block, head) tile
-    static constexpr int kScaleBytes = kI8 ? 64 : 0;                // 16 k + 16 v fp16 scales
+    static constexpr int kScaleBytes = kCoded ? 64 : 0;             // 16 k + 16 v fp16 scales
     static constexpr int kStage = ((2 * kTile + kScaleBytes + 1023) / 1024) * 1024;
     static constexpr int kNw = kHeadWarps;
-    // The int8 kernel is issue-bound: the pool's bookkeeping costs it more than
-    // the tail it removes (measured), so it keeps the static partition.
-    static constexpr int kTailChunks = kI8 ? 0 : kMaxTailChunks;
+    // The coded-cache kernels are issue-bound: the pool's bookkeeping costs
+    // them more than the tail it removes (measured on int8), so they keep the
+    // static partition.
+    static constexpr int kTailChunks = kCoded ? 0 : kMaxTailChunks;
     // CTAs per SM the register budget is cut for. The int8 kernel is bound by
     // issue and latency and gains from 12 warps per SM; the bf16/f16 kernels
     // would spill at that budget and keep 8 (both measured).
     static constexpr int kMinCtas =
-        (kHeadWarps == 1 && kKind == kKernelMma && D == 128) ? (kI8 ? GQA_MIN_CTAS_PER_SM_I8 : 2) : 1;
+        (kHeadWarps == 1 && kKind == kKernelMma && D == 128) ? (kCoded ? GQA_MIN_CTAS_PER_SM_I8 : 2) : 1;
     static constexpr int kWarps = kHeadWarps == 1 ? GQA_WARPS_PER_CTA : kHeadWarps;
     static constexpr int kRings = kHeadWarps == 1 ? kWarps : 1;
     static constexpr int kStages =
@@ -122,7 +125,7 @@ struct Cfg {
     // log2 of how far the block maximum may exceed the running maximum before
     // the state is rescaled (0 = always exact). The int8 path folds the V
     // scale into the fp16 P operand, so it keeps P <= 1.
-    static constexpr float kRescaleSlack = kI8 ? 0.f : 8.f;
+    static constexpr float kRescaleSlack = kCoded ? 0.f : 8.f;
     static constexpr int kMt = D / 16;                              // m-tiles of the P.V product
     static constexpr int kRuns = D / 64;                            // 8-dim output runs per head
     static constexpr int kDpl = D / 32;                             // CUDA-core kernel: dims per lane
@@ -224,6 +227,21 @@ __device__ __forceinline__ void lds_row_as_float(uint32_t addr, float (&v)[N]) {
         } else {
             const uint2 x = lds64(addr);
             v[0] = __uint_as_float(x.x); v[1] = __uint_as_float(x.y);
+        }
+    } else if constexpr (std::is_same<T, __nv_fp8_e4m3>::value) {
+        uint32_t w;
+        if constexpr (N == 4) {
+            w = lds32(addr);
+        } else {
+            unsigned short h;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr));
+            w = h;
+        }
+#pragma unroll
+        for (int e = 0; e < N; e += 2) {
+            const float2 f = unpack2<false>(e4m3x2_to_f16x2(w >> (8 * e)));
+            v[e] = f.x;
+            v[e + 1] = f.y;
         }
     } else if constexpr (std::is_same<T, int8_t>::value) {
         uint32_t w;
@@ -332,7 +350,7 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int b, int g, 
     const uint16_t* base = static_cast<const uint16_t*>(a.q) + ((long long)b * a.H + (long long)g * a.G + r) * D;
 #pragma unroll
     for (int t = 0; t < D / 16; ++t) {
-        if constexpr (!C::kI8) {
+        if constexpr (!C::kCoded) {
             qf[t].x = __ldg(reinterpret_cast<const uint32_t*>(base + 16 * t + 2 * c));
             qf[t].y = __ldg(reinterpret_cast<const uint32_t*>(base + 16 * t + 2 * c + 8));
         } else {
@@ -349,7 +367,7 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int b, int g, 
 // Output dim of accumulator row (j, rh): row r + 8*rh of m-tile j.
 template <class C, int D>
 __device__ __forceinline__ int acc_dim(int j, int rh, int r) {
-    if constexpr (C::kI8) return 16 * r + 2 * j + rh;
+    if constexpr (C::kCoded) return 16 * r + 2 * j + rh;
     else return 16 * j + r + 8 * rh;
 }
 
@@ -372,7 +390,7 @@ template <class C, int D>
 __device__ __forceinline__ void mma_load(MmaFrags<C, D>& f, uint32_t stage, int lane, int r, int c) {
     const uint32_t sk = stage, sv = stage + C::kTile;
     const int mi = lane >> 3, rr = lane & 7;
-    if constexpr (!C::kI8) {
+    if constexpr (!C::kCoded) {
         // K: matrices (toks 0-7 | 8-15) x (dims 16t..+7 | +8..+15) = a0, a1, a2, a3
 #pragma unroll
         for (int t = 0; t < D / 16; ++t)
@@ -414,7 +432,7 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
 
     // ---- scores: S^T[tok][head] = K_tile . Q^T (two accumulators halve the chain)
     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (!C::kI8) {
+    if constexpr (!C::kCoded) {
 #pragma unroll
         for (int t = 0; t < D / 16; ++t) {
             if (t & 1) mma_t<kB>(sb, f.k[t][0], f.k[t][1], f.k[t][2], f.k[t][3], st.qf[t].x, st.qf[t].y);
@@ -424,17 +442,24 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
 #pragma unroll
         for (int t = 0; t < D / 32; ++t) {
             uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
-            i8x4_to_f16x4(f.k[t][0], l0, h0);          // tok r,   chunk 2t
-            i8x4_to_f16x4(f.k[t][1], l1, h1);          // tok r+8, chunk 2t
-            i8x4_to_f16x4(f.k[t][2], l2, h2);          // tok r,   chunk 2t+1
-            i8x4_to_f16x4(f.k[t][3], l3, h3);          // tok r+8, chunk 2t+1
+            if constexpr (C::kFp8) {
+                e4m3x4_to_f16x4(f.k[t][0], l0, h0);        // tok r,   chunk 2t
+                e4m3x4_to_f16x4(f.k[t][1], l1, h1);        // tok r+8, chunk 2t
+                e4m3x4_to_f16x4(f.k[t][2], l2, h2);        // tok r,   chunk 2t+1
+                e4m3x4_to_f16x4(f.k[t][3], l3, h3);        // tok r+8, chunk 2t+1
+            } else {
+                i8x4_to_f16x4(f.k[t][0], l0, h0);
+                i8x4_to_f16x4(f.k[t][1], l1, h1);
+                i8x4_to_f16x4(f.k[t][2], l2, h2);
+                i8x4_to_f16x4(f.k[t][3], l3, h3);
+            }
             mma_f16(sa, l0, l1, h0, h1, st.qf[2 * t].x, st.qf[2 * t].y);
             mma_f16(sb, l2, l3, h2, h3, st.qf[2 * t + 1].x, st.qf[2 * t + 1].y);
         }
     }
     // fragment: [0] = (tok r, head 2c), [1] = (tok r, head 2c+1), [2]/[3] = tok r+8
     float kr = scale_log2, kr8 = scale_log2, vr_s = 1.f, vr8_s = 1.f;
-    if constexpr (C::kI8) {
+    if constexpr (C::kCoded) {
         kr = f.ks_r * scale_log2;
         kr8 = f.ks_r8 * scale_log2;
         vr_s = f.vs_r;
@@ -482,7 +507,7 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
     const uint32_t bl1 = __byte_perm(__shfl_sync(kFull, lr8, srcA), __shfl_sync(kFull, lr8, srcB), sel);
 
     // ---- O^T[dim][head] += V^T . P^T (high part, then low part)
-    if constexpr (!C::kI8) {
+    if constexpr (!C::kCoded) {
         if (nvalid < kBlock) {
             // zero V of tokens past the end: the slots hold arbitrary (even NaN) bits
             const uint32_t m01 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
@@ -510,16 +535,22 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
         // A fragment of m-tile j = 2w + e (dims 16r + 4w + 2e, +1) for the token
         // pair (x, y): interleave the two tokens' bytes, then widen each byte to
         // f16 exactly (1024 + (code ^ 0x80) - 1152).
+        // (e4m3 codes: the interleaved byte pairs convert directly, exactly.)
         const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
         auto widen = [&](uint32_t t, uint32_t sel) -> uint32_t {
-            const uint32_t hv = __byte_perm(t, 0x64646464u, sel);
-            __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&hv), bias);
-            return as_u32(h);
+            if constexpr (C::kFp8) {
+                return e4m3x2_to_f16x2(sel == 0x4140 ? t : t >> 16);
+            } else {
+                const uint32_t hv = __byte_perm(t, 0x64646464u, sel);
+                __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&hv), bias);
+                return as_u32(h);
+            }
         };
+        const uint32_t flip = C::kFp8 ? 0u : 0x80808080u;
 #pragma unroll
         for (int wd = 0; wd < 4; ++wd) {
-            const uint32_t x0 = f.v[0][wd] ^ 0x80808080u, y0 = f.v[1][wd] ^ 0x80808080u;
-            const uint32_t x1 = f.v[2][wd] ^ 0x80808080u, y1 = f.v[3][wd] ^ 0x80808080u;
+            const uint32_t x0 = f.v[0][wd] ^ flip, y0 = f.v[1][wd] ^ flip;
+            const uint32_t x1 = f.v[2][wd] ^ flip, y1 = f.v[3][wd] ^ flip;
             // bytes (x.b0, y.b0, x.b1, y.b1) and (x.b2, y.b2, x.b3, y.b3)
             const uint32_t lo0 = __byte_perm(x0, y0, 0x5140), hi0 = __byte_perm(x0, y0, 0x7362);
             const uint32_t lo1 = __byte_perm(x1, y1, 0x5140), hi1 = __byte_perm(x1, y1, 0x7362);
@@ -616,7 +647,7 @@ __device__ __forceinline__ void fma_block(const DecodeArgs& a, FmaState<C, D>& s
         lds_row_as_float<T, kN>(sk + t * D * C::kEs + lane * kN * C::kEs, kf);
         lds_row_as_float<T, kN>(sv + t * D * C::kEs + lane * kN * C::kEs, vf);
         float ksc = a.scale_log2, vsc = 1.f;
-        if constexpr (C::kI8) {
+        if constexpr (C::kCoded) {
             unsigned short hk, hv;
             asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hk) : "r"(stage + 2 * C::kTile + 2 * t));
             asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(stage + 2 * C::kTile + 32 + 2 * t));
@@ -868,7 +899,7 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 #pragma unroll
                 for (int x = 0; x < C::kNumBox; ++x)
                     tma_load_4d(dst + C::kTile + x * C::kBoxBytes, &vmap, x * C::kBoxInner, y, z, ww, bar, pol);
-                if constexpr (C::kI8) {
+                if constexpr (C::kCoded) {
                     const long long si = ((long long)ph * a.K + gg) * kBlock;
                     bulk_load(dst + 2 * C::kTile, a.k_scale + si, 32, bar, pol);
                     bulk_load(dst + 2 * C::kTile + 32, a.v_scale + si, 32, bar, pol);
@@ -1141,7 +1172,8 @@ Variant pick_width(int nw) {
 template <typename T, int D>
 bool pick_kind(int kind, int nw, Variant& v) {
     if (kind == kKernelMma) {
-        if constexpr (std::is_same<T, float>::value || (std::is_same<T, int8_t>::value && D != 128)) {
+        if constexpr (std::is_same<T, float>::value ||
+                      ((std::is_same<T, int8_t>::value || std::is_same<T, __nv_fp8_e4m3>::value) && D != 128)) {
             return false;
         } else {
             v = pick_width<kKernelMma, T, D>(nw);
@@ -1222,6 +1254,7 @@ size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int he
         if (pick_dim<__half>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
         if (pick_dim<__nv_bfloat16>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
         if (pick_dim<int8_t>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
+        if (pick_dim<__nv_fp8_e4m3>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
     }
     if (P == 0) P = num_sms * (kMaxWarpsPerSm / nw);      // no occupancy answer: the hard bound
     return ws_layout(batch, num_kv_heads, G, head_dim,
@@ -1232,7 +1265,7 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     const gqa_kv_cache_t& c = *L.cache;
     const int D = c.head_dim, K = c.num_kv_heads, G = L.num_heads / K;
     int kind = L.kernel;
-    if (kind == 0) kind = (c.dtype == GQA_DTYPE_F32 || (c.dtype == GQA_DTYPE_I8 && D != 128)) ? kKernelFma : kKernelMma;
+    if (kind == 0) kind = (c.dtype == GQA_DTYPE_F32 || (dtype_coded(c.dtype) && D != 128)) ? kKernelFma : kKernelMma;
     const int nw = G <= 8 ? 1 : G <= 16 ? 2 : G <= 32 ? 4 : 8;   // warps sharing one group's tiles
     Variant v{};
     bool ok = false;
@@ -1241,6 +1274,7 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
         case GQA_DTYPE_F16: ok = pick_dim<__half>(kind, D, nw, v); break;
         case GQA_DTYPE_BF16: ok = pick_dim<__nv_bfloat16>(kind, D, nw, v); break;
         case GQA_DTYPE_I8: ok = pick_dim<int8_t>(kind, D, nw, v); break;
+        case GQA_DTYPE_FP8_E4M3: ok = pick_dim<__nv_fp8_e4m3>(kind, D, nw, v); break;
         default: ok = false;
     }
     if (!ok) return GQA_ERR_UNSUPPORTED;

@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -227,6 +228,18 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
     lo = as_u32(ha);
     hi = as_u32(hb);
+}
+
+// Two e4m3 codes (16 bits, element 0 in the low byte) -> f16 pair, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// Four e4m3 codes (one 32-bit word) -> two f16 pairs (elements 0,1 and 2,3).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    lo = e4m3x2_to_f16x2(w);
+    hi = e4m3x2_to_f16x2(w >> 16);
 }
 
 }  // namespace gqa

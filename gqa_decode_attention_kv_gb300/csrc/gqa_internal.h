@@ -15,9 +15,13 @@ inline int dtype_size(int dt) {
         case GQA_DTYPE_F16: return 2;
         case GQA_DTYPE_BF16: return 2;
         case GQA_DTYPE_I8: return 1;
+        case GQA_DTYPE_FP8_E4M3: return 1;
         default: return 0;
     }
 }
+
+// One-byte code caches with per-(token, kv-head) fp16 scales.
+inline bool dtype_coded(int dt) { return dt == GQA_DTYPE_I8 || dt == GQA_DTYPE_FP8_E4M3; }
 
 // Which split-KV kernel runs.
 enum KernelKind { kKernelMma = 1, kKernelFma = 2 };

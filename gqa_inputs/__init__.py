@@ -32,8 +32,10 @@ import torch
 BLOCK_SIZE = 16
 
 # dtype names shared with the C-ABI enum (gqa_dtype_t in include/gqa_decode.h)
-DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "i8": torch.int8}
-DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3}
+DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "i8": torch.int8,
+          "fp8": torch.float8_e4m3fn}
+DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3, "fp8": 4}
+CODED = ("i8", "fp8")        # one-byte code caches with per-(token, kv-head) fp16 scales
 
 @dataclasses.dataclass(frozen=True)
 class Workload:
@@ -43,7 +45,7 @@ class Workload:
     num_heads: int
     num_kv_heads: int
     head_dim: int
-    cache_dtype: str            # "f32" | "f16" | "bf16" | "i8"
+    cache_dtype: str            # "f32" | "f16" | "bf16" | "i8" | "fp8"
     q_dtype: str                # "f32" | "f16" | "bf16"
     lens: str                   # "fixed:<a,b,...>" | "const:<S>" | "uniform:<lo>:<hi>"
     contiguous: bool = False    # un-paged [B, S_pad, K, d] buffer + identity table
@@ -68,6 +70,8 @@ WORKLOADS = {
                                          "bf16", "bf16", "const:131072"),
     "int8kv_b128_ragged": Workload("int8kv_b128_ragged", 128, 64, 8, 128, "i8", "bf16",
                                    "uniform:2048:8192"),
+    "fp8kv_b128_ragged": Workload("fp8kv_b128_ragged", 128, 64, 8, 128, "fp8", "bf16",
+                                  "uniform:2048:8192"),
 }
 
 
@@ -142,11 +146,13 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
     leaves room to append a token at position ``lens[b]``.
     Values: Q, K, V ~ N(0, 1) rounded to their storage dtype; int8 caches hold
     uniform codes in [-127, 127] with fp16 scales in [0.015, 0.035] (the scale a
-    row of 128 N(0,1) draws gets from its max magnitude)."""
+    row of 128 N(0,1) draws gets from its max magnitude); FP8 caches hold e4m3
+    codes of N(0, 128^2) draws clipped to +-448 with fp16 scales in
+    [0.006, 0.010]."""
     if q_dtype is None:
-        q_dtype = "bf16" if cache_dtype == "i8" else cache_dtype
+        q_dtype = "bf16" if cache_dtype in CODED else cache_dtype
     if new_dtype is None:
-        new_dtype = q_dtype if cache_dtype == "i8" else cache_dtype
+        new_dtype = q_dtype if cache_dtype in CODED else cache_dtype
     lens_t = torch.as_tensor(lens, dtype=torch.int32).reshape(-1).cpu()
     if lens_t.numel() != batch:
         raise ValueError("lens must have one entry per sequence")
@@ -185,6 +191,14 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
         sshape = (num_blocks, K, bs)
         ks = (torch.rand(sshape, generator=gen_dev, device=dev) * 0.02 + 0.015).to(torch.float16)
         vs = (torch.rand(sshape, generator=gen_dev, device=dev) * 0.02 + 0.015).to(torch.float16)
+    elif cache_dtype == "fp8":
+        def codes():
+            x = torch.randn(shape, generator=gen_dev, device=dev) * 128.0
+            return x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
+        kc, vc = codes(), codes()
+        sshape = (num_blocks, K, bs)
+        ks = (torch.rand(sshape, generator=gen_dev, device=dev) * 0.004 + 0.006).to(torch.float16)
+        vs = (torch.rand(sshape, generator=gen_dev, device=dev) * 0.004 + 0.006).to(torch.float16)
     else:
         dt = DTYPES[cache_dtype]
         kc = _randn(shape, gen_dev, dev, dt)
@@ -224,7 +238,7 @@ def _poison_unowned(kc, vc, ks, vs, table, lens, contiguous, cache_dtype):
         mask = bad_tok[:, :, None, None].expand_as(kc)
     else:
         mask = bad[:, None, :, None].expand_as(kc)
-    if cache_dtype == "i8":
+    if cache_dtype in CODED:
         smask = bad[:, None, :].expand_as(ks)
         ks.masked_fill_(smask, float("nan"))
         vs.masked_fill_(smask, float("nan"))

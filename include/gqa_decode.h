@@ -47,7 +47,8 @@ typedef enum {
     GQA_DTYPE_F32 = 0,
     GQA_DTYPE_F16 = 1,
     GQA_DTYPE_BF16 = 2,
-    GQA_DTYPE_I8 = 3          /* cache only: int8 codes + one fp16 scale per (token, kv-head) */
+    GQA_DTYPE_I8 = 3,         /* cache only: int8 codes + one fp16 scale per (token, kv-head) */
+    GQA_DTYPE_FP8_E4M3 = 4    /* cache only: e4m3 codes (max 448) + one fp16 scale per (token, kv-head) */
 } gqa_dtype_t;
 
 /* Return codes. */
@@ -77,9 +78,10 @@ typedef enum {
  * stride_head = d, stride_token = K*d and the identity block table
  * table[b][j] = b*(S_pad/16) + j.
  *
- * For GQA_DTYPE_I8, k_scale / v_scale hold one fp16 scale per (block, kv-head,
- * slot) as [num_blocks, K, 16]; the cached value is code * scale. Other dtypes
- * leave them NULL.
+ * For the coded caches (GQA_DTYPE_I8, GQA_DTYPE_FP8_E4M3), k_scale / v_scale
+ * hold one fp16 scale per (block, kv-head, slot) as [num_blocks, K, 16]; the
+ * cached value is code * scale (an int8 code, or the value of an e4m3 code).
+ * Other dtypes leave them NULL.
  *
  * Requirements: block_size == 16; head_dim in {64, 128}; k, v, k_scale,
  * v_scale 16-byte aligned; every stride times the element size a multiple of
@@ -88,8 +90,8 @@ typedef enum {
 typedef struct {
     void   *k;                /* device */
     void   *v;                /* device */
-    void   *k_scale;          /* device, fp16 [num_blocks, K, 16], I8 only */
-    void   *v_scale;          /* device, fp16 [num_blocks, K, 16], I8 only */
+    void   *k_scale;          /* device, fp16 [num_blocks, K, 16], coded caches only */
+    void   *v_scale;          /* device, fp16 [num_blocks, K, 16], coded caches only */
     int64_t num_blocks;
     int32_t num_kv_heads;     /* K */
     int32_t block_size;       /* must be 16 */
@@ -139,7 +141,10 @@ GQA_API int64_t gqa_kv_pool_elements(int64_t num_blocks, int32_t num_kv_heads, i
  *                 device: amax = max|x| (fp32); s = fp16_rne(min(amax/127, 65504));
  *                 code = s == 0 ? 0 : clamp(rint(x/s), -127, 127) with IEEE fp32
  *                 division (symmetric int8, "LLM 推理性能优化实战" sections 15.1,
- *                 15.2, 15.5). The scale goes to k_scale / v_scale.
+ *                 15.2, 15.5). For an FP8_E4M3 cache likewise with
+ *                 s = fp16_rne(min(amax/448, 65504)) and code = e4m3 of x/s,
+ *                 rounded to nearest even and saturated to +-448 (the FP8 option
+ *                 of section 15.5). The scale goes to k_scale / v_scale.
  *  block_tables   device int32 [batch, max_blocks_per_seq].
  *  positions      device int32 [batch]: slot index of the new token, i.e. the
  *                 context length BEFORE the append. Not modified; the caller
@@ -172,7 +177,7 @@ GQA_API size_t gqa_decode_workspace_size(int32_t batch, int32_t num_heads, int32
  * (length 0) yields a zero output row.
  *
  *  q              device [batch, num_heads, head_dim]; BF16 for a BF16 cache,
- *                 F16 for F16, F32 for F32, BF16 or F16 for an I8 cache.
+ *                 F16 for F16, F32 for F32, BF16 or F16 for a coded cache.
  *  block_tables   device int32 [batch, max_blocks_per_seq].
  *  context_lens   device int32 [batch], lengths AFTER the append, each in
  *                 [0, max_blocks_per_seq*16].
@@ -186,7 +191,7 @@ GQA_API size_t gqa_decode_workspace_size(int32_t batch, int32_t num_heads, int32
  *                 share a workspace must not overlap on the GPU.
  *  opts           NULL or tuning knobs (gqa_decode_opts_t).
  *  Limits: num_heads % K == 0; num_heads / K <= 64 (groups above 8 need a
- *  BF16/F16/I8 cache with head_dim 128 for I8, or an F32 cache); batch <= 8191;
+ *  BF16/F16 cache, a coded cache with head_dim 128, or an F32 cache); batch <= 8191;
  *  batch * K * max_blocks_per_seq < 2^31.
  */
 GQA_API int gqa_decode(const gqa_kv_cache_t *cache, const void *q, int32_t q_dtype,

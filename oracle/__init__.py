@@ -17,6 +17,8 @@ Functions and the passages they follow:
 * ``quantize_int8`` / ``dequantize_int8`` -- symmetric per-(token, kv-head) int8,
                             "LLM 推理性能优化实战" sections 15.1, 15.2 and 15.5
                             (rounding rule in ``gqa_oracle.c``).
+* ``quantize_fp8`` / ``dequantize_fp8`` -- FP8 E4M3 KV codes with per-(token,
+                            kv-head) fp16 scales (section 15.5's FP8 option).
 * ``kv_cache_elements``  -- the KV-size closed form 2 * layers * K * d * S * B,
                             "分组查询注意力 (GQA)" 关键参数 item 2 and
                             "LLM 推理性能优化实战" section 6.1.
@@ -73,6 +75,14 @@ def _load():
             lib.oracle_f32_to_f16_bits.restype = ctypes.c_uint16
             lib.oracle_f16_bits_to_f32.argtypes = [ctypes.c_uint16]
             lib.oracle_f16_bits_to_f32.restype = ctypes.c_float
+            lib.oracle_quantize_fp8.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int64,
+                                                ctypes.c_int32, ctypes.POINTER(ctypes.c_uint8),
+                                                ctypes.POINTER(ctypes.c_uint16)]
+            lib.oracle_quantize_fp8.restype = None
+            lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+            lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+            lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_f64.restype = ctypes.c_double
             lib.oracle_num_cpus.argtypes = []
             lib.oracle_num_cpus.restype = ctypes.c_int
             _lib = lib
@@ -194,6 +204,38 @@ def quantize_int8(x) -> tuple[np.ndarray, np.ndarray]:
     _load().oracle_quantize_int8(_ptr(x, ctypes.c_float), rows, d,
                                  _ptr(codes, ctypes.c_int8), _ptr(scales, ctypes.c_uint16))
     return codes, scales
+
+
+def quantize_fp8(x) -> tuple[np.ndarray, np.ndarray]:
+    """Rows of x -> (e4m3 codes as uint8, fp16 scale bits as uint16)."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    d = x.shape[-1]
+    rows = x.size // d if d else 0
+    codes = np.empty(x.shape, dtype=np.uint8)
+    scales = np.empty(x.shape[:-1], dtype=np.uint16)
+    _load().oracle_quantize_fp8(_ptr(x, ctypes.c_float), rows, d,
+                                _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint16))
+    return codes, scales
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Exact values of e4m3 codes (uint8) as fp64 (NaN for the NaN codes)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    table = np.array([_load().oracle_e4m3_to_f64(i) for i in range(256)], dtype=np.float64)
+    return table[c]
+
+
+def f32_to_e4m3(x) -> np.ndarray:
+    """Nearest-even e4m3 codes of fp32 values, saturated to +-448."""
+    a = np.asarray(x, dtype=np.float32)
+    lib = _load()
+    return np.asarray([lib.oracle_f32_to_e4m3(float(v)) for v in a.reshape(-1)],
+                      dtype=np.uint8).reshape(a.shape)
+
+
+def dequantize_fp8(codes, scale_values) -> np.ndarray:
+    """e4m3(code) * scale in fp64 (exact)."""
+    return e4m3_to_f64(codes) * np.asarray(scale_values, dtype=np.float64)[..., None]
 
 
 def f16_bits_to_f64(bits) -> np.ndarray:

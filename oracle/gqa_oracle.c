@@ -28,6 +28,12 @@
  *    with fp32 IEEE division and round-half-to-even. Dequantisation is q_i * s
  *    evaluated exactly in fp64.
  *
+ *  - oracle_quantize_fp8 / oracle_f32_to_e4m3 / oracle_e4m3_to_f64: the FP8
+ *    (E4M3) KV cache named among the KV quantisation options of "LLM 推理性能优化实战"
+ *    section 15.5 (FP8 E4M3/E5M2 for long-tailed K/V): per-(token, kv-head) fp16
+ *    scale s = fp16_rne(min(amax/448, 65504)), codes = nearest-even e4m3 of x/s,
+ *    saturated to +-448. Decoding is exact in fp64.
+ *
  *  - oracle_f32_to_f16_bits / oracle_f16_bits_to_f32: IEEE 754 binary16
  *    conversion with round-to-nearest-even, written from the format's
  *    definition (1 sign, 5 exponent, 10 fraction bits, bias 15).
@@ -137,6 +143,66 @@ void oracle_quantize_int8(const float *x, int64_t rows, int32_t d,
                 q = (int32_t)rq;
             }
             codes[r * (int64_t)d + i] = (int8_t)q;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* FP8 E4M3 (the "fn" variant: no infinities, max 448) and its quantisation  */
+/* ------------------------------------------------------------------------- */
+
+/* Value of an e4m3 code: sign bit, 4 exponent bits (bias 7), 3 fraction bits;
+ * exponent 0 is subnormal (2^-6 * f/8); code S.1111.111 is NaN. */
+double oracle_e4m3_to_f64(uint8_t code)
+{
+    int sign = code >> 7, e = (code >> 3) & 15, f = code & 7;
+    if (e == 15 && f == 7) return NAN;
+    double v = e == 0 ? ldexp(f / 8.0, -6) : ldexp(1.0 + f / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Nearest e4m3 code to a finite float, ties to the even code, magnitudes
+ * beyond 448 saturated to 448 (the reading of "round to nearest even,
+ * saturate to finite"). Brute force over the 127 non-negative finite codes. */
+uint8_t oracle_f32_to_e4m3(float x)
+{
+    double a = fabs((double)x);
+    int best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 0x7e; ++c) {
+        double d = fabs(oracle_e4m3_to_f64((uint8_t)c) - a);
+        if (d < bd || (d == bd && (c & 1) == 0)) { bd = d; best = c; }
+    }
+    if (a >= 448.0) best = 0x7e;
+    return (uint8_t)(best | (signbit(x) ? 0x80 : 0));
+}
+
+/* Per-row FP8 quantisation with an fp16 scale (same rule as int8 with the
+ * code range of e4m3):
+ *   s = fp16_rne(min(amax / 448, 65504)); code_i = s == 0 ? 0 : e4m3(x_i / s). */
+void oracle_quantize_fp8(const float *x, int64_t rows, int32_t d, uint8_t *codes,
+                         uint16_t *scale_bits)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xr = x + r * (int64_t)d;
+        float amax = 0.0f;
+        for (int32_t i = 0; i < d; ++i) {
+            float a = fabsf(xr[i]);
+            if (a > amax) amax = a;
+        }
+        volatile float s32 = amax / 448.0f;
+        float s = s32;
+        if (s > 65504.0f) s = 65504.0f;
+        uint16_t sb = oracle_f32_to_f16_bits(s);
+        float sf = oracle_f16_bits_to_f32(sb);
+        scale_bits[r] = sb;
+        for (int32_t i = 0; i < d; ++i) {
+            uint8_t c = 0;
+            if (sf != 0.0f) {
+                volatile float t = xr[i] / sf;
+                c = oracle_f32_to_e4m3(t);
+            }
+            codes[r * (int64_t)d + i] = c;
         }
     }
 }

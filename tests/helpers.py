@@ -15,6 +15,8 @@ def _host(t: torch.Tensor) -> np.ndarray:
     t = t.detach()
     if t.dtype == torch.int8:
         return t.cpu().numpy()
+    if t.dtype == torch.float8_e4m3fn:
+        return t.cpu().view(torch.uint8).numpy()       # raw codes; the oracle decodes them
     return t.float().cpu().numpy()
 
 
@@ -30,11 +32,17 @@ def oracle_for_case(case, rows=None, nthreads: int = 0, host_pools=None) -> np.n
                              case.stride_token, K, d, rows).astype(np.float64)
     vd = oracle.gather_dense(vp, table, lens, case.stride_block, case.stride_head,
                              case.stride_token, K, d, rows).astype(np.float64)
-    if case.cache_dtype == "i8":
+    if case.cache_dtype in ("i8", "fp8"):
         ks = oracle.gather_scales(case.k_scale.float().cpu().numpy(), table, lens, K, rows)
         vs = oracle.gather_scales(case.v_scale.float().cpu().numpy(), table, lens, K, rows)
-        kd = oracle.dequantize_int8(kd, ks)
-        vd = oracle.dequantize_int8(vd, vs)
+        if case.cache_dtype == "i8":
+            kd = oracle.dequantize_int8(kd, ks)
+            vd = oracle.dequantize_int8(vd, vs)
+        else:
+            kd = oracle.dequantize_fp8(oracle.gather_dense(kp, table, lens, case.stride_block,
+                                       case.stride_head, case.stride_token, K, d, rows), ks)
+            vd = oracle.dequantize_fp8(oracle.gather_dense(vp, table, lens, case.stride_block,
+                                       case.stride_head, case.stride_token, K, d, rows), vs)
     q = case.q.detach().float().cpu().numpy().astype(np.float64)[rows]
     return oracle.decode(q, kd, vd, lens[rows], case.scale, nthreads)
 

@@ -1,5 +1,5 @@
 """Paged KV append on the GPU, bit-exact against the oracle's host scatter (and,
-for int8 caches, against the oracle's quantiser). Calls go through the C ABI."""
+for int8 and FP8 caches, against the oracle's quantiser). Calls go through the C ABI."""
 import numpy as np
 import pytest
 import torch
@@ -48,11 +48,12 @@ def test_append_float_cache_is_bit_exact(gq, oracle_mod, dtype, d):
     assert np.array_equal(got_v, hv)
 
 
+@pytest.mark.parametrize("cache", ["i8", "fp8"])
 @pytest.mark.parametrize("in_dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("d", [128, 64])
-def test_append_int8_quantises_bit_exactly(gq, oracle_mod, in_dtype, d):
+def test_append_coded_cache_quantises_bit_exactly(gq, oracle_mod, cache, in_dtype, d):
     lens = [3, 16, 40, 1, 0, 255]
-    case = gi.make_case(len(lens), 16, 8, d, lens, "i8", q_dtype="bf16", seed=12, device="cuda",
+    case = gi.make_case(len(lens), 16, 8, d, lens, cache, q_dtype="bf16", seed=12, device="cuda",
                         extra_tokens=1, new_dtype=in_dtype)
     # a few awkward rows: all zeros, a tiny-magnitude row, a large one
     kn = case.k_new.clone()
@@ -60,22 +61,23 @@ def test_append_int8_quantises_bit_exactly(gq, oracle_mod, in_dtype, d):
     kn[1, 1] *= 1e-6
     kn[2, 2] *= 300.0
     case.k_new = kn
-    cache = gq.cache_from_case(case)
     before = [_raw(t).copy() for t in (case.k_cache, case.v_cache, case.k_scale, case.v_scale)]
-    gq.kv_append(cache, case.k_new, case.v_new, case.block_table, case.context_lens.clone())
+    gq.kv_append(gq.cache_from_case(case), case.k_new, case.v_new, case.block_table,
+                 case.context_lens.clone())
     torch.cuda.synchronize()
     table = case.block_table.cpu().numpy()
-    hk = before[0].view(np.int8).copy()
-    hv = before[1].view(np.int8).copy()
+    quantize = oracle_mod.quantize_int8 if cache == "i8" else oracle_mod.quantize_fp8
+    hk = before[0].view(np.uint8).copy()
+    hv = before[1].view(np.uint8).copy()
     hks = before[2].view(np.uint16).reshape(case.k_scale.shape).copy()
     hvs = before[3].view(np.uint16).reshape(case.v_scale.shape).copy()
     for new, pool, sc in ((case.k_new, hk, hks), (case.v_new, hv, hvs)):
-        codes, sbits = oracle_mod.quantize_int8(new.float().cpu().numpy())
-        oracle_mod.append(pool, codes, table, lens, case.stride_block, case.stride_head,
-                          case.stride_token)
+        codes, sbits = quantize(new.float().cpu().numpy())
+        oracle_mod.append(pool, codes.view(np.uint8), table, lens, case.stride_block,
+                          case.stride_head, case.stride_token)
         oracle_mod.append_scales(sc, sbits, table, lens)
-    assert np.array_equal(_raw(case.k_cache).view(np.int8), hk)
-    assert np.array_equal(_raw(case.v_cache).view(np.int8), hv)
+    assert np.array_equal(_raw(case.k_cache), hk)
+    assert np.array_equal(_raw(case.v_cache), hv)
     assert np.array_equal(_raw(case.k_scale).view(np.uint16).reshape(hks.shape), hks)
     assert np.array_equal(_raw(case.v_scale).view(np.uint16).reshape(hvs.shape), hvs)
 

@@ -92,6 +92,22 @@ def test_int8_cache(gq, kernel, d):
         assert max_abs_err(out, ref) <= TOL
 
 
+@pytest.mark.parametrize("kernel,d", [(1, 128), (2, 128), (2, 64)])
+def test_fp8_cache(gq, kernel, d):
+    lens = [1, 16, 17, 300, 2047, 0, 64]
+    case = gi.make_case(len(lens), 64, 8, d, lens, "fp8", q_dtype="bf16", seed=36, device="cuda")
+    ref = oracle_for_case(case)
+    for mw in (0, 3):
+        out = _run(gq, case, kernel=kernel, max_warps=mw, min_blocks_per_warp=1)
+        assert max_abs_err(out, ref) <= TOL
+
+
+def test_fp8_wide_group_f16_query(gq):
+    lens = [33, 700, 5]
+    case = gi.make_case(3, 64, 4, 128, lens, "fp8", q_dtype="f16", seed=37, device="cuda")
+    assert max_abs_err(_run(gq, case), oracle_for_case(case)) <= TOL
+
+
 def test_int8_cache_with_f16_query(gq):
     lens = [40, 333]
     case = gi.make_case(2, 32, 8, 128, lens, "i8", q_dtype="f16", seed=23, device="cuda")
@@ -258,7 +274,11 @@ def _sampled(gq, wl, rows, seed=0, **kw):
 
 def _host_pools(case):
     def host(t):
-        return t.cpu().numpy() if t.dtype == torch.int8 else t.float().cpu().numpy()
+        if t.dtype == torch.int8:
+            return t.cpu().numpy()
+        if t.dtype == torch.float8_e4m3fn:
+            return t.cpu().view(torch.uint8).numpy()
+        return t.float().cpu().numpy()
     return host(case.k_cache), host(case.v_cache)
 
 
@@ -267,6 +287,7 @@ def _host_pools(case):
     ("llama70b_bf16_b32_ragged", [0, 5, 31]),
     ("long_ctx_bf16_b1_s131072", [0]),
     ("int8kv_b128_ragged", [0, 64, 127]),
+    ("fp8kv_b128_ragged", [0, 77, 127]),
 ])
 def test_full_size_workloads_sampled(gq, name, rows):
     assert _sampled(gq, gi.WORKLOADS[name], rows) <= TOL

@@ -296,3 +296,51 @@ def test_generator_poisons_only_unowned_slots(oracle_mod):
         assert np.isfinite(dense[b, :L]).all()
     owned = 5 + 16 + 33
     assert np.count_nonzero(~np.isnan(pool)) == owned * 2 * 16
+
+
+# --------------------------------------------------------------------------- fp8 (e4m3)
+
+
+def test_e4m3_decoding_matches_torch_for_every_code(oracle_mod):
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle_mod.e4m3_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref)) and np.isnan(mine).sum() == 2
+    np.testing.assert_array_equal(mine[~np.isnan(mine)], ref[~np.isnan(ref)])
+    assert oracle_mod.e4m3_to_f64(np.uint8(0x7E)) == 448.0          # largest finite value
+    assert oracle_mod.e4m3_to_f64(np.uint8(0x01)) == 2.0 ** -9       # smallest subnormal
+
+
+def test_e4m3_rounding_matches_torch_in_range(oracle_mod):
+    rng = np.random.default_rng(41)
+    x = np.concatenate([
+        (rng.standard_normal(20000) * 10.0 ** rng.integers(-4, 3, 20000)).astype(np.float32),
+        # exact midpoints between neighbouring codes: ties must go to the even code
+        np.array([(oracle_mod.e4m3_to_f64(np.uint8(c)) + oracle_mod.e4m3_to_f64(np.uint8(c + 1))) / 2
+                  for c in range(0, 0x7E)], dtype=np.float32),
+    ]).clip(-460.0, 460.0)
+    mine = oracle_mod.f32_to_e4m3(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(mine, ref)
+    # beyond the range the reading saturates to +-448
+    assert oracle_mod.f32_to_e4m3(np.float32(1e6)) == 0x7E
+    assert oracle_mod.f32_to_e4m3(np.float32(-1e6)) == 0xFE
+
+
+def test_fp8_quantisation_invariants(oracle_mod):
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal((300, 128)).astype(np.float32) * np.float32(10.0) ** rng.integers(-2, 3, (300, 1))
+    codes, sbits = oracle_mod.quantize_fp8(x)
+    s = oracle_mod.f16_bits_to_f64(sbits)
+    vals = oracle_mod.e4m3_to_f64(codes)
+    # each row's largest magnitude lands on +-448 (scale is amax/448 to fp16 precision)
+    assert np.all(np.abs(vals).max(axis=1) == 448.0)
+    # relative error of each element within half an e4m3 step (2^-4) above the subnormals
+    recon = vals * s[:, None]
+    big = np.abs(x) >= 2.0 ** -6 * s[:, None]
+    assert np.all(np.abs(recon - x)[big] <= np.abs(x)[big] * 2.0 ** -4 * 1.0001)
+    c2, s2 = oracle_mod.quantize_fp8(-x)
+    np.testing.assert_array_equal(c2 ^ 0x80, codes)                 # sign bit only
+    np.testing.assert_array_equal(s2, sbits)
+    cz, sz = oracle_mod.quantize_fp8(np.zeros((1, 64), dtype=np.float32))
+    assert sz[0] == 0 and not cz.any()
