@@ -63,9 +63,9 @@ def _load():
             lib = ctypes.CDLL(build())
             dp = ctypes.POINTER(ctypes.c_double)
             ip = ctypes.POINTER(ctypes.c_int32)
-            lib.oracle_gqa_decode.argtypes = [dp, dp, dp, ip, ctypes.c_int32, ctypes.c_int32,
-                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                              ctypes.c_double, dp, ctypes.c_int32]
+            i32 = ctypes.c_int32
+            lib.oracle_gqa_decode.argtypes = [dp, dp, dp, ip, i32, i32, i32, i32, i32, i32, i32,
+                                              ctypes.c_double, dp, i32]
             lib.oracle_gqa_decode.restype = ctypes.c_int
             lib.oracle_quantize_int8.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int64,
                                                  ctypes.c_int32, ctypes.POINTER(ctypes.c_int8),
@@ -97,28 +97,35 @@ def _ptr(a: np.ndarray, ctype):
     return a.ctypes.data_as(ctypes.POINTER(ctype))
 
 
-def decode(q, k, v, lens, scale: float, nthreads: int = 0) -> np.ndarray:
-    """o[b,h,:] = softmax(scale * q[b,h] . K[b,:lens[b],g]^T) V[b,:lens[b],g], g = h // (H/K).
+def decode(q, k, v, lens, scale: float, nthreads: int = 0, window: int = 0) -> np.ndarray:
+    """Attention of each sequence's new token(s) over its cache, from the definition.
 
-    q: [B, H, d]; k, v: dense [B, S_max, K, d]; lens: [B]. Inputs are converted to
-    fp64 exactly (bf16/fp16/fp32 values are all representable). Returns fp64 [B, H, d].
+    q: [B, H, d] (one new token per sequence) or [B, T, H, d] (T new tokens);
+    k, v: dense [B, S_max, K, d]; lens: [B], counting the new tokens. Query i of
+    sequence b sits at position lens[b] - T + i and attends positions up to its
+    own (causal among the new tokens), the last ``window`` of them when window > 0.
+    Head h reads KV head h // (H/K). Inputs are converted to fp64 exactly
+    (bf16/fp16/fp32 values are all representable). Returns fp64 shaped like q.
     """
     q = np.ascontiguousarray(np.asarray(q, dtype=np.float64))
     k = np.ascontiguousarray(np.asarray(k, dtype=np.float64))
     v = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
     lens = np.ascontiguousarray(np.asarray(lens, dtype=np.int32))
-    B, H, d = q.shape
+    single = q.ndim == 3
+    q4 = q[:, None] if single else q
+    B, T, H, d = q4.shape
+    q4 = np.ascontiguousarray(q4)
     if k.ndim != 4 or k.shape[0] != B or k.shape[3] != d or v.shape != k.shape:
         raise ValueError("k/v must be [B, S_max, K, d] matching q")
     S_max, K = k.shape[1], k.shape[2]
-    out = np.empty((B, H, d), dtype=np.float64)
-    rc = _load().oracle_gqa_decode(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+    out = np.empty((B, T, H, d), dtype=np.float64)
+    rc = _load().oracle_gqa_decode(_ptr(q4, ctypes.c_double), _ptr(k, ctypes.c_double),
                                    _ptr(v, ctypes.c_double), _ptr(lens, ctypes.c_int32),
-                                   B, H, K, d, S_max, float(scale),
+                                   B, T, H, K, d, S_max, int(window), float(scale),
                                    _ptr(out, ctypes.c_double), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_gqa_decode failed with {rc}")
-    return out
+    return out[:, 0] if single else out
 
 
 def gather_dense(pool, block_table, lens, stride_block: int, stride_head: int,

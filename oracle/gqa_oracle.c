@@ -7,7 +7,7 @@
  *
  * What it computes, and where the pages define it:
  *
- *  - oracle_gqa_decode: grouped-query attention for one new token per sequence,
+ *  - oracle_gqa_decode: grouped-query attention for the new token(s) of each sequence,
  *    "分组查询注意力 (GQA)", section 技术原理, steps 2-4 and the attention
  *    equation softmax(Q_group K_g^T / sqrt(d_k)) V_g. Query head h uses KV head
  *    g = h / (H/K) (the [K, H/K] reshape of step 2; the head mapping j = i // 4
@@ -17,6 +17,17 @@
  *    num_kv_heads, head_dim] index of "LLM 推理性能优化实战", section 7.3).
  *    An empty context (length 0) yields a zero output (reading: the pages never
  *    decode an empty sequence).
+ *    Two widenings of the same definition, each only a change of the attended
+ *    token range:
+ *      * T >= 1 new tokens per sequence (speculative verification, "LLM 推理性能
+ *        优化实战" section 14.2; chunked prefill mixed with decode, section
+ *        11.7): the T queries of sequence b sit at positions lens[b]-T .. lens[b]-1
+ *        (lens counts the new tokens) and query i attends positions
+ *        0 .. lens[b]-T+i, causal among the new tokens. A query whose position
+ *        is negative (lens[b] < T) attends nothing and yields zeros.
+ *      * a sliding window W > 0 (section 6.4.1: only the most recent N tokens
+ *        are attended): each query attends the last W positions up to and
+ *        including its own. W = 0 is full attention.
  *
  *  - oracle_quantize_int8: symmetric int8 quantisation with one scale per
  *    (token, kv-head) row ("LLM 推理性能优化实战", section 15.1: symmetric range
@@ -214,44 +225,47 @@ void oracle_quantize_fp8(const float *x, int64_t rows, int32_t d, uint8_t *codes
 typedef struct {
     const double *q, *k, *v;
     const int32_t *lens;
-    int32_t B, H, K, d, S_max;
+    int32_t B, T, H, K, d, S_max, window;
     double scale;
     double *out;
-    int64_t next;              /* next (b, h) work item, shared */
+    int64_t next;              /* next (b, i, h) work item, shared */
     pthread_mutex_t lock;
 } decode_job;
 
-/* One (b, h) output row, straight from the definition. */
-static void decode_one(const decode_job *J, int32_t b, int32_t h, double *s)
+/* One (b, i, h) output row (query i of sequence b, head h), straight from the
+ * definition over the attended positions [lo, hi). */
+static void decode_one(const decode_job *J, int32_t b, int32_t i, int32_t h, double *s)
 {
     const int32_t G = J->H / J->K;
     const int32_t g = h / G;                     /* query head h reads KV head h / (H/K) */
     const int32_t d = J->d, K = J->K;
-    const int32_t n = J->lens[b];
-    const double *qh = J->q + ((int64_t)b * J->H + h) * d;
-    double *o = J->out + ((int64_t)b * J->H + h) * d;
+    const int64_t row = ((int64_t)b * J->T + i) * J->H + h;
+    const double *qh = J->q + row * d;
+    double *o = J->out + row * d;
 
-    for (int32_t i = 0; i < d; ++i) o[i] = 0.0;
-    if (n <= 0) return;
+    for (int32_t e = 0; e < d; ++e) o[e] = 0.0;
+    const int32_t hi = J->lens[b] - J->T + i + 1;          /* own position + 1 */
+    if (hi <= 0) return;
+    const int32_t lo = (J->window > 0 && hi > J->window) ? hi - J->window : 0;
 
     /* scores s_t = scale * <q_h, k_{t,g}> */
     double mx = -INFINITY;
-    for (int32_t t = 0; t < n; ++t) {
+    for (int32_t t = lo; t < hi; ++t) {
         const double *kt = J->k + (((int64_t)b * J->S_max + t) * K + g) * d;
         double acc = 0.0;
-        for (int32_t i = 0; i < d; ++i) acc += qh[i] * kt[i];
+        for (int32_t e = 0; e < d; ++e) acc += qh[e] * kt[e];
         s[t] = J->scale * acc;
         if (s[t] > mx) mx = s[t];
     }
     /* softmax weights and the weighted sum of values */
     double denom = 0.0;
-    for (int32_t t = 0; t < n; ++t) {
+    for (int32_t t = lo; t < hi; ++t) {
         double w = exp(s[t] - mx);
         denom += w;
         const double *vt = J->v + (((int64_t)b * J->S_max + t) * K + g) * d;
-        for (int32_t i = 0; i < d; ++i) o[i] += w * vt[i];
+        for (int32_t e = 0; e < d; ++e) o[e] += w * vt[e];
     }
-    for (int32_t i = 0; i < d; ++i) o[i] /= denom;
+    for (int32_t e = 0; e < d; ++e) o[e] /= denom;
 }
 
 static void *decode_worker(void *arg)
@@ -259,13 +273,14 @@ static void *decode_worker(void *arg)
     decode_job *J = (decode_job *)arg;
     double *s = (double *)malloc(sizeof(double) * (size_t)(J->S_max > 0 ? J->S_max : 1));
     if (!s) return (void *)1;
-    const int64_t total = (int64_t)J->B * J->H;
+    const int64_t total = (int64_t)J->B * J->T * J->H;
     for (;;) {
         pthread_mutex_lock(&J->lock);
         int64_t it = J->next++;
         pthread_mutex_unlock(&J->lock);
         if (it >= total) break;
-        decode_one(J, (int32_t)(it / J->H), (int32_t)(it % J->H), s);
+        const int64_t bi = it / J->H;
+        decode_one(J, (int32_t)(bi / J->T), (int32_t)(bi % J->T), (int32_t)(it % J->H), s);
     }
     free(s);
     return NULL;
@@ -277,22 +292,23 @@ int oracle_num_cpus(void)
     return n > 0 ? (int)n : 1;
 }
 
-/* q [B,H,d], k/v [B,S_max,K,d], lens [B], out [B,H,d]; all fp64, host memory.
- * nthreads <= 0 uses every online CPU. Returns 0, or -1 on bad arguments,
- * -2 when a thread or buffer could not be created. */
+/* q [B,T,H,d], k/v [B,S_max,K,d], lens [B] (new tokens included), out
+ * [B,T,H,d]; all fp64, host memory. window 0 = full attention. nthreads <= 0
+ * uses every online CPU. Returns 0, or -1 on bad arguments, -2 when a thread
+ * or buffer could not be created. */
 int oracle_gqa_decode(const double *q, const double *k, const double *v,
-                      const int32_t *lens, int32_t B, int32_t H, int32_t K,
-                      int32_t d, int32_t S_max, double scale, double *out,
+                      const int32_t *lens, int32_t B, int32_t T, int32_t H, int32_t K,
+                      int32_t d, int32_t S_max, int32_t window, double scale, double *out,
                       int32_t nthreads)
 {
-    if (B < 0 || H <= 0 || K <= 0 || d <= 0 || S_max < 0 || H % K != 0)
+    if (B < 0 || T <= 0 || H <= 0 || K <= 0 || d <= 0 || S_max < 0 || H % K != 0 || window < 0)
         return -1;
     for (int32_t b = 0; b < B; ++b)
         if (lens[b] < 0 || lens[b] > S_max) return -1;
-    decode_job J = {q, k, v, lens, B, H, K, d, S_max, scale, out, 0,
+    decode_job J = {q, k, v, lens, B, T, H, K, d, S_max, window, scale, out, 0,
                     PTHREAD_MUTEX_INITIALIZER};
     int32_t nt = nthreads > 0 ? nthreads : oracle_num_cpus();
-    int64_t items = (int64_t)B * H;
+    int64_t items = (int64_t)B * T * H;
     if (nt > items) nt = (int32_t)(items > 0 ? items : 1);
     pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
     if (!th) return -2;

@@ -145,6 +145,107 @@ def test_empty_context_gives_zero(oracle_mod):
     assert np.all(out[0] == 0.0) and np.all(np.isfinite(out[1]))
 
 
+def _sdpa_masked(q4, k, v, lens, scale, window):
+    """Library reference for T queries per sequence: torch SDPA (fp64, CPU) with an
+    explicit boolean mask; query i of sequence b is at position lens[b] - T + i."""
+    B, T, H, d = q4.shape
+    G = H // k.shape[2]
+    out = np.zeros(q4.shape)
+    for b in range(B):
+        L = int(lens[b])
+        pos = L - T + np.arange(T)
+        t = np.arange(L)
+        allow = t[None, :] <= pos[:, None]
+        if window:
+            allow &= t[None, :] > pos[:, None] - window
+        rows = allow.any(1)
+        if not rows.any():
+            continue
+        qb = torch.from_numpy(q4[b][rows]).permute(1, 0, 2).unsqueeze(0)           # [1, H, T', d]
+        kb = torch.from_numpy(k[b, :L]).permute(1, 0, 2).repeat_interleave(G, dim=0).unsqueeze(0)
+        vb = torch.from_numpy(v[b, :L]).permute(1, 0, 2).repeat_interleave(G, dim=0).unsqueeze(0)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qb, kb, vb, attn_mask=torch.from_numpy(allow[rows]), scale=scale)
+        out[b][rows] = o[0].permute(1, 0, 2).numpy()
+    return out
+
+
+@pytest.mark.parametrize("window,lens", [
+    (1, [1, 7, 40]), (5, [3, 5, 6, 100]), (16, [16, 17, 33]), (37, [36, 37, 38, 200]),
+])
+def test_sliding_window_matches_sdpa_with_band_mask(oracle_mod, window, lens):
+    B, H, K, d = len(lens), 8, 2, 32
+    q = _rand((B, H, d), 41)
+    k = _rand((B, max(lens), K, d), 42)
+    v = _rand((B, max(lens), K, d), 43)
+    got = oracle_mod.decode(q, k, v, lens, 0.2, window=window)
+    ref = _sdpa_masked(q[:, None], k, v, lens, 0.2, window)[:, 0]
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    # same as full attention over the last `window` tokens, cut out by hand
+    for b, L in enumerate(lens):
+        lo = max(0, L - window)
+        cut = oracle_mod.decode(q[b:b + 1], k[b:b + 1, lo:L], v[b:b + 1, lo:L], [L - lo], 0.2)
+        np.testing.assert_allclose(got[b:b + 1], cut, rtol=0, atol=1e-12)
+
+
+def test_window_of_one_returns_the_newest_value_exactly(oracle_mod):
+    lens = [1, 9, 30]
+    k = _rand((3, 30, 2, 16), 44)
+    v = _rand((3, 30, 2, 16), 45)
+    got = oracle_mod.decode(_rand((3, 4, 16), 46), k, v, lens, 1.0, window=1)
+    for b, L in enumerate(lens):
+        assert np.array_equal(got[b], np.repeat(v[b, L - 1], 2, axis=0))
+
+
+def test_window_covering_the_context_is_full_attention(oracle_mod):
+    lens = [5, 64]
+    q, k, v = _rand((2, 4, 16), 47), _rand((2, 64, 2, 16), 48), _rand((2, 64, 2, 16), 49)
+    full = oracle_mod.decode(q, k, v, lens, 0.3)
+    assert np.array_equal(oracle_mod.decode(q, k, v, lens, 0.3, window=64), full)
+    assert np.array_equal(oracle_mod.decode(q, k, v, lens, 0.3, window=1000), full)
+
+
+@pytest.mark.parametrize("T,window", [(2, 0), (4, 0), (8, 0), (3, 5), (8, 4)])
+def test_multi_token_matches_sdpa_with_causal_mask(oracle_mod, T, window):
+    lens = [T, T + 1, 17, 50]
+    B, H, K, d = len(lens), 8, 2, 32
+    q = _rand((B, T, H, d), 50)
+    k = _rand((B, max(lens), K, d), 51)
+    v = _rand((B, max(lens), K, d), 52)
+    got = oracle_mod.decode(q, k, v, lens, 0.25, window=window)
+    ref = _sdpa_masked(q, k, v, lens, 0.25, window)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_each_new_token_sees_exactly_its_prefix(oracle_mod):
+    """Query i of T equals a one-token decode over the prefix ending at its position."""
+    T, lens = 4, [6, 21]
+    q = _rand((2, T, 8, 16), 53)
+    k, v = _rand((2, 21, 4, 16), 54), _rand((2, 21, 4, 16), 55)
+    got = oracle_mod.decode(q, k, v, lens, 0.5)
+    for b, L in enumerate(lens):
+        for i in range(T):
+            one = oracle_mod.decode(q[b:b + 1, i], k[b:b + 1], v[b:b + 1], [L - T + i + 1], 0.5)
+            np.testing.assert_array_equal(got[b:b + 1, i], one)
+    # causality: changing the last new token's K/V leaves the earlier queries alone
+    k2, v2 = k.copy(), v.copy()
+    k2[0, lens[0] - 1] += 3.0
+    v2[0, lens[0] - 1] -= 2.0
+    got2 = oracle_mod.decode(q, k2, v2, lens, 0.5)
+    assert np.array_equal(got2[0, :T - 1], got[0, :T - 1])
+    assert not np.array_equal(got2[0, T - 1], got[0, T - 1])
+
+
+def test_queries_before_the_sequence_start_give_zero(oracle_mod):
+    """lens < T: the queries at negative positions attend nothing."""
+    T = 4
+    q = _rand((1, T, 4, 8), 56)
+    k, v = _rand((1, 2, 2, 8), 57), _rand((1, 2, 2, 8), 58)
+    got = oracle_mod.decode(q, k, v, [2], 1.0)
+    assert np.array_equal(got[0, :2], np.zeros((2, 4, 8)))
+    assert np.array_equal(got[0, 2], np.repeat(v[0, 0], 2, axis=0))   # one token: o = v
+
+
 def test_thread_count_does_not_change_result(oracle_mod):
     q, k, v = _rand((3, 8, 32), 25), _rand((3, 50, 2, 32), 26), _rand((3, 50, 2, 32), 27)
     a = oracle_mod.decode(q, k, v, [50, 7, 31], 0.2, nthreads=1)
