@@ -443,10 +443,15 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
         for (int t = 0; t < D / 32; ++t) {
             uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
             if constexpr (C::kFp8) {
-                e4m3x4_to_f16x4(f.k[t][0], l0, h0);        // tok r,   chunk 2t
-                e4m3x4_to_f16x4(f.k[t][1], l1, h1);        // tok r+8, chunk 2t
-                e4m3x4_to_f16x4(f.k[t][2], l2, h2);        // tok r,   chunk 2t+1
-                e4m3x4_to_f16x4(f.k[t][3], l3, h3);        // tok r+8, chunk 2t+1
+                // widened as 2^-8 x (integer ops; 256 goes into the K scale)
+                l0 = e4m3x2_to_f16x2_scaled(f.k[t][0], 0u, 0x9180u);   // elements 0, 1
+                h0 = e4m3x2_to_f16x2_scaled(f.k[t][0], 0u, 0xB3A2u);   // elements 2, 3
+                l1 = e4m3x2_to_f16x2_scaled(f.k[t][1], 0u, 0x9180u);
+                h1 = e4m3x2_to_f16x2_scaled(f.k[t][1], 0u, 0xB3A2u);
+                l2 = e4m3x2_to_f16x2_scaled(f.k[t][2], 0u, 0x9180u);
+                h2 = e4m3x2_to_f16x2_scaled(f.k[t][2], 0u, 0xB3A2u);
+                l3 = e4m3x2_to_f16x2_scaled(f.k[t][3], 0u, 0x9180u);
+                h3 = e4m3x2_to_f16x2_scaled(f.k[t][3], 0u, 0xB3A2u);
             } else {
                 i8x4_to_f16x4(f.k[t][0], l0, h0);
                 i8x4_to_f16x4(f.k[t][1], l1, h1);
@@ -460,8 +465,9 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
     // fragment: [0] = (tok r, head 2c), [1] = (tok r, head 2c+1), [2]/[3] = tok r+8
     float kr = scale_log2, kr8 = scale_log2, vr_s = 1.f, vr8_s = 1.f;
     if constexpr (C::kCoded) {
-        kr = f.ks_r * scale_log2;
-        kr8 = f.ks_r8 * scale_log2;
+        const float kfix = C::kFp8 ? 256.f : 1.f;
+        kr = f.ks_r * (kfix * scale_log2);
+        kr8 = f.ks_r8 * (kfix * scale_log2);
         vr_s = f.vs_r;
         vr8_s = f.vs_r8;
     }
@@ -532,21 +538,35 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
                 if (tok >= nvalid) f.v[i][0] = f.v[i][1] = f.v[i][2] = f.v[i][3] = 0u;
             }
         }
+        if constexpr (C::kFp8) {
+            // pair (x.b[k], y.b[k]) straight from the two tokens' words, with
+            // the sign bytes, then widened as 2^-8 x (undone at the flush)
+#pragma unroll
+            for (int wd = 0; wd < 4; ++wd) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t s0 = e ? 0xE6A2u : 0xC480u, s1 = e ? 0xF7B3u : 0xD591u;
+                    const uint32_t a0 = e4m3x2_to_f16x2_scaled(f.v[0][wd], f.v[1][wd], s0);
+                    const uint32_t a1 = e4m3x2_to_f16x2_scaled(f.v[0][wd], f.v[1][wd], s1);
+                    const uint32_t a2 = e4m3x2_to_f16x2_scaled(f.v[2][wd], f.v[3][wd], s0);
+                    const uint32_t a3 = e4m3x2_to_f16x2_scaled(f.v[2][wd], f.v[3][wd], s1);
+                    const int j = 2 * wd + e;
+                    mma_f16(st.acc[j], a0, a1, a2, a3, bh0, bh1);
+                    mma_f16(st.acc[j], a0, a1, a2, a3, bl0, bl1);
+                }
+            }
+            return;
+        }
         // A fragment of m-tile j = 2w + e (dims 16r + 4w + 2e, +1) for the token
         // pair (x, y): interleave the two tokens' bytes, then widen each byte to
         // f16 exactly (1024 + (code ^ 0x80) - 1152).
-        // (e4m3 codes: the interleaved byte pairs convert directly, exactly.)
         const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
         auto widen = [&](uint32_t t, uint32_t sel) -> uint32_t {
-            if constexpr (C::kFp8) {
-                return e4m3x2_to_f16x2(sel == 0x4140 ? t : t >> 16);
-            } else {
-                const uint32_t hv = __byte_perm(t, 0x64646464u, sel);
-                __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&hv), bias);
-                return as_u32(h);
-            }
+            const uint32_t hv = __byte_perm(t, 0x64646464u, sel);
+            __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&hv), bias);
+            return as_u32(h);
         };
-        const uint32_t flip = C::kFp8 ? 0u : 0x80808080u;
+        const uint32_t flip = 0x80808080u;
 #pragma unroll
         for (int wd = 0; wd < 4; ++wd) {
             const uint32_t x0 = f.v[0][wd] ^ flip, y0 = f.v[1][wd] ^ flip;
@@ -593,7 +613,7 @@ __device__ __forceinline__ void mma_flush(const DecodeArgs& a, MmaState<C, D>& s
 #pragma unroll
             for (int rh = 0; rh < 2; ++rh) {
                 const int dim = acc_dim<C, D>(j, rh, r);
-                const float v = st.acc[j][e + 2 * rh];
+                const float v = st.acc[j][e + 2 * rh] * (C::kFp8 ? 256.f : 1.f);
                 if (whole) store1(a.out, a.out_dtype, obase + dim, v * inv);
                 else a.ws_o[obase + dim] = v;
             }

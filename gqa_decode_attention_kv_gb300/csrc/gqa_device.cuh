@@ -236,10 +236,24 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
-// Four e4m3 codes (one 32-bit word) -> two f16 pairs (elements 0,1 and 2,3).
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    lo = e4m3x2_to_f16x2(w);
-    hi = e4m3x2_to_f16x2(w >> 16);
+// Byte permute with the PTX selector semantics: a selector nibble with bit 3
+// set writes the sign of the chosen byte replicated over all 8 bits.
+__device__ __forceinline__ uint32_t prmt(uint32_t x, uint32_t y, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(y), "r"(sel));
+    return r;
+}
+
+// Two e4m3 codes -> f16 pair holding 2^-8 times their values, exactly, with
+// integer ops only. e4m3 is s.eeee.mmm with bias 7, f16 is s.eeeee.m(10) with
+// bias 15: moving the seven exponent+mantissa bits up by 7 gives an f16 whose
+// exponent is 8 smaller, for normal and subnormal codes alike (the largest
+// code, 448, becomes 1.75; the smallest subnormal, 2^-9, becomes 2^-17).
+// `sel` picks the two codes into bytes 0 and 2 of the halves, with their
+// sign bytes (selector nibble | 8) in bytes 1 and 3; after the shift bit 15 of
+// each half holds the sign and the mask clears what spilled past it.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t x, uint32_t y, uint32_t sel) {
+    return (prmt(x, y, sel) << 7) & 0xBF80BF80u;
 }
 
 }  // namespace gqa
