@@ -9,8 +9,10 @@ library is missing, loading raises.
 Entry points (same names as the C ABI, without the ``gqa_`` prefix where it
 would repeat the module name):
 
-* ``kv_append``            -- write one new token per sequence into the paged cache
+* ``kv_append``            -- write the new token(s) of every sequence into the paged cache
 * ``gqa_decode``           -- grouped-query decode attention over the paged cache
+                              (one or T causal new tokens per sequence, optional
+                              sliding window)
 * ``decode_workspace_size``-- workspace bytes ``gqa_decode`` needs
 * ``kv_pool_elements``     -- elements a pool of ``num_blocks`` blocks holds (K and V)
 """
@@ -56,7 +58,8 @@ class KVCacheDesc(ctypes.Structure):
 
 class DecodeOpts(ctypes.Structure):
     """Mirror of gqa_decode_opts_t."""
-    _fields_ = [("kernel", ctypes.c_int32), ("max_warps", ctypes.c_int32),
+    _fields_ = [("tokens_per_seq", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
+                ("kernel", ctypes.c_int32), ("max_warps", ctypes.c_int32),
                 ("min_blocks_per_warp", ctypes.c_int32),
                 ("event_main_begin", ctypes.c_void_p), ("event_main_end", ctypes.c_void_p)]
 
@@ -87,9 +90,9 @@ def load() -> ctypes.CDLL:
             lib.gqa_kv_pool_elements.argtypes = [i64, i32, i32]
             lib.gqa_kv_pool_elements.restype = i64
             lib.gqa_kv_append.argtypes = [ctypes.POINTER(KVCacheDesc), vp, vp, i32, vp, i32, vp,
-                                          i32, vp, vp]
+                                          i32, i32, vp, vp]
             lib.gqa_kv_append.restype = ctypes.c_int
-            lib.gqa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+            lib.gqa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
             lib.gqa_decode_workspace_size.restype = ctypes.c_size_t
             lib.gqa_decode.argtypes = [ctypes.POINTER(KVCacheDesc), vp, i32, i32, vp, i32, vp, i32,
                                        ctypes.c_float, vp, i32, vp, ctypes.c_size_t,
@@ -177,29 +180,32 @@ def _check(status: int, where: str):
 def kv_append(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tensor,
               block_tables: torch.Tensor, positions: torch.Tensor,
               err: Optional[torch.Tensor] = None, stream=None) -> None:
-    """Write k_new/v_new [B, K, d] at slot positions[b] of each sequence's paged cache."""
+    """Write k_new/v_new [B, K, d] (one token) or [B, T, K, d] (T tokens) at
+    positions positions[b] .. positions[b]+T-1 of each sequence's paged cache."""
+    T = 1 if k_new.dim() == 3 else int(k_new.shape[1])
     desc = cache.desc()
     st = load().gqa_kv_append(ctypes.byref(desc), _ptr(k_new), _ptr(v_new),
                               DTYPE_CODE[k_new.dtype], _ptr(block_tables),
                               int(block_tables.shape[1]), _ptr(positions), int(positions.shape[0]),
-                              _ptr(err), _stream_ptr(stream))
+                              T, _ptr(err), _stream_ptr(stream))
     _check(st, "gqa_kv_append")
 
 
 def decode_workspace_size(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
-                          device: int = -1) -> int:
-    return int(load().gqa_decode_workspace_size(batch, num_heads, num_kv_heads, head_dim, device))
+                          device: int = -1, tokens_per_seq: int = 1) -> int:
+    return int(load().gqa_decode_workspace_size(batch, num_heads, num_kv_heads, head_dim,
+                                                tokens_per_seq, device))
 
 
 _ws_cache: dict = {}
 
 
 def workspace_for(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
-                  device: torch.device) -> torch.Tensor:
+                  device: torch.device, tokens_per_seq: int = 1) -> torch.Tensor:
     """A cached, zero-initialised device workspace large enough for this shape."""
     dev = torch.device(device)
     idx = dev.index if dev.index is not None else torch.cuda.current_device()
-    need = decode_workspace_size(batch, num_heads, num_kv_heads, head_dim, idx)
+    need = decode_workspace_size(batch, num_heads, num_kv_heads, head_dim, idx, tokens_per_seq)
     if need == 0:
         raise ValueError("no workspace size for this shape")
     buf = _ws_cache.get(idx)
@@ -215,14 +221,19 @@ def gqa_decode(cache: PagedKVCache, q: torch.Tensor, block_tables: torch.Tensor,
                out_dtype: torch.dtype = torch.float32, workspace: Optional[torch.Tensor] = None,
                kernel: int = KERNEL_AUTO, max_warps: int = 0, min_blocks_per_warp: int = 0,
                events: Optional[tuple] = None, err: Optional[torch.Tensor] = None,
-               stream=None) -> torch.Tensor:
-    """out[b,h] = softmax(scale * q[b,h] . K_g^T) V_g over context_lens[b] cached tokens."""
-    B, H, d = q.shape
+               stream=None, window: int = 0) -> torch.Tensor:
+    """out[b,h] = softmax(scale * q[b,h] . K_g^T) V_g over context_lens[b] cached tokens.
+
+    q is [B, H, d] (one new token per sequence) or [B, T, H, d] (T new tokens,
+    causal among themselves); ``window`` > 0 keeps each query's last ``window``
+    positions. ``out`` has q's shape."""
+    T = 1 if q.dim() == 3 else int(q.shape[1])
+    B, H, d = q.shape[0], q.shape[-2], q.shape[-1]
     if out is None:
-        out = torch.empty((B, H, d), dtype=out_dtype, device=q.device)
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     if workspace is None:
-        workspace = workspace_for(B, H, cache.num_kv_heads, d, q.device)
-    opts = DecodeOpts(kernel, max_warps, min_blocks_per_warp, None, None)
+        workspace = workspace_for(B, H, cache.num_kv_heads, d, q.device, T)
+    opts = DecodeOpts(T, window, kernel, max_warps, min_blocks_per_warp, None, None)
     if events is not None:
         opts.event_main_begin = events[0].cuda_event
         opts.event_main_end = events[1].cuda_event
@@ -238,16 +249,18 @@ def gqa_decode(cache: PagedKVCache, q: torch.Tensor, block_tables: torch.Tensor,
 def gqa_decode_noalloc(cache: PagedKVCache, q: torch.Tensor, block_tables: torch.Tensor,
                        context_lens: torch.Tensor, scale: float, out: Optional[torch.Tensor] = None,
                        out_dtype: torch.dtype = torch.float32, kernel: int = KERNEL_AUTO,
-                       err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                       err: Optional[torch.Tensor] = None, stream=None,
+                       window: int = 0) -> torch.Tensor:
     """gqa_decode with the library's built-in scratch instead of a workspace.
 
     For callers that may not allocate device memory; the output tensor is still
     the caller's (pass ``out`` to avoid even that allocation here). Calls that
     overlap on the GPU share one scratch array and race."""
-    B, H, d = q.shape
+    T = 1 if q.dim() == 3 else int(q.shape[1])
+    B, H, d = q.shape[0], q.shape[-2], q.shape[-1]
     if out is None:
-        out = torch.empty((B, H, d), dtype=out_dtype, device=q.device)
-    opts = DecodeOpts(kernel, 0, 0, None, None)
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    opts = DecodeOpts(T, window, kernel, 0, 0, None, None)
     desc = cache.desc()
     st = load().gqa_decode_noalloc(ctypes.byref(desc), _ptr(q), DTYPE_CODE[q.dtype], H,
                                    _ptr(block_tables), int(block_tables.shape[1]),

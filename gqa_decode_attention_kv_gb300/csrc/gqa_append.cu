@@ -1,7 +1,8 @@
-// gqa_append.cu -- paged KV append: the new token's K and V of every
+// gqa_append.cu -- paged KV append: the K and V of every new token of every
 // (sequence, kv-head) go to slot pos % 16 of block block_tables[b][pos / 16]
 // ("LLM 推理性能优化实战", sections 5.3-5.4 and 8.2). One warp per
-// (sequence, kv-head) writes both rows, so K and V of a token leave together.
+// (sequence, new token, kv-head) writes both rows, so K and V of a token leave
+// together.
 // For an int8 or FP8 (e4m3) cache each row is quantised on the way (one fp16
 // scale per (token, kv-head); sections 15.1, 15.2 and 15.5 of that page).
 #include "gqa_device.cuh"
@@ -23,14 +24,22 @@ struct AppendArgs {
     int32_t* err;
     long long num_blocks;
     long long sb, sh, st;   // element strides of the cache
-    int batch, K, d, max_blocks, es;
+    int batch, T, K, d, max_blocks, es;
 };
 
 constexpr int kWarpsPerCta = 4;
 
-// Resolve (b, g) -> element offset of the destination row, or -1 after flagging.
-__device__ __forceinline__ long long dest_offset(const AppendArgs& a, int b, int g, int lane) {
-    const int pos = a.positions[b];
+// Warp `row` of the grid -> (b, i, g): sequence, new token, kv-head.
+__device__ __forceinline__ void row_of(const AppendArgs& a, long long row, int& b, int& i, int& g) {
+    g = (int)(row % a.K);
+    const long long bi = row / a.K;
+    i = (int)(bi % a.T);
+    b = (int)(bi / a.T);
+}
+
+// Resolve (b, token position, g) -> element offset of the destination row, or -1
+// after flagging.
+__device__ __forceinline__ long long dest_offset(const AppendArgs& a, int b, int pos, int g, int lane) {
     if (pos < 0 || pos >= a.max_blocks * kBlock) {
         if (lane == 0 && g == 0) flag_error(a.err, GQA_DEVERR_POSITION);
         return -1;
@@ -48,17 +57,18 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) append_copy_kernel(const Ap
     grid_dependency_wait();
     launch_dependents();
     const int lane = threadIdx.x & 31;
-    const long long pair = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-    if (pair >= (long long)a.batch * a.K) return;
-    const int b = (int)(pair / a.K), g = (int)(pair % a.K);
-    const long long off = dest_offset(a, b, g, lane);
+    const long long row = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    if (row >= (long long)a.batch * a.T * a.K) return;
+    int b, i, g;
+    row_of(a, row, b, i, g);
+    const long long off = dest_offset(a, b, a.positions[b] + i, g, lane);
     if (off < 0) return;
     const int row_bytes = a.d * a.es;
     const int nvec = row_bytes / 16;                 // 16-byte vectors per row
-    const long long src = ((long long)b * a.K + g) * row_bytes;
-    for (int i = lane; i < 2 * nvec; i += 32) {
-        const bool is_v = i >= nvec;
-        const int vi = is_v ? i - nvec : i;
+    const long long src = row * row_bytes;           // k_new/v_new are [batch, T, K, d]
+    for (int x = lane; x < 2 * nvec; x += 32) {
+        const bool is_v = x >= nvec;
+        const int vi = is_v ? x - nvec : x;
         const uint8_t* s = static_cast<const uint8_t*>(is_v ? a.v_new : a.k_new) + src + vi * 16;
         uint8_t* dptr = static_cast<uint8_t*>(is_v ? a.v_cache : a.k_cache) + off * a.es + vi * 16;
         *reinterpret_cast<uint4*>(dptr) = *reinterpret_cast<const uint4*>(s);
@@ -123,15 +133,16 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) append_quant_kernel(const A
     grid_dependency_wait();
     launch_dependents();
     const int lane = threadIdx.x & 31;
-    const long long pair = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-    if (pair >= (long long)a.batch * a.K) return;
-    const int b = (int)(pair / a.K), g = (int)(pair % a.K);
-    const long long off = dest_offset(a, b, g, lane);
+    const long long row = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    if (row >= (long long)a.batch * a.T * a.K) return;
+    int b, i, g;
+    row_of(a, row, b, i, g);
+    const int pos = a.positions[b] + i;
+    const long long off = dest_offset(a, b, pos, g, lane);
     if (off < 0) return;
-    const int pos = a.positions[b];
     const int phys = a.block_tables[(long long)b * a.max_blocks + pos / kBlock];
     const long long sidx = ((long long)phys * a.K + g) * kBlock + pos % kBlock;
-    const long long src = ((long long)b * a.K + g) * a.d;
+    const long long src = row * a.d;
     quantise_row<In, EPL, kFp8>(a.k_new, src, static_cast<uint8_t*>(a.k_cache) + off, a.k_scale + sidx, lane);
     quantise_row<In, EPL, kFp8>(a.v_new, src, static_cast<uint8_t*>(a.v_cache) + off, a.v_scale + sidx, lane);
 }
@@ -155,7 +166,7 @@ const void* quant_kernel(int new_dtype, bool d64) {
 
 cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const void* v_new,
                              int new_dtype, const int32_t* block_tables, int max_blocks,
-                             const int32_t* positions, int batch, int32_t* err,
+                             const int32_t* positions, int batch, int tokens_per_seq, int32_t* err,
                              cudaStream_t stream) {
     AppendArgs a;
     a.k_cache = c.k;
@@ -172,11 +183,12 @@ cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const v
     a.sh = c.stride_head;
     a.st = c.stride_token;
     a.batch = batch;
+    a.T = tokens_per_seq;
     a.K = c.num_kv_heads;
     a.d = c.head_dim;
     a.max_blocks = max_blocks;
     a.es = dtype_size(c.dtype);
-    const long long warps = (long long)batch * c.num_kv_heads;
+    const long long warps = (long long)batch * tokens_per_seq * c.num_kv_heads;
     const int grid = (int)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
     if (grid == 0) return cudaSuccess;
     const void* fn;

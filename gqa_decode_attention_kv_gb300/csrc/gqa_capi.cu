@@ -111,7 +111,7 @@ const char* gqa_status_string(int status) {
     }
 }
 
-int gqa_version(void) { return 100; }
+int gqa_version(void) { return 200; }
 
 int64_t gqa_kv_pool_elements(int64_t num_blocks, int32_t num_kv_heads, int32_t head_dim) {
     if (num_blocks < 0 || num_kv_heads < 0 || head_dim < 0) return -1;
@@ -120,10 +120,13 @@ int64_t gqa_kv_pool_elements(int64_t num_blocks, int32_t num_kv_heads, int32_t h
 
 int gqa_kv_append(const gqa_kv_cache_t* cache, const void* k_new, const void* v_new,
                   int32_t new_dtype, const int32_t* block_tables, int32_t max_blocks_per_seq,
-                  const int32_t* positions, int32_t batch, int32_t* err_flag, void* stream) {
+                  const int32_t* positions, int32_t batch, int32_t tokens_per_seq, int32_t* err_flag,
+                  void* stream) {
     int st = check_cache(cache);
     if (st != GQA_OK) return st;
-    if (batch < 0 || max_blocks_per_seq <= 0) return GQA_ERR_INVALID;
+    if (batch < 0 || max_blocks_per_seq <= 0 || tokens_per_seq < 0) return GQA_ERR_INVALID;
+    const int T = std::max(1, (int)tokens_per_seq);
+    if ((long long)batch * T * cache->num_kv_heads >= 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
     if (batch == 0) return GQA_OK;
     if (!k_new || !v_new || !block_tables || !positions) return GQA_ERR_INVALID;
     if (!aligned16(k_new) || !aligned16(v_new)) return GQA_ERR_INVALID;
@@ -135,18 +138,19 @@ int gqa_kv_append(const gqa_kv_cache_t* cache, const void* k_new, const void* v_
         return GQA_ERR_UNSUPPORTED;
     }
     const cudaError_t e = launch_kv_append(*cache, k_new, v_new, new_dtype, block_tables,
-                                           max_blocks_per_seq, positions, batch, err_flag,
+                                           max_blocks_per_seq, positions, batch, T, err_flag,
                                            static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 size_t gqa_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t num_kv_heads,
-                                 int32_t head_dim, int32_t device) {
+                                 int32_t head_dim, int32_t tokens_per_seq, int32_t device) {
     if (batch < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return 0;
     if (head_dim != 64 && head_dim != 128) return 0;
+    if (tokens_per_seq < 0 || tokens_per_seq > kMaxGroup) return 0;
     const int sms = num_sms_of(device);
     if (sms <= 0) return 0;
-    return decode_workspace_bytes(batch, num_heads, num_kv_heads, head_dim, sms);
+    return decode_workspace_bytes(batch, num_heads, num_kv_heads, head_dim, tokens_per_seq, sms);
 }
 
 int gqa_decode(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int32_t num_heads,
@@ -158,7 +162,11 @@ int gqa_decode(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int3
     if (st != GQA_OK) return st;
     if (batch < 0 || num_heads <= 0 || max_blocks_per_seq <= 0) return GQA_ERR_INVALID;
     if (num_heads % cache->num_kv_heads) return GQA_ERR_INVALID;
-    if (num_heads / cache->num_kv_heads > kMaxGroup) return GQA_ERR_UNSUPPORTED;
+    const int T = opts ? opts->tokens_per_seq : 0;
+    const int window = opts ? opts->sliding_window : 0;
+    if (T < 0 || window < 0) return GQA_ERR_INVALID;
+    if ((long long)(num_heads / cache->num_kv_heads) * std::max(1, T) > kMaxGroup) return GQA_ERR_UNSUPPORTED;
+    if ((long long)batch * std::max(1, T) * num_heads >= 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
     if (batch > kMaxBatch) return GQA_ERR_UNSUPPORTED;
     if ((long long)batch * cache->num_kv_heads * max_blocks_per_seq >= 0x7fffffffLL)
         return GQA_ERR_UNSUPPORTED;
@@ -192,6 +200,8 @@ int gqa_decode(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int3
     L.out_dtype = out_dtype;
     L.workspace = workspace;
     L.workspace_bytes = workspace_bytes;
+    L.tokens_per_seq = std::max(1, T);
+    L.window = window;
     L.kernel = kernel;
     L.max_warps = opts ? std::max(0, opts->max_warps) : 0;
     L.min_blocks_per_warp = opts ? std::max(0, opts->min_blocks_per_warp) : 0;

@@ -1,1222 +1,20 @@
-// gqa_decode.cu -- split-KV grouped-query decode attention over a paged cache.
-//
-// What is computed (per sequence b, query head h, group g = h / G, G = H/K):
-//   out[b,h,:] = sum_t softmax_t(scale * q[b,h,:] . K[b,t,g,:]) V[b,t,g,:]
-// ("分组查询注意力 (GQA)", 技术原理 steps 2-4 and its attention equation).
-//
-// How (GB300 design):
-//  * Work unit = one 16-token cache block of one (sequence, kv-head) pair. All
-//    units are laid out in (b, g, block) order and cut into equal contiguous
-//    ranges, one per warp of a single resident wave (persistent, stream-K
-//    style). A pair that straddles ranges becomes several KV splits
-//    (Flash-Decoding, "LLM 推理性能优化实战" section 10.2); the cut is found on
-//    the device from context_lens, so no host synchronisation is needed.
-//  * Each warp streams its blocks through a private ring of shared-memory
-//    stages filled by TMA (cp.async.bulk.tensor, 4-D tensor map over the
-//    paged pool, mbarrier completion). The block table is consulted per unit;
-//    each K/V tile is read from HBM exactly once and serves all G query heads
-//    of its group (the group broadcast of the GQA page's 下游 section).
-//  * Tensor-core kernel: scores S^T[16 tokens x 8 heads] = K_tile Q^T and the
-//    update O^T[d x 8 heads] += V_tile^T P^T with mma.sync m16n8k16 (bf16 or
-//    f16 in, fp32 accumulate). P is split into a high and a low 16-bit part
-//    so the product keeps ~16 significant bits. Online softmax in fp32 with
-//    the running (m, l, o) state of "LLM 推理性能优化实战" section 9.2; the
-//    rescale is skipped while the block maximum stays within 2^kRescaleSlack
-//    of the running one (o and l share the stale maximum, so o/l is exact).
-//  * CUDA-core kernel: same pipeline, one token at a time with fp32 FMAs and
-//    warp-shuffle reductions; used for fp32 caches and as the measured
-//    alternative to the tensor-core kernel.
-//  * A second kernel merges the splits of each pair with their log-sum-exp
-//    weights: M = max m_s, L = sum l_s 2^(m_s-M), o = sum o_s 2^(m_s-M) / L
-//    (the "global max and sum" reduction of section 10.2), in base 2.
-#include <algorithm>
-#include <type_traits>
-
-#include "gqa_device.cuh"
-#include "gqa_internal.h"
+// gqa_decode.cu -- host side of the split-KV decode: kernel choice, workspace
+// layout, partition sizing and the launches (kernels in gqa_decode_kernels.cuh).
+// Instantiates the one-token, full-attention kernels and the combine kernels.
+#include "gqa_decode_kernels.cuh"
 
 namespace gqa {
+namespace dec {
+
+bool pick_plain(int dtype, int kind, int d, int nw, Variant& v) {
+    return pick_variant<false>(dtype, kind, d, nw, v);
+}
+
+}  // namespace dec
 
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
-
-struct DecodeArgs {
-    const void* q;
-    const __half* k_scale;
-    const __half* v_scale;
-    const int32_t* block_tables;
-    const int32_t* context_lens;
-    void* out;
-    int32_t* err;
-    int32_t* ws_hdr;     // the Partition: [0] R, [1] U, [2] Rs, [3] Cz, [4] P, [5] cpw
-    unsigned long long* ws_ctr;   // next dynamic chunk; zero between calls
-    int32_t* ws_pref;    // [B+1] exclusive prefix of blocks per sequence
-    float2* ws_ml;       // [slots][G] (running max m in log2 units, running sum l)
-    float* ws_o;         // [slots][G][D] un-normalised partial outputs
-    long long num_blocks;
-    int B, H, K, G, max_blocks, out_dtype, q_dtype, P, min_units;
-    int map_perm[3];     // tensor-map dims 1..3 -> 0 slot, 1 kv-head, 2 block
-    int max_tail_chunks; // pooled chunks per worker range (0 = static partition only)
-    float scale_log2;    // scale * log2(e)
-};
-
-// Warps per CTA and shared-memory ring bytes per warp of the split-KV kernel
-// (overridable at build time for tuning sweeps).
-#ifndef GQA_WARPS_PER_CTA
-#define GQA_WARPS_PER_CTA 4
-#endif
-#ifndef GQA_RING_BYTES_PER_WARP
-#define GQA_RING_BYTES_PER_WARP 16384
-#endif
-// CTAs per SM the narrow int8 tensor-core kernel is compiled to fit (registers).
-#ifndef GQA_MIN_CTAS_PER_SM_I8
-#define GQA_MIN_CTAS_PER_SM_I8 3
-#endif
-// Ring bytes of a CTA whose warps share one ring (groups of more than 8 heads).
-#ifndef GQA_SHARED_RING_BYTES
-#define GQA_SHARED_RING_BYTES 32768
-#endif
-
-// Tail balancing: about 1/8 of every worker's range, in at most kMaxTailChunks
-// chunks of at least kMinChunk blocks, is pooled and taken at run time by
-// whichever worker finishes its own part first.
-#ifndef GQA_MAX_TAIL_CHUNKS
-#define GQA_MAX_TAIL_CHUNKS 4
-#endif
-constexpr int kMaxTailChunks = GQA_MAX_TAIL_CHUNKS;
-constexpr int kMinChunk = 4;
-
-constexpr int kHeadsPerWarp = 8;   // query heads one warp serves (the MMA N dimension)
-
-// kHeadWarps == 1: every warp is an independent split-KV worker with its own
-// ring and serves all (<= 8) heads of its group. kHeadWarps > 1: the CTA is one
-// worker; its kHeadWarps warps take 8 heads each of a larger group and share
-// one ring, so each K/V tile is still loaded once for the whole group.
-template <int kKind, typename T, int D, int kHeadWarps = 1>
-struct Cfg {
-    static constexpr bool kI8 = std::is_same<T, int8_t>::value;
-    static constexpr bool kFp8 = std::is_same<T, __nv_fp8_e4m3>::value;
-    static constexpr bool kCoded = kI8 || kFp8;     // one-byte codes with fp16 scales
-    static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    static constexpr int kEs = sizeof(T);
-    static constexpr int kTile = 16 * D * kEs;                       // one (block, head) tile
-    static constexpr int kScaleBytes = kCoded ? 64 : 0;             // 16 k + 16 v fp16 scales
-    static constexpr int kStage = ((2 * kTile + kScaleBytes + 1023) / 1024) * 1024;
-    static constexpr int kNw = kHeadWarps;
-    // The coded-cache kernels are issue-bound: the pool's bookkeeping costs
-    // them more than the tail it removes (measured on int8), so they keep the
-    // static partition.
-    static constexpr int kTailChunks = kCoded ? 0 : kMaxTailChunks;
-    // CTAs per SM the register budget is cut for. The int8 kernel is bound by
-    // issue and latency and gains from 12 warps per SM; the bf16/f16 kernels
-    // would spill at that budget and keep 8 (both measured).
-    static constexpr int kMinCtas =
-        (kHeadWarps == 1 && kKind == kKernelMma && D == 128) ? (kCoded ? GQA_MIN_CTAS_PER_SM_I8 : 2) : 1;
-    static constexpr int kWarps = kHeadWarps == 1 ? GQA_WARPS_PER_CTA : kHeadWarps;
-    static constexpr int kRings = kHeadWarps == 1 ? kWarps : 1;
-    static constexpr int kStages =
-        std::max(2, std::min(8, (kHeadWarps == 1 ? GQA_RING_BYTES_PER_WARP : GQA_SHARED_RING_BYTES) / kStage));
-    static constexpr bool kSwizzle = (kKind == kKernelMma);
-    static constexpr int kBoxInner = kSwizzle ? 128 / kEs : D;        // elements per box row
-    static constexpr int kNumBox = kSwizzle ? (D * kEs) / 128 : 1;
-    static constexpr int kBoxBytes = 16 * kBoxInner * kEs;
-    static constexpr uint32_t kTxBytes = 2 * kTile + kScaleBytes;
-    // log2 of how far the block maximum may exceed the running maximum before
-    // the state is rescaled (0 = always exact). The int8 path folds the V
-    // scale into the fp16 P operand, so it keeps P <= 1.
-    static constexpr float kRescaleSlack = kCoded ? 0.f : 8.f;
-    static constexpr int kMt = D / 16;                              // m-tiles of the P.V product
-    static constexpr int kRuns = D / 64;                            // 8-dim output runs per head
-    static constexpr int kDpl = D / 32;                             // CUDA-core kernel: dims per lane
-};
-
-// Dynamic shared memory layout shared by host and device.
-template <class C>
-struct Smem {
-    static constexpr int kRing = C::kRings * C::kStages * C::kStage;
-    static constexpr int kBars = kRing;                                   // "full", 8 B per stage
-    static constexpr int kEmpty = kBars + C::kRings * C::kStages * 8;     // "empty" (shared ring)
-    static constexpr int kMeta = kEmpty + C::kStages * 8;                 // 4 ints per stage
-    static constexpr int kScan = kMeta + C::kRings * C::kStages * 16;     // 64 ints
-    static constexpr int kLens = kScan + 64 * 4;                          // B ints, then B+1 prefix
-    static int bytes(int B) { return 1024 + kLens + (2 * B + 1) * 4; }
-};
-
-// ------------------------------------------------------------------ prologue
-
-// Validated lengths into lens_s and the block prefix pref[0..B] (pref[0] = 0).
-__device__ void block_prefix(const DecodeArgs& a, int* lens_s, int* pref, int* tmp) {
-    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, wid = tid >> 5;
-    const int nw = nthr >> 5;
-    const int maxtok = a.max_blocks * kBlock;
-    int carry = 0;
-    for (int base = 0; base < a.B; base += nthr) {
-        const int i = base + tid;
-        int L = 0;
-        if (i < a.B) {
-            L = a.context_lens[i];
-            if (L < 0 || L > maxtok) {
-                if (blockIdx.x == 0) flag_error(a.err, GQA_DEVERR_CONTEXT_LEN);
-                L = 0;
-            }
-            lens_s[i] = L;
-        }
-        int x = (L + kBlock - 1) / kBlock;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(kFull, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) tmp[wid] = x;
-        __syncthreads();
-        if (wid == 0) {
-            int t = lane < nw ? tmp[lane] : 0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(kFull, t, o);
-                if (lane >= o) t += y;
-            }
-            tmp[32 + lane] = t;
-        }
-        __syncthreads();
-        if (i < a.B) pref[i + 1] = carry + (wid ? tmp[32 + wid - 1] : 0) + x;
-        carry += tmp[32 + nw - 1];
-        __syncthreads();
-    }
-    if (tid == 0) pref[0] = 0;
-    __syncthreads();
-}
-
-// Unit u -> (b, g, j): the largest b with K*pref[b] <= u, then the head and block.
-__device__ __forceinline__ void locate(int u, const int* pref, int B, int K, int& b, int& g,
-                                       int& j) {
-    int lo = 0, hi = B;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (K * pref[mid] <= u) lo = mid;
-        else hi = mid;
-    }
-    const int nb = pref[lo + 1] - pref[lo];
-    const int rem = u - K * pref[lo];
-    b = lo;
-    g = rem / nb;
-    j = rem - g * nb;
-}
-
-// The pair after (b, g) in unit order (skipping empty sequences); b = B if none.
-__device__ __forceinline__ void next_pair(const int* pref, int B, int K, int& b, int& g) {
-    if (g + 1 < K) {
-        ++g;
-        return;
-    }
-    g = 0;
-    ++b;
-    while (b < B && pref[b + 1] == pref[b]) ++b;
-}
-
-// ------------------------------------------------------------------ loads
-
-template <typename T, int N>
-__device__ __forceinline__ void lds_row_as_float(uint32_t addr, float (&v)[N]) {
-    if constexpr (std::is_same<T, float>::value) {
-        if constexpr (N == 4) {
-            const uint4 x = lds128(addr);
-            v[0] = __uint_as_float(x.x); v[1] = __uint_as_float(x.y);
-            v[2] = __uint_as_float(x.z); v[3] = __uint_as_float(x.w);
-        } else {
-            const uint2 x = lds64(addr);
-            v[0] = __uint_as_float(x.x); v[1] = __uint_as_float(x.y);
-        }
-    } else if constexpr (std::is_same<T, __nv_fp8_e4m3>::value) {
-        uint32_t w;
-        if constexpr (N == 4) {
-            w = lds32(addr);
-        } else {
-            unsigned short h;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr));
-            w = h;
-        }
-#pragma unroll
-        for (int e = 0; e < N; e += 2) {
-            const float2 f = unpack2<false>(e4m3x2_to_f16x2(w >> (8 * e)));
-            v[e] = f.x;
-            v[e + 1] = f.y;
-        }
-    } else if constexpr (std::is_same<T, int8_t>::value) {
-        uint32_t w;
-        if constexpr (N == 4) {
-            w = lds32(addr);
-        } else {
-            unsigned short h;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr));
-            w = h;
-        }
-#pragma unroll
-        for (int e = 0; e < N; ++e) v[e] = (float)(int8_t)((w >> (8 * e)) & 0xff);
-    } else {
-        constexpr bool bf = std::is_same<T, __nv_bfloat16>::value;
-        if constexpr (N == 4) {
-            const uint2 x = lds64(addr);
-            const float2 a = unpack2<bf>(x.x), b = unpack2<bf>(x.y);
-            v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
-        } else {
-            const float2 a = unpack2<bf>(lds32(addr));
-            v[0] = a.x; v[1] = a.y;
-        }
-    }
-}
-
-__device__ __forceinline__ float load_q_float(const void* q, int q_dtype, long long i) {
-    if (q_dtype == GQA_DTYPE_F32) return static_cast<const float*>(q)[i];
-    if (q_dtype == GQA_DTYPE_F16) return __half2float(static_cast<const __half*>(q)[i]);
-    return __bfloat162float(static_cast<const __nv_bfloat16*>(q)[i]);
-}
-
-__device__ __forceinline__ uint4 ldg128(const void* p) {
-    return __ldg(reinterpret_cast<const uint4*>(p));
-}
-
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-    const float2 f = unpack2<true>(w);
-    return pack2<false>(f.x, f.y);
-}
-
-// Store 8 consecutive output floats (scaled) in the output dtype.
-__device__ __forceinline__ void store8(void* out, int out_dtype, long long idx, const float (&v)[8],
-                                       float mul) {
-    if (out_dtype == GQA_DTYPE_F32) {
-        float4* p = reinterpret_cast<float4*>(static_cast<float*>(out) + idx);
-        p[0] = make_float4(v[0] * mul, v[1] * mul, v[2] * mul, v[3] * mul);
-        p[1] = make_float4(v[4] * mul, v[5] * mul, v[6] * mul, v[7] * mul);
-    } else {
-        uint4 w;
-        if (out_dtype == GQA_DTYPE_BF16) {
-            w.x = pack2<true>(v[0] * mul, v[1] * mul); w.y = pack2<true>(v[2] * mul, v[3] * mul);
-            w.z = pack2<true>(v[4] * mul, v[5] * mul); w.w = pack2<true>(v[6] * mul, v[7] * mul);
-        } else {
-            w.x = pack2<false>(v[0] * mul, v[1] * mul); w.y = pack2<false>(v[2] * mul, v[3] * mul);
-            w.z = pack2<false>(v[4] * mul, v[5] * mul); w.w = pack2<false>(v[6] * mul, v[7] * mul);
-        }
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + idx) = w;
-    }
-}
-
-__device__ __forceinline__ void store1(void* out, int out_dtype, long long idx, float v) {
-    if (out_dtype == GQA_DTYPE_F32) static_cast<float*>(out)[idx] = v;
-    else if (out_dtype == GQA_DTYPE_BF16) static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
-    else static_cast<__half*>(out)[idx] = __float2half_rn(v);
-}
-
-// ------------------------------------------------------------------ tensor-core state
-
-template <class C, int D>
-struct MmaState {
-    float m[2], l[2];          // heads 2c, 2c+1 of the group (log2 units)
-    float acc[C::kMt][4];      // O^T fragments: rows = dims, cols = heads 2c, 2c+1
-    uint2 qf[D / 16];          // Q^T B-fragments of the current pair, one per 16-dim k-step
-    uint2 qn[D / 16];          // prefetched fragments of the next pair
-
-    __device__ __forceinline__ void reset() {
-        m[0] = m[1] = -INFINITY;
-        l[0] = l[1] = 0.f;
-#pragma unroll
-        for (int j = 0; j < C::kMt; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-    }
-};
-
-// Everything one block needs from shared memory, gathered before any math so
-// the ring slot can be refilled while the block is being computed.
-template <class C, int D>
-struct MmaFrags {
-    uint32_t k[D / 16][4];     // bf16/f16: A fragments of K per k-step; int8: raw code quads
-    uint32_t v[C::kMt][4];     // bf16/f16: A fragments of V^T per m-tile; int8: raw rows of 4 tokens
-    float ks_r, ks_r8, vs_r, vs_r8;   // int8 scales of tokens r and r+8
-};
-
-// Q fragments (B operand of the score MMA) of query head g*G + r; zero for
-// padded heads r >= G. k-step t covers dims 16t..16t+15:
-//  bf16/f16: .x = dims 16t + 2c, +1;     .y = dims 16t + 2c + 8, +9  (standard layout)
-//  int8:     .x = dims 16t + 4c, +1;     .y = dims 16t + 4c + 2, +3  (matches the code quads)
-template <class C, int D>
-__device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int b, int g, int hbase, int r,
-                                             int c, uint2 (&qf)[D / 16]) {
-    r += hbase;
-    if (r >= a.G || b >= a.B) {
-#pragma unroll
-        for (int i = 0; i < D / 16; ++i) qf[i] = make_uint2(0, 0);
-        return;
-    }
-    const uint16_t* base = static_cast<const uint16_t*>(a.q) + ((long long)b * a.H + (long long)g * a.G + r) * D;
-#pragma unroll
-    for (int t = 0; t < D / 16; ++t) {
-        if constexpr (!C::kCoded) {
-            qf[t].x = __ldg(reinterpret_cast<const uint32_t*>(base + 16 * t + 2 * c));
-            qf[t].y = __ldg(reinterpret_cast<const uint32_t*>(base + 16 * t + 2 * c + 8));
-        } else {
-            uint2 raw = __ldg(reinterpret_cast<const uint2*>(base + 16 * t + 4 * c));
-            if (a.q_dtype == GQA_DTYPE_BF16) {
-                raw.x = bf16x2_to_f16x2(raw.x);
-                raw.y = bf16x2_to_f16x2(raw.y);
-            }
-            qf[t] = raw;
-        }
-    }
-}
-
-// Output dim of accumulator row (j, rh): row r + 8*rh of m-tile j.
-template <class C, int D>
-__device__ __forceinline__ int acc_dim(int j, int rh, int r) {
-    if constexpr (C::kCoded) return 16 * r + 2 * j + rh;
-    else return 16 * j + r + 8 * rh;
-}
-
-template <bool kBf16>
-__device__ __forceinline__ void mma_t(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                      uint32_t a3, uint32_t b0, uint32_t b1) {
-    if constexpr (kBf16) mma_bf16(d, a0, a1, a2, a3, b0, b1);
-    else mma_f16(d, a0, a1, a2, a3, b0, b1);
-}
-
-// Address of 16-byte chunk `chunk` of row `tok` in a tile written by TMA with
-// 128-byte swizzle (2 KB boxes of 16 rows x 128 B; chunk index XOR row % 8).
-__device__ __forceinline__ uint32_t swz(uint32_t tile, int tok, int chunk) {
-    return tile + (uint32_t)(chunk >> 3) * 2048u + (uint32_t)tok * 128u +
-           ((uint32_t)((chunk & 7) ^ (tok & 7)) << 4);
-}
-
-// Gather one block's operands from shared memory (all reads of the slot).
-template <class C, int D>
-__device__ __forceinline__ void mma_load(MmaFrags<C, D>& f, uint32_t stage, int lane, int r, int c) {
-    const uint32_t sk = stage, sv = stage + C::kTile;
-    const int mi = lane >> 3, rr = lane & 7;
-    if constexpr (!C::kCoded) {
-        // K: matrices (toks 0-7 | 8-15) x (dims 16t..+7 | +8..+15) = a0, a1, a2, a3
-#pragma unroll
-        for (int t = 0; t < D / 16; ++t)
-            ldsm_x4(swz(sk, rr + 8 * (mi & 1), 2 * t + (mi >> 1)), f.k[t]);
-        // V^T: transposed matrices (dims 16j..+7 | +8..+15) x (toks 0-7 | 8-15)
-#pragma unroll
-        for (int j = 0; j < C::kMt; ++j)
-            ldsm_x4_t(swz(sv, rr + 8 * (mi >> 1), 2 * j + (mi & 1)), f.v[j]);
-    } else {
-        // K codes: x4 number t holds chunks 2t (a0/a1) and 2t+1 (a2/a3), 16 codes each
-#pragma unroll
-        for (int t = 0; t < D / 32; ++t)
-            ldsm_x4(swz(sk, rr + 8 * (mi & 1), 2 * t + (mi >> 1)), f.k[t]);
-        // V codes: dims 16r..16r+15 of tokens 2c, 2c+1, 2c+8, 2c+9
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int tok = 2 * c + (i & 1) + 8 * (i >> 1);
-            const uint4 raw = lds128(swz(sv, tok, r));
-            f.v[i][0] = raw.x; f.v[i][1] = raw.y; f.v[i][2] = raw.z; f.v[i][3] = raw.w;
-        }
-        const uint32_t sc = stage + 2 * C::kTile;
-        unsigned short h0, h1, h2, h3;
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h0) : "r"(sc + 2 * r));
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h1) : "r"(sc + 2 * (r + 8)));
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h2) : "r"(sc + 32 + 2 * r));
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h3) : "r"(sc + 32 + 2 * (r + 8)));
-        f.ks_r = __half2float(__ushort_as_half(h0));
-        f.ks_r8 = __half2float(__ushort_as_half(h1));
-        f.vs_r = __half2float(__ushort_as_half(h2));
-        f.vs_r8 = __half2float(__ushort_as_half(h3));
-    }
-}
-
-// One 16-token block on the tensor cores, from gathered operands.
-template <class C, int D>
-__device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& f, int nvalid,
-                                            int r, int c, float scale_log2) {
-    constexpr bool kB = C::kBf16;            // P and V operand type: bf16, else f16
-
-    // ---- scores: S^T[tok][head] = K_tile . Q^T (two accumulators halve the chain)
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (!C::kCoded) {
-#pragma unroll
-        for (int t = 0; t < D / 16; ++t) {
-            if (t & 1) mma_t<kB>(sb, f.k[t][0], f.k[t][1], f.k[t][2], f.k[t][3], st.qf[t].x, st.qf[t].y);
-            else mma_t<kB>(sa, f.k[t][0], f.k[t][1], f.k[t][2], f.k[t][3], st.qf[t].x, st.qf[t].y);
-        }
-    } else {
-#pragma unroll
-        for (int t = 0; t < D / 32; ++t) {
-            uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
-            if constexpr (C::kFp8) {
-                // widened as 2^-8 x (integer ops; 256 goes into the K scale)
-                l0 = e4m3x2_to_f16x2_scaled(f.k[t][0], 0u, 0x9180u);   // elements 0, 1
-                h0 = e4m3x2_to_f16x2_scaled(f.k[t][0], 0u, 0xB3A2u);   // elements 2, 3
-                l1 = e4m3x2_to_f16x2_scaled(f.k[t][1], 0u, 0x9180u);
-                h1 = e4m3x2_to_f16x2_scaled(f.k[t][1], 0u, 0xB3A2u);
-                l2 = e4m3x2_to_f16x2_scaled(f.k[t][2], 0u, 0x9180u);
-                h2 = e4m3x2_to_f16x2_scaled(f.k[t][2], 0u, 0xB3A2u);
-                l3 = e4m3x2_to_f16x2_scaled(f.k[t][3], 0u, 0x9180u);
-                h3 = e4m3x2_to_f16x2_scaled(f.k[t][3], 0u, 0xB3A2u);
-            } else {
-                i8x4_to_f16x4(f.k[t][0], l0, h0);
-                i8x4_to_f16x4(f.k[t][1], l1, h1);
-                i8x4_to_f16x4(f.k[t][2], l2, h2);
-                i8x4_to_f16x4(f.k[t][3], l3, h3);
-            }
-            mma_f16(sa, l0, l1, h0, h1, st.qf[2 * t].x, st.qf[2 * t].y);
-            mma_f16(sb, l2, l3, h2, h3, st.qf[2 * t + 1].x, st.qf[2 * t + 1].y);
-        }
-    }
-    // fragment: [0] = (tok r, head 2c), [1] = (tok r, head 2c+1), [2]/[3] = tok r+8
-    float kr = scale_log2, kr8 = scale_log2, vr_s = 1.f, vr8_s = 1.f;
-    if constexpr (C::kCoded) {
-        const float kfix = C::kFp8 ? 256.f : 1.f;
-        kr = f.ks_r * (kfix * scale_log2);
-        kr8 = f.ks_r8 * (kfix * scale_log2);
-        vr_s = f.vs_r;
-        vr8_s = f.vs_r8;
-    }
-    float s0 = (sa[0] + sb[0]) * kr, s1 = (sa[1] + sb[1]) * kr;
-    float s2 = (sa[2] + sb[2]) * kr8, s3 = (sa[3] + sb[3]) * kr8;
-    if (r >= nvalid) { s0 = -INFINITY; s1 = -INFINITY; vr_s = 0.f; }
-    if (r + 8 >= nvalid) { s2 = -INFINITY; s3 = -INFINITY; vr8_s = 0.f; }
-
-    // ---- online softmax (per head, over the 16 tokens of this block)
-    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
-    }
-    const bool up0 = mx0 > st.m[0] + C::kRescaleSlack, up1 = mx1 > st.m[1] + C::kRescaleSlack;
-    if (__any_sync(kFull, up0 || up1)) {
-        const float n0 = up0 ? mx0 : st.m[0], n1 = up1 ? mx1 : st.m[1];
-        const float a0 = up0 ? fast_exp2(st.m[0] - n0) : 1.f;
-        const float a1 = up1 ? fast_exp2(st.m[1] - n1) : 1.f;
-        st.m[0] = n0; st.m[1] = n1;
-        st.l[0] *= a0; st.l[1] *= a1;
-#pragma unroll
-        for (int j = 0; j < C::kMt; ++j) {
-            st.acc[j][0] *= a0; st.acc[j][1] *= a1; st.acc[j][2] *= a0; st.acc[j][3] *= a1;
-        }
-    }
-    const float p0 = fast_exp2(s0 - st.m[0]), p1 = fast_exp2(s1 - st.m[1]);
-    const float p2 = fast_exp2(s2 - st.m[0]), p3 = fast_exp2(s3 - st.m[1]);
-    st.l[0] += p0 + p2;
-    st.l[1] += p1 + p3;
-
-    // ---- P -> 16-bit high + low parts, transposed to the B layout of P.V
-    const float w0 = p0 * vr_s, w1 = p1 * vr_s, w2 = p2 * vr8_s, w3 = p3 * vr8_s;
-    const uint32_t hr = pack2<kB>(w0, w1), hr8 = pack2<kB>(w2, w3);
-    const float2 fr = unpack2<kB>(hr), fr8 = unpack2<kB>(hr8);
-    const uint32_t lr = pack2<kB>(w0 - fr.x, w1 - fr.y), lr8 = pack2<kB>(w2 - fr8.x, w3 - fr8.y);
-    const int srcA = 8 * c + (r >> 1), srcB = srcA + 4;
-    const uint32_t sel = (r & 1) ? 0x7632u : 0x5410u;
-    const uint32_t bh0 = __byte_perm(__shfl_sync(kFull, hr, srcA), __shfl_sync(kFull, hr, srcB), sel);
-    const uint32_t bh1 = __byte_perm(__shfl_sync(kFull, hr8, srcA), __shfl_sync(kFull, hr8, srcB), sel);
-    const uint32_t bl0 = __byte_perm(__shfl_sync(kFull, lr, srcA), __shfl_sync(kFull, lr, srcB), sel);
-    const uint32_t bl1 = __byte_perm(__shfl_sync(kFull, lr8, srcA), __shfl_sync(kFull, lr8, srcB), sel);
-
-    // ---- O^T[dim][head] += V^T . P^T (high part, then low part)
-    if constexpr (!C::kCoded) {
-        if (nvalid < kBlock) {
-            // zero V of tokens past the end: the slots hold arbitrary (even NaN) bits
-            const uint32_t m01 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
-            const uint32_t m89 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
-#pragma unroll
-            for (int j = 0; j < C::kMt; ++j) {
-                f.v[j][0] &= m01; f.v[j][1] &= m01; f.v[j][2] &= m89; f.v[j][3] &= m89;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < C::kMt; ++j) {
-            mma_t<kB>(st.acc[j], f.v[j][0], f.v[j][1], f.v[j][2], f.v[j][3], bh0, bh1);
-            mma_t<kB>(st.acc[j], f.v[j][0], f.v[j][1], f.v[j][2], f.v[j][3], bl0, bl1);
-        }
-    } else {
-        // f.v[i][w] holds dims 16r + 4w .. +3 (one byte each) of token i in
-        // {2c, 2c+1, 2c+8, 2c+9}. Tokens past the end hold arbitrary codes.
-        if (nvalid < kBlock) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tok = 2 * c + (i & 1) + 8 * (i >> 1);
-                if (tok >= nvalid) f.v[i][0] = f.v[i][1] = f.v[i][2] = f.v[i][3] = 0u;
-            }
-        }
-        if constexpr (C::kFp8) {
-            // pair (x.b[k], y.b[k]) straight from the two tokens' words, with
-            // the sign bytes, then widened as 2^-8 x (undone at the flush)
-#pragma unroll
-            for (int wd = 0; wd < 4; ++wd) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const uint32_t s0 = e ? 0xE6A2u : 0xC480u, s1 = e ? 0xF7B3u : 0xD591u;
-                    const uint32_t a0 = e4m3x2_to_f16x2_scaled(f.v[0][wd], f.v[1][wd], s0);
-                    const uint32_t a1 = e4m3x2_to_f16x2_scaled(f.v[0][wd], f.v[1][wd], s1);
-                    const uint32_t a2 = e4m3x2_to_f16x2_scaled(f.v[2][wd], f.v[3][wd], s0);
-                    const uint32_t a3 = e4m3x2_to_f16x2_scaled(f.v[2][wd], f.v[3][wd], s1);
-                    const int j = 2 * wd + e;
-                    mma_f16(st.acc[j], a0, a1, a2, a3, bh0, bh1);
-                    mma_f16(st.acc[j], a0, a1, a2, a3, bl0, bl1);
-                }
-            }
-            return;
-        }
-        // A fragment of m-tile j = 2w + e (dims 16r + 4w + 2e, +1) for the token
-        // pair (x, y): interleave the two tokens' bytes, then widen each byte to
-        // f16 exactly (1024 + (code ^ 0x80) - 1152).
-        const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-        auto widen = [&](uint32_t t, uint32_t sel) -> uint32_t {
-            const uint32_t hv = __byte_perm(t, 0x64646464u, sel);
-            __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&hv), bias);
-            return as_u32(h);
-        };
-        const uint32_t flip = 0x80808080u;
-#pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
-            const uint32_t x0 = f.v[0][wd] ^ flip, y0 = f.v[1][wd] ^ flip;
-            const uint32_t x1 = f.v[2][wd] ^ flip, y1 = f.v[3][wd] ^ flip;
-            // bytes (x.b0, y.b0, x.b1, y.b1) and (x.b2, y.b2, x.b3, y.b3)
-            const uint32_t lo0 = __byte_perm(x0, y0, 0x5140), hi0 = __byte_perm(x0, y0, 0x7362);
-            const uint32_t lo1 = __byte_perm(x1, y1, 0x5140), hi1 = __byte_perm(x1, y1, 0x7362);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const uint32_t t0 = e ? hi0 : lo0, t1 = e ? hi1 : lo1;
-                // rows r (dim 4wd + 2e) and r+8 (dim 4wd + 2e + 1): tokens (2c, 2c+1)
-                const uint32_t a0 = widen(t0, 0x4140), a1 = widen(t0, 0x4342);
-                const uint32_t a2 = widen(t1, 0x4140), a3 = widen(t1, 0x4342);
-                const int j = 2 * wd + e;
-                mma_f16(st.acc[j], a0, a1, a2, a3, bh0, bh1);
-                mma_f16(st.acc[j], a0, a1, a2, a3, bl0, bl1);
-            }
-        }
-    }
-}
-
-// Write the state of pair (b, g): final output if this warp saw the whole pair,
-// else a partial (o, m, l) into split slot (b*K + g) + warp.
-template <class C, int D>
-__device__ __forceinline__ void mma_flush(const DecodeArgs& a, MmaState<C, D>& st, int b, int g,
-                                          int hbase, bool whole, int w, int r, int c) {
-    float l0 = st.l[0], l1 = st.l[1];
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        l0 += __shfl_xor_sync(kFull, l0, o);
-        l1 += __shfl_xor_sync(kFull, l1, o);
-    }
-    const long long slot = (long long)b * a.K + g + w;
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int hh = hbase + 2 * c + e;
-        if (hh >= a.G) continue;
-        const float lsum = e ? l1 : l0;
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-        const long long obase = whole ? ((long long)b * a.H + (long long)g * a.G + hh) * D
-                                      : (slot * a.G + hh) * D;
-#pragma unroll
-        for (int j = 0; j < C::kMt; ++j) {
-#pragma unroll
-            for (int rh = 0; rh < 2; ++rh) {
-                const int dim = acc_dim<C, D>(j, rh, r);
-                const float v = st.acc[j][e + 2 * rh] * (C::kFp8 ? 256.f : 1.f);
-                if (whole) store1(a.out, a.out_dtype, obase + dim, v * inv);
-                else a.ws_o[obase + dim] = v;
-            }
-        }
-        if (!whole && r == 0) a.ws_ml[slot * a.G + hh] = make_float2(st.m[e], lsum);
-    }
-}
-
-// ------------------------------------------------------------------ CUDA-core state
-
-template <class C, int D>
-struct FmaState {
-    static constexpr int kN = C::kDpl;
-    float m[kHeadsPerWarp], l[kHeadsPerWarp];
-    float acc[kHeadsPerWarp][kN];
-    float q[kHeadsPerWarp][kN];
-
-    __device__ __forceinline__ void reset() {
-#pragma unroll
-        for (int h = 0; h < kHeadsPerWarp; ++h) {
-            m[h] = -INFINITY;
-            l[h] = 0.f;
-#pragma unroll
-            for (int i = 0; i < kN; ++i) acc[h][i] = 0.f;
-        }
-    }
-};
-
-template <class C, int D>
-__device__ __forceinline__ void fma_load_q(const DecodeArgs& a, FmaState<C, D>& st, int b, int g,
-                                           int hbase, int lane) {
-#pragma unroll
-    for (int h = 0; h < kHeadsPerWarp; ++h)
-#pragma unroll
-        for (int i = 0; i < C::kDpl; ++i)
-            st.q[h][i] = (hbase + h < a.G && b < a.B)
-                             ? load_q_float(a.q, a.q_dtype,
-                                            ((long long)b * a.H + (long long)g * a.G + hbase + h) * D + lane * C::kDpl + i)
-                             : 0.f;
-}
-
-// One block, token by token: fp32 FMAs, butterfly reductions, per-token online softmax.
-template <class C, int D, typename T>
-__device__ __forceinline__ void fma_block(const DecodeArgs& a, FmaState<C, D>& st, uint32_t stage,
-                                          int nvalid, int hbase, int lane) {
-    constexpr int kN = C::kDpl;
-    const uint32_t sk = stage, sv = stage + C::kTile;
-    const int G = a.G - hbase;                   // heads of this warp: hbase .. hbase+7
-    for (int t = 0; t < nvalid; ++t) {
-        float kf[kN], vf[kN];
-        lds_row_as_float<T, kN>(sk + t * D * C::kEs + lane * kN * C::kEs, kf);
-        lds_row_as_float<T, kN>(sv + t * D * C::kEs + lane * kN * C::kEs, vf);
-        float ksc = a.scale_log2, vsc = 1.f;
-        if constexpr (C::kCoded) {
-            unsigned short hk, hv;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hk) : "r"(stage + 2 * C::kTile + 2 * t));
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(stage + 2 * C::kTile + 32 + 2 * t));
-            ksc *= __half2float(__ushort_as_half(hk));
-            vsc = __half2float(__ushort_as_half(hv));
-        }
-#pragma unroll
-        for (int h = 0; h < kHeadsPerWarp; ++h) {
-            if (h >= G) break;
-            float dot = 0.f;
-#pragma unroll
-            for (int i = 0; i < kN; ++i) dot = fmaf(st.q[h][i], kf[i], dot);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(kFull, dot, o);
-            const float s = dot * ksc;
-            const float mn = fmaxf(st.m[h], s);
-            const float al = fast_exp2(st.m[h] - mn);
-            const float p = fast_exp2(s - mn);
-            st.l[h] = st.l[h] * al + p;
-            const float pv = p * vsc;
-#pragma unroll
-            for (int i = 0; i < kN; ++i) st.acc[h][i] = fmaf(st.acc[h][i], al, pv * vf[i]);
-            st.m[h] = mn;
-        }
-    }
-}
-
-template <class C, int D>
-__device__ __forceinline__ void fma_flush(const DecodeArgs& a, FmaState<C, D>& st, int b, int g,
-                                          int hbase, bool whole, int w, int lane) {
-    const long long slot = (long long)b * a.K + g + w;
-#pragma unroll
-    for (int h = 0; h < kHeadsPerWarp; ++h) {
-        const int hh = hbase + h;
-        if (hh >= a.G) break;
-        const float inv = st.l[h] > 0.f ? 1.f / st.l[h] : 0.f;
-#pragma unroll
-        for (int i = 0; i < C::kDpl; ++i) {
-            const int dim = lane * C::kDpl + i;
-            if (whole) store1(a.out, a.out_dtype, ((long long)b * a.H + (long long)g * a.G + hh) * D + dim, st.acc[h][i] * inv);
-            else a.ws_o[(slot * a.G + hh) * D + dim] = st.acc[h][i];
-        }
-        if (!whole && lane == 0) a.ws_ml[slot * a.G + hh] = make_float2(st.m[h], st.l[h]);
-    }
-}
-
-// ------------------------------------------------------------------ the split-KV kernel
-
-// Slot metadata the producer writes before a slot's barrier completes.
-enum SlotKind : int { kSlotData = 0, kSlotSkip = 1, kSlotEnd = 2 };
-
-// The partition of the U units, identical on every CTA and in the combine.
-// Worker w's range is [w*R, min(U, (w+1)*R)); its first Rs units are its own
-// (static segment), the remaining cpw chunks of Cz units go to a pool. Segment
-// index of worker w's static part is w*(1+cpw), of its chunk i w*(1+cpw)+1+i:
-// indices grow with unit position, so a split slot (b*K + g) + segment is unique
-// and every pair's pieces are the consecutive segments that cover it.
-struct Partition {
-    int U, R, Rs, Cz, cpw, P;
-    __device__ __forceinline__ int segment_of(int u) const {
-        const int w = u / R, off = u - w * R;
-        return w * (1 + cpw) + (off < Rs ? 0 : 1 + (off - Rs) / Cz);
-    }
-};
-
-__device__ __forceinline__ Partition make_partition(const DecodeArgs& a, int U) {
-    Partition pt;
-    pt.U = U;
-    pt.P = max(a.P, 1);
-    pt.R = max((U + pt.P - 1) / pt.P, a.min_units);
-    pt.Cz = max(kMinChunk, (pt.R + 31) / 32);
-    pt.cpw = min(a.max_tail_chunks, pt.R / (8 * pt.Cz));
-    pt.Rs = pt.R - pt.cpw * pt.Cz;
-    return pt;
-}
-
-template <int kKind, typename T, int D, int kHeadWarps>
-__global__ void __launch_bounds__(Cfg<kKind, T, D, kHeadWarps>::kWarps * 32,
-                                  Cfg<kKind, T, D, kHeadWarps>::kMinCtas)
-split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                const DecodeArgs a) {
-    using C = Cfg<kKind, T, D, kHeadWarps>;
-    using S = Smem<C>;
-    constexpr bool kShared = kHeadWarps > 1;     // one ring, one worker per CTA
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_addr(smem_raw);
-    const uint32_t sbase = (raw + 1023u) & ~1023u;
-    uint8_t* gbase = smem_raw + (sbase - raw);
-    int* tmp = reinterpret_cast<int*>(gbase + S::kScan);
-    int* lens_s = reinterpret_cast<int*>(gbase + S::kLens);
-    int* pref = lens_s + a.B;
-
-    if (threadIdx.x == 0) {
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&vmap);
-    }
-    launch_dependents();                       // the combine kernel may take its place now
-    grid_dependency_wait();                    // inputs may come from the previous kernel
-    block_prefix(a, lens_s, pref, tmp);
-    const Partition pt = make_partition(a, a.K * pref[a.B]);
-    if (blockIdx.x == 0) {
-        for (int i = threadIdx.x; i <= a.B; i += blockDim.x) a.ws_pref[i] = pref[i];
-        if (threadIdx.x == 0) {
-            a.ws_hdr[0] = pt.R;
-            a.ws_hdr[1] = pt.U;
-            a.ws_hdr[2] = pt.Rs;
-            a.ws_hdr[3] = pt.Cz;
-            a.ws_hdr[4] = pt.P;
-            a.ws_hdr[5] = pt.cpw;
-        }
-    }
-    if (pt.U == 0) return;                     // uniform: every row is empty (combine zeroes them)
-
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int w = kShared ? (int)blockIdx.x : (int)blockIdx.x * C::kWarps + warp;   // worker
-    const int hbase = kShared ? warp * kHeadsPerWarp : 0;
-    if (w >= pt.P) return;                     // uniform per worker (grid is sized to P)
-    const long long sl = (long long)w * pt.R;
-    const int st_lo = (int)min((long long)pt.U, sl);
-    const int st_hi = (int)min((long long)pt.U, sl + pt.Rs);
-
-    const int ring_id = kShared ? 0 : warp;
-    const uint32_t ring = sbase + ring_id * C::kStages * C::kStage;
-    const uint32_t bar0 = sbase + S::kBars + ring_id * C::kStages * 8;
-    const uint32_t ebar0 = sbase + S::kEmpty;
-    volatile int* meta = reinterpret_cast<volatile int*>(gbase + S::kMeta) + ring_id * C::kStages * 4;
-    const bool producer = !kShared || warp == 0;  // the warp that issues this ring's copies
-    if (kShared) {
-        if (threadIdx.x == 0) {
-            for (int s = 0; s < C::kStages; ++s) {
-                mbar_init(bar0 + 8 * s, 1);
-                mbar_init(ebar0 + 8 * s, kHeadWarps);
-            }
-            fence_mbar_init();
-        }
-        __syncthreads();                       // every warp of this CTA reached here (same worker)
-    } else {
-        if (lane == 0) {
-            for (int s = 0; s < C::kStages; ++s) mbar_init(bar0 + 8 * s, 1);
-            fence_mbar_init();
-        }
-        __syncwarp();
-    }
-    const uint64_t pol = l2_policy_evict_first();
-
-    // ---- producer: segments (static range first, then pooled chunks) and copies
-    // The pool is asked for the next chunk kLookahead units before the current
-    // segment runs out, and that chunk's block-table entries are fetched as soon
-    // as its id is known, so switching segments costs no round trip.
-    constexpr int kLookahead = 2;
-    const unsigned long long pool = (unsigned long long)pt.P * pt.cpw;
-    int iss_u = 0, iss_hi = 0, iss_seg = -1, n_issued = 0;
-    int nxt_lo = 0, nxt_hi = 0, nxt_seg = -1;
-    bool iss_done = false, nxt_ok = false, pend_out = false, exhausted = pool == 0;
-    unsigned long long pend = 0;                           // lane 0: in-flight pool ticket
-    int win_base = -(1 << 30), win_phys = -1, win_g = 0;   // lane l: unit win_base + l
-    auto refill = [&](int base) {
-        win_base = base;
-        const int u = base + lane;
-        win_phys = -1;
-        win_g = 0;
-        if (u < pt.U) {
-            int b, g, j;
-            locate(u, pref, a.B, a.K, b, g, j);
-            const int ph = a.block_tables[(long long)b * a.max_blocks + j];
-            if (ph < 0 || ph >= a.num_blocks) flag_error(a.err, GQA_DEVERR_BLOCK_INDEX);
-            else win_phys = ph;
-            win_g = g;
-        }
-    };
-    auto request = [&]() {
-        if (pend_out || exhausted) return;
-        if (lane == 0) pend = atomicAdd(a.ws_ctr, 1ull);
-        pend_out = true;
-    };
-    auto resolve = [&]() {                 // the in-flight ticket -> the next segment
-        while (pend_out) {
-            const unsigned long long cidx = __shfl_sync(kFull, pend, 0);
-            pend_out = false;
-            if (cidx >= pool) {
-                exhausted = true;
-                return;
-            }
-            const int wc = (int)(cidx % pt.P), ic = (int)(cidx / pt.P);
-            const long long lo = (long long)wc * pt.R + pt.Rs + (long long)ic * pt.Cz;
-            if (lo >= pt.U) {              // a chunk past the last unit: take another
-                request();
-                continue;
-            }
-            nxt_lo = (int)lo;
-            nxt_hi = (int)min((long long)pt.U, lo + pt.Cz);
-            nxt_seg = wc * (1 + pt.cpw) + 1 + ic;
-            nxt_ok = true;
-        }
-    };
-    if (producer) {
-        if (st_lo < st_hi) {
-            iss_u = st_lo;
-            iss_hi = st_hi;
-            iss_seg = w * (1 + pt.cpw);
-            if (iss_hi - iss_u <= kLookahead) request();
-        } else {
-            request();
-        }
-    }
-    // Fill ring slot s with the next unit of this worker, or with the end marker.
-    auto issue_next = [&](int s) {
-        if (iss_done) return;
-        const uint32_t bar = bar0 + 8 * s;
-        ++n_issued;
-        if (iss_u >= iss_hi) {
-            if (!nxt_ok) {
-                request();
-                resolve();
-            }
-            if (!nxt_ok) {
-                iss_done = true;
-                if (lane == 0) {
-                    meta[4 * s] = kSlotEnd;
-                    mbar_arrive(bar);
-                }
-                return;
-            }
-            iss_u = nxt_lo;
-            iss_hi = nxt_hi;
-            iss_seg = nxt_seg;
-            nxt_ok = false;
-            if (iss_hi - iss_u <= kLookahead) request();
-        }
-        const int u = iss_u++;
-        // pooled chunks can lie before this worker's own range: refill on any jump
-        if (u < win_base || u - win_base >= 32) refill(u);
-        const int ph = __shfl_sync(kFull, win_phys, u - win_base);
-        const int gg = __shfl_sync(kFull, win_g, u - win_base);
-        if (lane == 0) {
-            meta[4 * s + 1] = u;
-            meta[4 * s + 2] = iss_seg;
-            meta[4 * s + 3] = iss_hi;
-            if (ph >= 0) {
-                const uint32_t dst = ring + s * C::kStage;
-                auto coord = [&](int which) { return which == 0 ? 0 : (which == 1 ? gg : ph); };
-                const int y = coord(a.map_perm[0]), z = coord(a.map_perm[1]), ww = coord(a.map_perm[2]);
-                meta[4 * s] = kSlotData;
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar, C::kTxBytes);
-#pragma unroll
-                for (int x = 0; x < C::kNumBox; ++x)
-                    tma_load_4d(dst + x * C::kBoxBytes, &kmap, x * C::kBoxInner, y, z, ww, bar, pol);
-#pragma unroll
-                for (int x = 0; x < C::kNumBox; ++x)
-                    tma_load_4d(dst + C::kTile + x * C::kBoxBytes, &vmap, x * C::kBoxInner, y, z, ww, bar, pol);
-                if constexpr (C::kCoded) {
-                    const long long si = ((long long)ph * a.K + gg) * kBlock;
-                    bulk_load(dst + 2 * C::kTile, a.k_scale + si, 32, bar, pol);
-                    bulk_load(dst + 2 * C::kTile + 32, a.v_scale + si, 32, bar, pol);
-                }
-            } else {
-                meta[4 * s] = kSlotSkip;
-                mbar_arrive(bar);
-            }
-        }
-        if (iss_hi - iss_u == kLookahead) request();
-        if (iss_u == iss_hi) {             // segment issued: learn the next one, prefetch its table
-            resolve();
-            if (nxt_ok) refill(nxt_lo);
-        }
-    };
-    // Bounded waits whose verdict is warp-uniform, so a timeout never splits a warp.
-    auto wait_all = [&](uint32_t bar, uint32_t parity) {
-        return __all_sync(kFull, mbar_wait(bar, parity));
-    };
-    auto bail = [&](int k) {
-        // A copy (or a peer warp) did not arrive in time: report, let this ring's
-        // in-flight copies land, leave.
-        if (lane == 0) flag_error(a.err, GQA_DEVERR_TIMEOUT);
-        if (producer)
-            for (int q = k; q < n_issued; ++q)
-                mbar_wait(bar0 + 8 * (q % C::kStages), (uint32_t)(q / C::kStages) & 1u, kWaitLimitNs / 4);
-    };
-    // Hand slot s (use k, just read) back; the producer refills it.
-    auto release_and_refill = [&](int k, int s) -> bool {
-        __syncwarp();
-        if (kShared && lane == 0) mbar_arrive(ebar0 + 8 * s);
-        if (producer && !iss_done) {
-            if (kShared && !wait_all(ebar0 + 8 * s, (uint32_t)(k / C::kStages) & 1u)) return false;
-            issue_next(s);
-        }
-        return true;
-    };
-
-    if (producer)
-        for (int s = 0; s < C::kStages; ++s) issue_next(s);
-
-    // ---- consumer: walk the units as they arrive
-    const int r = lane >> 2, c = lane & 3;
-    using State = typename std::conditional<kKind == kKernelMma, MmaState<C, D>, FmaState<C, D>>::type;
-    State st;
-    int cb = 0, cg = 0, cj = 0, cnb = 1, clen = 0, first_j = 0, cu_pair = 0;
-    int nb_b = 0, nb_g = 0, next_u = -1;
-
-    for (int k = 0;; ++k) {
-        const int s = k % C::kStages;
-        // every lane observes the phase, which acquires the TMA writes and the metadata
-        if (!wait_all(bar0 + 8 * s, (uint32_t)(k / C::kStages) & 1u)) {
-            bail(k);
-            return;
-        }
-        const int kind = meta[4 * s];
-        if (kind == kSlotEnd) break;
-        const int u = meta[4 * s + 1], seg = meta[4 * s + 2], seg_end = meta[4 * s + 3];
-        if (u != next_u) {
-            // first unit of a segment: find its pair and load that pair's queries
-            locate(u, pref, a.B, a.K, cb, cg, cj);
-            cnb = pref[cb + 1] - pref[cb];
-            clen = lens_s[cb];
-            first_j = cj;
-            cu_pair = a.K * pref[cb] + cg * cnb;
-            st.reset();
-            nb_b = cb;
-            nb_g = cg;
-            next_pair(pref, a.B, a.K, nb_b, nb_g);
-            if constexpr (kKind == kKernelMma) {
-                load_q_frags<C, D>(a, cb, cg, hbase, r, c, st.qf);
-                if (cu_pair + cnb < seg_end) load_q_frags<C, D>(a, nb_b, nb_g, hbase, r, c, st.qn);
-            } else {
-                fma_load_q<C, D>(a, st, cb, cg, hbase, lane);
-            }
-        }
-        const int nvalid = min((int)kBlock, clen - kBlock * cj);
-        const bool unit_ok = kind == kSlotData;
-        if constexpr (kKind == kKernelMma) {
-            // read the whole slot, hand it back to TMA, then compute from registers
-            MmaFrags<C, D> fr;
-            if (unit_ok) mma_load<C, D>(fr, ring + s * C::kStage, lane, r, c);
-            if (!release_and_refill(k, s)) {
-                bail(k + 1);
-                return;
-            }
-            if (unit_ok) mma_compute<C, D>(st, fr, nvalid, r, c, a.scale_log2);
-        } else {
-            if (unit_ok) fma_block<C, D, T>(a, st, ring + s * C::kStage, nvalid, hbase, lane);
-            if (!release_and_refill(k, s)) {
-                bail(k + 1);
-                return;
-            }
-        }
-
-        const bool last_of_pair = (cj == cnb - 1);
-        const bool last_of_seg = (u == seg_end - 1);
-        next_u = u + 1;
-        if (last_of_pair || last_of_seg) {
-            const bool whole = (first_j == 0) && last_of_pair;
-            if constexpr (kKind == kKernelMma) mma_flush<C, D>(a, st, cb, cg, hbase, whole, seg, r, c);
-            else fma_flush<C, D>(a, st, cb, cg, hbase, whole, seg, lane);
-            if (last_of_seg) {
-                next_u = -1;                   // the next unit starts a new segment
-                continue;
-            }
-            cb = nb_b;
-            cg = nb_g;
-            cj = 0;
-            first_j = 0;
-            cnb = pref[cb + 1] - pref[cb];
-            clen = lens_s[cb];
-            cu_pair = a.K * pref[cb] + cg * cnb;
-            st.reset();
-            next_pair(pref, a.B, a.K, nb_b, nb_g);
-            if constexpr (kKind == kKernelMma) {
-#pragma unroll
-                for (int q = 0; q < D / 16; ++q) st.qf[q] = st.qn[q];
-                if (cu_pair + cnb < seg_end) load_q_frags<C, D>(a, nb_b, nb_g, hbase, r, c, st.qn);
-            } else {
-                fma_load_q<C, D>(a, st, cb, cg, hbase, lane);
-            }
-        } else {
-            ++cj;
-        }
-    }
-}
-
-// ------------------------------------------------------------------ combine
-
-// Merge the splits of each (sequence, query head) row; zero rows of empty
-// sequences. kRowWarps warps share a row (they take its splits in turn and meet
-// in shared memory); a CTA holds kRows rows. CTA 0 also rewinds the run-time
-// work counter for the next call (every split-KV CTA has finished by now).
-template <int D, int kRowWarps, int kRows>
-__global__ void __launch_bounds__(kRowWarps * kRows * 32) combine_kernel(const DecodeArgs a) {
-    static_assert(kRowWarps == 1 || kRows == 1, "rows of several warps need a CTA each");
-    __shared__ float s_red[kRowWarps];
-    __shared__ float s_acc[kRowWarps > 1 ? kRowWarps : 1][kRowWarps > 1 ? D : 1];
-    __shared__ float s_l[kRowWarps];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int sub = warp % kRowWarps;
-    const long long bh = (long long)blockIdx.x * kRows + warp / kRowWarps;
-    launch_dependents();
-    grid_dependency_wait();                    // the split-KV kernel's partials
-    if (blockIdx.x == 0 && tid == 0) *a.ws_ctr = 0ull;
-    if (bh >= (long long)a.B * a.H) return;
-    const int b = (int)(bh / a.H), h = (int)(bh % a.H), g = h / a.G, hh = h % a.G;
-    const long long orow = bh * D;
-    const int p0 = a.ws_pref[b];
-    const int nb = a.ws_pref[b + 1] - p0;
-    if (nb == 0) {
-        for (int i = sub * 32 + lane; i < D; i += kRowWarps * 32) store1(a.out, a.out_dtype, orow + i, 0.f);
-        return;
-    }
-    Partition pt;
-    pt.R = a.ws_hdr[0];
-    pt.U = a.ws_hdr[1];
-    pt.Rs = a.ws_hdr[2];
-    pt.Cz = a.ws_hdr[3];
-    pt.P = a.ws_hdr[4];
-    pt.cpw = a.ws_hdr[5];
-    const int u0 = a.K * p0 + g * nb;
-    const int s0 = pt.segment_of(u0), s1 = pt.segment_of(u0 + nb - 1);
-    if (s0 == s1) return;                      // one segment held the whole pair and wrote it
-    const long long first = (long long)b * a.K + g + s0;   // slot of the first piece
-    const int n = s1 - s0 + 1;
-
-    // pass 1: the largest running maximum (one piece per lane)
-    float M = -INFINITY;
-    for (int p = sub * 32 + lane; p < n; p += kRowWarps * 32)
-        M = fmaxf(M, __ldcg(&a.ws_ml[(first + p) * a.G + hh]).x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-    if constexpr (kRowWarps > 1) {
-        if (lane == 0) s_red[sub] = M;
-        __syncthreads();
-        M = s_red[0];
-#pragma unroll
-        for (int w = 1; w < kRowWarps; ++w) M = fmaxf(M, s_red[w]);
-    }
-
-    // pass 2: each warp takes 32 pieces at a time: lane j learns piece j's weight,
-    // then every lane gathers its dims of all 32 partial vectors with independent
-    // loads. Pieces that saw only skipped blocks hold m = -inf and o = 0.
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const bool has_dims = 4 * lane < D;
-    if (M != -INFINITY) {
-        for (int base = sub * 32; base < n; base += kRowWarps * 32) {
-            const int p = base + lane;
-            float e = 0.f;
-            if (p < n) {
-                const float2 ml = __ldcg(&a.ws_ml[(first + p) * a.G + hh]);
-                e = fast_exp2(ml.x - M);
-                L += ml.y * e;
-            }
-            const int cnt = min(32, n - base);
-            const float* op = a.ws_o + ((first + base) * a.G + hh) * D + 4 * lane;
-            const long long step = (long long)a.G * D;
-#pragma unroll 8
-            for (int j = 0; j < cnt; ++j) {
-                const float ej = __shfl_sync(kFull, e, j);
-                if (has_dims) {
-                    const float4 o = __ldcg(reinterpret_cast<const float4*>(op + j * step));
-                    acc.x += o.x * ej; acc.y += o.y * ej; acc.z += o.z * ej; acc.w += o.w * ej;
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
-    if constexpr (kRowWarps > 1) {
-        if (has_dims) {
-            s_acc[sub][4 * lane + 0] = acc.x;
-            s_acc[sub][4 * lane + 1] = acc.y;
-            s_acc[sub][4 * lane + 2] = acc.z;
-            s_acc[sub][4 * lane + 3] = acc.w;
-        }
-        if (lane == 0) s_l[sub] = L;
-        __syncthreads();
-        float Lt = 0.f;
-#pragma unroll
-        for (int w = 0; w < kRowWarps; ++w) Lt += s_l[w];
-        const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
-        for (int i = tid; i < D; i += blockDim.x) {
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < kRowWarps; ++w) v += s_acc[w][i];
-            store1(a.out, a.out_dtype, orow + i, v * inv);
-        }
-    } else {
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        if (has_dims) {
-            store1(a.out, a.out_dtype, orow + 4 * lane + 0, acc.x * inv);
-            store1(a.out, a.out_dtype, orow + 4 * lane + 1, acc.y * inv);
-            store1(a.out, a.out_dtype, orow + 4 * lane + 2, acc.z * inv);
-            store1(a.out, a.out_dtype, orow + 4 * lane + 3, acc.w * inv);
-        }
-    }
-}
-
-// ------------------------------------------------------------------ host side
-
-struct Variant {
-    const void* fn;
-    int tail_chunks;     // pooled chunks per worker range
-    int warps;           // threads / 32
-    int workers_per_cta; // split-KV workers per CTA
-    int box_inner;       // elements per TMA box row
-    bool swizzle;
-    int (*smem)(int);
-};
-
-template <int kKind, typename T, int D, int NW>
-Variant make_variant() {
-    using C = Cfg<kKind, T, D, NW>;
-    return Variant{reinterpret_cast<const void*>(&split_kv_kernel<kKind, T, D, NW>), C::kTailChunks, C::kWarps,
-                   NW == 1 ? C::kWarps : 1, C::kBoxInner, C::kSwizzle, &Smem<C>::bytes};
-}
-
-template <int kKind, typename T, int D>
-Variant pick_width(int nw) {
-    if (nw == 1) return make_variant<kKind, T, D, 1>();
-    if (nw == 2) return make_variant<kKind, T, D, 2>();
-    if (nw == 4) return make_variant<kKind, T, D, 4>();
-    return make_variant<kKind, T, D, 8>();
-}
-
-template <typename T, int D>
-bool pick_kind(int kind, int nw, Variant& v) {
-    if (kind == kKernelMma) {
-        if constexpr (std::is_same<T, float>::value ||
-                      ((std::is_same<T, int8_t>::value || std::is_same<T, __nv_fp8_e4m3>::value) && D != 128)) {
-            return false;
-        } else {
-            v = pick_width<kKernelMma, T, D>(nw);
-            return true;
-        }
-    }
-    if constexpr (std::is_same<T, float>::value) {
-        v = pick_width<kKernelFma, T, D>(nw);
-        return true;
-    } else {
-        // the CUDA-core kernel serves fp32 caches, and <= 8-head groups of the others
-        if (nw > 1) return false;
-        v = make_variant<kKernelFma, T, D, 1>();
-        return true;
-    }
-}
-
-template <typename T>
-bool pick_dim(int kind, int d, int nw, Variant& v) {
-    if (d == 64) return pick_kind<T, 64>(kind, nw, v);
-    if (d == 128) return pick_kind<T, 128>(kind, nw, v);
-    return false;
-}
+using namespace dec;
 
 struct WsLayout {
     size_t hdr, pref, ml, o, total;
@@ -1238,13 +36,13 @@ long long max_slots(int B, int K, int P, int max_blocks, int min_units, int tail
     return (long long)B * K + (long long)P * (1 + cpw);
 }
 
-WsLayout ws_layout(int B, int K, int G, int D, long long slots) {
+WsLayout ws_layout(int B, int K, int rows, int D, long long slots) {
     WsLayout w;
     w.hdr = 0;
     w.pref = align256(kWsHeaderInts * 4);
     w.ml = w.pref + align256((size_t)(B + 1) * 4);
-    w.o = w.ml + align256((size_t)slots * G * 8);
-    w.total = w.o + align256((size_t)slots * G * D * 4);
+    w.o = w.ml + align256((size_t)slots * rows * 8);
+    w.total = w.o + align256((size_t)slots * rows * D * 4);
     return w;
 }
 
@@ -1262,41 +60,38 @@ int workers_of(const Variant& v, int batch, int num_sms) {
 
 }  // namespace
 
+// Warps that share one pair's tiles for GT query rows per pair (8 rows each).
+int warps_for_rows(int GT) { return GT <= 8 ? 1 : GT <= 16 ? 2 : GT <= 32 ? 4 : 8; }
+
 // The largest workspace any kernel choice needs for this shape: workers are
-// taken from the occupancy of every variant that can serve (G, head_dim).
-size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int head_dim, int num_sms) {
-    const int G = num_heads / num_kv_heads;
-    const int nw = G <= 8 ? 1 : G <= 16 ? 2 : G <= 32 ? 4 : 8;
+// taken from the occupancy of every variant that can serve (G*T, head_dim).
+size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int head_dim, int tokens_per_seq,
+                              int num_sms) {
+    const int GT = num_heads / num_kv_heads * std::max(1, tokens_per_seq);
+    const int nw = warps_for_rows(GT);
     int P = 0;
     for (int kind : {kKernelMma, kKernelFma}) {
-        Variant v{};
-        if (pick_dim<float>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
-        if (pick_dim<__half>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
-        if (pick_dim<__nv_bfloat16>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
-        if (pick_dim<int8_t>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
-        if (pick_dim<__nv_fp8_e4m3>(kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
+        for (int dt : {GQA_DTYPE_F32, GQA_DTYPE_F16, GQA_DTYPE_BF16, GQA_DTYPE_I8, GQA_DTYPE_FP8_E4M3}) {
+            Variant v{};
+            if (pick_plain(dt, kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
+            if (pick_general(dt, kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
+        }
     }
     if (P == 0) P = num_sms * (kMaxWarpsPerSm / nw);      // no occupancy answer: the hard bound
-    return ws_layout(batch, num_kv_heads, G, head_dim,
+    return ws_layout(batch, num_kv_heads, GT, head_dim,
                      max_slots(batch, num_kv_heads, P, 0, 0, kMaxTailChunks)).total;
 }
 
 int launch_decode(const DecodeLaunch& L, int num_sms) {
     const gqa_kv_cache_t& c = *L.cache;
     const int D = c.head_dim, K = c.num_kv_heads, G = L.num_heads / K;
+    const int T = std::max(1, L.tokens_per_seq), GT = G * T;
     int kind = L.kernel;
     if (kind == 0) kind = (c.dtype == GQA_DTYPE_F32 || (dtype_coded(c.dtype) && D != 128)) ? kKernelFma : kKernelMma;
-    const int nw = G <= 8 ? 1 : G <= 16 ? 2 : G <= 32 ? 4 : 8;   // warps sharing one group's tiles
+    const int nw = warps_for_rows(GT);   // warps sharing one pair's tiles
     Variant v{};
-    bool ok = false;
-    switch (c.dtype) {
-        case GQA_DTYPE_F32: ok = pick_dim<float>(kind, D, nw, v); break;
-        case GQA_DTYPE_F16: ok = pick_dim<__half>(kind, D, nw, v); break;
-        case GQA_DTYPE_BF16: ok = pick_dim<__nv_bfloat16>(kind, D, nw, v); break;
-        case GQA_DTYPE_I8: ok = pick_dim<int8_t>(kind, D, nw, v); break;
-        case GQA_DTYPE_FP8_E4M3: ok = pick_dim<__nv_fp8_e4m3>(kind, D, nw, v); break;
-        default: ok = false;
-    }
+    const bool general = T > 1 || L.window > 0;
+    const bool ok = general ? pick_general(c.dtype, kind, D, nw, v) : pick_plain(c.dtype, kind, D, nw, v);
     if (!ok) return GQA_ERR_UNSUPPORTED;
 
     CUtensorMap kmap, vmap;
@@ -1316,7 +111,7 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
 
     const int min_units = L.min_blocks_per_warp > 0 ? L.min_blocks_per_warp : 4;
     const WsLayout wl =
-        ws_layout(L.batch, K, G, D, max_slots(L.batch, K, P, L.max_blocks, min_units, v.tail_chunks));
+        ws_layout(L.batch, K, GT, D, max_slots(L.batch, K, P, L.max_blocks, min_units, v.tail_chunks));
     if (L.workspace == nullptr || L.workspace_bytes < wl.total) return GQA_ERR_WORKSPACE;
 
     DecodeArgs a;
@@ -1338,6 +133,9 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     a.H = L.num_heads;
     a.K = K;
     a.G = G;
+    a.T = T;
+    a.GT = GT;
+    a.window = L.window;
     a.max_blocks = L.max_blocks;
     a.out_dtype = L.out_dtype;
     a.q_dtype = L.q_dtype;
@@ -1392,7 +190,7 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
         rows_per_cta = 1;
         cthreads = 1024;
     }
-    const long long rows = (long long)L.batch * L.num_heads;
+    const long long rows = (long long)L.batch * T * L.num_heads;
     cudaLaunchConfig_t ccfg = {};
     ccfg.gridDim = dim3((unsigned)((rows + rows_per_cta - 1) / rows_per_cta));
     ccfg.blockDim = dim3(cthreads);

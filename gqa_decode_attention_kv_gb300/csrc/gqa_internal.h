@@ -35,7 +35,7 @@ constexpr int kMaxGroup = 64;   // query heads per KV head the kernels serve
 
 cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const void* v_new,
                              int new_dtype, const int32_t* block_tables, int max_blocks,
-                             const int32_t* positions, int batch, int32_t* err,
+                             const int32_t* positions, int batch, int tokens_per_seq, int32_t* err,
                              cudaStream_t stream);
 
 struct DecodeLaunch {
@@ -52,6 +52,8 @@ struct DecodeLaunch {
     int out_dtype;
     void* workspace;
     size_t workspace_bytes;
+    int tokens_per_seq;         // T >= 1 queries per sequence (q, out: [B, T, H, d])
+    int window;                 // sliding window in tokens, 0 = full attention
     int kernel;                 // KernelKind
     int max_warps;              // 0 = fill the GPU
     int min_blocks_per_warp;
@@ -60,8 +62,10 @@ struct DecodeLaunch {
     cudaStream_t stream;
 };
 
-// Bytes of workspace for a shape given the device's SM count.
-size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int head_dim, int num_sms);
+// Bytes of workspace for a shape (T query tokens per sequence) given the
+// device's SM count.
+size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int head_dim, int tokens_per_seq,
+                              int num_sms);
 
 // Validated launch; returns a gqa_status_t.
 int launch_decode(const DecodeLaunch& L, int num_sms);

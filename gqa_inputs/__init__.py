@@ -49,6 +49,8 @@ class Workload:
     q_dtype: str                # "f32" | "f16" | "bf16"
     lens: str                   # "fixed:<a,b,...>" | "const:<S>" | "uniform:<lo>:<hi>"
     contiguous: bool = False    # un-paged [B, S_pad, K, d] buffer + identity table
+    queries: int = 1            # new tokens per sequence (causal among themselves)
+    window: int = 0             # sliding window in tokens; 0 = full attention
 
     @property
     def group_size(self) -> int:
@@ -110,7 +112,7 @@ class DecodeCase:
     cache_dtype: str
     q_dtype: str
     scale: float
-    q: torch.Tensor                 # [B, H, d] q_dtype
+    q: torch.Tensor                 # [B, H, d] q_dtype ([B, T, H, d] for T > 1 queries)
     k_cache: torch.Tensor           # pool or contiguous buffer, cache dtype
     v_cache: torch.Tensor
     k_scale: Optional[torch.Tensor]  # [num_blocks, K, 16] fp16 (int8 caches only)
@@ -121,8 +123,9 @@ class DecodeCase:
     stride_token: int
     block_table: torch.Tensor       # [B, max_blocks] int32
     context_lens: torch.Tensor      # [B] int32, tokens valid for the decode
-    k_new: torch.Tensor             # [B, K, d] new token (input dtype of append)
+    k_new: torch.Tensor             # [B, K, d] new token(s) (input dtype of append; [B, T, K, d])
     v_new: torch.Tensor
+    queries: int = 1                # T new tokens per sequence
 
     @property
     def max_blocks(self) -> int:
@@ -138,12 +141,13 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
               q_dtype: Optional[str] = None, seed: int = 0, device: str = "cpu",
               contiguous: bool = False, shuffle: bool = True, spare_blocks: int = 0,
               extra_tokens: int = 0, max_blocks: Optional[int] = None, poison: bool = True,
-              new_dtype: Optional[str] = None, q_zero: bool = False) -> DecodeCase:
+              new_dtype: Optional[str] = None, q_zero: bool = False, queries: int = 1) -> DecodeCase:
     """Draw one seeded decode case.
 
     ``lens`` are the lengths the decode attends to. Sequence ``b`` owns
     ``ceil((lens[b] + extra_tokens) / 16)`` physical blocks, so ``extra_tokens=1``
-    leaves room to append a token at position ``lens[b]``.
+    leaves room to append a token at position ``lens[b]``. ``queries`` = T > 1
+    draws T query tokens and T new K/V tokens per sequence ([B, T, ...] shapes).
     Values: Q, K, V ~ N(0, 1) rounded to their storage dtype; int8 caches hold
     uniform codes in [-127, 127] with fp16 scales in [0.015, 0.035] (the scale a
     row of 128 N(0,1) draws gets from its max magnitude); FP8 caches hold e4m3
@@ -208,14 +212,15 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
     if poison:
         _poison_unowned(kc, vc, ks, vs, table, lens_t, contiguous, cache_dtype)
 
-    q = _randn((batch, num_heads, d), gen_dev, dev, DTYPES[q_dtype])
+    tq = (queries,) if queries > 1 else ()
+    q = _randn((batch, *tq, num_heads, d), gen_dev, dev, DTYPES[q_dtype])
     if q_zero:
         q.zero_()
-    k_new = _randn((batch, K, d), gen_dev, dev, DTYPES[new_dtype])
-    v_new = _randn((batch, K, d), gen_dev, dev, DTYPES[new_dtype])
+    k_new = _randn((batch, *tq, K, d), gen_dev, dev, DTYPES[new_dtype])
+    v_new = _randn((batch, *tq, K, d), gen_dev, dev, DTYPES[new_dtype])
     return DecodeCase(batch, num_heads, K, d, cache_dtype, q_dtype, 1.0 / math.sqrt(d),
                       q, kc, vc, ks, vs, num_blocks, sb, sh, st, table.to(dev),
-                      lens_t.to(dev), k_new, v_new)
+                      lens_t.to(dev), k_new, v_new, queries)
 
 
 def _poison_unowned(kc, vc, ks, vs, table, lens, contiguous, cache_dtype):

@@ -102,8 +102,22 @@ typedef struct {
     int64_t stride_token;     /* elements */
 } gqa_kv_cache_t;
 
-/* Optional knobs of gqa_decode (pass NULL for the defaults). */
+/*
+ * Options of gqa_decode. NULL, or a zero-filled struct, gives the plain decode
+ * step: one new token per sequence, full attention, automatic kernel choice.
+ *  tokens_per_seq  T >= 1 new tokens (queries) per sequence, causal among
+ *                  themselves (speculative verification, "LLM 推理性能优化实战"
+ *                  section 14.2; chunked prefill next to decode, section 11.7).
+ *                  0 means 1. q and out become [batch, T, num_heads, head_dim].
+ *  sliding_window  W > 0: every query attends only the last W positions up to
+ *                  and including its own (sliding-window attention, section
+ *                  6.4.1); 0 = full attention. Blocks wholly before a query's
+ *                  window are never read, so their table entries may hold
+ *                  anything (a caller may recycle those blocks).
+ */
 typedef struct {
+    int32_t tokens_per_seq;       /* 0 or 1: one new token per sequence */
+    int32_t sliding_window;       /* 0: full attention */
     int32_t kernel;               /* 0 auto, 1 tensor-core (mma.sync) kernel, 2 CUDA-core kernel */
     int32_t max_warps;            /* 0 = fill the GPU; > 0 caps the split-KV workers, i.e. KV splits */
     int32_t min_blocks_per_warp;  /* 0 = default (4): smallest KV range one warp takes */
@@ -127,14 +141,14 @@ GQA_API int gqa_version(void);
 GQA_API int64_t gqa_kv_pool_elements(int64_t num_blocks, int32_t num_kv_heads, int32_t head_dim);
 
 /*
- * Paged KV append: write the new token of every sequence into the cache.
- * For each b < batch and kv-head g < K, with pos = positions[b]:
+ * Paged KV append: write the T new tokens of every sequence into the cache.
+ * For each b < batch, i < T and kv-head g < K, with pos = positions[b] + i:
  *   block = block_tables[b*max_blocks_per_seq + pos/16], slot = pos % 16,
- *   K[block, g, slot, :] = k_new[b, g, :],  V[...] = v_new[b, g, :].
+ *   K[block, g, slot, :] = k_new[b, i, g, :],  V[...] = v_new[b, i, g, :].
  * (The write of one token's K and V per step, "LLM 推理性能优化实战" sections
  * 5.3-5.4; the block table of section 8.2.)
  *
- *  k_new, v_new   device, [batch, K, head_dim] of new_dtype, 16-byte aligned.
+ *  k_new, v_new   device, [batch, T, K, head_dim] of new_dtype, 16-byte aligned.
  *                 For F32/F16/BF16 caches new_dtype must equal the cache dtype
  *                 and the copy is bit-exact. For an I8 cache new_dtype is F32,
  *                 F16 or BF16 and each (token, kv-head) row is quantised on the
@@ -146,29 +160,36 @@ GQA_API int64_t gqa_kv_pool_elements(int64_t num_blocks, int32_t num_kv_heads, i
  *                 rounded to nearest even and saturated to +-448 (the FP8 option
  *                 of section 15.5). The scale goes to k_scale / v_scale.
  *  block_tables   device int32 [batch, max_blocks_per_seq].
- *  positions      device int32 [batch]: slot index of the new token, i.e. the
- *                 context length BEFORE the append. Not modified; the caller
- *                 advances its context lengths.
+ *  positions      device int32 [batch]: position of the first new token, i.e.
+ *                 the context length BEFORE the append. Not modified; the
+ *                 caller advances its context lengths by T.
+ *  tokens_per_seq T >= 1 (0 means 1).
  *  err_flag       device int32 or NULL (GQA_DEVERR_POSITION / _BLOCK_INDEX).
+ *                 A token whose position or block is out of range is skipped.
  */
 GQA_API int gqa_kv_append(const gqa_kv_cache_t *cache, const void *k_new, const void *v_new,
                   int32_t new_dtype, const int32_t *block_tables,
                   int32_t max_blocks_per_seq, const int32_t *positions, int32_t batch,
-                  int32_t *err_flag, void *stream);
+                  int32_t tokens_per_seq, int32_t *err_flag, void *stream);
 
 /*
- * Bytes of device workspace gqa_decode needs for this shape on `device`
- * (-1 = the current device). Returns 0 on bad arguments. The bound covers every
- * kernel choice and every context-length mix of this shape.
+ * Bytes of device workspace gqa_decode needs for this shape (tokens_per_seq as
+ * in gqa_decode_opts_t, 0 meaning 1) on `device` (-1 = the current device).
+ * Returns 0 on bad arguments. The bound covers every kernel choice, window and
+ * context-length mix of this shape.
  */
 GQA_API size_t gqa_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t num_kv_heads,
-                                 int32_t head_dim, int32_t device);
+                                 int32_t head_dim, int32_t tokens_per_seq, int32_t device);
 
 /*
  * Grouped-query decode attention over the paged cache:
  *   out[b, h, :] = sum_t softmax_t(scale * q[b,h,:] . K[b, t, g]) V[b, t, g],
  *   g = h / (num_heads / K), t in [0, context_lens[b]),
- * where K[b, t, g] is read through block_tables as in gqa_kv_append.
+ * where K[b, t, g] is read through block_tables as in gqa_kv_append. With
+ * T = opts->tokens_per_seq > 1 the queries q[b, i] (i < T) sit at positions
+ * context_lens[b] - T + i and query i attends t <= context_lens[b] - T + i
+ * (a query at a negative position gets a zero row); with W =
+ * opts->sliding_window > 0 only t > (its position) - W.
  * The KV range of each (sequence, kv-head) is split across warps
  * (split-KV flash decoding, "LLM 推理性能优化实战" section 10.2); each split
  * keeps a running (max, sum, weighted V) state (online softmax, section 9.2)
@@ -176,23 +197,23 @@ GQA_API size_t gqa_decode_workspace_size(int32_t batch, int32_t num_heads, int32
  * ("global max and sum" reduction of section 10.2). An empty context
  * (length 0) yields a zero output row.
  *
- *  q              device [batch, num_heads, head_dim]; BF16 for a BF16 cache,
+ *  q              device [batch, T, num_heads, head_dim]; BF16 for a BF16 cache,
  *                 F16 for F16, F32 for F32, BF16 or F16 for a coded cache.
  *  block_tables   device int32 [batch, max_blocks_per_seq].
- *  context_lens   device int32 [batch], lengths AFTER the append, each in
- *                 [0, max_blocks_per_seq*16].
+ *  context_lens   device int32 [batch], lengths AFTER the append (the T new
+ *                 tokens included), each in [0, max_blocks_per_seq*16].
  *  scale          softmax scale (1/sqrt(head_dim) for standard attention).
- *  out            device [batch, num_heads, head_dim] of out_dtype (F32, BF16
- *                 or F16); 16-byte aligned.
+ *  out            device [batch, T, num_heads, head_dim] of out_dtype (F32,
+ *                 BF16 or F16); 16-byte aligned.
  *  workspace      device, >= gqa_decode_workspace_size(...) bytes, 256-byte
  *                 aligned, zero-filled before its first use (one word of it, the
  *                 run-time work counter, must start at zero; every call leaves it
  *                 at zero again). Otherwise clobbered by each call. Calls that
  *                 share a workspace must not overlap on the GPU.
- *  opts           NULL or tuning knobs (gqa_decode_opts_t).
- *  Limits: num_heads % K == 0; num_heads / K <= 64 (groups above 8 need a
- *  BF16/F16 cache, a coded cache with head_dim 128, or an F32 cache); batch <= 8191;
- *  batch * K * max_blocks_per_seq < 2^31.
+ *  opts           NULL or options (gqa_decode_opts_t).
+ *  Limits: num_heads % K == 0; T * num_heads / K <= 64 query rows per kv-head
+ *  (above 8 rows: a BF16/F16 cache, a coded cache with head_dim 128, or an F32
+ *  cache); sliding_window >= 0; batch <= 8191; batch * K * max_blocks_per_seq < 2^31.
  */
 GQA_API int gqa_decode(const gqa_kv_cache_t *cache, const void *q, int32_t q_dtype,
                int32_t num_heads, const int32_t *block_tables, int32_t max_blocks_per_seq,

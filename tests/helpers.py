@@ -20,8 +20,8 @@ def _host(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy()
 
 
-def oracle_for_case(case, rows=None, nthreads: int = 0, host_pools=None) -> np.ndarray:
-    """fp64 oracle output [len(rows), H, d] for the sequences in ``rows``."""
+def oracle_for_case(case, rows=None, nthreads: int = 0, host_pools=None, window: int = 0) -> np.ndarray:
+    """fp64 oracle output [len(rows), (T,) H, d] for the sequences in ``rows``."""
     import oracle
     lens = case.context_lens.cpu().numpy()
     table = case.block_table.cpu().numpy()
@@ -44,7 +44,7 @@ def oracle_for_case(case, rows=None, nthreads: int = 0, host_pools=None) -> np.n
             vd = oracle.dequantize_fp8(oracle.gather_dense(vp, table, lens, case.stride_block,
                                        case.stride_head, case.stride_token, K, d, rows), vs)
     q = case.q.detach().float().cpu().numpy().astype(np.float64)[rows]
-    return oracle.decode(q, kd, vd, lens[rows], case.scale, nthreads)
+    return oracle.decode(q, kd, vd, lens[rows], case.scale, nthreads, window=window)
 
 
 def max_abs_err(gpu_out: torch.Tensor, ref: np.ndarray, rows=None) -> float:

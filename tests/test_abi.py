@@ -67,9 +67,10 @@ def _desc(**kw):
 
 
 def _decode(lib, desc, q=0x30000, q_dtype=2, H=32, table=0x40000, maxb=8, lens=0x50000, B=4,
-            scale=0.1, out=0x60000, out_dtype=0, ws=0x70000, ws_bytes=1 << 20):
+            scale=0.1, out=0x60000, out_dtype=0, ws=0x70000, ws_bytes=1 << 20, T=0, window=0):
+    opts = gq.DecodeOpts(T, window, 0, 0, 0, None, None)
     return lib.gqa_decode(ctypes.byref(desc), q, q_dtype, H, table, maxb, lens, B, scale, out,
-                          out_dtype, ws, ws_bytes, None, None, None)
+                          out_dtype, ws, ws_bytes, ctypes.byref(opts), None, None)
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -98,6 +99,11 @@ def test_cache_description_checks(lib, kw, expect):
     (dict(scale=float("nan")), INVALID),
     (dict(out=None), INVALID),
     (dict(B=0), OK),                                 # empty batch: nothing to launch
+    (dict(T=-1), INVALID),
+    (dict(window=-5), INVALID),
+    (dict(T=17), UNSUPPORTED),                       # G*T = 4*17 = 68 query rows > 64
+    (dict(T=16, B=0), OK),                           # 64 rows: allowed
+    (dict(window=7, B=0), OK),
 ])
 def test_decode_argument_checks(lib, kw, expect):
     assert _decode(lib, _desc(), **kw) == expect
@@ -106,12 +112,13 @@ def test_decode_argument_checks(lib, kw, expect):
 def test_append_argument_checks(lib):
     d = _desc()
     f = lib.gqa_kv_append
-    assert f(ctypes.byref(d), 0x1000, 0x2000, 2, 0x3000, 8, 0x4000, 0, None, None) == OK
-    assert f(ctypes.byref(d), 0x1004, 0x2000, 2, 0x3000, 8, 0x4000, 4, None, None) == INVALID
-    assert f(ctypes.byref(d), 0x1000, 0x2000, 0, 0x3000, 8, 0x4000, 4, None, None) == UNSUPPORTED
-    assert f(ctypes.byref(d), None, 0x2000, 2, 0x3000, 8, 0x4000, 4, None, None) == INVALID
+    assert f(ctypes.byref(d), 0x1000, 0x2000, 2, 0x3000, 8, 0x4000, 0, 1, None, None) == OK
+    assert f(ctypes.byref(d), 0x1004, 0x2000, 2, 0x3000, 8, 0x4000, 4, 1, None, None) == INVALID
+    assert f(ctypes.byref(d), 0x1000, 0x2000, 0, 0x3000, 8, 0x4000, 4, 1, None, None) == UNSUPPORTED
+    assert f(ctypes.byref(d), None, 0x2000, 2, 0x3000, 8, 0x4000, 4, 1, None, None) == INVALID
+    assert f(ctypes.byref(d), 0x1000, 0x2000, 2, 0x3000, 8, 0x4000, 4, -1, None, None) == INVALID
     i8 = _desc(dtype=3, k_scale=0x80000, v_scale=0x90000)
-    assert f(ctypes.byref(i8), 0x1000, 0x2000, 3, 0x3000, 8, 0x4000, 4, None, None) == UNSUPPORTED
+    assert f(ctypes.byref(i8), 0x1000, 0x2000, 3, 0x3000, 8, 0x4000, 4, 1, None, None) == UNSUPPORTED
 
 
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
