@@ -39,23 +39,34 @@ KERNEL_NAME = "split_kv_kernel"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kv_kernel_traffic.txt")
 
 
+def attended_range(wl, L: int) -> tuple:
+    """First position any query of a length-L sequence attends, and L: with T
+    new tokens and a window W the union of the queries' ranges is
+    [max(0, L - T + 1 - W), L)."""
+    lo = max(0, L - wl.queries + 1 - wl.window) if wl.window > 0 else 0
+    return lo, L
+
+
 def algorithmic_bytes(wl, lens) -> dict:
-    """Bytes a decode step must move: KV (+scales) of every cached token once,
-    q in, out (fp32) out, block-table entries and lengths, plus the append."""
+    """Bytes a decode step must move: KV (+scales) of every attended cached
+    token once, q in, out (fp32) out, block-table entries and lengths, plus the
+    append of the T new tokens."""
     es = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1, "fp8": 1}[wl.cache_dtype]
     qes = {"f32": 4, "f16": 2, "bf16": 2}[wl.q_dtype]
-    tokens = int(sum(int(x) for x in lens))
+    T = wl.queries
+    ranges = [attended_range(wl, int(x)) for x in lens]
+    tokens = int(sum(hi - lo for lo, hi in ranges))
     per_token = 2 * wl.num_kv_heads * wl.head_dim * es
     if wl.cache_dtype in ("i8", "fp8"):
         per_token += 2 * wl.num_kv_heads * 2
-    blocks = int(sum(-(-int(x) // 16) for x in lens))
+    blocks = int(sum(-(-hi // 16) - lo // 16 for lo, hi in ranges))
     B = len(lens)
     kv = tokens * per_token
-    q = B * wl.num_heads * wl.head_dim * qes
-    o = B * wl.num_heads * wl.head_dim * 4
+    q = B * T * wl.num_heads * wl.head_dim * qes
+    o = B * T * wl.num_heads * wl.head_dim * 4
     meta = blocks * 4 + B * 4
     new_es = qes if wl.cache_dtype in ("i8", "fp8") else es
-    append = B * 2 * wl.num_kv_heads * wl.head_dim * (new_es + es) + B * 4
+    append = B * T * 2 * wl.num_kv_heads * wl.head_dim * (new_es + es) + B * 4
     decode = kv + q + o + meta
     return {"kv": kv, "decode": decode, "append": append, "step": decode + append,
             "tokens": tokens, "blocks": blocks}
@@ -215,10 +226,10 @@ def run_ours(args):
     case = gi.case_for(wl, seed=args.seed + rank, device=str(dev), extra_tokens=0)
     cache = gq.cache_from_case(case)
     lens = case.context_lens
-    pos = (lens - 1).clamp(min=0)             # the step re-appends the last token
+    pos = (lens - wl.queries).clamp(min=0)    # the step re-appends the last T tokens
     ab = algorithmic_bytes(wl, lens.cpu().tolist())
-    out = torch.empty((wl.batch, wl.num_heads, wl.head_dim), dtype=torch.float32, device=dev)
-    ws = gq.workspace_for(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim, dev)
+    out = torch.empty(case.q.shape, dtype=torch.float32, device=dev)
+    ws = gq.workspace_for(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim, dev, wl.queries)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     kern = kernel_code(args.kernel)
     stream = torch.cuda.current_stream()
@@ -227,7 +238,7 @@ def run_ours(args):
     def step(events=None):
         gq.kv_append(cache, case.k_new, case.v_new, case.block_table, pos, err=err)
         gq.gqa_decode(cache, case.q, case.block_table, lens, case.scale, out=out, workspace=ws,
-                      kernel=kern, events=events, err=err)
+                      kernel=kern, events=events, err=err, window=wl.window)
 
     # warm-up
     for _ in range(max(3, args.warmup)):
@@ -286,7 +297,7 @@ def run_ours(args):
         vn_d.copy_(vn_h, non_blocking=True)
         gq.kv_append(cache, kn_d, vn_d, case.block_table, pos, err=err)
         gq.gqa_decode(cache, q_d, case.block_table, lens, case.scale, out=out, workspace=ws,
-                      kernel=kern, err=err)
+                      kernel=kern, err=err, window=wl.window)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
@@ -331,11 +342,12 @@ def run_ours(args):
                        "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
                        "context_lens": wl.lens, "cache_dtype": wl.cache_dtype,
                        "q_dtype": wl.q_dtype, "block_size": 16, "block_table": "seeded shuffle",
+                       "tokens_per_seq": wl.queries, "sliding_window": wl.window,
                        "kernel": args.kernel,
                        "l2": f"inputs larger than L2: {ab['kv'] / 1e9:.2f} GB of K/V per step > 129 MB",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "step": "kv_append + gqa_decode (split-KV + combine), one attention layer"},
-            "tokens_per_s": round(wl.batch * world / (ms * 1e-3), 1),
+            "tokens_per_s": round(wl.batch * wl.queries * world / (ms * 1e-3), 1),
             "pct_of_peak": {"measured_hbm": round(100 * gbs / world / hbm, 2),
                             "nominal_8tbs": round(100 * gbs / world / 8000.0, 2)},
             "roofline": {"bound": "hbm", "achieved": round(kern_gbs, 2), "peak": hbm,
@@ -405,6 +417,11 @@ def _oracle_inputs(wl, case, rows):
     return q, kd, vd, sub_lens
 
 
+def _oracle_decode(wl, q, kd, vd, sl, scale, threads):
+    import oracle
+    return oracle.decode(q, kd, vd, sl, scale, nthreads=threads, window=wl.window)
+
+
 def cpu_baseline(wl, case, seconds: float) -> dict:
     """Time the oracle, as it stands, on a bounded sample of the workload: as
     many sequences as fit in about `seconds` of host time, repeating the whole
@@ -414,19 +431,19 @@ def cpu_baseline(wl, case, seconds: float) -> dict:
     threads = oracle.num_cpus()
     q, kd, vd, sl = _oracle_inputs(wl, case, [0])
     t = time.perf_counter()
-    oracle.decode(q, kd, vd, sl, case.scale, nthreads=threads)
+    _oracle_decode(wl, q, kd, vd, sl, case.scale, threads)
     one = max(time.perf_counter() - t, 1e-4)
     n = max(1, min(wl.batch, int(seconds / one)))
     rows = list(range(n))
     q, kd, vd, sl = _oracle_inputs(wl, case, rows)
     t = time.perf_counter()
-    oracle.decode(q, kd, vd, sl, case.scale, nthreads=threads)
+    _oracle_decode(wl, q, kd, vd, sl, case.scale, threads)
     dt = time.perf_counter() - t
     reps = max(1, int(seconds / max(dt, 1e-3))) if n == wl.batch else 1
     if reps > 1:
         t = time.perf_counter()
         for _ in range(reps):
-            oracle.decode(q, kd, vd, sl, case.scale, nthreads=threads)
+            _oracle_decode(wl, q, kd, vd, sl, case.scale, threads)
         dt = (time.perf_counter() - t) / reps
     lens = case.context_lens.cpu().tolist()
     sub = algorithmic_bytes(wl, [lens[b] for b in rows])
@@ -455,11 +472,11 @@ def run_reference(args):
     lens = case.context_lens.cpu().tolist()
     sample_bytes = algorithmic_bytes(wl, [lens[b] for b in rows])["decode"]
     for _ in range(max(3, args.warmup)):
-        oracle.decode(q, kd, vd, sl, case.scale, nthreads=threads)
+        _oracle_decode(wl, q, kd, vd, sl, case.scale, threads)
     times = []
     for _ in range(args.steps):
         t = time.perf_counter()
-        oracle.decode(q, kd, vd, sl, case.scale, nthreads=threads)
+        _oracle_decode(wl, q, kd, vd, sl, case.scale, threads)
         times.append(time.perf_counter() - t)
     dt = statistics.mean(times)
     v = round(sample_bytes / dt / 1e9, 4)

@@ -57,7 +57,7 @@ class Workload:
         return self.num_heads // self.num_kv_heads
 
 
-# The five decode-step workloads. Names say what they are; sizes are the ones the
+# The decode-step workloads. Names say what they are; sizes are the ones the
 # tests and the benchmark use.
 WORKLOADS = {
     "tiny_f32_contiguous": Workload("tiny_f32_contiguous", 2, 8, 2, 64, "f32", "f32",
@@ -74,6 +74,13 @@ WORKLOADS = {
                                    "uniform:2048:8192"),
     "fp8kv_b128_ragged": Workload("fp8kv_b128_ragged", 128, 64, 8, 128, "fp8", "bf16",
                                   "uniform:2048:8192"),
+    # four new tokens per sequence (speculative verification of three drafts),
+    # Llama-3-8B shape; the lengths include the new tokens
+    "spec_verify_bf16_b64_s4096_t4": Workload("spec_verify_bf16_b64_s4096_t4", 64, 32, 8, 128,
+                                              "bf16", "bf16", "const:4096", queries=4),
+    # sliding window of 4096 tokens over 16K-token contexts, Mistral-7B shape
+    "mistral7b_swa_bf16_b64_s16384_w4096": Workload("mistral7b_swa_bf16_b64_s16384_w4096", 64, 32, 8,
+                                                    128, "bf16", "bf16", "const:16384", window=4096),
 }
 
 
@@ -256,4 +263,5 @@ def case_for(workload: Workload, seed: int = 0, device: str = "cpu", **kw) -> De
     lens = draw_lens(workload.lens, workload.batch, seed)
     return make_case(workload.batch, workload.num_heads, workload.num_kv_heads,
                      workload.head_dim, lens, workload.cache_dtype, workload.q_dtype,
-                     seed=seed, device=device, contiguous=workload.contiguous, **kw)
+                     seed=seed, device=device, contiguous=workload.contiguous,
+                     queries=workload.queries, **kw)

@@ -267,8 +267,8 @@ def _sampled(gq, wl, rows, seed=0, **kw):
     """Decode a full-size workload with the default launch, then check the
     sampled sequences (every head) against the oracle."""
     case = gi.case_for(wl, seed=seed, device="cuda")
-    out = _run(gq, case, **kw)
-    ref = oracle_for_case(case, rows=rows, host_pools=_host_pools(case))
+    out = _run(gq, case, window=wl.window, **kw)
+    ref = oracle_for_case(case, rows=rows, host_pools=_host_pools(case), window=wl.window)
     return max_abs_err(out, ref, rows=rows)
 
 
@@ -288,6 +288,8 @@ def _host_pools(case):
     ("long_ctx_bf16_b1_s131072", [0]),
     ("int8kv_b128_ragged", [0, 64, 127]),
     ("fp8kv_b128_ragged", [0, 77, 127]),
+    ("spec_verify_bf16_b64_s4096_t4", [0, 40, 63]),
+    ("mistral7b_swa_bf16_b64_s16384_w4096", [0, 63]),
 ])
 def test_full_size_workloads_sampled(gq, name, rows):
     assert _sampled(gq, gi.WORKLOADS[name], rows) <= TOL
