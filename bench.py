@@ -185,6 +185,20 @@ def dist_info():
     return world, rank, local
 
 
+def resolve_workload(name: str):
+    """A named workload, or the 70B-shaped KV-head sweep point '<70B name>_k<K>'."""
+    import gqa_inputs as gi
+    if name in gi.WORKLOADS:
+        return gi.WORKLOADS[name]
+    base, _, k = name.rpartition("_k")
+    if base == "llama70b_bf16_b32_ragged" and k.isdigit():
+        return gi.kv_sweep_workload(int(k))
+    raise SystemExit(f"unknown workload {name!r}")
+
+
+ROW_LAYOUT = {"auto": 0, "split": 1, "shared": 2}
+
+
 def kernel_code(name: str) -> int:
     return {"auto": 0, "mma": 1, "fma": 2}[name]
 
@@ -222,7 +236,7 @@ def run_ours(args):
     gbuild.build()
     gq.load()
 
-    wl = gi.WORKLOADS[args.workload]
+    wl = resolve_workload(args.workload)
     case = gi.case_for(wl, seed=args.seed + rank, device=str(dev), extra_tokens=0)
     cache = gq.cache_from_case(case)
     lens = case.context_lens
@@ -232,13 +246,14 @@ def run_ours(args):
     ws = gq.workspace_for(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim, dev, wl.queries)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     kern = kernel_code(args.kernel)
+    layout = ROW_LAYOUT[args.row_layout]
     stream = torch.cuda.current_stream()
     launches_per_step = 3
 
     def step(events=None):
         gq.kv_append(cache, case.k_new, case.v_new, case.block_table, pos, err=err)
         gq.gqa_decode(cache, case.q, case.block_table, lens, case.scale, out=out, workspace=ws,
-                      kernel=kern, events=events, err=err, window=wl.window)
+                      kernel=kern, events=events, err=err, window=wl.window, row_layout=layout)
 
     # warm-up
     for _ in range(max(3, args.warmup)):
@@ -297,7 +312,7 @@ def run_ours(args):
         vn_d.copy_(vn_h, non_blocking=True)
         gq.kv_append(cache, kn_d, vn_d, case.block_table, pos, err=err)
         gq.gqa_decode(cache, q_d, case.block_table, lens, case.scale, out=out, workspace=ws,
-                      kernel=kern, err=err, window=wl.window)
+                      kernel=kern, err=err, window=wl.window, row_layout=layout)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
@@ -343,7 +358,7 @@ def run_ours(args):
                        "context_lens": wl.lens, "cache_dtype": wl.cache_dtype,
                        "q_dtype": wl.q_dtype, "block_size": 16, "block_table": "seeded shuffle",
                        "tokens_per_seq": wl.queries, "sliding_window": wl.window,
-                       "kernel": args.kernel,
+                       "kernel": args.kernel, "row_layout": args.row_layout,
                        "l2": f"inputs larger than L2: {ab['kv'] / 1e9:.2f} GB of K/V per step > 129 MB",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "step": "kv_append + gqa_decode (split-KV + combine), one attention layer"},
@@ -463,7 +478,7 @@ def run_reference(args):
     import gqa_inputs as gi
     import oracle
     oracle.build()
-    wl = gi.WORKLOADS[args.workload]
+    wl = resolve_workload(args.workload)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     case = gi.case_for(wl, seed=args.seed, device=dev, extra_tokens=0)
     threads = oracle.num_cpus()
@@ -504,6 +519,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--kernel", choices=["auto", "mma", "fma"], default="auto")
+    ap.add_argument("--row-layout", choices=list(ROW_LAYOUT), default="auto",
+                    help="more than 8 query rows per kv-head: 8-row unit streams or a shared ring")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -60,7 +60,7 @@ class DecodeOpts(ctypes.Structure):
     """Mirror of gqa_decode_opts_t."""
     _fields_ = [("tokens_per_seq", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
                 ("kernel", ctypes.c_int32), ("max_warps", ctypes.c_int32),
-                ("min_blocks_per_warp", ctypes.c_int32),
+                ("min_blocks_per_warp", ctypes.c_int32), ("row_layout", ctypes.c_int32),
                 ("event_main_begin", ctypes.c_void_p), ("event_main_end", ctypes.c_void_p)]
 
 
@@ -221,7 +221,7 @@ def gqa_decode(cache: PagedKVCache, q: torch.Tensor, block_tables: torch.Tensor,
                out_dtype: torch.dtype = torch.float32, workspace: Optional[torch.Tensor] = None,
                kernel: int = KERNEL_AUTO, max_warps: int = 0, min_blocks_per_warp: int = 0,
                events: Optional[tuple] = None, err: Optional[torch.Tensor] = None,
-               stream=None, window: int = 0) -> torch.Tensor:
+               stream=None, window: int = 0, row_layout: int = 0) -> torch.Tensor:
     """out[b,h] = softmax(scale * q[b,h] . K_g^T) V_g over context_lens[b] cached tokens.
 
     q is [B, H, d] (one new token per sequence) or [B, T, H, d] (T new tokens,
@@ -233,7 +233,7 @@ def gqa_decode(cache: PagedKVCache, q: torch.Tensor, block_tables: torch.Tensor,
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     if workspace is None:
         workspace = workspace_for(B, H, cache.num_kv_heads, d, q.device, T)
-    opts = DecodeOpts(T, window, kernel, max_warps, min_blocks_per_warp, None, None)
+    opts = DecodeOpts(T, window, kernel, max_warps, min_blocks_per_warp, row_layout, None, None)
     if events is not None:
         opts.event_main_begin = events[0].cuda_event
         opts.event_main_end = events[1].cuda_event
@@ -260,7 +260,7 @@ def gqa_decode_noalloc(cache: PagedKVCache, q: torch.Tensor, block_tables: torch
     B, H, d = q.shape[0], q.shape[-2], q.shape[-1]
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
-    opts = DecodeOpts(T, window, kernel, 0, 0, None, None)
+    opts = DecodeOpts(T, window, kernel, 0, 0, 0, None, None)
     desc = cache.desc()
     st = load().gqa_decode_noalloc(ctypes.byref(desc), _ptr(q), DTYPE_CODE[q.dtype], H,
                                    _ptr(block_tables), int(block_tables.shape[1]),

@@ -183,6 +183,7 @@ int gqa_decode(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int3
     if (!q_ok) return GQA_ERR_UNSUPPORTED;
     int kernel = opts ? opts->kernel : 0;
     if (kernel < 0 || kernel > 2) return GQA_ERR_INVALID;
+    if (opts && (opts->row_layout < 0 || opts->row_layout > 2)) return GQA_ERR_INVALID;
     const int sms = num_sms_of(-1);
     if (sms <= 0) return GQA_ERR_CUDA;
 
@@ -205,6 +206,7 @@ int gqa_decode(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int3
     L.kernel = kernel;
     L.max_warps = opts ? std::max(0, opts->max_warps) : 0;
     L.min_blocks_per_warp = opts ? std::max(0, opts->min_blocks_per_warp) : 0;
+    L.row_layout = opts ? opts->row_layout : 0;
     L.ev_begin = opts ? static_cast<cudaEvent_t>(opts->event_main_begin) : nullptr;
     L.ev_end = opts ? static_cast<cudaEvent_t>(opts->event_main_end) : nullptr;
     L.err = err_flag;

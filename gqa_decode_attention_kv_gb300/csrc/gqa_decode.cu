@@ -62,9 +62,12 @@ int workers_of(const Variant& v, int batch, int num_sms) {
 
 // Warps that share one pair's tiles for GT query rows per pair (8 rows each).
 int warps_for_rows(int GT) { return GT <= 8 ? 1 : GT <= 16 ? 2 : GT <= 32 ? 4 : 8; }
+int row_groups(int GT) { return (GT + kHeadsPerWarp - 1) / kHeadsPerWarp; }
+
 
 // The largest workspace any kernel choice needs for this shape: workers are
-// taken from the occupancy of every variant that can serve (G*T, head_dim).
+// taken from the occupancy of every variant that can serve (G*T, head_dim), in
+// both the shared-ring and the virtual-head layout.
 size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int head_dim, int tokens_per_seq,
                               int num_sms) {
     const int GT = num_heads / num_kv_heads * std::max(1, tokens_per_seq);
@@ -72,14 +75,22 @@ size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int he
     int P = 0;
     for (int kind : {kKernelMma, kKernelFma}) {
         for (int dt : {GQA_DTYPE_F32, GQA_DTYPE_F16, GQA_DTYPE_BF16, GQA_DTYPE_I8, GQA_DTYPE_FP8_E4M3}) {
-            Variant v{};
-            if (pick_plain(dt, kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
-            if (pick_general(dt, kind, head_dim, nw, v)) P = std::max(P, workers_of(v, batch, num_sms));
+            for (int w : {1, nw}) {
+                Variant v{};
+                if (pick_plain(dt, kind, head_dim, w, v)) P = std::max(P, workers_of(v, batch, num_sms));
+                if (pick_general(dt, kind, head_dim, w, v)) P = std::max(P, workers_of(v, batch, num_sms));
+            }
         }
     }
-    if (P == 0) P = num_sms * (kMaxWarpsPerSm / nw);      // no occupancy answer: the hard bound
-    return ws_layout(batch, num_kv_heads, GT, head_dim,
-                     max_slots(batch, num_kv_heads, P, 0, 0, kMaxTailChunks)).total;
+    if (P == 0) P = num_sms * kMaxWarpsPerSm;             // no occupancy answer: the hard bound
+    size_t bytes = ws_layout(batch, num_kv_heads, GT, head_dim,
+                             max_slots(batch, num_kv_heads, P, 0, 0, kMaxTailChunks)).total;
+    if (GT > kHeadsPerWarp) {
+        const int Kv = num_kv_heads * row_groups(GT);
+        bytes = std::max(bytes, ws_layout(batch, Kv, kHeadsPerWarp, head_dim,
+                                          max_slots(batch, Kv, P, 0, 0, kMaxTailChunks)).total);
+    }
+    return bytes;
 }
 
 int launch_decode(const DecodeLaunch& L, int num_sms) {
@@ -88,11 +99,36 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     const int T = std::max(1, L.tokens_per_seq), GT = G * T;
     int kind = L.kernel;
     if (kind == 0) kind = (c.dtype == GQA_DTYPE_F32 || (dtype_coded(c.dtype) && D != 128)) ? kKernelFma : kKernelMma;
-    const int nw = warps_for_rows(GT);   // warps sharing one pair's tiles
     Variant v{};
     const bool general = T > 1 || L.window > 0;
-    const bool ok = general ? pick_general(c.dtype, kind, D, nw, v) : pick_plain(c.dtype, kind, D, nw, v);
+    auto pick = [&](int warps) {
+        return general ? pick_general(c.dtype, kind, D, warps, v) : pick_plain(c.dtype, kind, D, warps, v);
+    };
+    // More than 8 rows: by default the CTA's warps share each tile (measured
+    // faster than 8-row unit streams at 16, 32 and 64 rows: the per-block
+    // latency, not the worker count, bounds these shapes); unit streams where
+    // no shared-ring kernel exists or when asked for. (Virtual heads multiply
+    // the unit count, which must stay below 2^31.)
+    int nrg = 1;
+    bool ok = false;
+    if (GT <= kHeadsPerWarp) {
+        ok = pick(1);
+    } else {
+        const int groups = row_groups(GT);
+        const bool virt_fits = (long long)L.batch * K * groups * L.max_blocks < 0x7fffffffLL;
+        const bool want_virt = L.row_layout == 1;
+        if (virt_fits && want_virt && pick(1)) {
+            ok = true;
+            nrg = groups;
+        } else if (pick(warps_for_rows(GT))) {
+            ok = true;
+        } else if (virt_fits && pick(1)) {
+            ok = true;
+            nrg = groups;
+        }
+    }
     if (!ok) return GQA_ERR_UNSUPPORTED;
+    const int Kv = K * nrg, RS = nrg > 1 ? kHeadsPerWarp : GT;
 
     CUtensorMap kmap, vmap;
     int perm[3];
@@ -111,7 +147,7 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
 
     const int min_units = L.min_blocks_per_warp > 0 ? L.min_blocks_per_warp : 4;
     const WsLayout wl =
-        ws_layout(L.batch, K, GT, D, max_slots(L.batch, K, P, L.max_blocks, min_units, v.tail_chunks));
+        ws_layout(L.batch, Kv, RS, D, max_slots(L.batch, Kv, P, L.max_blocks, min_units, v.tail_chunks));
     if (L.workspace == nullptr || L.workspace_bytes < wl.total) return GQA_ERR_WORKSPACE;
 
     DecodeArgs a;
@@ -135,6 +171,9 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     a.G = G;
     a.T = T;
     a.GT = GT;
+    a.Kv = Kv;
+    a.NRG = nrg;
+    a.RS = RS;
     a.window = L.window;
     a.max_blocks = L.max_blocks;
     a.out_dtype = L.out_dtype;
@@ -170,7 +209,7 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
 
     // Combine width from the expected pieces per row (about 1.5 workers' worth
     // of segments per pair when lengths are even).
-    const long long pairs = (long long)L.batch * K;
+    const long long pairs = (long long)L.batch * Kv;
     const long long est = (3LL * P) / (2 * pairs) + 1;
     const void* cfn;
     int rows_per_cta, cthreads;

@@ -65,13 +65,19 @@ struct DecodeArgs {
     int32_t* ws_hdr;     // the Partition: [0] R, [1] U, [2] Rs, [3] Cz, [4] P, [5] cpw
     unsigned long long* ws_ctr;   // next dynamic chunk; zero between calls
     int32_t* ws_pref;    // [B+1] exclusive prefix of blocks per sequence
-    float2* ws_ml;       // [slots][GT] (running max m in log2 units, running sum l)
-    float* ws_o;         // [slots][GT][D] un-normalised partial outputs
+    float2* ws_ml;       // [slots][RS] (running max m in log2 units, running sum l)
+    float* ws_o;         // [slots][RS][D] un-normalised partial outputs
     long long num_blocks;
     int B, H, K, G, max_blocks, out_dtype, q_dtype, P, min_units;
     int T;               // new tokens (queries) per sequence
     int GT;              // query rows per (sequence, kv-head) pair: G * T
     int window;          // sliding window in tokens; 0 = full attention
+    // Unit space: Kv = K * NRG heads per sequence. NRG > 1 splits a pair's GT
+    // rows into groups of 8 ("virtual kv-heads" gv = g * NRG + group), each an
+    // independent unit stream that re-reads the pair's tiles (from L2, since
+    // the groups of a pair are adjacent in unit order). RS = rows per split
+    // slot of the workspace (GT, or 8 with NRG > 1).
+    int Kv, NRG, RS;
     int map_perm[3];     // tensor-map dims 1..3 -> 0 slot, 1 kv-head, 2 block
     int max_tail_chunks; // pooled chunks per worker range (0 = static partition only)
     float scale_log2;    // scale * log2(e)
@@ -670,25 +676,27 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
     }
 }
 
-// Write the state of pair (b, g): final output if this warp saw the whole pair,
-// else a partial (o, m, l) into split slot (b*K + g) + warp.
+// Write the state of unit-space pair (b, gv): final output if this warp saw the
+// whole pair, else a partial (o, m, l) into split slot (b*Kv + gv) + segment w,
+// rows counted from row0 (the slot's first row).
 template <class C, int D>
-__device__ __forceinline__ void mma_flush(const DecodeArgs& a, MmaState<C, D>& st, int b, int g,
-                                          int hbase, bool whole, int w, int r, int c) {
+__device__ __forceinline__ void mma_flush(const DecodeArgs& a, MmaState<C, D>& st, int b, int gv,
+                                          int hbase, int row0, bool whole, int w, int r, int c) {
     float l0 = st.l[0], l1 = st.l[1];
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
         l0 += __shfl_xor_sync(kFull, l0, o);
         l1 += __shfl_xor_sync(kFull, l1, o);
     }
-    const long long slot = (long long)b * a.K + g + w;
+    const long long slot = (long long)b * a.Kv + gv + w;
+    const int g = gv / a.NRG;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
         const int hh = hbase + 2 * c + e;               // row of the pair
         if (hh >= a.GT) continue;
         const float lsum = e ? l1 : l0;
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-        const long long obase = whole ? q_row<C::kGen>(a, b, g, hh) * D : (slot * a.GT + hh) * D;
+        const long long obase = whole ? q_row<C::kGen>(a, b, g, hh) * D : (slot * a.RS + hh - row0) * D;
 #pragma unroll
         for (int j = 0; j < C::kMt; ++j) {
 #pragma unroll
@@ -699,7 +707,7 @@ __device__ __forceinline__ void mma_flush(const DecodeArgs& a, MmaState<C, D>& s
                 else a.ws_o[obase + dim] = v;
             }
         }
-        if (!whole && r == 0) a.ws_ml[slot * a.GT + hh] = make_float2(st.m[e], lsum);
+        if (!whole && r == 0) a.ws_ml[slot * a.RS + hh - row0] = make_float2(st.m[e], lsum);
     }
 }
 
@@ -785,22 +793,23 @@ __device__ __forceinline__ void fma_block(const DecodeArgs& a, FmaState<C, D>& s
 }
 
 template <class C, int D>
-__device__ __forceinline__ void fma_flush(const DecodeArgs& a, FmaState<C, D>& st, int b, int g,
-                                          int hbase, bool whole, int w, int lane) {
-    const long long slot = (long long)b * a.K + g + w;
+__device__ __forceinline__ void fma_flush(const DecodeArgs& a, FmaState<C, D>& st, int b, int gv,
+                                          int hbase, int row0, bool whole, int w, int lane) {
+    const long long slot = (long long)b * a.Kv + gv + w;
+    const int g = gv / a.NRG;
 #pragma unroll
     for (int h = 0; h < kHeadsPerWarp; ++h) {
         const int hh = hbase + h;                // row of the pair
         if (hh >= a.GT) break;
         const float inv = st.l[h] > 0.f ? 1.f / st.l[h] : 0.f;
-        const long long obase = whole ? q_row<C::kGen>(a, b, g, hh) * D : (slot * a.GT + hh) * D;
+        const long long obase = whole ? q_row<C::kGen>(a, b, g, hh) * D : (slot * a.RS + hh - row0) * D;
 #pragma unroll
         for (int i = 0; i < C::kDpl; ++i) {
             const int dim = lane * C::kDpl + i;
             if (whole) store1(a.out, a.out_dtype, obase + dim, st.acc[h][i] * inv);
             else a.ws_o[obase + dim] = st.acc[h][i];
         }
-        if (!whole && lane == 0) a.ws_ml[slot * a.GT + hh] = make_float2(st.m[h], st.l[h]);
+        if (!whole && lane == 0) a.ws_ml[slot * a.RS + hh - row0] = make_float2(st.m[h], st.l[h]);
     }
 }
 
@@ -857,7 +866,7 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     launch_dependents();                       // the combine kernel may take its place now
     grid_dependency_wait();                    // inputs may come from the previous kernel
     block_prefix<kGen>(a, lens_s, pref, tmp);
-    const Partition pt = make_partition(a, a.K * pref[a.B]);
+    const Partition pt = make_partition(a, a.Kv * pref[a.B]);
     if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i <= a.B; i += blockDim.x) a.ws_pref[i] = pref[i];
         if (threadIdx.x == 0) {
@@ -873,7 +882,9 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int w = kShared ? (int)blockIdx.x : (int)blockIdx.x * C::kWarps + warp;   // worker
-    const int hbase = kShared ? warp * kHeadsPerWarp : 0;
+    // first query row this warp serves: fixed per warp when the CTA's warps
+    // share a pair, else set per pair from its row group
+    int hbase = kShared ? warp * kHeadsPerWarp : 0;
     if (w >= pt.P) return;                     // uniform per worker (grid is sized to P)
     const long long sl = (long long)w * pt.R;
     const int st_lo = (int)min((long long)pt.U, sl);
@@ -921,11 +932,11 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         win_g = 0;
         if (u < pt.U) {
             int b, g, j;
-            locate(u, pref, a.B, a.K, b, g, j);
+            locate(u, pref, a.B, a.Kv, b, g, j);
             const int ph = a.block_tables[(long long)b * a.max_blocks + first_block<C::kGen>(a, lens_s[b]) + j];
             if (ph < 0 || ph >= a.num_blocks) flag_error(a.err, GQA_DEVERR_BLOCK_INDEX);
             else win_phys = ph;
-            win_g = g;
+            win_g = g / a.NRG;                 // the real kv-head
         }
     };
     auto request = [&]() {
@@ -1083,21 +1094,24 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         const int u = meta[4 * s + 1], seg = meta[4 * s + 2], seg_end = meta[4 * s + 3];
         if (u != next_u) {
             // first unit of a segment: find its pair and load that pair's queries
-            locate(u, pref, a.B, a.K, cb, cg, cj);
+            locate(u, pref, a.B, a.Kv, cb, cg, cj);
+            if (!kShared) hbase = (cg % a.NRG) * kHeadsPerWarp;
             cnb = pref[cb + 1] - pref[cb];
             clen = lens_s[cb];
             pair_ranges();
             first_j = cj;
-            cu_pair = a.K * pref[cb] + cg * cnb;
+            cu_pair = a.Kv * pref[cb] + cg * cnb;
             st.reset();
             nb_b = cb;
             nb_g = cg;
-            next_pair(pref, a.B, a.K, nb_b, nb_g);
+            next_pair(pref, a.B, a.Kv, nb_b, nb_g);
             if constexpr (kKind == kKernelMma) {
-                load_q_frags<C, D>(a, cb, cg, hbase, r, c, st.qf);
-                if (cu_pair + cnb < seg_end) load_q_frags<C, D>(a, nb_b, nb_g, hbase, r, c, st.qn);
+                load_q_frags<C, D>(a, cb, cg / a.NRG, hbase, r, c, st.qf);
+                if (cu_pair + cnb < seg_end)
+                    load_q_frags<C, D>(a, nb_b, nb_g / a.NRG, kShared ? hbase : (nb_g % a.NRG) * kHeadsPerWarp,
+                                       r, c, st.qn);
             } else {
-                fma_load_q<C, D>(a, st, cb, cg, hbase, lane);
+                fma_load_q<C, D>(a, st, cb, cg / a.NRG, hbase, lane);
             }
         }
         bool partial;
@@ -1144,28 +1158,32 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         next_u = u + 1;
         if (last_of_pair || last_of_seg) {
             const bool whole = (first_j == 0) && last_of_pair;
-            if constexpr (kKind == kKernelMma) mma_flush<C, D>(a, st, cb, cg, hbase, whole, seg, r, c);
-            else fma_flush<C, D>(a, st, cb, cg, hbase, whole, seg, lane);
+            const int row0 = kShared ? 0 : hbase;
+            if constexpr (kKind == kKernelMma) mma_flush<C, D>(a, st, cb, cg, hbase, row0, whole, seg, r, c);
+            else fma_flush<C, D>(a, st, cb, cg, hbase, row0, whole, seg, lane);
             if (last_of_seg) {
                 next_u = -1;                   // the next unit starts a new segment
                 continue;
             }
             cb = nb_b;
             cg = nb_g;
+            if (!kShared) hbase = (cg % a.NRG) * kHeadsPerWarp;
             cj = 0;
             first_j = 0;
             cnb = pref[cb + 1] - pref[cb];
             clen = lens_s[cb];
             pair_ranges();
-            cu_pair = a.K * pref[cb] + cg * cnb;
+            cu_pair = a.Kv * pref[cb] + cg * cnb;
             st.reset();
-            next_pair(pref, a.B, a.K, nb_b, nb_g);
+            next_pair(pref, a.B, a.Kv, nb_b, nb_g);
             if constexpr (kKind == kKernelMma) {
 #pragma unroll
                 for (int q = 0; q < D / 16; ++q) st.qf[q] = st.qn[q];
-                if (cu_pair + cnb < seg_end) load_q_frags<C, D>(a, nb_b, nb_g, hbase, r, c, st.qn);
+                if (cu_pair + cnb < seg_end)
+                    load_q_frags<C, D>(a, nb_b, nb_g / a.NRG, kShared ? hbase : (nb_g % a.NRG) * kHeadsPerWarp,
+                                       r, c, st.qn);
             } else {
-                fma_load_q<C, D>(a, st, cb, cg, hbase, lane);
+                fma_load_q<C, D>(a, st, cb, cg / a.NRG, hbase, lane);
             }
         } else {
             ++cj;
@@ -1195,7 +1213,10 @@ __global__ void __launch_bounds__(kRowWarps * kRows * 32) combine_kernel(const D
     if (bh >= a.B * TH) return;
     const int b = bh / TH, ih = bh - b * TH;                          // ih = i * H + h
     const int i = ih / a.H, h = ih - i * a.H, g = h / a.G;
-    const int hh = i * a.G + (h - g * a.G);                           // row of the pair
+    const int rr = i * a.G + (h - g * a.G);                           // row of the pair
+    const int rg = a.NRG > 1 ? rr / kHeadsPerWarp : 0;                // its row group
+    const int gv = g * a.NRG + rg;                                    // unit-space head
+    const int hh = rr - rg * kHeadsPerWarp;                           // row in the slot
     const long long orow = (long long)bh * D;                         // out is [B, T, H, d]
     const int p0 = a.ws_pref[b];
     const int nb = a.ws_pref[b + 1] - p0;
@@ -1210,16 +1231,16 @@ __global__ void __launch_bounds__(kRowWarps * kRows * 32) combine_kernel(const D
     pt.Cz = a.ws_hdr[3];
     pt.P = a.ws_hdr[4];
     pt.cpw = a.ws_hdr[5];
-    const int u0 = a.K * p0 + g * nb;
+    const int u0 = a.Kv * p0 + gv * nb;
     const int s0 = pt.segment_of(u0), s1 = pt.segment_of(u0 + nb - 1);
     if (s0 == s1) return;                      // one segment held the whole pair and wrote it
-    const long long first = (long long)b * a.K + g + s0;   // slot of the first piece
+    const long long first = (long long)b * a.Kv + gv + s0;   // slot of the first piece
     const int n = s1 - s0 + 1;
 
     // pass 1: the largest running maximum (one piece per lane)
     float M = -INFINITY;
     for (int p = sub * 32 + lane; p < n; p += kRowWarps * 32)
-        M = fmaxf(M, __ldcg(&a.ws_ml[(first + p) * a.GT + hh]).x);
+        M = fmaxf(M, __ldcg(&a.ws_ml[(first + p) * a.RS + hh]).x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
     if constexpr (kRowWarps > 1) {
@@ -1241,13 +1262,13 @@ __global__ void __launch_bounds__(kRowWarps * kRows * 32) combine_kernel(const D
             const int p = base + lane;
             float e = 0.f;
             if (p < n) {
-                const float2 ml = __ldcg(&a.ws_ml[(first + p) * a.GT + hh]);
+                const float2 ml = __ldcg(&a.ws_ml[(first + p) * a.RS + hh]);
                 e = fast_exp2(ml.x - M);
                 L += ml.y * e;
             }
             const int cnt = min(32, n - base);
-            const float* op = a.ws_o + ((first + base) * a.GT + hh) * D + 4 * lane;
-            const long long step = (long long)a.GT * D;
+            const float* op = a.ws_o + ((first + base) * a.RS + hh) * D + 4 * lane;
+            const long long step = (long long)a.RS * D;
 #pragma unroll 8
             for (int j = 0; j < cnt; ++j) {
                 const float ej = __shfl_sync(kFull, e, j);

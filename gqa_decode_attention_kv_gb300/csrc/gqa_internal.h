@@ -57,6 +57,7 @@ struct DecodeLaunch {
     int kernel;                 // KernelKind
     int max_warps;              // 0 = fill the GPU
     int min_blocks_per_warp;
+    int row_layout;             // 0 auto, 1 virtual heads, 2 shared ring (G*T > 8)
     cudaEvent_t ev_begin, ev_end;
     int32_t* err;
     cudaStream_t stream;

@@ -121,6 +121,10 @@ typedef struct {
     int32_t kernel;               /* 0 auto, 1 tensor-core (mma.sync) kernel, 2 CUDA-core kernel */
     int32_t max_warps;            /* 0 = fill the GPU; > 0 caps the split-KV workers, i.e. KV splits */
     int32_t min_blocks_per_warp;  /* 0 = default (4): smallest KV range one warp takes */
+    int32_t row_layout;           /* more than 8 query rows per kv-head (G*T > 8): 0 auto
+                                     (2 where that kernel exists, else 1), 1 every 8 rows
+                                     stream the tiles on their own (the re-reads hit L2),
+                                     2 the warps of a CTA share each tile */
     void   *event_main_begin;     /* optional cudaEvent_t recorded just before the split-KV kernel */
     void   *event_main_end;       /* optional cudaEvent_t recorded just after it */
 } gqa_decode_opts_t;
@@ -211,9 +215,10 @@ GQA_API size_t gqa_decode_workspace_size(int32_t batch, int32_t num_heads, int32
  *                 at zero again). Otherwise clobbered by each call. Calls that
  *                 share a workspace must not overlap on the GPU.
  *  opts           NULL or options (gqa_decode_opts_t).
- *  Limits: num_heads % K == 0; T * num_heads / K <= 64 query rows per kv-head
- *  (above 8 rows: a BF16/F16 cache, a coded cache with head_dim 128, or an F32
- *  cache); sliding_window >= 0; batch <= 8191; batch * K * max_blocks_per_seq < 2^31.
+ *  Limits: num_heads % K == 0; T * num_heads / K <= 64 query rows per kv-head;
+ *  sliding_window >= 0; batch <= 8191; batch * K * max_blocks_per_seq < 2^31
+ *  (above 8 rows per kv-head on a kernel without a shared-ring form, times the
+ *  number of 8-row groups).
  */
 GQA_API int gqa_decode(const gqa_kv_cache_t *cache, const void *q, int32_t q_dtype,
                int32_t num_heads, const int32_t *block_tables, int32_t max_blocks_per_seq,

@@ -67,8 +67,9 @@ def _desc(**kw):
 
 
 def _decode(lib, desc, q=0x30000, q_dtype=2, H=32, table=0x40000, maxb=8, lens=0x50000, B=4,
-            scale=0.1, out=0x60000, out_dtype=0, ws=0x70000, ws_bytes=1 << 20, T=0, window=0):
-    opts = gq.DecodeOpts(T, window, 0, 0, 0, None, None)
+            scale=0.1, out=0x60000, out_dtype=0, ws=0x70000, ws_bytes=1 << 20, T=0, window=0,
+            layout=0):
+    opts = gq.DecodeOpts(T, window, 0, 0, 0, layout, None, None)
     return lib.gqa_decode(ctypes.byref(desc), q, q_dtype, H, table, maxb, lens, B, scale, out,
                           out_dtype, ws, ws_bytes, ctypes.byref(opts), None, None)
 
@@ -104,6 +105,7 @@ def test_cache_description_checks(lib, kw, expect):
     (dict(T=17), UNSUPPORTED),                       # G*T = 4*17 = 68 query rows > 64
     (dict(T=16, B=0), OK),                           # 64 rows: allowed
     (dict(window=7, B=0), OK),
+    (dict(layout=3), INVALID),
 ])
 def test_decode_argument_checks(lib, kw, expect):
     assert _decode(lib, _desc(), **kw) == expect

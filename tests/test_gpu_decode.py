@@ -56,27 +56,42 @@ def test_ragged_multi_tile(gq, kernel, dtype, d, H, K):
     ("bf16", 128, 64, 4, 1), ("bf16", 128, 48, 4, 1), ("bf16", 128, 64, 2, 1),
     ("bf16", 128, 64, 1, 1), ("f16", 64, 32, 1, 1), ("f32", 64, 64, 1, 2), ("f32", 128, 16, 1, 2),
 ])
-def test_groups_larger_than_one_warp(gq, dtype, d, H, K, kernel):
-    """G = 16, 12, 32, 64: the CTA's warps split the heads and share one ring."""
-    _ragged(gq, kernel, dtype, d, H, K)
+@pytest.mark.parametrize("layout", [1, 2])
+def test_groups_larger_than_one_warp(gq, dtype, d, H, K, kernel, layout):
+    """G = 16, 12, 32, 64: every 8 heads stream the tiles on their own (layout 1),
+    or the CTA's warps split the heads and share one ring (layout 2)."""
+    _ragged(gq, kernel, dtype, d, H, K, row_layout=layout)
 
 
-def _ragged(gq, kernel, dtype, d, H, K):
+def _ragged(gq, kernel, dtype, d, H, K, **kw):
     lens = [1, 15, 16, 17, 33, 200, 511, 0, 1000]
     case = gi.make_case(len(lens), H, K, d, lens, dtype, seed=21, device="cuda")
     ref = oracle_for_case(case)
     for mw in (0, 1, 5, 37):          # 0 = fill the GPU; 1 = one warp does everything
-        out = _run(gq, case, kernel=kernel, max_warps=mw, min_blocks_per_warp=1)
+        out = _run(gq, case, kernel=kernel, max_warps=mw, min_blocks_per_warp=1, **kw)
         err = max_abs_err(out, ref)
         assert err <= TOL, (mw, err)
 
 
-def test_int8_wide_group(gq):
+@pytest.mark.parametrize("layout", [0, 1, 2])
+def test_int8_wide_group(gq, layout):
     lens = [1, 16, 17, 300, 2047, 0, 64]
     case = gi.make_case(len(lens), 64, 2, 128, lens, "i8", q_dtype="bf16", seed=35, device="cuda")
     ref = oracle_for_case(case)
     for mw in (0, 3):
-        assert max_abs_err(_run(gq, case, max_warps=mw, min_blocks_per_warp=1), ref) <= TOL
+        out = _run(gq, case, max_warps=mw, min_blocks_per_warp=1, row_layout=layout)
+        assert max_abs_err(out, ref) <= TOL
+
+
+@pytest.mark.parametrize("dtype", ["i8", "fp8", "bf16"])
+def test_head_dim_64_groups_above_8_on_the_cuda_core_kernel(gq, dtype):
+    """G = 16 with head_dim 64: the CUDA-core kernel serves it as 8-row unit streams."""
+    lens = [1, 17, 300, 0, 64]
+    case = gi.make_case(len(lens), 32, 2, 64, lens, dtype, seed=36, device="cuda")
+    ref = oracle_for_case(case)
+    for mw in (0, 3):
+        out = _run(gq, case, kernel=2, max_warps=mw, min_blocks_per_warp=1)
+        assert max_abs_err(out, ref) <= TOL
 
 
 @pytest.mark.parametrize("kernel", KERNELS)

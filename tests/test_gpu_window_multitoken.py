@@ -112,14 +112,18 @@ def test_multi_token_with_window(gq, T, window):
     assert max_abs_err(_run(gq, case, window=window), ref) <= TOL
 
 
+@pytest.mark.parametrize("layout", [0, 1, 2])
 @pytest.mark.parametrize("H,K,T,dtype", [(64, 8, 8, "bf16"), (32, 4, 8, "i8"), (8, 8, 4, "f16"),
-                                         (16, 1, 4, "bf16")])
-def test_multi_token_rows_span_several_warps(gq, H, K, T, dtype):
-    """G*T query rows per kv-head up to 64: the warps of one CTA share the tiles."""
+                                         (16, 1, 4, "bf16"), (24, 8, 4, "fp8")])
+def test_multi_token_rows_span_several_warps(gq, H, K, T, dtype, layout):
+    """G*T query rows per kv-head up to 64, as 8-row unit streams (layout 1) or
+    with the warps of one CTA sharing the tiles (layout 2)."""
     lens = [3, 16, 100, 513]
     case = gi.make_case(len(lens), H, K, 128, lens, dtype, seed=68, device="cuda", queries=T)
     ref = oracle_for_case(case)
-    assert max_abs_err(_run(gq, case), ref) <= TOL
+    for mw in (0, 7):
+        out = _run(gq, case, row_layout=layout, max_warps=mw, min_blocks_per_warp=1)
+        assert max_abs_err(out, ref) <= TOL, (mw,)
 
 
 def test_last_new_token_equals_a_single_token_decode(gq):
