@@ -82,25 +82,29 @@ def kernel_source_hash() -> str:
 
 
 def read_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel source for this workload; else None."""
+    """DRAM bytes per launch from the committed ncu summary (blocks of
+    'key: value' lines separated by blank lines, one per workload), if one was
+    taken on the current kernel source for this workload; else None."""
     try:
-        lines = open(TRAFFIC_FILE).read().splitlines()
+        text = open(TRAFFIC_FILE).read()
     except OSError:
         return None
-    vals = {}
-    for ln in lines:
-        if ":" in ln and not ln.startswith("#"):
-            k, _, v = ln.partition(":")
-            vals[k.strip()] = v.strip()
-    if vals.get("source_hash") != kernel_source_hash():
-        return None
-    if vals.get("workload") != workload or vals.get("kernel_variant", "auto") != kernel:
-        return None
-    try:
-        return float(vals["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    src = kernel_source_hash()
+    for block in text.split("\n\n"):
+        vals = {}
+        for ln in block.splitlines():
+            if ":" in ln and not ln.startswith("#"):
+                k, _, v = ln.partition(":")
+                vals[k.strip()] = v.strip()
+        if vals.get("source_hash") != src or vals.get("workload") != workload:
+            continue
+        if vals.get("kernel_variant", "auto") != kernel:
+            continue
+        try:
+            return float(vals["traffic_bytes_per_launch"])
+        except (KeyError, ValueError):
+            return None
+    return None
 
 
 def measured_peaks():

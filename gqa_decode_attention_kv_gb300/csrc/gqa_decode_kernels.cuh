@@ -912,7 +912,11 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
         }
         __syncwarp();
     }
+    // K/V tiles are read once: evict them first. The 32-byte scale rows of a
+    // (block, kv-head) share L2 lines with the other heads' rows, which other
+    // workers read later; keep those lines (all scales are ~1.6% of the pool).
     const uint64_t pol = l2_policy_evict_first();
+    const uint64_t pol_keep = C::kCoded ? l2_policy_evict_last() : pol;
 
     // ---- producer: segments (static range first, then pooled chunks) and copies
     // The pool is asked for the next chunk kLookahead units before the current
@@ -1022,8 +1026,8 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                     tma_load_4d(dst + C::kTile + x * C::kBoxBytes, &vmap, x * C::kBoxInner, y, z, ww, bar, pol);
                 if constexpr (C::kCoded) {
                     const long long si = ((long long)ph * a.K + gg) * kBlock;
-                    bulk_load(dst + 2 * C::kTile, a.k_scale + si, 32, bar, pol);
-                    bulk_load(dst + 2 * C::kTile + 32, a.v_scale + si, 32, bar, pol);
+                    bulk_load(dst + 2 * C::kTile, a.k_scale + si, 32, bar, pol_keep);
+                    bulk_load(dst + 2 * C::kTile + 32, a.v_scale + si, 32, bar, pol_keep);
                 }
             } else {
                 meta[4 * s] = kSlotSkip;

@@ -106,6 +106,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // 4-D tiled tensor copy global -> shared, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             int z, int w, uint32_t bar, uint64_t policy) {
