@@ -75,6 +75,10 @@ def _load():
             lib.oracle_f32_to_f16_bits.restype = ctypes.c_uint16
             lib.oracle_f16_bits_to_f32.argtypes = [ctypes.c_uint16]
             lib.oracle_f16_bits_to_f32.restype = ctypes.c_float
+            lib.oracle_quantize_int4.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int64,
+                                                 ctypes.c_int32, ctypes.POINTER(ctypes.c_int8),
+                                                 ctypes.POINTER(ctypes.c_uint16)]
+            lib.oracle_quantize_int4.restype = None
             lib.oracle_quantize_fp8.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int64,
                                                 ctypes.c_int32, ctypes.POINTER(ctypes.c_uint8),
                                                 ctypes.POINTER(ctypes.c_uint16)]
@@ -213,6 +217,34 @@ def quantize_int8(x) -> tuple[np.ndarray, np.ndarray]:
     return codes, scales
 
 
+def quantize_int4(x) -> tuple[np.ndarray, np.ndarray]:
+    """Rows of x -> (codes in [-7, 7] as int8, one per element; fp16 scale bits as uint16)."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    d = x.shape[-1]
+    rows = x.size // d if d else 0
+    codes = np.empty(x.shape, dtype=np.int8)
+    scales = np.empty(x.shape[:-1], dtype=np.uint16)
+    _load().oracle_quantize_int4(_ptr(x, ctypes.c_float), rows, d,
+                                 _ptr(codes, ctypes.c_int8), _ptr(scales, ctypes.c_uint16))
+    return codes, scales
+
+
+def pack_int4(codes) -> np.ndarray:
+    """[..., d] codes in [-8, 7] -> [..., d/2] bytes: element 2j in the low nibble,
+    2j+1 in the high nibble, each as a two's-complement nibble."""
+    c = np.asarray(codes).astype(np.int16)
+    lo = c[..., 0::2] & 0xF
+    hi = c[..., 1::2] & 0xF
+    return (lo | (hi << 4)).astype(np.uint8)
+
+
+def unpack_int4(packed) -> np.ndarray:
+    """Inverse of pack_int4: [..., d/2] bytes -> [..., d] int8 codes."""
+    b = np.asarray(packed, dtype=np.uint8).astype(np.int16)
+    nib = np.stack([b & 0xF, b >> 4], axis=-1).reshape(*b.shape[:-1], 2 * b.shape[-1])
+    return np.where(nib >= 8, nib - 16, nib).astype(np.int8)
+
+
 def quantize_fp8(x) -> tuple[np.ndarray, np.ndarray]:
     """Rows of x -> (e4m3 codes as uint8, fp16 scale bits as uint16)."""
     x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
@@ -259,6 +291,11 @@ def f32_to_f16_bits(x) -> np.ndarray:
     lib = _load()
     flat = [lib.oracle_f32_to_f16_bits(float(v)) for v in a.reshape(-1)]
     return np.asarray(flat, dtype=np.uint16).reshape(a.shape)
+
+
+def dequantize_int4(packed, scale_values) -> np.ndarray:
+    """Packed int4 rows [..., d/2] -> code * scale in fp64 (exact)."""
+    return dequantize_int8(unpack_int4(packed), scale_values)
 
 
 def dequantize_int8(codes, scale_values) -> np.ndarray:

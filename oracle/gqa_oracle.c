@@ -39,6 +39,14 @@
  *    with fp32 IEEE division and round-half-to-even. Dequantisation is q_i * s
  *    evaluated exactly in fp64.
  *
+ *  - oracle_quantize_int4: the INT4 KV cache of "LLM 推理性能优化实战" section
+ *    15.5 (KV quantised to INT4; section 15.3 lists INT4 among the low-precision
+ *    formats) with the same symmetric per-(token, kv-head) rule, range [-7, 7]:
+ *      s = fp16_rne(min(amax / 7, 65504)),  q_i = clamp(rint(x_i / s), -7, 7).
+ *    (Reading: the symmetric range of section 15.1 narrowed to four bits, -8
+ *    unused so the range stays symmetric.) Two codes share a byte, element 2j
+ *    in the low nibble, as two's-complement nibbles.
+ *
  *  - oracle_quantize_fp8 / oracle_f32_to_e4m3 / oracle_e4m3_to_f64: the FP8
  *    (E4M3) KV cache named among the KV quantisation options of "LLM 推理性能优化实战"
  *    section 15.5 (FP8 E4M3/E5M2 for long-tailed K/V): per-(token, kv-head) fp16
@@ -128,8 +136,10 @@ float oracle_f16_bits_to_f32(uint16_t h)
 /* int8 KV quantisation, one scale per row                                   */
 /* ------------------------------------------------------------------------- */
 
-void oracle_quantize_int8(const float *x, int64_t rows, int32_t d,
-                          int8_t *codes, uint16_t *scale_bits)
+/* Symmetric integer quantisation of rows of d values to [-qmax, qmax] with
+ * one fp16 scale per row (the rule above, with 127 replaced by qmax). */
+static void quantize_symmetric(const float *x, int64_t rows, int32_t d, float qmax,
+                               int8_t *codes, uint16_t *scale_bits)
 {
     for (int64_t r = 0; r < rows; ++r) {
         const float *xr = x + r * (int64_t)d;
@@ -138,7 +148,7 @@ void oracle_quantize_int8(const float *x, int64_t rows, int32_t d,
             float a = fabsf(xr[i]);
             if (a > amax) amax = a;
         }
-        volatile float s32 = amax / 127.0f;      /* IEEE fp32 division */
+        volatile float s32 = amax / qmax;        /* IEEE fp32 division */
         float s = s32;
         if (s > 65504.0f) s = 65504.0f;
         uint16_t sb = oracle_f32_to_f16_bits(s);
@@ -149,13 +159,26 @@ void oracle_quantize_int8(const float *x, int64_t rows, int32_t d,
             if (sf != 0.0f) {
                 volatile float t = xr[i] / sf;   /* IEEE fp32 division */
                 float rq = rintf(t);             /* round half to even (default mode) */
-                if (rq > 127.0f) rq = 127.0f;
-                if (rq < -127.0f) rq = -127.0f;
+                if (rq > qmax) rq = qmax;
+                if (rq < -qmax) rq = -qmax;
                 q = (int32_t)rq;
             }
             codes[r * (int64_t)d + i] = (int8_t)q;
         }
     }
+}
+
+void oracle_quantize_int8(const float *x, int64_t rows, int32_t d,
+                          int8_t *codes, uint16_t *scale_bits)
+{
+    quantize_symmetric(x, rows, d, 127.0f, codes, scale_bits);
+}
+
+/* Codes in [-7, 7], one per int8 (packing two per byte is the caller's). */
+void oracle_quantize_int4(const float *x, int64_t rows, int32_t d,
+                          int8_t *codes, uint16_t *scale_bits)
+{
+    quantize_symmetric(x, rows, d, 7.0f, codes, scale_bits);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -372,6 +372,58 @@ def test_int8_quantisation_invariants(oracle_mod):
     assert sz[0] == 0 and not cz.any()
 
 
+def test_int4_rounding_worked_example(oracle_mod):
+    """amax = 7 gives scale exactly 1.0, so codes are rint(x) with ties to even."""
+    x = np.array([[7.0, -6.5, 0.5, 1.5, 2.5, -2.5, 3.5, 0.0]], dtype=np.float32)
+    codes, scale = oracle_mod.quantize_int4(x)
+    assert scale[0] == np.float16(1.0).view(np.uint16)
+    assert codes[0].tolist() == [7, -6, 0, 2, 2, -2, 4, 0]
+
+
+def test_int4_quantisation_invariants(oracle_mod):
+    rng = np.random.default_rng(33)
+    x = rng.standard_normal((500, 128)).astype(np.float32) * np.float32(10.0) ** rng.integers(-3, 4, (500, 1))
+    codes, sbits = oracle_mod.quantize_int4(x)
+    s = oracle_mod.f16_bits_to_f64(sbits)
+    assert np.all(np.abs(codes.astype(np.int32)).max(axis=1) == 7)
+    assert codes.min() >= -7 and codes.max() <= 7
+    err = np.abs(x.astype(np.float64) - codes * s[:, None])
+    assert np.all(err <= s[:, None] / 2 * (1 + 1e-6))
+    c2, s2 = oracle_mod.quantize_int4(-x)
+    np.testing.assert_array_equal(c2, -codes)
+    np.testing.assert_array_equal(s2, sbits)
+    cz, sz = oracle_mod.quantize_int4(np.zeros((1, 64), dtype=np.float32))
+    assert sz[0] == 0 and not cz.any()
+    # the int4 step is 127/7 times the int8 one (before fp16 rounding of each)
+    _, s8 = oracle_mod.quantize_int8(x)
+    ratio = s / oracle_mod.f16_bits_to_f64(s8)
+    normal = oracle_mod.f16_bits_to_f64(s8) >= 2.0 ** -14
+    np.testing.assert_allclose(ratio[normal], 127 / 7, rtol=2 ** -10)
+
+
+def test_int4_packing_bytes(oracle_mod):
+    """Element 2j in the low nibble, two's complement: -7 -> 0x9, -1 -> 0xF, -4 -> 0xC."""
+    codes = np.array([[-7, 7, 0, -1, 3, -4]], dtype=np.int8)
+    packed = oracle_mod.pack_int4(codes)
+    assert packed[0].tolist() == [0x79, 0xF0, 0xC3]
+    every = np.array([[a, b] for a in range(-8, 8) for b in range(-8, 8)], dtype=np.int8).reshape(1, -1)
+    np.testing.assert_array_equal(oracle_mod.unpack_int4(oracle_mod.pack_int4(every)), every)
+    assert sorted(set(oracle_mod.pack_int4(every)[0].tolist())) == list(range(256))
+
+
+def test_int4_dequantised_attention_matches_sdpa(oracle_mod):
+    rng = np.random.default_rng(34)
+    kv = rng.standard_normal((1, 20, 2, 64)).astype(np.float32)
+    codes, sbits = oracle_mod.quantize_int4(kv)
+    deq = oracle_mod.dequantize_int4(oracle_mod.pack_int4(codes), oracle_mod.f16_bits_to_f64(sbits))
+    assert deq.shape == kv.shape
+    np.testing.assert_array_equal(deq, codes * oracle_mod.f16_bits_to_f64(sbits)[..., None])
+    q = rng.standard_normal((1, 8, 64))
+    got = oracle_mod.decode(q, deq, deq, [20], 0.125)
+    ref = _sdpa_reference(q, deq, deq, [20], 0.125)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
 def test_dequantised_attention_equals_attention_on_dequantised_values(oracle_mod):
     """The int8 path is the float path fed q*s: the dequantised cache is exact in fp64."""
     rng = np.random.default_rng(33)
