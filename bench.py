@@ -51,13 +51,13 @@ def algorithmic_bytes(wl, lens) -> dict:
     """Bytes a decode step must move: KV (+scales) of every attended cached
     token once, q in, out (fp32) out, block-table entries and lengths, plus the
     append of the T new tokens."""
-    es = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1, "fp8": 1}[wl.cache_dtype]
+    es = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1, "fp8": 1, "i4": 0.5}[wl.cache_dtype]
     qes = {"f32": 4, "f16": 2, "bf16": 2}[wl.q_dtype]
     T = wl.queries
     ranges = [attended_range(wl, int(x)) for x in lens]
     tokens = int(sum(hi - lo for lo, hi in ranges))
-    per_token = 2 * wl.num_kv_heads * wl.head_dim * es
-    if wl.cache_dtype in ("i8", "fp8"):
+    per_token = int(2 * wl.num_kv_heads * wl.head_dim * es)
+    if wl.cache_dtype in ("i8", "fp8", "i4"):
         per_token += 2 * wl.num_kv_heads * 2
     blocks = int(sum(-(-hi // 16) - lo // 16 for lo, hi in ranges))
     B = len(lens)
@@ -65,8 +65,8 @@ def algorithmic_bytes(wl, lens) -> dict:
     q = B * T * wl.num_heads * wl.head_dim * qes
     o = B * T * wl.num_heads * wl.head_dim * 4
     meta = blocks * 4 + B * 4
-    new_es = qes if wl.cache_dtype in ("i8", "fp8") else es
-    append = B * T * 2 * wl.num_kv_heads * wl.head_dim * (new_es + es) + B * 4
+    new_es = qes if wl.cache_dtype in ("i8", "fp8", "i4") else es
+    append = int(B * T * 2 * wl.num_kv_heads * wl.head_dim * (new_es + es)) + B * 4
     decode = kv + q + o + meta
     return {"kv": kv, "decode": decode, "append": append, "step": decode + append,
             "tokens": tokens, "blocks": blocks}
@@ -405,7 +405,7 @@ def _oracle_inputs(wl, case, rows):
     ids = torch.from_numpy(np.concatenate(sel).astype(np.int64)).to(case.k_cache.device)
     def host(t):
         t = t.index_select(0, ids)
-        if t.dtype == torch.int8:
+        if t.dtype in (torch.int8, torch.uint8):
             return t.cpu().numpy()
         if t.dtype == torch.float8_e4m3fn:
             return t.cpu().view(torch.uint8).numpy()
@@ -418,10 +418,13 @@ def _oracle_inputs(wl, case, rows):
         off += len(s)
     sub_lens = lens[rows]
     K, d = wl.num_kv_heads, wl.head_dim
-    sb, sh, st = K * 16 * d, 16 * d, d
-    kd = oracle.gather_dense(kp, new_table, sub_lens, sb, sh, st, K, d).astype(np.float64)
-    vd = oracle.gather_dense(vp, new_table, sub_lens, sb, sh, st, K, d).astype(np.float64)
-    if wl.cache_dtype in ("i8", "fp8"):
+    rd = d // 2 if wl.cache_dtype == "i4" else d          # stored row (4-bit: bytes)
+    sb, sh, st = K * 16 * rd, 16 * rd, rd
+    kd = oracle.gather_dense(kp, new_table, sub_lens, sb, sh, st, K, rd)
+    vd = oracle.gather_dense(vp, new_table, sub_lens, sb, sh, st, K, rd)
+    if wl.cache_dtype not in ("i4",):
+        kd, vd = kd.astype(np.float64), vd.astype(np.float64)
+    if wl.cache_dtype in ("i8", "fp8", "i4"):
         ksp = case.k_scale.index_select(0, ids).float().cpu().numpy()
         vsp = case.v_scale.index_select(0, ids).float().cpu().numpy()
         kss = oracle.gather_scales(ksp, new_table, sub_lens, K)
@@ -429,6 +432,9 @@ def _oracle_inputs(wl, case, rows):
         if wl.cache_dtype == "i8":
             kd = oracle.dequantize_int8(kd, kss)
             vd = oracle.dequantize_int8(vd, vss)
+        elif wl.cache_dtype == "i4":
+            kd = oracle.dequantize_int4(kd, kss)
+            vd = oracle.dequantize_int4(vd, vss)
         else:
             kd = oracle.dequantize_fp8(kd.astype(np.uint8), kss)
             vd = oracle.dequantize_fp8(vd.astype(np.uint8), vss)

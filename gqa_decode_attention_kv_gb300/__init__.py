@@ -38,6 +38,7 @@ GQA_DEVERR_POSITION = 4
 GQA_DEVERR_TIMEOUT = 8
 
 KERNEL_AUTO, KERNEL_MMA, KERNEL_FMA = 0, 1, 2
+GQA_DTYPE_I4 = 5
 
 
 class GqaError(RuntimeError):
@@ -135,20 +136,24 @@ class PagedKVCache:
     stride_token: int
     k_scale: Optional[torch.Tensor] = None
     v_scale: Optional[torch.Tensor] = None
+    dtype_code: Optional[int] = None   # set for storage the tensor dtype does not name (int4)
 
     @staticmethod
-    def allocate(num_blocks: int, num_kv_heads: int, head_dim: int, dtype: torch.dtype,
+    def allocate(num_blocks: int, num_kv_heads: int, head_dim: int, dtype,
                  device="cuda") -> "PagedKVCache":
-        shape = (num_blocks, num_kv_heads, BLOCK_SIZE, head_dim)
-        k = torch.empty(shape, dtype=dtype, device=device)
-        v = torch.empty(shape, dtype=dtype, device=device)
+        """dtype: a torch dtype, or "int4" for two 4-bit codes per byte (uint8
+        storage [num_blocks, K, 16, d/2]; strides still count 4-bit elements)."""
+        int4 = dtype == "int4"
+        shape = (num_blocks, num_kv_heads, BLOCK_SIZE, head_dim // 2 if int4 else head_dim)
+        k = torch.empty(shape, dtype=torch.uint8 if int4 else dtype, device=device)
+        v = torch.empty_like(k)
         ks = vs = None
-        if dtype in (torch.int8, torch.float8_e4m3fn):
+        if int4 or dtype in (torch.int8, torch.float8_e4m3fn):
             ks = torch.empty((num_blocks, num_kv_heads, BLOCK_SIZE), dtype=torch.float16, device=device)
             vs = torch.empty_like(ks)
         return PagedKVCache(k, v, num_blocks, num_kv_heads, head_dim,
                             num_kv_heads * BLOCK_SIZE * head_dim, BLOCK_SIZE * head_dim, head_dim,
-                            ks, vs)
+                            ks, vs, GQA_DTYPE_I4 if int4 else None)
 
     @property
     def dtype(self) -> torch.dtype:
@@ -160,7 +165,8 @@ class PagedKVCache:
             self.k_scale.data_ptr() if self.k_scale is not None else None,
             self.v_scale.data_ptr() if self.v_scale is not None else None,
             self.num_blocks, self.num_kv_heads, BLOCK_SIZE, self.head_dim,
-            DTYPE_CODE[self.k.dtype], self.stride_block, self.stride_head, self.stride_token)
+            self.dtype_code if self.dtype_code is not None else DTYPE_CODE[self.k.dtype],
+            self.stride_block, self.stride_head, self.stride_token)
 
 
 def _stream_ptr(stream) -> Optional[int]:
@@ -275,4 +281,5 @@ def cache_from_case(case) -> PagedKVCache:
     """Wrap the device tensors of a generated decode case (gqa_inputs.DecodeCase)."""
     return PagedKVCache(case.k_cache, case.v_cache, case.num_blocks, case.num_kv_heads,
                         case.head_dim, case.stride_block, case.stride_head, case.stride_token,
-                        case.k_scale, case.v_scale)
+                        case.k_scale, case.v_scale,
+                        GQA_DTYPE_I4 if case.cache_dtype == "i4" else None)

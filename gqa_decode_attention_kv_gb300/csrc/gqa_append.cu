@@ -3,8 +3,8 @@
 // ("LLM 推理性能优化实战", sections 5.3-5.4 and 8.2). One warp per
 // (sequence, new token, kv-head) writes both rows, so K and V of a token leave
 // together.
-// For an int8 or FP8 (e4m3) cache each row is quantised on the way (one fp16
-// scale per (token, kv-head); sections 15.1, 15.2 and 15.5 of that page).
+// For an int8, int4 or FP8 (e4m3) cache each row is quantised on the way (one
+// fp16 scale per (token, kv-head); sections 15.1, 15.2 and 15.5 of that page).
 #include "gqa_device.cuh"
 #include "gqa_internal.h"
 
@@ -82,12 +82,19 @@ __device__ __forceinline__ float load_as_float(const void* p, long long i) {
     else return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
 }
 
+// Code formats of the quantising append.
+enum CodeKind : int { kCodeI8 = 0, kCodeFp8 = 1, kCodeI4 = 2 };
+
 // Quantise one row of d values held EPL per lane; writes codes and the scale.
 // kFp8: e4m3 codes, s = amax/448, nearest-even with saturation to +-448;
-// else int8 codes, s = amax/127, rint with ties to even, clamped to +-127.
-template <typename In, int EPL, bool kFp8>
+// kI8: int8 codes, s = amax/127, rint with ties to even, clamped to +-127;
+// kI4: the same with 7, two codes per byte (element 2j in the low nibble).
+// dst is the row's first byte.
+template <typename In, int EPL, int kCode>
 __device__ __forceinline__ void quantise_row(const void* src, long long src_off, uint8_t* dst,
                                              __half* scale_dst, int lane) {
+    constexpr bool kFp8 = kCode == kCodeFp8;
+    constexpr float kQmax = kCode == kCodeI4 ? 7.0f : 127.0f;
     float x[EPL];
     float amax = 0.f;
 #pragma unroll
@@ -97,7 +104,7 @@ __device__ __forceinline__ void quantise_row(const void* src, long long src_off,
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-    float s32 = __fdiv_rn(amax, kFp8 ? 448.0f : 127.0f);
+    float s32 = __fdiv_rn(amax, kFp8 ? 448.0f : kQmax);
     s32 = fminf(s32, 65504.0f);
     const __half sh = __float2half_rn(s32);
     const float sf = __half2float(sh);
@@ -110,12 +117,18 @@ __device__ __forceinline__ void quantise_row(const void* src, long long src_off,
             if constexpr (kFp8) {
                 q = (uint8_t)__nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
             } else {
-                q = (uint8_t)(int8_t)max(-127, min(127, __float2int_rn(t)));
+                const int qm = (int)kQmax;
+                q = (uint8_t)(int8_t)max(-qm, min(qm, __float2int_rn(t)));
             }
         }
         codes[e] = q;
     }
-    if constexpr (EPL % 4 == 0) {
+    if constexpr (kCode == kCodeI4) {
+        // EPL (even) codes -> EPL/2 bytes at byte lane*EPL/2
+#pragma unroll
+        for (int e = 0; e < EPL; e += 2)
+            dst[lane * (EPL / 2) + e / 2] = (uint8_t)((codes[e] & 0xF) | ((codes[e + 1] & 0xF) << 4));
+    } else if constexpr (EPL % 4 == 0) {
 #pragma unroll
         for (int w = 0; w < EPL / 4; ++w)
             reinterpret_cast<uint32_t*>(dst + lane * EPL)[w] =
@@ -128,7 +141,7 @@ __device__ __forceinline__ void quantise_row(const void* src, long long src_off,
     if (lane == 0) *scale_dst = sh;
 }
 
-template <typename In, int EPL, bool kFp8>
+template <typename In, int EPL, int kCode>
 __global__ void __launch_bounds__(kWarpsPerCta * 32) append_quant_kernel(const AppendArgs a) {
     grid_dependency_wait();
     launch_dependents();
@@ -143,22 +156,23 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) append_quant_kernel(const A
     const int phys = a.block_tables[(long long)b * a.max_blocks + pos / kBlock];
     const long long sidx = ((long long)phys * a.K + g) * kBlock + pos % kBlock;
     const long long src = row * a.d;
-    quantise_row<In, EPL, kFp8>(a.k_new, src, static_cast<uint8_t*>(a.k_cache) + off, a.k_scale + sidx, lane);
-    quantise_row<In, EPL, kFp8>(a.v_new, src, static_cast<uint8_t*>(a.v_cache) + off, a.v_scale + sidx, lane);
+    const long long boff = kCode == kCodeI4 ? off / 2 : off;      // element -> byte offset
+    quantise_row<In, EPL, kCode>(a.k_new, src, static_cast<uint8_t*>(a.k_cache) + boff, a.k_scale + sidx, lane);
+    quantise_row<In, EPL, kCode>(a.v_new, src, static_cast<uint8_t*>(a.v_cache) + boff, a.v_scale + sidx, lane);
 }
 
-template <bool kFp8>
+template <int kCode>
 const void* quant_kernel(int new_dtype, bool d64) {
     switch (new_dtype) {
         case GQA_DTYPE_F32:
-            return d64 ? reinterpret_cast<const void*>(&append_quant_kernel<float, 2, kFp8>)
-                       : reinterpret_cast<const void*>(&append_quant_kernel<float, 4, kFp8>);
+            return d64 ? reinterpret_cast<const void*>(&append_quant_kernel<float, 2, kCode>)
+                       : reinterpret_cast<const void*>(&append_quant_kernel<float, 4, kCode>);
         case GQA_DTYPE_F16:
-            return d64 ? reinterpret_cast<const void*>(&append_quant_kernel<__half, 2, kFp8>)
-                       : reinterpret_cast<const void*>(&append_quant_kernel<__half, 4, kFp8>);
+            return d64 ? reinterpret_cast<const void*>(&append_quant_kernel<__half, 2, kCode>)
+                       : reinterpret_cast<const void*>(&append_quant_kernel<__half, 4, kCode>);
         default:
-            return d64 ? reinterpret_cast<const void*>(&append_quant_kernel<__nv_bfloat16, 2, kFp8>)
-                       : reinterpret_cast<const void*>(&append_quant_kernel<__nv_bfloat16, 4, kFp8>);
+            return d64 ? reinterpret_cast<const void*>(&append_quant_kernel<__nv_bfloat16, 2, kCode>)
+                       : reinterpret_cast<const void*>(&append_quant_kernel<__nv_bfloat16, 4, kCode>);
     }
 }
 
@@ -187,13 +201,14 @@ cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const v
     a.K = c.num_kv_heads;
     a.d = c.head_dim;
     a.max_blocks = max_blocks;
-    a.es = dtype_size(c.dtype);
+    a.es = dtype_bits(c.dtype) / 8;             // bytes per element of the copy path
     const long long warps = (long long)batch * tokens_per_seq * c.num_kv_heads;
     const int grid = (int)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
     if (grid == 0) return cudaSuccess;
     const void* fn;
-    if (c.dtype == GQA_DTYPE_I8) fn = quant_kernel<false>(new_dtype, a.d == 64);
-    else if (c.dtype == GQA_DTYPE_FP8_E4M3) fn = quant_kernel<true>(new_dtype, a.d == 64);
+    if (c.dtype == GQA_DTYPE_I8) fn = quant_kernel<kCodeI8>(new_dtype, a.d == 64);
+    else if (c.dtype == GQA_DTYPE_FP8_E4M3) fn = quant_kernel<kCodeFp8>(new_dtype, a.d == 64);
+    else if (c.dtype == GQA_DTYPE_I4) fn = quant_kernel<kCodeI4>(new_dtype, a.d == 64);
     else fn = reinterpret_cast<const void*>(&append_copy_kernel);
     // programmatic serialisation: the kernel waits on the device for its predecessor
     cudaLaunchAttribute pdl[1];

@@ -44,11 +44,11 @@ int check_cache(const gqa_kv_cache_t* c) {
     if (c->num_blocks <= 0 || c->num_blocks > 0x7fffffffLL || c->num_kv_heads <= 0)
         return GQA_ERR_INVALID;
     if (c->head_dim != 64 && c->head_dim != 128) return GQA_ERR_UNSUPPORTED;
-    const int es = dtype_size(c->dtype);
-    if (es == 0) return GQA_ERR_INVALID;
+    const int bits = dtype_bits(c->dtype);
+    if (bits == 0) return GQA_ERR_INVALID;
     if (c->stride_block <= 0 || c->stride_head <= 0 || c->stride_token < c->head_dim)
         return GQA_ERR_INVALID;
-    if ((c->stride_block * es) % 16 || (c->stride_head * es) % 16 || (c->stride_token * es) % 16)
+    if ((c->stride_block * bits) % 128 || (c->stride_head * bits) % 128 || (c->stride_token * bits) % 128)
         return GQA_ERR_INVALID;
     if (!aligned16(c->k) || !aligned16(c->v)) return GQA_ERR_INVALID;
     if (dtype_coded(c->dtype)) {
@@ -71,20 +71,21 @@ bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* bas
         case GQA_DTYPE_BF16: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; break;
         default: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;   // one-byte codes
     }
-    const int es = dtype_size(c.dtype);
-    // outer axes: 0 slot, 1 kv-head, 2 block; sort by stride
+    // outer axes: 0 slot, 1 kv-head, 2 block; sort by stride. A 4-bit cache is
+    // described as one-byte elements (d/2 per row).
     const long long stride[3] = {c.stride_token, c.stride_head, c.stride_block};
     const long long extent[3] = {GQA_BLOCK_SIZE, c.num_kv_heads, c.num_blocks};
     int order[3] = {0, 1, 2};
     std::stable_sort(order, order + 3, [&](int x, int y) { return stride[x] < stride[y]; });
-    cuuint64_t gdim[4] = {(cuuint64_t)c.head_dim, 0, 0, 0};
+    const bool i4 = c.dtype == GQA_DTYPE_I4;
+    cuuint64_t gdim[4] = {(cuuint64_t)(i4 ? c.head_dim / 2 : c.head_dim), 0, 0, 0};
     cuuint64_t gstride[3];
     cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, 1, 1};
     cuuint32_t estride[4] = {1, 1, 1, 1};
     for (int i = 0; i < 3; ++i) {
         perm[i] = order[i];
         gdim[i + 1] = (cuuint64_t)extent[order[i]];
-        gstride[i] = (cuuint64_t)(stride[order[i]] * es);
+        gstride[i] = (cuuint64_t)dtype_bytes(c.dtype, stride[order[i]]);
         if (order[i] == 0) box[i + 1] = GQA_BLOCK_SIZE;
     }
     const CUresult r = enc(map, dt, 4, const_cast<void*>(base), gdim, gstride, box, estride,

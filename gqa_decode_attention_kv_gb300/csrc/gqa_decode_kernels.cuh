@@ -122,10 +122,12 @@ struct Cfg {
     static constexpr bool kGen = kGeneral;
     static constexpr bool kI8 = std::is_same<T, int8_t>::value;
     static constexpr bool kFp8 = std::is_same<T, __nv_fp8_e4m3>::value;
-    static constexpr bool kCoded = kI8 || kFp8;     // one-byte codes with fp16 scales
+    static constexpr bool kI4 = std::is_same<T, int4x2>::value;
+    static constexpr bool kCoded = kI8 || kFp8 || kI4;   // codes with fp16 scales
     static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    static constexpr int kEs = sizeof(T);
-    static constexpr int kTile = 16 * D * kEs;                       // one (block, head) tile
+    static constexpr int kEs = sizeof(T);                           // bytes per copied element
+    static constexpr int kRowBytes = kI4 ? D / 2 : D * kEs;          // one token's row
+    static constexpr int kTile = 16 * kRowBytes;                    // one (block, head) tile
     static constexpr int kScaleBytes = kCoded ? 64 : 0;             // 16 k + 16 v fp16 scales
     static constexpr int kStage = ((2 * kTile + kScaleBytes + 1023) / 1024) * 1024;
     static constexpr int kNw = kHeadWarps;
@@ -142,9 +144,11 @@ struct Cfg {
     static constexpr int kRings = kHeadWarps == 1 ? kWarps : 1;
     static constexpr int kStages =
         std::max(2, std::min(8, (kHeadWarps == 1 ? GQA_RING_BYTES_PER_WARP : GQA_SHARED_RING_BYTES) / kStage));
-    static constexpr bool kSwizzle = (kKind == kKernelMma);
-    static constexpr int kBoxInner = kSwizzle ? 128 / kEs : D;        // elements per box row
-    static constexpr int kNumBox = kSwizzle ? (D * kEs) / 128 : 1;
+    // 128-byte swizzled boxes for the tensor-core kernel; a 4-bit tile (64-byte
+    // rows) is read conflict-free without one.
+    static constexpr bool kSwizzle = (kKind == kKernelMma) && !kI4;
+    static constexpr int kBoxInner = kSwizzle ? 128 / kEs : kRowBytes / kEs;   // elements per box row
+    static constexpr int kNumBox = kSwizzle ? kRowBytes / 128 : 1;
     static constexpr int kBoxBytes = 16 * kBoxInner * kEs;
     static constexpr uint32_t kTxBytes = 2 * kTile + kScaleBytes;
     // log2 of how far the block maximum may exceed the running maximum before
@@ -154,6 +158,7 @@ struct Cfg {
     static constexpr int kMt = D / 16;                              // m-tiles of the P.V product
     static constexpr int kRuns = D / 64;                            // 8-dim output runs per head
     static constexpr int kDpl = D / 32;                             // CUDA-core kernel: dims per lane
+    static constexpr int kLaneBytes = kRowBytes / 32;               // ... and their bytes
 };
 
 // Dynamic shared memory layout shared by host and device.
@@ -302,6 +307,20 @@ __device__ __forceinline__ void lds_row_as_float(uint32_t addr, float (&v)[N]) {
             v[e] = f.x;
             v[e + 1] = f.y;
         }
+    } else if constexpr (std::is_same<T, int4x2>::value) {
+        // N 4-bit codes in N/2 bytes, element 2j in the low nibble
+        uint32_t w;
+        if constexpr (N == 4) {
+            unsigned short h;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr));
+            w = h;
+        } else {
+            unsigned short h;
+            asm volatile("ld.shared.u8 %0, [%1];" : "=h"(h) : "r"(addr));
+            w = h;
+        }
+#pragma unroll
+        for (int e = 0; e < N; ++e) v[e] = (float)((int)(((w >> (4 * e)) & 0xFu) ^ 8u) - 8);
     } else if constexpr (std::is_same<T, int8_t>::value) {
         uint32_t w;
         if constexpr (N == 4) {
@@ -388,8 +407,12 @@ struct MmaState {
 // the ring slot can be refilled while the block is being computed.
 template <class C, int D>
 struct MmaFrags {
-    uint32_t k[D / 16][4];     // bf16/f16: A fragments of K per k-step; int8: raw code quads
-    uint32_t v[C::kMt][4];     // bf16/f16: A fragments of V^T per m-tile; int8: raw rows of 4 tokens
+    // bf16/f16: A fragments of K per k-step; int8/fp8: raw code quads; int4:
+    // k[0] / k[1] = the 16 code bytes of tokens r / r+8 at byte 16c
+    uint32_t k[D / 16][4];
+    // bf16/f16: A fragments of V^T per m-tile; int8/fp8: raw rows of 4 tokens;
+    // int4: v[i][0..1] = 8 code bytes (dims 16r..16r+15) of token i
+    uint32_t v[C::kMt][4];
     float ks_r, ks_r8, vs_r, vs_r8;   // int8 scales of tokens r and r+8
 };
 
@@ -407,6 +430,26 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int b, int g, 
         return;
     }
     const uint16_t* base = static_cast<const uint16_t*>(a.q) + q_row<C::kGen>(a, b, g, r) * D;
+    if constexpr (C::kI4) {
+        // 4-bit K: lane c holds dims 32c .. 32c+31 of its tokens; k-step 2u+h
+        // takes dims 32c + 8u + 2h + {0, 4} (.x) and + {1, 5} (.y)
+        static_assert(D == 128, "the 4-bit tensor-core path reads 64-byte rows");
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            uint4 raw = __ldg(reinterpret_cast<const uint4*>(base + 32 * c + 8 * u));
+            if (a.q_dtype == GQA_DTYPE_BF16) {
+                raw.x = bf16x2_to_f16x2(raw.x);
+                raw.y = bf16x2_to_f16x2(raw.y);
+                raw.z = bf16x2_to_f16x2(raw.z);
+                raw.w = bf16x2_to_f16x2(raw.w);
+            }
+            qf[2 * u].x = __byte_perm(raw.x, raw.z, 0x5410);       // dims +0, +4
+            qf[2 * u].y = __byte_perm(raw.x, raw.z, 0x7632);       // dims +1, +5
+            qf[2 * u + 1].x = __byte_perm(raw.y, raw.w, 0x5410);   // dims +2, +6
+            qf[2 * u + 1].y = __byte_perm(raw.y, raw.w, 0x7632);   // dims +3, +7
+        }
+        return;
+    }
 #pragma unroll
     for (int t = 0; t < D / 16; ++t) {
         if constexpr (!C::kCoded) {
@@ -458,6 +501,21 @@ __device__ __forceinline__ void mma_load(MmaFrags<C, D>& f, uint32_t stage, int 
 #pragma unroll
         for (int j = 0; j < C::kMt; ++j)
             ldsm_x4_t(swz(sv, rr + 8 * (mi >> 1), 2 * j + (mi & 1)), f.v[j]);
+    } else if constexpr (C::kI4) {
+        // K: 16 bytes (32 codes) of tokens r and r+8 at byte 16c; V: 8 bytes
+        // (dims 16r..16r+15) of tokens 2c, 2c+1, 2c+8, 2c+9. 64-byte rows, no
+        // swizzle: both patterns touch each bank once per phase, or twice (V).
+        const uint4 k0 = lds128(sk + r * C::kRowBytes + 16 * c);
+        const uint4 k1 = lds128(sk + (r + 8) * C::kRowBytes + 16 * c);
+        f.k[0][0] = k0.x; f.k[0][1] = k0.y; f.k[0][2] = k0.z; f.k[0][3] = k0.w;
+        f.k[1][0] = k1.x; f.k[1][1] = k1.y; f.k[1][2] = k1.z; f.k[1][3] = k1.w;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int tok = 2 * c + (i & 1) + 8 * (i >> 1);
+            const uint2 w = lds64(sv + tok * C::kRowBytes + 8 * r);
+            f.v[i][0] = w.x;
+            f.v[i][1] = w.y;
+        }
     } else {
         // K codes: x4 number t holds chunks 2t (a0/a1) and 2t+1 (a2/a3), 16 codes each
 #pragma unroll
@@ -470,6 +528,8 @@ __device__ __forceinline__ void mma_load(MmaFrags<C, D>& f, uint32_t stage, int 
             const uint4 raw = lds128(swz(sv, tok, r));
             f.v[i][0] = raw.x; f.v[i][1] = raw.y; f.v[i][2] = raw.z; f.v[i][3] = raw.w;
         }
+    }
+    if constexpr (C::kCoded) {
         const uint32_t sc = stage + 2 * C::kTile;
         unsigned short h0, h1, h2, h3;
         asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h0) : "r"(sc + 2 * r));
@@ -507,6 +567,17 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
         for (int t = 0; t < D / 16; ++t) {
             if (t & 1) mma_t<kB>(sb, f.k[t][0], f.k[t][1], f.k[t][2], f.k[t][3], st.qf[t].x, st.qf[t].y);
             else mma_t<kB>(sa, f.k[t][0], f.k[t][1], f.k[t][2], f.k[t][3], st.qf[t].x, st.qf[t].y);
+        }
+    } else if constexpr (C::kI4) {
+        // word u of tokens r / r+8: bytes 4u..4u+3 = dims 32c + 8u + 0..7;
+        // lo/hi nibbles of bytes 0,2 feed k-step 2u, of bytes 1,3 k-step 2u+1
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t w = f.k[0][u], w8 = f.k[1][u];
+            mma_f16(sa, i4_lo_pair(w), i4_lo_pair(w8), i4_hi_pair(w), i4_hi_pair(w8),
+                    st.qf[2 * u].x, st.qf[2 * u].y);
+            mma_f16(sb, i4_lo_pair(w >> 8), i4_lo_pair(w8 >> 8), i4_hi_pair(w >> 8), i4_hi_pair(w8 >> 8),
+                    st.qf[2 * u + 1].x, st.qf[2 * u + 1].y);
         }
     } else {
 #pragma unroll
@@ -645,6 +716,29 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
             }
             return;
         }
+        if constexpr (C::kI4) {
+            // byte j of a token's 8 bytes holds dims 16r + 2j (low nibble, row r
+            // of m-tile j) and 16r + 2j + 1 (high nibble, row r+8). Pair the bytes
+            // of tokens (2c, 2c+1) and (2c+8, 2c+9): (x.bj, x.bj+1, y.bj, y.bj+1).
+#pragma unroll
+            for (int wd = 0; wd < 2; ++wd) {
+                const uint32_t t0 = __byte_perm(f.v[0][wd], f.v[1][wd], 0x5410);
+                const uint32_t t1 = __byte_perm(f.v[0][wd], f.v[1][wd], 0x7632);
+                const uint32_t u0 = __byte_perm(f.v[2][wd], f.v[3][wd], 0x5410);
+                const uint32_t u1 = __byte_perm(f.v[2][wd], f.v[3][wd], 0x7632);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t tx = (e < 2 ? t0 : t1) >> (8 * (e & 1));
+                    const uint32_t ux = (e < 2 ? u0 : u1) >> (8 * (e & 1));
+                    const uint32_t a0 = i4_lo_pair(tx), a1 = i4_hi_pair(tx);
+                    const uint32_t a2 = i4_lo_pair(ux), a3 = i4_hi_pair(ux);
+                    const int j = 4 * wd + e;
+                    mma_f16(st.acc[j], a0, a1, a2, a3, bh0, bh1);
+                    mma_f16(st.acc[j], a0, a1, a2, a3, bl0, bl1);
+                }
+            }
+            return;
+        }
         // A fragment of m-tile j = 2w + e (dims 16r + 4w + 2e, +1) for the token
         // pair (x, y): interleave the two tokens' bytes, then widen each byte to
         // f16 exactly (1024 + (code ^ 0x80) - 1152).
@@ -754,8 +848,8 @@ __device__ __forceinline__ void fma_block(const DecodeArgs& a, FmaState<C, D>& s
     const int G = a.GT - hbase;                  // rows of this warp: hbase .. hbase+7
     for (int t = 0; t < nvalid; ++t) {
         float kf[kN], vf[kN];
-        lds_row_as_float<T, kN>(sk + t * D * C::kEs + lane * kN * C::kEs, kf);
-        lds_row_as_float<T, kN>(sv + t * D * C::kEs + lane * kN * C::kEs, vf);
+        lds_row_as_float<T, kN>(sk + t * C::kRowBytes + lane * C::kLaneBytes, kf);
+        lds_row_as_float<T, kN>(sv + t * C::kRowBytes + lane * C::kLaneBytes, vf);
         float ksc = a.scale_log2, vsc = 1.f;
         if constexpr (C::kCoded) {
             unsigned short hk, hv;
@@ -1346,7 +1440,8 @@ template <typename T, int D, bool kGen>
 bool pick_kind(int kind, int nw, Variant& v) {
     if (kind == kKernelMma) {
         if constexpr (std::is_same<T, float>::value ||
-                      ((std::is_same<T, int8_t>::value || std::is_same<T, __nv_fp8_e4m3>::value) && D != 128)) {
+                      ((std::is_same<T, int8_t>::value || std::is_same<T, __nv_fp8_e4m3>::value ||
+                        std::is_same<T, int4x2>::value) && D != 128)) {
             return false;
         } else {
             v = pick_width<kKernelMma, T, D, kGen>(nw);
@@ -1381,6 +1476,7 @@ bool pick_variant(int dtype, int kind, int d, int nw, Variant& v) {
         case GQA_DTYPE_BF16: return pick_dim<__nv_bfloat16, kGen>(kind, d, nw, v);
         case GQA_DTYPE_I8: return pick_dim<int8_t, kGen>(kind, d, nw, v);
         case GQA_DTYPE_FP8_E4M3: return pick_dim<__nv_fp8_e4m3, kGen>(kind, d, nw, v);
+        case GQA_DTYPE_I4: return pick_dim<int4x2, kGen>(kind, d, nw, v);
         default: return false;
     }
 }

@@ -242,6 +242,39 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
+// Element tag of a 4-bit cache: one byte holds two codes (element 2j in the
+// low nibble). Only its size (1) and identity are used.
+struct int4x2 {
+    uint8_t v;
+};
+
+// d = b ? (a ^ c) : c, bit by bit (one LOP3): with b a mask and c holding the
+// bits to flip under the mask and the bits to set elsewhere.
+__device__ __forceinline__ uint32_t lop3_select_xor(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Two signed 4-bit codes -> f16 pair, exactly. From the low nibbles of bytes 0
+// and 2 of w: each becomes the fp16 1024 + (code ^ 8) = 1032 + code (nibble
+// under the exponent of 1024), then 1032 is subtracted.
+__device__ __forceinline__ uint32_t i4_lo_pair(uint32_t w) {
+    uint32_t h = lop3_select_xor(w, 0x000F000Fu, 0x64086408u);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+// The same from the high nibbles of bytes 0 and 2: 1024 + 16*(code ^ 8) =
+// 1152 + 16*code, so code = x/16 - 72 (one exact fma).
+__device__ __forceinline__ uint32_t i4_hi_pair(uint32_t w) {
+    uint32_t h = lop3_select_xor(w, 0x00F000F0u, 0x64806480u);
+    const __half2 m = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));   // 1/16
+    const __half2 c = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));   // -72
+    const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&h), m, c);
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 // Byte permute with the PTX selector semantics: a selector nibble with bit 3
 // set writes the sign of the chosen byte replicated over all 8 bits.
 __device__ __forceinline__ uint32_t prmt(uint32_t x, uint32_t y, uint32_t sel) {

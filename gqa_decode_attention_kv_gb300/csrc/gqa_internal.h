@@ -9,19 +9,24 @@
 
 namespace gqa {
 
-inline int dtype_size(int dt) {
+inline int dtype_bits(int dt) {
     switch (dt) {
-        case GQA_DTYPE_F32: return 4;
-        case GQA_DTYPE_F16: return 2;
-        case GQA_DTYPE_BF16: return 2;
-        case GQA_DTYPE_I8: return 1;
-        case GQA_DTYPE_FP8_E4M3: return 1;
+        case GQA_DTYPE_F32: return 32;
+        case GQA_DTYPE_F16: return 16;
+        case GQA_DTYPE_BF16: return 16;
+        case GQA_DTYPE_I8: return 8;
+        case GQA_DTYPE_FP8_E4M3: return 8;
+        case GQA_DTYPE_I4: return 4;
         default: return 0;
     }
 }
+// Bytes of n elements of a cache dtype (n even for 4-bit elements).
+inline long long dtype_bytes(int dt, long long n) { return n * dtype_bits(dt) / 8; }
 
-// One-byte code caches with per-(token, kv-head) fp16 scales.
-inline bool dtype_coded(int dt) { return dt == GQA_DTYPE_I8 || dt == GQA_DTYPE_FP8_E4M3; }
+// Code caches (8- or 4-bit codes) with per-(token, kv-head) fp16 scales.
+inline bool dtype_coded(int dt) {
+    return dt == GQA_DTYPE_I8 || dt == GQA_DTYPE_FP8_E4M3 || dt == GQA_DTYPE_I4;
+}
 
 // Which split-KV kernel runs.
 enum KernelKind { kKernelMma = 1, kKernelFma = 2 };

@@ -33,9 +33,9 @@ BLOCK_SIZE = 16
 
 # dtype names shared with the C-ABI enum (gqa_dtype_t in include/gqa_decode.h)
 DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "i8": torch.int8,
-          "fp8": torch.float8_e4m3fn}
-DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3, "fp8": 4}
-CODED = ("i8", "fp8")        # one-byte code caches with per-(token, kv-head) fp16 scales
+          "fp8": torch.float8_e4m3fn, "i4": torch.uint8}     # i4: two codes per byte
+DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3, "fp8": 4, "i4": 5}
+CODED = ("i8", "fp8", "i4")  # code caches with per-(token, kv-head) fp16 scales
 
 @dataclasses.dataclass(frozen=True)
 class Workload:
@@ -74,6 +74,8 @@ WORKLOADS = {
                                    "uniform:2048:8192"),
     "fp8kv_b128_ragged": Workload("fp8kv_b128_ragged", 128, 64, 8, 128, "fp8", "bf16",
                                   "uniform:2048:8192"),
+    "int4kv_b128_ragged": Workload("int4kv_b128_ragged", 128, 64, 8, 128, "i4", "bf16",
+                                   "uniform:2048:8192"),
     # four new tokens per sequence (speculative verification of three drafts),
     # Llama-3-8B shape; the lengths include the new tokens
     "spec_verify_bf16_b64_s4096_t4": Workload("spec_verify_bf16_b64_s4096_t4", 64, 32, 8, 128,
@@ -159,7 +161,9 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
     uniform codes in [-127, 127] with fp16 scales in [0.015, 0.035] (the scale a
     row of 128 N(0,1) draws gets from its max magnitude); FP8 caches hold e4m3
     codes of N(0, 128^2) draws clipped to +-448 with fp16 scales in
-    [0.006, 0.010]."""
+    [0.006, 0.010]; int4 caches hold uniform codes in [-7, 7], two per byte
+    (the row's last dim is d/2), with fp16 scales in [0.35, 0.50] (amax/7 of
+    128 N(0,1) draws)."""
     if q_dtype is None:
         q_dtype = "bf16" if cache_dtype in CODED else cache_dtype
     if new_dtype is None:
@@ -202,6 +206,16 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
         sshape = (num_blocks, K, bs)
         ks = (torch.rand(sshape, generator=gen_dev, device=dev) * 0.02 + 0.015).to(torch.float16)
         vs = (torch.rand(sshape, generator=gen_dev, device=dev) * 0.02 + 0.015).to(torch.float16)
+    elif cache_dtype == "i4":
+        pshape = shape[:-1] + (d // 2,)
+        def packed():
+            lo = torch.randint(-7, 8, pshape, generator=gen_dev, device=dev, dtype=torch.int32)
+            hi = torch.randint(-7, 8, pshape, generator=gen_dev, device=dev, dtype=torch.int32)
+            return ((lo & 0xF) | ((hi & 0xF) << 4)).to(torch.uint8)
+        kc, vc = packed(), packed()
+        sshape = (num_blocks, K, bs)
+        ks = (torch.rand(sshape, generator=gen_dev, device=dev) * 0.15 + 0.35).to(torch.float16)
+        vs = (torch.rand(sshape, generator=gen_dev, device=dev) * 0.15 + 0.35).to(torch.float16)
     elif cache_dtype == "fp8":
         def codes():
             x = torch.randn(shape, generator=gen_dev, device=dev) * 128.0

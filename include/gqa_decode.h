@@ -48,7 +48,9 @@ typedef enum {
     GQA_DTYPE_F16 = 1,
     GQA_DTYPE_BF16 = 2,
     GQA_DTYPE_I8 = 3,         /* cache only: int8 codes + one fp16 scale per (token, kv-head) */
-    GQA_DTYPE_FP8_E4M3 = 4    /* cache only: e4m3 codes (max 448) + one fp16 scale per (token, kv-head) */
+    GQA_DTYPE_FP8_E4M3 = 4,   /* cache only: e4m3 codes (max 448) + one fp16 scale per (token, kv-head) */
+    GQA_DTYPE_I4 = 5          /* cache only: 4-bit codes in [-7, 7], two per byte + one fp16 scale
+                                 per (token, kv-head) */
 } gqa_dtype_t;
 
 /* Return codes. */
@@ -78,10 +80,13 @@ typedef enum {
  * stride_head = d, stride_token = K*d and the identity block table
  * table[b][j] = b*(S_pad/16) + j.
  *
- * For the coded caches (GQA_DTYPE_I8, GQA_DTYPE_FP8_E4M3), k_scale / v_scale
- * hold one fp16 scale per (block, kv-head, slot) as [num_blocks, K, 16]; the
- * cached value is code * scale (an int8 code, or the value of an e4m3 code).
- * Other dtypes leave them NULL.
+ * For the coded caches (GQA_DTYPE_I8, GQA_DTYPE_FP8_E4M3, GQA_DTYPE_I4),
+ * k_scale / v_scale hold one fp16 scale per (block, kv-head, slot) as
+ * [num_blocks, K, 16]; the cached value is code * scale (an int8 or int4
+ * code, or the value of an e4m3 code). Other dtypes leave them NULL. An I4
+ * element is half a byte: elements 2j and 2j+1 of a row share byte j, 2j in
+ * the low nibble, each a two's-complement 4-bit code; strides still count
+ * elements (byte offset = element offset / 2).
  *
  * Requirements: block_size == 16; head_dim in {64, 128}; k, v, k_scale,
  * v_scale 16-byte aligned; every stride times the element size a multiple of
@@ -159,7 +164,10 @@ GQA_API int64_t gqa_kv_pool_elements(int64_t num_blocks, int32_t num_kv_heads, i
  *                 device: amax = max|x| (fp32); s = fp16_rne(min(amax/127, 65504));
  *                 code = s == 0 ? 0 : clamp(rint(x/s), -127, 127) with IEEE fp32
  *                 division (symmetric int8, "LLM 推理性能优化实战" sections 15.1,
- *                 15.2, 15.5). For an FP8_E4M3 cache likewise with
+ *                 15.2, 15.5). For an I4 cache likewise with
+ *                 s = fp16_rne(min(amax/7, 65504)), code = clamp(rint(x/s), -7, 7)
+ *                 (the INT4 KV option of section 15.5), two codes per byte.
+ *                 For an FP8_E4M3 cache likewise with
  *                 s = fp16_rne(min(amax/448, 65504)) and code = e4m3 of x/s,
  *                 rounded to nearest even and saturated to +-448 (the FP8 option
  *                 of section 15.5). The scale goes to k_scale / v_scale.

@@ -48,7 +48,7 @@ def test_append_float_cache_is_bit_exact(gq, oracle_mod, dtype, d):
     assert np.array_equal(got_v, hv)
 
 
-@pytest.mark.parametrize("cache", ["i8", "fp8"])
+@pytest.mark.parametrize("cache", ["i8", "fp8", "i4"])
 @pytest.mark.parametrize("in_dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("d", [128, 64])
 def test_append_coded_cache_quantises_bit_exactly(gq, oracle_mod, cache, in_dtype, d):
@@ -66,15 +66,19 @@ def test_append_coded_cache_quantises_bit_exactly(gq, oracle_mod, cache, in_dtyp
                  case.context_lens.clone())
     torch.cuda.synchronize()
     table = case.block_table.cpu().numpy()
-    quantize = oracle_mod.quantize_int8 if cache == "i8" else oracle_mod.quantize_fp8
+    quantize = {"i8": oracle_mod.quantize_int8, "fp8": oracle_mod.quantize_fp8,
+                "i4": oracle_mod.quantize_int4}[cache]
     hk = before[0].view(np.uint8).copy()
     hv = before[1].view(np.uint8).copy()
     hks = before[2].view(np.uint16).reshape(case.k_scale.shape).copy()
     hvs = before[3].view(np.uint16).reshape(case.v_scale.shape).copy()
+    # a 4-bit pool is written as bytes: packed rows, element strides halved
+    div = 2 if cache == "i4" else 1
     for new, pool, sc in ((case.k_new, hk, hks), (case.v_new, hv, hvs)):
         codes, sbits = quantize(new.float().cpu().numpy())
-        oracle_mod.append(pool, codes.view(np.uint8), table, lens, case.stride_block,
-                          case.stride_head, case.stride_token)
+        rows = oracle_mod.pack_int4(codes) if cache == "i4" else codes.view(np.uint8)
+        oracle_mod.append(pool, rows, table, lens, case.stride_block // div,
+                          case.stride_head // div, case.stride_token // div)
         oracle_mod.append_scales(sc, sbits, table, lens)
     assert np.array_equal(_raw(case.k_cache), hk)
     assert np.array_equal(_raw(case.v_cache), hv)

@@ -123,6 +123,23 @@ def test_fp8_wide_group_f16_query(gq):
     assert max_abs_err(_run(gq, case), oracle_for_case(case)) <= TOL
 
 
+@pytest.mark.parametrize("kernel,d", [(1, 128), (2, 128), (2, 64)])
+def test_int4_cache(gq, kernel, d):
+    lens = [1, 16, 17, 300, 2047, 0, 64]
+    case = gi.make_case(len(lens), 64, 8, d, lens, "i4", q_dtype="bf16", seed=38, device="cuda")
+    ref = oracle_for_case(case)
+    for mw in (0, 3):
+        out = _run(gq, case, kernel=kernel, max_warps=mw, min_blocks_per_warp=1)
+        assert max_abs_err(out, ref) <= TOL
+
+
+@pytest.mark.parametrize("layout", [0, 1, 2])
+def test_int4_wide_group_f16_query(gq, layout):
+    lens = [33, 700, 5, 0]
+    case = gi.make_case(4, 64, 4, 128, lens, "i4", q_dtype="f16", seed=39, device="cuda")
+    assert max_abs_err(_run(gq, case, row_layout=layout), oracle_for_case(case)) <= TOL
+
+
 def test_int8_cache_with_f16_query(gq):
     lens = [40, 333]
     case = gi.make_case(2, 32, 8, 128, lens, "i8", q_dtype="f16", seed=23, device="cuda")
@@ -289,7 +306,7 @@ def _sampled(gq, wl, rows, seed=0, **kw):
 
 def _host_pools(case):
     def host(t):
-        if t.dtype == torch.int8:
+        if t.dtype in (torch.int8, torch.uint8):
             return t.cpu().numpy()
         if t.dtype == torch.float8_e4m3fn:
             return t.cpu().view(torch.uint8).numpy()
@@ -303,6 +320,7 @@ def _host_pools(case):
     ("long_ctx_bf16_b1_s131072", [0]),
     ("int8kv_b128_ragged", [0, 64, 127]),
     ("fp8kv_b128_ragged", [0, 77, 127]),
+    ("int4kv_b128_ragged", [0, 100, 127]),
     ("spec_verify_bf16_b64_s4096_t4", [0, 40, 63]),
     ("mistral7b_swa_bf16_b64_s16384_w4096", [0, 63]),
 ])

@@ -39,7 +39,7 @@ LENS = [1, 5, 15, 16, 17, 31, 33, 100, 300, 0, 1000]
 
 @pytest.mark.parametrize("window", [1, 5, 16, 17, 100, 4096])
 @pytest.mark.parametrize("dtype,kernel", [("bf16", 1), ("bf16", 2), ("f16", 1), ("f32", 2),
-                                          ("i8", 1), ("fp8", 1)])
+                                          ("i8", 1), ("fp8", 1), ("i4", 1), ("i4", 2)])
 def test_sliding_window(gq, dtype, kernel, window):
     case = gi.make_case(len(LENS), 32, 8, 128, LENS, dtype, seed=61, device="cuda")
     ref = oracle_for_case(case, window=window)
@@ -91,7 +91,7 @@ def test_window_wide_group(gq):
 
 @pytest.mark.parametrize("T", [2, 4, 8])
 @pytest.mark.parametrize("dtype,kernel", [("bf16", 1), ("f16", 1), ("bf16", 2), ("f32", 2),
-                                          ("i8", 1), ("fp8", 1)])
+                                          ("i8", 1), ("fp8", 1), ("i4", 1)])
 def test_multi_token_causal(gq, dtype, kernel, T):
     lens = [1, 2, T, T + 1, 16, 17, 64, 300, 0, 1000]
     if kernel == 2 and dtype != "f32" and 4 * T > 8:
@@ -160,7 +160,7 @@ def test_multi_token_append_then_decode(gq, oracle_mod):
     assert max_abs_err(_run(gq, case), ref) <= TOL
 
 
-@pytest.mark.parametrize("cache", ["i8", "fp8"])
+@pytest.mark.parametrize("cache", ["i8", "fp8", "i4"])
 def test_multi_token_append_quantises_bit_exactly(gq, oracle_mod, cache):
     T = 3
     lens = [2, 15, 31]
@@ -171,13 +171,16 @@ def test_multi_token_append_quantises_bit_exactly(gq, oracle_mod, cache):
     gq.kv_append(gq.cache_from_case(case), case.k_new, case.v_new, case.block_table,
                  case.context_lens.clone())
     torch.cuda.synchronize()
-    quantize = oracle_mod.quantize_int8 if cache == "i8" else oracle_mod.quantize_fp8
+    quantize = {"i8": oracle_mod.quantize_int8, "fp8": oracle_mod.quantize_fp8,
+                "i4": oracle_mod.quantize_int4}[cache]
+    div = 2 if cache == "i4" else 1                  # 4-bit pools are written as bytes
     table = case.block_table.cpu().numpy()
     for i in range(T):
         codes, sbits = quantize(case.k_new[:, i].float().cpu().numpy())
+        rows = oracle_mod.pack_int4(codes) if cache == "i4" else codes.view(np.uint8)
         pos = [L + i for L in lens]
-        oracle_mod.append(hk, codes.view(np.uint8), table, pos, case.stride_block,
-                          case.stride_head, case.stride_token)
+        oracle_mod.append(hk, rows, table, pos, case.stride_block // div,
+                          case.stride_head // div, case.stride_token // div)
         oracle_mod.append_scales(hks, sbits, table, pos)
     assert np.array_equal(case.k_cache.detach().cpu().view(torch.uint8).numpy().reshape(-1), hk)
     assert np.array_equal(case.k_scale.detach().cpu().view(torch.int16).numpy().view(np.uint16), hks)
