@@ -13,6 +13,8 @@ would repeat the module name):
 * ``gqa_decode``           -- grouped-query decode attention over the paged cache
                               (one or T causal new tokens per sequence, optional
                               sliding window)
+* ``kv_append_varlen``     -- the same for a different number of new tokens per sequence
+* ``gqa_prefill``          -- causal attention of prompts (any length) over the paged cache
 * ``decode_workspace_size``-- workspace bytes ``gqa_decode`` needs
 * ``kv_pool_elements``     -- elements a pool of ``num_blocks`` blocks holds (K and V)
 """
@@ -103,6 +105,12 @@ def load() -> ctypes.CDLL:
                                                vp, i32, ctypes.c_float, vp, i32,
                                                ctypes.POINTER(DecodeOpts), vp, vp]
             lib.gqa_decode_noalloc.restype = ctypes.c_int
+            lib.gqa_kv_append_varlen.argtypes = [ctypes.POINTER(KVCacheDesc), vp, vp, i32, vp, i32, vp,
+                                                 i32, vp, i32, vp, vp]
+            lib.gqa_kv_append_varlen.restype = ctypes.c_int
+            lib.gqa_prefill.argtypes = [ctypes.POINTER(KVCacheDesc), vp, i32, i32, vp, i32, vp, i32, vp,
+                                        i32, ctypes.c_float, i32, vp, i32, vp, vp]
+            lib.gqa_prefill.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -274,6 +282,37 @@ def gqa_decode_noalloc(cache: PagedKVCache, q: torch.Tensor, block_tables: torch
                                    DTYPE_CODE[out.dtype], ctypes.byref(opts), _ptr(err),
                                    _stream_ptr(stream))
     _check(st, "gqa_decode_noalloc")
+    return out
+
+
+def kv_append_varlen(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tensor,
+                     token_start: torch.Tensor, max_new_tokens: int, block_tables: torch.Tensor,
+                     positions: torch.Tensor, err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Write rows token_start[b] .. token_start[b+1]-1 of k_new/v_new [total, K, d] at
+    positions positions[b], positions[b]+1, ... of sequence b."""
+    desc = cache.desc()
+    st = load().gqa_kv_append_varlen(ctypes.byref(desc), _ptr(k_new), _ptr(v_new),
+                                     DTYPE_CODE[k_new.dtype], _ptr(token_start), int(max_new_tokens),
+                                     _ptr(block_tables), int(block_tables.shape[1]), _ptr(positions),
+                                     int(positions.shape[0]), _ptr(err), _stream_ptr(stream))
+    _check(st, "gqa_kv_append_varlen")
+
+
+def gqa_prefill(cache: PagedKVCache, q: torch.Tensor, q_start: torch.Tensor, max_new_tokens: int,
+                block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.float32,
+                window: int = 0, err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal attention of each sequence's new tokens (rows q_start[b] .. of q
+    [total, H, d]) over its paged cache, new tokens included."""
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    desc = cache.desc()
+    B = int(context_lens.shape[0])
+    st = load().gqa_prefill(ctypes.byref(desc), _ptr(q), DTYPE_CODE[q.dtype], int(q.shape[1]),
+                            _ptr(q_start), int(max_new_tokens), _ptr(block_tables),
+                            int(block_tables.shape[1]), _ptr(context_lens), B, float(scale), int(window),
+                            _ptr(out), DTYPE_CODE[out.dtype], _ptr(err), _stream_ptr(stream))
+    _check(st, "gqa_prefill")
     return out
 
 

@@ -21,6 +21,7 @@ struct AppendArgs {
     const void* v_new;
     const int32_t* block_tables;
     const int32_t* positions;
+    const int32_t* token_start;   // NULL, or [batch+1] row offsets of k_new/v_new
     int32_t* err;
     long long num_blocks;
     long long sb, sh, st;   // element strides of the cache
@@ -29,12 +30,25 @@ struct AppendArgs {
 
 constexpr int kWarpsPerCta = 4;
 
-// Warp `row` of the grid -> (b, i, g): sequence, new token, kv-head.
-__device__ __forceinline__ void row_of(const AppendArgs& a, long long row, int& b, int& i, int& g) {
+// Warp `row` of the grid -> (b, i, g): sequence, new token, kv-head, and the
+// source row of k_new/v_new; false when sequence b has fewer than i+1 tokens.
+__device__ __forceinline__ bool row_of(const AppendArgs& a, long long row, int& b, int& i, int& g,
+                                       long long& src_row) {
     g = (int)(row % a.K);
     const long long bi = row / a.K;
     i = (int)(bi % a.T);
     b = (int)(bi / a.T);
+    if (a.token_start == nullptr) {
+        src_row = row;
+        return true;
+    }
+    const int t0 = a.token_start[b], n = a.token_start[b + 1] - t0;
+    if (n < 0 || n > a.T) {
+        if (i == 0 && g == 0 && (threadIdx.x & 31) == 0) flag_error(a.err, GQA_DEVERR_POSITION);
+        return false;
+    }
+    src_row = ((long long)t0 + i) * a.K + g;
+    return i < n;
 }
 
 // Resolve (b, token position, g) -> element offset of the destination row, or -1
@@ -60,12 +74,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) append_copy_kernel(const Ap
     const long long row = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
     if (row >= (long long)a.batch * a.T * a.K) return;
     int b, i, g;
-    row_of(a, row, b, i, g);
+    long long srow;
+    if (!row_of(a, row, b, i, g, srow)) return;
     const long long off = dest_offset(a, b, a.positions[b] + i, g, lane);
     if (off < 0) return;
     const int row_bytes = a.d * a.es;
     const int nvec = row_bytes / 16;                 // 16-byte vectors per row
-    const long long src = row * row_bytes;           // k_new/v_new are [batch, T, K, d]
+    const long long src = srow * row_bytes;          // k_new/v_new rows of [*, K, d]
     for (int x = lane; x < 2 * nvec; x += 32) {
         const bool is_v = x >= nvec;
         const int vi = is_v ? x - nvec : x;
@@ -149,13 +164,14 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) append_quant_kernel(const A
     const long long row = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
     if (row >= (long long)a.batch * a.T * a.K) return;
     int b, i, g;
-    row_of(a, row, b, i, g);
+    long long srow;
+    if (!row_of(a, row, b, i, g, srow)) return;
     const int pos = a.positions[b] + i;
     const long long off = dest_offset(a, b, pos, g, lane);
     if (off < 0) return;
     const int phys = a.block_tables[(long long)b * a.max_blocks + pos / kBlock];
     const long long sidx = ((long long)phys * a.K + g) * kBlock + pos % kBlock;
-    const long long src = row * a.d;
+    const long long src = srow * a.d;
     const long long boff = kCode == kCodeI4 ? off / 2 : off;      // element -> byte offset
     quantise_row<In, EPL, kCode>(a.k_new, src, static_cast<uint8_t*>(a.k_cache) + boff, a.k_scale + sidx, lane);
     quantise_row<In, EPL, kCode>(a.v_new, src, static_cast<uint8_t*>(a.v_cache) + boff, a.v_scale + sidx, lane);
@@ -180,8 +196,8 @@ const void* quant_kernel(int new_dtype, bool d64) {
 
 cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const void* v_new,
                              int new_dtype, const int32_t* block_tables, int max_blocks,
-                             const int32_t* positions, int batch, int tokens_per_seq, int32_t* err,
-                             cudaStream_t stream) {
+                             const int32_t* positions, int batch, int tokens_per_seq,
+                             const int32_t* token_start, int32_t* err, cudaStream_t stream) {
     AppendArgs a;
     a.k_cache = c.k;
     a.v_cache = c.v;
@@ -191,6 +207,7 @@ cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const v
     a.v_new = v_new;
     a.block_tables = block_tables;
     a.positions = positions;
+    a.token_start = token_start;
     a.err = err;
     a.num_blocks = c.num_blocks;
     a.sb = c.stride_block;

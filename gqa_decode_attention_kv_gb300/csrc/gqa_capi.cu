@@ -139,9 +139,70 @@ int gqa_kv_append(const gqa_kv_cache_t* cache, const void* k_new, const void* v_
         return GQA_ERR_UNSUPPORTED;
     }
     const cudaError_t e = launch_kv_append(*cache, k_new, v_new, new_dtype, block_tables,
-                                           max_blocks_per_seq, positions, batch, T, err_flag,
+                                           max_blocks_per_seq, positions, batch, T, nullptr, err_flag,
                                            static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+int gqa_kv_append_varlen(const gqa_kv_cache_t* cache, const void* k_new, const void* v_new,
+                         int32_t new_dtype, const int32_t* token_start, int32_t max_new_tokens,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* positions, int32_t batch, int32_t* err_flag, void* stream) {
+    int st = check_cache(cache);
+    if (st != GQA_OK) return st;
+    if (batch < 0 || max_blocks_per_seq <= 0 || max_new_tokens < 0) return GQA_ERR_INVALID;
+    if ((long long)batch * max_new_tokens * cache->num_kv_heads >= 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+    if (batch == 0 || max_new_tokens == 0) return GQA_OK;
+    if (!k_new || !v_new || !token_start || !block_tables || !positions) return GQA_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new)) return GQA_ERR_INVALID;
+    if ((long long)max_blocks_per_seq * GQA_BLOCK_SIZE > 0x7fffffffLL) return GQA_ERR_INVALID;
+    if (dtype_coded(cache->dtype)) {
+        if (new_dtype != GQA_DTYPE_F32 && new_dtype != GQA_DTYPE_F16 && new_dtype != GQA_DTYPE_BF16)
+            return GQA_ERR_UNSUPPORTED;
+    } else if (new_dtype != cache->dtype) {
+        return GQA_ERR_UNSUPPORTED;
+    }
+    const cudaError_t e = launch_kv_append(*cache, k_new, v_new, new_dtype, block_tables,
+                                           max_blocks_per_seq, positions, batch, max_new_tokens,
+                                           token_start, err_flag, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+int gqa_prefill(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int32_t num_heads,
+                const int32_t* q_start, int32_t max_new_tokens, const int32_t* block_tables,
+                int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch, float scale,
+                int32_t sliding_window, void* out, int32_t out_dtype, int32_t* err_flag, void* stream) {
+    int st = check_cache(cache);
+    if (st != GQA_OK) return st;
+    if (batch < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || max_new_tokens < 0 || sliding_window < 0)
+        return GQA_ERR_INVALID;
+    if (num_heads % cache->num_kv_heads) return GQA_ERR_INVALID;
+    if (cache->dtype != GQA_DTYPE_BF16 && cache->dtype != GQA_DTYPE_F16) return GQA_ERR_UNSUPPORTED;
+    if (q_dtype != cache->dtype) return GQA_ERR_UNSUPPORTED;
+    if (out_dtype != GQA_DTYPE_F32 && out_dtype != GQA_DTYPE_BF16 && out_dtype != GQA_DTYPE_F16)
+        return GQA_ERR_UNSUPPORTED;
+    if (batch > 65535 || cache->num_kv_heads > 65535) return GQA_ERR_UNSUPPORTED;   // grid y, z
+    if (!std::isfinite(scale)) return GQA_ERR_INVALID;
+    if (batch == 0 || max_new_tokens == 0) return GQA_OK;
+    if (!q || !q_start || !block_tables || !context_lens || !out) return GQA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(out)) return GQA_ERR_INVALID;
+    PrefillLaunch L;
+    L.cache = cache;
+    L.q = q;
+    L.num_heads = num_heads;
+    L.q_start = q_start;
+    L.max_new_tokens = max_new_tokens;
+    L.block_tables = block_tables;
+    L.max_blocks = max_blocks_per_seq;
+    L.context_lens = context_lens;
+    L.batch = batch;
+    L.scale = scale;
+    L.window = sliding_window;
+    L.out = out;
+    L.out_dtype = out_dtype;
+    L.err = err_flag;
+    L.stream = static_cast<cudaStream_t>(stream);
+    return launch_prefill(L);
 }
 
 size_t gqa_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t num_kv_heads,

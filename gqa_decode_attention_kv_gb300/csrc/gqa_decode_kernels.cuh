@@ -480,12 +480,6 @@ __device__ __forceinline__ void mma_t(float (&d)[4], uint32_t a0, uint32_t a1, u
     else mma_f16(d, a0, a1, a2, a3, b0, b1);
 }
 
-// Address of 16-byte chunk `chunk` of row `tok` in a tile written by TMA with
-// 128-byte swizzle (2 KB boxes of 16 rows x 128 B; chunk index XOR row % 8).
-__device__ __forceinline__ uint32_t swz(uint32_t tile, int tok, int chunk) {
-    return tile + (uint32_t)(chunk >> 3) * 2048u + (uint32_t)tok * 128u +
-           ((uint32_t)((chunk & 7) ^ (tok & 7)) << 4);
-}
 
 // Gather one block's operands from shared memory (all reads of the slot).
 template <class C, int D>

@@ -173,6 +173,13 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     return v;
 }
 
+// Address of 16-byte chunk `chunk` of row `tok` in a tile written by TMA with
+// 128-byte swizzle (2 KB boxes of 16 rows x 128 B; chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int tok, int chunk) {
+    return tile + (uint32_t)(chunk >> 3) * 2048u + (uint32_t)tok * 128u +
+           ((uint32_t)((chunk & 7) ^ (tok & 7)) << 4);
+}
+
 // ---------------------------------------------------------------- math
 
 // 2^x on the SFU (ex2.approx; -inf -> +0).

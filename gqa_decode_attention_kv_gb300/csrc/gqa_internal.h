@@ -38,10 +38,34 @@ constexpr int kMaxWarpsPerSm = 64;
 constexpr int kMaxBatch = 8191;
 constexpr int kMaxGroup = 64;   // query heads per KV head the kernels serve
 
+// token_start: NULL (every sequence appends tokens_per_seq tokens, rows
+// b*T + i of k_new) or [batch+1] row offsets (sequence b appends rows
+// token_start[b] .. token_start[b+1]-1, at most tokens_per_seq of them).
 cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const void* v_new,
                              int new_dtype, const int32_t* block_tables, int max_blocks,
-                             const int32_t* positions, int batch, int tokens_per_seq, int32_t* err,
-                             cudaStream_t stream);
+                             const int32_t* positions, int batch, int tokens_per_seq,
+                             const int32_t* token_start, int32_t* err, cudaStream_t stream);
+
+struct PrefillLaunch {
+    const gqa_kv_cache_t* cache;
+    const void* q;
+    int num_heads;
+    const int32_t* q_start;
+    int max_new_tokens;
+    const int32_t* block_tables;
+    int max_blocks;
+    const int32_t* context_lens;
+    int batch;
+    float scale;
+    int window;
+    void* out;
+    int out_dtype;
+    int32_t* err;
+    cudaStream_t stream;
+};
+
+// Validated launch; returns a gqa_status_t.
+int launch_prefill(const PrefillLaunch& L);
 
 struct DecodeLaunch {
     const gqa_kv_cache_t* cache;

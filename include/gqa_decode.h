@@ -185,6 +185,48 @@ GQA_API int gqa_kv_append(const gqa_kv_cache_t *cache, const void *k_new, const 
                   int32_t tokens_per_seq, int32_t *err_flag, void *stream);
 
 /*
+ * Paged KV append with a different number of new tokens per sequence (a batch
+ * of prompts, or chunks of them): sequence b writes rows token_start[b] ..
+ * token_start[b+1]-1 of k_new / v_new ([total, K, head_dim], 16-byte aligned)
+ * at positions positions[b], positions[b]+1, ... Quantisation and exactness as
+ * gqa_kv_append ("LLM 推理性能优化实战" section 5.3.1: prefill writes every new
+ * token's K and V at increasing positions).
+ *  token_start    device int32 [batch+1], non-decreasing.
+ *  max_new_tokens host bound on token_start[b+1] - token_start[b]; a sequence
+ *                 with more (or a negative count) is skipped and flagged
+ *                 (GQA_DEVERR_POSITION).
+ */
+GQA_API int gqa_kv_append_varlen(const gqa_kv_cache_t *cache, const void *k_new, const void *v_new,
+                  int32_t new_dtype, const int32_t *token_start, int32_t max_new_tokens,
+                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                  const int32_t *positions, int32_t batch, int32_t *err_flag, void *stream);
+
+/*
+ * Paged prefill attention: the n_b = q_start[b+1] - q_start[b] new tokens of
+ * sequence b, at positions context_lens[b] - n_b .. context_lens[b] - 1, each
+ * attend causally to the sequence's cache (their own K/V already appended, e.g.
+ * by gqa_kv_append_varlen) -- the same per-query definition as gqa_decode with
+ * T = n_b, for prompts of any length ("LLM 推理性能优化实战" sections 9.2-9.4:
+ * FlashAttention's tiled Q x KV with the online softmax, reading the paged cache
+ * block by block). With sliding_window W > 0 each query attends only its last W
+ * positions. No workspace: every (query tile, kv-head, sequence) is one CTA.
+ *
+ *  q              device [total new tokens, num_heads, head_dim], rows of
+ *                 sequence b from q_start[b]; the cache dtype (BF16 or F16 caches).
+ *  q_start        device int32 [batch+1], non-decreasing.
+ *  max_new_tokens host bound on every n_b (sizes the grid); a sequence with a
+ *                 larger or negative n_b, or context_lens[b] < n_b, or
+ *                 context_lens[b] > max_blocks_per_seq*16, is skipped and flagged
+ *                 (GQA_DEVERR_CONTEXT_LEN); its output rows are not written.
+ *  out            device [total new tokens, num_heads, head_dim] of out_dtype.
+ *  Limits: BF16/F16 caches; head_dim 64 or 128; batch and K <= 65535.
+ */
+GQA_API int gqa_prefill(const gqa_kv_cache_t *cache, const void *q, int32_t q_dtype, int32_t num_heads,
+                const int32_t *q_start, int32_t max_new_tokens, const int32_t *block_tables,
+                int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch, float scale,
+                int32_t sliding_window, void *out, int32_t out_dtype, int32_t *err_flag, void *stream);
+
+/*
  * Bytes of device workspace gqa_decode needs for this shape (tokens_per_seq as
  * in gqa_decode_opts_t, 0 meaning 1) on `device` (-1 = the current device).
  * Returns 0 on bad arguments. The bound covers every kernel choice, window and
