@@ -224,6 +224,188 @@ def whole_job_gbs(bytes_per_rank: float, world: int, ms: float) -> float:
 
 # ----------------------------------------------------------------------------- our arm
 
+def prefill_flops(wl, lens) -> float:
+    """Algorithmic flops of causal prefill: query i of a length-L sequence with T
+    new tokens attends min(L - T + i + 1, W) positions; 4*d flops per head and
+    attended position (q.k and p.v, multiply-add each)."""
+    T = wl.queries
+    total = 0
+    for L in lens:
+        L = int(L)
+        for i in range(T):
+            n = L - T + i + 1
+            if n <= 0:
+                continue
+            total += min(n, wl.window) if wl.window > 0 else n
+    return 4.0 * wl.head_dim * wl.num_heads * total
+
+
+def run_prefill(args, wl):
+    """One prefill step: the varlen append of every prompt's K/V, then causal
+    attention of all prompt tokens over the paged cache."""
+    import torch
+    import torch.distributed as dist
+
+    import gqa_inputs as gi
+    import gqa_decode_attention_kv_gb300 as gq
+    from gqa_decode_attention_kv_gb300 import build as gbuild
+
+    world, rank, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gbuild.build()
+    gq.load()
+    case = gi.case_for(wl, seed=args.seed + rank, device=str(dev), extra_tokens=0)
+    cache = gq.cache_from_case(case)
+    B, T, H, K, d = wl.batch, wl.queries, wl.num_heads, wl.num_kv_heads, wl.head_dim
+    q = case.q.reshape(B * T, H, d)
+    kn = case.k_new.reshape(B * T, K, d)
+    vn = case.v_new.reshape(B * T, K, d)
+    starts = torch.arange(0, B * T + 1, T, dtype=torch.int32, device=dev)
+    lens = case.context_lens
+    pos = (lens - T).clamp(min=0)
+    out = torch.empty((B * T, H, d), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flops = prefill_flops(wl, lens.cpu().tolist())
+    stream = torch.cuda.current_stream()
+
+    def step(qq=q, kk=kn, vv=vn):
+        gq.kv_append_varlen(cache, kk, vv, starts, T, case.block_table, pos, err=err)
+        gq.gqa_prefill(cache, qq, starts, T, case.block_table, lens, case.scale, out=out,
+                       window=wl.window, err=err)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if err.item() != 0:
+        raise RuntimeError(f"device error flags {err.item()}")
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.5)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    clk = clocks.stop(w0, w1)
+    if world > 1:
+        dist.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    # the attention kernel alone (events around each launch, own loop)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        gq.kv_append_varlen(cache, kn, vn, starts, T, case.block_table, pos, err=err)
+        kev[i][0].record(stream)
+        gq.gqa_prefill(cache, q, starts, T, case.block_table, lens, case.scale, out=out,
+                       window=wl.window, err=err)
+        kev[i][1].record(stream)
+    torch.cuda.synchronize()
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    # end to end with host buffers
+    q_h = torch.empty_like(q, device="cpu").pin_memory()
+    kn_h = torch.empty_like(kn, device="cpu").pin_memory()
+    vn_h = torch.empty_like(vn, device="cpu").pin_memory()
+    q_h.copy_(q)
+    kn_h.copy_(kn)
+    vn_h.copy_(vn)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, kn_d, vn_d = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        kn_d.copy_(kn_h, non_blocking=True)
+        vn_d.copy_(vn_h, non_blocking=True)
+        step(q_d, kn_d, vn_d)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, kn_h, vn_h))
+    d2h = out_h.numel() * out_h.element_size()
+    if err.item() != 0:
+        raise RuntimeError(f"device error flags {err.item()}")
+    ms, e2e_ms, kern_ms = max_over_ranks([ms, e2e_ms, kern_ms], dev)
+    if rank == 0:
+        peaks, peak_kind = measured_peaks()
+        peak = float(peaks["bf16_tflops"])
+        tf = flops * world / (ms * 1e-3) / 1e12
+        kern_tf = flops / (kern_ms * 1e-3) / 1e12
+        line = {
+            "metric": "prefill attention TFLOP/s (causal, algorithmic flops), 1 GPU",
+            "value": round(tf, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.cache_dtype, "data": "synthetic",
+            "config": {"workload": wl.name, "batch": B, "prompt_tokens": T, "num_heads": H,
+                       "num_kv_heads": K, "head_dim": d, "context_lens": wl.lens,
+                       "sliding_window": wl.window, "cache_dtype": wl.cache_dtype,
+                       "block_size": 16, "block_table": "seeded shuffle",
+                       "l2": "K/V re-read by every query tile of a sequence (mostly from L2)",
+                       "step": "kv_append_varlen + gqa_prefill, one attention layer"},
+            "tokens_per_s": round(B * T * world / (ms * 1e-3), 1),
+            "roofline": {"bound": "tensor", "achieved": round(kern_tf, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(kern_tf / peak, 4), "traffic": None,
+                         "kernel": "prefill_kernel", "algorithmic_flops_per_launch": flops,
+                         "avg_launch_ms": round(kern_ms, 5),
+                         "kernel_timing": "CUDA events around every prefill launch, own timed loop",
+                         "peak_source": f"{peak_kind} bf16_tflops (burst, cuBLAS; MEASURED_PEAKS.json)"},
+            "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = prefill_cpu_baseline(wl, case, flops, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def prefill_cpu_baseline(wl, case, flops_all, seconds: float) -> dict:
+    """The oracle on the last queries of sequence 0 (as many as fit in about
+    `seconds`), scaled to TFLOP/s by their own algorithmic flops."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    threads = oracle.num_cpus()
+    q, kd, vd, sl = _oracle_inputs(wl, case, [0])
+    T = wl.queries
+    n = 1
+    while True:
+        sub = q[:, T - n:]
+        t = time.perf_counter()
+        oracle.decode(sub, kd, vd, sl, case.scale, nthreads=threads, window=wl.window)
+        dt = time.perf_counter() - t
+        if dt * 2 > seconds or n == T:
+            break
+        n = min(T, n * 2)
+    L = int(sl[0])
+    att = sum(min(L - T + i + 1, wl.window) if wl.window > 0 else L - T + i + 1 for i in range(T - n, T))
+    f = 4.0 * wl.head_dim * wl.num_heads * att
+    return {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": f"last {n} of {T} prompt tokens of sequence 0 (all {wl.num_heads} heads), fp64 C oracle"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -232,6 +414,8 @@ def run_ours(args):
     import gqa_decode_attention_kv_gb300 as gq
     from gqa_decode_attention_kv_gb300 import build as gbuild
 
+    if resolve_workload(args.workload).kind == "prefill":
+        return run_prefill(args, resolve_workload(args.workload))
     world, rank, local = dist_info()
     if world > 1:
         dist.init_process_group("nccl")
@@ -492,6 +676,8 @@ def run_reference(args):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     case = gi.case_for(wl, seed=args.seed, device=dev, extra_tokens=0)
     threads = oracle.num_cpus()
+    if wl.kind == "prefill":
+        return run_reference_prefill(args, wl, case, threads, world)
     rows = [0]
     q, kd, vd, sl = _oracle_inputs(wl, case, rows)
     lens = case.context_lens.cpu().tolist()
@@ -519,6 +705,45 @@ def run_reference(args):
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def run_reference_prefill(args, wl, case, threads, world):
+    """Reference arm of a prefill workload: each step runs the oracle on the last
+    queries of sequence 0 (about a second of host time), in TFLOP/s."""
+    import oracle
+    q, kd, vd, sl = _oracle_inputs(wl, case, [0])
+    T, L = wl.queries, int(sl[0])
+    n = 1
+    while n < T:
+        t = time.perf_counter()
+        oracle.decode(q[:, T - n:], kd, vd, sl, case.scale, nthreads=threads, window=wl.window)
+        if time.perf_counter() - t > 0.5:
+            break
+        n = min(T, n * 2)
+    sub = q[:, T - n:]
+    att = sum(min(L - T + i + 1, wl.window) if wl.window > 0 else L - T + i + 1 for i in range(T - n, T))
+    f = 4.0 * wl.head_dim * wl.num_heads * att
+    for _ in range(max(3, args.warmup)):
+        oracle.decode(sub, kd, vd, sl, case.scale, nthreads=threads, window=wl.window)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.decode(sub, kd, vd, sl, case.scale, nthreads=threads, window=wl.window)
+        times.append(time.perf_counter() - t)
+    dt = statistics.mean(times)
+    v = round(f / dt / 1e12, 6)
+    sample = f"last {n} of {T} prompt tokens of sequence 0 (all {wl.num_heads} heads) per step, fp64 C oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": "prefill attention TFLOP/s (causal, algorithmic flops), 1 GPU",
+        "value": v, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "prompt_tokens": T,
+                   "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
+                   "head_dim": wl.head_dim, "context_lens": wl.lens},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
 
 
 def main():

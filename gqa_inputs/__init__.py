@@ -51,6 +51,7 @@ class Workload:
     contiguous: bool = False    # un-paged [B, S_pad, K, d] buffer + identity table
     queries: int = 1            # new tokens per sequence (causal among themselves)
     window: int = 0             # sliding window in tokens; 0 = full attention
+    kind: str = "decode"        # "decode" (gqa_decode) or "prefill" (gqa_prefill: queries = prompt)
 
     @property
     def group_size(self) -> int:
@@ -80,6 +81,10 @@ WORKLOADS = {
     # Llama-3-8B shape; the lengths include the new tokens
     "spec_verify_bf16_b64_s4096_t4": Workload("spec_verify_bf16_b64_s4096_t4", 64, 32, 8, 128,
                                               "bf16", "bf16", "const:4096", queries=4),
+    # prefill of 8 fresh 2048-token prompts, Llama-3-8B attention shape
+    "llama3_8b_prefill_bf16_b8_p2048": Workload("llama3_8b_prefill_bf16_b8_p2048", 8, 32, 8, 128,
+                                                "bf16", "bf16", "const:2048", queries=2048,
+                                                kind="prefill"),
     # sliding window of 4096 tokens over 16K-token contexts, Mistral-7B shape
     "mistral7b_swa_bf16_b64_s16384_w4096": Workload("mistral7b_swa_bf16_b64_s16384_w4096", 64, 32, 8,
                                                     128, "bf16", "bf16", "const:16384", window=4096),

@@ -163,3 +163,30 @@ def test_prefill_flags_bad_lengths(gq):
     gq.gqa_prefill(gq.cache_from_case(case), q, q_start, 10, case.block_table, bad, case.scale, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) & gq.GQA_DEVERR_CONTEXT_LEN
+
+
+def test_full_size_prefill_workload_sampled(gq, oracle_mod):
+    """The bench's prefill workload in its launch configuration; the last 24
+    prompt tokens of two sequences against the oracle."""
+    wl = gi.WORKLOADS["llama3_8b_prefill_bf16_b8_p2048"]
+    case = gi.case_for(wl, seed=0, device="cuda")
+    B, T, H, d = wl.batch, wl.queries, wl.num_heads, wl.head_dim
+    q = case.q.reshape(B * T, H, d)
+    starts = torch.arange(0, B * T + 1, T, dtype=torch.int32, device="cuda")
+    out = gq.gqa_prefill(gq.cache_from_case(case), q, starts, T, case.block_table, case.context_lens,
+                         case.scale)
+    torch.cuda.synchronize()
+    kp = case.k_cache.float().cpu().numpy()
+    vp = case.v_cache.float().cpu().numpy()
+    table = case.block_table.cpu().numpy()
+    lens = case.context_lens.cpu().numpy()
+    for b in (0, B - 1):
+        kd = oracle_mod.gather_dense(kp, table, lens, case.stride_block, case.stride_head,
+                                     case.stride_token, wl.num_kv_heads, d, [b])
+        vd = oracle_mod.gather_dense(vp, table, lens, case.stride_block, case.stride_head,
+                                     case.stride_token, wl.num_kv_heads, d, [b])
+        qb = q[b * T:(b + 1) * T].float().cpu().numpy().astype(np.float64)
+        # the last 24 queries: T' = 24 new tokens at the end of the same context
+        ref = oracle_mod.decode(qb[T - 24:][None], kd, vd, [lens[b]], case.scale)[0]
+        got = out[b * T + T - 24:(b + 1) * T].float().cpu().numpy().astype(np.float64)
+        assert np.abs(got - ref).max() <= TOL
