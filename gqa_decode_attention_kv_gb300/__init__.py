@@ -109,7 +109,7 @@ def load() -> ctypes.CDLL:
                                                  i32, vp, i32, vp, vp]
             lib.gqa_kv_append_varlen.restype = ctypes.c_int
             lib.gqa_prefill.argtypes = [ctypes.POINTER(KVCacheDesc), vp, i32, i32, vp, i32, vp, i32, vp,
-                                        i32, ctypes.c_float, i32, vp, i32, vp, vp]
+                                        i32, ctypes.c_float, i32, vp, i32, i32, vp, vp]
             lib.gqa_prefill.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -301,9 +301,11 @@ def kv_append_varlen(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tens
 def gqa_prefill(cache: PagedKVCache, q: torch.Tensor, q_start: torch.Tensor, max_new_tokens: int,
                 block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                 out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.float32,
-                window: int = 0, err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                window: int = 0, err: Optional[torch.Tensor] = None, stream=None,
+                kernel: int = 0) -> torch.Tensor:
     """Causal attention of each sequence's new tokens (rows q_start[b] .. of q
-    [total, H, d]) over its paged cache, new tokens included."""
+    [total, H, d]) over its paged cache, new tokens included. kernel: 0/1
+    tcgen05 (tensor memory), 2 warp-level mma.sync."""
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     desc = cache.desc()
@@ -311,7 +313,7 @@ def gqa_prefill(cache: PagedKVCache, q: torch.Tensor, q_start: torch.Tensor, max
     st = load().gqa_prefill(ctypes.byref(desc), _ptr(q), DTYPE_CODE[q.dtype], int(q.shape[1]),
                             _ptr(q_start), int(max_new_tokens), _ptr(block_tables),
                             int(block_tables.shape[1]), _ptr(context_lens), B, float(scale), int(window),
-                            _ptr(out), DTYPE_CODE[out.dtype], _ptr(err), _stream_ptr(stream))
+                            _ptr(out), DTYPE_CODE[out.dtype], int(kernel), _ptr(err), _stream_ptr(stream))
     _check(st, "gqa_prefill")
     return out
 

@@ -171,8 +171,10 @@ int gqa_kv_append_varlen(const gqa_kv_cache_t* cache, const void* k_new, const v
 int gqa_prefill(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int32_t num_heads,
                 const int32_t* q_start, int32_t max_new_tokens, const int32_t* block_tables,
                 int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch, float scale,
-                int32_t sliding_window, void* out, int32_t out_dtype, int32_t* err_flag, void* stream) {
+                int32_t sliding_window, void* out, int32_t out_dtype, int32_t kernel, int32_t* err_flag,
+                void* stream) {
     int st = check_cache(cache);
+    if (kernel < 0 || kernel > GQA_PREFILL_MMA_SYNC) return GQA_ERR_INVALID;
     if (st != GQA_OK) return st;
     if (batch < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || max_new_tokens < 0 || sliding_window < 0)
         return GQA_ERR_INVALID;
@@ -200,6 +202,7 @@ int gqa_prefill(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int
     L.window = sliding_window;
     L.out = out;
     L.out_dtype = out_dtype;
+    L.kernel = kernel;
     L.err = err_flag;
     L.stream = static_cast<cudaStream_t>(stream);
     return launch_prefill(L);

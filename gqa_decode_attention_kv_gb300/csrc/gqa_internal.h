@@ -60,6 +60,7 @@ struct PrefillLaunch {
     int window;
     void* out;
     int out_dtype;
+    int kernel;                 // GQA_PREFILL_* (0 = tcgen05)
     int32_t* err;
     cudaStream_t stream;
 };

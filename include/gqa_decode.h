@@ -219,12 +219,20 @@ GQA_API int gqa_kv_append_varlen(const gqa_kv_cache_t *cache, const void *k_new,
  *                 context_lens[b] > max_blocks_per_seq*16, is skipped and flagged
  *                 (GQA_DEVERR_CONTEXT_LEN); its output rows are not written.
  *  out            device [total new tokens, num_heads, head_dim] of out_dtype.
+ *  kernel         GQA_PREFILL_AUTO / _TCGEN05: 128-row query tiles on the
+ *                 5th-generation tensor cores (tcgen05.mma, accumulators in
+ *                 tensor memory); GQA_PREFILL_MMA_SYNC: 64-row tiles on
+ *                 warp-level mma.sync (the measured alternative).
  *  Limits: BF16/F16 caches; head_dim 64 or 128; batch and K <= 65535.
  */
+#define GQA_PREFILL_AUTO 0
+#define GQA_PREFILL_TCGEN05 1
+#define GQA_PREFILL_MMA_SYNC 2
 GQA_API int gqa_prefill(const gqa_kv_cache_t *cache, const void *q, int32_t q_dtype, int32_t num_heads,
                 const int32_t *q_start, int32_t max_new_tokens, const int32_t *block_tables,
                 int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch, float scale,
-                int32_t sliding_window, void *out, int32_t out_dtype, int32_t *err_flag, void *stream);
+                int32_t sliding_window, void *out, int32_t out_dtype, int32_t kernel, int32_t *err_flag,
+                void *stream);
 
 /*
  * Bytes of device workspace gqa_decode needs for this shape (tokens_per_seq as

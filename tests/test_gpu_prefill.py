@@ -61,33 +61,51 @@ def _run(gq, case, q, q_start, news, **kw):
     return out
 
 
+KERNELS = [1, 2]      # tcgen05 (tensor memory), warp-level mma.sync
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("H,K,d", [(32, 8, 128), (8, 8, 128), (64, 4, 128), (16, 4, 64), (8, 1, 64)])
-def test_prefill_mixed_prompts(gq, oracle_mod, dtype, H, K, d):
+def test_prefill_mixed_prompts(gq, oracle_mod, dtype, H, K, d, kernel):
     news = [1, 5, 16, 17, 64, 100, 33]
     prior = [0, 7, 40, 0, 500, 3, 16]
     lens = [n + p for n, p in zip(news, prior)]
     case, q, q_start = _case(lens, news, H, K, d, dtype, seed=81)
     ref = _reference(oracle_mod, case, q, news)
-    assert max_abs_err(_run(gq, case, q, q_start, news), ref) <= TOL
+    assert max_abs_err(_run(gq, case, q, q_start, news, kernel=kernel), ref) <= TOL
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("window", [1, 16, 37, 200])
-def test_prefill_sliding_window(gq, oracle_mod, window):
+def test_prefill_sliding_window(gq, oracle_mod, window, kernel):
     news = [3, 64, 129, 300]
     prior = [10, 0, 77, 256]
     lens = [n + p for n, p in zip(news, prior)]
     case, q, q_start = _case(lens, news, 32, 8, 128, "bf16", seed=82)
     ref = _reference(oracle_mod, case, q, news, window=window)
-    assert max_abs_err(_run(gq, case, q, q_start, news, window=window), ref) <= TOL
+    assert max_abs_err(_run(gq, case, q, q_start, news, window=window, kernel=kernel), ref) <= TOL
 
 
-def test_prefill_long_prompt_and_empty_sequences(gq, oracle_mod):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_long_prompt_and_empty_sequences(gq, oracle_mod, kernel):
     news = [0, 1000, 0, 513]
     lens = [5, 1000, 0, 1030]
     case, q, q_start = _case(lens, news, 32, 8, 128, "bf16", seed=83)
     ref = _reference(oracle_mod, case, q, news)
-    assert max_abs_err(_run(gq, case, q, q_start, news), ref) <= TOL
+    assert max_abs_err(_run(gq, case, q, q_start, news, kernel=kernel), ref) <= TOL
+
+
+def test_prefill_kernels_agree_on_large_scores(gq, oracle_mod):
+    """Scores spread over hundreds of log2 units: the lazy rescale of the tensor-
+    memory accumulator has to fire; both kernels match the oracle."""
+    news = [130, 257]
+    lens = [130, 300]
+    case, q, q_start = _case(lens, news, 16, 4, 128, "bf16", seed=89)
+    q = (q.float() * 40.0).to(torch.bfloat16)
+    ref = _reference(oracle_mod, case, q, news)
+    for kernel in KERNELS:
+        assert max_abs_err(_run(gq, case, q, q_start, news, kernel=kernel), ref) <= TOL, kernel
 
 
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
