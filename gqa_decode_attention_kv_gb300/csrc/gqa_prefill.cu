@@ -332,25 +332,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 // ============================================================================
 // The same prefill on the 5th-generation tensor cores (tcgen05.mma, fp32
 // accumulators in tensor memory). One CTA = 128 query rows (the MMA M; one
-// tensor-memory lane and one thread per row) of one (kv-head, sequence); the
-// KV range goes by in chunks of 64 tokens (4 paged blocks):
-//   S[128 x 64]  = Q[128 x d] K_chunk^T     Q, K: K-major 128-byte-swizzled tiles
+// tensor-memory lane per row) of one (kv-head, sequence); the KV range goes by
+// in chunks of 64 tokens (4 paged blocks):
+//   S[128 x 64]  = Q[128 x d] K_chunk^T     Q, K: K-major 128-byte-swizzled
+//                                            shared tiles
 //   softmax      one thread per row: tcgen05.ld of its 64 scores, mask, online
-//                (m, l) with the lazy rescale, P as a high and a low bf16/f16
-//                part written K-major to shared memory
-//   O[128 x d]  += P_hi V + P_lo V          V: the TMA tiles read MN-major
-// One thread issues TMA copies and MMAs; tcgen05.commit on an mbarrier tells
-// every thread when S (and every earlier MMA) is done. K is loaded for chunk
-// c+1 and V for chunk c as soon as S(c) lands (S(c) has read K(c); P(c-1).V(c-1),
-// issued before S(c), has read V(c-1)), so the copies hide behind the softmax.
-// Two CTAs share an SM (shared memory ~97 KB, 256 tensor-memory columns each),
-// so one CTA's softmax runs beside the other's MMAs.
+//                (m, l) with the lazy rescale; P as a high and a low 16-bit
+//                part written to tensor memory with tcgen05.st
+//   O[128 x d]  += P_hi V + P_lo V          A = P from tensor memory, B = the
+//                                            V tiles read MN-major
+// Warp roles: warps 0-3 own the 128 rows (softmax, epilogue); warp 4 issues
+// every TMA copy and every MMA. They meet only on mbarriers: tcgen05.commit
+// -> "S(c) done", each softmax warp -> "P(c) ready", TMA -> "K/V stage full",
+// and a per-slot barrier that publishes which blocks of a chunk exist. K and V
+// have two shared stages each; K(c+2) and V(c+1) load as soon as S(c) lands,
+// a chunk ahead of their use. Two CTAs share an SM (~97 KB of shared memory
+// and 256 tensor-memory columns each).
 
 constexpr int kTcRows = 128;                 // query rows per CTA = M = TMEM lanes
+constexpr int kTcThreads = kTcRows + 32;     // + the producer warp
 constexpr int kTcChunk = 64;                 // KV tokens per step = N of S = K of P.V
 constexpr int kTcBlocks = kTcChunk / kBlock;
-constexpr uint32_t kTmemCols = 256;          // S in columns [0, 64), O in [128, 128 + d)
-constexpr uint32_t kColO = 128;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0;                // S: 64 fp32 columns
+constexpr uint32_t kColPh = 64, kColPl = 96; // P high / low: 64 16-bit values in 32 columns each
+constexpr uint32_t kColO = 128;              // O: d fp32 columns
 constexpr float kTcSlack = 8.f;              // log2 headroom before (m, l, O) are rescaled
 
 template <typename T, int D>
@@ -361,15 +367,24 @@ struct TcCfg {
     static constexpr int kKc = kTcChunk * D * 2;                // K chunk: 64 rows per half
     static constexpr int kVb = kBlock * D * 2;                  // one block's V tile
     static constexpr int kVc = kTcBlocks * kVb;                 // V chunk
-    static constexpr int kP = kTcRows * kTcChunk * 2;           // one part of P
-    static constexpr int kOffK = kQ, kOffV = kOffK + kKc, kOffP = kOffV + kVc, kOffBar = kOffP + 2 * kP;
-    static constexpr int kSmem = 1024 + kOffBar + 64;
+    static constexpr int kOffK = kQ, kOffV = kOffK + 2 * kKc, kOffBar = kOffV + 2 * kVc;
+    static constexpr int kSmem = 1024 + kOffBar + 128;
     static constexpr uint32_t kIdescS = mma_idesc_f16(kTcRows, kTcChunk, kBf16, false, false);
     static constexpr uint32_t kIdescO = mma_idesc_f16(kTcRows, D, kBf16, false, true);
 };
 
+// D[tmem] (+)= A[tmem] * B[smem], issued by one thread.
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kTcRows, 2)
+__global__ void __launch_bounds__(kTcThreads, 2)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const PrefillArgs a) {
     using C = TcCfg<T, D>;
@@ -379,11 +394,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const uint32_t sb = (raw + 1023u) & ~1023u;
     uint8_t* gb = smem_raw + (sb - raw);
     const uint32_t sQ = sb, sK = sb + C::kOffK, sV = sb + C::kOffV;
-    const uint32_t sPh = sb + C::kOffP, sPl = sPh + C::kP;
-    const uint32_t bar_k = sb + C::kOffBar, bar_v = bar_k + 8, bar_s = bar_k + 16, tslot = bar_k + 24;
-    volatile uint32_t* cmask = reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 32);   // [2]
+    // barriers (8 B each): K stage 0/1, V stage 0/1, S done, P ready, mask slot 0..3;
+    // then the TMEM address and the 4 block masks
+    const uint32_t bar0 = sb + C::kOffBar;
+    const uint32_t bar_s = bar0 + 32, bar_p = bar0 + 40, tslot = bar0 + 80;
+    volatile uint32_t* cmask = reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 96);   // [4]
+    auto bar_k = [&](int c) { return bar0 + 8 * (c & 1); };
+    auto bar_v = [&](int c) { return bar0 + 16 + 8 * (c & 1); };
+    auto bar_m = [&](int c) { return bar0 + 48 + 8 * (c & 3); };
+    auto par2 = [](int c) { return (uint32_t)(c >> 1) & 1u; };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool producer = warp == 4;
     const int tile = a.tiles_per_seq - 1 - (int)blockIdx.x;    // heaviest first
     const int g = blockIdx.y, b = blockIdx.z;
     if (tid == 0) {
@@ -410,17 +432,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const int jb_hi = (base_pos + tok_hi + kBlock) / kBlock;
     const int nchunks = (jb_hi - jb_lo + kTcBlocks - 1) / kTcBlocks;
 
-    // ---- this thread's row and the positions it attends, [lo, hi)
-    const int rr = row0 + tid;
-    const bool live = rr < rows;
+    // ---- this thread's row (softmax warps) and the positions it attends, [lo, hi)
+    const int rr = row0 + (producer ? 0 : tid);
+    const bool live = !producer && rr < rows;
     const int tk = live ? rr / a.G : 0;
     const int hh = rr - tk * a.G;
     const int hi = live ? base_pos + tk + 1 : 0;
     const int lo = a.window > 0 ? hi - a.window : 0;
     const long long qrow = ((long long)(q0 + tk) * a.H + (long long)g * a.G + hh) * D;
 
-    // ---- Q row into the swizzled K-major tile (zeros past the tile)
-    {
+    if (!producer) {                           // Q row into the swizzled K-major tile
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + qrow);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
@@ -429,9 +450,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
     }
     if (tid == 0) {
-        mbar_init(bar_k, 1);
-        mbar_init(bar_v, 1);
-        mbar_init(bar_s, 1);
+        for (int i = 0; i < 5; ++i) mbar_init(bar0 + 8 * i, 1);
+        mbar_init(bar_p, 4);                   // one arrival per softmax warp
+        for (int i = 0; i < 4; ++i) mbar_init(bar0 + 48 + 8 * i, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tslot, kTmemCols);
@@ -439,209 +460,241 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 24);
-    const uint32_t t_lane = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 80);
+    bool ok = true;
 
-    // ---- copies (warp 0, warp-uniform): lane l holds the table entry of block win_base + l
-    const uint64_t pol = l2_policy_evict_last();   // every query tile of the sequence re-reads them
-    int win_base = -(1 << 30), win_phys = -1;
-    int k_issued = 0, v_issued = 0, s_committed = 0;
-    auto issue_kv = [&](int c, bool is_k) {
-        int ph[kTcBlocks];
-#pragma unroll
-        for (int q = 0; q < kTcBlocks; ++q) {
-            const int j = jb_lo + kTcBlocks * c + q;
-            if (j - win_base >= 32 || j < win_base) {
-                win_base = j;
-                const int jj = j + lane;
-                win_phys = -1;
-                if (jj < jb_hi) {
-                    const int p = a.block_tables[(long long)b * a.max_blocks + jj];
-                    if (p < 0 || p >= a.num_blocks) flag_error(a.err, GQA_DEVERR_BLOCK_INDEX);
-                    else win_phys = p;
-                }
-            }
-            ph[q] = __shfl_sync(kFull, win_phys, j - win_base);
-            if (j >= jb_hi) ph[q] = -1;
-        }
-        if (lane == 0) {
-            uint32_t mask = 0;
-            int nval = 0;
-#pragma unroll
-            for (int q = 0; q < kTcBlocks; ++q)
-                if (ph[q] >= 0) mask |= 1u << q, ++nval;
-            const uint32_t bar = is_k ? bar_k : bar_v;
-            if (is_k) cmask[c & 1] = mask;
-            fence_proxy_async_smem();          // earlier generic writes to the buffer come first
-            mbar_arrive_expect_tx(bar, (uint32_t)(nval * C::kVb));
+    if (producer) {
+        // ================================================== producer warp
+        const uint64_t pol = l2_policy_evict_last();   // every query tile of the sequence re-reads them
+        int win_base = -(1 << 30), win_phys = -1;
+        int k_issued = 0, v_issued = 0, s_committed = 0;
+        auto issue_kv = [&](int c, bool is_k) {
+            int ph[kTcBlocks];
 #pragma unroll
             for (int q = 0; q < kTcBlocks; ++q) {
-                if (ph[q] < 0) continue;
-                auto coord = [&](int which) { return which == 0 ? 0 : (which == 1 ? g : ph[q]); };
-                const int y = coord(a.map_perm[0]), z = coord(a.map_perm[1]), w = coord(a.map_perm[2]);
+                const int j = jb_lo + kTcBlocks * c + q;
+                if (j - win_base >= 32 || j < win_base) {
+                    win_base = j;
+                    const int jj = j + lane;
+                    win_phys = -1;
+                    if (jj < jb_hi) {
+                        const int p = a.block_tables[(long long)b * a.max_blocks + jj];
+                        if (p < 0 || p >= a.num_blocks) flag_error(a.err, GQA_DEVERR_BLOCK_INDEX);
+                        else win_phys = p;
+                    }
+                }
+                ph[q] = __shfl_sync(kFull, win_phys, j - win_base);
+                if (j >= jb_hi) ph[q] = -1;
+            }
+            if (lane == 0) {
+                uint32_t mask = 0;
+                int nval = 0;
 #pragma unroll
-                for (int h = 0; h < C::kHalves; ++h) {
-                    const uint32_t dst = is_k ? sK + h * (kTcChunk * 128) + q * (kBlock * 128)
-                                              : sV + q * C::kVb + h * (kBlock * 128);
-                    tma_load_4d(dst, is_k ? &kmap : &vmap, h * 64, y, z, w, bar, pol);
+                for (int q = 0; q < kTcBlocks; ++q)
+                    if (ph[q] >= 0) mask |= 1u << q, ++nval;
+                const uint32_t bar = is_k ? bar_k(c) : bar_v(c);
+                if (is_k) {
+                    cmask[c & 3] = mask;
+                    mbar_arrive(bar_m(c));     // publishes the mask (release)
+                }
+                fence_proxy_async_smem();      // earlier generic writes to the stage come first
+                mbar_arrive_expect_tx(bar, (uint32_t)(nval * C::kVb));
+                const uint32_t base = is_k ? sK + (c & 1) * C::kKc : sV + (c & 1) * C::kVc;
+#pragma unroll
+                for (int q = 0; q < kTcBlocks; ++q) {
+                    if (ph[q] < 0) continue;
+                    auto coord = [&](int which) { return which == 0 ? 0 : (which == 1 ? g : ph[q]); };
+                    const int y = coord(a.map_perm[0]), z = coord(a.map_perm[1]), w = coord(a.map_perm[2]);
+#pragma unroll
+                    for (int h = 0; h < C::kHalves; ++h) {
+                        const uint32_t dst = is_k ? base + h * (kTcChunk * 128) + q * (kBlock * 128)
+                                                  : base + q * C::kVb + h * (kBlock * 128);
+                        tma_load_4d(dst, is_k ? &kmap : &vmap, h * 64, y, z, w, bar, pol);
+                    }
                 }
             }
-        }
-        if (is_k) ++k_issued;
-        else ++v_issued;
-    };
-    auto issue_s = [&]() {                     // thread 0: S = Q K^T into columns [0, 64)
+            if (is_k) ++k_issued;
+            else ++v_issued;
+        };
+        auto issue_s = [&](int c) {            // S = Q K(c)^T into columns [0, 64)
+            const uint32_t kb = sK + (c & 1) * C::kKc;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t ad = smem_desc_sw128(sQ + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(sK + (ks >> 2) * (kTcChunk * 128) + (ks & 3) * 32, 16, 1024);
-            tc_mma_f16(tmem, ad, bd, C::kIdescS, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint64_t ad = smem_desc_sw128(sQ + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * (kTcChunk * 128) + (ks & 3) * 32, 16, 1024);
+                tc_mma_f16(tmem + kColS, ad, bd, C::kIdescS, ks > 0);
+            }
+        };
+        issue_kv(0, true);
+        if (nchunks > 1) issue_kv(1, true);
+        issue_kv(0, false);
+        if (lane == 0) {
+            ok = mbar_wait(bar_k(0), par2(0));
+            tc_fence_after();
+            if (ok) issue_s(0);
+            tc_commit(bar_s);
         }
-    };
-
-    bool ok = true;
-    if (warp == 0) issue_kv(0, true);
-    if (tid == 0) {
-        ok = mbar_wait(bar_k, 0);
-        tc_fence_after();
-        if (ok) issue_s();
-        tc_commit(bar_s);
-    }
-    s_committed = 1;
-    __syncthreads();                           // chunk 0's block mask is visible to every thread
-
-    float m = -INFINITY, l = 0.f;
-    for (int c = 0; c < nchunks; ++c) {
-        ok = mbar_wait(bar_s, (uint32_t)c & 1u) && ok;      // S(c) and every earlier MMA done
-        tc_fence_after();
-        if (warp == 0) {
-            issue_kv(c, false);                             // V(c): P(c-1).V(c-1) is done
-            if (c + 1 < nchunks) issue_kv(c + 1, true);     // K(c+1): S(c) is done
+        s_committed = 1;
+        ok = __shfl_sync(kFull, ok, 0);
+        for (int c = 0; c < nchunks && ok; ++c) {
+            // S(c) done: its K stage and (via P(c-1).V(c-1) before it) the other V stage are free
+            ok = __all_sync(kFull, mbar_wait(bar_s, (uint32_t)c & 1u));
+            if (!ok) break;
+            if (c + 2 < nchunks) issue_kv(c + 2, true);
+            if (c + 1 < nchunks) issue_kv(c + 1, false);
+            // P(c) written, S(c) read, V(c) rows zeroed by the softmax warps
+            ok = __all_sync(kFull, mbar_wait(bar_p, (uint32_t)c & 1u));
+            if (!ok) break;
+            if (lane == 0) {
+                tc_fence_after();
+                bool w = mbar_wait(bar_v(c), par2(c));
+                if (w) {
+                    const uint32_t vb = sV + (c & 1) * C::kVc;
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                        for (int jl = 0; jl < kTcBlocks; ++jl)
+                            tc_mma_f16_ta(tmem + kColO, tmem + (part ? kColPl : kColPh) + 8 * jl,
+                                          smem_desc_sw128(vb + jl * C::kVb, kBlock * 128, 1024), C::kIdescO,
+                                          !(c == 0 && part == 0 && jl == 0));
+                    }
+                    if (c + 1 < nchunks) {
+                        w = mbar_wait(bar_k(c + 1), par2(c + 1));
+                        tc_fence_after();
+                        if (w) issue_s(c + 1);
+                    }
+                }
+                tc_commit(bar_s);              // phase c+1: P(c).V(c) (and S(c+1)) done
+                ok = w;
+            }
+            ok = __shfl_sync(kFull, ok, 0);
+            s_committed = c + 2;
         }
-        const int cpos = (jb_lo + kTcBlocks * c) * kBlock;
-        const uint32_t bm = cmask[c & 1];
-        // ---- this row's 64 scores
-        float sv[kTcChunk];
-#pragma unroll
-        for (int q = 0; q < kTcChunk / 16; ++q) {
-            uint32_t r16[16];
-            tmem_ld16(t_lane + 16 * q, r16);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) sv[16 * q + j] = __uint_as_float(r16[j]) * a.scale_log2;
-        }
-        const bool whole = bm == 0xFu && cpos >= lo && cpos + kTcChunk <= hi;
-        if (!whole) {
-#pragma unroll
-            for (int j = 0; j < kTcChunk; ++j) {
-                const int pos = cpos + j;
-                if (!((bm >> (j / kBlock)) & 1u) || pos < lo || pos >= hi) sv[j] = -INFINITY;
+        if (!ok) {
+            // let this CTA's copies and MMAs land before the tensor memory goes
+            if (lane == 0) {
+                flag_error(a.err, GQA_DEVERR_TIMEOUT);
+                mbar_wait(bar_s, (uint32_t)(s_committed - 1) & 1u, kWaitLimitNs / 4);
+                for (int c = max(0, k_issued - 2); c < k_issued; ++c) mbar_wait(bar_k(c), par2(c), kWaitLimitNs / 4);
+                for (int c = max(0, v_issued - 2); c < v_issued; ++c) mbar_wait(bar_v(c), par2(c), kWaitLimitNs / 4);
             }
         }
-        float mx = sv[0];
+    } else {
+        // ================================================== softmax warps: one row per thread
+        const uint32_t t_lane = tmem + ((uint32_t)(32 * warp) << 16);
+        float m = -INFINITY, l = 0.f;
+        int c = 0;
+        for (; c < nchunks; ++c) {
+            ok = __all_sync(kFull, mbar_wait(bar_s, (uint32_t)c & 1u));   // S(c), earlier MMAs done
+            ok = ok && __all_sync(kFull, mbar_wait(bar_m(c), (uint32_t)(c >> 2) & 1u));
+            if (!ok) break;
+            tc_fence_after();
+            const int cpos = (jb_lo + kTcBlocks * c) * kBlock;
+            const uint32_t bm = cmask[c & 3];
+            float sv[kTcChunk];
+            {
+                uint32_t r0[16], r1[16], r2[16], r3[16];
+                tmem_ld16(t_lane + kColS, r0);
+                tmem_ld16(t_lane + kColS + 16, r1);
+                tmem_ld16(t_lane + kColS + 32, r2);
+                tmem_ld16(t_lane + kColS + 48, r3);
+                tmem_wait_ld();
 #pragma unroll
-        for (int j = 1; j < kTcChunk; ++j) mx = fmaxf(mx, sv[j]);
-        // lazy rescale: keep the stale maximum while the new one stays within 2^slack
-        const bool old_live = m != -INFINITY;
-        const bool resc = mx > m + kTcSlack;
-        float alpha = 1.f;
-        if (resc) {
-            alpha = old_live ? fast_exp2(m - mx) : 0.f;
-            m = mx;
+                for (int j = 0; j < 16; ++j) {
+                    sv[j] = __uint_as_float(r0[j]) * a.scale_log2;
+                    sv[16 + j] = __uint_as_float(r1[j]) * a.scale_log2;
+                    sv[32 + j] = __uint_as_float(r2[j]) * a.scale_log2;
+                    sv[48 + j] = __uint_as_float(r3[j]) * a.scale_log2;
+                }
+            }
+            const bool whole = bm == 0xFu && cpos >= lo && cpos + kTcChunk <= hi;
+            if (!whole) {
+#pragma unroll
+                for (int j = 0; j < kTcChunk; ++j) {
+                    const int pos = cpos + j;
+                    if (!((bm >> (j / kBlock)) & 1u) || pos < lo || pos >= hi) sv[j] = -INFINITY;
+                }
+            }
+            float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};      // short chains
+#pragma unroll
+            for (int j = 4; j < kTcChunk; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], sv[j]);
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            // lazy rescale: keep the stale maximum while the new one stays within 2^slack
+            const bool old_live = m != -INFINITY;
+            const bool resc = mx > m + kTcSlack;
+            float alpha = 1.f;
+            if (resc) {
+                alpha = old_live ? fast_exp2(m - mx) : 0.f;
+                m = mx;
+            }
+            l *= alpha;
+            if (c > 0 && __any_sync(kFull, resc && old_live)) {       // O holds earlier chunks: scale it
+                const float f = (resc && old_live) ? alpha : 1.f;
+#pragma unroll
+                for (int q = 0; q < D / 16; ++q) {
+                    uint32_t r16[16];
+                    tmem_ld16(t_lane + kColO + 16 * q, r16);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r16[j] = __float_as_uint(__uint_as_float(r16[j]) * f);
+                    tmem_st16(t_lane + kColO + 16 * q, r16);
+                }
+            }
+            const float mu = m == -INFINITY ? 0.f : m;    // a row with nothing attended yet: p = 0
+            float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq) {               // 32 tokens -> 16 packed columns each
+                uint32_t ph16[16], pl16[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float x = fast_exp2(sv[32 * hq + 2 * e] - mu), y = fast_exp2(sv[32 * hq + 2 * e + 1] - mu);
+                    ps4[e & 3] += x + y;
+                    ph16[e] = pack2<kB>(x, y);
+                    const float2 f = unpack2<kB>(ph16[e]);
+                    pl16[e] = pack2<kB>(x - f.x, y - f.y);
+                }
+                tmem_st16(t_lane + kColPh + 16 * hq, ph16);
+                tmem_st16(t_lane + kColPl + 16 * hq, pl16);
+            }
+            tmem_wait_st();
+            l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+            // V rows of tokens outside the sequence or of missing blocks hold arbitrary bits
+            if (bm != 0xFu || cpos + kTcChunk > L) {
+                ok = __all_sync(kFull, mbar_wait(bar_v(c), par2(c)));
+                const uint32_t vb = sV + (c & 1) * C::kVc;
+                for (int i = tid; i < kTcChunk * C::kHalves * 8; i += kTcRows) {
+                    const int t = i / (C::kHalves * 8), h = (i / 8) % C::kHalves, ck = i % 8;
+                    if (((bm >> (t / kBlock)) & 1u) && cpos + t < L) continue;
+                    sts128(vb + (t / kBlock) * C::kVb + h * (kBlock * 128) + (t % kBlock) * 128 + ck * 16,
+                           make_uint4(0u, 0u, 0u, 0u));
+                }
+                fence_proxy_async_smem();      // zeroed V visible to the tensor core (the
+                                               // producer reads it after every warp's arrival)
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_p);
+            if (!ok) break;
         }
-        l *= alpha;
-        if (c > 0 && __any_sync(kFull, resc && old_live)) {       // O holds earlier chunks: scale it
-            const float f = (resc && old_live) ? alpha : 1.f;
+        // ---- wait for the last MMAs, then normalise and store this row
+        if (ok) ok = __all_sync(kFull, mbar_wait(bar_s, (uint32_t)nchunks & 1u));
+        tc_fence_after();
+        if (ok) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
             for (int q = 0; q < D / 16; ++q) {
                 uint32_t r16[16];
                 tmem_ld16(t_lane + kColO + 16 * q, r16);
                 tmem_wait_ld();
+                if (live) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) r16[j] = __float_as_uint(__uint_as_float(r16[j]) * f);
-                tmem_st16(t_lane + kColO + 16 * q, r16);
-            }
-            tmem_wait_st();
-        }
-        const float mu = m == -INFINITY ? 0.f : m;    // a row with nothing attended yet: p = 0
-        float psum = 0.f;
-#pragma unroll
-        for (int q = 0; q < kTcChunk / 8; ++q) {
-            uint32_t h4[4], l4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float x = fast_exp2(sv[8 * q + 2 * e] - mu), y = fast_exp2(sv[8 * q + 2 * e + 1] - mu);
-                psum += x + y;
-                h4[e] = pack2<kB>(x, y);
-                const float2 f = unpack2<kB>(h4[e]);
-                l4[e] = pack2<kB>(x - f.x, y - f.y);
-            }
-            const uint32_t off = tid * 128 + ((q ^ (tid & 7)) << 4);
-            sts128(sPh + off, make_uint4(h4[0], h4[1], h4[2], h4[3]));
-            sts128(sPl + off, make_uint4(l4[0], l4[1], l4[2], l4[3]));
-        }
-        l += psum;
-        // ---- V rows of tokens outside the sequence or of missing blocks hold arbitrary bits
-        if (bm != 0xFu || cpos + kTcChunk > L) {
-            ok = mbar_wait(bar_v, (uint32_t)c & 1u) && ok;
-            for (int i = tid; i < kTcChunk * C::kHalves * 8; i += kTcRows) {
-                const int t = i / (C::kHalves * 8), h = (i / 8) % C::kHalves, ck = i % 8;
-                if (((bm >> (t / kBlock)) & 1u) && cpos + t < L) continue;
-                sts128(sV + (t / kBlock) * C::kVb + h * (kBlock * 128) + (t % kBlock) * 128 + ck * 16,
-                       make_uint4(0u, 0u, 0u, 0u));
-            }
-        }
-        fence_proxy_async_smem();              // P (and zeroed V) visible to the tensor core
-        tc_fence_before();
-        ok = __syncthreads_and(ok);
-        tc_fence_after();
-        if (!ok) break;
-        if (tid == 0) {
-            bool w = mbar_wait(bar_v, (uint32_t)c & 1u);
-            if (w) {
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const uint32_t sp = part ? sPl : sPh;
-#pragma unroll
-                    for (int jl = 0; jl < kTcBlocks; ++jl)
-                        tc_mma_f16(tmem + kColO, smem_desc_sw128(sp + jl * 32, 16, 1024),
-                                   smem_desc_sw128(sV + jl * C::kVb, kBlock * 128, 1024), C::kIdescO,
-                                   !(c == 0 && part == 0 && jl == 0));
-                }
-                if (c + 1 < nchunks) {
-                    w = mbar_wait(bar_k, (uint32_t)(c + 1) & 1u);
-                    tc_fence_after();
-                    if (w) issue_s();
+                    for (int j = 0; j < 16; j += 2)
+                        store2(a.out, a.out_dtype, qrow + 16 * q + j, __uint_as_float(r16[j]) * inv,
+                               __uint_as_float(r16[j + 1]) * inv);
                 }
             }
-            tc_commit(bar_s);                  // phase c+1: P(c).V(c) (and S(c+1)) done
-        }
-        s_committed = c + 2;
-    }
-    // ---- wait for the last MMAs, then normalise and store this row
-    if (ok) ok = mbar_wait(bar_s, (uint32_t)nchunks & 1u);
-    tc_fence_after();
-    if (ok) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-        for (int q = 0; q < D / 16; ++q) {
-            uint32_t r16[16];
-            tmem_ld16(t_lane + kColO + 16 * q, r16);
-            tmem_wait_ld();
-            if (live) {
-#pragma unroll
-                for (int j = 0; j < 16; j += 2)
-                    store2(a.out, a.out_dtype, qrow + 16 * q + j, __uint_as_float(r16[j]) * inv,
-                           __uint_as_float(r16[j + 1]) * inv);
-            }
-        }
-    } else {
-        if (tid == 0) flag_error(a.err, GQA_DEVERR_TIMEOUT);
-        // let this CTA's copies and MMAs land before the tensor memory goes
-        if (tid == 0) {
-            mbar_wait(bar_s, (uint32_t)(s_committed - 1) & 1u, kWaitLimitNs / 4);
-            if (k_issued > 0) mbar_wait(bar_k, (uint32_t)(k_issued - 1) & 1u, kWaitLimitNs / 4);
-            if (v_issued > 0) mbar_wait(bar_v, (uint32_t)(v_issued - 1) & 1u, kWaitLimitNs / 4);
+        } else if (lane == 0) {
+            flag_error(a.err, GQA_DEVERR_TIMEOUT);
         }
     }
     tc_fence_before();
@@ -722,7 +775,7 @@ int launch_prefill(const PrefillLaunch& L) {
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.tiles_per_seq, (unsigned)K, (unsigned)L.batch);
-    cfg.blockDim = dim3(tc ? kTcRows : kPfWarps * 32);
+    cfg.blockDim = dim3(tc ? kTcThreads : kPfWarps * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = L.stream;
     cfg.attrs = pdl;
