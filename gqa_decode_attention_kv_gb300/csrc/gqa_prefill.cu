@@ -486,31 +486,35 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 ph[q] = __shfl_sync(kFull, win_phys, j - win_base);
                 if (j >= jb_hi) ph[q] = -1;
             }
+            const uint32_t bar = is_k ? bar_k(c) : bar_v(c);
             if (lane == 0) {
                 uint32_t mask = 0;
                 int nval = 0;
 #pragma unroll
                 for (int q = 0; q < kTcBlocks; ++q)
                     if (ph[q] >= 0) mask |= 1u << q, ++nval;
-                const uint32_t bar = is_k ? bar_k(c) : bar_v(c);
                 if (is_k) {
                     cmask[c & 3] = mask;
                     mbar_arrive(bar_m(c));     // publishes the mask (release)
                 }
-                fence_proxy_async_smem();      // earlier generic writes to the stage come first
                 mbar_arrive_expect_tx(bar, (uint32_t)(nval * C::kVb));
-                const uint32_t base = is_k ? sK + (c & 1) * C::kKc : sV + (c & 1) * C::kVc;
+            }
+            fence_proxy_async_smem();          // earlier generic writes to the stage come first
+            __syncwarp();
+            // one lane per (block, half) box
+            if (lane < kTcBlocks * C::kHalves) {
+                const int q = lane / C::kHalves, h = lane % C::kHalves;
+                int pq = ph[0];
 #pragma unroll
-                for (int q = 0; q < kTcBlocks; ++q) {
-                    if (ph[q] < 0) continue;
-                    auto coord = [&](int which) { return which == 0 ? 0 : (which == 1 ? g : ph[q]); };
+                for (int i = 1; i < kTcBlocks; ++i)
+                    if (q == i) pq = ph[i];
+                if (pq >= 0) {
+                    auto coord = [&](int which) { return which == 0 ? 0 : (which == 1 ? g : pq); };
                     const int y = coord(a.map_perm[0]), z = coord(a.map_perm[1]), w = coord(a.map_perm[2]);
-#pragma unroll
-                    for (int h = 0; h < C::kHalves; ++h) {
-                        const uint32_t dst = is_k ? base + h * (kTcChunk * 128) + q * (kBlock * 128)
-                                                  : base + q * C::kVb + h * (kBlock * 128);
-                        tma_load_4d(dst, is_k ? &kmap : &vmap, h * 64, y, z, w, bar, pol);
-                    }
+                    const uint32_t base = is_k ? sK + (c & 1) * C::kKc : sV + (c & 1) * C::kVc;
+                    const uint32_t dst = is_k ? base + h * (kTcChunk * 128) + q * (kBlock * 128)
+                                              : base + q * C::kVb + h * (kBlock * 128);
+                    tma_load_4d(dst, is_k ? &kmap : &vmap, h * 64, y, z, w, bar, pol);
                 }
             }
             if (is_k) ++k_issued;
