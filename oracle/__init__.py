@@ -19,6 +19,9 @@ Functions and the passages they follow:
                             (rounding rule in ``gqa_oracle.c``).
 * ``quantize_fp8`` / ``dequantize_fp8`` -- FP8 E4M3 KV codes with per-(token,
                             kv-head) fp16 scales (section 15.5's FP8 option).
+* ``quantize_int4_channels`` / ``gather_channel_scales`` / ``append_int4_channels``
+                         -- the KIVI-style K cache of section 15.5 (K per channel, V per
+                            token, INT4): one scale per (block, kv-head, channel).
 * ``kv_cache_elements``  -- the KV-size closed form 2 * layers * K * d * S * B,
                             "分组查询注意力 (GQA)" 关键参数 item 2 and
                             "LLM 推理性能优化实战" section 6.1.
@@ -79,6 +82,10 @@ def _load():
                                                  ctypes.c_int32, ctypes.POINTER(ctypes.c_int8),
                                                  ctypes.POINTER(ctypes.c_uint16)]
             lib.oracle_quantize_int4.restype = None
+            lib.oracle_quantize_int4_channels.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int32,
+                                                          ctypes.c_int32, ctypes.POINTER(ctypes.c_int8),
+                                                          ctypes.POINTER(ctypes.c_uint16)]
+            lib.oracle_quantize_int4_channels.restype = None
             lib.oracle_quantize_fp8.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_int64,
                                                 ctypes.c_int32, ctypes.POINTER(ctypes.c_uint8),
                                                 ctypes.POINTER(ctypes.c_uint16)]
@@ -227,6 +234,72 @@ def quantize_int4(x) -> tuple[np.ndarray, np.ndarray]:
     _load().oracle_quantize_int4(_ptr(x, ctypes.c_float), rows, d,
                                  _ptr(codes, ctypes.c_int8), _ptr(scales, ctypes.c_uint16))
     return codes, scales
+
+
+def quantize_int4_channels(x) -> tuple[np.ndarray, np.ndarray]:
+    """One block's K values [n, d] (n <= 16 present tokens) -> (codes [n, d] in
+    [-7, 7] as int8, [d] fp16 scale bits as uint16): one scale per channel over
+    the block's tokens (the KIVI-style K of section 15.5; rule in gqa_oracle.c)."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    n, d = x.shape
+    codes = np.zeros((n, d), dtype=np.int8)
+    scales = np.zeros(d, dtype=np.uint16)
+    if n:
+        _load().oracle_quantize_int4_channels(_ptr(x, ctypes.c_float), n, d,
+                                              _ptr(codes, ctypes.c_int8), _ptr(scales, ctypes.c_uint16))
+    return codes, scales
+
+
+def gather_channel_scales(scale_pool, block_table, lens, batch_index=None):
+    """Dense [B, S_max, K, d] view of per-(block, kv-head, channel) scales held as
+    [NB, K, d]: every token of a block carries its block's channel scales."""
+    sp = np.asarray(scale_pool)
+    table = np.asarray(block_table)
+    lens = np.asarray(lens).reshape(-1)
+    rows = list(range(len(lens)) if batch_index is None else batch_index)
+    S_max = int(max([int(lens[b]) for b in rows] + [0]))
+    out = np.zeros((len(rows), S_max) + sp.shape[1:], dtype=sp.dtype)
+    for n, b in enumerate(rows):
+        L = int(lens[b])
+        t = np.arange(L)
+        out[n, :L] = sp[table[b, t // BLOCK_SIZE].astype(np.int64)]
+    return out
+
+
+def append_int4_channels(pool_bytes, scale_pool, residual, k_rows, block_table, positions,
+                         counts, stride_block: int, stride_head: int, stride_token: int):
+    """The KIVI-style K append: sequence b adds counts[b] tokens (rows of
+    k_rows[b], each [K, d] fp32) at positions[b] ..; every block they touch is
+    re-quantised per channel over all the tokens it then holds, the older ones
+    taken from residual[b] (fp32 [K, 16, d], the unquantised K of the block
+    that was filling), and the rows of a block left unfinished are kept in
+    residual[b]. pool_bytes: flat uint8 K pool (strides in 4-bit elements);
+    scale_pool: [NB, K, d] uint16 fp16 bits. All modified in place."""
+    flat = np.asarray(pool_bytes).reshape(-1)
+    sp = np.asarray(scale_pool)
+    res = np.asarray(residual)
+    for b in range(len(counts)):
+        n, p0 = int(counts[b]), int(positions[b])
+        if n == 0:
+            continue
+        rows = np.asarray(k_rows[b], dtype=np.float32)
+        K = rows.shape[1]
+        for jb in range(p0 // BLOCK_SIZE, (p0 + n - 1) // BLOCK_SIZE + 1):
+            first = jb * BLOCK_SIZE
+            tend = min(BLOCK_SIZE, p0 + n - first)
+            phys = int(block_table[b, jb])
+            for g in range(K):
+                x = np.stack([res[b, g, t] if first + t < p0 else rows[first + t - p0, g]
+                              for t in range(tend)])
+                codes, sbits = quantize_int4_channels(x)
+                packed = pack_int4(codes)
+                for t in range(tend):
+                    off = (phys * stride_block + g * stride_head + t * stride_token) // 2
+                    flat[off:off + packed.shape[1]] = packed[t]
+                sp[phys, g] = sbits
+                if tend < BLOCK_SIZE:
+                    res[b, g, :tend] = x
+    return pool_bytes
 
 
 def pack_int4(codes) -> np.ndarray:

@@ -47,6 +47,17 @@
  *    unused so the range stays symmetric.) Two codes share a byte, element 2j
  *    in the low nibble, as two's-complement nibbles.
  *
+ *  - oracle_quantize_int4_channels: the KIVI-style K cache named in "LLM 推理性能
+ *    优化实战" section 15.5 (K quantised per channel, V per token, both to
+ *    INT4; section 15.2 describes per-channel quantisation as one scale per
+ *    channel). Reading: a channel's group is the tokens one 16-token cache block
+ *    holds for one kv-head (the unit the paged cache stores), with the same
+ *    symmetric rule as the per-token codes, applied down each channel:
+ *      amax_i = max over the block's n present tokens t of |x[t][i]|,
+ *      s_i = fp16_rne(min(amax_i / 7, 65504)),  q[t][i] = clamp(rint(x[t][i] / s_i), -7, 7).
+ *    A block that is still filling is quantised over the tokens it holds so
+ *    far, and again, from the unquantised values, each time a token joins it.
+ *
  *  - oracle_quantize_fp8 / oracle_f32_to_e4m3 / oracle_e4m3_to_f64: the FP8
  *    (E4M3) KV cache named among the KV quantisation options of "LLM 推理性能优化实战"
  *    section 15.5 (FP8 E4M3/E5M2 for long-tailed K/V): per-(token, kv-head) fp16
@@ -136,16 +147,20 @@ float oracle_f16_bits_to_f32(uint16_t h)
 /* int8 KV quantisation, one scale per row                                   */
 /* ------------------------------------------------------------------------- */
 
-/* Symmetric integer quantisation of rows of d values to [-qmax, qmax] with
- * one fp16 scale per row (the rule above, with 127 replaced by qmax). */
-static void quantize_symmetric(const float *x, int64_t rows, int32_t d, float qmax,
-                               int8_t *codes, uint16_t *scale_bits)
+/* Symmetric integer quantisation to [-qmax, qmax] of `groups` groups of
+ * `members` values with one fp16 scale per group (the rule above, with 127
+ * replaced by qmax). Member m of group g sits at x[g*gstride + m*mstride], and
+ * its code goes to the same index of `codes`. Rows of a [rows, d] array are
+ * (groups = rows, gstride = d, members = d, mstride = 1); its channels are
+ * (groups = d, gstride = 1, members = rows, mstride = d). */
+static void quantize_symmetric(const float *x, int64_t groups, int64_t gstride, int32_t members,
+                               int64_t mstride, float qmax, int8_t *codes, uint16_t *scale_bits)
 {
-    for (int64_t r = 0; r < rows; ++r) {
-        const float *xr = x + r * (int64_t)d;
+    for (int64_t g = 0; g < groups; ++g) {
+        const int64_t base = g * gstride;
         float amax = 0.0f;
-        for (int32_t i = 0; i < d; ++i) {
-            float a = fabsf(xr[i]);
+        for (int32_t m = 0; m < members; ++m) {
+            float a = fabsf(x[base + m * mstride]);
             if (a > amax) amax = a;
         }
         volatile float s32 = amax / qmax;        /* IEEE fp32 division */
@@ -153,17 +168,17 @@ static void quantize_symmetric(const float *x, int64_t rows, int32_t d, float qm
         if (s > 65504.0f) s = 65504.0f;
         uint16_t sb = oracle_f32_to_f16_bits(s);
         float sf = oracle_f16_bits_to_f32(sb);
-        scale_bits[r] = sb;
-        for (int32_t i = 0; i < d; ++i) {
+        scale_bits[g] = sb;
+        for (int32_t m = 0; m < members; ++m) {
             int32_t q = 0;
             if (sf != 0.0f) {
-                volatile float t = xr[i] / sf;   /* IEEE fp32 division */
+                volatile float t = x[base + m * mstride] / sf;   /* IEEE fp32 division */
                 float rq = rintf(t);             /* round half to even (default mode) */
                 if (rq > qmax) rq = qmax;
                 if (rq < -qmax) rq = -qmax;
                 q = (int32_t)rq;
             }
-            codes[r * (int64_t)d + i] = (int8_t)q;
+            codes[base + m * mstride] = (int8_t)q;
         }
     }
 }
@@ -171,14 +186,21 @@ static void quantize_symmetric(const float *x, int64_t rows, int32_t d, float qm
 void oracle_quantize_int8(const float *x, int64_t rows, int32_t d,
                           int8_t *codes, uint16_t *scale_bits)
 {
-    quantize_symmetric(x, rows, d, 127.0f, codes, scale_bits);
+    quantize_symmetric(x, rows, d, d, 1, 127.0f, codes, scale_bits);
 }
 
 /* Codes in [-7, 7], one per int8 (packing two per byte is the caller's). */
 void oracle_quantize_int4(const float *x, int64_t rows, int32_t d,
                           int8_t *codes, uint16_t *scale_bits)
 {
-    quantize_symmetric(x, rows, d, 7.0f, codes, scale_bits);
+    quantize_symmetric(x, rows, d, d, 1, 7.0f, codes, scale_bits);
+}
+
+/* One block's [n, d] K values -> codes [n, d] in [-7, 7] and d channel scales. */
+void oracle_quantize_int4_channels(const float *x, int32_t n, int32_t d,
+                                   int8_t *codes, uint16_t *scale_bits)
+{
+    quantize_symmetric(x, d, 1, n, d, 7.0f, codes, scale_bits);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -437,6 +437,100 @@ def test_dequantised_attention_equals_attention_on_dequantised_values(oracle_mod
     assert np.abs(kv - x).max() <= oracle_mod.f16_bits_to_f64(sb).max() / 2 * (1 + 1e-6)
 
 
+# --------------------------------------------------------------------------- KIVI-style K (per channel)
+
+
+def test_int4_channel_rounding_worked_example(oracle_mod):
+    """Worked by hand: channel 0 = (0.7, -1.4, 0.35) has amax 1.4, scale
+    fp16(0.2) = 0.199951171875 (0x3266), and 0.7/s = 3.5009 -> 4, -1.4/s =
+    -7.0017 -> -7, 0.35/s = 1.7504 -> 2. Channel 1 = (1, 0.5, -0.25): scale
+    fp16(1/7) = 0.142822265625 (0x3092), codes 7, 4 (3.5009), -2 (-1.7504).
+    Channel 2 = (3.5, -7, 0): amax 7 gives scale 1, codes rint with ties to even."""
+    x = np.array([[0.7, 1.0, 3.5], [-1.4, 0.5, -7.0], [0.35, -0.25, 0.0]], dtype=np.float32)
+    codes, sbits = oracle_mod.quantize_int4_channels(x)
+    assert sbits.tolist() == [0x3266, 0x3092, 0x3C00]
+    assert codes.tolist() == [[4, 7, 4], [-7, 4, -7], [2, -2, 0]]
+
+
+def test_int4_channel_scales_follow_channels_not_tokens(oracle_mod):
+    """Channel i scaled by 2^i: the scales double channel by channel and the
+    codes of every channel are the same column (a token-wise grouping would
+    give each token one scale instead)."""
+    rng = np.random.default_rng(35)
+    base = rng.uniform(0.5, 2.0, (16, 1)).astype(np.float32)
+    x = base * (np.float32(2.0) ** np.arange(8, dtype=np.float32))[None, :]
+    codes, sbits = oracle_mod.quantize_int4_channels(x)
+    s = oracle_mod.f16_bits_to_f64(sbits)
+    np.testing.assert_array_equal(s[1:] / s[:-1], np.full(7, 2.0))
+    for i in range(1, 8):
+        np.testing.assert_array_equal(codes[:, i], codes[:, 0])
+
+
+def test_int4_channel_quantisation_invariants(oracle_mod):
+    rng = np.random.default_rng(36)
+    for n in (1, 2, 7, 16):
+        x = rng.standard_normal((n, 128)).astype(np.float32) * np.float32(10.0) ** rng.integers(-3, 4, (1, 128))
+        codes, sbits = oracle_mod.quantize_int4_channels(x)
+        s = oracle_mod.f16_bits_to_f64(sbits)
+        # each channel's largest magnitude lands on +-7; codes stay in [-7, 7]
+        assert np.all(np.abs(codes.astype(np.int32)).max(axis=0) == 7)
+        assert codes.min() >= -7 and codes.max() <= 7
+        # reconstruction error is at most half a step of the element's channel
+        err = np.abs(x.astype(np.float64) - codes * s[None, :])
+        assert np.all(err <= s[None, :] / 2 * (1 + 1e-6))
+        # changing one channel changes no other channel's codes or scale
+        y = x.copy()
+        y[:, 5] *= np.float32(-3.0)
+        c2, s2 = oracle_mod.quantize_int4_channels(y)
+        keep = np.arange(128) != 5
+        np.testing.assert_array_equal(c2[:, keep], codes[:, keep])
+        np.testing.assert_array_equal(s2[keep], sbits[keep])
+        # the per-channel codes of x are the per-token codes of x transposed
+        ct, st = oracle_mod.quantize_int4(x.T)
+        np.testing.assert_array_equal(ct.T, codes)
+        np.testing.assert_array_equal(st, sbits)
+    cz, sz = oracle_mod.quantize_int4_channels(np.zeros((3, 64), dtype=np.float32))
+    assert not sz.any() and not cz.any()
+
+
+def test_channel_scale_gather_and_append_on_a_tiny_pool(oracle_mod):
+    """Token by token through a shuffled pool: after each append the block a
+    token landed in holds the per-channel codes of everything in it so far
+    (re-quantised from the unquantised values), finished blocks keep theirs,
+    and the gathered scales follow the block table."""
+    rng = np.random.default_rng(37)
+    K, d, NB = 2, 8, 6
+    table = np.array([[4, 1, 3]], dtype=np.int32)
+    sb_, sh_, st_ = K * 16 * d, 16 * d, d
+    pool = np.zeros(NB * sb_ // 2, dtype=np.uint8)
+    scales = np.zeros((NB, K, d), dtype=np.uint16)
+    resid = np.zeros((1, K, 16, d), dtype=np.float32)
+    xs = rng.standard_normal((40, K, d)).astype(np.float32)
+    for pos in range(40):
+        oracle_mod.append_int4_channels(pool, scales, resid, [xs[pos:pos + 1]], table, [pos], [1],
+                                        sb_, sh_, st_)
+        jb, L = pos // 16, pos + 1
+        for g in range(K):
+            blk = xs[16 * jb:L, g]
+            codes, sbits = oracle_mod.quantize_int4_channels(blk)
+            ph = table[0, jb]
+            np.testing.assert_array_equal(scales[ph, g], sbits)
+            got = pool[(ph * sb_ + g * sh_) // 2:(ph * sb_ + g * sh_) // 2 + len(blk) * d // 2]
+            np.testing.assert_array_equal(oracle_mod.unpack_int4(got.reshape(len(blk), d // 2)), codes)
+    # all 40 appended one at a time == the same 40 appended in one call
+    pool2 = np.zeros_like(pool)
+    scales2 = np.zeros_like(scales)
+    resid2 = np.zeros_like(resid)
+    oracle_mod.append_int4_channels(pool2, scales2, resid2, [xs], table, [0], [40], sb_, sh_, st_)
+    np.testing.assert_array_equal(pool2, pool)
+    np.testing.assert_array_equal(scales2, scales)
+    np.testing.assert_array_equal(resid2[0, :, :8], resid[0, :, :8])
+    dense = oracle_mod.gather_channel_scales(scales, table, [40])
+    assert dense.shape == (1, 40, K, d)
+    for t in (0, 15, 16, 39):
+        np.testing.assert_array_equal(dense[0, t], scales[table[0, t // 16]])
+
+
 # --------------------------------------------------------------------------- generator
 
 
