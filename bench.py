@@ -20,7 +20,6 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-import glob
 import json
 import os
 import statistics
@@ -51,32 +50,56 @@ def algorithmic_bytes(wl, lens) -> dict:
     """Bytes a decode step must move: KV (+scales) of every attended cached
     token once, q in, out (fp32) out, block-table entries and lengths, plus the
     append of the T new tokens."""
-    es = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1, "fp8": 1, "i4": 0.5}[wl.cache_dtype]
+    es = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1, "fp8": 1, "i4": 0.5, "i4kc": 0.5}[wl.cache_dtype]
     qes = {"f32": 4, "f16": 2, "bf16": 2}[wl.q_dtype]
-    T = wl.queries
+    coded = wl.cache_dtype in ("i8", "fp8", "i4", "i4kc")
+    kc = wl.cache_dtype == "i4kc"                  # K scales per (block, kv-head, channel)
+    K, d, T = wl.num_kv_heads, wl.head_dim, wl.queries
     ranges = [attended_range(wl, int(x)) for x in lens]
     tokens = int(sum(hi - lo for lo, hi in ranges))
-    per_token = int(2 * wl.num_kv_heads * wl.head_dim * es)
-    if wl.cache_dtype in ("i8", "fp8", "i4"):
-        per_token += 2 * wl.num_kv_heads * 2
+    per_token = int(2 * K * d * es)
+    if coded:
+        per_token += (1 if kc else 2) * K * 2     # fp16 scales per (token, kv-head)
     blocks = int(sum(-(-hi // 16) - lo // 16 for lo, hi in ranges))
     B = len(lens)
-    kv = tokens * per_token
-    q = B * T * wl.num_heads * wl.head_dim * qes
-    o = B * T * wl.num_heads * wl.head_dim * 4
+    kv = tokens * per_token + (blocks * K * 2 * d if kc else 0)
+    q = B * T * wl.num_heads * d * qes
+    o = B * T * wl.num_heads * d * 4
     meta = blocks * 4 + B * 4
-    new_es = qes if wl.cache_dtype in ("i8", "fp8", "i4") else es
-    append = int(B * T * 2 * wl.num_kv_heads * wl.head_dim * (new_es + es)) + B * 4
+    new_es = qes if coded else es
+    append = int(B * T * 2 * K * d * (new_es + es)) + B * 4
+    if kc:
+        # K: every block the new tokens reach is rewritten whole (codes of its
+        # present slots, d scales), its older slots read from the fp32
+        # residual, and new rows of an unfinished block written back to it;
+        # V: per-token scales
+        append = int(B * T * K * (2 * d * new_es + d * es + 2)) + B * 4
+        for L in lens:
+            p0 = max(0, int(L) - T)
+            for jb in range(p0 // 16, (p0 + T - 1) // 16 + 1):
+                first = 16 * jb
+                tend = min(16, p0 + T - first)
+                old = max(0, p0 - first)
+                append += K * (old * d * 4 + int(tend * d * es) + 2 * d)
+                if tend < 16:
+                    append += K * (tend - old) * d * 4
     decode = kv + q + o + meta
     return {"kv": kv, "decode": decode, "append": append, "step": decode + append,
             "tokens": tokens, "blocks": blocks}
 
 
-def kernel_source_hash() -> str:
+# The sources the split-KV kernel is compiled from: a traffic figure taken on
+# other sources no longer describes it.
+SPLIT_KV_SOURCES = ("gqa_decode_kernels.cuh", "gqa_device.cuh", "gqa_internal.h", "gqa_decode.cu",
+                    "gqa_decode_general.cu")
+
+
+def kernel_source_hash(files=SPLIT_KV_SOURCES) -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "gqa_decode_attention_kv_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    csrc = os.path.join(ROOT, "gqa_decode_attention_kv_gb300", "csrc")
+    for name in sorted(files):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -602,24 +625,31 @@ def _oracle_inputs(wl, case, rows):
         off += len(s)
     sub_lens = lens[rows]
     K, d = wl.num_kv_heads, wl.head_dim
-    rd = d // 2 if wl.cache_dtype == "i4" else d          # stored row (4-bit: bytes)
+    packed4 = wl.cache_dtype in ("i4", "i4kc")
+    rd = d // 2 if packed4 else d                        # stored row (4-bit: bytes)
     sb, sh, st = K * 16 * rd, 16 * rd, rd
     kd = oracle.gather_dense(kp, new_table, sub_lens, sb, sh, st, K, rd)
     vd = oracle.gather_dense(vp, new_table, sub_lens, sb, sh, st, K, rd)
-    if wl.cache_dtype not in ("i4",):
+    if not packed4:
         kd, vd = kd.astype(np.float64), vd.astype(np.float64)
-    if wl.cache_dtype in ("i8", "fp8", "i4"):
+    if wl.cache_dtype in ("i8", "fp8", "i4", "i4kc"):
         ksp = case.k_scale.index_select(0, ids).float().cpu().numpy()
         vsp = case.v_scale.index_select(0, ids).float().cpu().numpy()
-        kss = oracle.gather_scales(ksp, new_table, sub_lens, K)
         vss = oracle.gather_scales(vsp, new_table, sub_lens, K)
-        if wl.cache_dtype == "i8":
+        if wl.cache_dtype == "i4kc":                     # K scales per (block, kv-head, channel)
+            kcs = oracle.gather_channel_scales(ksp.astype(np.float64), new_table, sub_lens)
+            kd = oracle.unpack_int4(kd).astype(np.float64) * kcs
+            vd = oracle.dequantize_int4(vd, vss)
+        elif wl.cache_dtype == "i8":
+            kss = oracle.gather_scales(ksp, new_table, sub_lens, K)
             kd = oracle.dequantize_int8(kd, kss)
             vd = oracle.dequantize_int8(vd, vss)
         elif wl.cache_dtype == "i4":
+            kss = oracle.gather_scales(ksp, new_table, sub_lens, K)
             kd = oracle.dequantize_int4(kd, kss)
             vd = oracle.dequantize_int4(vd, vss)
         else:
+            kss = oracle.gather_scales(ksp, new_table, sub_lens, K)
             kd = oracle.dequantize_fp8(kd.astype(np.uint8), kss)
             vd = oracle.dequantize_fp8(vd.astype(np.uint8), vss)
     q = case.q.float().cpu().numpy().astype(np.float64)[rows]

@@ -41,6 +41,7 @@ GQA_DEVERR_TIMEOUT = 8
 
 KERNEL_AUTO, KERNEL_MMA, KERNEL_FMA = 0, 1, 2
 GQA_DTYPE_I4 = 5
+GQA_DTYPE_I4_KC = 6
 
 
 class GqaError(RuntimeError):
@@ -56,7 +57,9 @@ class KVCacheDesc(ctypes.Structure):
                 ("num_blocks", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("stride_block", ctypes.c_int64),
-                ("stride_head", ctypes.c_int64), ("stride_token", ctypes.c_int64)]
+                ("stride_head", ctypes.c_int64), ("stride_token", ctypes.c_int64),
+                ("k_residual", ctypes.c_void_p), ("residual_rows", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class DecodeOpts(ctypes.Structure):
@@ -145,23 +148,33 @@ class PagedKVCache:
     k_scale: Optional[torch.Tensor] = None
     v_scale: Optional[torch.Tensor] = None
     dtype_code: Optional[int] = None   # set for storage the tensor dtype does not name (int4)
+    k_residual: Optional[torch.Tensor] = None   # KIVI-style cache: fp32 [rows, K, 16, d]
 
     @staticmethod
     def allocate(num_blocks: int, num_kv_heads: int, head_dim: int, dtype,
-                 device="cuda") -> "PagedKVCache":
-        """dtype: a torch dtype, or "int4" for two 4-bit codes per byte (uint8
-        storage [num_blocks, K, 16, d/2]; strides still count 4-bit elements)."""
-        int4 = dtype == "int4"
+                 device="cuda", residual_rows: int = 0) -> "PagedKVCache":
+        """dtype: a torch dtype; "int4" for two 4-bit codes per byte (uint8
+        storage [num_blocks, K, 16, d/2]; strides still count 4-bit elements);
+        "int4kc" for the same codes with K scaled per (block, kv-head, channel)
+        (k_scale [num_blocks, K, d]) and a zeroed fp32 residual of
+        ``residual_rows`` sequences."""
+        int4 = dtype in ("int4", "int4kc")
+        kc = dtype == "int4kc"
         shape = (num_blocks, num_kv_heads, BLOCK_SIZE, head_dim // 2 if int4 else head_dim)
         k = torch.empty(shape, dtype=torch.uint8 if int4 else dtype, device=device)
         v = torch.empty_like(k)
-        ks = vs = None
+        ks = vs = res = None
         if int4 or dtype in (torch.int8, torch.float8_e4m3fn):
-            ks = torch.empty((num_blocks, num_kv_heads, BLOCK_SIZE), dtype=torch.float16, device=device)
-            vs = torch.empty_like(ks)
+            vs = torch.empty((num_blocks, num_kv_heads, BLOCK_SIZE), dtype=torch.float16, device=device)
+            ks = torch.empty((num_blocks, num_kv_heads, head_dim), dtype=torch.float16,
+                             device=device) if kc else torch.empty_like(vs)
+        if kc:
+            res = torch.zeros((residual_rows, num_kv_heads, BLOCK_SIZE, head_dim), dtype=torch.float32,
+                              device=device)
+        code = GQA_DTYPE_I4_KC if kc else GQA_DTYPE_I4 if int4 else None
         return PagedKVCache(k, v, num_blocks, num_kv_heads, head_dim,
                             num_kv_heads * BLOCK_SIZE * head_dim, BLOCK_SIZE * head_dim, head_dim,
-                            ks, vs, GQA_DTYPE_I4 if int4 else None)
+                            ks, vs, code, res)
 
     @property
     def dtype(self) -> torch.dtype:
@@ -174,7 +187,9 @@ class PagedKVCache:
             self.v_scale.data_ptr() if self.v_scale is not None else None,
             self.num_blocks, self.num_kv_heads, BLOCK_SIZE, self.head_dim,
             self.dtype_code if self.dtype_code is not None else DTYPE_CODE[self.k.dtype],
-            self.stride_block, self.stride_head, self.stride_token)
+            self.stride_block, self.stride_head, self.stride_token,
+            self.k_residual.data_ptr() if self.k_residual is not None else None,
+            int(self.k_residual.shape[0]) if self.k_residual is not None else 0, 0)
 
 
 def _stream_ptr(stream) -> Optional[int]:
@@ -323,4 +338,5 @@ def cache_from_case(case) -> PagedKVCache:
     return PagedKVCache(case.k_cache, case.v_cache, case.num_blocks, case.num_kv_heads,
                         case.head_dim, case.stride_block, case.stride_head, case.stride_token,
                         case.k_scale, case.v_scale,
-                        GQA_DTYPE_I4 if case.cache_dtype == "i4" else None)
+                        {"i4": GQA_DTYPE_I4, "i4kc": GQA_DTYPE_I4_KC}.get(case.cache_dtype),
+                        getattr(case, "k_residual", None))

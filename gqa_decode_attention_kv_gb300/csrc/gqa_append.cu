@@ -5,6 +5,9 @@
 // together.
 // For an int8, int4 or FP8 (e4m3) cache each row is quantised on the way (one
 // fp16 scale per (token, kv-head); sections 15.1, 15.2 and 15.5 of that page).
+// The KIVI-style 4-bit cache (section 15.5: K per channel, V per token) takes
+// one warp per (sequence, kv-head) instead: every block the new tokens reach is
+// re-quantised channel by channel over all the tokens it then holds.
 #include "gqa_device.cuh"
 #include "gqa_internal.h"
 
@@ -22,6 +25,7 @@ struct AppendArgs {
     const int32_t* block_tables;
     const int32_t* positions;
     const int32_t* token_start;   // NULL, or [batch+1] row offsets of k_new/v_new
+    float* k_residual;            // KIVI-style cache: fp32 [rows, K, 16, d]
     int32_t* err;
     long long num_blocks;
     long long sb, sh, st;   // element strides of the cache
@@ -177,6 +181,122 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) append_quant_kernel(const A
     quantise_row<In, EPL, kCode>(a.v_new, src, static_cast<uint8_t*>(a.v_cache) + boff, a.v_scale + sidx, lane);
 }
 
+// KIVI-style cache, one warp per (sequence b, kv-head g); lane l owns the EPL
+// channels EPL*l .. EPL*l+EPL-1, so a channel's amax, scale and codes stay in
+// one lane and the slice of a residual row a lane reads is the slice it
+// writes. The n new tokens of b sit at positions p0 .. p0+n-1. Each block
+// they reach is taken whole: its slots before p0 from the residual row, the
+// rest from k_new; per channel over its tend present tokens s_i =
+// fp16(amax_i / 7) and code = clamp(rint(x / s_i), -7, 7) (fp32 IEEE
+// division); codes of every present slot and the d scales are written, and
+// the new rows of a block left unfinished go to the residual. V rows are
+// quantised per token.
+template <typename In, int EPL>
+__global__ void __launch_bounds__(kWarpsPerCta * 32) append_kc_kernel(const AppendArgs a) {
+    grid_dependency_wait();
+    launch_dependents();
+    constexpr int D = 32 * EPL;
+    const int lane = threadIdx.x & 31;
+    const long long pair = (long long)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+    if (pair >= (long long)a.batch * a.K) return;
+    const int b = (int)(pair / a.K), g = (int)(pair % a.K);
+    const bool reporter = g == 0 && lane == 0;
+    int n = a.T;
+    long long t0 = (long long)b * a.T;                   // first source token of b
+    if (a.token_start != nullptr) {
+        t0 = a.token_start[b];
+        n = a.token_start[b + 1] - (int)t0;
+        if (n < 0 || n > a.T) {
+            if (reporter) flag_error(a.err, GQA_DEVERR_POSITION);
+            return;
+        }
+    }
+    if (n == 0) return;
+    const int p0 = a.positions[b];
+    if (p0 < 0 || (long long)p0 + n > (long long)a.max_blocks * kBlock) {
+        if (reporter) flag_error(a.err, GQA_DEVERR_POSITION);
+        return;
+    }
+    float* res = a.k_residual + ((long long)b * a.K + g) * kBlock * D + lane * EPL;
+    const int jb_end = (p0 + n - 1) / kBlock;
+    for (int jb = p0 / kBlock; jb <= jb_end; ++jb) {
+        const int first = jb * kBlock;
+        const int tend = min((int)kBlock, p0 + n - first);
+        const int ph = a.block_tables[(long long)b * a.max_blocks + jb];
+        if (ph < 0 || ph >= a.num_blocks) {
+            if (reporter) flag_error(a.err, GQA_DEVERR_BLOCK_INDEX);
+            continue;
+        }
+        float x[kBlock][EPL];
+        float amax[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) amax[e] = 0.f;
+#pragma unroll
+        for (int t = 0; t < kBlock; ++t) {
+            if (t >= tend) break;
+            const int p = first + t;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                x[t][e] = p < p0 ? res[t * D + e]
+                                 : load_as_float<In>(a.k_new, ((t0 + p - p0) * a.K + g) * D + lane * EPL + e);
+                amax[e] = fmaxf(amax[e], fabsf(x[t][e]));
+            }
+        }
+        float sf[EPL];
+        uint16_t sbits[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            const __half sh = __float2half_rn(fminf(__fdiv_rn(amax[e], 7.0f), 65504.0f));
+            sf[e] = __half2float(sh);
+            sbits[e] = __half_as_ushort(sh);
+        }
+        __half* ks = a.k_scale + ((long long)ph * a.K + g) * D + lane * EPL;
+        if constexpr (EPL == 4)
+            *reinterpret_cast<uint2*>(ks) = make_uint2(sbits[0] | ((uint32_t)sbits[1] << 16),
+                                                       sbits[2] | ((uint32_t)sbits[3] << 16));
+        else
+            *reinterpret_cast<uint32_t*>(ks) = sbits[0] | ((uint32_t)sbits[1] << 16);
+        uint8_t* kb = static_cast<uint8_t*>(a.k_cache) + ((long long)ph * a.sb + (long long)g * a.sh) / 2 +
+                      lane * (EPL / 2);
+#pragma unroll
+        for (int t = 0; t < kBlock; ++t) {
+            if (t >= tend) break;
+            uint32_t packed = 0;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                const int q = sf[e] != 0.f ? max(-7, min(7, __float2int_rn(__fdiv_rn(x[t][e], sf[e])))) : 0;
+                packed |= (uint32_t)(q & 0xF) << (4 * e);
+            }
+            uint8_t* row = kb + (long long)t * (a.st / 2);
+            if constexpr (EPL == 4) *reinterpret_cast<uint16_t*>(row) = (uint16_t)packed;
+            else *row = (uint8_t)packed;
+            if (tend < kBlock && first + t >= p0) {       // the block stays unfinished: keep the row
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) res[t * D + e] = x[t][e];
+            }
+        }
+    }
+    // V: per-token scale, the whole warp per row
+    for (int i = 0; i < n; ++i) {
+        const int pos = p0 + i;
+        const int ph = a.block_tables[(long long)b * a.max_blocks + pos / kBlock];
+        if (ph < 0 || ph >= a.num_blocks) continue;                        // flagged above
+        const long long off = (long long)ph * a.sb + (long long)g * a.sh + (long long)(pos % kBlock) * a.st;
+        quantise_row<In, EPL, kCodeI4>(a.v_new, ((t0 + i) * a.K + g) * D,
+                                       static_cast<uint8_t*>(a.v_cache) + off / 2,
+                                       a.v_scale + ((long long)ph * a.K + g) * kBlock + pos % kBlock, lane);
+    }
+}
+
+template <int EPL>
+const void* kc_kernel(int new_dtype) {
+    switch (new_dtype) {
+        case GQA_DTYPE_F32: return reinterpret_cast<const void*>(&append_kc_kernel<float, EPL>);
+        case GQA_DTYPE_F16: return reinterpret_cast<const void*>(&append_kc_kernel<__half, EPL>);
+        default: return reinterpret_cast<const void*>(&append_kc_kernel<__nv_bfloat16, EPL>);
+    }
+}
+
 template <int kCode>
 const void* quant_kernel(int new_dtype, bool d64) {
     switch (new_dtype) {
@@ -208,6 +328,7 @@ cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const v
     a.block_tables = block_tables;
     a.positions = positions;
     a.token_start = token_start;
+    a.k_residual = static_cast<float*>(c.k_residual);
     a.err = err;
     a.num_blocks = c.num_blocks;
     a.sb = c.stride_block;
@@ -220,10 +341,14 @@ cudaError_t launch_kv_append(const gqa_kv_cache_t& c, const void* k_new, const v
     a.max_blocks = max_blocks;
     a.es = dtype_bits(c.dtype) / 8;             // bytes per element of the copy path
     const long long warps = (long long)batch * tokens_per_seq * c.num_kv_heads;
-    const int grid = (int)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
+    int grid = (int)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
     if (grid == 0) return cudaSuccess;
     const void* fn;
-    if (c.dtype == GQA_DTYPE_I8) fn = quant_kernel<kCodeI8>(new_dtype, a.d == 64);
+    if (c.dtype == GQA_DTYPE_I4_KC) {
+        // one warp per (sequence, kv-head) instead of per row
+        fn = a.d == 64 ? kc_kernel<2>(new_dtype) : kc_kernel<4>(new_dtype);
+        grid = (int)(((long long)batch * c.num_kv_heads + kWarpsPerCta - 1) / kWarpsPerCta);
+    } else if (c.dtype == GQA_DTYPE_I8) fn = quant_kernel<kCodeI8>(new_dtype, a.d == 64);
     else if (c.dtype == GQA_DTYPE_FP8_E4M3) fn = quant_kernel<kCodeFp8>(new_dtype, a.d == 64);
     else if (c.dtype == GQA_DTYPE_I4) fn = quant_kernel<kCodeI4>(new_dtype, a.d == 64);
     else fn = reinterpret_cast<const void*>(&append_copy_kernel);

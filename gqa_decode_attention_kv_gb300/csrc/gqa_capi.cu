@@ -58,6 +58,13 @@ int check_cache(const gqa_kv_cache_t* c) {
     return GQA_OK;
 }
 
+// The appends of a GQA_DTYPE_I4_KC cache also need the residual rows.
+int check_residual(const gqa_kv_cache_t* c, int batch) {
+    if (c->dtype != GQA_DTYPE_I4_KC) return GQA_OK;
+    if (!c->k_residual || !aligned16(c->k_residual) || c->residual_rows < batch) return GQA_ERR_INVALID;
+    return GQA_OK;
+}
+
 }  // namespace
 
 bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int box_inner,
@@ -77,7 +84,7 @@ bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* bas
     const long long extent[3] = {GQA_BLOCK_SIZE, c.num_kv_heads, c.num_blocks};
     int order[3] = {0, 1, 2};
     std::stable_sort(order, order + 3, [&](int x, int y) { return stride[x] < stride[y]; });
-    const bool i4 = c.dtype == GQA_DTYPE_I4;
+    const bool i4 = dtype_bits(c.dtype) == 4;
     cuuint64_t gdim[4] = {(cuuint64_t)(i4 ? c.head_dim / 2 : c.head_dim), 0, 0, 0};
     cuuint64_t gstride[3];
     cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, 1, 1};
@@ -112,7 +119,7 @@ const char* gqa_status_string(int status) {
     }
 }
 
-int gqa_version(void) { return 200; }
+int gqa_version(void) { return 300; }
 
 int64_t gqa_kv_pool_elements(int64_t num_blocks, int32_t num_kv_heads, int32_t head_dim) {
     if (num_blocks < 0 || num_kv_heads < 0 || head_dim < 0) return -1;
@@ -138,6 +145,7 @@ int gqa_kv_append(const gqa_kv_cache_t* cache, const void* k_new, const void* v_
     } else if (new_dtype != cache->dtype) {
         return GQA_ERR_UNSUPPORTED;
     }
+    if ((st = check_residual(cache, batch)) != GQA_OK) return st;
     const cudaError_t e = launch_kv_append(*cache, k_new, v_new, new_dtype, block_tables,
                                            max_blocks_per_seq, positions, batch, T, nullptr, err_flag,
                                            static_cast<cudaStream_t>(stream));
@@ -162,6 +170,7 @@ int gqa_kv_append_varlen(const gqa_kv_cache_t* cache, const void* k_new, const v
     } else if (new_dtype != cache->dtype) {
         return GQA_ERR_UNSUPPORTED;
     }
+    if ((st = check_residual(cache, batch)) != GQA_OK) return st;
     const cudaError_t e = launch_kv_append(*cache, k_new, v_new, new_dtype, block_tables,
                                            max_blocks_per_seq, positions, batch, max_new_tokens,
                                            token_start, err_flag, static_cast<cudaStream_t>(stream));

@@ -75,7 +75,7 @@ size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int he
     int P = 0;
     for (int kind : {kKernelMma, kKernelFma}) {
         for (int dt : {GQA_DTYPE_F32, GQA_DTYPE_F16, GQA_DTYPE_BF16, GQA_DTYPE_I8, GQA_DTYPE_FP8_E4M3,
-                       GQA_DTYPE_I4}) {
+                       GQA_DTYPE_I4, GQA_DTYPE_I4_KC}) {
             for (int w : {1, nw}) {
                 Variant v{};
                 if (pick_plain(dt, kind, head_dim, w, v)) P = std::max(P, workers_of(v, batch, num_sms));

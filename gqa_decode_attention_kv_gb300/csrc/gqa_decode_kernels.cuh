@@ -122,14 +122,21 @@ struct Cfg {
     static constexpr bool kGen = kGeneral;
     static constexpr bool kI8 = std::is_same<T, int8_t>::value;
     static constexpr bool kFp8 = std::is_same<T, __nv_fp8_e4m3>::value;
-    static constexpr bool kI4 = std::is_same<T, int4x2>::value;
+    static constexpr bool kKc = std::is_same<T, int4kc>::value;   // K scales per channel
+    static constexpr bool kI4 = std::is_same<T, int4x2>::value || kKc;
     static constexpr bool kCoded = kI8 || kFp8 || kI4;   // codes with fp16 scales
     static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     static constexpr int kEs = sizeof(T);                           // bytes per copied element
     static constexpr int kRowBytes = kI4 ? D / 2 : D * kEs;          // one token's row
     static constexpr int kTile = 16 * kRowBytes;                    // one (block, head) tile
-    static constexpr int kScaleBytes = kCoded ? 64 : 0;             // 16 k + 16 v fp16 scales
-    static constexpr int kStage = ((2 * kTile + kScaleBytes + 1023) / 1024) * 1024;
+    // fp16 scales after the two tiles: 16 k + 16 v, or (KIVI-style) D k + 16 v
+    static constexpr int kScaleBytes = kKc ? 2 * D + 32 : kCoded ? 64 : 0;
+    static constexpr int kVsOff = kKc ? 2 * D : 32;                 // v scales within them
+    // 128-byte swizzled boxes for the tensor-core kernel; a 4-bit tile (64-byte
+    // rows) is read conflict-free without one.
+    static constexpr bool kSwizzle = (kKind == kKernelMma) && !kI4;
+    static constexpr int kStageAlign = kSwizzle ? 1024 : 128;      // swizzle atom / TMA box
+    static constexpr int kStage = ((2 * kTile + kScaleBytes + kStageAlign - 1) / kStageAlign) * kStageAlign;
     static constexpr int kNw = kHeadWarps;
     // The coded-cache kernels are issue-bound: the pool's bookkeeping costs
     // them more than the tail it removes (measured on int8), so they keep the
@@ -144,9 +151,6 @@ struct Cfg {
     static constexpr int kRings = kHeadWarps == 1 ? kWarps : 1;
     static constexpr int kStages =
         std::max(2, std::min(8, (kHeadWarps == 1 ? GQA_RING_BYTES_PER_WARP : GQA_SHARED_RING_BYTES) / kStage));
-    // 128-byte swizzled boxes for the tensor-core kernel; a 4-bit tile (64-byte
-    // rows) is read conflict-free without one.
-    static constexpr bool kSwizzle = (kKind == kKernelMma) && !kI4;
     static constexpr int kBoxInner = kSwizzle ? 128 / kEs : kRowBytes / kEs;   // elements per box row
     static constexpr int kNumBox = kSwizzle ? kRowBytes / 128 : 1;
     static constexpr int kBoxBytes = 16 * kBoxInner * kEs;
@@ -307,7 +311,7 @@ __device__ __forceinline__ void lds_row_as_float(uint32_t addr, float (&v)[N]) {
             v[e] = f.x;
             v[e + 1] = f.y;
         }
-    } else if constexpr (std::is_same<T, int4x2>::value) {
+    } else if constexpr (std::is_same<T, int4x2>::value || std::is_same<T, int4kc>::value) {
         // N 4-bit codes in N/2 bytes, element 2j in the low nibble
         uint32_t w;
         if constexpr (N == 4) {
@@ -414,6 +418,8 @@ struct MmaFrags {
     // int4: v[i][0..1] = 8 code bytes (dims 16r..16r+15) of token i
     uint32_t v[C::kMt][4];
     float ks_r, ks_r8, vs_r, vs_r8;   // int8 scales of tokens r and r+8
+    // KIVI-style K: the fp16 channel scales of dims 32c .. 32c+31 (8 per word)
+    uint4 kc[C::kKc ? 4 : 1];
 };
 
 // Q fragments (B operand of the score MMA) of query head g*G + r; zero for
@@ -525,13 +531,22 @@ __device__ __forceinline__ void mma_load(MmaFrags<C, D>& f, uint32_t stage, int 
     }
     if constexpr (C::kCoded) {
         const uint32_t sc = stage + 2 * C::kTile;
-        unsigned short h0, h1, h2, h3;
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h0) : "r"(sc + 2 * r));
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h1) : "r"(sc + 2 * (r + 8)));
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h2) : "r"(sc + 32 + 2 * r));
-        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h3) : "r"(sc + 32 + 2 * (r + 8)));
-        f.ks_r = __half2float(__ushort_as_half(h0));
-        f.ks_r8 = __half2float(__ushort_as_half(h1));
+        unsigned short h2, h3;
+        if constexpr (C::kKc) {
+            // lanes of one c read the same 64 bytes (a broadcast); the four c
+            // cover 256 distinct bytes
+#pragma unroll
+            for (int u = 0; u < 4; ++u) f.kc[u] = lds128(sc + 64 * c + 16 * u);
+            f.ks_r = f.ks_r8 = 1.f;
+        } else {
+            unsigned short h0, h1;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h0) : "r"(sc + 2 * r));
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h1) : "r"(sc + 2 * (r + 8)));
+            f.ks_r = __half2float(__ushort_as_half(h0));
+            f.ks_r8 = __half2float(__ushort_as_half(h1));
+        }
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h2) : "r"(sc + C::kVsOff + 2 * r));
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h3) : "r"(sc + C::kVsOff + 2 * (r + 8)));
         f.vs_r = __half2float(__ushort_as_half(h2));
         f.vs_r8 = __half2float(__ushort_as_half(h3));
     }
@@ -565,13 +580,49 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
     } else if constexpr (C::kI4) {
         // word u of tokens r / r+8: bytes 4u..4u+3 = dims 32c + 8u + 0..7;
         // lo/hi nibbles of bytes 0,2 feed k-step 2u, of bytes 1,3 k-step 2u+1
+        if constexpr (C::kKc) {
+            // The per-channel K scales fold into q: q_i * s_i has at most 22
+            // significant bits (11 x 11), so it is carried exactly as an f16
+            // high part (the rounded product) plus an f16 low part (the
+            // product minus the high part, one rounding), each with its own
+            // MMA. Scales are permuted like the q fragments: (+0, +4), (+1, +5),
+            // (+2, +6), (+3, +7).
+            float sc_[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+            constexpr uint32_t kNeg = 0x80008000u;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint32_t w = f.k[0][u], w8 = f.k[1][u];
-            mma_f16(sa, i4_lo_pair(w), i4_lo_pair(w8), i4_hi_pair(w), i4_hi_pair(w8),
-                    st.qf[2 * u].x, st.qf[2 * u].y);
-            mma_f16(sb, i4_lo_pair(w >> 8), i4_lo_pair(w8 >> 8), i4_hi_pair(w >> 8), i4_hi_pair(w8 >> 8),
-                    st.qf[2 * u + 1].x, st.qf[2 * u + 1].y);
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t w = f.k[0][u], w8 = f.k[1][u];
+                const uint4 sc = f.kc[u];
+                const uint32_t s0 = __byte_perm(sc.x, sc.z, 0x5410), s1 = __byte_perm(sc.x, sc.z, 0x7632);
+                const uint32_t s2 = __byte_perm(sc.y, sc.w, 0x5410), s3 = __byte_perm(sc.y, sc.w, 0x7632);
+                const uint32_t q0 = st.qf[2 * u].x, q1 = st.qf[2 * u].y;
+                const uint32_t q2 = st.qf[2 * u + 1].x, q3 = st.qf[2 * u + 1].y;
+                const uint32_t h0 = hmul2_u32(q0, s0), h1 = hmul2_u32(q1, s1);
+                const uint32_t h2 = hmul2_u32(q2, s2), h3 = hmul2_u32(q3, s3);
+                const uint32_t l0 = hfma2_u32(q0, s0, h0 ^ kNeg), l1 = hfma2_u32(q1, s1, h1 ^ kNeg);
+                const uint32_t l2 = hfma2_u32(q2, s2, h2 ^ kNeg), l3 = hfma2_u32(q3, s3, h3 ^ kNeg);
+                const uint32_t a0 = i4_lo_pair(w), a1 = i4_lo_pair(w8), a2 = i4_hi_pair(w), a3 = i4_hi_pair(w8);
+                const uint32_t c0 = i4_lo_pair(w >> 8), c1 = i4_lo_pair(w8 >> 8);
+                const uint32_t c2 = i4_hi_pair(w >> 8), c3 = i4_hi_pair(w8 >> 8);
+                mma_f16(sa, a0, a1, a2, a3, h0, h1);
+                mma_f16(sb, c0, c1, c2, c3, h2, h3);
+                mma_f16(sc_, a0, a1, a2, a3, l0, l1);
+                mma_f16(sd, c0, c1, c2, c3, l2, l3);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sa[e] += sc_[e];
+                sb[e] += sd[e];
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t w = f.k[0][u], w8 = f.k[1][u];
+                mma_f16(sa, i4_lo_pair(w), i4_lo_pair(w8), i4_hi_pair(w), i4_hi_pair(w8),
+                        st.qf[2 * u].x, st.qf[2 * u].y);
+                mma_f16(sb, i4_lo_pair(w >> 8), i4_lo_pair(w8 >> 8), i4_hi_pair(w >> 8), i4_hi_pair(w8 >> 8),
+                        st.qf[2 * u + 1].x, st.qf[2 * u + 1].y);
+            }
         }
     } else {
 #pragma unroll
@@ -840,16 +891,24 @@ __device__ __forceinline__ void fma_block(const DecodeArgs& a, FmaState<C, D>& s
     constexpr int kN = C::kDpl;
     const uint32_t sk = stage, sv = stage + C::kTile;
     const int G = a.GT - hbase;                  // rows of this warp: hbase .. hbase+7
+    float kcs[kN];                               // KIVI-style K: this lane's channel scales
+    if constexpr (C::kKc) lds_row_as_float<__half, kN>(stage + 2 * C::kTile + 2 * kN * lane, kcs);
     for (int t = 0; t < nvalid; ++t) {
         float kf[kN], vf[kN];
         lds_row_as_float<T, kN>(sk + t * C::kRowBytes + lane * C::kLaneBytes, kf);
         lds_row_as_float<T, kN>(sv + t * C::kRowBytes + lane * C::kLaneBytes, vf);
         float ksc = a.scale_log2, vsc = 1.f;
         if constexpr (C::kCoded) {
-            unsigned short hk, hv;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hk) : "r"(stage + 2 * C::kTile + 2 * t));
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(stage + 2 * C::kTile + 32 + 2 * t));
-            ksc *= __half2float(__ushort_as_half(hk));
+            unsigned short hv;
+            if constexpr (C::kKc) {
+#pragma unroll
+                for (int i = 0; i < kN; ++i) kf[i] *= kcs[i];          // exact: code * fp16
+            } else {
+                unsigned short hk;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hk) : "r"(stage + 2 * C::kTile + 2 * t));
+                ksc *= __half2float(__ushort_as_half(hk));
+            }
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hv) : "r"(stage + 2 * C::kTile + C::kVsOff + 2 * t));
             vsc = __half2float(__ushort_as_half(hv));
         }
 #pragma unroll
@@ -1114,8 +1173,11 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                     tma_load_4d(dst + C::kTile + x * C::kBoxBytes, &vmap, x * C::kBoxInner, y, z, ww, bar, pol);
                 if constexpr (C::kCoded) {
                     const long long si = ((long long)ph * a.K + gg) * kBlock;
-                    bulk_load(dst + 2 * C::kTile, a.k_scale + si, 32, bar, pol_keep);
-                    bulk_load(dst + 2 * C::kTile + 32, a.v_scale + si, 32, bar, pol_keep);
+                    if constexpr (C::kKc)   // whole 256-byte rows of their own: read once
+                        bulk_load(dst + 2 * C::kTile, a.k_scale + ((long long)ph * a.K + gg) * D, 2 * D, bar, pol);
+                    else
+                        bulk_load(dst + 2 * C::kTile, a.k_scale + si, 32, bar, pol_keep);
+                    bulk_load(dst + 2 * C::kTile + C::kVsOff, a.v_scale + si, 32, bar, pol_keep);
                 }
             } else {
                 meta[4 * s] = kSlotSkip;
@@ -1435,7 +1497,7 @@ bool pick_kind(int kind, int nw, Variant& v) {
     if (kind == kKernelMma) {
         if constexpr (std::is_same<T, float>::value ||
                       ((std::is_same<T, int8_t>::value || std::is_same<T, __nv_fp8_e4m3>::value ||
-                        std::is_same<T, int4x2>::value) && D != 128)) {
+                        std::is_same<T, int4x2>::value || std::is_same<T, int4kc>::value) && D != 128)) {
             return false;
         } else {
             v = pick_width<kKernelMma, T, D, kGen>(nw);
@@ -1471,6 +1533,7 @@ bool pick_variant(int dtype, int kind, int d, int nw, Variant& v) {
         case GQA_DTYPE_I8: return pick_dim<int8_t, kGen>(kind, d, nw, v);
         case GQA_DTYPE_FP8_E4M3: return pick_dim<__nv_fp8_e4m3, kGen>(kind, d, nw, v);
         case GQA_DTYPE_I4: return pick_dim<int4x2, kGen>(kind, d, nw, v);
+        case GQA_DTYPE_I4_KC: return pick_dim<int4kc, kGen>(kind, d, nw, v);
         default: return false;
     }
 }

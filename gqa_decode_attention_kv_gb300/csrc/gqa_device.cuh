@@ -254,6 +254,23 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
 struct int4x2 {
     uint8_t v;
 };
+// The same codes with K scaled per (block, kv-head, channel) (KIVI-style).
+struct int4kc {
+    uint8_t v;
+};
+
+// Lane-wise product of two f16 pairs, rounded to nearest.
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// Lane-wise a*b + c of f16 pairs with one rounding.
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 
 // d = b ? (a ^ c) : c, bit by bit (one LOP3): with b a mask and c holding the
 // bits to flip under the mask and the bits to set elsewhere.

@@ -17,15 +17,17 @@ inline int dtype_bits(int dt) {
         case GQA_DTYPE_I8: return 8;
         case GQA_DTYPE_FP8_E4M3: return 8;
         case GQA_DTYPE_I4: return 4;
+        case GQA_DTYPE_I4_KC: return 4;
         default: return 0;
     }
 }
 // Bytes of n elements of a cache dtype (n even for 4-bit elements).
 inline long long dtype_bytes(int dt, long long n) { return n * dtype_bits(dt) / 8; }
 
-// Code caches (8- or 4-bit codes) with per-(token, kv-head) fp16 scales.
+// Code caches (8- or 4-bit codes) with fp16 scales: per (token, kv-head), or
+// for the K of GQA_DTYPE_I4_KC per (block, kv-head, channel).
 inline bool dtype_coded(int dt) {
-    return dt == GQA_DTYPE_I8 || dt == GQA_DTYPE_FP8_E4M3 || dt == GQA_DTYPE_I4;
+    return dt == GQA_DTYPE_I8 || dt == GQA_DTYPE_FP8_E4M3 || dt == GQA_DTYPE_I4 || dt == GQA_DTYPE_I4_KC;
 }
 
 // Which split-KV kernel runs.

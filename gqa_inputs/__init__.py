@@ -33,9 +33,12 @@ BLOCK_SIZE = 16
 
 # dtype names shared with the C-ABI enum (gqa_dtype_t in include/gqa_decode.h)
 DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "i8": torch.int8,
-          "fp8": torch.float8_e4m3fn, "i4": torch.uint8}     # i4: two codes per byte
-DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3, "fp8": 4, "i4": 5}
-CODED = ("i8", "fp8", "i4")  # code caches with per-(token, kv-head) fp16 scales
+          "fp8": torch.float8_e4m3fn, "i4": torch.uint8, "i4kc": torch.uint8}   # i4*: two codes per byte
+DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3, "fp8": 4, "i4": 5, "i4kc": 6}
+# code caches with fp16 scales: per (token, kv-head); for the K of "i4kc"
+# (KIVI-style) per (block, kv-head, channel)
+CODED = ("i8", "fp8", "i4", "i4kc")
+PACKED4 = ("i4", "i4kc")     # two 4-bit codes per byte
 
 @dataclasses.dataclass(frozen=True)
 class Workload:
@@ -45,7 +48,7 @@ class Workload:
     num_heads: int
     num_kv_heads: int
     head_dim: int
-    cache_dtype: str            # "f32" | "f16" | "bf16" | "i8" | "fp8"
+    cache_dtype: str            # "f32" | "f16" | "bf16" | "i8" | "fp8" | "i4" | "i4kc"
     q_dtype: str                # "f32" | "f16" | "bf16"
     lens: str                   # "fixed:<a,b,...>" | "const:<S>" | "uniform:<lo>:<hi>"
     contiguous: bool = False    # un-paged [B, S_pad, K, d] buffer + identity table
@@ -76,6 +79,9 @@ WORKLOADS = {
     "fp8kv_b128_ragged": Workload("fp8kv_b128_ragged", 128, 64, 8, 128, "fp8", "bf16",
                                   "uniform:2048:8192"),
     "int4kv_b128_ragged": Workload("int4kv_b128_ragged", 128, 64, 8, 128, "i4", "bf16",
+                                   "uniform:2048:8192"),
+    # KIVI-style 4-bit cache (K per channel, V per token), same shape
+    "int4kc_b128_ragged": Workload("int4kc_b128_ragged", 128, 64, 8, 128, "i4kc", "bf16",
                                    "uniform:2048:8192"),
     # four new tokens per sequence (speculative verification of three drafts),
     # Llama-3-8B shape; the lengths include the new tokens
@@ -129,7 +135,7 @@ class DecodeCase:
     q: torch.Tensor                 # [B, H, d] q_dtype ([B, T, H, d] for T > 1 queries)
     k_cache: torch.Tensor           # pool or contiguous buffer, cache dtype
     v_cache: torch.Tensor
-    k_scale: Optional[torch.Tensor]  # [num_blocks, K, 16] fp16 (int8 caches only)
+    k_scale: Optional[torch.Tensor]  # [num_blocks, K, 16] fp16 (code caches; [num_blocks, K, d] for i4kc)
     v_scale: Optional[torch.Tensor]
     num_blocks: int
     stride_block: int               # element strides of the cache description
@@ -140,6 +146,7 @@ class DecodeCase:
     k_new: torch.Tensor             # [B, K, d] new token(s) (input dtype of append; [B, T, K, d])
     v_new: torch.Tensor
     queries: int = 1                # T new tokens per sequence
+    k_residual: Optional[torch.Tensor] = None   # i4kc: fp32 [B, K, 16, d], unquantised K of the open block
 
     @property
     def max_blocks(self) -> int:
@@ -168,7 +175,12 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
     codes of N(0, 128^2) draws clipped to +-448 with fp16 scales in
     [0.006, 0.010]; int4 caches hold uniform codes in [-7, 7], two per byte
     (the row's last dim is d/2), with fp16 scales in [0.35, 0.50] (amax/7 of
-    128 N(0,1) draws)."""
+    128 N(0,1) draws); "i4kc" caches hold the same codes with K scales per
+    (block, kv-head, channel) and V scales per (token, kv-head), both in
+    [0.35, 0.50], and an fp32 residual [B, K, 16, d] of N(0,1) draws standing
+    for the unquantised K of each sequence's open block (drawn independently
+    of that block's codes: decode reads only codes and scales, an append
+    re-quantises the block from the residual)."""
     if q_dtype is None:
         q_dtype = "bf16" if cache_dtype in CODED else cache_dtype
     if new_dtype is None:
@@ -211,7 +223,7 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
         sshape = (num_blocks, K, bs)
         ks = (torch.rand(sshape, generator=gen_dev, device=dev) * 0.02 + 0.015).to(torch.float16)
         vs = (torch.rand(sshape, generator=gen_dev, device=dev) * 0.02 + 0.015).to(torch.float16)
-    elif cache_dtype == "i4":
+    elif cache_dtype in PACKED4:
         pshape = shape[:-1] + (d // 2,)
         def packed():
             lo = torch.randint(-7, 8, pshape, generator=gen_dev, device=dev, dtype=torch.int32)
@@ -219,7 +231,8 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
             return ((lo & 0xF) | ((hi & 0xF) << 4)).to(torch.uint8)
         kc, vc = packed(), packed()
         sshape = (num_blocks, K, bs)
-        ks = (torch.rand(sshape, generator=gen_dev, device=dev) * 0.15 + 0.35).to(torch.float16)
+        kshape = (num_blocks, K, d) if cache_dtype == "i4kc" else sshape
+        ks = (torch.rand(kshape, generator=gen_dev, device=dev) * 0.15 + 0.35).to(torch.float16)
         vs = (torch.rand(sshape, generator=gen_dev, device=dev) * 0.15 + 0.35).to(torch.float16)
     elif cache_dtype == "fp8":
         def codes():
@@ -244,9 +257,10 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
         q.zero_()
     k_new = _randn((batch, *tq, K, d), gen_dev, dev, DTYPES[new_dtype])
     v_new = _randn((batch, *tq, K, d), gen_dev, dev, DTYPES[new_dtype])
+    res = _randn((batch, K, bs, d), gen_dev, dev, torch.float32) if cache_dtype == "i4kc" else None
     return DecodeCase(batch, num_heads, K, d, cache_dtype, q_dtype, 1.0 / math.sqrt(d),
                       q, kc, vc, ks, vs, num_blocks, sb, sh, st, table.to(dev),
-                      lens_t.to(dev), k_new, v_new, queries)
+                      lens_t.to(dev), k_new, v_new, queries, res)
 
 
 def _poison_unowned(kc, vc, ks, vs, table, lens, contiguous, cache_dtype):
@@ -270,9 +284,12 @@ def _poison_unowned(kc, vc, ks, vs, table, lens, contiguous, cache_dtype):
     else:
         mask = bad[:, None, :, None].expand_as(kc)
     if cache_dtype in CODED:
-        smask = bad[:, None, :].expand_as(ks)
-        ks.masked_fill_(smask, float("nan"))
+        smask = bad[:, None, :].expand_as(vs)
         vs.masked_fill_(smask, float("nan"))
+        if cache_dtype == "i4kc":      # channel scales: of blocks holding no valid token
+            ks.masked_fill_(bad.all(dim=1)[:, None, None].to(ks.device).expand_as(ks), float("nan"))
+        else:
+            ks.masked_fill_(smask, float("nan"))
     else:
         kc.masked_fill_(mask, float("nan"))
         vc.masked_fill_(mask, float("nan"))

@@ -49,8 +49,10 @@ typedef enum {
     GQA_DTYPE_BF16 = 2,
     GQA_DTYPE_I8 = 3,         /* cache only: int8 codes + one fp16 scale per (token, kv-head) */
     GQA_DTYPE_FP8_E4M3 = 4,   /* cache only: e4m3 codes (max 448) + one fp16 scale per (token, kv-head) */
-    GQA_DTYPE_I4 = 5          /* cache only: 4-bit codes in [-7, 7], two per byte + one fp16 scale
+    GQA_DTYPE_I4 = 5,         /* cache only: 4-bit codes in [-7, 7], two per byte + one fp16 scale
                                  per (token, kv-head) */
+    GQA_DTYPE_I4_KC = 6       /* cache only: 4-bit codes as GQA_DTYPE_I4; K with one fp16 scale per
+                                 (block, kv-head, channel), V with one per (token, kv-head) */
 } gqa_dtype_t;
 
 /* Return codes. */
@@ -88,6 +90,20 @@ typedef enum {
  * the low nibble, each a two's-complement 4-bit code; strides still count
  * elements (byte offset = element offset / 2).
  *
+ * GQA_DTYPE_I4_KC is the KIVI-style cache ("LLM 推理性能优化实战" section 15.5:
+ * K quantised per channel, V per token, both to INT4). V is stored as for
+ * GQA_DTYPE_I4. K keeps one fp16 scale per channel for each (block, kv-head):
+ * k_scale is [num_blocks, K, head_dim], and the cached K of slot t, channel i
+ * is code[t][i] * k_scale[p][g][i]. The scales of a block cover the tokens it
+ * holds: the append re-quantises a block, per channel, over all its tokens
+ * each time tokens join it (symmetric: s_i = fp16(max_t |k[t][i]| / 7),
+ * code = clamp(rint(k / s_i), -7, 7)). To do so without compounding rounding
+ * it keeps the unquantised K of every sequence's unfinished block in
+ * k_residual: fp32 [residual_rows, K, 16, head_dim], row b serving the
+ * sequence an append call passes as batch row b (a caller that moves a
+ * sequence to another row moves its residual row with it). Only the appends
+ * read or write k_residual; decode reads codes and scales alone.
+ *
  * Requirements: block_size == 16; head_dim in {64, 128}; k, v, k_scale,
  * v_scale 16-byte aligned; every stride times the element size a multiple of
  * 16 bytes; stride_token >= head_dim.
@@ -105,6 +121,9 @@ typedef struct {
     int64_t stride_block;     /* elements */
     int64_t stride_head;      /* elements */
     int64_t stride_token;     /* elements */
+    void   *k_residual;       /* device, fp32 [residual_rows, K, 16, d], GQA_DTYPE_I4_KC only */
+    int32_t residual_rows;    /* rows of k_residual (>= the batch of every append) */
+    int32_t reserved;         /* zero */
 } gqa_kv_cache_t;
 
 /*
@@ -171,6 +190,14 @@ GQA_API int64_t gqa_kv_pool_elements(int64_t num_blocks, int32_t num_kv_heads, i
  *                 s = fp16_rne(min(amax/448, 65504)) and code = e4m3 of x/s,
  *                 rounded to nearest even and saturated to +-448 (the FP8 option
  *                 of section 15.5). The scale goes to k_scale / v_scale.
+ *                 For an I4_KC cache V is quantised as for I4, and every block
+ *                 the new tokens reach is re-quantised per channel over all
+ *                 the tokens it then holds (codes of its older slots included),
+ *                 the older tokens' K read from k_residual row b; the new
+ *                 tokens' K of a block left unfinished is kept there.
+ *                 k_residual must be non-NULL, 16-byte aligned, with
+ *                 residual_rows >= batch; sequences of one call must not
+ *                 share a block.
  *  block_tables   device int32 [batch, max_blocks_per_seq].
  *  positions      device int32 [batch]: position of the first new token, i.e.
  *                 the context length BEFORE the append. Not modified; the

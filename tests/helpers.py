@@ -28,16 +28,22 @@ def oracle_for_case(case, rows=None, nthreads: int = 0, host_pools=None, window:
     rows = list(range(case.batch)) if rows is None else list(rows)
     kp, vp = host_pools if host_pools is not None else (_host(case.k_cache), _host(case.v_cache))
     K, d = case.num_kv_heads, case.head_dim
-    if case.cache_dtype == "i4":
+    if case.cache_dtype in ("i4", "i4kc"):
         # bytes: element strides halve, a row is d/2 bytes
         kb = oracle.gather_dense(kp, table, lens, case.stride_block // 2, case.stride_head // 2,
                                  case.stride_token // 2, K, d // 2, rows)
         vb = oracle.gather_dense(vp, table, lens, case.stride_block // 2, case.stride_head // 2,
                                  case.stride_token // 2, K, d // 2, rows)
-        ks = oracle.gather_scales(case.k_scale.float().cpu().numpy(), table, lens, K, rows)
         vs = oracle.gather_scales(case.v_scale.float().cpu().numpy(), table, lens, K, rows)
+        if case.cache_dtype == "i4kc":     # K: code * its block's channel scale
+            kcs = oracle.gather_channel_scales(case.k_scale.float().cpu().numpy().astype(np.float64),
+                                               table, lens, rows)
+            kd = oracle.unpack_int4(kb).astype(np.float64) * kcs
+        else:
+            ks = oracle.gather_scales(case.k_scale.float().cpu().numpy(), table, lens, K, rows)
+            kd = oracle.dequantize_int4(kb, ks)
         q = case.q.detach().float().cpu().numpy().astype(np.float64)[rows]
-        return oracle.decode(q, oracle.dequantize_int4(kb, ks), oracle.dequantize_int4(vb, vs),
+        return oracle.decode(q, kd, oracle.dequantize_int4(vb, vs),
                              lens[rows], case.scale, nthreads, window=window)
     kd = oracle.gather_dense(kp, table, lens, case.stride_block, case.stride_head,
                              case.stride_token, K, d, rows).astype(np.float64)

@@ -123,6 +123,21 @@ def test_append_argument_checks(lib):
     assert f(ctypes.byref(i8), 0x1000, 0x2000, 3, 0x3000, 8, 0x4000, 4, 1, None, None) == UNSUPPORTED
 
 
+def test_kivi_cache_appends_need_the_residual(lib):
+    """GQA_DTYPE_I4_KC: appends read and write k_residual (one row per batch
+    row); a missing, misaligned or too short residual is refused before any
+    launch, by both append entry points."""
+    base = dict(dtype=6, k_scale=0x80000, v_scale=0x90000)
+    f, fv = lib.gqa_kv_append, lib.gqa_kv_append_varlen
+    for kw in (dict(), dict(k_residual=0xA0008, residual_rows=4), dict(k_residual=0xA0000, residual_rows=3)):
+        d = _desc(**base, **kw)
+        assert f(ctypes.byref(d), 0x1000, 0x2000, 2, 0x3000, 8, 0x4000, 4, 1, None, None) == INVALID
+        assert fv(ctypes.byref(d), 0x1000, 0x2000, 2, 0x5000, 3, 0x3000, 8, 0x4000, 4, None, None) == INVALID
+    # an empty batch needs no residual
+    d = _desc(**base)
+    assert f(ctypes.byref(d), 0x1000, 0x2000, 2, 0x3000, 8, 0x4000, 0, 1, None, None) == OK
+
+
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gq, "_lib", None)
     monkeypatch.setattr(gbuild, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -321,6 +321,7 @@ def _host_pools(case):
     ("int8kv_b128_ragged", [0, 64, 127]),
     ("fp8kv_b128_ragged", [0, 77, 127]),
     ("int4kv_b128_ragged", [0, 100, 127]),
+    ("int4kc_b128_ragged", [0, 50, 127]),
     ("spec_verify_bf16_b64_s4096_t4", [0, 40, 63]),
     ("mistral7b_swa_bf16_b64_s16384_w4096", [0, 63]),
 ])
