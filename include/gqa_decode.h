@@ -204,7 +204,9 @@ GQA_API int64_t gqa_kv_pool_elements(int64_t num_blocks, int32_t num_kv_heads, i
  *                 caller advances its context lengths by T.
  *  tokens_per_seq T >= 1 (0 means 1).
  *  err_flag       device int32 or NULL (GQA_DEVERR_POSITION / _BLOCK_INDEX).
- *                 A token whose position or block is out of range is skipped.
+ *                 A token whose position or block is out of range is skipped
+ *                 (for an I4_KC cache: an out-of-range position skips the
+ *                 sequence's whole append, an out-of-range block that block).
  */
 GQA_API int gqa_kv_append(const gqa_kv_cache_t *cache, const void *k_new, const void *v_new,
                   int32_t new_dtype, const int32_t *block_tables,
