@@ -340,3 +340,37 @@ def test_kv_head_sweep_sampled(gq, kv_heads):
     import dataclasses
     wl = dataclasses.replace(gi.kv_sweep_workload(kv_heads), batch=6)
     assert _sampled(gq, wl, [1, 5]) <= TOL
+
+
+def test_step_replays_from_a_cuda_graph(gq):
+    """append + decode captured in a CUDA graph (the kernels keep their
+    programmatic-launch edges) replays to the eager result bit for bit."""
+    lens = [100, 4000, 17, 1]
+    case = gi.make_case(len(lens), 32, 8, 128, lens, "bf16", seed=41, device="cuda", extra_tokens=1)
+    cache = gq.cache_from_case(case)
+    pos = case.context_lens.clone()
+    after = case.context_lens + 1
+    out = torch.empty(case.q.shape, dtype=torch.float32, device="cuda")
+    ws = gq.workspace_for(len(lens), 32, 8, 128, torch.device("cuda"), 1)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step():
+        gq.kv_append(cache, case.k_new, case.v_new, case.block_table, pos, err=err)
+        gq.gqa_decode(cache, case.q, case.block_table, after, case.scale, out=out, workspace=ws, err=err)
+
+    step()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            for _ in range(3):
+                step()
+    torch.cuda.current_stream().wait_stream(s)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(out, eager)
