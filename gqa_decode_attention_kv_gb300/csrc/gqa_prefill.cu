@@ -342,15 +342,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 //   O[128 x d]  += P_hi V + P_lo V          A = P from tensor memory, B = the
 //                                            V tiles read MN-major
 // Warp roles: warps 0-3 own the 128 rows (softmax, epilogue); warp 4 issues
-// every TMA copy and every MMA. They meet only on mbarriers: tcgen05.commit
-// -> "S(c) done", each softmax warp -> "P(c) ready", TMA -> "K/V stage full",
-// and a per-slot barrier that publishes which blocks of a chunk exist. K and V
-// have two shared stages each; K(c+2) and V(c+1) load as soon as S(c) lands,
-// a chunk ahead of their use. Two CTAs share an SM (~97 KB of shared memory
-// and 256 tensor-memory columns each).
+// every MMA; warp 5 issues every TMA copy (a chunk's 16 page boxes take the
+// copy engine ~1.5 us, which kept the MMAs waiting while one warp did both).
+// They meet only on mbarriers: tcgen05.commit -> "S(c) done" (two barriers,
+// alternating by chunk, so that no waiter can fall two phases behind one),
+// each softmax warp -> "P(c) ready", TMA -> "K/V stage full", and a per-slot
+// barrier that publishes which blocks of a chunk exist. K and V have two
+// shared stages each; K(c+2) and V(c+1) load as soon as S(c) lands, a chunk
+// ahead of their use. Two CTAs share an SM (~97 KB of shared memory and 256
+// tensor-memory columns each).
 
 constexpr int kTcRows = 128;                 // query rows per CTA = M = TMEM lanes
-constexpr int kTcThreads = kTcRows + 32;     // + the producer warp
+constexpr int kTcThreads = kTcRows + 64;     // + the MMA warp and the copy warp
 constexpr int kTcChunk = 64;                 // KV tokens per step = N of S = K of P.V
 constexpr int kTcBlocks = kTcChunk / kBlock;
 constexpr uint32_t kTmemCols = 256;
@@ -394,18 +397,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const uint32_t sb = (raw + 1023u) & ~1023u;
     uint8_t* gb = smem_raw + (sb - raw);
     const uint32_t sQ = sb, sK = sb + C::kOffK, sV = sb + C::kOffV;
-    // barriers (8 B each): K stage 0/1, V stage 0/1, S done, P ready, mask slot 0..3;
-    // then the TMEM address and the 4 block masks
+    // barriers (8 B each): K stage 0/1, V stage 0/1, "S(c) done" for even / odd c,
+    // P ready, mask slot 0..3; then the TMEM address and the 4 block masks
     const uint32_t bar0 = sb + C::kOffBar;
-    const uint32_t bar_s = bar0 + 32, bar_p = bar0 + 40, tslot = bar0 + 80;
-    volatile uint32_t* cmask = reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 96);   // [4]
+    const uint32_t bar_p = bar0 + 48, tslot = bar0 + 88;
+    volatile uint32_t* cmask = reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 92);   // [4]
     auto bar_k = [&](int c) { return bar0 + 8 * (c & 1); };
     auto bar_v = [&](int c) { return bar0 + 16 + 8 * (c & 1); };
-    auto bar_m = [&](int c) { return bar0 + 48 + 8 * (c & 3); };
+    // phase c of "S(c) done, with P(c-1).V(c-1)" = completion c >> 1 of bar_s(c)
+    auto bar_s = [&](int c) { return bar0 + 32 + 8 * (c & 1); };
+    auto bar_m = [&](int c) { return bar0 + 56 + 8 * (c & 3); };
     auto par2 = [](int c) { return (uint32_t)(c >> 1) & 1u; };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool producer = warp == 4;
+    const bool softmax = warp < 4, mma_warp = warp == 4, loader = warp == 5;
     const int tile = a.tiles_per_seq - 1 - (int)blockIdx.x;    // heaviest first
     const int g = blockIdx.y, b = blockIdx.z;
     if (tid == 0) {
@@ -433,15 +438,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const int nchunks = (jb_hi - jb_lo + kTcBlocks - 1) / kTcBlocks;
 
     // ---- this thread's row (softmax warps) and the positions it attends, [lo, hi)
-    const int rr = row0 + (producer ? 0 : tid);
-    const bool live = !producer && rr < rows;
+    const int rr = row0 + (softmax ? tid : 0);
+    const bool live = softmax && rr < rows;
     const int tk = live ? rr / a.G : 0;
     const int hh = rr - tk * a.G;
     const int hi = live ? base_pos + tk + 1 : 0;
     const int lo = a.window > 0 ? hi - a.window : 0;
     const long long qrow = ((long long)(q0 + tk) * a.H + (long long)g * a.G + hh) * D;
 
-    if (!producer) {                           // Q row into the swizzled K-major tile
+    if (softmax) {                             // Q row into the swizzled K-major tile
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + qrow);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
@@ -450,9 +455,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
     }
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(bar0 + 8 * i, 1);
+        for (int i = 0; i < 6; ++i) mbar_init(bar0 + 8 * i, 1);        // K, V stages; S done x2
         mbar_init(bar_p, 4);                   // one arrival per softmax warp
-        for (int i = 0; i < 4; ++i) mbar_init(bar0 + 48 + 8 * i, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bar_m(i), 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tslot, kTmemCols);
@@ -460,14 +465,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 80);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + (tslot - sb));
     bool ok = true;
 
-    if (producer) {
-        // ================================================== producer warp
+    if (loader) {
+        // ================================================== copy warp
         const uint64_t pol = l2_policy_evict_last();   // every query tile of the sequence re-reads them
         int win_base = -(1 << 30), win_phys = -1;
-        int k_issued = 0, v_issued = 0, s_committed = 0;
+        int k_issued = 0, v_issued = 0;
         auto issue_kv = [&](int c, bool is_k) {
             int ph[kTcBlocks];
 #pragma unroll
@@ -520,6 +525,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             if (is_k) ++k_issued;
             else ++v_issued;
         };
+        issue_kv(0, true);
+        if (nchunks > 1) issue_kv(1, true);
+        issue_kv(0, false);
+        for (int c = 0; c + 1 < nchunks && ok; ++c) {
+            // S(c) done, and P(c-1).V(c-1) before it: K(c)'s stage takes K(c+2),
+            // V(c-1)'s stage takes V(c+1)
+            ok = __all_sync(kFull, mbar_wait(bar_s(c), par2(c)));
+            if (!ok) break;
+            if (c + 2 < nchunks) issue_kv(c + 2, true);
+            issue_kv(c + 1, false);
+        }
+        if (!ok && lane == 0) {
+            // let this CTA's copies land before the shared memory goes
+            flag_error(a.err, GQA_DEVERR_TIMEOUT);
+            for (int c = max(0, k_issued - 2); c < k_issued; ++c) mbar_wait(bar_k(c), par2(c), kWaitLimitNs / 4);
+            for (int c = max(0, v_issued - 2); c < v_issued; ++c) mbar_wait(bar_v(c), par2(c), kWaitLimitNs / 4);
+        }
+    } else if (mma_warp) {
+        // ================================================== MMA warp
         auto issue_s = [&](int c) {            // S = Q K(c)^T into columns [0, 64)
             const uint32_t kb = sK + (c & 1) * C::kKc;
 #pragma unroll
@@ -529,23 +553,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 tc_mma_f16(tmem + kColS, ad, bd, C::kIdescS, ks > 0);
             }
         };
-        issue_kv(0, true);
-        if (nchunks > 1) issue_kv(1, true);
-        issue_kv(0, false);
+        int s_committed = 0;
         if (lane == 0) {
             ok = mbar_wait(bar_k(0), par2(0));
             tc_fence_after();
             if (ok) issue_s(0);
-            tc_commit(bar_s);
+            tc_commit(bar_s(0));               // phase 0: S(0) done
         }
         s_committed = 1;
         ok = __shfl_sync(kFull, ok, 0);
         for (int c = 0; c < nchunks && ok; ++c) {
-            // S(c) done: its K stage and (via P(c-1).V(c-1) before it) the other V stage are free
-            ok = __all_sync(kFull, mbar_wait(bar_s, (uint32_t)c & 1u));
-            if (!ok) break;
-            if (c + 2 < nchunks) issue_kv(c + 2, true);
-            if (c + 1 < nchunks) issue_kv(c + 1, false);
             // P(c) written, S(c) read, V(c) rows zeroed by the softmax warps
             ok = __all_sync(kFull, mbar_wait(bar_p, (uint32_t)c & 1u));
             if (!ok) break;
@@ -568,20 +585,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                         if (w) issue_s(c + 1);
                     }
                 }
-                tc_commit(bar_s);              // phase c+1: P(c).V(c) (and S(c+1)) done
+                tc_commit(bar_s(c + 1));       // phase c+1: P(c).V(c) (and S(c+1)) done
                 ok = w;
             }
             ok = __shfl_sync(kFull, ok, 0);
             s_committed = c + 2;
         }
-        if (!ok) {
-            // let this CTA's copies and MMAs land before the tensor memory goes
-            if (lane == 0) {
-                flag_error(a.err, GQA_DEVERR_TIMEOUT);
-                mbar_wait(bar_s, (uint32_t)(s_committed - 1) & 1u, kWaitLimitNs / 4);
-                for (int c = max(0, k_issued - 2); c < k_issued; ++c) mbar_wait(bar_k(c), par2(c), kWaitLimitNs / 4);
-                for (int c = max(0, v_issued - 2); c < v_issued; ++c) mbar_wait(bar_v(c), par2(c), kWaitLimitNs / 4);
-            }
+        if (!ok && lane == 0) {
+            // let this CTA's MMAs land before the tensor memory goes: the last
+            // phases in order (a parity wait cannot tell a phase from the one
+            // two before it)
+            flag_error(a.err, GQA_DEVERR_TIMEOUT);
+            for (int k = max(0, s_committed - 4); k < s_committed; ++k)
+                mbar_wait(bar_s(k), par2(k), kWaitLimitNs / 4);
         }
     } else {
         // ================================================== softmax warps: one row per thread
@@ -589,7 +605,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         float m = -INFINITY, l = 0.f;
         int c = 0;
         for (; c < nchunks; ++c) {
-            ok = __all_sync(kFull, mbar_wait(bar_s, (uint32_t)c & 1u));   // S(c), earlier MMAs done
+            ok = __all_sync(kFull, mbar_wait(bar_s(c), par2(c)));   // S(c), earlier MMAs done
             ok = ok && __all_sync(kFull, mbar_wait(bar_m(c), (uint32_t)(c >> 2) & 1u));
             if (!ok) break;
             tc_fence_after();
@@ -681,7 +697,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             if (!ok) break;
         }
         // ---- wait for the last MMAs, then normalise and store this row
-        if (ok) ok = __all_sync(kFull, mbar_wait(bar_s, (uint32_t)nchunks & 1u));
+        if (ok) ok = __all_sync(kFull, mbar_wait(bar_s(nchunks), par2(nchunks)));   // the last P.V
         tc_fence_after();
         if (ok) {
             const float inv = l > 0.f ? 1.f / l : 0.f;
