@@ -74,6 +74,19 @@ __device__ __forceinline__ void store2(void* out, int dt, long long idx, float x
     }
 }
 
+// Four consecutive outputs of a row.
+__device__ __forceinline__ void store4(void* out, int dt, long long idx, float4 v) {
+    if (dt == GQA_DTYPE_F32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = v;
+    } else if (dt == GQA_DTYPE_BF16) {
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + idx) =
+            make_uint2(pack2<true>(v.x, v.y), pack2<true>(v.z, v.w));
+    } else {
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + idx) =
+            make_uint2(pack2<false>(v.x, v.y), pack2<false>(v.z, v.w));
+    }
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kPfWarps * 32)
 prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -372,6 +385,7 @@ struct TcCfg {
     static constexpr int kVc = kTcBlocks * kVb;                 // V chunk
     static constexpr int kOffK = kQ, kOffV = kOffK + 2 * kKc, kOffBar = kOffV + 2 * kVc;
     static constexpr int kSmem = 1024 + kOffBar + 128;
+    static_assert(4 * 32 * (D + 4) * 4 <= kOffBar, "the epilogue stages 4 warps x 32 padded rows below the barriers");
     static constexpr uint32_t kIdescS = mma_idesc_f16(kTcRows, kTcChunk, kBf16, false, false);
     static constexpr uint32_t kIdescO = mma_idesc_f16(kTcRows, D, kBf16, false, true);
 };
@@ -700,17 +714,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (ok) ok = __all_sync(kFull, mbar_wait(bar_s(nchunks), par2(nchunks)));   // the last P.V
         tc_fence_after();
         if (ok) {
+            // This warp's 32 rows leave through shared memory (Q and the K/V
+            // stages are idle now: every copy has landed and every MMA is done),
+            // so that each store writes whole rows: one lane per 4 dims of a row.
             const float inv = l > 0.f ? 1.f / l : 0.f;
+            constexpr int kRowF = D + 4;       // padded row: 16-byte stores stay conflict-free
+            float* stage = reinterpret_cast<float*>(gb) + warp * 32 * kRowF;
 #pragma unroll
             for (int q = 0; q < D / 16; ++q) {
                 uint32_t r16[16];
                 tmem_ld16(t_lane + kColO + 16 * q, r16);
                 tmem_wait_ld();
-                if (live) {
 #pragma unroll
-                    for (int j = 0; j < 16; j += 2)
-                        store2(a.out, a.out_dtype, qrow + 16 * q + j, __uint_as_float(r16[j]) * inv,
-                               __uint_as_float(r16[j + 1]) * inv);
+                for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4*>(stage + lane * kRowF + 16 * q + j) =
+                        make_float4(__uint_as_float(r16[j]) * inv, __uint_as_float(r16[j + 1]) * inv,
+                                    __uint_as_float(r16[j + 2]) * inv, __uint_as_float(r16[j + 3]) * inv);
+            }
+            __syncwarp();
+            for (int r = 0; r < 32; ++r) {
+                const int rw = row0 + 32 * warp + r;
+                if (rw >= rows) break;
+                if (4 * lane < D) {
+                    const int tkr = rw / a.G, hr = rw - tkr * a.G;
+                    const long long orow = ((long long)(q0 + tkr) * a.H + (long long)g * a.G + hr) * D;
+                    store4(a.out, a.out_dtype, orow + 4 * lane,
+                           *reinterpret_cast<const float4*>(stage + r * kRowF + 4 * lane));
                 }
             }
         } else if (lane == 0) {
