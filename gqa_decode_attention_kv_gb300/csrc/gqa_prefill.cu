@@ -455,17 +455,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const int rr = row0 + (softmax ? tid : 0);
     const bool live = softmax && rr < rows;
     const int tk = live ? rr / a.G : 0;
-    const int hh = rr - tk * a.G;
     const int hi = live ? base_pos + tk + 1 : 0;
     const int lo = a.window > 0 ? hi - a.window : 0;
-    const long long qrow = ((long long)(q0 + tk) * a.H + (long long)g * a.G + hh) * D;
 
-    if (softmax) {                             // Q row into the swizzled K-major tile
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + qrow);
+    if (softmax) {
+        // This warp's 32 Q rows into the swizzled K-major tile, loaded whole
+        // rows at a time (D/8 lanes per row, 16 bytes each; rows past the
+        // prompt are zero).
+        constexpr int kLanesPerRow = D / 8, kRowsPerStep = 32 / kLanesPerRow, kSteps = 32 / kRowsPerStep;
+        const int c = lane % kLanesPerRow;
+        const int rl0 = 32 * warp + lane / kLanesPerRow;               // first row of this lane
+        int tq = (row0 + rl0) / a.G, hq = (row0 + rl0) - tq * a.G;      // its token and head
+        uint4 v[kSteps];
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-            sts128(sQ + (c >> 3) * (kTcRows * 128) + tid * 128 + (((c & 7) ^ (tid & 7)) << 4), v);
+        for (int i = 0; i < kSteps; ++i) {          // every load in flight before any store
+            const int rq = row0 + rl0 + i * kRowsPerStep;
+            v[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (rq < rows) {
+                const long long src = ((long long)(q0 + tq) * a.H + (long long)g * a.G + hq) * D;
+                v[i] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + src) + c);
+            }
+            hq += kRowsPerStep;                     // next row: kRowsPerStep heads on
+            while (hq >= a.G) {
+                hq -= a.G;
+                ++tq;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kSteps; ++i) {
+            const int rl = rl0 + i * kRowsPerStep;
+            sts128(sQ + (c >> 3) * (kTcRows * 128) + rl * 128 + (((c & 7) ^ (rl & 7)) << 4), v[i]);
         }
     }
     if (tid == 0) {
