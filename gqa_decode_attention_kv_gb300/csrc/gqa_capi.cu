@@ -102,6 +102,32 @@ bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* bas
     return r == CUDA_SUCCESS;
 }
 
+// Whole 16-token pages of 128-element 16-bit rows in one box: dims (64
+// elements, 16 slots, 2 row halves, then the kv-head and block axes by
+// stride), box (64, 16, 2, 1, 1), 128-byte swizzle, so that a page lands as
+// [half][slot][128 B]. perm[i] names dim 3 + i: 1 kv-head, 2 block.
+bool encode_page_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int perm[2]) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc || c.head_dim != 128 || dtype_bits(c.dtype) != 16) return false;
+    const CUtensorMapDataType dt =
+        c.dtype == GQA_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const long long stride[2] = {c.stride_head, c.stride_block};
+    const long long extent[2] = {c.num_kv_heads, c.num_blocks};
+    const int o0 = stride[0] <= stride[1] ? 0 : 1, o1 = 1 - o0;
+    cuuint64_t gdim[5] = {64, GQA_BLOCK_SIZE, 2, (cuuint64_t)extent[o0], (cuuint64_t)extent[o1]};
+    cuuint64_t gstride[4] = {(cuuint64_t)dtype_bytes(c.dtype, c.stride_token), 128,
+                             (cuuint64_t)dtype_bytes(c.dtype, stride[o0]),
+                             (cuuint64_t)dtype_bytes(c.dtype, stride[o1])};
+    cuuint32_t box[5] = {64, GQA_BLOCK_SIZE, 2, 1, 1};
+    cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    perm[0] = o0 + 1;
+    perm[1] = o1 + 1;
+    const CUresult r = enc(map, dt, 5, const_cast<void*>(base), gdim, gstride, box, estride,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace gqa
 
 using namespace gqa;

@@ -25,7 +25,20 @@
 
 namespace gqa {
 
+// In gqa_capi.cu: a tensor map whose box is a whole 16-token page of 128-element
+// rows, laid out [half][slot][128 B] (perm: dims 3 and 4 -> 1 kv-head, 2 block).
+bool encode_page_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int perm[2]);
+
 namespace {
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            int w, int v, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(bar), "l"(policy)
+        : "memory");
+}
 
 constexpr int kPfWarps = 4;                  // warps per CTA, 16 query rows each
 constexpr int kPfRows = 16 * kPfWarps;       // query rows per tile
@@ -42,6 +55,7 @@ struct PrefillArgs {
     long long num_blocks;
     int B, H, K, G, max_blocks, out_dtype, tiles_per_seq, max_new, window;
     int map_perm[3];
+    int page_perm[2];           // tcgen05 kernel, d = 128: dims 3, 4 of the V page map
     float scale_log2;
 };
 
@@ -540,7 +554,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             fence_proxy_async_smem();          // earlier generic writes to the stage come first
             __syncwarp();
             // one lane per (block, half) box
-            if (lane < kTcBlocks * C::kHalves) {
+            if (!is_k && C::kHalves == 2) {
+                // V: one box per page (the page map lands it as [half][slot][128 B])
+                if (lane < kTcBlocks) {
+                    int pq = ph[0];
+#pragma unroll
+                    for (int i = 1; i < kTcBlocks; ++i)
+                        if (lane == i) pq = ph[i];
+                    if (pq >= 0) {
+                        auto coord = [&](int which) { return which == 1 ? g : pq; };
+                        tma_load_5d(sV + (c & 1) * C::kVc + lane * C::kVb, &vmap, 0, 0, 0,
+                                    coord(a.page_perm[0]), coord(a.page_perm[1]), bar, pol);
+                    }
+                }
+            } else if (lane < kTcBlocks * C::kHalves) {
                 const int q = lane / C::kHalves, h = lane % C::kHalves;
                 int pq = ph[0];
 #pragma unroll
@@ -812,6 +839,9 @@ int launch_prefill(const PrefillLaunch& L) {
     int perm[3];
     if (!encode_cache_map(&kmap, c, c.k, 64, true, perm) || !encode_cache_map(&vmap, c, c.v, 64, true, perm))
         return GQA_ERR_UNSUPPORTED;
+    int page_perm[2] = {1, 2};
+    if (tc && D == 128 && !encode_page_map(&vmap, c, c.v, page_perm))   // V a page per box
+        return GQA_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return GQA_ERR_CUDA;
 
@@ -835,6 +865,8 @@ int launch_prefill(const PrefillLaunch& L) {
     a.map_perm[0] = perm[0];
     a.map_perm[1] = perm[1];
     a.map_perm[2] = perm[2];
+    a.page_perm[0] = page_perm[0];
+    a.page_perm[1] = page_perm[1];
     a.scale_log2 = L.scale * kLog2eP;
     if (a.tiles_per_seq == 0) return GQA_OK;
 
