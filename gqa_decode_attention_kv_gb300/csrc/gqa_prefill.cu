@@ -371,21 +371,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 // Warp roles: warps 0-3 own the 128 rows (softmax, epilogue); warp 4 issues
 // every MMA; warp 5 issues every TMA copy (a chunk's 16 page boxes take the
 // copy engine ~1.5 us, which kept the MMAs waiting while one warp did both).
-// They meet only on mbarriers: tcgen05.commit -> "S(c) done" (two barriers,
-// alternating by chunk, so that no waiter can fall two phases behind one),
-// each softmax warp -> "P(c) ready", TMA -> "K/V stage full", and a per-slot
-// barrier that publishes which blocks of a chunk exist. K and V have two
-// shared stages each; K(c+2) and V(c+1) load as soon as S(c) lands, a chunk
-// ahead of their use. Two CTAs share an SM (~97 KB of shared memory and 256
-// tensor-memory columns each).
+// They meet only on mbarriers: tcgen05.commit -> "S(c) done" and "P(c).V(c)
+// done", each softmax warp -> "P(c) ready", TMA -> "K/V stage full", and a
+// per-slot barrier that publishes which blocks of a chunk exist; every
+// per-chunk barrier comes in two, alternating by chunk, so that no waiter can
+// fall two phases behind one. S has two tensor-memory buffers and P(c) is
+// written over the S(c) it comes from (a row's scores are all in registers by
+// then), so S(c+1) and P(c-1).V(c-1) run on the tensor cores while the
+// softmax works on S(c); S(c+2) goes into S(c)'s buffer once P(c).V(c) has
+// read it. K and V have two shared stages each: K(c+2) loads once S(c) has
+// read K(c), V(c+2) once P(c).V(c) has read V(c). Two CTAs share an SM
+// (~97 KB of shared memory and 256 tensor-memory columns each).
 
 constexpr int kTcRows = 128;                 // query rows per CTA = M = TMEM lanes
 constexpr int kTcThreads = kTcRows + 64;     // + the MMA warp and the copy warp
 constexpr int kTcChunk = 64;                 // KV tokens per step = N of S = K of P.V
 constexpr int kTcBlocks = kTcChunk / kBlock;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;                // S: 64 fp32 columns
-constexpr uint32_t kColPh = 64, kColPl = 96; // P high / low: 64 16-bit values in 32 columns each
+constexpr uint32_t kColBuf = 64;             // S buffer b at columns [64b, 64b+64): S(c) in buffer
+constexpr uint32_t kColPl = 32;              // c & 1, then P(c) over it: high part +0, low part +32
 constexpr uint32_t kColO = 128;              // O: d fp32 columns
 constexpr float kTcSlack = 8.f;              // log2 headroom before (m, l, O) are rescaled
 
@@ -398,7 +402,7 @@ struct TcCfg {
     static constexpr int kVb = kBlock * D * 2;                  // one block's V tile
     static constexpr int kVc = kTcBlocks * kVb;                 // V chunk
     static constexpr int kOffK = kQ, kOffV = kOffK + 2 * kKc, kOffBar = kOffV + 2 * kVc;
-    static constexpr int kSmem = 1024 + kOffBar + 128;
+    static constexpr int kSmem = 1024 + kOffBar + 256;
     static_assert(4 * 32 * (D + 4) * 4 <= kOffBar, "the epilogue stages 4 warps x 32 padded rows below the barriers");
     static constexpr uint32_t kIdescS = mma_idesc_f16(kTcRows, kTcChunk, kBf16, false, false);
     static constexpr uint32_t kIdescO = mma_idesc_f16(kTcRows, D, kBf16, false, true);
@@ -425,16 +429,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const uint32_t sb = (raw + 1023u) & ~1023u;
     uint8_t* gb = smem_raw + (sb - raw);
     const uint32_t sQ = sb, sK = sb + C::kOffK, sV = sb + C::kOffV;
-    // barriers (8 B each): K stage 0/1, V stage 0/1, "S(c) done" for even / odd c,
-    // P ready, mask slot 0..3; then the TMEM address and the 4 block masks
+    // barriers (8 B each), every per-chunk one alternating by chunk so that no
+    // waiter can fall two phases behind one (event c is completion c >> 1 of
+    // barrier c & 1): K stage, V stage, "S(c) done", "P(c).V(c) done", "P(c)
+    // ready"; then mask slot 0..3, the TMEM address and the 4 block masks
     const uint32_t bar0 = sb + C::kOffBar;
-    const uint32_t bar_p = bar0 + 48, tslot = bar0 + 88;
-    volatile uint32_t* cmask = reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 92);   // [4]
+    const uint32_t tslot = bar0 + 112;
+    volatile uint32_t* cmask = reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 116);   // [4]
     auto bar_k = [&](int c) { return bar0 + 8 * (c & 1); };
     auto bar_v = [&](int c) { return bar0 + 16 + 8 * (c & 1); };
-    // phase c of "S(c) done, with P(c-1).V(c-1)" = completion c >> 1 of bar_s(c)
     auto bar_s = [&](int c) { return bar0 + 32 + 8 * (c & 1); };
-    auto bar_m = [&](int c) { return bar0 + 56 + 8 * (c & 3); };
+    auto bar_o = [&](int c) { return bar0 + 48 + 8 * (c & 1); };
+    auto bar_p = [&](int c) { return bar0 + 64 + 8 * (c & 1); };
+    auto bar_m = [&](int c) { return bar0 + 80 + 8 * (c & 3); };
     auto par2 = [](int c) { return (uint32_t)(c >> 1) & 1u; };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -502,8 +509,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
     }
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(bar0 + 8 * i, 1);        // K, V stages; S done x2
-        mbar_init(bar_p, 4);                   // one arrival per softmax warp
+        for (int i = 0; i < 8; ++i) mbar_init(bar0 + 8 * i, 1);        // K, V, S done, P.V done
+        mbar_init(bar_p(0), 4);                // one arrival per softmax warp
+        mbar_init(bar_p(1), 4);
         for (int i = 0; i < 4; ++i) mbar_init(bar_m(i), 1);
         fence_mbar_init();
     }
@@ -586,15 +594,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             else ++v_issued;
         };
         issue_kv(0, true);
-        if (nchunks > 1) issue_kv(1, true);
         issue_kv(0, false);
-        for (int c = 0; c + 1 < nchunks && ok; ++c) {
-            // S(c) done, and P(c-1).V(c-1) before it: K(c)'s stage takes K(c+2),
-            // V(c-1)'s stage takes V(c+1)
+        if (nchunks > 1) {
+            issue_kv(1, true);
+            issue_kv(1, false);
+        }
+        for (int c = 0; c + 2 < nchunks && ok; ++c) {
+            // S(c) has read K(c): its stage takes K(c+2); P(c).V(c) has read V(c):
+            // its stage takes V(c+2)
             ok = __all_sync(kFull, mbar_wait(bar_s(c), par2(c)));
             if (!ok) break;
-            if (c + 2 < nchunks) issue_kv(c + 2, true);
-            issue_kv(c + 1, false);
+            issue_kv(c + 2, true);
+            ok = __all_sync(kFull, mbar_wait(bar_o(c), par2(c)));
+            if (!ok) break;
+            issue_kv(c + 2, false);
         }
         if (!ok && lane == 0) {
             // let this CTA's copies land before the shared memory goes
@@ -604,60 +617,66 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         }
     } else if (mma_warp) {
         // ================================================== MMA warp
-        auto issue_s = [&](int c) {            // S = Q K(c)^T into columns [0, 64)
+        auto issue_s = [&](int c) {            // S(c) = Q K(c)^T into buffer c & 1
             const uint32_t kb = sK + (c & 1) * C::kKc;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
                 const uint64_t ad = smem_desc_sw128(sQ + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
                 const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * (kTcChunk * 128) + (ks & 3) * 32, 16, 1024);
-                tc_mma_f16(tmem + kColS, ad, bd, C::kIdescS, ks > 0);
+                tc_mma_f16(tmem + (c & 1) * kColBuf, ad, bd, C::kIdescS, ks > 0);
             }
         };
-        int s_committed = 0;
+        int s_issued = 0, o_issued = 0;        // events committed (for the failure path)
         if (lane == 0) {
-            ok = mbar_wait(bar_k(0), par2(0));
-            tc_fence_after();
-            if (ok) issue_s(0);
-            tc_commit(bar_s(0));               // phase 0: S(0) done
+            for (int c = 0; c < min(2, nchunks); ++c) {
+                const bool w = ok && mbar_wait(bar_k(c), par2(c));
+                tc_fence_after();
+                if (w) issue_s(c);
+                tc_commit(bar_s(c));           // S(c) done
+                ++s_issued;
+                ok = w;
+            }
         }
-        s_committed = 1;
         ok = __shfl_sync(kFull, ok, 0);
         for (int c = 0; c < nchunks && ok; ++c) {
-            // P(c) written, S(c) read, V(c) rows zeroed by the softmax warps
-            ok = __all_sync(kFull, mbar_wait(bar_p, (uint32_t)c & 1u));
+            // P(c) written over S(c), V(c) rows zeroed by the softmax warps
+            ok = __all_sync(kFull, mbar_wait(bar_p(c), par2(c)));
             if (!ok) break;
             if (lane == 0) {
                 tc_fence_after();
                 bool w = mbar_wait(bar_v(c), par2(c));
                 if (w) {
                     const uint32_t vb = sV + (c & 1) * C::kVc;
+                    const uint32_t pb = tmem + (c & 1) * kColBuf;
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
 #pragma unroll
                         for (int jl = 0; jl < kTcBlocks; ++jl)
-                            tc_mma_f16_ta(tmem + kColO, tmem + (part ? kColPl : kColPh) + 8 * jl,
+                            tc_mma_f16_ta(tmem + kColO, pb + (part ? kColPl : 0) + 8 * jl,
                                           smem_desc_sw128(vb + jl * C::kVb, kBlock * 128, 1024), C::kIdescO,
                                           !(c == 0 && part == 0 && jl == 0));
                     }
-                    if (c + 1 < nchunks) {
-                        w = mbar_wait(bar_k(c + 1), par2(c + 1));
-                        tc_fence_after();
-                        if (w) issue_s(c + 1);
-                    }
                 }
-                tc_commit(bar_s(c + 1));       // phase c+1: P(c).V(c) (and S(c+1)) done
+                tc_commit(bar_o(c));           // P(c).V(c) done
+                ++o_issued;
+                if (w && c + 2 < nchunks) {
+                    // S(c+2) goes over P(c): after P(c).V(c) has read it
+                    w = mbar_wait(bar_o(c), par2(c)) && mbar_wait(bar_k(c + 2), par2(c + 2));
+                    tc_fence_after();
+                    if (w) issue_s(c + 2);
+                    tc_commit(bar_s(c + 2));
+                    ++s_issued;
+                }
                 ok = w;
             }
             ok = __shfl_sync(kFull, ok, 0);
-            s_committed = c + 2;
         }
         if (!ok && lane == 0) {
-            // let this CTA's MMAs land before the tensor memory goes: the last
-            // phases in order (a parity wait cannot tell a phase from the one
-            // two before it)
+            // let this CTA's MMAs land before the tensor memory goes, each
+            // barrier's events in order
             flag_error(a.err, GQA_DEVERR_TIMEOUT);
-            for (int k = max(0, s_committed - 4); k < s_committed; ++k)
-                mbar_wait(bar_s(k), par2(k), kWaitLimitNs / 4);
+            for (int k = max(0, s_issued - 2); k < s_issued; ++k) mbar_wait(bar_s(k), par2(k), kWaitLimitNs / 4);
+            for (int k = max(0, o_issued - 2); k < o_issued; ++k) mbar_wait(bar_o(k), par2(k), kWaitLimitNs / 4);
         }
     } else {
         // ================================================== softmax warps: one row per thread
@@ -665,19 +684,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         float m = -INFINITY, l = 0.f;
         int c = 0;
         for (; c < nchunks; ++c) {
-            ok = __all_sync(kFull, mbar_wait(bar_s(c), par2(c)));   // S(c), earlier MMAs done
+            ok = __all_sync(kFull, mbar_wait(bar_s(c), par2(c)));   // S(c) done
             ok = ok && __all_sync(kFull, mbar_wait(bar_m(c), (uint32_t)(c >> 2) & 1u));
             if (!ok) break;
             tc_fence_after();
             const int cpos = (jb_lo + kTcBlocks * c) * kBlock;
             const uint32_t bm = cmask[c & 3];
+            const uint32_t t_buf = t_lane + (uint32_t)(c & 1) * kColBuf;
             float sv[kTcChunk];
             {
                 uint32_t r0[16], r1[16], r2[16], r3[16];
-                tmem_ld16(t_lane + kColS, r0);
-                tmem_ld16(t_lane + kColS + 16, r1);
-                tmem_ld16(t_lane + kColS + 32, r2);
-                tmem_ld16(t_lane + kColS + 48, r3);
+                tmem_ld16(t_buf, r0);
+                tmem_ld16(t_buf + 16, r1);
+                tmem_ld16(t_buf + 32, r2);
+                tmem_ld16(t_buf + 48, r3);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -709,6 +729,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             l *= alpha;
             if (c > 0 && __any_sync(kFull, resc && old_live)) {       // O holds earlier chunks: scale it
+                // once P(c-1).V(c-1) has landed in it
+                ok = __all_sync(kFull, mbar_wait(bar_o(c - 1), par2(c - 1)));
+                if (!ok) break;
+                tc_fence_after();
                 const float f = (resc && old_live) ? alpha : 1.f;
 #pragma unroll
                 for (int q = 0; q < D / 16; ++q) {
@@ -733,8 +757,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                     const float2 f = unpack2<kB>(ph16[e]);
                     pl16[e] = pack2<kB>(x - f.x, y - f.y);
                 }
-                tmem_st16(t_lane + kColPh + 16 * hq, ph16);
-                tmem_st16(t_lane + kColPl + 16 * hq, pl16);
+                tmem_st16(t_buf + 16 * hq, ph16);              // over this row's S(c)
+                tmem_st16(t_buf + kColPl + 16 * hq, pl16);
             }
             tmem_wait_st();
             l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
@@ -753,11 +777,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_p);
+            if (lane == 0) mbar_arrive(bar_p(c));
             if (!ok) break;
         }
         // ---- wait for the last MMAs, then normalise and store this row
-        if (ok) ok = __all_sync(kFull, mbar_wait(bar_s(nchunks), par2(nchunks)));   // the last P.V
+        // the last P.V (P(n-3).V(n-3), the previous event on its barrier, landed
+        // before S(n-1) was issued)
+        if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(nchunks - 1), par2(nchunks - 1)));
         tc_fence_after();
         if (ok) {
             // This warp's 32 rows leave through shared memory (Q and the K/V
