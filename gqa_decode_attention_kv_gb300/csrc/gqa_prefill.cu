@@ -378,8 +378,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 // fall two phases behind one. S has two tensor-memory buffers and P(c) is
 // written over the S(c) it comes from (a row's scores are all in registers by
 // then), so S(c+1) and P(c-1).V(c-1) run on the tensor cores while the
-// softmax works on S(c); S(c+2) goes into S(c)'s buffer once P(c).V(c) has
-// read it. K and V have two shared stages each: K(c+2) loads once S(c) has
+// softmax works on S(c); S(c+1) goes into P(c-1)'s buffer once P(c-1).V(c-1)
+// has read it, before the MMA warp waits for P(c). K and V have two shared stages each: K(c+2) loads once S(c) has
 // read K(c), V(c+2) once P(c).V(c) has read V(c). Two CTAs share an SM
 // (~97 KB of shared memory and 256 tensor-memory columns each).
 
@@ -628,17 +628,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         };
         int s_issued = 0, o_issued = 0;        // events committed (for the failure path)
         if (lane == 0) {
-            for (int c = 0; c < min(2, nchunks); ++c) {
-                const bool w = ok && mbar_wait(bar_k(c), par2(c));
-                tc_fence_after();
-                if (w) issue_s(c);
-                tc_commit(bar_s(c));           // S(c) done
-                ++s_issued;
-                ok = w;
-            }
+            ok = mbar_wait(bar_k(0), par2(0));
+            tc_fence_after();
+            if (ok) issue_s(0);
+            tc_commit(bar_s(0));               // S(0) done
+            ++s_issued;
         }
         ok = __shfl_sync(kFull, ok, 0);
         for (int c = 0; c < nchunks && ok; ++c) {
+            // S(c+1) first, so that it is ready when the softmax finishes S(c):
+            // it goes over P(c-1), once P(c-1).V(c-1) has read it
+            if (lane == 0 && c + 1 < nchunks) {
+                bool w = c == 0 || mbar_wait(bar_o(c - 1), par2(c - 1));
+                w = w && mbar_wait(bar_k(c + 1), par2(c + 1));
+                tc_fence_after();
+                if (w) issue_s(c + 1);
+                tc_commit(bar_s(c + 1));
+                ++s_issued;
+                ok = w;
+            }
+            ok = __shfl_sync(kFull, ok, 0);
+            if (!ok) break;
             // P(c) written over S(c), V(c) rows zeroed by the softmax warps
             ok = __all_sync(kFull, mbar_wait(bar_p(c), par2(c)));
             if (!ok) break;
@@ -659,14 +669,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 }
                 tc_commit(bar_o(c));           // P(c).V(c) done
                 ++o_issued;
-                if (w && c + 2 < nchunks) {
-                    // S(c+2) goes over P(c): after P(c).V(c) has read it
-                    w = mbar_wait(bar_o(c), par2(c)) && mbar_wait(bar_k(c + 2), par2(c + 2));
-                    tc_fence_after();
-                    if (w) issue_s(c + 2);
-                    tc_commit(bar_s(c + 2));
-                    ++s_issued;
-                }
                 ok = w;
             }
             ok = __shfl_sync(kFull, ok, 0);
