@@ -208,3 +208,18 @@ def test_full_size_prefill_workload_sampled(gq, oracle_mod):
         ref = oracle_mod.decode(qb[T - 24:][None], kd, vd, [lens[b]], case.scale)[0]
         got = out[b * T + T - 24:(b + 1) * T].float().cpu().numpy().astype(np.float64)
         assert np.abs(got - ref).max() <= TOL
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_prefill_on_the_unpaged_layout(gq, oracle_mod, kernel):
+    """The contiguous [B, S_pad, K, d] buffer with an identity table: token,
+    head and block strides differ from the pool's, and the page copies follow."""
+    news = [40, 7, 100]
+    prior = [60, 0, 13]
+    lens = [n + p for n, p in zip(news, prior)]
+    case = gi.make_case(len(lens), 32, 8, 128, lens, "bf16", seed=90, device="cuda", contiguous=True)
+    g = torch.Generator(device="cuda").manual_seed(91)
+    q = torch.randn((sum(news), 32, 128), generator=g, device="cuda").to(torch.bfloat16)
+    q_start = torch.tensor(np.concatenate([[0], np.cumsum(news)]), dtype=torch.int32, device="cuda")
+    ref = _reference(oracle_mod, case, q, news)
+    assert max_abs_err(_run(gq, case, q, q_start, news, kernel=kernel), ref) <= TOL
