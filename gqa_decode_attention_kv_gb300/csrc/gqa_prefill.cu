@@ -368,20 +368,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 //                part written to tensor memory with tcgen05.st
 //   O[128 x d]  += P_hi V + P_lo V          A = P from tensor memory, B = the
 //                                            V tiles read MN-major
-// Warp roles: warps 0-3 own the 128 rows (softmax, epilogue); warp 4 issues
-// every MMA; warp 5 issues every TMA copy (a chunk's 16 page boxes take the
-// copy engine ~1.5 us, which kept the MMAs waiting while one warp did both).
-// They meet only on mbarriers: tcgen05.commit -> "S(c) done" and "P(c).V(c)
+// Warp roles: warps 0-3 own the 128 rows (Q load, softmax, epilogue); warp 4
+// issues every MMA; warp 5 issues every TMA copy (the copy engine takes ~100 ns
+// a box, which kept the MMAs waiting while one warp did both). A K page is two
+// 2 KB boxes (128-byte swizzle rows are half a row); a V page is one 4 KB box
+// through a 5-D map that splits the row into two halves.
+// The warps meet only on mbarriers: tcgen05.commit -> "S(c) done" and "P(c).V(c)
 // done", each softmax warp -> "P(c) ready", TMA -> "K/V stage full", and a
-// per-slot barrier that publishes which blocks of a chunk exist; every
+// per-slot barrier that publishes which blocks of a chunk exist. Every
 // per-chunk barrier comes in two, alternating by chunk, so that no waiter can
-// fall two phases behind one. S has two tensor-memory buffers and P(c) is
-// written over the S(c) it comes from (a row's scores are all in registers by
-// then), so S(c+1) and P(c-1).V(c-1) run on the tensor cores while the
-// softmax works on S(c); S(c+1) goes into P(c-1)'s buffer once P(c-1).V(c-1)
-// has read it, before the MMA warp waits for P(c). K and V have two shared stages each: K(c+2) loads once S(c) has
-// read K(c), V(c+2) once P(c).V(c) has read V(c). Two CTAs share an SM
-// (~97 KB of shared memory and 256 tensor-memory columns each).
+// fall two phases behind one (a parity wait cannot tell those apart).
+// S has two tensor-memory buffers and P(c) is written over the S(c) it comes
+// from (a row's scores are all in registers by then), so S(c+1) and
+// P(c-1).V(c-1) run on the tensor cores while the softmax works on S(c). The
+// MMA warp issues S(c+1) into P(c-1)'s buffer once P(c-1).V(c-1) has read it,
+// before it waits for P(c). K and V have two shared stages each: K(c+2) loads
+// once S(c) has read K(c), V(c+2) once P(c).V(c) has read V(c). The Q tile is
+// read whole rows at a time, and the epilogue writes whole output rows through
+// the then idle Q/K/V stages. Two CTAs share an SM (~97 KB of shared memory and
+// 256 tensor-memory columns each).
 
 constexpr int kTcRows = 128;                 // query rows per CTA = M = TMEM lanes
 constexpr int kTcThreads = kTcRows + 64;     // + the MMA warp and the copy warp
