@@ -68,7 +68,7 @@ int check_residual(const gqa_kv_cache_t* c, int batch) {
 }  // namespace
 
 bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int box_inner,
-                      bool swizzle128, int perm[3]) {
+                      int swizzle_bytes, int perm[3]) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
     if (!enc) return false;
     CUtensorMapDataType dt;
@@ -97,7 +97,9 @@ bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* bas
     }
     const CUresult r = enc(map, dt, 4, const_cast<void*>(base), gdim, gstride, box, estride,
                            CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                           : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                 : CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

@@ -133,8 +133,8 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
 
     CUtensorMap kmap, vmap;
     int perm[3];
-    if (!encode_cache_map(&kmap, c, c.k, v.box_inner, v.swizzle, perm) ||
-        !encode_cache_map(&vmap, c, c.v, v.box_inner, v.swizzle, perm))
+    if (!encode_cache_map(&kmap, c, c.k, v.box_inner, v.swizzle_bytes, perm) ||
+        !encode_cache_map(&vmap, c, c.v, v.box_inner, v.swizzle_bytes, perm))
         return GQA_ERR_UNSUPPORTED;
 
     const int smem = v.smem(L.batch);

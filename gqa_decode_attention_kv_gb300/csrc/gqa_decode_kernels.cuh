@@ -133,9 +133,12 @@ struct Cfg {
     static constexpr int kScaleBytes = kKc ? 2 * D + 32 : kCoded ? 64 : 0;
     static constexpr int kVsOff = kKc ? 2 * D : 32;                 // v scales within them
     // 128-byte swizzled boxes for the tensor-core kernel; a 4-bit tile (64-byte
-    // rows) is read conflict-free without one.
+    // rows) takes the 64-byte swizzle (16-byte chunk ^= (row >> 1) & 3), which
+    // spreads its V reads over twice the banks. The CUDA-core kernel reads rows
+    // whole and needs none.
     static constexpr bool kSwizzle = (kKind == kKernelMma) && !kI4;
-    static constexpr int kStageAlign = kSwizzle ? 1024 : 128;      // swizzle atom / TMA box
+    static constexpr int kSwizzleBytes = kKind != kKernelMma ? 0 : kI4 ? 64 : 128;
+    static constexpr int kStageAlign = kSwizzleBytes == 128 ? 1024 : kSwizzleBytes == 64 ? 512 : 128;
     static constexpr int kStage = ((2 * kTile + kScaleBytes + kStageAlign - 1) / kStageAlign) * kStageAlign;
     static constexpr int kNw = kHeadWarps;
     // The coded-cache kernels are issue-bound: the pool's bookkeeping costs
@@ -502,17 +505,19 @@ __device__ __forceinline__ void mma_load(MmaFrags<C, D>& f, uint32_t stage, int 
         for (int j = 0; j < C::kMt; ++j)
             ldsm_x4_t(swz(sv, rr + 8 * (mi >> 1), 2 * j + (mi & 1)), f.v[j]);
     } else if constexpr (C::kI4) {
-        // K: 16 bytes (32 codes) of tokens r and r+8 at byte 16c; V: 8 bytes
-        // (dims 16r..16r+15) of tokens 2c, 2c+1, 2c+8, 2c+9. 64-byte rows, no
-        // swizzle: both patterns touch each bank once per phase, or twice (V).
-        const uint4 k0 = lds128(sk + r * C::kRowBytes + 16 * c);
-        const uint4 k1 = lds128(sk + (r + 8) * C::kRowBytes + 16 * c);
+        // K: 16 bytes (32 codes) of tokens r and r+8 at chunk c; V: 8 bytes
+        // (dims 16r..16r+15) of tokens 2c, 2c+1, 2c+8, 2c+9. 64-byte rows with
+        // the 64-byte swizzle (chunk ^ (row >> 1) & 3): K touches each bank once
+        // per phase, V twice.
+        const uint32_t kx = (uint32_t)((c ^ (r >> 1)) & 3) * 16;         // rows r, r+8 alike
+        const uint4 k0 = lds128(sk + r * C::kRowBytes + kx);
+        const uint4 k1 = lds128(sk + (r + 8) * C::kRowBytes + kx);
         f.k[0][0] = k0.x; f.k[0][1] = k0.y; f.k[0][2] = k0.z; f.k[0][3] = k0.w;
         f.k[1][0] = k1.x; f.k[1][1] = k1.y; f.k[1][2] = k1.z; f.k[1][3] = k1.w;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int tok = 2 * c + (i & 1) + 8 * (i >> 1);
-            const uint2 w = lds64(sv + tok * C::kRowBytes + 8 * r);
+            const uint2 w = lds64(sv + tok * C::kRowBytes + 16 * ((r >> 1) ^ ((tok >> 1) & 3)) + 8 * (r & 1));
             f.v[i][0] = w.x;
             f.v[i][1] = w.y;
         }
@@ -1473,7 +1478,7 @@ struct Variant {
     int warps;           // threads / 32
     int workers_per_cta; // split-KV workers per CTA
     int box_inner;       // elements per TMA box row
-    bool swizzle;
+    int swizzle_bytes;   // TMA swizzle of the tiles: 0, 64 or 128
     int (*smem)(int);
 };
 
@@ -1481,7 +1486,7 @@ template <int kKind, typename T, int D, int NW, bool kGen>
 Variant make_variant() {
     using C = Cfg<kKind, T, D, NW, kGen>;
     return Variant{reinterpret_cast<const void*>(&split_kv_kernel<kKind, T, D, NW, kGen>), C::kTailChunks, C::kWarps,
-                   NW == 1 ? C::kWarps : 1, C::kBoxInner, C::kSwizzle, &Smem<C>::bytes};
+                   NW == 1 ? C::kWarps : 1, C::kBoxInner, C::kSwizzleBytes, &Smem<C>::bytes};
 }
 
 template <int kKind, typename T, int D, bool kGen>

@@ -106,9 +106,9 @@ int launch_decode(const DecodeLaunch& L, int num_sms);
 // 4-D tensor map over one cache tensor. Dim 0 is the head dimension d; dims
 // 1..3 are the slot (16), kv-head (K) and block (num_blocks) axes sorted by
 // increasing stride, and perm[i] names which of them (0 slot, 1 head, 2 block)
-// map dim i+1 is. The box is box_inner elements by 16 slots. 128-byte swizzle or
-// none. Returns false if the driver rejects the description.
+// map dim i+1 is. The box is box_inner elements by 16 slots; swizzle_bytes is
+// 0 (none), 64 or 128. Returns false if the driver rejects the description.
 bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base,
-                      int box_inner, bool swizzle128, int perm[3]);
+                      int box_inner, int swizzle_bytes, int perm[3]);
 
 }  // namespace gqa

@@ -870,7 +870,7 @@ int launch_prefill(const PrefillLaunch& L) {
     }
     CUtensorMap kmap, vmap;
     int perm[3];
-    if (!encode_cache_map(&kmap, c, c.k, 64, true, perm) || !encode_cache_map(&vmap, c, c.v, 64, true, perm))
+    if (!encode_cache_map(&kmap, c, c.k, 64, 128, perm) || !encode_cache_map(&vmap, c, c.v, 64, 128, perm))
         return GQA_ERR_UNSUPPORTED;
     int page_perm[2] = {1, 2};
     if (tc && D == 128 && !encode_page_map(&vmap, c, c.v, page_perm))   // V a page per box
