@@ -811,14 +811,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                                     __uint_as_float(r16[j + 2]) * inv, __uint_as_float(r16[j + 3]) * inv);
             }
             __syncwarp();
+            int tkr = (row0 + 32 * warp) / a.G, hr = (row0 + 32 * warp) - tkr * a.G;   // token, head of row r
             for (int r = 0; r < 32; ++r) {
-                const int rw = row0 + 32 * warp + r;
-                if (rw >= rows) break;
+                if (row0 + 32 * warp + r >= rows) break;
                 if (4 * lane < D) {
-                    const int tkr = rw / a.G, hr = rw - tkr * a.G;
                     const long long orow = ((long long)(q0 + tkr) * a.H + (long long)g * a.G + hr) * D;
                     store4(a.out, a.out_dtype, orow + 4 * lane,
                            *reinterpret_cast<const float4*>(stage + r * kRowF + 4 * lane));
+                }
+                if (++hr == a.G) {
+                    hr = 0;
+                    ++tkr;
                 }
             }
         } else if (lane == 0) {

@@ -140,6 +140,32 @@ def test_int4_wide_group_f16_query(gq, layout):
     assert max_abs_err(_run(gq, case, row_layout=layout), oracle_for_case(case)) <= TOL
 
 
+# bound per cache: the f16 low part of p s_v resolves 2^-24 absolute, which the
+# small FP8 scales (~0.008) turn into ~1e-4 of output; int8 and INT4 scales leave
+# the fp32 accumulation (~1e-5) as the floor
+_SAME_ROW_BOUND = {"i8": 1e-4, "i4": 1e-4, "i4kc": 1e-4, "fp8": TOL / 4}
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype", ["i8", "fp8", "i4", "i4kc"])
+def test_one_value_row_everywhere_comes_back_exactly(gq, dtype, kernel):
+    """Every cached token holds the same V codes and scale: whatever the scores,
+    the output is that row. The tensor-core kernel feeds the weights p s_v to
+    P.V as an f16 high plus low part, so what remains is the low part's
+    resolution and the fp32 accumulation; the high part alone would miss by
+    about 2^-12 |v| (5e-4 to 8e-4 at these values)."""
+    lens = [2, 3, 9, 17, 300]
+    case = gi.make_case(len(lens), 32, 8, 128, lens, dtype, q_dtype="bf16", seed=41, device="cuda")
+    case.q = (case.q.float() * 3).to(torch.bfloat16)          # a few tokens carry the weight
+    blk = int(case.block_table[0, 0])
+    case.v_cache.copy_(case.v_cache[blk, 0, 0].expand_as(case.v_cache))
+    case.v_scale.fill_(float(case.v_scale[blk, 0, 0]))
+    ref = oracle_for_case(case)
+    for mw in (0, 3):
+        out = _run(gq, case, kernel=kernel, max_warps=mw, min_blocks_per_warp=1)
+        assert max_abs_err(out, ref) <= _SAME_ROW_BOUND[dtype]
+
+
 def test_int8_cache_with_f16_query(gq):
     lens = [40, 333]
     case = gi.make_case(2, 32, 8, 128, lens, "i8", q_dtype="f16", seed=23, device="cuda")
