@@ -360,54 +360,59 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 // The same prefill on the 5th-generation tensor cores (tcgen05.mma, fp32
 // accumulators in tensor memory). One CTA = 128 query rows (the MMA M; one
 // tensor-memory lane per row) of one (kv-head, sequence); the KV range goes by
-// in chunks of 64 tokens (4 paged blocks):
-//   S[128 x 64]  = Q[128 x d] K_chunk^T     Q, K: K-major 128-byte-swizzled
-//                                            shared tiles
-//   softmax      one thread per row: tcgen05.ld of its 64 scores, mask, online
+// in chunks of 32 tokens (2 paged blocks):
+//   S[128 x 32]  = Q[128 x d] K_chunk^T     A = Q from tensor memory (each row
+//                                            thread writes its own), B = the
+//                                            K-major 128-byte-swizzled K tile
+//   softmax      one thread per row: tcgen05.ld of its 32 scores, mask, online
 //                (m, l) with the lazy rescale; P as a high and a low 16-bit
 //                part written to tensor memory with tcgen05.st
 //   O[128 x d]  += P_hi V + P_lo V          A = P from tensor memory, B = the
 //                                            V tiles read MN-major
-// Warp roles: warps 0-3 own the 128 rows (Q load, softmax, epilogue); warp 4
-// issues every MMA; warp 5 issues every TMA copy (the copy engine takes ~100 ns
-// a box, which kept the MMAs waiting while one warp did both). A K page is two
-// 2 KB boxes (128-byte swizzle rows are half a row); a V page is one 4 KB box
-// through a 5-D map that splits the row into two halves.
+// Tensor memory (256 columns): two 32-column S buffers, Q (d/2 columns), O (d).
+// Warp roles: warps 0-3 own the 128 rows (Q, softmax, epilogue); warp 4 issues
+// every MMA; warp 5 issues the K copies and warp 6 the V copies, so that K runs
+// ahead of the P.V products (the copy engine takes ~100 ns a box). A K page is
+// two 2 KB boxes (128-byte swizzle rows are half a row); a V page is one 4 KB
+// box through a 5-D map that splits the row into two halves.
 // The warps meet only on mbarriers: tcgen05.commit -> "S(c) done" and "P(c).V(c)
-// done", each softmax warp -> "P(c) ready", TMA -> "K/V stage full", and a
-// per-slot barrier that publishes which blocks of a chunk exist. Every
-// per-chunk barrier comes in two, alternating by chunk, so that no waiter can
-// fall two phases behind one (a parity wait cannot tell those apart).
-// S has two tensor-memory buffers and P(c) is written over the S(c) it comes
-// from (a row's scores are all in registers by then), so S(c+1) and
-// P(c-1).V(c-1) run on the tensor cores while the softmax works on S(c). The
-// MMA warp issues S(c+1) into P(c-1)'s buffer once P(c-1).V(c-1) has read it,
-// before it waits for P(c). K and V have two shared stages each: K(c+2) loads
-// once S(c) has read K(c), V(c+2) once P(c).V(c) has read V(c). The Q tile is
-// read whole rows at a time, and the epilogue writes whole output rows through
-// the then idle Q/K/V stages. Two CTAs share an SM (~97 KB of shared memory and
-// 256 tensor-memory columns each).
+// done", each softmax warp -> "P(c) ready" and once "Q stored", TMA -> "K/V stage
+// full", and a per-slot barrier that publishes which blocks of a chunk exist.
+// Every per-chunk barrier comes in four copies taken in turn by chunk, so that
+// no waiter can fall two phases behind one (a parity wait cannot tell those
+// apart). P(c) is written over the S(c) it comes from (a row's scores are all
+// in registers by then), so S(c+1) and P(c-1).V(c-1) run on the tensor cores
+// while the softmax works on S(c): the MMA warp issues S(c+1) into P(c-1)'s
+// buffer once P(c-1).V(c-1) has read it, before it waits for P(c). K and V have
+// four shared stages each: K(c+4) loads once S(c) has read K(c), V(c+4) once
+// P(c).V(c) has read V(c). The epilogue writes whole output rows through the
+// idle Q/K/V stages. Two CTAs share an SM (~97 KB of shared memory and 256
+// tensor-memory columns each).
 
 constexpr int kTcRows = 128;                 // query rows per CTA = M = TMEM lanes
-constexpr int kTcThreads = kTcRows + 64;     // + the MMA warp and the copy warp
-constexpr int kTcChunk = 64;                 // KV tokens per step = N of S = K of P.V
+constexpr int kTcThreads = kTcRows + 96;     // + the MMA warp and the K and V copy warps
+constexpr int kTcChunk = 32;                 // KV tokens per step = N of S = K of P.V
 constexpr int kTcBlocks = kTcChunk / kBlock;
+constexpr int kTcBufs = 4;                   // K and V stages, per-chunk barrier copies: c & 3
+constexpr int kTcMasks = 8;                  // block-mask slots: chunk c uses c & 7
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColBuf = 64;             // S buffer b at columns [64b, 64b+64): S(c) in buffer
-constexpr uint32_t kColPl = 32;              // c & 1, then P(c) over it: high part +0, low part +32
+constexpr uint32_t kColBuf = kTcChunk;       // S buffer b at columns [32b, 32b+32): S(c) in buffer
+constexpr uint32_t kColPl = kTcChunk / 2;    // c & 1, then P(c) over it: high part +0, low part +16
+constexpr uint32_t kColQ = 2 * kColBuf;      // Q: d 16-bit values per row, two per column
 constexpr uint32_t kColO = 128;              // O: d fp32 columns
+static_assert(kColQ + 64 <= kColO && kColO + 128 <= kTmemCols, "S, Q and O share the CTA's tensor-memory columns");
 constexpr float kTcSlack = 8.f;              // log2 headroom before (m, l, O) are rescaled
 
 template <typename T, int D>
 struct TcCfg {
     static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     static constexpr int kHalves = D / 64;                      // 128-byte column halves of a row
-    static constexpr int kQ = kTcRows * D * 2;                  // Q tile
-    static constexpr int kKc = kTcChunk * D * 2;                // K chunk: 64 rows per half
+    static constexpr int kQ = kTcRows * D * 2;                  // Q-sized area: epilogue staging
+    static constexpr int kKc = kTcChunk * D * 2;                // K chunk: 32 rows per half
     static constexpr int kVb = kBlock * D * 2;                  // one block's V tile
     static constexpr int kVc = kTcBlocks * kVb;                 // V chunk
-    static constexpr int kOffK = kQ, kOffV = kOffK + 2 * kKc, kOffBar = kOffV + 2 * kVc;
-    static constexpr int kSmem = 1024 + kOffBar + 256;
+    static constexpr int kOffK = kQ, kOffV = kOffK + kTcBufs * kKc, kOffBar = kOffV + kTcBufs * kVc;
+    static constexpr int kSmem = 1024 + kOffBar + 512;
     static_assert(4 * 32 * (D + 4) * 4 <= kOffBar, "the epilogue stages 4 warps x 32 padded rows below the barriers");
     static constexpr uint32_t kIdescS = mma_idesc_f16(kTcRows, kTcChunk, kBf16, false, false);
     static constexpr uint32_t kIdescO = mma_idesc_f16(kTcRows, D, kBf16, false, true);
@@ -433,24 +438,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t sb = (raw + 1023u) & ~1023u;
     uint8_t* gb = smem_raw + (sb - raw);
-    const uint32_t sQ = sb, sK = sb + C::kOffK, sV = sb + C::kOffV;
-    // barriers (8 B each), every per-chunk one alternating by chunk so that no
-    // waiter can fall two phases behind one (event c is completion c >> 1 of
-    // barrier c & 1): K stage, V stage, "S(c) done", "P(c).V(c) done", "P(c)
-    // ready"; then mask slot 0..3, the TMEM address and the 4 block masks
+    const uint32_t sK = sb + C::kOffK, sV = sb + C::kOffV;   // the Q stage only stages the epilogue
+    // barriers (8 B each), every per-chunk one in four copies taken in turn by
+    // chunk, so that no waiter can fall two phases behind one (event c is
+    // completion c >> 2 of copy c & 3): K stage, V stage, "S(c) done", "P(c).V(c)
+    // done", "P(c) ready"; then mask slots 0..7 (c & 7), the TMEM address and the
+    // 8 block masks
     const uint32_t bar0 = sb + C::kOffBar;
-    const uint32_t tslot = bar0 + 112;
-    volatile uint32_t* cmask = reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 116);   // [4]
-    auto bar_k = [&](int c) { return bar0 + 8 * (c & 1); };
-    auto bar_v = [&](int c) { return bar0 + 16 + 8 * (c & 1); };
-    auto bar_s = [&](int c) { return bar0 + 32 + 8 * (c & 1); };
-    auto bar_o = [&](int c) { return bar0 + 48 + 8 * (c & 1); };
-    auto bar_p = [&](int c) { return bar0 + 64 + 8 * (c & 1); };
-    auto bar_m = [&](int c) { return bar0 + 80 + 8 * (c & 3); };
-    auto par2 = [](int c) { return (uint32_t)(c >> 1) & 1u; };
+    const uint32_t bar_q = bar0 + 224;         // "Q is in tensor memory": one arrival per softmax warp
+    const uint32_t tslot = bar0 + 232;
+    volatile uint32_t* cmask = reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 236);   // [8]
+    auto bar_k = [&](int c) { return bar0 + 8 * (c & 3); };
+    auto bar_v = [&](int c) { return bar0 + 32 + 8 * (c & 3); };
+    auto bar_s = [&](int c) { return bar0 + 64 + 8 * (c & 3); };
+    auto bar_o = [&](int c) { return bar0 + 96 + 8 * (c & 3); };
+    auto bar_p = [&](int c) { return bar0 + 128 + 8 * (c & 3); };
+    auto bar_m = [&](int c) { return bar0 + 160 + 8 * (c & 7); };
+    auto par4 = [](int c) { return (uint32_t)(c >> 2) & 1u; };
+    auto par8 = [](int c) { return (uint32_t)(c >> 3) & 1u; };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool softmax = warp < 4, mma_warp = warp == 4, loader = warp == 5;
+    const bool softmax = warp < 4, mma_warp = warp == 4, loader = warp >= 5;
     const int tile = a.tiles_per_seq - 1 - (int)blockIdx.x;    // heaviest first
     const int g = blockIdx.y, b = blockIdx.z;
     if (tid == 0) {
@@ -484,52 +492,50 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     const int hi = live ? base_pos + tk + 1 : 0;
     const int lo = a.window > 0 ? hi - a.window : 0;
 
+    // This thread's Q row (rows past the prompt are zero), loaded now and
+    // written to its tensor-memory lane once the columns are allocated: the S
+    // products then read Q from tensor memory, not from shared memory.
+    uint4 qv[D / 8];
     if (softmax) {
-        // This warp's 32 Q rows into the swizzled K-major tile, loaded whole
-        // rows at a time (D/8 lanes per row, 16 bytes each; rows past the
-        // prompt are zero).
-        constexpr int kLanesPerRow = D / 8, kRowsPerStep = 32 / kLanesPerRow, kSteps = 32 / kRowsPerStep;
-        const int c = lane % kLanesPerRow;
-        const int rl0 = 32 * warp + lane / kLanesPerRow;               // first row of this lane
-        int tq = (row0 + rl0) / a.G, hq = (row0 + rl0) - tq * a.G;      // its token and head
-        uint4 v[kSteps];
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
+                                                          ((long long)(q0 + tk) * a.H + (long long)g * a.G + (rr - tk * a.G)) * D);
 #pragma unroll
-        for (int i = 0; i < kSteps; ++i) {          // every load in flight before any store
-            const int rq = row0 + rl0 + i * kRowsPerStep;
-            v[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (rq < rows) {
-                const long long src = ((long long)(q0 + tq) * a.H + (long long)g * a.G + hq) * D;
-                v[i] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + src) + c);
-            }
-            hq += kRowsPerStep;                     // next row: kRowsPerStep heads on
-            while (hq >= a.G) {
-                hq -= a.G;
-                ++tq;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kSteps; ++i) {
-            const int rl = rl0 + i * kRowsPerStep;
-            sts128(sQ + (c >> 3) * (kTcRows * 128) + rl * 128 + (((c & 7) ^ (rl & 7)) << 4), v[i]);
-        }
+        for (int i = 0; i < D / 8; ++i) qv[i] = live ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
     }
     if (tid == 0) {
-        for (int i = 0; i < 8; ++i) mbar_init(bar0 + 8 * i, 1);        // K, V, S done, P.V done
-        mbar_init(bar_p(0), 4);                // one arrival per softmax warp
-        mbar_init(bar_p(1), 4);
-        for (int i = 0; i < 4; ++i) mbar_init(bar_m(i), 1);
+        for (int i = 0; i < 4 * kTcBufs; ++i) mbar_init(bar0 + 8 * i, 1);   // K, V, S done, P.V done
+        for (int i = 0; i < kTcBufs; ++i) mbar_init(bar_p(i), 4);         // one arrival per softmax warp
+        for (int i = 0; i < kTcMasks; ++i) mbar_init(bar_m(i), 1);
+        mbar_init(bar_q, 4);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tslot, kTmemCols);
-    fence_proxy_async_smem();                  // Q visible to the tensor core
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + (tslot - sb));
     bool ok = true;
+    if (softmax) {
+        const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16) + kColQ;
+#pragma unroll
+        for (int u = 0; u < D / 32; ++u) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                w[4 * i] = qv[4 * u + i].x; w[4 * i + 1] = qv[4 * u + i].y;
+                w[4 * i + 2] = qv[4 * u + i].z; w[4 * i + 3] = qv[4 * u + i].w;
+            }
+            tmem_st16(t_row + 16 * u, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_q);
+    }
 
     if (loader) {
-        // ================================================== copy warp
+        // ================================================== copy warps: 5 = K, 6 = V
+        const bool k_warp = warp == 5;
         const uint64_t pol = l2_policy_evict_last();   // every query tile of the sequence re-reads them
         int win_base = -(1 << 30), win_phys = -1;
         int k_issued = 0, v_issued = 0;
@@ -559,7 +565,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 for (int q = 0; q < kTcBlocks; ++q)
                     if (ph[q] >= 0) mask |= 1u << q, ++nval;
                 if (is_k) {
-                    cmask[c & 3] = mask;
+                    cmask[c & (kTcMasks - 1)] = mask;
                     mbar_arrive(bar_m(c));     // publishes the mask (release)
                 }
                 mbar_arrive_expect_tx(bar, (uint32_t)(nval * C::kVb));
@@ -576,7 +582,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                         if (lane == i) pq = ph[i];
                     if (pq >= 0) {
                         auto coord = [&](int which) { return which == 1 ? g : pq; };
-                        tma_load_5d(sV + (c & 1) * C::kVc + lane * C::kVb, &vmap, 0, 0, 0,
+                        tma_load_5d(sV + (c & 3) * C::kVc + lane * C::kVb, &vmap, 0, 0, 0,
                                     coord(a.page_perm[0]), coord(a.page_perm[1]), bar, pol);
                     }
                 }
@@ -589,7 +595,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
                 if (pq >= 0) {
                     auto coord = [&](int which) { return which == 0 ? 0 : (which == 1 ? g : pq); };
                     const int y = coord(a.map_perm[0]), z = coord(a.map_perm[1]), w = coord(a.map_perm[2]);
-                    const uint32_t base = is_k ? sK + (c & 1) * C::kKc : sV + (c & 1) * C::kVc;
+                    const uint32_t base = is_k ? sK + (c & 3) * C::kKc : sV + (c & 3) * C::kVc;
                     const uint32_t dst = is_k ? base + h * (kTcChunk * 128) + q * (kBlock * 128)
                                               : base + q * C::kVb + h * (kBlock * 128);
                     tma_load_4d(dst, is_k ? &kmap : &vmap, h * 64, y, z, w, bar, pol);
@@ -598,42 +604,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             if (is_k) ++k_issued;
             else ++v_issued;
         };
-        issue_kv(0, true);
-        issue_kv(0, false);
-        if (nchunks > 1) {
-            issue_kv(1, true);
-            issue_kv(1, false);
-        }
-        for (int c = 0; c + 2 < nchunks && ok; ++c) {
-            // S(c) has read K(c): its stage takes K(c+2); P(c).V(c) has read V(c):
-            // its stage takes V(c+2)
-            ok = __all_sync(kFull, mbar_wait(bar_s(c), par2(c)));
+        for (int c = 0; c < min(nchunks, kTcBufs); ++c) issue_kv(c, k_warp);
+        for (int c = 0; c + kTcBufs < nchunks && ok; ++c) {
+            // S(c) has read K(c): its stage takes K(c+4); P(c).V(c) has read V(c):
+            // its stage takes V(c+4). Each tensor has its own warp, so that K runs
+            // ahead of the P.V products.
+            ok = __all_sync(kFull, mbar_wait(k_warp ? bar_s(c) : bar_o(c), par4(c)));
             if (!ok) break;
-            issue_kv(c + 2, true);
-            ok = __all_sync(kFull, mbar_wait(bar_o(c), par2(c)));
-            if (!ok) break;
-            issue_kv(c + 2, false);
+            issue_kv(c + kTcBufs, k_warp);
         }
         if (!ok && lane == 0) {
             // let this CTA's copies land before the shared memory goes
             flag_error(a.err, GQA_DEVERR_TIMEOUT);
-            for (int c = max(0, k_issued - 2); c < k_issued; ++c) mbar_wait(bar_k(c), par2(c), kWaitLimitNs / 4);
-            for (int c = max(0, v_issued - 2); c < v_issued; ++c) mbar_wait(bar_v(c), par2(c), kWaitLimitNs / 4);
+            for (int c = max(0, k_issued - kTcBufs); c < k_issued; ++c) mbar_wait(bar_k(c), par4(c), kWaitLimitNs / 4);
+            for (int c = max(0, v_issued - kTcBufs); c < v_issued; ++c) mbar_wait(bar_v(c), par4(c), kWaitLimitNs / 4);
         }
     } else if (mma_warp) {
         // ================================================== MMA warp
-        auto issue_s = [&](int c) {            // S(c) = Q K(c)^T into buffer c & 1
-            const uint32_t kb = sK + (c & 1) * C::kKc;
+        auto issue_s = [&](int c) {            // S(c) = Q K(c)^T into buffer c & 1, Q from tensor memory
+            const uint32_t kb = sK + (c & 3) * C::kKc;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                const uint64_t ad = smem_desc_sw128(sQ + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
                 const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * (kTcChunk * 128) + (ks & 3) * 32, 16, 1024);
-                tc_mma_f16(tmem + (c & 1) * kColBuf, ad, bd, C::kIdescS, ks > 0);
+                tc_mma_f16_ta(tmem + (c & 1) * kColBuf, tmem + kColQ + 8 * ks, bd, C::kIdescS, ks > 0);
             }
         };
         int s_issued = 0, o_issued = 0;        // events committed (for the failure path)
         if (lane == 0) {
-            ok = mbar_wait(bar_k(0), par2(0));
+            ok = mbar_wait(bar_q, 0u) && mbar_wait(bar_k(0), par4(0));
             tc_fence_after();
             if (ok) issue_s(0);
             tc_commit(bar_s(0));               // S(0) done
@@ -644,8 +642,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             // S(c+1) first, so that it is ready when the softmax finishes S(c):
             // it goes over P(c-1), once P(c-1).V(c-1) has read it
             if (lane == 0 && c + 1 < nchunks) {
-                bool w = c == 0 || mbar_wait(bar_o(c - 1), par2(c - 1));
-                w = w && mbar_wait(bar_k(c + 1), par2(c + 1));
+                bool w = c == 0 || mbar_wait(bar_o(c - 1), par4(c - 1));
+                w = w && mbar_wait(bar_k(c + 1), par4(c + 1));
                 tc_fence_after();
                 if (w) issue_s(c + 1);
                 tc_commit(bar_s(c + 1));
@@ -655,13 +653,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             ok = __shfl_sync(kFull, ok, 0);
             if (!ok) break;
             // P(c) written over S(c), V(c) rows zeroed by the softmax warps
-            ok = __all_sync(kFull, mbar_wait(bar_p(c), par2(c)));
+            ok = __all_sync(kFull, mbar_wait(bar_p(c), par4(c)));
             if (!ok) break;
             if (lane == 0) {
                 tc_fence_after();
-                bool w = mbar_wait(bar_v(c), par2(c));
+                bool w = mbar_wait(bar_v(c), par4(c));
                 if (w) {
-                    const uint32_t vb = sV + (c & 1) * C::kVc;
+                    const uint32_t vb = sV + (c & 3) * C::kVc;
                     const uint32_t pb = tmem + (c & 1) * kColBuf;
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
@@ -682,8 +680,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             // let this CTA's MMAs land before the tensor memory goes, each
             // barrier's events in order
             flag_error(a.err, GQA_DEVERR_TIMEOUT);
-            for (int k = max(0, s_issued - 2); k < s_issued; ++k) mbar_wait(bar_s(k), par2(k), kWaitLimitNs / 4);
-            for (int k = max(0, o_issued - 2); k < o_issued; ++k) mbar_wait(bar_o(k), par2(k), kWaitLimitNs / 4);
+            for (int k = max(0, s_issued - kTcBufs); k < s_issued; ++k) mbar_wait(bar_s(k), par4(k), kWaitLimitNs / 4);
+            for (int k = max(0, o_issued - kTcBufs); k < o_issued; ++k) mbar_wait(bar_o(k), par4(k), kWaitLimitNs / 4);
         }
     } else {
         // ================================================== softmax warps: one row per thread
@@ -691,30 +689,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         float m = -INFINITY, l = 0.f;
         int c = 0;
         for (; c < nchunks; ++c) {
-            ok = __all_sync(kFull, mbar_wait(bar_s(c), par2(c)));   // S(c) done
-            ok = ok && __all_sync(kFull, mbar_wait(bar_m(c), (uint32_t)(c >> 2) & 1u));
+            ok = __all_sync(kFull, mbar_wait(bar_s(c), par4(c)));   // S(c) done
+            ok = ok && __all_sync(kFull, mbar_wait(bar_m(c), par8(c)));
             if (!ok) break;
             tc_fence_after();
             const int cpos = (jb_lo + kTcBlocks * c) * kBlock;
-            const uint32_t bm = cmask[c & 3];
+            const uint32_t bm = cmask[c & (kTcMasks - 1)];
             const uint32_t t_buf = t_lane + (uint32_t)(c & 1) * kColBuf;
             float sv[kTcChunk];
             {
-                uint32_t r0[16], r1[16], r2[16], r3[16];
-                tmem_ld16(t_buf, r0);
-                tmem_ld16(t_buf + 16, r1);
-                tmem_ld16(t_buf + 32, r2);
-                tmem_ld16(t_buf + 48, r3);
+                uint32_t r[kTcChunk / 16][16];
+#pragma unroll
+                for (int u = 0; u < kTcChunk / 16; ++u) tmem_ld16(t_buf + 16 * u, r[u]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    sv[j] = __uint_as_float(r0[j]) * a.scale_log2;
-                    sv[16 + j] = __uint_as_float(r1[j]) * a.scale_log2;
-                    sv[32 + j] = __uint_as_float(r2[j]) * a.scale_log2;
-                    sv[48 + j] = __uint_as_float(r3[j]) * a.scale_log2;
-                }
+                for (int u = 0; u < kTcChunk / 16; ++u)
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) sv[16 * u + j] = __uint_as_float(r[u][j]) * a.scale_log2;
             }
-            const bool whole = bm == 0xFu && cpos >= lo && cpos + kTcChunk <= hi;
+            const bool whole = bm == (1u << kTcBlocks) - 1u && cpos >= lo && cpos + kTcChunk <= hi;
             if (!whole) {
 #pragma unroll
                 for (int j = 0; j < kTcChunk; ++j) {
@@ -737,7 +730,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             l *= alpha;
             if (c > 0 && __any_sync(kFull, resc && old_live)) {       // O holds earlier chunks: scale it
                 // once P(c-1).V(c-1) has landed in it
-                ok = __all_sync(kFull, mbar_wait(bar_o(c - 1), par2(c - 1)));
+                ok = __all_sync(kFull, mbar_wait(bar_o(c - 1), par4(c - 1)));
                 if (!ok) break;
                 tc_fence_after();
                 const float f = (resc && old_live) ? alpha : 1.f;
@@ -754,7 +747,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             const float mu = m == -INFINITY ? 0.f : m;    // a row with nothing attended yet: p = 0
             float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int hq = 0; hq < 2; ++hq) {               // 32 tokens -> 16 packed columns each
+            for (int hq = 0; hq < kTcChunk / 32; ++hq) {   // 32 tokens -> 16 packed columns each
                 uint32_t ph16[16], pl16[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -770,9 +763,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             tmem_wait_st();
             l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
             // V rows of tokens outside the sequence or of missing blocks hold arbitrary bits
-            if (bm != 0xFu || cpos + kTcChunk > L) {
-                ok = __all_sync(kFull, mbar_wait(bar_v(c), par2(c)));
-                const uint32_t vb = sV + (c & 1) * C::kVc;
+            if (bm != (1u << kTcBlocks) - 1u || cpos + kTcChunk > L) {
+                ok = __all_sync(kFull, mbar_wait(bar_v(c), par4(c)));
+                const uint32_t vb = sV + (c & 3) * C::kVc;
                 for (int i = tid; i < kTcChunk * C::kHalves * 8; i += kTcRows) {
                     const int t = i / (C::kHalves * 8), h = (i / 8) % C::kHalves, ck = i % 8;
                     if (((bm >> (t / kBlock)) & 1u) && cpos + t < L) continue;
@@ -788,9 +781,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
             if (!ok) break;
         }
         // ---- wait for the last MMAs, then normalise and store this row
-        // the last P.V (P(n-3).V(n-3), the previous event on its barrier, landed
+        // the last P.V (P(n-5).V(n-5), the previous event on its barrier, landed
         // before S(n-1) was issued)
-        if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(nchunks - 1), par2(nchunks - 1)));
+        if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(nchunks - 1), par4(nchunks - 1)));
         tc_fence_after();
         if (ok) {
             // This warp's 32 rows leave through shared memory (Q and the K/V
