@@ -36,6 +36,7 @@ DEFAULT_WORKLOAD = "llama3_8b_bf16_b64_s4096"
 L2_BYTES = 129 * 2 ** 20
 KERNEL_NAME = "split_kv_kernel"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kv_kernel_traffic.txt")
+PREFILL_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "prefill_tc_kernel_traffic.txt")
 
 
 def attended_range(wl, L: int) -> tuple:
@@ -92,6 +93,7 @@ def algorithmic_bytes(wl, lens) -> dict:
 # other sources no longer describes it.
 SPLIT_KV_SOURCES = ("gqa_decode_kernels.cuh", "gqa_device.cuh", "gqa_internal.h", "gqa_decode.cu",
                     "gqa_decode_general.cu")
+PREFILL_SOURCES = ("gqa_prefill.cu", "gqa_device.cuh", "gqa_internal.h")
 
 
 def kernel_source_hash(files=SPLIT_KV_SOURCES) -> str:
@@ -104,15 +106,15 @@ def kernel_source_hash(files=SPLIT_KV_SOURCES) -> str:
     return h.hexdigest()[:16]
 
 
-def read_traffic(workload: str, kernel: str):
-    """DRAM bytes per launch from the committed ncu summary (blocks of
+def read_traffic(workload: str, kernel: str, path: str = TRAFFIC_FILE, sources=SPLIT_KV_SOURCES):
+    """DRAM bytes per launch from a committed ncu summary (blocks of
     'key: value' lines separated by blank lines, one per workload), if one was
-    taken on the current kernel source for this workload; else None."""
+    taken on the current source of that kernel for this workload; else None."""
     try:
-        text = open(TRAFFIC_FILE).read()
+        text = open(path).read()
     except OSError:
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(sources)
     for block in text.split("\n\n"):
         vals = {}
         for ln in block.splitlines():
@@ -418,8 +420,9 @@ def run_prefill(args, wl):
                        "step": "kv_append_varlen + gqa_prefill, one attention layer"},
             "tokens_per_s": round(B * T * world / (ms * 1e-3), 1),
             "roofline": {"bound": "tensor", "achieved": round(kern_tf, 2), "peak": peak,
-                         "unit": "TFLOP/s", "frac": round(kern_tf / peak, 4), "traffic": None,
-                         "kernel": "prefill_kernel", "algorithmic_flops_per_launch": flops,
+                         "unit": "TFLOP/s", "frac": round(kern_tf / peak, 4),
+                         "traffic": read_traffic(wl.name, "auto", PREFILL_TRAFFIC_FILE, PREFILL_SOURCES),
+                         "kernel": "prefill_tc_kernel", "algorithmic_flops_per_launch": flops,
                          "avg_launch_ms": round(kern_ms, 5),
                          "kernel_timing": "CUDA events around every prefill launch, own timed loop",
                          "peak_source": f"{peak_kind} bf16_tflops (burst, cuBLAS; MEASURED_PEAKS.json)"},
