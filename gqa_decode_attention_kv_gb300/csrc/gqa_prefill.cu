@@ -386,7 +386,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 // buffer once P(c-1).V(c-1) has read it, before it waits for P(c). K and V have
 // four shared stages each: K(c+4) loads once S(c) has read K(c), V(c+4) once
 // P(c).V(c) has read V(c). The epilogue writes whole output rows through the
-// idle Q/K/V stages. Two CTAs share an SM (~97 KB of shared memory and 256
+// idle shared stages. Two CTAs share an SM (~100 KB of shared memory and 256
 // tensor-memory columns each).
 
 constexpr int kTcRows = 128;                 // query rows per CTA = M = TMEM lanes
@@ -786,8 +786,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
         if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(nchunks - 1), par4(nchunks - 1)));
         tc_fence_after();
         if (ok) {
-            // This warp's 32 rows leave through shared memory (Q and the K/V
-            // stages are idle now: every copy has landed and every MMA is done),
+            // This warp's 32 rows leave through shared memory (the staging area
+            // and the K/V stages are idle now: every copy has landed and every
+            // MMA is done),
             // so that each store writes whole rows: one lane per 4 dims of a row.
             const float inv = l > 0.f ? 1.f / l : 0.f;
             constexpr int kRowF = D + 4;       // padded row: 16-byte stores stay conflict-free
