@@ -197,8 +197,25 @@ def _stream_ptr(stream) -> Optional[int]:
     return s.cuda_stream
 
 
-def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else t.data_ptr()
+def _dev(t: Optional[torch.Tensor], name: str, index: bool = False, optional: bool = False):
+    """Device pointer of a tensor the library reads or writes as a packed array.
+
+    The C ABI sees a bare pointer, so what it cannot check is checked here:
+    the tensor must be contiguous, an index array must be int32, and the memory
+    must be on a CUDA device."""
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (the library reads it as a packed array)")
+    if index and t.dtype != torch.int32:
+        raise ValueError(f"{name} must be int32, not {t.dtype}")
+    if not index and t.dtype not in DTYPE_CODE and t.dtype != torch.uint8:
+        raise ValueError(f"{name} has unsupported dtype {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t.data_ptr()
 
 
 def _check(status: int, where: str):
@@ -212,11 +229,12 @@ def kv_append(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tensor,
     """Write k_new/v_new [B, K, d] (one token) or [B, T, K, d] (T tokens) at
     positions positions[b] .. positions[b]+T-1 of each sequence's paged cache."""
     T = 1 if k_new.dim() == 3 else int(k_new.shape[1])
+    args = (_dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(block_tables, "block_tables", True),
+            _dev(positions, "positions", True), _dev(err, "err", True, True))
     desc = cache.desc()
-    st = load().gqa_kv_append(ctypes.byref(desc), _ptr(k_new), _ptr(v_new),
-                              DTYPE_CODE[k_new.dtype], _ptr(block_tables),
-                              int(block_tables.shape[1]), _ptr(positions), int(positions.shape[0]),
-                              T, _ptr(err), _stream_ptr(stream))
+    st = load().gqa_kv_append(ctypes.byref(desc), args[0], args[1], DTYPE_CODE[k_new.dtype], args[2],
+                              int(block_tables.shape[1]), args[3], int(positions.shape[0]),
+                              T, args[4], _stream_ptr(stream))
     _check(st, "gqa_kv_append")
 
 
@@ -258,19 +276,22 @@ def gqa_decode(cache: PagedKVCache, q: torch.Tensor, block_tables: torch.Tensor,
     positions. ``out`` has q's shape."""
     T = 1 if q.dim() == 3 else int(q.shape[1])
     B, H, d = q.shape[0], q.shape[-2], q.shape[-1]
+    qp, tp, lp = _dev(q, "q"), _dev(block_tables, "block_tables", True), _dev(context_lens, "context_lens", True)
+    ep = _dev(err, "err", True, True)
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     if workspace is None:
         workspace = workspace_for(B, H, cache.num_kv_heads, d, q.device, T)
+    op, wp = _dev(out, "out"), _dev(workspace, "workspace")
     opts = DecodeOpts(T, window, kernel, max_warps, min_blocks_per_warp, row_layout, None, None)
     if events is not None:
         opts.event_main_begin = events[0].cuda_event
         opts.event_main_end = events[1].cuda_event
     desc = cache.desc()
-    st = load().gqa_decode(ctypes.byref(desc), _ptr(q), DTYPE_CODE[q.dtype], H, _ptr(block_tables),
-                           int(block_tables.shape[1]), _ptr(context_lens), B, float(scale),
-                           _ptr(out), DTYPE_CODE[out.dtype], _ptr(workspace), workspace.numel(),
-                           ctypes.byref(opts), _ptr(err), _stream_ptr(stream))
+    st = load().gqa_decode(ctypes.byref(desc), qp, DTYPE_CODE[q.dtype], H, tp,
+                           int(block_tables.shape[1]), lp, B, float(scale),
+                           op, DTYPE_CODE[out.dtype], wp, workspace.numel() * workspace.element_size(),
+                           ctypes.byref(opts), ep, _stream_ptr(stream))
     _check(st, "gqa_decode")
     return out
 
@@ -287,14 +308,17 @@ def gqa_decode_noalloc(cache: PagedKVCache, q: torch.Tensor, block_tables: torch
     overlap on the GPU share one scratch array and race."""
     T = 1 if q.dim() == 3 else int(q.shape[1])
     B, H, d = q.shape[0], q.shape[-2], q.shape[-1]
+    qp, tp, lp = _dev(q, "q"), _dev(block_tables, "block_tables", True), _dev(context_lens, "context_lens", True)
+    ep = _dev(err, "err", True, True)
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    op = _dev(out, "out")
     opts = DecodeOpts(T, window, kernel, 0, 0, 0, None, None)
     desc = cache.desc()
-    st = load().gqa_decode_noalloc(ctypes.byref(desc), _ptr(q), DTYPE_CODE[q.dtype], H,
-                                   _ptr(block_tables), int(block_tables.shape[1]),
-                                   _ptr(context_lens), B, float(scale), _ptr(out),
-                                   DTYPE_CODE[out.dtype], ctypes.byref(opts), _ptr(err),
+    st = load().gqa_decode_noalloc(ctypes.byref(desc), qp, DTYPE_CODE[q.dtype], H,
+                                   tp, int(block_tables.shape[1]),
+                                   lp, B, float(scale), op,
+                                   DTYPE_CODE[out.dtype], ctypes.byref(opts), ep,
                                    _stream_ptr(stream))
     _check(st, "gqa_decode_noalloc")
     return out
@@ -305,11 +329,14 @@ def kv_append_varlen(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tens
                      positions: torch.Tensor, err: Optional[torch.Tensor] = None, stream=None) -> None:
     """Write rows token_start[b] .. token_start[b+1]-1 of k_new/v_new [total, K, d] at
     positions positions[b], positions[b]+1, ... of sequence b."""
+    args = (_dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(token_start, "token_start", True),
+            _dev(block_tables, "block_tables", True), _dev(positions, "positions", True),
+            _dev(err, "err", True, True))
     desc = cache.desc()
-    st = load().gqa_kv_append_varlen(ctypes.byref(desc), _ptr(k_new), _ptr(v_new),
-                                     DTYPE_CODE[k_new.dtype], _ptr(token_start), int(max_new_tokens),
-                                     _ptr(block_tables), int(block_tables.shape[1]), _ptr(positions),
-                                     int(positions.shape[0]), _ptr(err), _stream_ptr(stream))
+    st = load().gqa_kv_append_varlen(ctypes.byref(desc), args[0], args[1],
+                                     DTYPE_CODE[k_new.dtype], args[2], int(max_new_tokens),
+                                     args[3], int(block_tables.shape[1]), args[4],
+                                     int(positions.shape[0]), args[5], _stream_ptr(stream))
     _check(st, "gqa_kv_append_varlen")
 
 
@@ -321,14 +348,17 @@ def gqa_prefill(cache: PagedKVCache, q: torch.Tensor, q_start: torch.Tensor, max
     """Causal attention of each sequence's new tokens (rows q_start[b] .. of q
     [total, H, d]) over its paged cache, new tokens included. kernel: 0/1
     tcgen05 (tensor memory), 2 warp-level mma.sync."""
+    args = (_dev(q, "q"), _dev(q_start, "q_start", True), _dev(block_tables, "block_tables", True),
+            _dev(context_lens, "context_lens", True), _dev(err, "err", True, True))
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    op = _dev(out, "out")
     desc = cache.desc()
     B = int(context_lens.shape[0])
-    st = load().gqa_prefill(ctypes.byref(desc), _ptr(q), DTYPE_CODE[q.dtype], int(q.shape[1]),
-                            _ptr(q_start), int(max_new_tokens), _ptr(block_tables),
-                            int(block_tables.shape[1]), _ptr(context_lens), B, float(scale), int(window),
-                            _ptr(out), DTYPE_CODE[out.dtype], int(kernel), _ptr(err), _stream_ptr(stream))
+    st = load().gqa_prefill(ctypes.byref(desc), args[0], DTYPE_CODE[q.dtype], int(q.shape[1]),
+                            args[1], int(max_new_tokens), args[2],
+                            int(block_tables.shape[1]), args[3], B, float(scale), int(window),
+                            op, DTYPE_CODE[out.dtype], int(kernel), args[4], _stream_ptr(stream))
     _check(st, "gqa_prefill")
     return out
 

@@ -143,3 +143,29 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gbuild, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         gq.load()
+
+
+def test_binding_rejects_arrays_the_library_cannot_read():
+    """The C ABI sees bare pointers; the binding refuses what they cannot
+    describe: strided views, index arrays that are not int32, host memory."""
+    import torch
+    with pytest.raises(ValueError, match="contiguous"):
+        gq._dev(torch.zeros(4, 6).t(), "q")
+    with pytest.raises(ValueError, match="int32"):
+        gq._dev(torch.zeros(4, dtype=torch.int64), "context_lens", index=True)
+    with pytest.raises(ValueError, match="dtype"):
+        gq._dev(torch.zeros(4, dtype=torch.float64), "q")
+    with pytest.raises(ValueError, match="CUDA"):
+        gq._dev(torch.zeros(4, dtype=torch.int32), "context_lens", index=True)
+    with pytest.raises(ValueError, match="required"):
+        gq._dev(None, "q")
+    assert gq._dev(None, "err", index=True, optional=True) is None
+    # the public calls check before they touch the cache or the library
+    q = torch.zeros(3, 8, 64, dtype=torch.bfloat16)
+    lens = torch.zeros(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        gq.gqa_prefill(None, q, lens, 3, lens.reshape(1, 1), lens, 0.125)
+    with pytest.raises(ValueError, match="contiguous"):
+        gq.gqa_decode(None, q.transpose(0, 1), lens.reshape(1, 1), lens, 0.125)
+    with pytest.raises(ValueError, match="contiguous"):
+        gq.kv_append(None, q.transpose(0, 1), q, lens.reshape(1, 1), lens)
