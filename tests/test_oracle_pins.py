@@ -545,6 +545,39 @@ def test_generator_poisons_only_unowned_slots(oracle_mod):
     assert np.count_nonzero(~np.isnan(pool)) == owned * 2 * 16
 
 
+@pytest.mark.parametrize("dtype,code_lo,code_hi,s_lo,s_hi", [
+    ("i8", -127, 127, 0.015, 0.035), ("fp8", -448.0, 448.0, 0.006, 0.010),
+    ("i4", -7, 7, 0.35, 0.50), ("i4kc", -7, 7, 0.35, 0.50),
+])
+def test_generator_recipe(oracle_mod, dtype, code_lo, code_hi, s_lo, s_hi):
+    """The seeded inputs are what the input recipe states: a shuffled table that
+    hands every physical block to one sequence, codes and scales in the stated
+    ranges, NaN scales on the slots no sequence holds, and the same case for
+    the same seed."""
+    lens = [5, 16, 33, 0]
+    case = gi.make_case(4, 8, 2, 128, lens, dtype, seed=7)
+    table = case.block_table.numpy()
+    owned = table[table >= 0]
+    assert sorted(owned.tolist()) == list(range(case.num_blocks))    # each block exactly once
+    assert not np.array_equal(owned, np.sort(owned))                  # and shuffled
+    if dtype in ("i4", "i4kc"):
+        codes = oracle_mod.unpack_int4(case.v_cache.numpy())
+    elif dtype == "fp8":
+        codes = oracle_mod.e4m3_to_f64(case.v_cache.view(torch.uint8).numpy())
+    else:
+        codes = case.v_cache.numpy()
+    assert codes.min() >= code_lo and codes.max() <= code_hi
+    vs = case.v_scale.float().numpy()
+    held = oracle_mod.gather_scales(vs, table, np.array(lens), 2)
+    for b, L in enumerate(lens):
+        assert np.isfinite(held[b, :L]).all()
+        assert ((held[b, :L] >= s_lo - 1e-3) & (held[b, :L] <= s_hi + 1e-3)).all()
+    assert np.isnan(vs).sum() == (case.num_blocks * 16 - sum(lens)) * 2     # the rest are poisoned
+    again = gi.make_case(4, 8, 2, 128, lens, dtype, seed=7)
+    for x, y in ((case.q, again.q), (case.k_cache, again.k_cache), (case.v_scale, again.v_scale)):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+
+
 # --------------------------------------------------------------------------- fp8 (e4m3)
 
 
