@@ -284,6 +284,53 @@ def test_append_then_gather_round_trips_through_a_shuffled_pool(oracle_mod):
     assert np.count_nonzero(~np.isnan(pool)) == B * S * K * d
 
 
+def _labelled_scale_pool(nb, K):
+    """[nb, K, 16] pool whose entry (block p, kv-head g, slot s) holds 1000*p + 100*g + s,
+    so every gathered value names the slot it came from."""
+    return np.array([[[1000 * p + 100 * g + s for s in range(16)] for g in range(K)]
+                     for p in range(nb)], dtype=np.int64)
+
+
+def test_scale_gather_reads_the_slots_the_table_names(oracle_mod):
+    """Per-(token, kv-head) scales gathered through a shuffled table, checked
+    against expected values written out by hand: sequence 0 holds 18 tokens in
+    blocks 2 then 0, sequence 1 holds 3 tokens in block 3."""
+    pool = _labelled_scale_pool(4, 2)
+    table = np.array([[2, 0], [3, -1]], dtype=np.int32)
+    got = oracle_mod.gather_scales(pool, table, [18, 3], 2)
+    assert got.shape == (2, 18, 2)
+    seq0_head0 = list(range(2000, 2016)) + [0, 1]
+    seq0_head1 = list(range(2100, 2116)) + [100, 101]
+    seq1_head0 = [3000, 3001, 3002] + [0] * 15          # past the length: left at zero
+    seq1_head1 = [3100, 3101, 3102] + [0] * 15
+    np.testing.assert_array_equal(got[0, :, 0], seq0_head0)
+    np.testing.assert_array_equal(got[0, :, 1], seq0_head1)
+    np.testing.assert_array_equal(got[1, :, 0], seq1_head0)
+    np.testing.assert_array_equal(got[1, :, 1], seq1_head1)
+    # a subset of rows, in the order asked for
+    sub = oracle_mod.gather_scales(pool, table, [18, 3], 2, batch_index=[1])
+    assert sub.shape == (1, 3, 2)
+    np.testing.assert_array_equal(sub[0], [[3000, 3100], [3001, 3101], [3002, 3102]])
+
+
+def test_scale_append_writes_only_the_named_slot(oracle_mod):
+    """Appending at positions 17 and 2 writes block table[0][1] = 0, slot 1 and
+    block table[1][0] = 3, slot 2, for both kv-heads, and nothing else."""
+    pool = _labelled_scale_pool(4, 2)
+    before = pool.copy()
+    table = np.array([[2, 0], [3, -1]], dtype=np.int32)
+    new = np.array([[-7, -8], [-9, -10]], dtype=np.int64)         # [B, K]
+    oracle_mod.append_scales(pool, new, table, [17, 2])
+    expect = before.copy()
+    expect[0, 0, 1], expect[0, 1, 1] = -7, -8
+    expect[3, 0, 2], expect[3, 1, 2] = -9, -10
+    np.testing.assert_array_equal(pool, expect)
+    # and the gather sees the new values at those positions
+    got = oracle_mod.gather_scales(pool, table, [18, 3], 2)
+    np.testing.assert_array_equal(got[0, 17], [-7, -8])
+    np.testing.assert_array_equal(got[1, 2], [-9, -10])
+
+
 def test_block_padding_example_from_the_pages(oracle_mod):
     with open(os.path.join(GOLDEN, "block_padding.json")) as f:
         gold = json.load(f)
@@ -576,6 +623,70 @@ def test_generator_recipe(oracle_mod, dtype, code_lo, code_hi, s_lo, s_hi):
     again = gi.make_case(4, 8, 2, 128, lens, dtype, seed=7)
     for x, y in ((case.q, again.q), (case.k_cache, again.k_cache), (case.v_scale, again.v_scale)):
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+
+
+@pytest.mark.parametrize("dtype", ["i8", "fp8", "i4", "i4kc"])
+def test_generator_normal_source_recipe(dtype):
+    """source="normal": unquantised K/V rows N(0, 1) in fp32, one per cached
+    token, packed by sequence; the cache itself is left for the consumer to
+    fill (codes zero, every scale NaN), and the same seed gives the same rows."""
+    lens = [5, 16, 33, 0, 300]
+    case = gi.make_case(5, 8, 2, 128, lens, dtype, seed=9, source="normal")
+    assert case.k_src.shape == (sum(lens), 2, 128) and case.k_src.dtype == torch.float32
+    assert case.v_src.shape == case.k_src.shape
+    assert case.src_start.tolist() == [0, 5, 21, 54, 54, 354]
+    for src in (case.k_src, case.v_src):
+        assert abs(float(src.mean())) < 0.02 and abs(float(src.std()) - 1.0) < 0.02
+    assert not torch.equal(case.k_src, case.v_src)
+    assert not case.k_cache.view(torch.uint8).any() and not case.v_cache.view(torch.uint8).any()
+    assert torch.isnan(case.k_scale).all() and torch.isnan(case.v_scale).all()
+    again = gi.make_case(5, 8, 2, 128, lens, dtype, seed=9, source="normal")
+    assert torch.equal(case.k_src, again.k_src) and torch.equal(case.v_src, again.v_src)
+    wl = gi.WORKLOADS["int8kv_b128_ragged"]
+    assert wl.source == "normal" and wl.cache_dtype == "i8"
+
+
+def test_quantised_sequence_per_token_rules(oracle_mod):
+    """Rows of one sequence quantise independently by the per-token rules: each
+    row's largest magnitude lands on the top code (+-127, +-448, +-7) and every
+    value is within half a step of its input."""
+    rng = np.random.default_rng(51)
+    x = rng.standard_normal((21, 3, 64)).astype(np.float32)
+    for dtype, top in (("i8", 127), ("fp8", 448), ("i4", 7)):
+        vals, codes, sbits = oracle_mod.quantised_sequence(x, dtype)
+        assert vals.shape == x.shape and sbits.shape == (21, 3)
+        s = oracle_mod.f16_bits_value(sbits)
+        assert np.all(s > 0)
+        arg = np.abs(x).argmax(axis=-1)
+        top_vals = np.take_along_axis(vals, arg[..., None], -1)[..., 0]
+        np.testing.assert_allclose(np.abs(top_vals), top * s, rtol=0, atol=0)
+        if dtype == "fp8":
+            # e4m3 spacing near |x|/s is at most 2^-3 of it: relative error <= 1/16
+            assert np.all(np.abs(vals - x) <= np.abs(x) / 16 + s[..., None] * 2.0 ** -9)
+        else:
+            assert np.all(np.abs(vals - x) <= s[..., None] / 2 * (1 + 1e-3))
+
+
+def test_quantised_sequence_per_channel_matches_token_by_token_appends(oracle_mod):
+    """The KIVI-style K written from position 0 in one go equals 37 single-token
+    appends through a shuffled pool (the last block left partial): same codes,
+    same per-(block, channel) scales."""
+    rng = np.random.default_rng(52)
+    K, d, L = 2, 8, 37
+    x = rng.standard_normal((L, K, d)).astype(np.float32)
+    _, codes, sbits = oracle_mod.quantised_sequence(x, "i4kc", per_channel=True)
+    assert codes.shape == (L, K, d) and sbits.shape == (3, K, d)
+    table = np.array([[5, 0, 2]], dtype=np.int32)
+    sb_, sh_, st_ = K * 16 * d, 16 * d, d
+    pool = np.zeros(6 * sb_ // 2, dtype=np.uint8)
+    scales = np.zeros((6, K, d), dtype=np.uint16)
+    resid = np.zeros((1, K, 16, d), dtype=np.float32)
+    for pos in range(L):
+        oracle_mod.append_int4_channels(pool, scales, resid, [x[pos:pos + 1]], table, [pos], [1],
+                                        sb_, sh_, st_)
+    dense = oracle_mod.gather_dense(pool, table, [L], sb_ // 2, sh_ // 2, st_ // 2, K, d // 2)[0]
+    np.testing.assert_array_equal(oracle_mod.unpack_int4(dense), codes)
+    np.testing.assert_array_equal(scales[table[0]], sbits)
 
 
 # --------------------------------------------------------------------------- fp8 (e4m3)
