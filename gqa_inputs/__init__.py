@@ -55,6 +55,10 @@ class Workload:
     queries: int = 1            # new tokens per sequence (causal among themselves)
     window: int = 0             # sliding window in tokens; 0 = full attention
     kind: str = "decode"        # "decode" (gqa_decode) or "prefill" (gqa_prefill: queries = prompt)
+    # code caches: "codes" = codes and scales drawn directly (ranges in make_case);
+    # "normal" = K/V rows drawn N(0, 1) in fp32 and left for the consumer to
+    # quantise into the cache (make_case's ``source``)
+    source: str = "codes"
 
     @property
     def group_size(self) -> int:
@@ -74,15 +78,16 @@ WORKLOADS = {
                                          "bf16", "bf16", "const:131072"),
     "long_ctx_bf16_b4_s131072": Workload("long_ctx_bf16_b4_s131072", 4, 32, 8, 128,
                                          "bf16", "bf16", "const:131072"),
+    # K/V drawn N(0, 1), then quantised per (token, kv-head) into the cache
     "int8kv_b128_ragged": Workload("int8kv_b128_ragged", 128, 64, 8, 128, "i8", "bf16",
-                                   "uniform:2048:8192"),
+                                   "uniform:2048:8192", source="normal"),
     "fp8kv_b128_ragged": Workload("fp8kv_b128_ragged", 128, 64, 8, 128, "fp8", "bf16",
-                                  "uniform:2048:8192"),
+                                  "uniform:2048:8192", source="normal"),
     "int4kv_b128_ragged": Workload("int4kv_b128_ragged", 128, 64, 8, 128, "i4", "bf16",
-                                   "uniform:2048:8192"),
+                                   "uniform:2048:8192", source="normal"),
     # KIVI-style 4-bit cache (K per channel, V per token), same shape
     "int4kc_b128_ragged": Workload("int4kc_b128_ragged", 128, 64, 8, 128, "i4kc", "bf16",
-                                   "uniform:2048:8192"),
+                                   "uniform:2048:8192", source="normal"),
     # four new tokens per sequence (speculative verification of three drafts),
     # Llama-3-8B shape; the lengths include the new tokens
     "spec_verify_bf16_b64_s4096_t4": Workload("spec_verify_bf16_b64_s4096_t4", 64, 32, 8, 128,
@@ -147,6 +152,12 @@ class DecodeCase:
     v_new: torch.Tensor
     queries: int = 1                # T new tokens per sequence
     k_residual: Optional[torch.Tensor] = None   # i4kc: fp32 [B, K, 16, d], unquantised K of the open block
+    # source="normal" code caches: the unquantised rows the cache is to hold,
+    # fp32 [sum(lens), K, d], rows src_start[b] .. src_start[b+1]-1 being
+    # positions 0 .. lens[b]-1 of sequence b (codes and scales still empty)
+    k_src: Optional[torch.Tensor] = None
+    v_src: Optional[torch.Tensor] = None
+    src_start: Optional[torch.Tensor] = None    # [B+1] int32
 
     @property
     def max_blocks(self) -> int:
@@ -162,7 +173,8 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
               q_dtype: Optional[str] = None, seed: int = 0, device: str = "cpu",
               contiguous: bool = False, shuffle: bool = True, spare_blocks: int = 0,
               extra_tokens: int = 0, max_blocks: Optional[int] = None, poison: bool = True,
-              new_dtype: Optional[str] = None, q_zero: bool = False, queries: int = 1) -> DecodeCase:
+              new_dtype: Optional[str] = None, q_zero: bool = False, queries: int = 1,
+              source: str = "codes") -> DecodeCase:
     """Draw one seeded decode case.
 
     ``lens`` are the lengths the decode attends to. Sequence ``b`` owns
@@ -180,7 +192,14 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
     [0.35, 0.50], and an fp32 residual [B, K, 16, d] of N(0,1) draws standing
     for the unquantised K of each sequence's open block (drawn independently
     of that block's codes: decode reads only codes and scales, an append
-    re-quantises the block from the residual)."""
+    re-quantises the block from the residual).
+
+    ``source="normal"`` (code caches only) draws instead the unquantised K/V
+    rows of every cached token, N(0, 1) in fp32, packed ``[sum(lens), K, d]``
+    in ``k_src``/``v_src`` with row offsets ``src_start``: the codes are left
+    zero and every scale NaN until the consumer quantises the rows into the
+    cache (the CUDA path through its append, the oracle with its own rule);
+    a slot the quantisation does not reach keeps its NaN scale."""
     if q_dtype is None:
         q_dtype = "bf16" if cache_dtype in CODED else cache_dtype
     if new_dtype is None:
@@ -194,6 +213,9 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
         max_blocks = max([1] + own)
     if max(own, default=0) > max_blocks:
         raise ValueError("max_blocks is smaller than a sequence's block count")
+    if source not in ("codes", "normal"):
+        raise ValueError(f"unknown source {source!r}")
+    normal = source == "normal" and cache_dtype in CODED
     gen_cpu = torch.Generator().manual_seed(seed)
     dev = torch.device(device)
     gen_dev = gen_cpu if dev.type == "cpu" else torch.Generator(device=dev).manual_seed(seed)
@@ -217,7 +239,15 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
         shape = (num_blocks, K, bs, d)
         sb, sh, st = K * bs * d, bs * d, d
 
-    if cache_dtype == "i8":
+    if normal:
+        es_shape = shape[:-1] + (d // 2,) if cache_dtype in PACKED4 else shape
+        kc = torch.zeros(es_shape, dtype=DTYPES[cache_dtype], device=dev)
+        vc = torch.zeros_like(kc)
+        sshape = (num_blocks, K, bs)
+        kshape = (num_blocks, K, d) if cache_dtype == "i4kc" else sshape
+        ks = torch.full(kshape, float("nan"), dtype=torch.float16, device=dev)
+        vs = torch.full(sshape, float("nan"), dtype=torch.float16, device=dev)
+    elif cache_dtype == "i8":
         kc = torch.randint(-127, 128, shape, generator=gen_dev, device=dev, dtype=torch.int8)
         vc = torch.randint(-127, 128, shape, generator=gen_dev, device=dev, dtype=torch.int8)
         sshape = (num_blocks, K, bs)
@@ -248,8 +278,16 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
         vc = _randn(shape, gen_dev, dev, dt)
         ks = vs = None
 
-    if poison:
+    if poison and not normal:
         _poison_unowned(kc, vc, ks, vs, table, lens_t, contiguous, cache_dtype)
+    k_src = v_src = src_start = None
+    if normal:
+        total = int(lens_t.sum())
+        k_src = _randn((total, K, d), gen_dev, dev, torch.float32)
+        v_src = _randn((total, K, d), gen_dev, dev, torch.float32)
+        src_start = torch.zeros(batch + 1, dtype=torch.int32)
+        src_start[1:] = torch.cumsum(lens_t, 0)
+        src_start = src_start.to(dev)
 
     tq = (queries,) if queries > 1 else ()
     q = _randn((batch, *tq, num_heads, d), gen_dev, dev, DTYPES[q_dtype])
@@ -257,10 +295,13 @@ def make_case(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
         q.zero_()
     k_new = _randn((batch, *tq, K, d), gen_dev, dev, DTYPES[new_dtype])
     v_new = _randn((batch, *tq, K, d), gen_dev, dev, DTYPES[new_dtype])
-    res = _randn((batch, K, bs, d), gen_dev, dev, torch.float32) if cache_dtype == "i4kc" else None
+    res = None
+    if cache_dtype == "i4kc":
+        res = (torch.zeros((batch, K, bs, d), dtype=torch.float32, device=dev) if normal
+               else _randn((batch, K, bs, d), gen_dev, dev, torch.float32))
     return DecodeCase(batch, num_heads, K, d, cache_dtype, q_dtype, 1.0 / math.sqrt(d),
                       q, kc, vc, ks, vs, num_blocks, sb, sh, st, table.to(dev),
-                      lens_t.to(dev), k_new, v_new, queries, res)
+                      lens_t.to(dev), k_new, v_new, queries, res, k_src, v_src, src_start)
 
 
 def _poison_unowned(kc, vc, ks, vs, table, lens, contiguous, cache_dtype):
@@ -300,4 +341,4 @@ def case_for(workload: Workload, seed: int = 0, device: str = "cpu", **kw) -> De
     return make_case(workload.batch, workload.num_heads, workload.num_kv_heads,
                      workload.head_dim, lens, workload.cache_dtype, workload.q_dtype,
                      seed=seed, device=device, contiguous=workload.contiguous,
-                     queries=workload.queries, **kw)
+                     queries=workload.queries, **{"source": workload.source, **kw})

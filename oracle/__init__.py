@@ -22,6 +22,9 @@ Functions and the passages they follow:
 * ``quantize_int4_channels`` / ``gather_channel_scales`` / ``append_int4_channels``
                          -- the KIVI-style K cache of section 15.5 (K per channel, V per
                             token, INT4): one scale per (block, kv-head, channel).
+* ``quantised_sequence`` -- what a code cache holds for one sequence's K or V rows
+                            written from position 0 (the rules above, row by row or,
+                            for the KIVI-style K, block by block per channel).
 * ``kv_cache_elements``  -- the KV-size closed form 2 * layers * K * d * S * B,
                             "分组查询注意力 (GQA)" 关键参数 item 2 and
                             "LLM 推理性能优化实战" section 6.1.
@@ -376,6 +379,48 @@ def dequantize_int8(codes, scale_values) -> np.ndarray:
     c = np.asarray(codes, dtype=np.float64)
     s = np.asarray(scale_values, dtype=np.float64)
     return c * s[..., None]
+
+
+def f16_bits_value(bits) -> np.ndarray:
+    """fp16 bit patterns as fp64 values (numpy's binary16 decode; exact)."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def quantised_sequence(rows, cache_dtype: str, per_channel: bool = False):
+    """Codes, scales and exact values a code cache holds for the rows [L, K, d]
+    of one sequence written at positions 0 .. L-1.
+
+    cache_dtype "i8" / "fp8" / "i4": one fp16 scale per (token, kv-head), the
+    rules of ``quantize_int8`` / ``quantize_fp8`` / ``quantize_int4``.
+    ``per_channel`` (the K of the KIVI-style cache, "i4kc"): each 16-token
+    block of each kv-head is quantised per channel over the tokens it holds
+    (``quantize_int4_channels``); the last block may be partial.
+    Returns (values fp64 [L, K, d], codes [L, K, d] (int8, or uint8 e4m3
+    codes), scale bits uint16 ([L, K], or [ceil(L/16), K, d] per channel))."""
+    x = np.ascontiguousarray(np.asarray(rows, dtype=np.float32))
+    L, K, d = x.shape
+    if per_channel:
+        nblk = -(-L // BLOCK_SIZE)
+        codes = np.zeros((L, K, d), dtype=np.int8)
+        sbits = np.zeros((nblk, K, d), dtype=np.uint16)
+        for jb in range(nblk):
+            t0, t1 = jb * BLOCK_SIZE, min(L, (jb + 1) * BLOCK_SIZE)
+            for g in range(K):
+                c, s = quantize_int4_channels(x[t0:t1, g])
+                codes[t0:t1, g] = c
+                sbits[jb, g] = s
+        per_tok = np.repeat(f16_bits_value(sbits), BLOCK_SIZE, axis=0)[:L]      # [L, K, d]
+        return codes.astype(np.float64) * per_tok, codes, sbits
+    if cache_dtype == "i8":
+        codes, sbits = quantize_int8(x)
+        return dequantize_int8(codes, f16_bits_value(sbits)), codes, sbits
+    if cache_dtype == "fp8":
+        codes, sbits = quantize_fp8(x)
+        return dequantize_fp8(codes, f16_bits_value(sbits)), codes, sbits
+    if cache_dtype in ("i4", "i4kc"):
+        codes, sbits = quantize_int4(x)
+        return dequantize_int8(codes, f16_bits_value(sbits)), codes, sbits
+    raise ValueError(f"not a code cache: {cache_dtype!r}")
 
 
 def kv_cache_elements(layers: int, kv_heads: int, head_dim: int, seq_len: int,

@@ -64,6 +64,64 @@ def oracle_for_case(case, rows=None, nthreads: int = 0, host_pools=None, window:
     return oracle.decode(q, kd, vd, lens[rows], case.scale, nthreads, window=window)
 
 
+def source_rows(case, b):
+    """Host copies of sequence b's unquantised K and V rows ([L, K, d] fp32) of a
+    case drawn with source="normal"."""
+    st = case.src_start.cpu()
+    lo, hi = int(st[b]), int(st[b + 1])
+    return case.k_src[lo:hi].cpu().numpy(), case.v_src[lo:hi].cpu().numpy()
+
+
+def fill_from_source(gq, case):
+    """Quantise a source="normal" case's rows into its device cache with the
+    library's varlen append (every sequence written from position 0)."""
+    lens = case.context_lens
+    zeros = torch.zeros_like(lens)
+    gq.kv_append_varlen(gq.cache_from_case(case), case.k_src, case.v_src, case.src_start,
+                        int(lens.max().item()) if lens.numel() else 0, case.block_table, zeros)
+
+
+def oracle_for_source_case(case, rows, nthreads: int = 0, window: int = 0) -> np.ndarray:
+    """fp64 oracle output for the sequences in ``rows`` of a case whose cache is
+    filled from unquantised rows: the oracle quantises those rows itself
+    (oracle.quantised_sequence) and never reads the device cache."""
+    import oracle
+    lens = case.context_lens.cpu().numpy()
+    rows = list(rows)
+    S = max([int(lens[b]) for b in rows] + [0])
+    K, d = case.num_kv_heads, case.head_dim
+    kd = np.zeros((len(rows), S, K, d))
+    vd = np.zeros((len(rows), S, K, d))
+    for n, b in enumerate(rows):
+        ks, vs = source_rows(case, b)
+        L = ks.shape[0]
+        kd[n, :L] = oracle.quantised_sequence(ks, case.cache_dtype, case.cache_dtype == "i4kc")[0]
+        vd[n, :L] = oracle.quantised_sequence(vs, case.cache_dtype)[0]
+    q = case.q.detach().float().cpu().numpy().astype(np.float64)[rows]
+    return oracle.decode(q, kd, vd, lens[rows], case.scale, nthreads, window=window)
+
+
+def cache_codes_of(case, b, which: str):
+    """Codes ([L, K, d]) and scale bits the device cache holds for sequence b:
+    per token [L, K], or for the KIVI-style K per block [nblk, K, d]."""
+    import oracle
+    lens = case.context_lens.cpu().numpy()
+    L = int(lens[b])
+    nblk = -(-L // 16)
+    ids = case.block_table[b, :nblk].long()
+    pool = (case.k_cache if which == "k" else case.v_cache).index_select(0, ids)
+    sc = (case.k_scale if which == "k" else case.v_scale).index_select(0, ids)
+    pool = pool.view(torch.uint8) if pool.dtype == torch.float8_e4m3fn else pool
+    pool = pool.cpu().numpy()                           # [nblk, K, 16, row]
+    sbits = sc.cpu().view(torch.int16).numpy().view(np.uint16)
+    codes = pool.transpose(0, 2, 1, 3).reshape(nblk * 16, pool.shape[1], pool.shape[3])[:L]
+    if case.cache_dtype in ("i4", "i4kc"):
+        codes = oracle.unpack_int4(codes)
+    if which == "k" and case.cache_dtype == "i4kc":
+        return codes, sbits                             # [nblk, K, d]
+    return codes, sbits.transpose(0, 2, 1).reshape(nblk * 16, -1)[:L]
+
+
 def max_abs_err(gpu_out: torch.Tensor, ref: np.ndarray, rows=None) -> float:
     got = gpu_out.detach().float().cpu().numpy().astype(np.float64)
     if rows is not None:

@@ -11,7 +11,8 @@ import pytest
 import torch
 
 import gqa_inputs as gi
-from helpers import TOL, max_abs_err, oracle_for_case
+from helpers import (TOL, cache_codes_of, fill_from_source, max_abs_err, oracle_for_case,
+                     oracle_for_source_case, source_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -323,11 +324,34 @@ def test_int8_append_then_decode(gq, oracle_mod):
 
 def _sampled(gq, wl, rows, seed=0, **kw):
     """Decode a full-size workload with the default launch, then check the
-    sampled sequences (every head) against the oracle."""
+    sampled sequences (every head) against the oracle. Code caches drawn as
+    N(0, 1) rows are quantised into the cache by the library's append; the
+    oracle quantises the sampled rows itself, and the cache must hold exactly
+    its codes and scales for them."""
     case = gi.case_for(wl, seed=seed, device="cuda")
+    if case.k_src is not None:
+        fill_from_source(gq, case)
+        torch.cuda.synchronize()
+        _codes_match_the_oracle(case, rows)
+        out = _run(gq, case, window=wl.window, **kw)
+        ref = oracle_for_source_case(case, rows, window=wl.window)
+        return max_abs_err(out, ref, rows=rows)
     out = _run(gq, case, window=wl.window, **kw)
     ref = oracle_for_case(case, rows=rows, host_pools=_host_pools(case), window=wl.window)
     return max_abs_err(out, ref, rows=rows)
+
+
+def _codes_match_the_oracle(case, rows):
+    import oracle
+    for b in rows:
+        for which, src in zip("kv", source_rows(case, b)):
+            kc = which == "k" and case.cache_dtype == "i4kc"
+            _, codes, sbits = oracle.quantised_sequence(src, case.cache_dtype, kc)
+            got_codes, got_bits = cache_codes_of(case, b, which)
+            if case.cache_dtype == "fp8":
+                got_codes = got_codes.view(np.uint8)
+            assert np.array_equal(got_codes, codes), (b, which)
+            assert np.array_equal(got_bits, sbits), (b, which)
 
 
 def _host_pools(case):
