@@ -218,6 +218,51 @@ def _dev(t: Optional[torch.Tensor], name: str, index: bool = False, optional: bo
     return t.data_ptr()
 
 
+def _on_cache_device(cache: "PagedKVCache", **tensors):
+    """Every array must sit on the cache's device, and that device must be the
+    current one: the library launches on the current device and reads the
+    pointers it is given there."""
+    dev = cache.k.device
+    cur = torch.cuda.current_device() if torch.cuda.is_available() else None
+    if dev.type == "cuda" and cur is not None and dev.index != cur:
+        raise ValueError(f"the cache is on {dev} but the current device is cuda:{cur}")
+    for name, t in tensors.items():
+        if t is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the cache on {dev}")
+
+
+def _check_table_and_lens(block_tables: torch.Tensor, lens: torch.Tensor, batch: int, lens_name: str,
+                          lens_min: int):
+    if block_tables.dim() != 2 or block_tables.shape[0] < batch:
+        raise ValueError(f"block_tables must be [>= {batch}, max_blocks], not {tuple(block_tables.shape)}")
+    if lens.dim() != 1 or lens.numel() < lens_min:
+        raise ValueError(f"{lens_name} must be 1-D with >= {lens_min} entries, not {tuple(lens.shape)}")
+
+
+def _check_query(cache: "PagedKVCache", q: torch.Tensor, dims: tuple):
+    if q.dim() not in dims:
+        raise ValueError(f"q must have {' or '.join(str(x) for x in dims)} dims, not {q.dim()}")
+    H, d = int(q.shape[-2]), int(q.shape[-1])
+    if d != cache.head_dim:
+        raise ValueError(f"q's head_dim {d} differs from the cache's {cache.head_dim}")
+    if H % cache.num_kv_heads:
+        raise ValueError(f"{H} query heads are not a multiple of {cache.num_kv_heads} kv-heads")
+
+
+def _check_out(q: torch.Tensor, out: Optional[torch.Tensor]):
+    if out is not None and tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out must have q's shape {tuple(q.shape)}, not {tuple(out.shape)}")
+
+
+def _check_new_rows(cache: "PagedKVCache", k_new: torch.Tensor, v_new: torch.Tensor, dims: tuple):
+    if k_new.dim() not in dims or tuple(v_new.shape) != tuple(k_new.shape):
+        raise ValueError(f"k_new and v_new must share one shape with {dims} dims, "
+                         f"not {tuple(k_new.shape)} and {tuple(v_new.shape)}")
+    if tuple(k_new.shape[-2:]) != (cache.num_kv_heads, cache.head_dim):
+        raise ValueError(f"new rows end in {tuple(k_new.shape[-2:])}, the cache's heads and "
+                         f"head_dim are {(cache.num_kv_heads, cache.head_dim)}")
+
+
 def _check(status: int, where: str):
     if status != 0:
         raise GqaError(status, where)
@@ -231,6 +276,13 @@ def kv_append(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tensor,
     T = 1 if k_new.dim() == 3 else int(k_new.shape[1])
     args = (_dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(block_tables, "block_tables", True),
             _dev(positions, "positions", True), _dev(err, "err", True, True))
+    _check_new_rows(cache, k_new, v_new, (3, 4))
+    B = int(positions.shape[0]) if positions.dim() == 1 else -1
+    if B < 0 or int(k_new.shape[0]) != B:
+        raise ValueError(f"positions must be [B] with B = k_new.shape[0] = {int(k_new.shape[0])}")
+    _check_table_and_lens(block_tables, positions, B, "positions", B)
+    _on_cache_device(cache, k_new=k_new, v_new=v_new, block_tables=block_tables,
+                     positions=positions, err=err)
     desc = cache.desc()
     st = load().gqa_kv_append(ctypes.byref(desc), args[0], args[1], DTYPE_CODE[k_new.dtype], args[2],
                               int(block_tables.shape[1]), args[3], int(positions.shape[0]),
@@ -248,18 +300,25 @@ _ws_cache: dict = {}
 
 
 def workspace_for(batch: int, num_heads: int, num_kv_heads: int, head_dim: int,
-                  device: torch.device, tokens_per_seq: int = 1) -> torch.Tensor:
-    """A cached, zero-initialised device workspace large enough for this shape."""
+                  device: torch.device, tokens_per_seq: int = 1, stream=None) -> torch.Tensor:
+    """A cached, zero-initialised device workspace large enough for this shape,
+    one per (device, stream): calls on one stream run in order, so they may
+    share it; calls on different streams get different workspaces. The buffer
+    is allocated on that stream, so a larger one replacing it is ordered after
+    the calls already queued there."""
     dev = torch.device(device)
     idx = dev.index if dev.index is not None else torch.cuda.current_device()
     need = decode_workspace_size(batch, num_heads, num_kv_heads, head_dim, idx, tokens_per_seq)
     if need == 0:
         raise ValueError("no workspace size for this shape")
-    buf = _ws_cache.get(idx)
+    s = stream if stream is not None else torch.cuda.current_stream(torch.device("cuda", idx))
+    key = (idx, s.cuda_stream)
+    buf = _ws_cache.get(key)
     if buf is None or buf.numel() < need:
         # zero-filled once: the library keeps its run-time work counter at zero between calls
-        buf = torch.zeros(need, dtype=torch.uint8, device=dev)
-        _ws_cache[idx] = buf
+        with torch.cuda.stream(s):
+            buf = torch.zeros(need, dtype=torch.uint8, device=dev)
+        _ws_cache[key] = buf
     return buf
 
 
@@ -278,10 +337,15 @@ def gqa_decode(cache: PagedKVCache, q: torch.Tensor, block_tables: torch.Tensor,
     B, H, d = q.shape[0], q.shape[-2], q.shape[-1]
     qp, tp, lp = _dev(q, "q"), _dev(block_tables, "block_tables", True), _dev(context_lens, "context_lens", True)
     ep = _dev(err, "err", True, True)
+    _check_query(cache, q, (3, 4))
+    _check_table_and_lens(block_tables, context_lens, B, "context_lens", B)
+    _check_out(q, out)
+    _on_cache_device(cache, q=q, block_tables=block_tables, context_lens=context_lens, out=out,
+                     workspace=workspace, err=err)
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     if workspace is None:
-        workspace = workspace_for(B, H, cache.num_kv_heads, d, q.device, T)
+        workspace = workspace_for(B, H, cache.num_kv_heads, d, q.device, T, stream)
     op, wp = _dev(out, "out"), _dev(workspace, "workspace")
     opts = DecodeOpts(T, window, kernel, max_warps, min_blocks_per_warp, row_layout, None, None)
     if events is not None:
@@ -310,6 +374,10 @@ def gqa_decode_noalloc(cache: PagedKVCache, q: torch.Tensor, block_tables: torch
     B, H, d = q.shape[0], q.shape[-2], q.shape[-1]
     qp, tp, lp = _dev(q, "q"), _dev(block_tables, "block_tables", True), _dev(context_lens, "context_lens", True)
     ep = _dev(err, "err", True, True)
+    _check_query(cache, q, (3, 4))
+    _check_table_and_lens(block_tables, context_lens, B, "context_lens", B)
+    _check_out(q, out)
+    _on_cache_device(cache, q=q, block_tables=block_tables, context_lens=context_lens, out=out, err=err)
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     op = _dev(out, "out")
@@ -332,6 +400,15 @@ def kv_append_varlen(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tens
     args = (_dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(token_start, "token_start", True),
             _dev(block_tables, "block_tables", True), _dev(positions, "positions", True),
             _dev(err, "err", True, True))
+    _check_new_rows(cache, k_new, v_new, (3,))
+    B = int(positions.shape[0]) if positions.dim() == 1 else -1
+    if B < 0:
+        raise ValueError("positions must be 1-D")
+    _check_table_and_lens(block_tables, positions, B, "positions", B)
+    if token_start.dim() != 1 or token_start.numel() < B + 1:
+        raise ValueError(f"token_start must be 1-D with >= {B + 1} entries")
+    _on_cache_device(cache, k_new=k_new, v_new=v_new, token_start=token_start,
+                     block_tables=block_tables, positions=positions, err=err)
     desc = cache.desc()
     st = load().gqa_kv_append_varlen(ctypes.byref(desc), args[0], args[1],
                                      DTYPE_CODE[k_new.dtype], args[2], int(max_new_tokens),
@@ -350,11 +427,20 @@ def gqa_prefill(cache: PagedKVCache, q: torch.Tensor, q_start: torch.Tensor, max
     tcgen05 (tensor memory), 2 warp-level mma.sync."""
     args = (_dev(q, "q"), _dev(q_start, "q_start", True), _dev(block_tables, "block_tables", True),
             _dev(context_lens, "context_lens", True), _dev(err, "err", True, True))
+    _check_query(cache, q, (3,))
+    B = int(context_lens.shape[0]) if context_lens.dim() == 1 else -1
+    if B < 0:
+        raise ValueError("context_lens must be 1-D")
+    _check_table_and_lens(block_tables, context_lens, B, "context_lens", B)
+    if q_start.dim() != 1 or q_start.numel() < B + 1:
+        raise ValueError(f"q_start must be 1-D with >= {B + 1} entries")
+    _check_out(q, out)
+    _on_cache_device(cache, q=q, q_start=q_start, block_tables=block_tables,
+                     context_lens=context_lens, out=out, err=err)
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     op = _dev(out, "out")
     desc = cache.desc()
-    B = int(context_lens.shape[0])
     st = load().gqa_prefill(ctypes.byref(desc), args[0], DTYPE_CODE[q.dtype], int(q.shape[1]),
                             args[1], int(max_new_tokens), args[2],
                             int(block_tables.shape[1]), args[3], B, float(scale), int(window),

@@ -206,7 +206,15 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     void* args[] = {&kmap, &vmap, &a};
     e = cudaLaunchKernelExC(&cfg, v.fn, args);
     if (e != cudaSuccess) return GQA_ERR_CUDA;
-    if (L.ev_end && cudaEventRecord(L.ev_end, L.stream) != cudaSuccess) return GQA_ERR_CUDA;
+    // From here the split-KV kernel has advanced the pool's ticket counter,
+    // which only the combine rewinds: a failure before the combine is queued
+    // rewinds it on the stream instead, so the next call on this workspace
+    // starts from zero.
+    auto fail_after_split = [&]() {
+        cudaMemsetAsync(a.ws_ctr, 0, sizeof(unsigned long long), L.stream);
+        return GQA_ERR_CUDA;
+    };
+    if (L.ev_end && cudaEventRecord(L.ev_end, L.stream) != cudaSuccess) return fail_after_split();
 
     // Combine width from the expected pieces per row (about 1.5 workers' worth
     // of segments per pair when lengths are even).
@@ -238,7 +246,7 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     ccfg.attrs = pdl;
     ccfg.numAttrs = timed ? 0 : 1;
     void* cargs[] = {&a};
-    if (cudaLaunchKernelExC(&ccfg, cfn, cargs) != cudaSuccess) return GQA_ERR_CUDA;
+    if (cudaLaunchKernelExC(&ccfg, cfn, cargs) != cudaSuccess) return fail_after_split();
     return GQA_OK;
 }
 

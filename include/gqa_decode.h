@@ -299,7 +299,9 @@ GQA_API size_t gqa_decode_workspace_size(int32_t batch, int32_t num_heads, int32
  *  workspace      device, >= gqa_decode_workspace_size(...) bytes, 256-byte
  *                 aligned, zero-filled before its first use (one word of it, the
  *                 run-time work counter, must start at zero; every call leaves it
- *                 at zero again). Otherwise clobbered by each call. Calls that
+ *                 at zero again, a call failing with GQA_ERR_CUDA after its first
+ *                 kernel was queued by a reset queued on the stream). Otherwise
+ *                 clobbered by each call. Calls that
  *                 share a workspace must not overlap on the GPU.
  *  opts           NULL or options (gqa_decode_opts_t).
  *  Limits: num_heads % K == 0; T * num_heads / K <= 64 query rows per kv-head;
@@ -332,7 +334,9 @@ GQA_API int gqa_decode(const gqa_kv_cache_t *cache, const void *q, int32_t q_dty
  *    before any stream capture on the device.
  *  - Every call shares the one array and it keeps the last call's contents.
  *    The one word that must start at zero does: the array is zero when the
- *    library loads and every call leaves that word at zero. Calls whose GPU
+ *    library loads and every call leaves that word at zero (a call that fails
+ *    with GQA_ERR_CUDA after its first kernel was queued also queues a reset
+ *    of that word on the stream). Calls whose GPU
  *    work overlaps -- different streams, or different host threads -- race on
  *    it; serialise them.
  */

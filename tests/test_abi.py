@@ -169,3 +169,70 @@ def test_binding_rejects_arrays_the_library_cannot_read():
         gq.gqa_decode(None, q.transpose(0, 1), lens.reshape(1, 1), lens, 0.125)
     with pytest.raises(ValueError, match="contiguous"):
         gq.kv_append(None, q.transpose(0, 1), q, lens.reshape(1, 1), lens)
+
+
+def _cpu_cache(K=2, d=64, nb=4):
+    import torch
+    k = torch.zeros(nb, K, 16, d, dtype=torch.bfloat16)
+    return gq.PagedKVCache(k, k.clone(), nb, K, d, K * 16 * d, 16 * d, d)
+
+
+def test_binding_rejects_a_query_the_cache_cannot_serve():
+    """The library takes head_dim from the cache and the batch from q, so a q
+    of another head_dim, or a head count that is not a multiple of the
+    kv-heads, would be read out of bounds: refused before any call."""
+    import torch
+    cache = _cpu_cache()
+    gq._check_query(cache, torch.zeros(3, 8, 64), (3, 4))           # fits
+    with pytest.raises(ValueError, match="head_dim"):
+        gq._check_query(cache, torch.zeros(3, 8, 128), (3, 4))
+    with pytest.raises(ValueError, match="multiple"):
+        gq._check_query(cache, torch.zeros(3, 7, 64), (3, 4))
+    with pytest.raises(ValueError, match="dims"):
+        gq._check_query(cache, torch.zeros(3, 2, 8, 64), (3,))
+
+
+def test_binding_rejects_short_tables_and_lengths():
+    import torch
+    lens = torch.zeros(4, dtype=torch.int32)
+    gq._check_table_and_lens(torch.zeros(4, 9, dtype=torch.int32), lens, 4, "context_lens", 4)
+    with pytest.raises(ValueError, match="block_tables"):
+        gq._check_table_and_lens(torch.zeros(3, 9, dtype=torch.int32), lens, 4, "context_lens", 4)
+    with pytest.raises(ValueError, match="block_tables"):
+        gq._check_table_and_lens(torch.zeros(36, dtype=torch.int32), lens, 4, "context_lens", 4)
+    with pytest.raises(ValueError, match="context_lens"):
+        gq._check_table_and_lens(torch.zeros(4, 9, dtype=torch.int32), lens[:3], 4, "context_lens", 4)
+    with pytest.raises(ValueError, match="q_start|positions"):
+        gq._check_table_and_lens(torch.zeros(4, 9, dtype=torch.int32), lens, 4, "positions", 5)
+
+
+def test_binding_rejects_an_output_of_another_shape():
+    import torch
+    q = torch.zeros(3, 8, 64)
+    gq._check_out(q, None)
+    gq._check_out(q, torch.zeros(3, 8, 64, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="out"):
+        gq._check_out(q, torch.zeros(3, 8, 32))
+
+
+def test_binding_rejects_new_rows_of_another_shape():
+    import torch
+    cache = _cpu_cache()
+    x = torch.zeros(5, 2, 64)
+    gq._check_new_rows(cache, x, x.clone(), (3, 4))
+    with pytest.raises(ValueError, match="share one shape"):
+        gq._check_new_rows(cache, x, torch.zeros(5, 2, 32), (3, 4))
+    with pytest.raises(ValueError, match="heads and head_dim"):
+        gq._check_new_rows(cache, torch.zeros(5, 4, 64), torch.zeros(5, 4, 64), (3, 4))
+    with pytest.raises(ValueError, match="dims"):
+        gq._check_new_rows(cache, torch.zeros(5, 1, 2, 64), torch.zeros(5, 1, 2, 64), (3,))
+
+
+def test_binding_rejects_arrays_on_another_device():
+    """Every array must sit where the cache is (meta tensors stand in for a
+    second device here)."""
+    import torch
+    cache = _cpu_cache()
+    gq._on_cache_device(cache, q=torch.zeros(2), err=None)
+    with pytest.raises(ValueError, match="q is on meta"):
+        gq._on_cache_device(cache, q=torch.zeros(2, device="meta"))
