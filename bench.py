@@ -1,7 +1,8 @@
 """Benchmark: one GQA decode step (paged KV append + split-KV decode + combine).
 
-Default workload: the Llama-3-8B-shaped paged decode (bf16, H=32, K=8, d=128,
-batch 64, every context 4096 tokens, block_size 16, shuffled block table).
+Default workload: the Llama-2/3-70B-shaped paged decode (bf16, H=64, K=8,
+d=128, batch 32, context lengths seeded uniform in [128, 32768], block_size 16,
+shuffled block table), the largest single-GPU configuration.
 Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -32,7 +33,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode-attention HBM GB/s (% of GB300 peak) and tokens/s per decode step, 1 GPU"
-DEFAULT_WORKLOAD = "llama3_8b_bf16_b64_s4096"
+DEFAULT_WORKLOAD = "llama70b_bf16_b32_ragged"
 L2_BYTES = 129 * 2 ** 20
 KERNEL_NAME = "split_kv_kernel"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kv_kernel_traffic.txt")
@@ -245,6 +246,56 @@ def max_over_ranks(vals, device):
 def whole_job_gbs(bytes_per_rank: float, world: int, ms: float) -> float:
     """Aggregate bandwidth of N replicas that each moved bytes_per_rank in ms."""
     return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
+# ----------------------------------------------------------------------------- read ceiling
+
+READ_PROBE_FORMS = ((0, 2, "bulk copies, 8 KB chunks, 2 stages per warp, 2 CTAs/SM"),
+                    (0, 3, "bulk copies, 8 KB chunks, 2 stages per warp, 3 CTAs/SM"),
+                    (1, 2, "bulk copies, 8 KB chunks, 3 stages per warp, 2 CTAs/SM"),
+                    (2, 3, "bulk copies, 4 KB chunks, 4 stages per warp, 3 CTAs/SM"),
+                    (3, 4, "16-byte loads, 4 x 256 threads per SM"),
+                    (3, 8, "16-byte loads, 8 x 256 threads per SM"))
+
+
+def read_probe(dev, gib: float = 4.0, reps: int = 10) -> dict:
+    """Measured HBM read ceiling: the probe library's pure read streams over a
+    buffer larger than L2 (each form warmed up, then `reps` launches timed with
+    CUDA events on the launching stream); the best form is reported."""
+    import ctypes
+    import torch
+    from gqa_decode_attention_kv_gb300 import build as gbuild
+    lib = ctypes.CDLL(gbuild.PROBE_LIB_PATH)
+    lib.hbm_read_probe.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_void_p]
+    lib.hbm_read_probe.restype = ctypes.c_int
+    nbytes = int(gib * 2 ** 30) // 8192 * 8192
+    buf = torch.full((nbytes // 4,), 0x01020304, dtype=torch.int32, device=dev)
+    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream()
+    results = {}
+    for form, cps, how in READ_PROBE_FORMS:
+        def launch():
+            rc = lib.hbm_read_probe(buf.data_ptr(), nbytes, sink.data_ptr(), form, cps, stream.cuda_stream)
+            if rc != 0:
+                raise RuntimeError(f"hbm_read_probe failed with {rc}")
+        for _ in range(3):
+            launch()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            launch()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        results[how] = round(nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+    if int(sink.item()) >= 1 << 40:
+        raise RuntimeError("hbm_read_probe: a bounded wait expired")
+    best = max(results, key=results.get)
+    del buf
+    return {"gbs": results[best], "form": best, "bytes_per_launch": nbytes, "forms": results,
+            "how": f"pure read of a {nbytes / 2 ** 30:.0f} GiB buffer (> L2), {reps} launches per form "
+                   "after 3 warm-ups, CUDA events; best form"}
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -488,6 +539,11 @@ def run_ours(args):
     case = gi.case_for(wl, seed=args.seed + rank, device=str(dev), extra_tokens=0)
     cache = gq.cache_from_case(case)
     lens = case.context_lens
+    if case.k_src is not None:
+        # code cache drawn as N(0, 1) rows: the library's append quantises them in
+        gq.kv_append_varlen(cache, case.k_src, case.v_src, case.src_start, int(lens.max().item()),
+                            case.block_table, torch.zeros_like(lens))
+        torch.cuda.synchronize()
     pos = (lens - wl.queries).clamp(min=0)    # the step re-appends the last T tokens
     ab = algorithmic_bytes(wl, lens.cpu().tolist())
     out = torch.empty(case.q.shape, dtype=torch.float32, device=dev)
@@ -575,6 +631,8 @@ def run_ours(args):
     if err.item() != 0:
         raise RuntimeError(f"device error flags {err.item()}")
 
+    probe = read_probe(dev) if not args.no_read_probe else None
+
     # slowest rank decides
     ms, e2e_ms, kern_ms = max_over_ranks([ms, e2e_ms, kern_ms], dev)
 
@@ -625,6 +683,9 @@ def run_ours(args):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
+        if probe is not None:
+            line["read_probe"] = probe
+            line["roofline"]["frac_of_read_probe"] = round(kern_gbs / probe["gbs"], 4)
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl, case, args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -638,6 +699,21 @@ def _oracle_inputs(wl, case, rows):
     import numpy as np
     import oracle
     lens = case.context_lens.cpu().numpy()
+    if case.k_src is not None:
+        # code cache drawn as N(0, 1) rows: the oracle quantises the sampled
+        # rows with its own rule (it never reads the device cache)
+        S = max(int(lens[b]) for b in rows)
+        K, d = wl.num_kv_heads, wl.head_dim
+        kd = np.zeros((len(rows), S, K, d))
+        vd = np.zeros((len(rows), S, K, d))
+        st = case.src_start.cpu().numpy()
+        for n, b in enumerate(rows):
+            ks = case.k_src[int(st[b]):int(st[b + 1])].cpu().numpy()
+            vs = case.v_src[int(st[b]):int(st[b + 1])].cpu().numpy()
+            kd[n, :len(ks)] = oracle.quantised_sequence(ks, wl.cache_dtype, wl.cache_dtype == "i4kc")[0]
+            vd[n, :len(vs)] = oracle.quantised_sequence(vs, wl.cache_dtype)[0]
+        q = case.q.float().cpu().numpy().astype(np.float64)[rows]
+        return q, kd, vd, lens[rows]
     table = case.block_table.cpu().numpy()
     sel = []
     for b in rows:
@@ -722,10 +798,20 @@ def cpu_baseline(wl, case, seconds: float) -> dict:
         dt = (time.perf_counter() - t) / reps
     lens = case.context_lens.cpu().tolist()
     sub = algorithmic_bytes(wl, [lens[b] for b in rows])
+    # the same oracle on one thread, on sequence 0 alone
+    q1, kd1, vd1, sl1 = _oracle_inputs(wl, case, [0])
+    t = time.perf_counter()
+    _oracle_decode(wl, q1, kd1, vd1, sl1, case.scale, 1)
+    dt1 = time.perf_counter() - t
+    one = algorithmic_bytes(wl, [lens[0]])
     return {"value": round(sub["decode"] / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle", "seconds": round(dt * reps, 3),
             "sample": f"{n} of {wl.batch} sequences (all {wl.num_heads} heads) x {reps} passes, "
-                      f"fp64 C oracle, decode only"}
+                      f"fp64 C oracle, decode only",
+            "one_thread": {"value": round(one["decode"] / dt1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                           "seconds": round(dt1, 3),
+                           "sample": f"sequence 0 ({lens[0]} tokens, all {wl.num_heads} heads), "
+                                     "fp64 C oracle on one thread"}}
 
 
 def run_reference(args):
@@ -825,6 +911,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-read-probe", action="store_true",
+                    help="skip the HBM read-ceiling probe (decode workloads)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

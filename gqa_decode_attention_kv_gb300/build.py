@@ -1,7 +1,9 @@
 """Build the in-tree CUDA library (sm_103a) with nvcc.
 
 Each translation unit compiles in parallel to an object file, then one link
-makes ``_build/libgqa_decode.so``. No CMake; a minute or two on a cold cache.
+makes ``_build/libgqa_decode.so``. The HBM read probe the benchmark uses as a
+ceiling (``probe/hbm_read_probe.cu``) compiles alongside into its own
+``_build/libhbm_probe.so``. No CMake; a minute or two on a cold cache.
 """
 from __future__ import annotations
 
@@ -18,6 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libgqa_decode.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
+PROBE_SRC = os.path.join(HERE, "probe", "hbm_read_probe.cu")
+PROBE_LIB_PATH = os.path.join(OUT_DIR, "libhbm_probe.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-diag-suppress", "177", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
@@ -41,10 +45,10 @@ def _headers():
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+    if not os.path.exists(LIB_PATH) or not os.path.exists(PROBE_LIB_PATH):
         return True
-    t = os.path.getmtime(LIB_PATH)
-    return any(os.path.getmtime(p) > t for p in _sources() + _headers() + [__file__])
+    t = min(os.path.getmtime(LIB_PATH), os.path.getmtime(PROBE_LIB_PATH))
+    return any(os.path.getmtime(p) > t for p in _sources() + _headers() + [__file__, PROBE_SRC])
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
@@ -63,8 +67,18 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             raise RuntimeError(f"nvcc failed for {src}:\n{res.stderr}")
         return obj, res.stderr
 
+    def build_probe():
+        tmp = PROBE_LIB_PATH + f".tmp{os.getpid()}"
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-shared", PROBE_SRC, "-o", tmp]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {PROBE_SRC}:\n{res.stderr}")
+        os.replace(tmp, PROBE_LIB_PATH)
+
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as ex:
+        probe = ex.submit(build_probe)
         results = list(ex.map(compile_one, _sources()))
+        probe.result()
     if verbose or ptxas_info:
         for _, err in results:
             if err:
