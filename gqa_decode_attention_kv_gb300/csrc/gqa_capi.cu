@@ -30,10 +30,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// SM count per device, asked of the runtime once per device.
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices] = {};
+std::mutex g_sms_mutex;
+
 int num_sms_of(int device) {
     if (device < 0 && cudaGetDevice(&device) != cudaSuccess) return -1;
+    if (device < kMaxDevices) {
+        std::lock_guard<std::mutex> lock(g_sms_mutex);
+        if (g_sms[device] > 0) return g_sms[device];
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return -1;
+    if (device < kMaxDevices && n > 0) {
+        std::lock_guard<std::mutex> lock(g_sms_mutex);
+        g_sms[device] = n;
+    }
     return n;
 }
 
@@ -65,10 +78,93 @@ int check_residual(const gqa_kv_cache_t* c, int batch) {
     return GQA_OK;
 }
 
+// Tensor maps already encoded, keyed by everything an encoding reads (the
+// base address, the cache's shape, strides and element type, the box and the
+// swizzle): a serving loop calls with the same cache every step, and encoding
+// costs more host time than the launch. A map depends only on its key, so an
+// entry stays right even if the memory behind it is freed and reused.
+struct MapKey {
+    const void* base;
+    long long num_blocks, stride_block, stride_head, stride_token;
+    int num_kv_heads, head_dim, dtype, box_inner, swizzle_bytes, form;
+    bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    int perm[3];
+};
+constexpr int kMapCacheSize = 32;
+MapEntry g_maps[kMapCacheSize];
+int g_maps_used = 0, g_maps_next = 0;
+std::mutex g_maps_mutex;
+
+MapKey map_key(const gqa_kv_cache_t& c, const void* base, int box_inner, int swizzle_bytes, int form) {
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));   // padding bytes take part in the comparison
+    k.base = base;
+    k.num_blocks = c.num_blocks;
+    k.stride_block = c.stride_block;
+    k.stride_head = c.stride_head;
+    k.stride_token = c.stride_token;
+    k.num_kv_heads = c.num_kv_heads;
+    k.head_dim = c.head_dim;
+    k.dtype = c.dtype;
+    k.box_inner = box_inner;
+    k.swizzle_bytes = swizzle_bytes;
+    k.form = form;
+    return k;
+}
+
+bool cached_map(const MapKey& k, CUtensorMap* map, int* perm, int nperm) {
+    std::lock_guard<std::mutex> lock(g_maps_mutex);
+    for (int i = 0; i < g_maps_used; ++i) {
+        if (g_maps[i].key == k) {
+            *map = g_maps[i].map;
+            for (int j = 0; j < nperm; ++j) perm[j] = g_maps[i].perm[j];
+            return true;
+        }
+    }
+    return false;
+}
+
+void remember_map(const MapKey& k, const CUtensorMap& map, const int* perm, int nperm) {
+    std::lock_guard<std::mutex> lock(g_maps_mutex);
+    MapEntry& e = g_maps[g_maps_next];
+    e.key = k;
+    e.map = map;
+    for (int j = 0; j < 3; ++j) e.perm[j] = j < nperm ? perm[j] : 0;
+    g_maps_next = (g_maps_next + 1) % kMapCacheSize;
+    g_maps_used = std::max(g_maps_used, g_maps_next == 0 ? kMapCacheSize : g_maps_next);
+}
+
+bool encode_cache_map_uncached(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int box_inner,
+                               int swizzle_bytes, int perm[3]);
+bool encode_page_map_uncached(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int perm[2]);
+
 }  // namespace
 
 bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int box_inner,
                       int swizzle_bytes, int perm[3]) {
+    const MapKey k = map_key(c, base, box_inner, swizzle_bytes, 0);
+    if (cached_map(k, map, perm, 3)) return true;
+    if (!encode_cache_map_uncached(map, c, base, box_inner, swizzle_bytes, perm)) return false;
+    remember_map(k, *map, perm, 3);
+    return true;
+}
+
+bool encode_page_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int perm[2]) {
+    const MapKey k = map_key(c, base, 64, 128, 1);
+    if (cached_map(k, map, perm, 2)) return true;
+    if (!encode_page_map_uncached(map, c, base, perm)) return false;
+    remember_map(k, *map, perm, 2);
+    return true;
+}
+
+namespace {
+
+bool encode_cache_map_uncached(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int box_inner,
+                               int swizzle_bytes, int perm[3]) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
     if (!enc) return false;
     CUtensorMapDataType dt;
@@ -108,7 +204,7 @@ bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* bas
 // elements, 16 slots, 2 row halves, then the kv-head and block axes by
 // stride), box (64, 16, 2, 1, 1), 128-byte swizzle, so that a page lands as
 // [half][slot][128 B]. perm[i] names dim 3 + i: 1 kv-head, 2 block.
-bool encode_page_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int perm[2]) {
+bool encode_page_map_uncached(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int perm[2]) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
     if (!enc || c.head_dim != 128 || dtype_bits(c.dtype) != 16) return false;
     const CUtensorMapDataType dt =
@@ -129,6 +225,8 @@ bool encode_page_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+
+}  // namespace
 
 }  // namespace gqa
 

@@ -1,6 +1,8 @@
 // gqa_decode.cu -- host side of the split-KV decode: kernel choice, workspace
 // layout, partition sizing and the launches (kernels in gqa_decode_kernels.cuh).
 // Instantiates the one-token, full-attention kernels and the combine kernels.
+#include <mutex>
+
 #include "gqa_decode_kernels.cuh"
 
 namespace gqa {
@@ -11,6 +13,63 @@ bool pick_plain(int dtype, int kind, int d, int nw, Variant& v) {
 }
 
 }  // namespace dec
+
+// Resident CTAs per SM of a kernel at a dynamic shared-memory size, asked of
+// the runtime once per (device, kernel, size) and remembered: a decode step
+// asks on every call. The kernel's shared-memory limit is raised to the
+// largest size asked for so far on the device (a limit set for one size
+// serves every smaller one).
+namespace {
+struct OccEntry {
+    int device;
+    const void* fn;
+    int smem, threads, per_sm;
+};
+struct LimitEntry {
+    int device;
+    const void* fn;
+    int smem;
+};
+constexpr int kOccCacheSize = 128;
+OccEntry g_occ[kOccCacheSize];
+LimitEntry g_limit[kOccCacheSize];
+int g_occ_used = 0, g_occ_next = 0, g_limit_used = 0;
+std::mutex g_occ_mutex;
+
+// Raises fn's dynamic shared-memory limit to at least smem; g_occ_mutex held.
+bool ensure_limit(int dev, const void* fn, int smem) {
+    for (int i = 0; i < g_limit_used; ++i) {
+        LimitEntry& e = g_limit[i];
+        if (e.device == dev && e.fn == fn) {
+            if (e.smem >= smem) return true;
+            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+                return false;
+            e.smem = smem;
+            return true;
+        }
+    }
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
+    if (g_limit_used < kOccCacheSize) g_limit[g_limit_used++] = LimitEntry{dev, fn, smem};
+    return true;
+}
+}  // namespace
+
+int ctas_per_sm(const void* fn, int threads, int smem) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    if (!ensure_limit(dev, fn, smem)) return 0;
+    for (int i = 0; i < g_occ_used; ++i) {
+        const OccEntry& e = g_occ[i];
+        if (e.device == dev && e.fn == fn && e.smem == smem && e.threads == threads) return e.per_sm;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess) return 0;
+    g_occ[g_occ_next] = OccEntry{dev, fn, smem, threads, per_sm};
+    g_occ_next = (g_occ_next + 1) % kOccCacheSize;
+    g_occ_used = std::max(g_occ_used, g_occ_next == 0 ? kOccCacheSize : g_occ_next);
+    return per_sm;
+}
 
 namespace {
 
@@ -49,13 +108,7 @@ WsLayout ws_layout(int B, int K, int rows, int D, long long slots) {
 // Split-KV workers one launch uses for variant v at this batch (occupancy of a
 // single resident wave); 0 if the variant cannot launch.
 int workers_of(const Variant& v, int batch, int num_sms) {
-    const int smem = v.smem(batch);
-    if (cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return 0;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, v.fn, v.warps * 32, smem) != cudaSuccess)
-        return 0;
-    return num_sms * per_sm * v.workers_per_cta;
+    return num_sms * ctas_per_sm(v.fn, v.warps * 32, v.smem(batch)) * v.workers_per_cta;
 }
 
 }  // namespace

@@ -95,6 +95,12 @@ struct DecodeLaunch {
     cudaStream_t stream;
 };
 
+// Resident CTAs per SM of kernel fn with `threads` threads and `smem` bytes of
+// dynamic shared memory on the current device (its shared-memory limit set to
+// smem on the way); asked of the runtime once per (device, kernel, size) and
+// remembered. 0 if the kernel cannot launch so.
+int ctas_per_sm(const void* fn, int threads, int smem);
+
 // Bytes of workspace for a shape (T query tokens per sequence) given the
 // device's SM count.
 size_t decode_workspace_bytes(int batch, int num_heads, int num_kv_heads, int head_dim, int tokens_per_seq,

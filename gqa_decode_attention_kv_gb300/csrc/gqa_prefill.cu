@@ -872,8 +872,7 @@ int launch_prefill(const PrefillLaunch& L) {
     int page_perm[2] = {1, 2};
     if (tc && D == 128 && !encode_page_map(&vmap, c, c.v, page_perm))   // V a page per box
         return GQA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return GQA_ERR_CUDA;
+    if (ctas_per_sm(fn, tc ? kTcThreads : kPfWarps * 32, smem) < 1) return GQA_ERR_CUDA;
 
     PrefillArgs a;
     a.q = L.q;
