@@ -215,15 +215,23 @@ def dist_info():
     return world, rank, local
 
 
-def resolve_workload(name: str):
-    """A named workload, or the 70B-shaped KV-head sweep point '<70B name>_k<K>'."""
+def resolve_workload(name: str, batch: int = 0):
+    """A named workload, or the 70B-shaped KV-head sweep point '<70B name>_k<K>';
+    batch > 0 keeps only the first `batch` sequences (a smaller case of the same
+    workload, for profiling; named '<name>_first<batch>')."""
+    import dataclasses
     import gqa_inputs as gi
     if name in gi.WORKLOADS:
-        return gi.WORKLOADS[name]
-    base, _, k = name.rpartition("_k")
-    if base == "llama70b_bf16_b32_ragged" and k.isdigit():
-        return gi.kv_sweep_workload(int(k))
-    raise SystemExit(f"unknown workload {name!r}")
+        wl = gi.WORKLOADS[name]
+    else:
+        base, _, k = name.rpartition("_k")
+        if base == "llama70b_bf16_b32_ragged" and k.isdigit():
+            wl = gi.kv_sweep_workload(int(k))
+        else:
+            raise SystemExit(f"unknown workload {name!r}")
+    if 0 < batch < wl.batch:
+        wl = dataclasses.replace(wl, name=f"{wl.name}_first{batch}", batch=batch)
+    return wl
 
 
 ROW_LAYOUT = {"auto": 0, "split": 1, "shared": 2}
@@ -526,7 +534,7 @@ def run_ours(args):
     from gqa_decode_attention_kv_gb300 import build as gbuild
 
     if resolve_workload(args.workload).kind == "prefill":
-        return run_prefill(args, resolve_workload(args.workload))
+        return run_prefill(args, resolve_workload(args.workload, args.batch))
     world, rank, local = dist_info()
     if world > 1:
         dist.init_process_group("nccl")
@@ -535,7 +543,7 @@ def run_ours(args):
     gbuild.build()
     gq.load()
 
-    wl = resolve_workload(args.workload)
+    wl = resolve_workload(args.workload, args.batch)
     case = gi.case_for(wl, seed=args.seed + rank, device=str(dev), extra_tokens=0)
     cache = gq.cache_from_case(case)
     lens = case.context_lens
@@ -641,7 +649,7 @@ def run_ours(args):
         hbm = float(peaks["hbm_gbs"])
         gbs = whole_job_gbs(ab["step"], world, ms)
         kern_gbs = ab["decode"] / (kern_ms * 1e-3) / 1e9
-        traffic = read_traffic(args.workload, args.kernel)
+        traffic = read_traffic(wl.name, args.kernel)
         line = {
             "metric": METRIC,
             "value": round(gbs, 2),
@@ -824,7 +832,7 @@ def run_reference(args):
     import gqa_inputs as gi
     import oracle
     oracle.build()
-    wl = resolve_workload(args.workload)
+    wl = resolve_workload(args.workload, args.batch)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     case = gi.case_for(wl, seed=args.seed, device=dev, extra_tokens=0)
     threads = oracle.num_cpus()
@@ -909,6 +917,8 @@ def main():
     ap.add_argument("--row-layout", choices=list(ROW_LAYOUT), default="auto",
                     help="more than 8 query rows per kv-head: 8-row unit streams or a shared ring")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="keep only the first N sequences of the workload (smaller case for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-read-probe", action="store_true",

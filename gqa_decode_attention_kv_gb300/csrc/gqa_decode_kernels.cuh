@@ -99,6 +99,10 @@ struct DecodeArgs {
 #ifndef GQA_SHARED_RING_BYTES
 #define GQA_SHARED_RING_BYTES 32768
 #endif
+// Warps per SM the tensor-core shared-ring kernels are compiled to fit (registers).
+#ifndef GQA_SHARED_MIN_WARPS_PER_SM
+#define GQA_SHARED_MIN_WARPS_PER_SM 1
+#endif
 
 // Tail balancing: about 1/8 of every worker's range, in at most kMaxTailChunks
 // chunks of at least kMinChunk blocks, is pooled and taken at run time by
@@ -149,7 +153,15 @@ struct Cfg {
     // issue and latency and gains from 12 warps per SM; the bf16/f16 kernels
     // would spill at that budget and keep 8 (both measured).
     static constexpr int kMinCtas =
-        (kHeadWarps == 1 && kKind == kKernelMma && D == 128) ? (kCoded ? GQA_MIN_CTAS_PER_SM_I8 : 2) : 1;
+        (kHeadWarps == 1 && kKind == kKernelMma && D == 128) ? (kCoded ? GQA_MIN_CTAS_PER_SM_I8 : 2)
+        : (kHeadWarps > 1 && kKind == kKernelMma) ? std::max(1, GQA_SHARED_MIN_WARPS_PER_SM / kHeadWarps)
+                                                  : 1;
+    // Load the next pair's query fragments while the current pair runs (16
+    // registers). A worker meets a new pair once every few hundred blocks on
+    // the benchmark workloads, so kernels short of registers load them when
+    // the pair starts instead.
+    static constexpr bool kPrefetchQ =
+        !(kCoded && kMinCtas >= 4) && !(kHeadWarps > 1 && kHeadWarps * kMinCtas >= 12);
     static constexpr int kWarps = kHeadWarps == 1 ? GQA_WARPS_PER_CTA : kHeadWarps;
     static constexpr int kRings = kHeadWarps == 1 ? kWarps : 1;
     static constexpr int kStages =
@@ -400,7 +412,7 @@ struct MmaState {
     float m[2], l[2];          // heads 2c, 2c+1 of the group (log2 units)
     float acc[C::kMt][4];      // O^T fragments: rows = dims, cols = heads 2c, 2c+1
     uint2 qf[D / 16];          // Q^T B-fragments of the current pair, one per 16-dim k-step
-    uint2 qn[D / 16];          // prefetched fragments of the next pair
+    uint2 qn[C::kPrefetchQ ? D / 16 : 1];   // prefetched fragments of the next pair
 
     __device__ __forceinline__ void reset() {
         m[0] = m[1] = -INFINITY;
@@ -1266,9 +1278,11 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             next_pair(pref, a.B, a.Kv, nb_b, nb_g);
             if constexpr (kKind == kKernelMma) {
                 load_q_frags<C, D>(a, cb, cg / a.NRG, hbase, r, c, st.qf);
-                if (cu_pair + cnb < seg_end)
-                    load_q_frags<C, D>(a, nb_b, nb_g / a.NRG, kShared ? hbase : (nb_g % a.NRG) * kHeadsPerWarp,
-                                       r, c, st.qn);
+                if constexpr (C::kPrefetchQ) {
+                    if (cu_pair + cnb < seg_end)
+                        load_q_frags<C, D>(a, nb_b, nb_g / a.NRG,
+                                           kShared ? hbase : (nb_g % a.NRG) * kHeadsPerWarp, r, c, st.qn);
+                }
             } else {
                 fma_load_q<C, D>(a, st, cb, cg / a.NRG, hbase, lane);
             }
@@ -1336,11 +1350,15 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
             st.reset();
             next_pair(pref, a.B, a.Kv, nb_b, nb_g);
             if constexpr (kKind == kKernelMma) {
+                if constexpr (C::kPrefetchQ) {
 #pragma unroll
-                for (int q = 0; q < D / 16; ++q) st.qf[q] = st.qn[q];
-                if (cu_pair + cnb < seg_end)
-                    load_q_frags<C, D>(a, nb_b, nb_g / a.NRG, kShared ? hbase : (nb_g % a.NRG) * kHeadsPerWarp,
-                                       r, c, st.qn);
+                    for (int q = 0; q < D / 16; ++q) st.qf[q] = st.qn[q];
+                    if (cu_pair + cnb < seg_end)
+                        load_q_frags<C, D>(a, nb_b, nb_g / a.NRG,
+                                           kShared ? hbase : (nb_g % a.NRG) * kHeadsPerWarp, r, c, st.qn);
+                } else {
+                    load_q_frags<C, D>(a, cb, cg / a.NRG, hbase, r, c, st.qf);
+                }
             } else {
                 fma_load_q<C, D>(a, st, cb, cg / a.NRG, hbase, lane);
             }
