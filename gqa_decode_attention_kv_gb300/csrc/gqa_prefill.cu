@@ -827,6 +827,464 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ============================================================================
+// Wide form of the tcgen05 prefill (head_dim 128): one CTA per SM holds two
+// 128-row query tiles of one (kv-head, sequence) -- 256 consecutive rows --
+// that both read every K/V chunk of 64 tokens (4 paged blocks), so K/V tiles
+// are copied once per 256 rows and each S product is 128 x 64. The SM's 512
+// tensor-memory columns hold, per tile t, two S buffers at columns 256t and
+// 256t + 64 (S(c) in buffer c & 1, P(c) written over it) and O at 256t + 128:
+//   S_t(c) = Q_t K(c)^T     A = Q_t from shared memory (K-major, 128-byte swizzle)
+//   softmax of tile t       one thread per row: its 64 scores in registers in
+//                           one tensor-memory round trip; P as a high and a low
+//                           16-bit part over the same columns
+//   O_t   += P_t(c) V(c)    A = P from tensor memory, B = V pages MN-major
+// The MMA warp issues S_0(0..1), S_1(0..1), then per chunk PV_0(c), S_0(c+2),
+// PV_1(c), S_1(c+2). The tensor pipe runs in issue order, so S_t(c+2)
+// overwrites P_t(c) only after PV_t(c) has read it, and S_t(c+1) is ready when
+// tile t's softmax finishes chunk c: each tile's softmax runs back to back
+// while the pipe works through both tiles' products. Warps 0-3 own tile 0's
+// rows, 4-7 tile 1's, 8 issues the MMAs, 9 copies K and 10 copies V (four
+// 16 KB stages each). Per-chunk barriers (stages, S done, P ready, P.V done)
+// come in four copies taken in turn by chunk and the block masks in eight, so
+// that no parity wait can fall two phases behind (as in the 32-token kernel).
+constexpr int kW2Tiles = 2;
+constexpr int kW2Rows = kW2Tiles * kTcRows;      // query rows per CTA
+constexpr int kW2Threads = kW2Rows + 96;         // + MMA warp, K and V copy warps
+constexpr int kW2Chunk = 64;                     // KV tokens per chunk: N of S, K of P.V
+constexpr int kW2Blocks = kW2Chunk / kBlock;
+constexpr int kW2Bufs = 4;                       // K and V stages; per-chunk barrier copies
+constexpr uint32_t kW2TmemCols = 512;
+constexpr uint32_t kW2ColTile = 256;             // tile t: S buffers at 256t, 256t + 64
+constexpr uint32_t kW2ColO = 128;                //         O at 256t + 128
+
+struct W2Cfg {
+    static constexpr int D = 128;
+    static constexpr int kQt = kTcRows * D * 2;          // one Q tile: 2 halves x 128 rows x 128 B
+    static constexpr int kKc = kW2Chunk * D * 2;         // K chunk: 2 halves x 64 rows x 128 B
+    static constexpr int kVb = kBlock * D * 2;           // one V page
+    static constexpr int kVc = kW2Blocks * kVb;          // V chunk
+    static constexpr int kOffQ = 0, kOffK = kW2Tiles * kQt, kOffV = kOffK + kW2Bufs * kKc,
+                         kOffBar = kOffV + kW2Bufs * kVc;
+    static constexpr int kSmem = 1024 + kOffBar + 512;
+    static_assert(8 * 32 * (D + 4) * 4 <= kOffBar, "the epilogue stages 8 warps x 32 padded rows below the barriers");
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kW2Threads, 1)
+prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                   const PrefillArgs a) {
+    using C = W2Cfg;
+    constexpr int D = C::D;
+    constexpr bool kB = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t kIdescS = mma_idesc_f16(kTcRows, kW2Chunk, kB, false, false);
+    constexpr uint32_t kIdescO = mma_idesc_f16(kTcRows, D, kB, false, true);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t sb = (raw + 1023u) & ~1023u;
+    uint8_t* gb = smem_raw + (sb - raw);
+    const uint32_t sQ = sb + C::kOffQ, sK = sb + C::kOffK, sV = sb + C::kOffV;
+    // barriers, 8 B each (copy c & 3 of each per-chunk one): K stages, V stages,
+    // then per tile t "S_t(c) done", "P_t(c).V(c) done", "P_t(c) ready"; then the
+    // block-mask slots (c & 7) and "Q stored"; then the TMEM address and masks
+    const uint32_t bar0 = sb + C::kOffBar;
+    auto bar_k = [&](int c) { return bar0 + 8 * (c & 3); };
+    auto bar_v = [&](int c) { return bar0 + 32 + 8 * (c & 3); };
+    auto bar_s = [&](int t, int c) { return bar0 + 64 + 96 * t + 8 * (c & 3); };
+    auto bar_o = [&](int t, int c) { return bar0 + 96 + 96 * t + 8 * (c & 3); };
+    auto bar_p = [&](int t, int c) { return bar0 + 128 + 96 * t + 8 * (c & 3); };
+    auto bar_m = [&](int c) { return bar0 + 256 + 8 * (c & 7); };
+    const uint32_t bar_q = bar0 + 320;
+    const uint32_t tslot = bar0 + 328;
+    volatile uint32_t* cmask = reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 336);   // [8]
+    auto par4 = [](int c) { return (uint32_t)(c >> 2) & 1u; };
+    auto par8 = [](int c) { return (uint32_t)(c >> 3) & 1u; };
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool softmax = warp < 8, mma_warp = warp == 8, loader = warp >= 9;
+    const int tt = warp >> 2;                                   // softmax warps: their tile
+    const int tile = a.tiles_per_seq - 1 - (int)blockIdx.x;    // heaviest first
+    const int g = blockIdx.y, b = blockIdx.z;
+    if (tid == 0) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    grid_dependency_wait();
+    launch_dependents();
+
+    const int q0 = a.q_start[b];
+    const int n = a.q_start[b + 1] - q0;
+    const int L = a.context_lens[b];
+    if (n < 0 || n > a.max_new || L < n || L > a.max_blocks * kBlock) {
+        if (tile == 0 && g == 0 && tid == 0) flag_error(a.err, GQA_DEVERR_CONTEXT_LEN);
+        return;                                // uniform per CTA, before any allocation
+    }
+    const int rows = n * a.G;
+    const int row0 = tile * kW2Rows;
+    if (row0 >= rows) return;
+    const int base_pos = L - n;
+    const int tok_lo = row0 / a.G, tok_hi = min(rows - 1, row0 + kW2Rows - 1) / a.G;
+    const int att_lo = a.window > 0 ? max(0, base_pos + tok_lo - a.window + 1) : 0;
+    const int jb_lo = att_lo / kBlock;
+    const int jb_hi = (base_pos + tok_hi + kBlock) / kBlock;
+    const int nchunks = (jb_hi - jb_lo + kW2Blocks - 1) / kW2Blocks;
+
+    // ---- this thread's row (softmax warps) and the positions it attends, [lo, hi)
+    const int rr = row0 + (softmax ? tid : 0);                 // tid = 128 t + row of tile t
+    const bool live = softmax && rr < rows;
+    const int tk = live ? rr / a.G : 0;
+    const int hi = live ? base_pos + tk + 1 : 0;
+    const int lo = a.window > 0 ? hi - a.window : 0;
+
+    if (softmax) {
+        // This warp's 32 Q rows into its tile's swizzled K-major layout, whole
+        // rows at a time (16 lanes per row, 16 bytes each; rows past the
+        // prompt are zero), every load in flight before the stores.
+        constexpr int kLanesPerRow = D / 8, kRowsPerStep = 32 / kLanesPerRow, kSteps = 32 / kRowsPerStep;
+        const int c16 = lane % kLanesPerRow;
+        const int rl0 = 32 * (warp & 3) + lane / kLanesPerRow;        // first row of this lane in its tile
+        const int rq0 = row0 + 128 * tt + rl0;
+        int tq = rq0 / a.G, hq = rq0 - tq * a.G;
+        uint4 v[kSteps];
+#pragma unroll
+        for (int i = 0; i < kSteps; ++i) {
+            const int rq = rq0 + i * kRowsPerStep;
+            v[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (rq < rows) {
+                const long long src = ((long long)(q0 + tq) * a.H + (long long)g * a.G + hq) * D;
+                v[i] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + src) + c16);
+            }
+            hq += kRowsPerStep;
+            while (hq >= a.G) {
+                hq -= a.G;
+                ++tq;
+            }
+        }
+        const uint32_t qt = sQ + tt * C::kQt;
+#pragma unroll
+        for (int i = 0; i < kSteps; ++i) {
+            const int rl = rl0 + i * kRowsPerStep;
+            sts128(qt + (c16 >> 3) * (kTcRows * 128) + rl * 128 + (((c16 & 7) ^ (rl & 7)) << 4), v[i]);
+        }
+        fence_proxy_async_smem();              // Q visible to the tensor core
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 2 * kW2Bufs; ++i) mbar_init(bar0 + 8 * i, 1);       // K, V stages
+        for (int t = 0; t < kW2Tiles; ++t)
+            for (int i = 0; i < kW2Bufs; ++i) {
+                mbar_init(bar_s(t, i), 1);
+                mbar_init(bar_o(t, i), 1);
+                mbar_init(bar_p(t, i), 4);     // one arrival per softmax warp of the tile
+            }
+        for (int i = 0; i < 8; ++i) mbar_init(bar_m(i), 1);
+        mbar_init(bar_q, 8);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, kW2TmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + (tslot - sb));
+    if (softmax && lane == 0) mbar_arrive(bar_q);
+    bool ok = true;
+
+    if (loader) {
+        // ================================================== copy warps: 9 = K, 10 = V
+        const bool k_warp = warp == 9;
+        const uint64_t pol = l2_policy_evict_last();   // every query tile of the sequence re-reads them
+        int win_base = -(1 << 30), win_phys = -1;
+        int issued = 0;
+        auto issue_kv = [&](int c) {
+            int ph[kW2Blocks];
+#pragma unroll
+            for (int q = 0; q < kW2Blocks; ++q) {
+                const int j = jb_lo + kW2Blocks * c + q;
+                if (j - win_base >= 32 || j < win_base) {
+                    win_base = j;
+                    const int jj = j + lane;
+                    win_phys = -1;
+                    if (jj < jb_hi) {
+                        const int p = a.block_tables[(long long)b * a.max_blocks + jj];
+                        if (p < 0 || p >= a.num_blocks) flag_error(a.err, GQA_DEVERR_BLOCK_INDEX);
+                        else win_phys = p;
+                    }
+                }
+                ph[q] = __shfl_sync(kFull, win_phys, j - win_base);
+                if (j >= jb_hi) ph[q] = -1;
+            }
+            const uint32_t bar = k_warp ? bar_k(c) : bar_v(c);
+            if (lane == 0) {
+                uint32_t mask = 0;
+                int nval = 0;
+#pragma unroll
+                for (int q = 0; q < kW2Blocks; ++q)
+                    if (ph[q] >= 0) mask |= 1u << q, ++nval;
+                if (k_warp) {
+                    cmask[c & 7] = mask;
+                    mbar_arrive(bar_m(c));     // publishes the mask (release)
+                }
+                mbar_arrive_expect_tx(bar, (uint32_t)(nval * C::kVb));
+            }
+            fence_proxy_async_smem();          // earlier generic writes to the stage come first
+            __syncwarp();
+            if (!k_warp) {
+                // V: one box per page (the page map lands it as [half][slot][128 B])
+                if (lane < kW2Blocks) {
+                    int pq = ph[0];
+#pragma unroll
+                    for (int i = 1; i < kW2Blocks; ++i)
+                        if (lane == i) pq = ph[i];
+                    if (pq >= 0) {
+                        auto coord = [&](int which) { return which == 1 ? g : pq; };
+                        tma_load_5d(sV + (c & 3) * C::kVc + lane * C::kVb, &vmap, 0, 0, 0,
+                                    coord(a.page_perm[0]), coord(a.page_perm[1]), bar, pol);
+                    }
+                }
+            } else if (lane < 2 * kW2Blocks) {
+                // K: one lane per (block, 64-element half) box
+                const int q = lane >> 1, h = lane & 1;
+                int pq = ph[0];
+#pragma unroll
+                for (int i = 1; i < kW2Blocks; ++i)
+                    if (q == i) pq = ph[i];
+                if (pq >= 0) {
+                    auto coord = [&](int which) { return which == 0 ? 0 : (which == 1 ? g : pq); };
+                    const int y = coord(a.map_perm[0]), z = coord(a.map_perm[1]), w = coord(a.map_perm[2]);
+                    tma_load_4d(sK + (c & 3) * C::kKc + h * (kW2Chunk * 128) + q * (kBlock * 128), &kmap, h * 64,
+                                y, z, w, bar, pol);
+                }
+            }
+            ++issued;
+        };
+        for (int c = 0; c < min(nchunks, kW2Bufs); ++c) issue_kv(c);
+        for (int c = 0; c + kW2Bufs < nchunks && ok; ++c) {
+            // K(c+4) once both tiles' S(c) have read K(c); V(c+4) once both
+            // tiles' P(c).V(c) have read V(c)
+            ok = __all_sync(kFull, mbar_wait(k_warp ? bar_s(0, c) : bar_o(0, c), par4(c)) &&
+                                       mbar_wait(k_warp ? bar_s(1, c) : bar_o(1, c), par4(c)));
+            if (!ok) break;
+            issue_kv(c + kW2Bufs);
+        }
+        if (!ok && lane == 0) {
+            // let this CTA's copies land before the shared memory goes
+            flag_error(a.err, GQA_DEVERR_TIMEOUT);
+            for (int c = max(0, issued - kW2Bufs); c < issued; ++c)
+                mbar_wait(k_warp ? bar_k(c) : bar_v(c), par4(c), kWaitLimitNs / 4);
+        }
+    } else if (mma_warp) {
+        // ================================================== MMA warp (one lane issues)
+        if (lane == 0) {
+            auto issue_s = [&](int t, int c) {     // S_t(c) = Q_t K(c)^T into buffer c & 1
+                const uint32_t kb = sK + (c & 3) * C::kKc, qb = sQ + t * C::kQt;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint64_t ad = smem_desc_sw128(qb + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * (kW2Chunk * 128) + (ks & 3) * 32, 16, 1024);
+                    tc_mma_f16(tmem + kW2ColTile * t + kW2Chunk * (c & 1), ad, bd, kIdescS, ks > 0);
+                }
+            };
+            auto issue_pv = [&](int t, int c) {    // O_t += P_t(c) V(c), high part then low part per block
+                const uint32_t vb = sV + (c & 3) * C::kVc, pb = tmem + kW2ColTile * t + kW2Chunk * (c & 1);
+#pragma unroll
+                for (int jl = 0; jl < kW2Blocks; ++jl)
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+                        tc_mma_f16_ta(tmem + kW2ColTile * t + kW2ColO, pb + 16 * jl + 8 * part,
+                                      smem_desc_sw128(vb + jl * C::kVb, kBlock * 128, 1024), kIdescO,
+                                      !(c == 0 && jl == 0 && part == 0));
+            };
+            int s_done[kW2Tiles] = {0, 0}, o_done[kW2Tiles] = {0, 0};   // commits issued (failure path)
+            ok = mbar_wait(bar_q, 0u);
+            for (int c = 0; c < min(nchunks, 2) && ok; ++c) {
+                ok = mbar_wait(bar_k(c), par4(c));
+                tc_fence_after();
+                for (int t = 0; t < kW2Tiles && ok; ++t) {
+                    issue_s(t, c);
+                    tc_commit(bar_s(t, c));
+                    ++s_done[t];
+                }
+            }
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const bool more = c + 2 < nchunks;
+                for (int t = 0; t < kW2Tiles && ok; ++t) {
+                    // P_t(c) written over S_t(c); V(c) rows zeroed by tile 0's softmax
+                    ok = mbar_wait(bar_p(t, c), par4(c)) && mbar_wait(bar_v(c), par4(c));
+                    tc_fence_after();
+                    if (!ok) break;
+                    issue_pv(t, c);
+                    tc_commit(bar_o(t, c));
+                    ++o_done[t];
+                    if (more) {
+                        if (t == 0) {
+                            ok = mbar_wait(bar_k(c + 2), par4(c + 2));
+                            tc_fence_after();
+                            if (!ok) break;
+                        }
+                        issue_s(t, c + 2);     // after PV_t(c) in issue order: P_t(c) is read first
+                        tc_commit(bar_s(t, c + 2));
+                        ++s_done[t];
+                    }
+                }
+            }
+            if (!ok) {
+                // let this CTA's MMAs land before the tensor memory goes, each
+                // barrier's events in order
+                flag_error(a.err, GQA_DEVERR_TIMEOUT);
+                for (int t = 0; t < kW2Tiles; ++t) {
+                    for (int k = max(0, s_done[t] - kW2Bufs); k < s_done[t]; ++k)
+                        mbar_wait(bar_s(t, k), par4(k), kWaitLimitNs / 4);
+                    for (int k = max(0, o_done[t] - kW2Bufs); k < o_done[t]; ++k)
+                        mbar_wait(bar_o(t, k), par4(k), kWaitLimitNs / 4);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================================================== softmax warps: one row per thread
+        const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kW2ColTile * tt;
+        const uint32_t t_o = t_lane + kW2ColO;
+        float m = -INFINITY, l = 0.f;
+        for (int c = 0; c < nchunks; ++c) {
+            ok = __all_sync(kFull, mbar_wait(bar_s(tt, c), par4(c)));   // S_t(c) done
+            ok = ok && __all_sync(kFull, mbar_wait(bar_m(c), par8(c)));
+            if (!ok) break;
+            tc_fence_after();
+            const int cpos = (jb_lo + kW2Blocks * c) * kBlock;
+            const uint32_t bm = cmask[c & 7];
+            const uint32_t t_buf = t_lane + kW2Chunk * (c & 1);
+            float sv[kW2Chunk];
+            {
+                uint32_t r[kW2Chunk / 16][16];
+#pragma unroll
+                for (int u = 0; u < kW2Chunk / 16; ++u) tmem_ld16(t_buf + 16 * u, r[u]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < kW2Chunk / 16; ++u)
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) sv[16 * u + j] = __uint_as_float(r[u][j]) * a.scale_log2;
+            }
+            const bool whole = bm == (1u << kW2Blocks) - 1u && cpos >= lo && cpos + kW2Chunk <= hi;
+            if (!whole) {
+#pragma unroll
+                for (int j = 0; j < kW2Chunk; ++j) {
+                    const int pos = cpos + j;
+                    if (!((bm >> (j / kBlock)) & 1u) || pos < lo || pos >= hi) sv[j] = -INFINITY;
+                }
+            }
+            float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};      // short chains
+#pragma unroll
+            for (int j = 4; j < kW2Chunk; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], sv[j]);
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            // lazy rescale: keep the stale maximum while the new one stays within 2^slack
+            const bool old_live = m != -INFINITY;
+            const bool resc = mx > m + kTcSlack;
+            float alpha = 1.f;
+            if (resc) {
+                alpha = old_live ? fast_exp2(m - mx) : 0.f;
+                m = mx;
+            }
+            l *= alpha;
+            if (c > 0 && __any_sync(kFull, resc && old_live)) {       // O holds earlier chunks: scale it
+                // once P_t(c-1).V(c-1) has landed in it
+                ok = __all_sync(kFull, mbar_wait(bar_o(tt, c - 1), par4(c - 1)));
+                if (!ok) break;
+                tc_fence_after();
+                const float f = (resc && old_live) ? alpha : 1.f;
+#pragma unroll
+                for (int q = 0; q < D / 16; ++q) {
+                    uint32_t r16[16];
+                    tmem_ld16(t_o + 16 * q, r16);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r16[j] = __float_as_uint(__uint_as_float(r16[j]) * f);
+                    tmem_st16(t_o + 16 * q, r16);
+                }
+            }
+            const float mu = m == -INFINITY ? 0.f : m;    // a row with nothing attended yet: p = 0
+            float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+            // P over S: block jl's 16 tokens to columns [16jl, 16jl+16) of the
+            // buffer, 8 high then 8 low columns
+#pragma unroll
+            for (int jl = 0; jl < kW2Blocks; ++jl) {
+                uint32_t w16[16];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float x = fast_exp2(sv[16 * jl + 2 * e] - mu), y = fast_exp2(sv[16 * jl + 2 * e + 1] - mu);
+                    ps4[e & 3] += x + y;
+                    w16[e] = pack2<kB>(x, y);
+                    const float2 f = unpack2<kB>(w16[e]);
+                    w16[8 + e] = pack2<kB>(x - f.x, y - f.y);
+                }
+                tmem_st16(t_buf + 16 * jl, w16);
+            }
+            tmem_wait_st();
+            l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+            // V rows of tokens outside the sequence or of missing blocks hold
+            // arbitrary bits: tile 0 zeroes them (PV_1(c) is issued after PV_0(c))
+            if (tt == 0 && (bm != (1u << kW2Blocks) - 1u || cpos + kW2Chunk > L)) {
+                ok = __all_sync(kFull, mbar_wait(bar_v(c), par4(c)));
+                const uint32_t vb = sV + (c & 3) * C::kVc;
+                for (int i = tid; i < kW2Chunk * 2 * 8; i += kTcRows) {
+                    const int t = i / 16, h = (i / 8) % 2, ck = i % 8;
+                    if (((bm >> (t / kBlock)) & 1u) && cpos + t < L) continue;
+                    sts128(vb + (t / kBlock) * C::kVb + h * (kBlock * 128) + (t % kBlock) * 128 + ck * 16,
+                           make_uint4(0u, 0u, 0u, 0u));
+                }
+                fence_proxy_async_smem();      // zeroed V visible to the tensor core
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_p(tt, c));
+            if (!ok) break;
+        }
+        // ---- wait for both tiles' last P.V (its barrier copy's previous event,
+        // PV(n-5), was done before S(n-1) was), then normalise and store. Every
+        // copy has landed and every MMA is done once both have arrived, so the
+        // shared memory below the barriers stages the output.
+        if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(tt, nchunks - 1), par4(nchunks - 1)));
+        if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(1 - tt, nchunks - 1), par4(nchunks - 1)));
+        tc_fence_after();
+        if (ok) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            constexpr int kRowF = D + 4;       // padded row: 16-byte stores stay conflict-free
+            float* stage = reinterpret_cast<float*>(gb) + warp * 32 * kRowF;
+#pragma unroll
+            for (int q = 0; q < D / 16; ++q) {
+                uint32_t r16[16];
+                tmem_ld16(t_o + 16 * q, r16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4*>(stage + lane * kRowF + 16 * q + j) =
+                        make_float4(__uint_as_float(r16[j]) * inv, __uint_as_float(r16[j + 1]) * inv,
+                                    __uint_as_float(r16[j + 2]) * inv, __uint_as_float(r16[j + 3]) * inv);
+            }
+            __syncwarp();
+            const int wr0 = row0 + 32 * warp;  // this warp's first row (tile 1 = warps 4-7)
+            int tkr = wr0 / a.G, hr = wr0 - tkr * a.G;
+            for (int r = 0; r < 32; ++r) {
+                if (wr0 + r >= rows) break;
+                const long long orow = ((long long)(q0 + tkr) * a.H + (long long)g * a.G + hr) * D;
+                store4(a.out, a.out_dtype, orow + 4 * lane, *reinterpret_cast<const float4*>(stage + r * kRowF + 4 * lane));
+                if (++hr == a.G) {
+                    hr = 0;
+                    ++tkr;
+                }
+            }
+        } else if (lane == 0) {
+            flag_error(a.err, GQA_DEVERR_TIMEOUT);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kW2TmemCols);
+}
+
+template <typename T>
+const void* prefill_tc2_fn() {
+    return reinterpret_cast<const void*>(&prefill_tc2_kernel<T>);
+}
+
 template <typename T, int D>
 const void* prefill_tc_fn() {
     return reinterpret_cast<const void*>(&prefill_tc_kernel<T, D>);
@@ -843,10 +1301,16 @@ int launch_prefill(const PrefillLaunch& L) {
     const gqa_kv_cache_t& c = *L.cache;
     const int D = c.head_dim, K = c.num_kv_heads, G = L.num_heads / K;
     const bool tc = L.kernel != GQA_PREFILL_MMA_SYNC;
-    const int rows_per_cta = tc ? kTcRows : kPfRows;
+    // the wide tcgen05 form (two query tiles per CTA, 128-token chunks) serves head_dim 128
+    const bool wide = tc && D == 128 && (L.kernel == GQA_PREFILL_AUTO || L.kernel == GQA_PREFILL_TCGEN05_WIDE);
+    const int rows_per_cta = wide ? kW2Rows : tc ? kTcRows : kPfRows;
     const void* fn = nullptr;
     int smem = 0;
-    if (c.dtype == GQA_DTYPE_BF16) {
+    if (wide) {
+        if (c.dtype != GQA_DTYPE_BF16 && c.dtype != GQA_DTYPE_F16) return GQA_ERR_UNSUPPORTED;
+        fn = c.dtype == GQA_DTYPE_BF16 ? prefill_tc2_fn<__nv_bfloat16>() : prefill_tc2_fn<__half>();
+        smem = W2Cfg::kSmem;
+    } else if (c.dtype == GQA_DTYPE_BF16) {
         if (tc) {
             fn = D == 64 ? prefill_tc_fn<__nv_bfloat16, 64>() : prefill_tc_fn<__nv_bfloat16, 128>();
             smem = D == 64 ? TcCfg<__nv_bfloat16, 64>::kSmem : TcCfg<__nv_bfloat16, 128>::kSmem;
@@ -872,7 +1336,8 @@ int launch_prefill(const PrefillLaunch& L) {
     int page_perm[2] = {1, 2};
     if (tc && D == 128 && !encode_page_map(&vmap, c, c.v, page_perm))   // V a page per box
         return GQA_ERR_UNSUPPORTED;
-    if (ctas_per_sm(fn, tc ? kTcThreads : kPfWarps * 32, smem) < 1) return GQA_ERR_CUDA;
+    const int threads = wide ? kW2Threads : tc ? kTcThreads : kPfWarps * 32;
+    if (ctas_per_sm(fn, threads, smem) < 1) return GQA_ERR_CUDA;
 
     PrefillArgs a;
     a.q = L.q;
@@ -904,7 +1369,7 @@ int launch_prefill(const PrefillLaunch& L) {
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.tiles_per_seq, (unsigned)K, (unsigned)L.batch);
-    cfg.blockDim = dim3(tc ? kTcThreads : kPfWarps * 32);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = L.stream;
     cfg.attrs = pdl;

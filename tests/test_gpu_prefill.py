@@ -61,7 +61,7 @@ def _run(gq, case, q, q_start, news, **kw):
     return out
 
 
-KERNELS = [1, 2]      # tcgen05 (tensor memory), warp-level mma.sync
+KERNELS = [3, 1, 2]   # tcgen05 two-tile (head_dim 128; 64 takes the one-tile form), tcgen05 one-tile, mma.sync
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
