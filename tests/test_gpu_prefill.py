@@ -96,6 +96,19 @@ def test_prefill_long_prompt_and_empty_sequences(gq, oracle_mod, kernel):
     assert max_abs_err(_run(gq, case, q, q_start, news, kernel=kernel), ref) <= TOL
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("sign", [-1.0, 0.0])
+def test_prefill_negative_and_zero_scale(gq, oracle_mod, kernel, sign):
+    """A negative scale flips which key dominates (the wide kernel takes the
+    raw minimum then); a zero scale weights every attended position alike."""
+    news = [70, 200, 1]
+    lens = [90, 200, 40]
+    case, q, q_start = _case(lens, news, 32, 8, 128, "bf16", seed=95)
+    case.scale = sign * case.scale
+    ref = _reference(oracle_mod, case, q, news)
+    assert max_abs_err(_run(gq, case, q, q_start, news, kernel=kernel), ref) <= TOL
+
+
 def test_prefill_kernels_agree_on_large_scores(gq, oracle_mod):
     """Scores spread over hundreds of log2 units: the lazy rescale of the tensor-
     memory accumulator has to fire; both kernels match the oracle."""
