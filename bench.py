@@ -37,7 +37,9 @@ DEFAULT_WORKLOAD = "llama70b_bf16_b32_ragged"
 L2_BYTES = 129 * 2 ** 20
 KERNEL_NAME = "split_kv_kernel"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kv_kernel_traffic.txt")
-PREFILL_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "prefill_tc_kernel_traffic.txt")
+PREFILL_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "prefill_tc2_kernel_traffic.txt")
+# gqa_prefill's kernel choice (include/gqa_decode.h GQA_PREFILL_*) and the kernel it runs
+PREFILL_KERNEL = {"auto": 0, "tc1": 1, "mma_sync": 2, "tc2": 3}
 
 
 def attended_range(wl, L: int) -> tuple:
@@ -407,10 +409,14 @@ def run_prefill(args, wl):
     flops = prefill_flops(wl, lens.cpu().tolist())
     stream = torch.cuda.current_stream()
 
+    pk = PREFILL_KERNEL[args.prefill_kernel]
+    kname = {0: "prefill_tc2_kernel" if d == 128 else "prefill_tc_kernel", 1: "prefill_tc_kernel",
+             2: "prefill_kernel", 3: "prefill_tc2_kernel" if d == 128 else "prefill_tc_kernel"}[pk]
+
     def step(qq=q, kk=kn, vv=vn):
         gq.kv_append_varlen(cache, kk, vv, starts, T, case.block_table, pos, err=err)
         gq.gqa_prefill(cache, qq, starts, T, case.block_table, lens, case.scale, out=out,
-                       window=wl.window, err=err)
+                       window=wl.window, err=err, kernel=pk)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -444,7 +450,7 @@ def run_prefill(args, wl):
         gq.kv_append_varlen(cache, kn, vn, starts, T, case.block_table, pos, err=err)
         kev[i][0].record(stream)
         gq.gqa_prefill(cache, q, starts, T, case.block_table, lens, case.scale, out=out,
-                       window=wl.window, err=err)
+                       window=wl.window, err=err, kernel=pk)
         kev[i][1].record(stream)
     torch.cuda.synchronize()
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
@@ -454,7 +460,7 @@ def run_prefill(args, wl):
         stream, host_in, out, lambda qd, knd, vnd, od: (
             gq.kv_append_varlen(cache, knd, vnd, starts, T, case.block_table, pos, err=err),
             gq.gqa_prefill(cache, qd, starts, T, case.block_table, lens, case.scale, out=od,
-                           window=wl.window, err=err)),
+                           window=wl.window, err=err, kernel=pk)),
         args.steps, max(3, args.warmup))
     if err.item() != 0:
         raise RuntimeError(f"device error flags {err.item()}")
@@ -472,6 +478,7 @@ def run_prefill(args, wl):
             "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.cache_dtype, "data": "synthetic",
             "config": {"workload": wl.name, "batch": B, "prompt_tokens": T, "num_heads": H,
+                       "prefill_kernel": args.prefill_kernel,
                        "num_kv_heads": K, "head_dim": d, "context_lens": wl.lens,
                        "sliding_window": wl.window, "cache_dtype": wl.cache_dtype,
                        "block_size": 16, "block_table": "seeded shuffle",
@@ -480,8 +487,9 @@ def run_prefill(args, wl):
             "tokens_per_s": round(B * T * world / (ms * 1e-3), 1),
             "roofline": {"bound": "tensor", "achieved": round(kern_tf, 2), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(kern_tf / peak, 4),
-                         "traffic": read_traffic(wl.name, "auto", PREFILL_TRAFFIC_FILE, PREFILL_SOURCES),
-                         "kernel": "prefill_tc_kernel", "algorithmic_flops_per_launch": flops,
+                         "traffic": read_traffic(wl.name, args.prefill_kernel, PREFILL_TRAFFIC_FILE,
+                                                 PREFILL_SOURCES),
+                         "kernel": kname, "algorithmic_flops_per_launch": flops,
                          "avg_launch_ms": round(kern_ms, 5),
                          "kernel_timing": "CUDA events around every prefill launch, own timed loop",
                          "peak_source": f"{peak_kind} bf16_tflops (burst, cuBLAS; MEASURED_PEAKS.json)"},
@@ -914,6 +922,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--kernel", choices=["auto", "mma", "fma"], default="auto")
+    ap.add_argument("--prefill-kernel", choices=list(PREFILL_KERNEL), default="auto",
+                    help="prefill workloads: two-tile tcgen05 (tc2), one-tile tcgen05 (tc1) or mma.sync")
     ap.add_argument("--row-layout", choices=list(ROW_LAYOUT), default="auto",
                     help="more than 8 query rows per kv-head: 8-row unit streams or a shared ring")
     ap.add_argument("--seed", type=int, default=0)
