@@ -735,11 +735,17 @@ def _oracle_inputs(wl, case, rows):
     for b in rows:
         nb = -(-int(lens[b]) // 16)
         sel.append(table[b, :nb])
-    # copy only the blocks the sampled sequences use
+    # copy only the blocks the sampled sequences use. Any cache layout is one
+    # row of stride_block elements per physical block (the paged pool and the
+    # un-paged [B, S_pad, K, d] buffer alike); the ids are checked here, on the
+    # host, before they index device memory.
     import torch
-    ids = torch.from_numpy(np.concatenate(sel).astype(np.int64)).to(case.k_cache.device)
+    ids_np = np.concatenate(sel).astype(np.int64)
+    if ids_np.size and (ids_np.min() < 0 or ids_np.max() >= case.num_blocks):
+        raise ValueError("block table entry outside the cache")
+    ids = torch.from_numpy(ids_np).to(case.k_cache.device)
     def host(t):
-        t = t.index_select(0, ids)
+        t = t.reshape(case.num_blocks, -1).index_select(0, ids)
         if t.dtype in (torch.int8, torch.uint8):
             return t.cpu().numpy()
         if t.dtype == torch.float8_e4m3fn:
@@ -755,7 +761,8 @@ def _oracle_inputs(wl, case, rows):
     K, d = wl.num_kv_heads, wl.head_dim
     packed4 = wl.cache_dtype in ("i4", "i4kc")
     rd = d // 2 if packed4 else d                        # stored row (4-bit: bytes)
-    sb, sh, st = K * 16 * rd, 16 * rd, rd
+    div = 2 if packed4 else 1                            # strides count 4-bit elements
+    sb, sh, st = kp.shape[1], case.stride_head // div, case.stride_token // div
     kd = oracle.gather_dense(kp, new_table, sub_lens, sb, sh, st, K, rd)
     vd = oracle.gather_dense(vp, new_table, sub_lens, sb, sh, st, K, rd)
     if not packed4:

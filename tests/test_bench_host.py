@@ -70,3 +70,20 @@ def test_traffic_is_read_only_for_the_source_it_was_taken_on(tmp_path):
     assert bench.read_traffic("w", "auto", str(tmp_path / "missing.txt")) is None
     # the prefill kernel's figure is keyed to its own sources
     assert bench.read_traffic("w", "auto", str(f), bench.PREFILL_SOURCES) is None
+
+
+def test_oracle_inputs_follow_the_cache_layout(oracle_mod):
+    """The CPU baseline gathers its sequences from the cache block by block: on
+    the un-paged [B, S_pad, K, d] buffer and on a paged pool alike it must hand
+    the oracle the same inputs the parity tests build (so the same output)."""
+    import numpy as np
+    from helpers import oracle_for_case
+    wl = gi.WORKLOADS["tiny_f32_contiguous"]
+    case = gi.case_for(wl, seed=0, device="cpu", extra_tokens=0)
+    q, kd, vd, sl = bench._oracle_inputs(wl, case, [0, 1])
+    np.testing.assert_array_equal(oracle_mod.decode(q, kd, vd, sl, case.scale), oracle_for_case(case))
+    paged = dataclasses.replace(wl, cache_dtype="bf16", q_dtype="bf16", contiguous=False, batch=3)
+    case = gi.make_case(3, 8, 2, 64, [20, 33, 5], "bf16", seed=3)
+    q, kd, vd, sl = bench._oracle_inputs(paged, case, [0, 2])
+    np.testing.assert_array_equal(oracle_mod.decode(q, kd, vd, sl, case.scale),
+                                  oracle_for_case(case, rows=[0, 2]))

@@ -424,3 +424,18 @@ def test_step_replays_from_a_cuda_graph(gq):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert torch.equal(out, eager)
+
+
+def test_alternating_caches_keep_their_own_tensor_maps(gq):
+    """The library remembers encoded tensor maps by the cache's address, shape and
+    strides. Decoding two caches of the same shape in turn, and a third cache
+    with more blocks, must each give exactly what a first call on it gives."""
+    lens = [300, 17, 1000]
+    cases = [gi.make_case(len(lens), 32, 8, 128, lens, "bf16", seed=60 + i, device="cuda") for i in range(2)]
+    cases.append(gi.make_case(len(lens), 32, 8, 128, lens, "bf16", seed=62, device="cuda", spare_blocks=40))
+    first = [_run(gq, case).clone() for case in cases]
+    for _ in range(2):
+        for case, ref in zip(cases, first):
+            assert torch.equal(_run(gq, case), ref)
+    for case, ref in zip(cases, first):
+        assert max_abs_err(ref, oracle_for_case(case)) <= TOL
