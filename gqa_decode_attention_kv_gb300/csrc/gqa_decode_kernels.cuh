@@ -731,12 +731,11 @@ __device__ __forceinline__ void mma_compute(MmaState<C, D>& st, MmaFrags<C, D>& 
     const uint32_t hr = pack2<kB>(w0, w1), hr8 = pack2<kB>(w2, w3);
     const float2 fr = unpack2<kB>(hr), fr8 = unpack2<kB>(hr8);
     const uint32_t lr = pack2<kB>(w0 - fr.x, w1 - fr.y), lr8 = pack2<kB>(w2 - fr8.x, w3 - fr8.y);
-    const int srcA = 8 * c + (r >> 1), srcB = srcA + 4;
-    const uint32_t sel = (r & 1) ? 0x7632u : 0x5410u;
-    const uint32_t bh0 = __byte_perm(__shfl_sync(kFull, hr, srcA), __shfl_sync(kFull, hr, srcB), sel);
-    const uint32_t bh1 = __byte_perm(__shfl_sync(kFull, hr8, srcA), __shfl_sync(kFull, hr8, srcB), sel);
-    const uint32_t bl0 = __byte_perm(__shfl_sync(kFull, lr, srcA), __shfl_sync(kFull, lr, srcB), sel);
-    const uint32_t bl1 = __byte_perm(__shfl_sync(kFull, lr8, srcA), __shfl_sync(kFull, lr8, srcB), sel);
+    // hr holds (token r; heads 2c, 2c+1), hr8 the same for token r+8: an 8x8
+    // token x head matrix each, whose transposes are exactly the B fragments
+    // (tokens 2c, 2c+1 | 2c+8, 2c+9; head r) of P^T
+    const uint32_t bh0 = movmatrix_t(hr), bh1 = movmatrix_t(hr8);
+    const uint32_t bl0 = movmatrix_t(lr), bl1 = movmatrix_t(lr8);
 
     // ---- O^T[dim][head] += V^T . P^T (high part, then low part)
     if constexpr (!C::kCoded) {

@@ -300,6 +300,15 @@ __device__ __forceinline__ uint32_t i4_hi_pair(uint32_t w) {
 }
 
 // Byte permute with the PTX selector semantics: a selector nibble with bit 3
+// Transpose of an 8x8 matrix of 16-bit values held one register per lane in
+// the mma fragment layout (lane l: row l / 4, columns 2 (l % 4) and +1): lane l
+// gets row l / 4 of the transpose, columns 2 (l % 4) and +1 (warp-collective).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // set writes the sign of the chosen byte replicated over all 8 bits.
 __device__ __forceinline__ uint32_t prmt(uint32_t x, uint32_t y, uint32_t sel) {
     uint32_t r;
