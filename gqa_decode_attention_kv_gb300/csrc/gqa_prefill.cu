@@ -839,18 +839,56 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 //                           one tensor-memory round trip; P as a high and a low
 //                           16-bit part over the same columns
 //   O_t   += P_t(c) V(c)    A = P from tensor memory, B = V pages MN-major
-// The MMA warp issues S_0(0..1), S_1(0..1), then per chunk PV_0(c), S_0(c+2),
-// PV_1(c), S_1(c+2). The tensor pipe runs in issue order, so S_t(c+2)
-// overwrites P_t(c) only after PV_t(c) has read it, and S_t(c+1) is ready when
-// tile t's softmax finishes chunk c: each tile's softmax runs back to back
-// while the pipe works through both tiles' products. Warps 0-3 own tile 0's
-// rows, 4-7 tile 1's, 8 issues the MMAs, 9 copies K and 10 copies V (four
-// 16 KB stages each). Per-chunk barriers (stages, S done, P ready, P.V done)
+// Each tile has its own MMA warp, which issues S_t(0..1) and then per chunk
+// PV_t(c), S_t(c+2). Products into different accumulators are not ordered by
+// issue alone, so S_t(c+2) goes over P_t(c) only once PV_t(c)'s commit says it
+// has read it; S_t(c+1) is then ready when tile t's softmax finishes chunk c
+// (it was issued one chunk earlier). A single issuing thread gets about one
+// tcgen05.mma per ~100 cycles through, whatever the shape; M=128 products of
+// N <= 128 finish faster than that, so one issuer per tile doubles the rate at
+// which the SM's tensor core is fed. Warps 0-3 own tile 0's rows, 4-7 tile
+// 1's, 8 and 9 issue tile 0's and tile 1's MMAs, 10 copies K and 11 copies V
+// (four 16 KB stages each). Per-chunk barriers (stages, S done, P ready, P.V done)
 // come in four copies taken in turn by chunk and the block masks in eight, so
 // that no parity wait can fall two phases behind (as in the 32-token kernel).
+// Packed fp32 pairs (one 64-bit register pair): add, subtract and multiply
+// both halves in one instruction, each half rounded to nearest like the scalar
+// operation; and the three-input maximum. They halve the softmax's arithmetic
+// instruction count per score.
+__device__ __forceinline__ uint64_t f2_make(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 f2_split(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 constexpr int kW2Tiles = 2;
 constexpr int kW2Rows = kW2Tiles * kTcRows;      // query rows per CTA
-constexpr int kW2Threads = kW2Rows + 96;         // + MMA warp, K and V copy warps
+constexpr int kW2Threads = kW2Rows + 128;        // + two MMA warps, K and V copy warps
 constexpr int kW2Chunk = 64;                     // KV tokens per chunk: N of S, K of P.V
 constexpr int kW2Blocks = kW2Chunk / kBlock;
 constexpr int kW2Bufs = 4;                       // K and V stages; per-chunk barrier copies
@@ -901,7 +939,7 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     auto par8 = [](int c) { return (uint32_t)(c >> 3) & 1u; };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool softmax = warp < 8, mma_warp = warp == 8, loader = warp >= 9;
+    const bool softmax = warp < 8, mma_warp = warp == 8 || warp == 9, loader = warp >= 10;
     const int tt = warp >> 2;                                   // softmax warps: their tile
     const int tile = a.tiles_per_seq - 1 - (int)blockIdx.x;    // heaviest first
     const int g = blockIdx.y, b = blockIdx.z;
@@ -989,8 +1027,8 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     bool ok = true;
 
     if (loader) {
-        // ================================================== copy warps: 9 = K, 10 = V
-        const bool k_warp = warp == 9;
+        // ================================================== copy warps: 10 = K, 11 = V
+        const bool k_warp = warp == 10;
         const uint64_t pol = l2_policy_evict_last();   // every query tile of the sequence re-reads them
         int win_base = -(1 << 30), win_phys = -1;
         int issued = 0;
@@ -1072,9 +1110,10 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                 mbar_wait(k_warp ? bar_k(c) : bar_v(c), par4(c), kWaitLimitNs / 4);
         }
     } else if (mma_warp) {
-        // ================================================== MMA warp (one lane issues)
+        // ================================================== MMA warps: tile t = warp - 8 (one lane issues)
+        const int t = warp - 8;
         if (lane == 0) {
-            auto issue_s = [&](int t, int c) {     // S_t(c) = Q_t K(c)^T into buffer c & 1
+            auto issue_s = [&](int c) {            // S_t(c) = Q_t K(c)^T into buffer c & 1
                 const uint32_t kb = sK + (c & 3) * C::kKc, qb = sQ + t * C::kQt;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
@@ -1083,7 +1122,7 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                     tc_mma_f16(tmem + kW2ColTile * t + kW2Chunk * (c & 1), ad, bd, kIdescS, ks > 0);
                 }
             };
-            auto issue_pv = [&](int t, int c) {    // O_t += P_t(c) V(c), high part then low part per block
+            auto issue_pv = [&](int c) {           // O_t += P_t(c) V(c), high part then low part per block
                 const uint32_t vb = sV + (c & 3) * C::kVc, pb = tmem + kW2ColTile * t + kW2Chunk * (c & 1);
 #pragma unroll
                 for (int jl = 0; jl < kW2Blocks; ++jl)
@@ -1093,49 +1132,42 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                                       smem_desc_sw128(vb + jl * C::kVb, kBlock * 128, 1024), kIdescO,
                                       !(c == 0 && jl == 0 && part == 0));
             };
-            int s_done[kW2Tiles] = {0, 0}, o_done[kW2Tiles] = {0, 0};   // commits issued (failure path)
+            int s_done = 0, o_done = 0;            // commits issued (failure path)
             ok = mbar_wait(bar_q, 0u);
             for (int c = 0; c < min(nchunks, 2) && ok; ++c) {
                 ok = mbar_wait(bar_k(c), par4(c));
                 tc_fence_after();
-                for (int t = 0; t < kW2Tiles && ok; ++t) {
-                    issue_s(t, c);
-                    tc_commit(bar_s(t, c));
-                    ++s_done[t];
-                }
+                if (!ok) break;
+                issue_s(c);
+                tc_commit(bar_s(t, c));
+                ++s_done;
             }
             for (int c = 0; c < nchunks && ok; ++c) {
-                const bool more = c + 2 < nchunks;
-                for (int t = 0; t < kW2Tiles && ok; ++t) {
-                    // P_t(c) written over S_t(c); V(c) rows zeroed by tile 0's softmax
-                    ok = mbar_wait(bar_p(t, c), par4(c)) && mbar_wait(bar_v(c), par4(c));
+                // P_t(c) written over S_t(c); V(c) rows of missing tokens zeroed by tile t's softmax
+                ok = mbar_wait(bar_p(t, c), par4(c)) && mbar_wait(bar_v(c), par4(c));
+                tc_fence_after();
+                if (!ok) break;
+                issue_pv(c);
+                tc_commit(bar_o(t, c));
+                ++o_done;
+                if (c + 2 < nchunks) {
+                    // S_t(c+2) overwrites P_t(c): wait until PV_t(c) has read it
+                    ok = mbar_wait(bar_o(t, c), par4(c)) && mbar_wait(bar_k(c + 2), par4(c + 2));
                     tc_fence_after();
                     if (!ok) break;
-                    issue_pv(t, c);
-                    tc_commit(bar_o(t, c));
-                    ++o_done[t];
-                    if (more) {
-                        if (t == 0) {
-                            ok = mbar_wait(bar_k(c + 2), par4(c + 2));
-                            tc_fence_after();
-                            if (!ok) break;
-                        }
-                        issue_s(t, c + 2);     // after PV_t(c) in issue order: P_t(c) is read first
-                        tc_commit(bar_s(t, c + 2));
-                        ++s_done[t];
-                    }
+                    issue_s(c + 2);
+                    tc_commit(bar_s(t, c + 2));
+                    ++s_done;
                 }
             }
             if (!ok) {
-                // let this CTA's MMAs land before the tensor memory goes, each
+                // let this tile's MMAs land before the tensor memory goes, each
                 // barrier's events in order
                 flag_error(a.err, GQA_DEVERR_TIMEOUT);
-                for (int t = 0; t < kW2Tiles; ++t) {
-                    for (int k = max(0, s_done[t] - kW2Bufs); k < s_done[t]; ++k)
-                        mbar_wait(bar_s(t, k), par4(k), kWaitLimitNs / 4);
-                    for (int k = max(0, o_done[t] - kW2Bufs); k < o_done[t]; ++k)
-                        mbar_wait(bar_o(t, k), par4(k), kWaitLimitNs / 4);
-                }
+                for (int k = max(0, s_done - kW2Bufs); k < s_done; ++k)
+                    mbar_wait(bar_s(t, k), par4(k), kWaitLimitNs / 4);
+                for (int k = max(0, o_done - kW2Bufs); k < o_done; ++k)
+                    mbar_wait(bar_o(t, k), par4(k), kWaitLimitNs / 4);
             }
         }
         __syncwarp();
@@ -1158,10 +1190,15 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
 #pragma unroll
                 for (int u = 0; u < kW2Chunk / 16; ++u) tmem_ld16(t_buf + 16 * u, r[u]);
                 tmem_wait_ld();
+                const uint64_t sc2 = f2_make(a.scale_log2, a.scale_log2);
 #pragma unroll
                 for (int u = 0; u < kW2Chunk / 16; ++u)
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) sv[16 * u + j] = __uint_as_float(r[u][j]) * a.scale_log2;
+                    for (int j = 0; j < 16; j += 2) {
+                        const float2 v = f2_split(f2_mul(f2_make(__uint_as_float(r[u][j]), __uint_as_float(r[u][j + 1])), sc2));
+                        sv[16 * u + j] = v.x;
+                        sv[16 * u + j + 1] = v.y;
+                    }
             }
             const bool whole = bm == (1u << kW2Blocks) - 1u && cpos >= lo && cpos + kW2Chunk <= hi;
             if (!whole) {
@@ -1171,10 +1208,15 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                     if (!((bm >> (j / kBlock)) & 1u) || pos < lo || pos >= hi) sv[j] = -INFINITY;
                 }
             }
-            float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};      // short chains
+            float mx4[4];                                     // four short chains of 3-input maxima
 #pragma unroll
-            for (int j = 4; j < kW2Chunk; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], sv[j]);
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            for (int k = 0; k < 4; ++k) {
+                float v = fmaxf(sv[16 * k], sv[16 * k + 15]);
+#pragma unroll
+                for (int i = 1; i < 15; i += 2) v = fmax3(v, sv[16 * k + i], sv[16 * k + i + 1]);
+                mx4[k] = v;
+            }
+            const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
             // lazy rescale: keep the stale maximum while the new one stays within 2^slack
             const bool old_live = m != -INFINITY;
             const bool resc = mx > m + kTcSlack;
@@ -1201,7 +1243,8 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                 }
             }
             const float mu = m == -INFINITY ? 0.f : m;    // a row with nothing attended yet: p = 0
-            float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t mu2 = f2_make(mu, mu);
+            uint64_t ps2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
             // P over S: block jl's 16 tokens to columns [16jl, 16jl+16) of the
             // buffer, 8 high then 8 low columns
 #pragma unroll
@@ -1209,22 +1252,29 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                 uint32_t w16[16];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float x = fast_exp2(sv[16 * jl + 2 * e] - mu), y = fast_exp2(sv[16 * jl + 2 * e + 1] - mu);
-                    ps4[e & 3] += x + y;
+                    const float2 d = f2_split(f2_sub(f2_make(sv[16 * jl + 2 * e], sv[16 * jl + 2 * e + 1]), mu2));
+                    const float x = fast_exp2(d.x), y = fast_exp2(d.y);
+                    const uint64_t xy = f2_make(x, y);
+                    ps2[e & 1] = f2_add(ps2[e & 1], xy);
                     w16[e] = pack2<kB>(x, y);
                     const float2 f = unpack2<kB>(w16[e]);
-                    w16[8 + e] = pack2<kB>(x - f.x, y - f.y);
+                    const float2 r = f2_split(f2_sub(xy, f2_make(f.x, f.y)));
+                    w16[8 + e] = pack2<kB>(r.x, r.y);
                 }
                 tmem_st16(t_buf + 16 * jl, w16);
             }
             tmem_wait_st();
-            l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+            {
+                const float2 p0 = f2_split(ps2[0]), p1 = f2_split(ps2[1]);
+                l += (p0.x + p1.x) + (p0.y + p1.y);
+            }
             // V rows of tokens outside the sequence or of missing blocks hold
-            // arbitrary bits: tile 0 zeroes them (PV_1(c) is issued after PV_0(c))
-            if (tt == 0 && (bm != (1u << kW2Blocks) - 1u || cpos + kW2Chunk > L)) {
+            // arbitrary bits: each tile zeroes them before its P(c) is ready (its
+            // MMA warp issues P_t(c).V(c) only then); both tiles write the same zeros
+            if (bm != (1u << kW2Blocks) - 1u || cpos + kW2Chunk > L) {
                 ok = __all_sync(kFull, mbar_wait(bar_v(c), par4(c)));
                 const uint32_t vb = sV + (c & 3) * C::kVc;
-                for (int i = tid; i < kW2Chunk * 2 * 8; i += kTcRows) {
+                for (int i = tid & (kTcRows - 1); i < kW2Chunk * 2 * 8; i += kTcRows) {
                     const int t = i / 16, h = (i / 8) % 2, ck = i % 8;
                     if (((bm >> (t / kBlock)) & 1u) && cpos + t < L) continue;
                     sts128(vb + (t / kBlock) * C::kVb + h * (kBlock * 128) + (t % kBlock) * 128 + ck * 16,
@@ -1237,11 +1287,17 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             if (lane == 0) mbar_arrive(bar_p(tt, c));
             if (!ok) break;
         }
-        // ---- wait for both tiles' last P.V (its barrier copy's previous event,
-        // PV(n-5), was done before S(n-1) was), then normalise and store. Every
+        // ---- wait for both tiles' last P.V, then normalise and store. Every
         // copy has landed and every MMA is done once both have arrived, so the
-        // shared memory below the barriers stages the output.
+        // shared memory below the barriers stages the output. A parity wait on
+        // a barrier copy is sound for the copy's newest event once the event
+        // before it (four chunks back) is known to be done. Own tile: S_t(n-1)
+        // was seen, and it was issued only after PV_t(n-3) was done. Other
+        // tile: K(n-1) was copied only after its S(n-5), issued after its
+        // PV(n-7) was done; so its PV(n-3) is awaited first, whose commit
+        // covers PV(n-5), and then PV(n-1).
         if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(tt, nchunks - 1), par4(nchunks - 1)));
+        if (ok && nchunks >= 3) ok = __all_sync(kFull, mbar_wait(bar_o(1 - tt, nchunks - 3), par4(nchunks - 3)));
         if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(1 - tt, nchunks - 1), par4(nchunks - 1)));
         tc_fence_after();
         if (ok) {
@@ -1301,7 +1357,7 @@ int launch_prefill(const PrefillLaunch& L) {
     const gqa_kv_cache_t& c = *L.cache;
     const int D = c.head_dim, K = c.num_kv_heads, G = L.num_heads / K;
     const bool tc = L.kernel != GQA_PREFILL_MMA_SYNC;
-    // the wide tcgen05 form (two query tiles per CTA, 128-token chunks) serves head_dim 128
+    // the wide tcgen05 form (two query tiles per CTA, 64-token chunks) serves head_dim 128
     const bool wide = tc && D == 128 && (L.kernel == GQA_PREFILL_AUTO || L.kernel == GQA_PREFILL_TCGEN05_WIDE);
     const int rows_per_cta = wide ? kW2Rows : tc ? kTcRows : kPfRows;
     const void* fn = nullptr;
