@@ -39,7 +39,7 @@ KERNEL_NAME = "split_kv_kernel"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kv_kernel_traffic.txt")
 PREFILL_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "prefill_tc2_kernel_traffic.txt")
 # gqa_prefill's kernel choice (include/gqa_decode.h GQA_PREFILL_*) and the kernel it runs
-PREFILL_KERNEL = {"auto": 0, "tc1": 1, "mma_sync": 2, "tc2": 3}
+PREFILL_KERNEL = {"auto": 0, "tc1": 1, "mma_sync": 2, "tc2": 3, "tc2_paired": 4}
 
 
 def attended_range(wl, L: int) -> tuple:
@@ -411,7 +411,8 @@ def run_prefill(args, wl):
 
     pk = PREFILL_KERNEL[args.prefill_kernel]
     kname = {0: "prefill_tc2_kernel" if d == 128 else "prefill_tc_kernel", 1: "prefill_tc_kernel",
-             2: "prefill_kernel", 3: "prefill_tc2_kernel" if d == 128 else "prefill_tc_kernel"}[pk]
+             2: "prefill_kernel", 3: "prefill_tc2_kernel" if d == 128 else "prefill_tc_kernel",
+             4: "prefill_tc2_kernel" if d == 128 else "prefill_tc_kernel"}[pk]
 
     def step(qq=q, kk=kn, vv=vn):
         gq.kv_append_varlen(cache, kk, vv, starts, T, case.block_table, pos, err=err)

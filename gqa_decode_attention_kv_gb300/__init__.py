@@ -423,8 +423,10 @@ def gqa_prefill(cache: PagedKVCache, q: torch.Tensor, q_start: torch.Tensor, max
                 window: int = 0, err: Optional[torch.Tensor] = None, stream=None,
                 kernel: int = 0) -> torch.Tensor:
     """Causal attention of each sequence's new tokens (rows q_start[b] .. of q
-    [total, H, d]) over its paged cache, new tokens included. kernel: 0/1
-    tcgen05 (tensor memory), 2 warp-level mma.sync."""
+    [total, H, d]) over its paged cache, new tokens included. kernel: 0 auto,
+    1 tcgen05 one-tile (32-token chunks), 2 warp-level mma.sync, 3 tcgen05
+    two-tile (64-token chunks, head_dim 128), 4 tcgen05 one-tile with 64-token
+    chunks and two CTAs per SM (head_dim 128)."""
     args = (_dev(q, "q"), _dev(q_start, "q_start", True), _dev(block_tables, "block_tables", True),
             _dev(context_lens, "context_lens", True), _dev(err, "err", True, True))
     _check_query(cache, q, (3,))

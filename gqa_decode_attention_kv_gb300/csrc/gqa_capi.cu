@@ -309,7 +309,7 @@ int gqa_prefill(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int
                 int32_t sliding_window, void* out, int32_t out_dtype, int32_t kernel, int32_t* err_flag,
                 void* stream) {
     int st = check_cache(cache);
-    if (kernel < 0 || kernel > GQA_PREFILL_TCGEN05_WIDE) return GQA_ERR_INVALID;
+    if (kernel < 0 || kernel > GQA_PREFILL_TCGEN05_PAIRED) return GQA_ERR_INVALID;
     if (st != GQA_OK) return st;
     if (batch < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || max_new_tokens < 0 || sliding_window < 0)
         return GQA_ERR_INVALID;

@@ -886,33 +886,41 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return r;
 }
 
-constexpr int kW2Tiles = 2;
-constexpr int kW2Rows = kW2Tiles * kTcRows;      // query rows per CTA
-constexpr int kW2Threads = kW2Rows + 128;        // + two MMA warps, K and V copy warps
 constexpr int kW2Chunk = 64;                     // KV tokens per chunk: N of S, K of P.V
 constexpr int kW2Blocks = kW2Chunk / kBlock;
-constexpr int kW2Bufs = 4;                       // K and V stages; per-chunk barrier copies
-constexpr uint32_t kW2TmemCols = 512;
+constexpr int kW2Bufs = 4;                       // per-chunk barrier copies (c & 3)
 constexpr uint32_t kW2ColTile = 256;             // tile t: S buffers at 256t, 256t + 64
 constexpr uint32_t kW2ColO = 128;                //         O at 256t + 128
 
+// kTiles query tiles of 128 rows per CTA. Two tiles: one CTA per SM (512
+// tensor-memory columns, four K and four V stages). One tile: two CTAs per SM
+// (256 columns, two stages each, ~98 KB of shared memory), so that one CTA's
+// Q load and output store run under the other's products.
+template <int kTiles>
 struct W2Cfg {
     static constexpr int D = 128;
+    static constexpr int kRows = kTiles * kTcRows;       // query rows per CTA
+    static constexpr int kSoftWarps = 4 * kTiles;
+    static constexpr int kThreads = kRows + 32 * kTiles + 64;   // + an MMA warp per tile, K and V copy warps
+    static constexpr int kStages = kTiles == 2 ? 4 : 2;  // K and V stages
+    static constexpr int kCtasPerSm = kTiles == 2 ? 1 : 2;
+    static constexpr uint32_t kTmemCols = 256u * kTiles;
     static constexpr int kQt = kTcRows * D * 2;          // one Q tile: 2 halves x 128 rows x 128 B
     static constexpr int kKc = kW2Chunk * D * 2;         // K chunk: 2 halves x 64 rows x 128 B
     static constexpr int kVb = kBlock * D * 2;           // one V page
     static constexpr int kVc = kW2Blocks * kVb;          // V chunk
-    static constexpr int kOffQ = 0, kOffK = kW2Tiles * kQt, kOffV = kOffK + kW2Bufs * kKc,
-                         kOffBar = kOffV + kW2Bufs * kVc;
+    static constexpr int kOffQ = 0, kOffK = kTiles * kQt, kOffV = kOffK + kStages * kKc,
+                         kOffBar = kOffV + kStages * kVc;
     static constexpr int kSmem = 1024 + kOffBar + 512;
-    static_assert(8 * 32 * (D + 4) * 4 <= kOffBar, "the epilogue stages 8 warps x 32 padded rows below the barriers");
+    static_assert(kSoftWarps * 32 * (D + 4) * 4 <= kOffBar, "the epilogue stages 32 padded rows per softmax warp below the barriers");
 };
 
-template <typename T>
-__global__ void __launch_bounds__(kW2Threads, 1)
+template <typename T, int kTiles>
+__global__ void __launch_bounds__(W2Cfg<kTiles>::kThreads, W2Cfg<kTiles>::kCtasPerSm)
 prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                    const PrefillArgs a) {
-    using C = W2Cfg;
+    using C = W2Cfg<kTiles>;
+    constexpr int kS = C::kStages;
     constexpr int D = C::D;
     constexpr bool kB = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kIdescS = mma_idesc_f16(kTcRows, kW2Chunk, kB, false, false);
@@ -922,12 +930,14 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     const uint32_t sb = (raw + 1023u) & ~1023u;
     uint8_t* gb = smem_raw + (sb - raw);
     const uint32_t sQ = sb + C::kOffQ, sK = sb + C::kOffK, sV = sb + C::kOffV;
-    // barriers, 8 B each (copy c & 3 of each per-chunk one): K stages, V stages,
-    // then per tile t "S_t(c) done", "P_t(c).V(c) done", "P_t(c) ready"; then the
+    // barriers, 8 B each: K stages, V stages (stage c % kS), then per tile t
+    // "S_t(c) done", "P_t(c).V(c) done", "P_t(c) ready" (copy c & 3); then the
     // block-mask slots (c & 7) and "Q stored"; then the TMEM address and masks
     const uint32_t bar0 = sb + C::kOffBar;
-    auto bar_k = [&](int c) { return bar0 + 8 * (c & 3); };
-    auto bar_v = [&](int c) { return bar0 + 32 + 8 * (c & 3); };
+    auto stage = [](int c) { return c % kS; };
+    auto par_st = [](int c) { return (uint32_t)(c / kS) & 1u; };
+    auto bar_k = [&](int c) { return bar0 + 8 * stage(c); };
+    auto bar_v = [&](int c) { return bar0 + 32 + 8 * stage(c); };
     auto bar_s = [&](int t, int c) { return bar0 + 64 + 96 * t + 8 * (c & 3); };
     auto bar_o = [&](int t, int c) { return bar0 + 96 + 96 * t + 8 * (c & 3); };
     auto bar_p = [&](int t, int c) { return bar0 + 128 + 96 * t + 8 * (c & 3); };
@@ -939,7 +949,8 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     auto par8 = [](int c) { return (uint32_t)(c >> 3) & 1u; };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool softmax = warp < 8, mma_warp = warp == 8 || warp == 9, loader = warp >= 10;
+    const bool softmax = warp < C::kSoftWarps, loader = warp >= C::kSoftWarps + kTiles;
+    const bool mma_warp = !softmax && !loader;
     const int tt = warp >> 2;                                   // softmax warps: their tile
     const int tile = a.tiles_per_seq - 1 - (int)blockIdx.x;    // heaviest first
     const int g = blockIdx.y, b = blockIdx.z;
@@ -958,10 +969,10 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         return;                                // uniform per CTA, before any allocation
     }
     const int rows = n * a.G;
-    const int row0 = tile * kW2Rows;
+    const int row0 = tile * C::kRows;
     if (row0 >= rows) return;
     const int base_pos = L - n;
-    const int tok_lo = row0 / a.G, tok_hi = min(rows - 1, row0 + kW2Rows - 1) / a.G;
+    const int tok_lo = row0 / a.G, tok_hi = min(rows - 1, row0 + C::kRows - 1) / a.G;
     const int att_lo = a.window > 0 ? max(0, base_pos + tok_lo - a.window + 1) : 0;
     const int jb_lo = att_lo / kBlock;
     const int jb_hi = (base_pos + tok_hi + kBlock) / kBlock;
@@ -1007,18 +1018,21 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         fence_proxy_async_smem();              // Q visible to the tensor core
     }
     if (tid == 0) {
-        for (int i = 0; i < 2 * kW2Bufs; ++i) mbar_init(bar0 + 8 * i, 1);       // K, V stages
-        for (int t = 0; t < kW2Tiles; ++t)
+        for (int i = 0; i < kS; ++i) {
+            mbar_init(bar_k(i), 1);            // K, V stages
+            mbar_init(bar_v(i), 1);
+        }
+        for (int t = 0; t < kTiles; ++t)
             for (int i = 0; i < kW2Bufs; ++i) {
                 mbar_init(bar_s(t, i), 1);
                 mbar_init(bar_o(t, i), 1);
                 mbar_init(bar_p(t, i), 4);     // one arrival per softmax warp of the tile
             }
         for (int i = 0; i < 8; ++i) mbar_init(bar_m(i), 1);
-        mbar_init(bar_q, 8);
+        mbar_init(bar_q, C::kSoftWarps);
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(tslot, kW2TmemCols);
+    if (warp == 0) tmem_alloc(tslot, C::kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1027,8 +1041,8 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     bool ok = true;
 
     if (loader) {
-        // ================================================== copy warps: 10 = K, 11 = V
-        const bool k_warp = warp == 10;
+        // ================================================== copy warps: K, then V
+        const bool k_warp = warp == C::kSoftWarps + kTiles;
         const uint64_t pol = l2_policy_evict_last();   // every query tile of the sequence re-reads them
         int win_base = -(1 << 30), win_phys = -1;
         int issued = 0;
@@ -1074,7 +1088,7 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                         if (lane == i) pq = ph[i];
                     if (pq >= 0) {
                         auto coord = [&](int which) { return which == 1 ? g : pq; };
-                        tma_load_5d(sV + (c & 3) * C::kVc + lane * C::kVb, &vmap, 0, 0, 0,
+                        tma_load_5d(sV + stage(c) * C::kVc + lane * C::kVb, &vmap, 0, 0, 0,
                                     coord(a.page_perm[0]), coord(a.page_perm[1]), bar, pol);
                     }
                 }
@@ -1088,33 +1102,35 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                 if (pq >= 0) {
                     auto coord = [&](int which) { return which == 0 ? 0 : (which == 1 ? g : pq); };
                     const int y = coord(a.map_perm[0]), z = coord(a.map_perm[1]), w = coord(a.map_perm[2]);
-                    tma_load_4d(sK + (c & 3) * C::kKc + h * (kW2Chunk * 128) + q * (kBlock * 128), &kmap, h * 64,
+                    tma_load_4d(sK + stage(c) * C::kKc + h * (kW2Chunk * 128) + q * (kBlock * 128), &kmap, h * 64,
                                 y, z, w, bar, pol);
                 }
             }
             ++issued;
         };
-        for (int c = 0; c < min(nchunks, kW2Bufs); ++c) issue_kv(c);
-        for (int c = 0; c + kW2Bufs < nchunks && ok; ++c) {
-            // K(c+4) once both tiles' S(c) have read K(c); V(c+4) once both
-            // tiles' P(c).V(c) have read V(c)
-            ok = __all_sync(kFull, mbar_wait(k_warp ? bar_s(0, c) : bar_o(0, c), par4(c)) &&
-                                       mbar_wait(k_warp ? bar_s(1, c) : bar_o(1, c), par4(c)));
+        for (int c = 0; c < min(nchunks, kS); ++c) issue_kv(c);
+        for (int c = 0; c + kS < nchunks && ok; ++c) {
+            // K(c+kS) once every tile's S(c) has read K(c); V(c+kS) once every
+            // tile's P(c).V(c) has read V(c)
+            bool w = true;
+#pragma unroll
+            for (int t = 0; t < kTiles; ++t) w = w && mbar_wait(k_warp ? bar_s(t, c) : bar_o(t, c), par4(c));
+            ok = __all_sync(kFull, w);
             if (!ok) break;
-            issue_kv(c + kW2Bufs);
+            issue_kv(c + kS);
         }
         if (!ok && lane == 0) {
             // let this CTA's copies land before the shared memory goes
             flag_error(a.err, GQA_DEVERR_TIMEOUT);
-            for (int c = max(0, issued - kW2Bufs); c < issued; ++c)
-                mbar_wait(k_warp ? bar_k(c) : bar_v(c), par4(c), kWaitLimitNs / 4);
+            for (int c = max(0, issued - kS); c < issued; ++c)
+                mbar_wait(k_warp ? bar_k(c) : bar_v(c), par_st(c), kWaitLimitNs / 4);
         }
     } else if (mma_warp) {
-        // ================================================== MMA warps: tile t = warp - 8 (one lane issues)
-        const int t = warp - 8;
+        // ================================================== MMA warps: one per tile (one lane issues)
+        const int t = warp - C::kSoftWarps;
         if (lane == 0) {
             auto issue_s = [&](int c) {            // S_t(c) = Q_t K(c)^T into buffer c & 1
-                const uint32_t kb = sK + (c & 3) * C::kKc, qb = sQ + t * C::kQt;
+                const uint32_t kb = sK + stage(c) * C::kKc, qb = sQ + t * C::kQt;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint64_t ad = smem_desc_sw128(qb + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
@@ -1123,7 +1139,7 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                 }
             };
             auto issue_pv = [&](int c) {           // O_t += P_t(c) V(c), high part then low part per block
-                const uint32_t vb = sV + (c & 3) * C::kVc, pb = tmem + kW2ColTile * t + kW2Chunk * (c & 1);
+                const uint32_t vb = sV + stage(c) * C::kVc, pb = tmem + kW2ColTile * t + kW2Chunk * (c & 1);
 #pragma unroll
                 for (int jl = 0; jl < kW2Blocks; ++jl)
 #pragma unroll
@@ -1135,7 +1151,7 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             int s_done = 0, o_done = 0;            // commits issued (failure path)
             ok = mbar_wait(bar_q, 0u);
             for (int c = 0; c < min(nchunks, 2) && ok; ++c) {
-                ok = mbar_wait(bar_k(c), par4(c));
+                ok = mbar_wait(bar_k(c), par_st(c));
                 tc_fence_after();
                 if (!ok) break;
                 issue_s(c);
@@ -1144,7 +1160,7 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             }
             for (int c = 0; c < nchunks && ok; ++c) {
                 // P_t(c) written over S_t(c); V(c) rows of missing tokens zeroed by tile t's softmax
-                ok = mbar_wait(bar_p(t, c), par4(c)) && mbar_wait(bar_v(c), par4(c));
+                ok = mbar_wait(bar_p(t, c), par4(c)) && mbar_wait(bar_v(c), par_st(c));
                 tc_fence_after();
                 if (!ok) break;
                 issue_pv(c);
@@ -1152,7 +1168,7 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                 ++o_done;
                 if (c + 2 < nchunks) {
                     // S_t(c+2) overwrites P_t(c): wait until PV_t(c) has read it
-                    ok = mbar_wait(bar_o(t, c), par4(c)) && mbar_wait(bar_k(c + 2), par4(c + 2));
+                    ok = mbar_wait(bar_o(t, c), par4(c)) && mbar_wait(bar_k(c + 2), par_st(c + 2));
                     tc_fence_after();
                     if (!ok) break;
                     issue_s(c + 2);
@@ -1272,8 +1288,8 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             // arbitrary bits: each tile zeroes them before its P(c) is ready (its
             // MMA warp issues P_t(c).V(c) only then); both tiles write the same zeros
             if (bm != (1u << kW2Blocks) - 1u || cpos + kW2Chunk > L) {
-                ok = __all_sync(kFull, mbar_wait(bar_v(c), par4(c)));
-                const uint32_t vb = sV + (c & 3) * C::kVc;
+                ok = __all_sync(kFull, mbar_wait(bar_v(c), par_st(c)));
+                const uint32_t vb = sV + stage(c) * C::kVc;
                 for (int i = tid & (kTcRows - 1); i < kW2Chunk * 2 * 8; i += kTcRows) {
                     const int t = i / 16, h = (i / 8) % 2, ck = i % 8;
                     if (((bm >> (t / kBlock)) & 1u) && cpos + t < L) continue;
@@ -1297,8 +1313,10 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         // PV(n-7) was done; so its PV(n-3) is awaited first, whose commit
         // covers PV(n-5), and then PV(n-1).
         if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(tt, nchunks - 1), par4(nchunks - 1)));
-        if (ok && nchunks >= 3) ok = __all_sync(kFull, mbar_wait(bar_o(1 - tt, nchunks - 3), par4(nchunks - 3)));
-        if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(1 - tt, nchunks - 1), par4(nchunks - 1)));
+        if (kTiles == 2) {
+            if (ok && nchunks >= 3) ok = __all_sync(kFull, mbar_wait(bar_o(1 - tt, nchunks - 3), par4(nchunks - 3)));
+            if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(1 - tt, nchunks - 1), par4(nchunks - 1)));
+        }
         tc_fence_after();
         if (ok) {
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -1333,12 +1351,12 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kW2TmemCols);
+    if (warp == 0) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <typename T>
+template <typename T, int kTiles>
 const void* prefill_tc2_fn() {
-    return reinterpret_cast<const void*>(&prefill_tc2_kernel<T>);
+    return reinterpret_cast<const void*>(&prefill_tc2_kernel<T, kTiles>);
 }
 
 template <typename T, int D>
@@ -1357,15 +1375,20 @@ int launch_prefill(const PrefillLaunch& L) {
     const gqa_kv_cache_t& c = *L.cache;
     const int D = c.head_dim, K = c.num_kv_heads, G = L.num_heads / K;
     const bool tc = L.kernel != GQA_PREFILL_MMA_SYNC;
-    // the wide tcgen05 form (two query tiles per CTA, 64-token chunks) serves head_dim 128
-    const bool wide = tc && D == 128 && (L.kernel == GQA_PREFILL_AUTO || L.kernel == GQA_PREFILL_TCGEN05_WIDE);
-    const int rows_per_cta = wide ? kW2Rows : tc ? kTcRows : kPfRows;
+    // the 64-token-chunk tcgen05 forms serve head_dim 128: two query tiles per
+    // CTA (one CTA per SM) or one (two CTAs per SM)
+    const bool wide2 = tc && D == 128 && (L.kernel == GQA_PREFILL_AUTO || L.kernel == GQA_PREFILL_TCGEN05_WIDE);
+    const bool wide1 = tc && D == 128 && L.kernel == GQA_PREFILL_TCGEN05_PAIRED;
+    const bool wide = wide1 || wide2;
+    const int rows_per_cta = wide2 ? W2Cfg<2>::kRows : wide1 ? W2Cfg<1>::kRows : tc ? kTcRows : kPfRows;
     const void* fn = nullptr;
     int smem = 0;
     if (wide) {
         if (c.dtype != GQA_DTYPE_BF16 && c.dtype != GQA_DTYPE_F16) return GQA_ERR_UNSUPPORTED;
-        fn = c.dtype == GQA_DTYPE_BF16 ? prefill_tc2_fn<__nv_bfloat16>() : prefill_tc2_fn<__half>();
-        smem = W2Cfg::kSmem;
+        const bool bf = c.dtype == GQA_DTYPE_BF16;
+        fn = wide2 ? (bf ? prefill_tc2_fn<__nv_bfloat16, 2>() : prefill_tc2_fn<__half, 2>())
+                   : (bf ? prefill_tc2_fn<__nv_bfloat16, 1>() : prefill_tc2_fn<__half, 1>());
+        smem = wide2 ? W2Cfg<2>::kSmem : W2Cfg<1>::kSmem;
     } else if (c.dtype == GQA_DTYPE_BF16) {
         if (tc) {
             fn = D == 64 ? prefill_tc_fn<__nv_bfloat16, 64>() : prefill_tc_fn<__nv_bfloat16, 128>();
@@ -1392,7 +1415,7 @@ int launch_prefill(const PrefillLaunch& L) {
     int page_perm[2] = {1, 2};
     if (tc && D == 128 && !encode_page_map(&vmap, c, c.v, page_perm))   // V a page per box
         return GQA_ERR_UNSUPPORTED;
-    const int threads = wide ? kW2Threads : tc ? kTcThreads : kPfWarps * 32;
+    const int threads = wide2 ? W2Cfg<2>::kThreads : wide1 ? W2Cfg<1>::kThreads : tc ? kTcThreads : kPfWarps * 32;
     if (ctas_per_sm(fn, threads, smem) < 1) return GQA_ERR_CUDA;
 
     PrefillArgs a;

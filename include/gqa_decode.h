@@ -251,10 +251,12 @@ GQA_API int gqa_kv_append_varlen(const gqa_kv_cache_t *cache, const void *k_new,
  *  kernel         GQA_PREFILL_AUTO: GQA_PREFILL_TCGEN05_WIDE for head_dim 128,
  *                 else GQA_PREFILL_TCGEN05. GQA_PREFILL_TCGEN05_WIDE (head_dim
  *                 128 only): one CTA per SM, two 128-row query tiles sharing
- *                 128-token K/V chunks on the 5th-generation tensor cores, all
- *                 512 tensor-memory columns. GQA_PREFILL_TCGEN05: 128-row query
- *                 tiles, 32-token chunks, two CTAs per SM. GQA_PREFILL_MMA_SYNC:
- *                 64-row tiles on warp-level mma.sync. The last two are the
+ *                 64-token K/V chunks on the 5th-generation tensor cores, all
+ *                 512 tensor-memory columns. GQA_PREFILL_TCGEN05_PAIRED (head_dim
+ *                 128 only): the same with one query tile per CTA and two CTAs
+ *                 per SM. GQA_PREFILL_TCGEN05: 128-row query tiles, 32-token
+ *                 chunks, two CTAs per SM. GQA_PREFILL_MMA_SYNC: 64-row tiles on
+ *                 warp-level mma.sync. The forms other than AUTO's choice are the
  *                 measured alternatives.
  *  Limits: BF16/F16 caches; head_dim 64 or 128; batch and K <= 65535.
  */
@@ -262,6 +264,7 @@ GQA_API int gqa_kv_append_varlen(const gqa_kv_cache_t *cache, const void *k_new,
 #define GQA_PREFILL_TCGEN05 1
 #define GQA_PREFILL_MMA_SYNC 2
 #define GQA_PREFILL_TCGEN05_WIDE 3
+#define GQA_PREFILL_TCGEN05_PAIRED 4
 GQA_API int gqa_prefill(const gqa_kv_cache_t *cache, const void *q, int32_t q_dtype, int32_t num_heads,
                 const int32_t *q_start, int32_t max_new_tokens, const int32_t *block_tables,
                 int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch, float scale,

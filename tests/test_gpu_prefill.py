@@ -61,7 +61,8 @@ def _run(gq, case, q, q_start, news, **kw):
     return out
 
 
-KERNELS = [3, 1, 2]   # tcgen05 two-tile (head_dim 128; 64 takes the one-tile form), tcgen05 one-tile, mma.sync
+KERNELS = [3, 4, 1, 2]   # tcgen05 two-tile and its one-tile-per-CTA twin (head_dim 128; 64 takes the
+                         # 32-token form), tcgen05 32-token one-tile, mma.sync
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
