@@ -338,6 +338,7 @@ int gqa_prefill(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int
     L.out = out;
     L.out_dtype = out_dtype;
     L.kernel = kernel;
+    L.num_sms = num_sms_of(-1);
     L.err = err_flag;
     L.stream = static_cast<cudaStream_t>(stream);
     return launch_prefill(L);

@@ -851,6 +851,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
 // (four 16 KB stages each). Per-chunk barriers (stages, S done, P ready, P.V done)
 // come in four copies taken in turn by chunk and the block masks in eight, so
 // that no parity wait can fall two phases behind (as in the 32-token kernel).
+// 16-byte cp.async into shared memory; src_bytes < 16 zero-fills the rest.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Packed fp32 pairs (one 64-bit register pair): add, subtract and multiply
 // both halves in one instruction, each half rounded to nearest like the scalar
 // operation; and the three-input maximum. They halve the softmax's arithmetic
@@ -894,8 +900,10 @@ constexpr uint32_t kW2ColO = 128;                //         O at 256t + 128
 
 // kTiles query tiles of 128 rows per CTA. Two tiles: one CTA per SM (512
 // tensor-memory columns, four K and four V stages). One tile: two CTAs per SM
-// (256 columns, two stages each, ~98 KB of shared memory), so that one CTA's
-// Q load and output store run under the other's products.
+// (256 columns, two stages each, ~108 KB of shared memory). Either way the CTAs
+// are persistent: each walks its share of the (query tile, kv-head, sequence)
+// items, and the next item's Q load and first S products run while the softmax
+// warps store the last item's output.
 template <int kTiles>
 struct W2Cfg {
     static constexpr int D = 128;
@@ -909,10 +917,11 @@ struct W2Cfg {
     static constexpr int kKc = kW2Chunk * D * 2;         // K chunk: 2 halves x 64 rows x 128 B
     static constexpr int kVb = kBlock * D * 2;           // one V page
     static constexpr int kVc = kW2Blocks * kVb;          // V chunk
+    static constexpr int kStgRowF = 20;                  // output staging: 16 columns + 4 pad per row
     static constexpr int kOffQ = 0, kOffK = kTiles * kQt, kOffV = kOffK + kStages * kKc,
-                         kOffBar = kOffV + kStages * kVc;
+                         kOffStg = kOffV + kStages * kVc, kOffBar = kOffStg + kSoftWarps * 32 * kStgRowF * 4;
     static constexpr int kSmem = 1024 + kOffBar + 512;
-    static_assert(kSoftWarps * 32 * (D + 4) * 4 <= kOffBar, "the epilogue stages 32 padded rows per softmax warp below the barriers");
+    static_assert(kSmem * kCtasPerSm <= 227 * 1024, "CTAs per SM fit the shared memory");
 };
 
 template <typename T, int kTiles>
@@ -930,9 +939,10 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     const uint32_t sb = (raw + 1023u) & ~1023u;
     uint8_t* gb = smem_raw + (sb - raw);
     const uint32_t sQ = sb + C::kOffQ, sK = sb + C::kOffK, sV = sb + C::kOffV;
-    // barriers, 8 B each: K stages, V stages (stage c % kS), then per tile t
-    // "S_t(c) done", "P_t(c).V(c) done", "P_t(c) ready" (copy c & 3); then the
-    // block-mask slots (c & 7) and "Q stored"; then the TMEM address and masks
+    // barriers, 8 B each: K stages, V stages (stage G % kS), then per tile t
+    // "S_t(G) done", "P_t(G).V(G) done", "P_t(G) ready" (copy G & 3); then the
+    // block-mask slots (G & 7), the TMEM address, the masks and per tile "Q_t
+    // stored". G counts the CTA's chunks across its items.
     const uint32_t bar0 = sb + C::kOffBar;
     auto stage = [](int c) { return c % kS; };
     auto par_st = [](int c) { return (uint32_t)(c / kS) & 1u; };
@@ -942,9 +952,9 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     auto bar_o = [&](int t, int c) { return bar0 + 96 + 96 * t + 8 * (c & 3); };
     auto bar_p = [&](int t, int c) { return bar0 + 128 + 96 * t + 8 * (c & 3); };
     auto bar_m = [&](int c) { return bar0 + 256 + 8 * (c & 7); };
-    const uint32_t bar_q = bar0 + 320;
-    const uint32_t tslot = bar0 + 328;
-    volatile uint32_t* cmask = reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 336);   // [8]
+    auto bar_q = [&](int t) { return bar0 + 320 + 8 * t; };
+    const uint32_t tslot = bar0 + 336;
+    volatile uint32_t* cmask = reinterpret_cast<volatile uint32_t*>(gb + C::kOffBar + 344);   // [8]
     auto par4 = [](int c) { return (uint32_t)(c >> 2) & 1u; };
     auto par8 = [](int c) { return (uint32_t)(c >> 3) & 1u; };
 
@@ -952,84 +962,69 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     const bool softmax = warp < C::kSoftWarps, loader = warp >= C::kSoftWarps + kTiles;
     const bool mma_warp = !softmax && !loader;
     const int tt = warp >> 2;                                   // softmax warps: their tile
-    const int tile = a.tiles_per_seq - 1 - (int)blockIdx.x;    // heaviest first
-    const int g = blockIdx.y, b = blockIdx.z;
     if (tid == 0) {
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
     }
+
+    // ---- the CTA's items: (query tile, kv-head, sequence), the heaviest tiles
+    // first, dealt to the CTAs in snake order (round r goes left to right when r
+    // is even, right to left when odd) so that each CTA's total stays close
+    struct Item {
+        int g, b, q0, n, L, rows, row0, base_pos, jb_lo, jb_hi, nchunks;
+    };
+    const int n_items = a.tiles_per_seq * a.K * a.B;
+    const int P = (int)gridDim.x, j = (int)blockIdx.x;
+    auto item_at = [&](int i, Item& it) -> bool {    // false: nothing to do
+        const int kb = a.K * a.B;
+        const int level = i / kb, rem = i - level * kb;
+        it.b = rem / a.K;
+        it.g = rem - it.b * a.K;
+        const int tile = a.tiles_per_seq - 1 - level;
+        it.q0 = a.q_start[it.b];
+        it.n = a.q_start[it.b + 1] - it.q0;
+        it.L = a.context_lens[it.b];
+        if (it.n < 0 || it.n > a.max_new || it.L < it.n || it.L > a.max_blocks * kBlock) {
+            if (tile == 0 && it.g == 0 && tid == 0) flag_error(a.err, GQA_DEVERR_CONTEXT_LEN);
+            return false;
+        }
+        it.rows = it.n * a.G;
+        it.row0 = tile * C::kRows;
+        if (it.row0 >= it.rows) return false;
+        it.base_pos = it.L - it.n;
+        const int tok_lo = it.row0 / a.G, tok_hi = min(it.rows - 1, it.row0 + C::kRows - 1) / a.G;
+        const int att_lo = a.window > 0 ? max(0, it.base_pos + tok_lo - a.window + 1) : 0;
+        it.jb_lo = att_lo / kBlock;
+        it.jb_hi = (it.base_pos + tok_hi + kBlock) / kBlock;
+        it.nchunks = (it.jb_hi - it.jb_lo + kW2Blocks - 1) / kW2Blocks;
+        return true;
+    };
+    auto next_item = [&](int& r, Item& it) -> bool {  // the next valid item from round r on
+        for (;;) {
+            const int base = r * P;
+            if (base >= n_items) return false;
+            const int i = base + ((r & 1) ? P - 1 - j : j);
+            ++r;
+            if (i < n_items && item_at(i, it)) return true;
+        }
+    };
+
     grid_dependency_wait();
     launch_dependents();
-
-    const int q0 = a.q_start[b];
-    const int n = a.q_start[b + 1] - q0;
-    const int L = a.context_lens[b];
-    if (n < 0 || n > a.max_new || L < n || L > a.max_blocks * kBlock) {
-        if (tile == 0 && g == 0 && tid == 0) flag_error(a.err, GQA_DEVERR_CONTEXT_LEN);
-        return;                                // uniform per CTA, before any allocation
-    }
-    const int rows = n * a.G;
-    const int row0 = tile * C::kRows;
-    if (row0 >= rows) return;
-    const int base_pos = L - n;
-    const int tok_lo = row0 / a.G, tok_hi = min(rows - 1, row0 + C::kRows - 1) / a.G;
-    const int att_lo = a.window > 0 ? max(0, base_pos + tok_lo - a.window + 1) : 0;
-    const int jb_lo = att_lo / kBlock;
-    const int jb_hi = (base_pos + tok_hi + kBlock) / kBlock;
-    const int nchunks = (jb_hi - jb_lo + kW2Blocks - 1) / kW2Blocks;
-
-    // ---- this thread's row (softmax warps) and the positions it attends, [lo, hi)
-    const int rr = row0 + (softmax ? tid : 0);                 // tid = 128 t + row of tile t
-    const bool live = softmax && rr < rows;
-    const int tk = live ? rr / a.G : 0;
-    const int hi = live ? base_pos + tk + 1 : 0;
-    const int lo = a.window > 0 ? hi - a.window : 0;
-
-    if (softmax) {
-        // This warp's 32 Q rows into its tile's swizzled K-major layout, whole
-        // rows at a time (16 lanes per row, 16 bytes each; rows past the
-        // prompt are zero), every load in flight before the stores.
-        constexpr int kLanesPerRow = D / 8, kRowsPerStep = 32 / kLanesPerRow, kSteps = 32 / kRowsPerStep;
-        const int c16 = lane % kLanesPerRow;
-        const int rl0 = 32 * (warp & 3) + lane / kLanesPerRow;        // first row of this lane in its tile
-        const int rq0 = row0 + 128 * tt + rl0;
-        int tq = rq0 / a.G, hq = rq0 - tq * a.G;
-        uint4 v[kSteps];
-#pragma unroll
-        for (int i = 0; i < kSteps; ++i) {
-            const int rq = rq0 + i * kRowsPerStep;
-            v[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (rq < rows) {
-                const long long src = ((long long)(q0 + tq) * a.H + (long long)g * a.G + hq) * D;
-                v[i] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) + src) + c16);
-            }
-            hq += kRowsPerStep;
-            while (hq >= a.G) {
-                hq -= a.G;
-                ++tq;
-            }
-        }
-        const uint32_t qt = sQ + tt * C::kQt;
-#pragma unroll
-        for (int i = 0; i < kSteps; ++i) {
-            const int rl = rl0 + i * kRowsPerStep;
-            sts128(qt + (c16 >> 3) * (kTcRows * 128) + rl * 128 + (((c16 & 7) ^ (rl & 7)) << 4), v[i]);
-        }
-        fence_proxy_async_smem();              // Q visible to the tensor core
-    }
     if (tid == 0) {
         for (int i = 0; i < kS; ++i) {
             mbar_init(bar_k(i), 1);            // K, V stages
             mbar_init(bar_v(i), 1);
         }
-        for (int t = 0; t < kTiles; ++t)
+        for (int t = 0; t < kTiles; ++t) {
             for (int i = 0; i < kW2Bufs; ++i) {
                 mbar_init(bar_s(t, i), 1);
                 mbar_init(bar_o(t, i), 1);
                 mbar_init(bar_p(t, i), 4);     // one arrival per softmax warp of the tile
             }
+            mbar_init(bar_q(t), 4);
+        }
         for (int i = 0; i < 8; ++i) mbar_init(bar_m(i), 1);
-        mbar_init(bar_q, C::kSoftWarps);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tslot, C::kTmemCols);
@@ -1037,87 +1032,93 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + (tslot - sb));
-    if (softmax && lane == 0) mbar_arrive(bar_q);
     bool ok = true;
+    int round = 0;
+    Item it;
+    bool have = next_item(round, it);
 
     if (loader) {
         // ================================================== copy warps: K, then V
         const bool k_warp = warp == C::kSoftWarps + kTiles;
         const uint64_t pol = l2_policy_evict_last();   // every query tile of the sequence re-reads them
-        int win_base = -(1 << 30), win_phys = -1;
-        int issued = 0;
-        auto issue_kv = [&](int c) {
-            int ph[kW2Blocks];
+        int issued = 0, gc = 0;
+        while (have && ok) {
+            int win_base = -(1 << 30), win_phys = -1;
+            for (int c = 0; c < it.nchunks && ok; ++c) {
+                const int G = gc + c;
+                if (G >= kS) {
+                    // K(G) once every tile's S(G-kS) has read K(G-kS); V(G) once
+                    // every tile's P(G-kS).V(G-kS) has read V(G-kS)
+                    bool w = true;
 #pragma unroll
-            for (int q = 0; q < kW2Blocks; ++q) {
-                const int j = jb_lo + kW2Blocks * c + q;
-                if (j - win_base >= 32 || j < win_base) {
-                    win_base = j;
-                    const int jj = j + lane;
-                    win_phys = -1;
-                    if (jj < jb_hi) {
-                        const int p = a.block_tables[(long long)b * a.max_blocks + jj];
-                        if (p < 0 || p >= a.num_blocks) flag_error(a.err, GQA_DEVERR_BLOCK_INDEX);
-                        else win_phys = p;
+                    for (int t = 0; t < kTiles; ++t)
+                        w = w && mbar_wait(k_warp ? bar_s(t, G - kS) : bar_o(t, G - kS), par4(G - kS));
+                    ok = __all_sync(kFull, w);
+                    if (!ok) break;
+                }
+                int ph[kW2Blocks];
+#pragma unroll
+                for (int q = 0; q < kW2Blocks; ++q) {
+                    const int jb = it.jb_lo + kW2Blocks * c + q;
+                    if (jb - win_base >= 32 || jb < win_base) {
+                        win_base = jb;
+                        const int jj = jb + lane;
+                        win_phys = -1;
+                        if (jj < it.jb_hi) {
+                            const int p = a.block_tables[(long long)it.b * a.max_blocks + jj];
+                            if (p < 0 || p >= a.num_blocks) flag_error(a.err, GQA_DEVERR_BLOCK_INDEX);
+                            else win_phys = p;
+                        }
                     }
+                    ph[q] = __shfl_sync(kFull, win_phys, jb - win_base);
+                    if (jb >= it.jb_hi) ph[q] = -1;
                 }
-                ph[q] = __shfl_sync(kFull, win_phys, j - win_base);
-                if (j >= jb_hi) ph[q] = -1;
-            }
-            const uint32_t bar = k_warp ? bar_k(c) : bar_v(c);
-            if (lane == 0) {
-                uint32_t mask = 0;
-                int nval = 0;
+                const uint32_t bar = k_warp ? bar_k(G) : bar_v(G);
+                if (lane == 0) {
+                    uint32_t mask = 0;
+                    int nval = 0;
 #pragma unroll
-                for (int q = 0; q < kW2Blocks; ++q)
-                    if (ph[q] >= 0) mask |= 1u << q, ++nval;
-                if (k_warp) {
-                    cmask[c & 7] = mask;
-                    mbar_arrive(bar_m(c));     // publishes the mask (release)
+                    for (int q = 0; q < kW2Blocks; ++q)
+                        if (ph[q] >= 0) mask |= 1u << q, ++nval;
+                    if (k_warp) {
+                        cmask[G & 7] = mask;
+                        mbar_arrive(bar_m(G));     // publishes the mask (release)
+                    }
+                    mbar_arrive_expect_tx(bar, (uint32_t)(nval * C::kVb));
                 }
-                mbar_arrive_expect_tx(bar, (uint32_t)(nval * C::kVb));
-            }
-            fence_proxy_async_smem();          // earlier generic writes to the stage come first
-            __syncwarp();
-            if (!k_warp) {
-                // V: one box per page (the page map lands it as [half][slot][128 B])
-                if (lane < kW2Blocks) {
+                fence_proxy_async_smem();          // earlier generic writes to the stage come first
+                __syncwarp();
+                if (!k_warp) {
+                    // V: one box per page (the page map lands it as [half][slot][128 B])
+                    if (lane < kW2Blocks) {
+                        int pq = ph[0];
+#pragma unroll
+                        for (int i = 1; i < kW2Blocks; ++i)
+                            if (lane == i) pq = ph[i];
+                        if (pq >= 0) {
+                            auto coord = [&](int which) { return which == 1 ? it.g : pq; };
+                            tma_load_5d(sV + stage(G) * C::kVc + lane * C::kVb, &vmap, 0, 0, 0,
+                                        coord(a.page_perm[0]), coord(a.page_perm[1]), bar, pol);
+                        }
+                    }
+                } else if (lane < 2 * kW2Blocks) {
+                    // K: one lane per (block, 64-element half) box
+                    const int q = lane >> 1, h = lane & 1;
                     int pq = ph[0];
 #pragma unroll
                     for (int i = 1; i < kW2Blocks; ++i)
-                        if (lane == i) pq = ph[i];
+                        if (q == i) pq = ph[i];
                     if (pq >= 0) {
-                        auto coord = [&](int which) { return which == 1 ? g : pq; };
-                        tma_load_5d(sV + stage(c) * C::kVc + lane * C::kVb, &vmap, 0, 0, 0,
-                                    coord(a.page_perm[0]), coord(a.page_perm[1]), bar, pol);
+                        auto coord = [&](int which) { return which == 0 ? 0 : (which == 1 ? it.g : pq); };
+                        const int y = coord(a.map_perm[0]), z = coord(a.map_perm[1]), w = coord(a.map_perm[2]);
+                        tma_load_4d(sK + stage(G) * C::kKc + h * (kW2Chunk * 128) + q * (kBlock * 128), &kmap,
+                                    h * 64, y, z, w, bar, pol);
                     }
                 }
-            } else if (lane < 2 * kW2Blocks) {
-                // K: one lane per (block, 64-element half) box
-                const int q = lane >> 1, h = lane & 1;
-                int pq = ph[0];
-#pragma unroll
-                for (int i = 1; i < kW2Blocks; ++i)
-                    if (q == i) pq = ph[i];
-                if (pq >= 0) {
-                    auto coord = [&](int which) { return which == 0 ? 0 : (which == 1 ? g : pq); };
-                    const int y = coord(a.map_perm[0]), z = coord(a.map_perm[1]), w = coord(a.map_perm[2]);
-                    tma_load_4d(sK + stage(c) * C::kKc + h * (kW2Chunk * 128) + q * (kBlock * 128), &kmap, h * 64,
-                                y, z, w, bar, pol);
-                }
+                ++issued;
             }
-            ++issued;
-        };
-        for (int c = 0; c < min(nchunks, kS); ++c) issue_kv(c);
-        for (int c = 0; c + kS < nchunks && ok; ++c) {
-            // K(c+kS) once every tile's S(c) has read K(c); V(c+kS) once every
-            // tile's P(c).V(c) has read V(c)
-            bool w = true;
-#pragma unroll
-            for (int t = 0; t < kTiles; ++t) w = w && mbar_wait(k_warp ? bar_s(t, c) : bar_o(t, c), par4(c));
-            ok = __all_sync(kFull, w);
-            if (!ok) break;
-            issue_kv(c + kS);
+            gc += it.nchunks;
+            have = next_item(round, it);
         }
         if (!ok && lane == 0) {
             // let this CTA's copies land before the shared memory goes
@@ -1129,52 +1130,61 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         // ================================================== MMA warps: one per tile (one lane issues)
         const int t = warp - C::kSoftWarps;
         if (lane == 0) {
-            auto issue_s = [&](int c) {            // S_t(c) = Q_t K(c)^T into buffer c & 1
-                const uint32_t kb = sK + stage(c) * C::kKc, qb = sQ + t * C::kQt;
+            auto issue_s = [&](int G) {            // S_t(G) = Q_t K(G)^T into buffer G & 1
+                const uint32_t kb = sK + stage(G) * C::kKc, qb = sQ + t * C::kQt;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint64_t ad = smem_desc_sw128(qb + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(kb + (ks >> 2) * (kW2Chunk * 128) + (ks & 3) * 32, 16, 1024);
-                    tc_mma_f16(tmem + kW2ColTile * t + kW2Chunk * (c & 1), ad, bd, kIdescS, ks > 0);
+                    tc_mma_f16(tmem + kW2ColTile * t + kW2Chunk * (G & 1), ad, bd, kIdescS, ks > 0);
                 }
             };
-            auto issue_pv = [&](int c) {           // O_t += P_t(c) V(c), high part then low part per block
-                const uint32_t vb = sV + stage(c) * C::kVc, pb = tmem + kW2ColTile * t + kW2Chunk * (c & 1);
+            auto issue_pv = [&](int G, bool first) {   // O_t (+)= P_t(G) V(G), high part then low part per block
+                const uint32_t vb = sV + stage(G) * C::kVc, pb = tmem + kW2ColTile * t + kW2Chunk * (G & 1);
 #pragma unroll
                 for (int jl = 0; jl < kW2Blocks; ++jl)
 #pragma unroll
                     for (int part = 0; part < 2; ++part)
                         tc_mma_f16_ta(tmem + kW2ColTile * t + kW2ColO, pb + 16 * jl + 8 * part,
                                       smem_desc_sw128(vb + jl * C::kVb, kBlock * 128, 1024), kIdescO,
-                                      !(c == 0 && jl == 0 && part == 0));
+                                      !(first && jl == 0 && part == 0));
             };
-            int s_done = 0, o_done = 0;            // commits issued (failure path)
-            ok = mbar_wait(bar_q, 0u);
-            for (int c = 0; c < min(nchunks, 2) && ok; ++c) {
-                ok = mbar_wait(bar_k(c), par_st(c));
-                tc_fence_after();
-                if (!ok) break;
-                issue_s(c);
-                tc_commit(bar_s(t, c));
-                ++s_done;
-            }
-            for (int c = 0; c < nchunks && ok; ++c) {
-                // P_t(c) written over S_t(c); V(c) rows of missing tokens zeroed by tile t's softmax
-                ok = mbar_wait(bar_p(t, c), par4(c)) && mbar_wait(bar_v(c), par_st(c));
-                tc_fence_after();
-                if (!ok) break;
-                issue_pv(c);
-                tc_commit(bar_o(t, c));
-                ++o_done;
-                if (c + 2 < nchunks) {
-                    // S_t(c+2) overwrites P_t(c): wait until PV_t(c) has read it
-                    ok = mbar_wait(bar_o(t, c), par4(c)) && mbar_wait(bar_k(c + 2), par_st(c + 2));
+            int s_done = 0, o_done = 0, gc = 0, qi = 0;   // commits issued (failure path), chunks, items
+            while (have && ok) {
+                // Q_t of this item stored; the previous item's last P.V done, so
+                // both S buffers are free (its commit covers every earlier product)
+                ok = mbar_wait(bar_q(t), (uint32_t)qi & 1u);
+                ++qi;
+                if (ok && gc > 0) ok = mbar_wait(bar_o(t, gc - 1), par4(gc - 1));
+                for (int c = 0; c < min(it.nchunks, 2) && ok; ++c) {
+                    ok = mbar_wait(bar_k(gc + c), par_st(gc + c));
                     tc_fence_after();
                     if (!ok) break;
-                    issue_s(c + 2);
-                    tc_commit(bar_s(t, c + 2));
+                    issue_s(gc + c);
+                    tc_commit(bar_s(t, gc + c));
                     ++s_done;
                 }
+                for (int c = 0; c < it.nchunks && ok; ++c) {
+                    const int G = gc + c;
+                    // P_t(G) written over S_t(G); V(G) rows of missing tokens zeroed by tile t's softmax
+                    ok = mbar_wait(bar_p(t, G), par4(G)) && mbar_wait(bar_v(G), par_st(G));
+                    tc_fence_after();
+                    if (!ok) break;
+                    issue_pv(G, c == 0);
+                    tc_commit(bar_o(t, G));
+                    ++o_done;
+                    if (c + 2 < it.nchunks) {
+                        // S_t(G+2) overwrites P_t(G): wait until PV_t(G) has read it
+                        ok = mbar_wait(bar_o(t, G), par4(G)) && mbar_wait(bar_k(G + 2), par_st(G + 2));
+                        tc_fence_after();
+                        if (!ok) break;
+                        issue_s(G + 2);
+                        tc_commit(bar_s(t, G + 2));
+                        ++s_done;
+                    }
+                }
+                gc += it.nchunks;
+                if (ok) have = next_item(round, it);
             }
             if (!ok) {
                 // let this tile's MMAs land before the tensor memory goes, each
@@ -1191,163 +1201,215 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         // ================================================== softmax warps: one row per thread
         const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kW2ColTile * tt;
         const uint32_t t_o = t_lane + kW2ColO;
-        float m = -INFINITY, l = 0.f;
-        for (int c = 0; c < nchunks; ++c) {
-            ok = __all_sync(kFull, mbar_wait(bar_s(tt, c), par4(c)));   // S_t(c) done
-            ok = ok && __all_sync(kFull, mbar_wait(bar_m(c), par8(c)));
-            if (!ok) break;
-            tc_fence_after();
-            const int cpos = (jb_lo + kW2Blocks * c) * kBlock;
-            const uint32_t bm = cmask[c & 7];
-            const uint32_t t_buf = t_lane + kW2Chunk * (c & 1);
-            float sv[kW2Chunk];
-            {
-                uint32_t r[kW2Chunk / 16][16];
+        const uint32_t qt = sQ + tt * C::kQt;
+        float* stg = reinterpret_cast<float*>(gb + C::kOffStg) + (warp * 32) * C::kStgRowF;
+        // This warp's 32 Q rows of item x into its tile's swizzled K-major
+        // layout by cp.async (16 lanes per row, 16 bytes each; rows past the
+        // prompt are zero-filled), then "Q_t stored" once they have landed.
+        auto load_q = [&](const Item& x) {
+            constexpr int kLanesPerRow = D / 8, kRowsPerStep = 32 / kLanesPerRow, kSteps = 32 / kRowsPerStep;
+            const int c16 = lane % kLanesPerRow;
+            const int rl0 = 32 * (warp & 3) + lane / kLanesPerRow;
+            const int rq0 = x.row0 + 128 * tt + rl0;
+            int tq = rq0 / a.G, hq = rq0 - tq * a.G;
 #pragma unroll
-                for (int u = 0; u < kW2Chunk / 16; ++u) tmem_ld16(t_buf + 16 * u, r[u]);
-                tmem_wait_ld();
-                const uint64_t sc2 = f2_make(a.scale_log2, a.scale_log2);
-#pragma unroll
-                for (int u = 0; u < kW2Chunk / 16; ++u)
-#pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const float2 v = f2_split(f2_mul(f2_make(__uint_as_float(r[u][j]), __uint_as_float(r[u][j + 1])), sc2));
-                        sv[16 * u + j] = v.x;
-                        sv[16 * u + j + 1] = v.y;
-                    }
-            }
-            const bool whole = bm == (1u << kW2Blocks) - 1u && cpos >= lo && cpos + kW2Chunk <= hi;
-            if (!whole) {
-#pragma unroll
-                for (int j = 0; j < kW2Chunk; ++j) {
-                    const int pos = cpos + j;
-                    if (!((bm >> (j / kBlock)) & 1u) || pos < lo || pos >= hi) sv[j] = -INFINITY;
+            for (int i = 0; i < kSteps; ++i) {
+                const int rl = rl0 + i * kRowsPerStep, rq = rq0 + i * kRowsPerStep;
+                const bool in = rq < x.rows;
+                const long long src = in ? ((long long)(x.q0 + tq) * a.H + (long long)x.g * a.G + hq) * D + 8 * c16 : 0;
+                cp_async16(qt + (c16 >> 3) * (kTcRows * 128) + rl * 128 + (((c16 & 7) ^ (rl & 7)) << 4),
+                           static_cast<const uint16_t*>(a.q) + src, in ? 16u : 0u);
+                hq += kRowsPerStep;
+                while (hq >= a.G) {
+                    hq -= a.G;
+                    ++tq;
                 }
             }
-            float mx4[4];                                     // four short chains of 3-input maxima
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                float v = fmaxf(sv[16 * k], sv[16 * k + 15]);
-#pragma unroll
-                for (int i = 1; i < 15; i += 2) v = fmax3(v, sv[16 * k + i], sv[16 * k + i + 1]);
-                mx4[k] = v;
-            }
-            const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
-            // lazy rescale: keep the stale maximum while the new one stays within 2^slack
-            const bool old_live = m != -INFINITY;
-            const bool resc = mx > m + kTcSlack;
-            float alpha = 1.f;
-            if (resc) {
-                alpha = old_live ? fast_exp2(m - mx) : 0.f;
-                m = mx;
-            }
-            l *= alpha;
-            if (c > 0 && __any_sync(kFull, resc && old_live)) {       // O holds earlier chunks: scale it
-                // once P_t(c-1).V(c-1) has landed in it
-                ok = __all_sync(kFull, mbar_wait(bar_o(tt, c - 1), par4(c - 1)));
+        };
+        auto q_stored = [&]() {
+            cp_async_wait_all();
+            fence_proxy_async_smem();          // Q visible to the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_q(tt));
+        };
+        if (have) {
+            load_q(it);
+            q_stored();
+        }
+        int gc = 0;
+        while (have && ok) {
+            Item nx;
+            int round_nx = round;
+            const bool have_nx = next_item(round_nx, nx);
+            // ---- this thread's row and the positions it attends, [lo, hi)
+            const int rr = it.row0 + tid;      // tid = 128 t + row of tile t
+            const bool live = rr < it.rows;
+            const int tk = live ? rr / a.G : 0;
+            const int hi = live ? it.base_pos + tk + 1 : 0;
+            const int lo = a.window > 0 ? hi - a.window : 0;
+            float m = -INFINITY, l = 0.f;
+            for (int c = 0; c < it.nchunks; ++c) {
+                const int G = gc + c;
+                ok = __all_sync(kFull, mbar_wait(bar_s(tt, G), par4(G)));   // S_t(G) done
+                ok = ok && __all_sync(kFull, mbar_wait(bar_m(G), par8(G)));
                 if (!ok) break;
                 tc_fence_after();
-                const float f = (resc && old_live) ? alpha : 1.f;
+                const int cpos = (it.jb_lo + kW2Blocks * c) * kBlock;
+                const uint32_t bm = cmask[G & 7];
+                const uint32_t t_buf = t_lane + kW2Chunk * (G & 1);
+                float sv[kW2Chunk];
+                {
+                    uint32_t r[kW2Chunk / 16][16];
 #pragma unroll
-                for (int q = 0; q < D / 16; ++q) {
-                    uint32_t r16[16];
-                    tmem_ld16(t_o + 16 * q, r16);
+                    for (int u = 0; u < kW2Chunk / 16; ++u) tmem_ld16(t_buf + 16 * u, r[u]);
                     tmem_wait_ld();
+                    const uint64_t sc2 = f2_make(a.scale_log2, a.scale_log2);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) r16[j] = __float_as_uint(__uint_as_float(r16[j]) * f);
-                    tmem_st16(t_o + 16 * q, r16);
-                }
-            }
-            const float mu = m == -INFINITY ? 0.f : m;    // a row with nothing attended yet: p = 0
-            const uint64_t mu2 = f2_make(mu, mu);
-            uint64_t ps2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
-            // P over S: block jl's 16 tokens to columns [16jl, 16jl+16) of the
-            // buffer, 8 high then 8 low columns
+                    for (int u = 0; u < kW2Chunk / 16; ++u)
 #pragma unroll
-            for (int jl = 0; jl < kW2Blocks; ++jl) {
-                uint32_t w16[16];
+                        for (int q = 0; q < 16; q += 2) {
+                            const float2 v = f2_split(f2_mul(f2_make(__uint_as_float(r[u][q]), __uint_as_float(r[u][q + 1])), sc2));
+                            sv[16 * u + q] = v.x;
+                            sv[16 * u + q + 1] = v.y;
+                        }
+                }
+                // the item's last S_t is in registers, and with it every S_t of the
+                // item is done: Q_t's buffer is free for the next item's rows
+                if (c == it.nchunks - 1 && have_nx) load_q(nx);
+                const bool whole = bm == (1u << kW2Blocks) - 1u && cpos >= lo && cpos + kW2Chunk <= hi;
+                if (!whole) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float2 d = f2_split(f2_sub(f2_make(sv[16 * jl + 2 * e], sv[16 * jl + 2 * e + 1]), mu2));
-                    const float x = fast_exp2(d.x), y = fast_exp2(d.y);
-                    const uint64_t xy = f2_make(x, y);
-                    ps2[e & 1] = f2_add(ps2[e & 1], xy);
-                    w16[e] = pack2<kB>(x, y);
-                    const float2 f = unpack2<kB>(w16[e]);
-                    const float2 r = f2_split(f2_sub(xy, f2_make(f.x, f.y)));
-                    w16[8 + e] = pack2<kB>(r.x, r.y);
+                    for (int q = 0; q < kW2Chunk; ++q) {
+                        const int pos = cpos + q;
+                        if (!((bm >> (q / kBlock)) & 1u) || pos < lo || pos >= hi) sv[q] = -INFINITY;
+                    }
                 }
-                tmem_st16(t_buf + 16 * jl, w16);
-            }
-            tmem_wait_st();
-            {
-                const float2 p0 = f2_split(ps2[0]), p1 = f2_split(ps2[1]);
-                l += (p0.x + p1.x) + (p0.y + p1.y);
-            }
-            // V rows of tokens outside the sequence or of missing blocks hold
-            // arbitrary bits: each tile zeroes them before its P(c) is ready (its
-            // MMA warp issues P_t(c).V(c) only then); both tiles write the same zeros
-            if (bm != (1u << kW2Blocks) - 1u || cpos + kW2Chunk > L) {
-                ok = __all_sync(kFull, mbar_wait(bar_v(c), par_st(c)));
-                const uint32_t vb = sV + stage(c) * C::kVc;
-                for (int i = tid & (kTcRows - 1); i < kW2Chunk * 2 * 8; i += kTcRows) {
-                    const int t = i / 16, h = (i / 8) % 2, ck = i % 8;
-                    if (((bm >> (t / kBlock)) & 1u) && cpos + t < L) continue;
-                    sts128(vb + (t / kBlock) * C::kVb + h * (kBlock * 128) + (t % kBlock) * 128 + ck * 16,
-                           make_uint4(0u, 0u, 0u, 0u));
+                float mx4[4];                                     // four short chains of 3-input maxima
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float v = fmaxf(sv[16 * k], sv[16 * k + 15]);
+#pragma unroll
+                    for (int i = 1; i < 15; i += 2) v = fmax3(v, sv[16 * k + i], sv[16 * k + i + 1]);
+                    mx4[k] = v;
                 }
-                fence_proxy_async_smem();      // zeroed V visible to the tensor core
+                const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
+                // lazy rescale: keep the stale maximum while the new one stays within 2^slack
+                const bool old_live = m != -INFINITY;
+                const bool resc = mx > m + kTcSlack;
+                float alpha = 1.f;
+                if (resc) {
+                    alpha = old_live ? fast_exp2(m - mx) : 0.f;
+                    m = mx;
+                }
+                l *= alpha;
+                if (c > 0 && __any_sync(kFull, resc && old_live)) {       // O holds earlier chunks: scale it
+                    // once P_t(G-1).V(G-1) has landed in it
+                    ok = __all_sync(kFull, mbar_wait(bar_o(tt, G - 1), par4(G - 1)));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const float f = (resc && old_live) ? alpha : 1.f;
+#pragma unroll
+                    for (int q = 0; q < D / 16; ++q) {
+                        uint32_t r16[16];
+                        tmem_ld16(t_o + 16 * q, r16);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) r16[k] = __float_as_uint(__uint_as_float(r16[k]) * f);
+                        tmem_st16(t_o + 16 * q, r16);
+                    }
+                }
+                const float mu = m == -INFINITY ? 0.f : m;    // a row with nothing attended yet: p = 0
+                const uint64_t mu2 = f2_make(mu, mu);
+                uint64_t ps2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
+                // P over S: block jl's 16 tokens to columns [16jl, 16jl+16) of the
+                // buffer, 8 high then 8 low columns
+#pragma unroll
+                for (int jl = 0; jl < kW2Blocks; ++jl) {
+                    uint32_t w16[16];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 d = f2_split(f2_sub(f2_make(sv[16 * jl + 2 * e], sv[16 * jl + 2 * e + 1]), mu2));
+                        const float x = fast_exp2(d.x), y = fast_exp2(d.y);
+                        const uint64_t xy = f2_make(x, y);
+                        ps2[e & 1] = f2_add(ps2[e & 1], xy);
+                        w16[e] = pack2<kB>(x, y);
+                        const float2 f = unpack2<kB>(w16[e]);
+                        const float2 r = f2_split(f2_sub(xy, f2_make(f.x, f.y)));
+                        w16[8 + e] = pack2<kB>(r.x, r.y);
+                    }
+                    tmem_st16(t_buf + 16 * jl, w16);
+                }
+                tmem_wait_st();
+                {
+                    const float2 p0 = f2_split(ps2[0]), p1 = f2_split(ps2[1]);
+                    l += (p0.x + p1.x) + (p0.y + p1.y);
+                }
+                // V rows of tokens outside the sequence or of missing blocks hold
+                // arbitrary bits: each tile zeroes them before its P(G) is ready (its
+                // MMA warp issues P_t(G).V(G) only then); both tiles write the same zeros
+                if (bm != (1u << kW2Blocks) - 1u || cpos + kW2Chunk > it.L) {
+                    ok = __all_sync(kFull, mbar_wait(bar_v(G), par_st(G)));
+                    const uint32_t vb = sV + stage(G) * C::kVc;
+                    for (int i = tid & (kTcRows - 1); i < kW2Chunk * 2 * 8; i += kTcRows) {
+                        const int tk2 = i / 16, h = (i / 8) % 2, ck = i % 8;
+                        if (((bm >> (tk2 / kBlock)) & 1u) && cpos + tk2 < it.L) continue;
+                        sts128(vb + (tk2 / kBlock) * C::kVb + h * (kBlock * 128) + (tk2 % kBlock) * 128 + ck * 16,
+                               make_uint4(0u, 0u, 0u, 0u));
+                    }
+                    fence_proxy_async_smem();      // zeroed V visible to the tensor core
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_p(tt, G));
+                if (!ok) break;
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_p(tt, c));
             if (!ok) break;
-        }
-        // ---- wait for both tiles' last P.V, then normalise and store. Every
-        // copy has landed and every MMA is done once both have arrived, so the
-        // shared memory below the barriers stages the output. A parity wait on
-        // a barrier copy is sound for the copy's newest event once the event
-        // before it (four chunks back) is known to be done. Own tile: S_t(n-1)
-        // was seen, and it was issued only after PV_t(n-3) was done. Other
-        // tile: K(n-1) was copied only after its S(n-5), issued after its
-        // PV(n-7) was done; so its PV(n-3) is awaited first, whose commit
-        // covers PV(n-5), and then PV(n-1).
-        if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(tt, nchunks - 1), par4(nchunks - 1)));
-        if (kTiles == 2) {
-            if (ok && nchunks >= 3) ok = __all_sync(kFull, mbar_wait(bar_o(1 - tt, nchunks - 3), par4(nchunks - 3)));
-            if (ok) ok = __all_sync(kFull, mbar_wait(bar_o(1 - tt, nchunks - 1), par4(nchunks - 1)));
-        }
-        tc_fence_after();
-        if (ok) {
+            // the next item's Q_t has landed: its MMA warp may start on it
+            if (have_nx) q_stored();
+            // ---- wait for this tile's last P.V (the copy's newest event; the one
+            // before it, four chunks back, was done before S_t(last) was issued),
+            // then normalise and store through this warp's staging rows, 16
+            // columns at a time: 64-byte row pieces, eight rows per instruction
+            const int G_last = gc + it.nchunks - 1;
+            ok = __all_sync(kFull, mbar_wait(bar_o(tt, G_last), par4(G_last)));
+            if (!ok) break;
+            tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            constexpr int kRowF = D + 4;       // padded row: 16-byte stores stay conflict-free
-            float* stage = reinterpret_cast<float*>(gb) + warp * 32 * kRowF;
+            const int wr0 = it.row0 + 32 * warp;  // this warp's first row (tile 1 = warps 4-7)
+            long long orow[4];
+            bool orow_ok[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int rw = wr0 + 8 * k + (lane >> 2);
+                const int tkr = rw / a.G, hr = rw - tkr * a.G;
+                orow_ok[k] = rw < it.rows;
+                orow[k] = ((long long)(it.q0 + tkr) * a.H + (long long)it.g * a.G + hr) * D + 4 * (lane & 3);
+            }
 #pragma unroll
             for (int q = 0; q < D / 16; ++q) {
                 uint32_t r16[16];
                 tmem_ld16(t_o + 16 * q, r16);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; j += 4)
-                    *reinterpret_cast<float4*>(stage + lane * kRowF + 16 * q + j) =
-                        make_float4(__uint_as_float(r16[j]) * inv, __uint_as_float(r16[j + 1]) * inv,
-                                    __uint_as_float(r16[j + 2]) * inv, __uint_as_float(r16[j + 3]) * inv);
+                for (int k = 0; k < 16; k += 4)
+                    *reinterpret_cast<float4*>(stg + lane * C::kStgRowF + k) =
+                        make_float4(__uint_as_float(r16[k]) * inv, __uint_as_float(r16[k + 1]) * inv,
+                                    __uint_as_float(r16[k + 2]) * inv, __uint_as_float(r16[k + 3]) * inv);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (orow_ok[k])
+                        store4(a.out, a.out_dtype, orow[k] + 16 * q,
+                               *reinterpret_cast<const float4*>(stg + (8 * k + (lane >> 2)) * C::kStgRowF + 4 * (lane & 3)));
+                __syncwarp();
             }
-            __syncwarp();
-            const int wr0 = row0 + 32 * warp;  // this warp's first row (tile 1 = warps 4-7)
-            int tkr = wr0 / a.G, hr = wr0 - tkr * a.G;
-            for (int r = 0; r < 32; ++r) {
-                if (wr0 + r >= rows) break;
-                const long long orow = ((long long)(q0 + tkr) * a.H + (long long)g * a.G + hr) * D;
-                store4(a.out, a.out_dtype, orow + 4 * lane, *reinterpret_cast<const float4*>(stage + r * kRowF + 4 * lane));
-                if (++hr == a.G) {
-                    hr = 0;
-                    ++tkr;
-                }
-            }
-        } else if (lane == 0) {
-            flag_error(a.err, GQA_DEVERR_TIMEOUT);
+            gc += it.nchunks;
+            it = nx;
+            round = round_nx;
+            have = have_nx;
         }
+        if (!ok && lane == 0) flag_error(a.err, GQA_DEVERR_TIMEOUT);
+        cp_async_wait_all();                   // nothing of this warp's still lands in shared memory
     }
     tc_fence_before();
     __syncthreads();
@@ -1447,7 +1509,15 @@ int launch_prefill(const PrefillLaunch& L) {
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.tiles_per_seq, (unsigned)K, (unsigned)L.batch);
+    if (wide) {
+        // persistent CTAs: as many as fit at once, each walking its items
+        const long long items = (long long)a.tiles_per_seq * K * L.batch;
+        if (items > INT32_MAX || L.num_sms <= 0) return GQA_ERR_UNSUPPORTED;
+        const long long fit = (long long)L.num_sms * (wide2 ? W2Cfg<2>::kCtasPerSm : W2Cfg<1>::kCtasPerSm);
+        cfg.gridDim = dim3((unsigned)(items < fit ? items : fit));
+    } else {
+        cfg.gridDim = dim3((unsigned)a.tiles_per_seq, (unsigned)K, (unsigned)L.batch);
+    }
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = L.stream;
