@@ -144,6 +144,10 @@ bool encode_page_map_uncached(CUtensorMap* map, const gqa_kv_cache_t& c, const v
 
 }  // namespace
 
+// SM count of a device (-1: the current one), remembered per device; the
+// prefill sizes its persistent grid with it.
+int device_sms(int device) { return num_sms_of(device); }
+
 bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int box_inner,
                       int swizzle_bytes, int perm[3]) {
     const MapKey k = map_key(c, base, box_inner, swizzle_bytes, 0);
@@ -338,7 +342,6 @@ int gqa_prefill(const gqa_kv_cache_t* cache, const void* q, int32_t q_dtype, int
     L.out = out;
     L.out_dtype = out_dtype;
     L.kernel = kernel;
-    L.num_sms = num_sms_of(-1);
     L.err = err_flag;
     L.stream = static_cast<cudaStream_t>(stream);
     return launch_prefill(L);

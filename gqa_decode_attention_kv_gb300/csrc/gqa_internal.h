@@ -63,7 +63,6 @@ struct PrefillLaunch {
     void* out;
     int out_dtype;
     int kernel;                 // GQA_PREFILL_* (0 = tcgen05)
-    int num_sms;                // SMs of the current device (persistent grids)
     int32_t* err;
     cudaStream_t stream;
 };

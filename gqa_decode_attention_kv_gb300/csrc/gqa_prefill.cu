@@ -1433,6 +1433,8 @@ const void* prefill_fn() {
 
 }  // namespace
 
+int device_sms(int device);   // gqa_capi.cu
+
 int launch_prefill(const PrefillLaunch& L) {
     const gqa_kv_cache_t& c = *L.cache;
     const int D = c.head_dim, K = c.num_kv_heads, G = L.num_heads / K;
@@ -1512,8 +1514,9 @@ int launch_prefill(const PrefillLaunch& L) {
     if (wide) {
         // persistent CTAs: as many as fit at once, each walking its items
         const long long items = (long long)a.tiles_per_seq * K * L.batch;
-        if (items > INT32_MAX || L.num_sms <= 0) return GQA_ERR_UNSUPPORTED;
-        const long long fit = (long long)L.num_sms * (wide2 ? W2Cfg<2>::kCtasPerSm : W2Cfg<1>::kCtasPerSm);
+        const int sms = device_sms(-1);
+        if (items > INT32_MAX || sms <= 0) return GQA_ERR_UNSUPPORTED;
+        const long long fit = (long long)sms * (wide2 ? W2Cfg<2>::kCtasPerSm : W2Cfg<1>::kCtasPerSm);
         cfg.gridDim = dim3((unsigned)(items < fit ? items : fit));
     } else {
         cfg.gridDim = dim3((unsigned)a.tiles_per_seq, (unsigned)K, (unsigned)L.batch);
