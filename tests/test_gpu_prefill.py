@@ -97,6 +97,23 @@ def test_prefill_long_prompt_and_empty_sequences(gq, oracle_mod, kernel):
     assert max_abs_err(_run(gq, case, q, q_start, news, kernel=kernel), ref) <= TOL
 
 
+@pytest.mark.parametrize("kernel", [3, 4])
+def test_prefill_many_items_per_persistent_cta(gq, oracle_mod, kernel):
+    """40 ragged prompts (0..300 new tokens over 0..70 cached ones). The
+    64-token forms' persistent CTAs (one or two per SM) deal out 1600 or 3200
+    (query tile, kv-head, sequence) items, so every CTA walks several of them,
+    skips those past a short prompt's end, and carries its barrier phases and
+    stage ring from one item to the next."""
+    rng = np.random.default_rng(91)
+    news = rng.integers(0, 301, size=40).tolist()
+    news[5], news[17] = 0, 300
+    prior = rng.integers(0, 71, size=40).tolist()
+    lens = [n + p for n, p in zip(news, prior)]
+    case, q, q_start = _case(lens, news, 32, 8, 128, "bf16", seed=93)
+    ref = _reference(oracle_mod, case, q, news)
+    assert max_abs_err(_run(gq, case, q, q_start, news, kernel=kernel), ref) <= TOL
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("sign", [-1.0, 0.0])
 def test_prefill_negative_and_zero_scale(gq, oracle_mod, kernel, sign):
