@@ -299,7 +299,6 @@ __device__ __forceinline__ uint32_t i4_hi_pair(uint32_t w) {
     return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// Byte permute with the PTX selector semantics: a selector nibble with bit 3
 // Transpose of an 8x8 matrix of 16-bit values held one register per lane in
 // the mma fragment layout (lane l: row l / 4, columns 2 (l % 4) and +1): lane l
 // gets row l / 4 of the transpose, columns 2 (l % 4) and +1 (warp-collective).
@@ -309,6 +308,7 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
     return y;
 }
 
+// Byte permute with the PTX selector semantics: a selector nibble with bit 3
 // set writes the sign of the chosen byte replicated over all 8 bits.
 __device__ __forceinline__ uint32_t prmt(uint32_t x, uint32_t y, uint32_t sel) {
     uint32_t r;
