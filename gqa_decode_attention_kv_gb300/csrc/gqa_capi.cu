@@ -148,6 +148,23 @@ bool encode_page_map_uncached(CUtensorMap* map, const gqa_kv_cache_t& c, const v
 // prefill sizes its persistent grid with it.
 int device_sms(int device) { return num_sms_of(device); }
 
+// 3-D tensor map over a prefill's fp32 output [tokens, num_heads, 128]: boxes of
+// 16 columns x min(G, 32) heads x 32 / min(G, 32) tokens, 64-byte swizzle (one
+// warp's 32 output rows, 16 columns at a time). `tokens` bounds the rows; the
+// kernel stores only rows it owns.
+bool encode_out_map(CUtensorMap* map, void* out, int num_heads, int G, long long tokens) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc || tokens <= 0) return false;
+    const int bh = G < 32 ? G : 32;
+    cuuint64_t gdim[3] = {128, (cuuint64_t)num_heads, (cuuint64_t)tokens};
+    cuuint64_t gstride[2] = {128 * 4, (cuuint64_t)num_heads * 128 * 4};
+    cuuint32_t box[3] = {16, (cuuint32_t)bh, (cuuint32_t)(32 / bh)};
+    cuuint32_t estride[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int box_inner,
                       int swizzle_bytes, int perm[3]) {
     const MapKey k = map_key(c, base, box_inner, swizzle_bytes, 0);

@@ -18,6 +18,7 @@
 // thread issuing. Tiles run heaviest first (the last query tiles of a
 // sequence attend the most blocks).
 #include <algorithm>
+#include <cstring>
 #include <type_traits>
 
 #include "gqa_device.cuh"
@@ -40,6 +41,19 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Bulk tensor store of a shared-memory box to global through `map`, in this
+// thread's bulk group; then the group's commit, and the waits for its reads of
+// shared memory (the box may be rewritten) or for its completion.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 constexpr int kPfWarps = 4;                  // warps per CTA, 16 query rows each
 constexpr int kPfRows = 16 * kPfWarps;       // query rows per tile
 constexpr int kPfStages = 4;                 // ring stages (one 16-token block each)
@@ -56,6 +70,7 @@ struct PrefillArgs {
     int B, H, K, G, max_blocks, out_dtype, tiles_per_seq, max_new, window;
     int map_perm[3];
     int page_perm[2];           // tcgen05 kernel, d = 128: dims 3, 4 of the V page map
+    int out_tma;                // 64-token tcgen05 forms: the output map is valid (fp32 out, G | 32 or 32 | G)
     float scale_log2;
 };
 
@@ -927,7 +942,7 @@ struct W2Cfg {
 template <typename T, int kTiles>
 __global__ void __launch_bounds__(W2Cfg<kTiles>::kThreads, W2Cfg<kTiles>::kCtasPerSm)
 prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                   const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap omap, const PrefillArgs a) {
     using C = W2Cfg<kTiles>;
     constexpr int kS = C::kStages;
     constexpr int D = C::D;
@@ -965,6 +980,7 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     if (tid == 0) {
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
+        if (a.out_tma) prefetch_tensormap(&omap);
     }
 
     // ---- the CTA's items: (query tile, kv-head, sequence). The (kv-head,
@@ -1375,40 +1391,75 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             if (have_nx) q_stored();
             // ---- wait for this tile's last P.V (the copy's newest event; the one
             // before it, four chunks back, was done before S_t(last) was issued),
-            // then normalise and store through this warp's staging rows, 16
-            // columns at a time: 64-byte row pieces, eight rows per instruction
+            // then normalise and store, 16 columns at a time through this warp's
+            // staging rows: by TMA, or with 64-byte row pieces, eight rows per
+            // store instruction, where a row is past the prompt or the output is
+            // not fp32
             const int G_last = gc + it.nchunks - 1;
             ok = __all_sync(kFull, mbar_wait(bar_o(tt, G_last), par4(G_last)));
             if (!ok) break;
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const int wr0 = it.row0 + 32 * warp;  // this warp's first row (tile 1 = warps 4-7)
-            long long orow[4];
-            bool orow_ok[4];
+            if (a.out_tma && wr0 + 32 <= it.rows) {
+                // every row of the warp is live: the 32 rows are (32/G tokens x G
+                // heads) or (1 token x 32 heads), one box of the output map per 16
+                // columns, stored by TMA from this warp's staging (unpadded rows,
+                // 16-byte chunk j of row r at chunk j ^ ((r >> 1) & 3): the map's
+                // 64-byte swizzle) while the warp goes on
+                const uint32_t sst = smem_addr(stg);
+                const int tq = wr0 / a.G, hq = wr0 - tq * a.G;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int rw = wr0 + 8 * k + (lane >> 2);
-                const int tkr = rw / a.G, hr = rw - tkr * a.G;
-                orow_ok[k] = rw < it.rows;
-                orow[k] = ((long long)(it.q0 + tkr) * a.H + (long long)it.g * a.G + hr) * D + 4 * (lane & 3);
-            }
+                for (int q = 0; q < D / 16; ++q) {
+                    uint32_t r16[16];
+                    tmem_ld16(t_o + 16 * q, r16);
+                    tmem_wait_ld();
+                    if (lane == 0) bulk_wait_read();        // the previous box has been read out
+                    __syncwarp();
 #pragma unroll
-            for (int q = 0; q < D / 16; ++q) {
-                uint32_t r16[16];
-                tmem_ld16(t_o + 16 * q, r16);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 16; k += 4)
-                    *reinterpret_cast<float4*>(stg + lane * C::kStgRowF + k) =
-                        make_float4(__uint_as_float(r16[k]) * inv, __uint_as_float(r16[k + 1]) * inv,
-                                    __uint_as_float(r16[k + 2]) * inv, __uint_as_float(r16[k + 3]) * inv);
+                    for (int k = 0; k < 4; ++k)
+                        sts128(sst + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4),
+                               make_uint4(__float_as_uint(__uint_as_float(r16[4 * k]) * inv),
+                                          __float_as_uint(__uint_as_float(r16[4 * k + 1]) * inv),
+                                          __float_as_uint(__uint_as_float(r16[4 * k + 2]) * inv),
+                                          __float_as_uint(__uint_as_float(r16[4 * k + 3]) * inv)));
+                    fence_proxy_async_smem();               // the box visible to the TMA unit
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&omap, sst, 16 * q, it.g * a.G + hq, it.q0 + tq);
+                        bulk_commit();
+                    }
+                }
+                if (lane == 0) bulk_wait_read();            // staging free for the next item
                 __syncwarp();
+            } else {
+                long long orow[4];
+                bool orow_ok[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    if (orow_ok[k])
-                        store4(a.out, a.out_dtype, orow[k] + 16 * q,
-                               *reinterpret_cast<const float4*>(stg + (8 * k + (lane >> 2)) * C::kStgRowF + 4 * (lane & 3)));
-                __syncwarp();
+                for (int k = 0; k < 4; ++k) {
+                    const int rw = wr0 + 8 * k + (lane >> 2);
+                    const int tkr = rw / a.G, hr = rw - tkr * a.G;
+                    orow_ok[k] = rw < it.rows;
+                    orow[k] = ((long long)(it.q0 + tkr) * a.H + (long long)it.g * a.G + hr) * D + 4 * (lane & 3);
+                }
+#pragma unroll
+                for (int q = 0; q < D / 16; ++q) {
+                    uint32_t r16[16];
+                    tmem_ld16(t_o + 16 * q, r16);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; k += 4)
+                        *reinterpret_cast<float4*>(stg + lane * C::kStgRowF + k) =
+                            make_float4(__uint_as_float(r16[k]) * inv, __uint_as_float(r16[k + 1]) * inv,
+                                        __uint_as_float(r16[k + 2]) * inv, __uint_as_float(r16[k + 3]) * inv);
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (orow_ok[k])
+                            store4(a.out, a.out_dtype, orow[k] + 16 * q,
+                                   *reinterpret_cast<const float4*>(stg + (8 * k + (lane >> 2)) * C::kStgRowF + 4 * (lane & 3)));
+                    __syncwarp();
+                }
             }
             gc += it.nchunks;
             it = nx;
@@ -1417,6 +1468,7 @@ prefill_tc2_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         }
         if (!ok && lane == 0) flag_error(a.err, GQA_DEVERR_TIMEOUT);
         cp_async_wait_all();                   // nothing of this warp's still lands in shared memory
+        if (lane == 0) bulk_wait_all();        // its output stores are done
     }
     tc_fence_before();
     __syncthreads();
@@ -1441,6 +1493,7 @@ const void* prefill_fn() {
 }  // namespace
 
 int device_sms(int device);   // gqa_capi.cu
+bool encode_out_map(CUtensorMap* map, void* out, int num_heads, int G, long long tokens);   // gqa_capi.cu
 
 int launch_prefill(const PrefillLaunch& L) {
     const gqa_kv_cache_t& c = *L.cache;
@@ -1513,6 +1566,13 @@ int launch_prefill(const PrefillLaunch& L) {
     a.page_perm[1] = page_perm[1];
     a.scale_log2 = L.scale * kLog2eP;
     if (a.tiles_per_seq == 0) return GQA_OK;
+    // the 64-token forms store whole-live warps' output by TMA: fp32 out, a
+    // warp's 32 rows a box of (32/G tokens x G heads) or (1 token x 32 heads)
+    CUtensorMap omap;
+    memset(&omap, 0, sizeof(omap));
+    a.out_tma = 0;
+    if (wide && L.out_dtype == GQA_DTYPE_F32 && (32 % G == 0 || G % 32 == 0))
+        a.out_tma = encode_out_map(&omap, L.out, L.num_heads, G, (long long)L.max_new_tokens * L.batch) ? 1 : 0;
 
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1534,7 +1594,8 @@ int launch_prefill(const PrefillLaunch& L) {
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     void* args[] = {&kmap, &vmap, &a};
-    return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    void* args_w[] = {&kmap, &vmap, &omap, &a};
+    return cudaLaunchKernelExC(&cfg, fn, wide ? args_w : args) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 }  // namespace gqa

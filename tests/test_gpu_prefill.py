@@ -98,6 +98,20 @@ def test_prefill_long_prompt_and_empty_sequences(gq, oracle_mod, kernel):
 
 
 @pytest.mark.parametrize("kernel", [3, 4])
+@pytest.mark.parametrize("H,K", [(48, 8), (96, 2), (64, 1), (128, 1)])
+def test_prefill_group_sizes(gq, oracle_mod, H, K, kernel):
+    """G = 6 and 48 (a warp's 32 rows are not whole tokens: the 64-token forms
+    store them row by row) and G = 64 and 128 (each warp's rows are 32 heads
+    of one token: stored as one box per 16 columns), ragged prompts."""
+    news = [1, 40, 130, 7]
+    prior = [0, 9, 33, 100]
+    lens = [n + p for n, p in zip(news, prior)]
+    case, q, q_start = _case(lens, news, H, K, 128, "bf16", seed=95)
+    ref = _reference(oracle_mod, case, q, news)
+    assert max_abs_err(_run(gq, case, q, q_start, news, kernel=kernel), ref) <= TOL
+
+
+@pytest.mark.parametrize("kernel", [3, 4])
 def test_prefill_many_items_per_persistent_cta(gq, oracle_mod, kernel):
     """40 ragged prompts (0..300 new tokens over 0..70 cached ones). The
     64-token forms' persistent CTAs (one or two per SM) deal out 1600 or 3200
