@@ -189,6 +189,18 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     if (!encode_cache_map(&kmap, c, c.k, v.box_inner, v.swizzle_bytes, perm) ||
         !encode_cache_map(&vmap, c, c.v, v.box_inner, v.swizzle_bytes, perm))
         return GQA_ERR_UNSUPPORTED;
+    // 16-bit tiles of 128-element rows come two 64-element boxes at a time
+    // through the maps above; a page map moves the whole tile in one copy
+    int page_perm[2] = {1, 2};
+    bool page_box = false;
+    if (dtype_bits(c.dtype) == 16 && D == 128 && v.box_inner == 64 && v.swizzle_bytes == 128) {
+        CUtensorMap kp, vp;
+        if (encode_page_map(&kp, c, c.k, page_perm) && encode_page_map(&vp, c, c.v, page_perm)) {
+            kmap = kp;
+            vmap = vp;
+            page_box = true;
+        }
+    }
 
     const int smem = v.smem(L.batch);
     const int workers = workers_of(v, L.batch, num_sms);
@@ -236,6 +248,9 @@ int launch_decode(const DecodeLaunch& L, int num_sms) {
     a.map_perm[0] = perm[0];
     a.map_perm[1] = perm[1];
     a.map_perm[2] = perm[2];
+    a.page_box = page_box ? 1 : 0;
+    a.page_perm[0] = page_perm[0];
+    a.page_perm[1] = page_perm[1];
     a.min_units = min_units;
     a.max_tail_chunks = v.tail_chunks;
     a.scale_log2 = L.scale * kLog2e;

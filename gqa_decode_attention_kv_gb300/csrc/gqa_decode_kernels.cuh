@@ -79,6 +79,8 @@ struct DecodeArgs {
     // slot of the workspace (GT, or 8 with NRG > 1).
     int Kv, NRG, RS;
     int map_perm[3];     // tensor-map dims 1..3 -> 0 slot, 1 kv-head, 2 block
+    int page_box;        // 16-bit caches, d = 128: the maps are page maps (one copy per tile)
+    int page_perm[2];    // page-map dims 3, 4 -> 1 kv-head, 2 block
     int max_tail_chunks; // pooled chunks per worker range (0 = static partition only)
     float scale_log2;    // scale * log2(e)
 };
@@ -123,7 +125,10 @@ constexpr int kHeadsPerWarp = 8;   // query heads one warp serves (the MMA N dim
 // kHeadWarps == 1: every warp is an independent split-KV worker with its own
 // ring and serves all (<= 8) heads of its group. kHeadWarps > 1: the CTA is one
 // worker; its kHeadWarps warps take 8 heads each of a larger group and share
-// one ring, so each K/V tile is still loaded once for the whole group.
+// one ring, so each K/V tile is still loaded once for the whole group. With two
+// such warps a third one only issues the copies: refilling a slot costs the
+// issuing warp ~1000 cycles a block, which a row warp would add to the pair's
+// pace while its partner waited.
 template <int kKind, typename T, int D, int kHeadWarps = 1, bool kGeneral = false>
 struct Cfg {
     // kGen: T > 1 queries per sequence or a sliding window (per-row ranges);
@@ -157,17 +162,18 @@ struct Cfg {
     // CTAs per SM the register budget is cut for. The int8 kernel is bound by
     // issue and latency and gains from 12 warps per SM; the bf16/f16 kernels
     // would spill at that budget and keep 8 (both measured).
+    static constexpr bool kCopyWarp = kHeadWarps == 2 && kKind == kKernelMma;   // a warp that only issues copies
+    static constexpr int kWarps = kHeadWarps == 1 ? GQA_WARPS_PER_CTA : kHeadWarps + (kCopyWarp ? 1 : 0);
     static constexpr int kMinCtas =
         (kHeadWarps == 1 && kKind == kKernelMma && D == 128) ? (kCoded ? GQA_MIN_CTAS_PER_SM_I8 : 2)
-        : (kHeadWarps > 1 && kKind == kKernelMma) ? std::max(1, GQA_SHARED_MIN_WARPS_PER_SM / kHeadWarps)
+        : (kHeadWarps > 1 && kKind == kKernelMma) ? std::max(1, GQA_SHARED_MIN_WARPS_PER_SM / kWarps)
                                                   : 1;
     // Load the next pair's query fragments while the current pair runs (16
     // registers). A worker meets a new pair once every few hundred blocks on
     // the benchmark workloads, so kernels short of registers load them when
     // the pair starts instead.
     static constexpr bool kPrefetchQ =
-        !(kCoded && kMinCtas >= 4) && !(kHeadWarps > 1 && kHeadWarps * kMinCtas >= 12);
-    static constexpr int kWarps = kHeadWarps == 1 ? GQA_WARPS_PER_CTA : kHeadWarps;
+        !(kCoded && kMinCtas >= 4) && !(kHeadWarps > 1 && kWarps * kMinCtas >= 12);
     static constexpr int kRings = kHeadWarps == 1 ? kWarps : 1;
     static constexpr int kStages =
         std::max(2, std::min(8, (kHeadWarps == 1 ? GQA_RING_BYTES_PER_WARP : GQA_SHARED_RING_BYTES) / kStage));
@@ -1063,7 +1069,9 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     const uint32_t bar0 = sbase + S::kBars + ring_id * C::kStages * 8;
     const uint32_t ebar0 = sbase + S::kEmpty;
     volatile int* meta = reinterpret_cast<volatile int*>(gbase + S::kMeta) + ring_id * C::kStages * 4;
-    const bool producer = !kShared || warp == 0;  // the warp that issues this ring's copies
+    // the warp that issues this ring's copies: each warp its own, else warp 0,
+    // or the copy warp (warp kHeadWarps) that does nothing else
+    const bool producer = !kShared || warp == (C::kCopyWarp ? kHeadWarps : 0);
     if (kShared) {
         if (threadIdx.x == 0) {
             for (int s = 0; s < C::kStages; ++s) {
@@ -1186,12 +1194,19 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                 meta[4 * s] = kSlotData;
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar, C::kTxBytes);
+                if (C::kNumBox == 2 && a.page_box) {
+                    // one copy per tile: the page map lands both 64-element halves
+                    const int p3 = coord(a.page_perm[0]), p4 = coord(a.page_perm[1]);
+                    tma_load_5d(dst, &kmap, 0, 0, 0, p3, p4, bar, pol);
+                    tma_load_5d(dst + C::kTile, &vmap, 0, 0, 0, p3, p4, bar, pol);
+                } else {
 #pragma unroll
-                for (int x = 0; x < C::kNumBox; ++x)
-                    tma_load_4d(dst + x * C::kBoxBytes, &kmap, x * C::kBoxInner, y, z, ww, bar, pol);
+                    for (int x = 0; x < C::kNumBox; ++x)
+                        tma_load_4d(dst + x * C::kBoxBytes, &kmap, x * C::kBoxInner, y, z, ww, bar, pol);
 #pragma unroll
-                for (int x = 0; x < C::kNumBox; ++x)
-                    tma_load_4d(dst + C::kTile + x * C::kBoxBytes, &vmap, x * C::kBoxInner, y, z, ww, bar, pol);
+                    for (int x = 0; x < C::kNumBox; ++x)
+                        tma_load_4d(dst + C::kTile + x * C::kBoxBytes, &vmap, x * C::kBoxInner, y, z, ww, bar, pol);
+                }
                 if constexpr (C::kCoded) {
                     const long long si = ((long long)ph * a.K + gg) * kBlock;
                     if constexpr (C::kKc)   // whole 256-byte rows of their own: read once
@@ -1236,6 +1251,19 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 
     if (producer)
         for (int s = 0; s < C::kStages; ++s) issue_next(s);
+    if (C::kCopyWarp && producer) {
+        // refill each slot once every row warp has released it, in use order;
+        // the last fill is the end marker, after which the row warps finish alone
+        for (int k = 0; !iss_done; ++k) {
+            const int s = k % C::kStages;
+            if (!wait_all(ebar0 + 8 * s, (uint32_t)(k / C::kStages) & 1u)) {
+                bail(k);
+                return;
+            }
+            issue_next(s);
+        }
+        return;
+    }
 
     // ---- consumer: walk the units as they arrive
     const int r = lane >> 2, c = lane & 3;

@@ -117,4 +117,10 @@ int launch_decode(const DecodeLaunch& L, int num_sms);
 bool encode_cache_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base,
                       int box_inner, int swizzle_bytes, int perm[3]);
 
+// 5-D tensor map whose box is one whole 16-token page of a 16-bit cache with
+// head_dim 128, landed as [half][slot][128 B] with the 128-byte swizzle (the
+// layout of two 64-element boxes of encode_cache_map); perm: dims 3 and 4 ->
+// 1 kv-head, 2 block. Returns false for other caches.
+bool encode_page_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int perm[2]);
+
 }  // namespace gqa

@@ -26,20 +26,7 @@
 
 namespace gqa {
 
-// In gqa_capi.cu: a tensor map whose box is a whole 16-token page of 128-element
-// rows, laid out [half][slot][128 B] (perm: dims 3 and 4 -> 1 kv-head, 2 block).
-bool encode_page_map(CUtensorMap* map, const gqa_kv_cache_t& c, const void* base, int perm[2]);
-
 namespace {
-
-__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
-                                            int w, int v, uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(bar), "l"(policy)
-        : "memory");
-}
 
 // Bulk tensor store of a shared-memory box to global through `map`, in this
 // thread's bulk group; then the group's commit, and the waits for its reads of
