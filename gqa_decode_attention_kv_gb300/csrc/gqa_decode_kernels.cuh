@@ -125,10 +125,11 @@ constexpr int kHeadsPerWarp = 8;   // query heads one warp serves (the MMA N dim
 // kHeadWarps == 1: every warp is an independent split-KV worker with its own
 // ring and serves all (<= 8) heads of its group. kHeadWarps > 1: the CTA is one
 // worker; its kHeadWarps warps take 8 heads each of a larger group and share
-// one ring, so each K/V tile is still loaded once for the whole group. With two
-// such warps a third one only issues the copies: refilling a slot costs the
-// issuing warp ~1000 cycles a block, which a row warp would add to the pair's
-// pace while its partner waited.
+// one ring, so each K/V tile is still loaded once for the whole group. One more
+// warp only issues the copies: refilling a slot costs the issuing warp ~1000
+// cycles a block, which a row warp would add to the group's pace while the
+// others waited (measured; with eight row warps the ninth caps registers at 168
+// and still wins).
 template <int kKind, typename T, int D, int kHeadWarps = 1, bool kGeneral = false>
 struct Cfg {
     // kGen: T > 1 queries per sequence or a sliding window (per-row ranges);
@@ -162,7 +163,7 @@ struct Cfg {
     // CTAs per SM the register budget is cut for. The int8 kernel is bound by
     // issue and latency and gains from 12 warps per SM; the bf16/f16 kernels
     // would spill at that budget and keep 8 (both measured).
-    static constexpr bool kCopyWarp = kHeadWarps == 2 && kKind == kKernelMma;   // a warp that only issues copies
+    static constexpr bool kCopyWarp = kHeadWarps >= 2 && kKind == kKernelMma;   // a warp that only issues copies
     static constexpr int kWarps = kHeadWarps == 1 ? GQA_WARPS_PER_CTA : kHeadWarps + (kCopyWarp ? 1 : 0);
     static constexpr int kMinCtas =
         (kHeadWarps == 1 && kKind == kKernelMma && D == 128) ? (kCoded ? GQA_MIN_CTAS_PER_SM_I8 : 2)
