@@ -98,15 +98,17 @@ struct DecodeArgs {
 #define GQA_MIN_CTAS_PER_SM_I8 3
 #endif
 // Ring bytes of a CTA whose warps share one ring (groups of more than 8 heads).
-// Measured on the T = 4 and G = 16 workloads at 12 warps per SM: 24 KB (three
-// bf16 stages) beats 32 KB by 3-4%.
+// Measured on the T = 4, G = 16 and G = 64 workloads at 12 warps per SM with
+// the copy warp: 32 KB (four bf16 stages) beats 24 KB by 2-4% and ties 40 KB;
+// 16 KB loses 5%.
 #ifndef GQA_SHARED_RING_BYTES
-#define GQA_SHARED_RING_BYTES 24576
+#define GQA_SHARED_RING_BYTES 32768
 #endif
 // Warps per SM the tensor-core shared-ring kernels are compiled to fit
-// (registers): 12 (170 registers, no next-pair query prefetch) beats the
-// unconstrained 244 registers by 19-23% on the T = 4 and G = 16 workloads;
-// 14 and 16 spill and lose 40%.
+// (registers), copy warps included: 12 (168 registers, no next-pair query
+// prefetch) beat the unconstrained 244 registers by 19-23% on the T = 4 and
+// G = 16 workloads before the copy warp; 14 and 16 spill and lose 40%; with
+// the copy warp, 9 (three CTAs of three warps) loses 15% to 12.
 #ifndef GQA_SHARED_MIN_WARPS_PER_SM
 #define GQA_SHARED_MIN_WARPS_PER_SM 12
 #endif
