@@ -1406,8 +1406,8 @@ split_kv_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
 // ------------------------------------------------------------------ combine
 
 // Merge the splits of each (sequence, new token, query head) row; zero rows
-// of empty sequences. kRowWarps warps share a row (they take its splits in turn and meet
-// in shared memory); a CTA holds kRows rows. CTA 0 also rewinds the run-time
+// of empty sequences. kRowWarps warps share a row (each takes an even share of its splits;
+// they meet in shared memory); a CTA holds kRows rows. CTA 0 also rewinds the run-time
 // work counter for the next call (every split-KV CTA has finished by now).
 template <int D, int kRowWarps, int kRows>
 __global__ void __launch_bounds__(kRowWarps * kRows * 32) combine_kernel(const DecodeArgs a) {
@@ -1449,42 +1449,42 @@ __global__ void __launch_bounds__(kRowWarps * kRows * 32) combine_kernel(const D
     const long long first = (long long)b * a.Kv + gv + s0;   // slot of the first piece
     const int n = s1 - s0 + 1;
 
-    // pass 1: the largest running maximum (one piece per lane)
-    float M = -INFINITY;
-    for (int p = sub * 32 + lane; p < n; p += kRowWarps * 32)
-        M = fmaxf(M, __ldcg(&a.ws_ml[(first + p) * a.RS + hh]).x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-    if constexpr (kRowWarps > 1) {
-        if (lane == 0) s_red[sub] = M;
-        __syncthreads();
-        M = s_red[0];
-#pragma unroll
-        for (int w = 1; w < kRowWarps; ++w) M = fmaxf(M, s_red[w]);
-    }
-
-    // pass 2: each warp takes 32 pieces at a time: lane j learns piece j's weight,
-    // then every lane gathers its dims of all 32 partial vectors with independent
-    // loads. Pieces that saw only skipped blocks hold m = -inf and o = 0.
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // One pass over the pieces. Each warp takes an even share of them (in
+    // chunks of 32 when the share is larger): lane j loads piece j's (m, l), the
+    // warp keeps a running maximum Mw and rescales what it holds when Mw grows,
+    // then every lane gathers its dims of the chunk's partial vectors with
+    // independent loads, 8 in flight. The warps of a row meet in shared memory,
+    // where each share is rescaled from its Mw to the row's maximum. Pieces that
+    // saw only skipped blocks hold m = -inf and o = 0 and weigh 0.
+    const int per = (n + kRowWarps - 1) / kRowWarps;
+    const int lo = min(n, sub * per), hi = min(n, lo + per);
     const bool has_dims = 4 * lane < D;
-    if (M != -INFINITY) {
-        for (int base = sub * 32; base < n; base += kRowWarps * 32) {
-            const int p = base + lane;
-            float e = 0.f;
-            if (p < n) {
-                const float2 ml = __ldcg(&a.ws_ml[(first + p) * a.RS + hh]);
-                e = fast_exp2(ml.x - M);
-                L += ml.y * e;
-            }
-            const int cnt = min(32, n - base);
-            const float* op = a.ws_o + ((first + base) * a.RS + hh) * D + 4 * lane;
-            const long long step = (long long)a.RS * D;
-#pragma unroll 8
-            for (int j = 0; j < cnt; ++j) {
-                const float ej = __shfl_sync(kFull, e, j);
-                if (has_dims) {
+    const long long step = (long long)a.RS * D;
+    float Mw = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int base = lo; base < hi; base += 32) {
+        const int p = base + lane;
+        float2 ml = make_float2(-INFINITY, 0.f);
+        if (p < hi) ml = __ldcg(&a.ws_ml[(first + p) * a.RS + hh]);
+        float mc = ml.x;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(kFull, mc, o));
+        const float Mn = fmaxf(Mw, mc);
+        if (Mn == -INFINITY) continue;         // warp-uniform: nothing seen yet
+        const float sc = fast_exp2(Mw - Mn);   // 0 while Mw = -inf, 1 if unchanged
+        acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+        L *= sc;
+        Mw = Mn;
+        const float e = fast_exp2(ml.x - Mw);
+        L += ml.y * e;
+        const int cnt = min(32, hi - base);
+        const float* op = a.ws_o + ((first + base) * a.RS + hh) * D + 4 * lane;
+        for (int j0 = 0; j0 < cnt; j0 += 8) {
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int j = j0 + jj;
+                const float ej = __shfl_sync(kFull, e, j & 31);
+                if (j < cnt && has_dims) {
                     const float4 o = __ldcg(reinterpret_cast<const float4*>(op + j * step));
                     acc.x += o.x * ej; acc.y += o.y * ej; acc.z += o.z * ej; acc.w += o.w * ej;
                 }
@@ -1500,16 +1500,25 @@ __global__ void __launch_bounds__(kRowWarps * kRows * 32) combine_kernel(const D
             s_acc[sub][4 * lane + 2] = acc.z;
             s_acc[sub][4 * lane + 3] = acc.w;
         }
-        if (lane == 0) s_l[sub] = L;
+        if (lane == 0) {
+            s_red[sub] = Mw;
+            s_l[sub] = L;
+        }
         __syncthreads();
+        float M = s_red[0];
+#pragma unroll
+        for (int w = 1; w < kRowWarps; ++w) M = fmaxf(M, s_red[w]);
+        auto share_scale = [&](int w) {        // a share with no pieces weighs 0
+            return s_red[w] == -INFINITY ? 0.f : fast_exp2(s_red[w] - M);
+        };
         float Lt = 0.f;
 #pragma unroll
-        for (int w = 0; w < kRowWarps; ++w) Lt += s_l[w];
+        for (int w = 0; w < kRowWarps; ++w) Lt += s_l[w] * share_scale(w);
         const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
         for (int i = tid; i < D; i += blockDim.x) {
             float v = 0.f;
 #pragma unroll
-            for (int w = 0; w < kRowWarps; ++w) v += s_acc[w][i];
+            for (int w = 0; w < kRowWarps; ++w) v += s_acc[w][i] * share_scale(w);
             store1(a.out, a.out_dtype, orow + i, v * inv);
         }
     } else {
