@@ -97,6 +97,17 @@ struct DecodeArgs {
 #ifndef GQA_MIN_CTAS_PER_SM_I8
 #define GQA_MIN_CTAS_PER_SM_I8 3
 #endif
+// The one-token INT4 tensor-core kernel (per-token scales) fits 128 registers
+// without spilling, so it runs 4 CTAs (16 warps) per SM, with a ring of five
+// 2.5 KB stages per warp so that four CTAs fit in shared memory. Measured on
+// the B=128 ragged INT4 workload: 2852 against 2647 GB/s at 3 CTAs and six
+// stages; four stages 2807. int8, FP8 and the KIVI-style cache spill at 128.
+#ifndef GQA_MIN_CTAS_PER_SM_I4
+#define GQA_MIN_CTAS_PER_SM_I4 4
+#endif
+#ifndef GQA_RING_BYTES_PER_WARP_I4
+#define GQA_RING_BYTES_PER_WARP_I4 12800
+#endif
 // Ring bytes of a CTA whose warps share one ring (groups of more than 8 heads).
 // Measured on the T = 4, G = 16 and G = 64 workloads at 12 warps per SM with
 // the copy warp: 32 KB (four bf16 stages) beats 24 KB by 2-4% and ties 40 KB;
@@ -162,13 +173,17 @@ struct Cfg {
     // them more than the tail it removes (measured on int8), so they keep the
     // static partition.
     static constexpr int kTailChunks = kCoded ? 0 : kMaxTailChunks;
-    // CTAs per SM the register budget is cut for. The int8 kernel is bound by
-    // issue and latency and gains from 12 warps per SM; the bf16/f16 kernels
-    // would spill at that budget and keep 8 (both measured).
+    // CTAs per SM the register budget is cut for. The code-cache kernels are
+    // bound by issue and latency and gain from 12 warps per SM (16 for the
+    // one-token INT4 kernel); the bf16/f16 kernels would spill at that budget
+    // and keep 8 (all measured).
     static constexpr bool kCopyWarp = kHeadWarps >= 2 && kKind == kKernelMma;   // a warp that only issues copies
     static constexpr int kWarps = kHeadWarps == 1 ? GQA_WARPS_PER_CTA : kHeadWarps + (kCopyWarp ? 1 : 0);
+    static constexpr bool kNarrowI4 =                // the one-token INT4 kernel with per-token scales
+        kI4 && !kKc && !kGen && kHeadWarps == 1 && kKind == kKernelMma && D == 128;
     static constexpr int kMinCtas =
-        (kHeadWarps == 1 && kKind == kKernelMma && D == 128) ? (kCoded ? GQA_MIN_CTAS_PER_SM_I8 : 2)
+        kNarrowI4 ? GQA_MIN_CTAS_PER_SM_I4
+        : (kHeadWarps == 1 && kKind == kKernelMma && D == 128) ? (kCoded ? GQA_MIN_CTAS_PER_SM_I8 : 2)
         : (kHeadWarps > 1 && kKind == kKernelMma) ? std::max(1, GQA_SHARED_MIN_WARPS_PER_SM / kWarps)
                                                   : 1;
     // Load the next pair's query fragments while the current pair runs (16
@@ -178,8 +193,9 @@ struct Cfg {
     static constexpr bool kPrefetchQ =
         !(kCoded && kMinCtas >= 4) && !(kHeadWarps > 1 && kWarps * kMinCtas >= 12);
     static constexpr int kRings = kHeadWarps == 1 ? kWarps : 1;
-    static constexpr int kStages =
-        std::max(2, std::min(8, (kHeadWarps == 1 ? GQA_RING_BYTES_PER_WARP : GQA_SHARED_RING_BYTES) / kStage));
+    static constexpr int kStages = std::max(
+        2, std::min(8, (kNarrowI4 ? GQA_RING_BYTES_PER_WARP_I4
+                        : kHeadWarps == 1 ? GQA_RING_BYTES_PER_WARP : GQA_SHARED_RING_BYTES) / kStage));
     static constexpr int kBoxInner = kSwizzle ? 128 / kEs : kRowBytes / kEs;   // elements per box row
     static constexpr int kNumBox = kSwizzle ? kRowBytes / 128 : 1;
     static constexpr int kBoxBytes = 16 * kBoxInner * kEs;
