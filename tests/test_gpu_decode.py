@@ -199,17 +199,19 @@ def test_split_count_does_not_change_the_answer(gq):
         assert (o - outs[0]).abs().max().item() <= 1e-4
 
 
-@pytest.mark.parametrize("lens,K,window,queries,max_warps", [
-    ([20000], 1, 0, 1, 0),                   # one pair, hundreds of pieces: 32 warps per row
-    ([20000], 1, 0, 1, 30),                  # about 45 pieces per row: 8 warps per row
-    ([20000] + [1] * 63, 8, 0, 1, 0),        # few pieces expected, one long row: chunks of 32
-    ([20000], 1, 5000, 1, 0),                # a window over the long row
-    ([3000, 40], 1, 64, 4, 0),               # causal new tokens under a window
+@pytest.mark.parametrize("lens,K,window,queries,max_warps,d", [
+    ([20000], 1, 0, 1, 0, 128),              # one pair, hundreds of pieces: 32 warps per row
+    ([20000], 1, 0, 1, 30, 128),             # about 45 pieces per row: 8 warps per row
+    ([20000] + [1] * 63, 8, 0, 1, 0, 128),   # few pieces expected, one long row: chunks of 32
+    ([20000], 1, 5000, 1, 0, 128),           # a window over the long row
+    ([3000, 40], 1, 64, 4, 0, 128),          # causal new tokens under a window
+    ([20000], 1, 0, 1, 0, 64),               # head_dim 64: half the lanes hold dims
+    ([20000] + [1] * 63, 8, 0, 1, 0, 64),
 ])
-def test_combine_forms_match_the_oracle(gq, lens, K, window, queries, max_warps):
+def test_combine_forms_match_the_oracle(gq, lens, K, window, queries, max_warps, d):
     """Rows merged by one warp (pieces in chunks of 32), by 8 warps or by 32 warps
     sharing a CTA, each against the oracle element by element."""
-    case = gi.make_case(len(lens), 8, K, 128, lens, "bf16", seed=33, device="cuda", queries=queries)
+    case = gi.make_case(len(lens), 8, K, d, lens, "bf16", seed=33, device="cuda", queries=queries)
     ref = oracle_for_case(case, window=window)
     out = _run(gq, case, window=window, max_warps=max_warps, min_blocks_per_warp=1)
     assert max_abs_err(out, ref) <= TOL
